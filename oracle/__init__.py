@@ -1,0 +1,224 @@
+"""CPU oracle for the ring collectives -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library under test never does: it
+shares no code with it, and a product path that reached this module would void
+every parity claim.
+
+The arithmetic lives in ``ring_oracle.c`` (plain C, built here with gcc
+``-O2 -ffp-contract=off``); this module only compiles it and marshals numpy
+arrays.  Buffers are numpy arrays: ``np.float32`` for fp32, ``np.uint16`` bit
+patterns for bf16 (the oracle never needs a bf16 numpy type).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "ring_oracle.c")
+LIB = os.path.join(HERE, "_build", "liboracle.so")
+
+FP32, BF16 = 0, 1
+SUM, AVG, MAX, PROD = 0, 1, 2, 3
+OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ring_oracle.c into oracle/_build/liboracle.so (gcc, no fast-math)."""
+    os.makedirs(os.path.dirname(LIB), exist_ok=True)
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
+        return LIB
+    tmp = LIB + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-Wall", "-Wextra", "-o", tmp, SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(LIB)
+            u64, i32, vp = ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p
+            pp = ctypes.POINTER(ctypes.c_void_p)
+            p64 = ctypes.POINTER(ctypes.c_uint64)
+            L.oracle_round_bf16.argtypes = [ctypes.c_uint32]
+            L.oracle_round_bf16.restype = ctypes.c_uint16
+            L.oracle_round_bf16_array.argtypes = [vp, vp, u64]
+            L.oracle_round_bf16_array.restype = None
+            L.oracle_partition.argtypes = [u64, i32, p64, p64]
+            L.oracle_partition.restype = None
+            L.oracle_ring_schedule.argtypes = [i32, ctypes.POINTER(ctypes.c_int32)]
+            L.oracle_ring_schedule.restype = None
+            L.oracle_ring_allreduce.argtypes = [pp, i32, u64, i32, i32, p64]
+            L.oracle_ring_allreduce_closed.argtypes = [pp, pp, i32, u64, i32, i32]
+            L.oracle_ring_allreduce_at.argtypes = [pp, i32, u64, i32, i32, p64, u64, vp]
+            L.oracle_reduce_scatter.argtypes = [pp, pp, i32, u64, i32, i32]
+            L.oracle_allgather.argtypes = [pp, pp, i32, u64, i32]
+            L.oracle_broadcast.argtypes = [pp, pp, i32, i32, u64, i32]
+            L.oracle_alltoallv.argtypes = [pp, pp, i32, p64, i32]
+            L.oracle_bucket_allreduce.argtypes = [pp, p64, i32, i32, u64, i32, i32]
+            L.oracle_sum_f64.argtypes = [pp, i32, u64, i32, i32, vp, vp]
+            for name in ("oracle_ring_allreduce", "oracle_ring_allreduce_closed", "oracle_ring_allreduce_at",
+                         "oracle_reduce_scatter", "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
+                         "oracle_bucket_allreduce", "oracle_sum_f64"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------- helpers
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return FP32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError("oracle buffers are float32 or uint16 (bf16 bit patterns), got %s" % a.dtype)
+
+
+def _ptrs(arrs) -> ctypes.Array:
+    for a in arrs:
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("oracle buffers must be C-contiguous")
+    return (ctypes.c_void_p * max(1, len(arrs)))(*[a.ctypes.data for a in arrs])
+
+
+def _u64(vals) -> ctypes.Array:
+    vals = list(vals)
+    return (ctypes.c_uint64 * max(1, len(vals)))(*vals)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise RuntimeError("%s failed with code %d" % (what, rc))
+
+
+def _op(op) -> int:
+    return OPS[op] if isinstance(op, str) else int(op)
+
+
+# ---------------------------------------------------------------- API
+
+def round_bf16(bits_f32: int) -> int:
+    """fp32 bit pattern -> bf16 bit pattern, round to nearest even."""
+    return int(lib().oracle_round_bf16(ctypes.c_uint32(bits_f32)))
+
+
+def round_bf16_array(bits_f32: np.ndarray) -> np.ndarray:
+    src = np.ascontiguousarray(bits_f32, dtype=np.uint32).ravel()
+    out = np.empty(src.size, dtype=np.uint16)
+    lib().oracle_round_bf16_array(src.ctypes.data, out.ctypes.data, src.size)
+    return out
+
+
+def partition(K: int, N: int):
+    off, ln = (ctypes.c_uint64 * N)(), (ctypes.c_uint64 * N)()
+    lib().oracle_partition(K, N, off, ln)
+    return list(off), list(ln)
+
+
+def ring_schedule(N: int) -> np.ndarray:
+    """[phase][s][rank] -> (send chunk, recv chunk, source rank)."""
+    steps = max(N - 1, 0)
+    tab = np.zeros((2, steps, N, 3), dtype=np.int32)
+    lib().oracle_ring_schedule(N, tab.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    return tab
+
+
+def ring_allreduce(bufs, op="sum"):
+    """Step-faithful ring AllReduce.  Returns (outputs, elements sent per rank)."""
+    outs = [np.array(b, copy=True, order="C") for b in bufs]
+    N, K = len(outs), outs[0].size
+    sent = (ctypes.c_uint64 * N)()
+    _check(lib().oracle_ring_allreduce(_ptrs(outs), N, K, _dtype_code(outs[0]), _op(op), sent),
+           "oracle_ring_allreduce")
+    return outs, list(sent)
+
+
+def ring_allreduce_closed(bufs, op="sum"):
+    ins = [np.ascontiguousarray(b) for b in bufs]
+    outs = [np.empty_like(b) for b in ins]
+    _check(lib().oracle_ring_allreduce_closed(_ptrs(ins), _ptrs(outs), len(ins), ins[0].size,
+                                              _dtype_code(ins[0]), _op(op)), "oracle_ring_allreduce_closed")
+    return outs
+
+
+def ring_allreduce_at(bufs, idx, op="sum") -> np.ndarray:
+    ins = [np.ascontiguousarray(b) for b in bufs]
+    idx = np.ascontiguousarray(idx, dtype=np.uint64)
+    out = np.empty(idx.size, dtype=ins[0].dtype)
+    _check(lib().oracle_ring_allreduce_at(_ptrs(ins), len(ins), ins[0].size, _dtype_code(ins[0]), _op(op),
+                                          idx.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), idx.size,
+                                          out.ctypes.data), "oracle_ring_allreduce_at")
+    return out
+
+
+def reduce_scatter(bufs, op="sum"):
+    ins = [np.ascontiguousarray(b) for b in bufs]
+    N, K = len(ins), ins[0].size
+    _, ln = partition(K, N)
+    outs = [np.empty(ln[r], dtype=ins[0].dtype) for r in range(N)]
+    _check(lib().oracle_reduce_scatter(_ptrs(ins), _ptrs(outs), N, K, _dtype_code(ins[0]), _op(op)),
+           "oracle_reduce_scatter")
+    return outs
+
+
+def allgather(chunks, K: int):
+    """chunks[r] = rank r's contribution (chunk r of the K-element result)."""
+    ins = [np.ascontiguousarray(c) for c in chunks]
+    N = len(ins)
+    outs = [np.zeros(K, dtype=ins[0].dtype) for _ in range(N)]
+    _check(lib().oracle_allgather(_ptrs(ins), _ptrs(outs), N, K, _dtype_code(ins[0])), "oracle_allgather")
+    return outs
+
+
+def broadcast(bufs, root: int):
+    ins = [np.ascontiguousarray(b) for b in bufs]
+    outs = [np.array(b, copy=True) for b in ins]
+    _check(lib().oracle_broadcast(_ptrs(ins), _ptrs(outs), len(ins), root, ins[0].size, _dtype_code(ins[0])),
+           "oracle_broadcast")
+    return outs
+
+
+def alltoallv(sends, counts: np.ndarray):
+    """counts[i, j] elements from rank i to rank j."""
+    ins = [np.ascontiguousarray(s) for s in sends]
+    N = len(ins)
+    counts = np.asarray(counts, dtype=np.uint64).reshape(N, N)
+    outs = [np.zeros(int(counts[:, j].sum()), dtype=ins[0].dtype) for j in range(N)]
+    _check(lib().oracle_alltoallv(_ptrs(ins), _ptrs(outs), N, _u64(counts.ravel()), _dtype_code(ins[0])),
+           "oracle_alltoallv")
+    return outs
+
+
+def bucket_allreduce(tensors, bucket_elems: int, op="sum"):
+    """tensors[r][t] = rank r's t-th registered gradient (flat arrays).  Returns new arrays."""
+    N, T = len(tensors), len(tensors[0])
+    outs = [[np.array(tensors[r][t], copy=True) for t in range(T)] for r in range(N)]
+    flat = [outs[r][t] for r in range(N) for t in range(T)]
+    numels = [outs[0][t].size for t in range(T)]
+    _check(lib().oracle_bucket_allreduce(_ptrs(flat), _u64(numels), T, N, bucket_elems,
+                                         _dtype_code(flat[0]), _op(op)), "oracle_bucket_allreduce")
+    return outs
+
+
+def sum_f64(bufs, op="sum"):
+    """fp64 plain sum (or mean) and sum of |x| per element."""
+    ins = [np.ascontiguousarray(b) for b in bufs]
+    K = ins[0].size
+    y, a = np.empty(K, np.float64), np.empty(K, np.float64)
+    _check(lib().oracle_sum_f64(_ptrs(ins), len(ins), K, _dtype_code(ins[0]), _op(op), y.ctypes.data,
+                                a.ctypes.data), "oracle_sum_f64")
+    return y, a

@@ -1,0 +1,554 @@
+/*
+ * ring_oracle.c -- CPU oracle for the ring collectives.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may load, link or call
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * use it.  It shares no code, header or table with the CUDA library.
+ *
+ * Plain, slow and step by step: N simulated ranks each own a buffer of K
+ * elements; every ring step snapshots what each rank sends, then applies what
+ * each rank receives, exactly as the pages' CPU ring simulator does (Lesson 3
+ * "Distributed communication primitives", fill-in exercise and reference
+ * solution).  Arithmetic is IEEE fp32 with round-to-nearest-even, followed by a
+ * round to the buffer type after every hop (fp32: identity; bf16: RNE from the
+ * IEEE definition).  Built with -O2 -ffp-contract=off and without fast-math, so
+ * no FMA contraction, flush-to-zero or reassociation can creep in.
+ *
+ * Conventions fixed here (the pages leave them open):
+ *   - chunk c of a K-element buffer has len_c = K/N + (c < K%N) elements, the
+ *     first K%N chunks taking one extra element;
+ *   - a NaN produced by an fp32 operation is the canonical quiet NaN 0x7FFFFFFF;
+ *     rounding a NaN to bf16 keeps its sign and top payload bits and sets the
+ *     quiet bit;
+ *   - MAX: NaN if either operand is NaN, else the larger, and for +0 vs -0 the
+ *     bitwise AND of the two (so +0 wins);
+ *   - AVG: SUM around the ring, then one fp32 division by N at the rank that
+ *     holds the finished chunk, rounded to the buffer type, before the gather.
+ *
+ * Parity pins live in tests/test_oracle_*.py; see each function's comment for
+ * which passage it follows.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_FP32 0
+#define OR_BF16 1
+
+#define OR_SUM 0
+#define OR_AVG 1
+#define OR_MAX 2
+#define OR_PROD 3
+
+#define OR_OK 0
+#define OR_EINVAL 1
+#define OR_ENOMEM 2
+
+/* ------------------------------------------------------------------ */
+/* scalar arithmetic                                                   */
+/* ------------------------------------------------------------------ */
+
+static float bits_to_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t f32_to_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static int f32_bits_is_nan(uint32_t u) { return (u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0; }
+
+/* IEEE-754 round-to-nearest, ties-to-even, of an fp32 bit pattern to bf16
+ * (keep the top 16 bits; the dropped 16 bits decide: above half rounds the
+ * magnitude up, below half truncates, exactly half rounds to the even result).
+ * The magnitude increment carries into the exponent, so the largest finite
+ * values round to infinity and subnormals round within the subnormal range. */
+uint16_t oracle_round_bf16(uint32_t u)
+{
+    if (f32_bits_is_nan(u))
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t kept = u >> 16;
+    uint32_t dropped = u & 0xffffu;
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))
+        kept += 1u;
+    return (uint16_t)kept;
+}
+
+/* Bulk form of oracle_round_bf16 (for exhaustive pattern checks). */
+void oracle_round_bf16_array(const uint32_t *in, uint16_t *out, uint64_t n)
+{
+    for (uint64_t i = 0; i < n; ++i)
+        out[i] = oracle_round_bf16(in[i]);
+}
+
+/* bf16 -> fp32 is exact: the bf16 pattern is the top half of the fp32 one. */
+static uint32_t widen_bits(uint32_t stored, int dtype)
+{
+    return dtype == OR_BF16 ? (stored << 16) : stored;
+}
+
+static uint32_t narrow_bits(uint32_t f32bits, int dtype)
+{
+    return dtype == OR_BF16 ? (uint32_t)oracle_round_bf16(f32bits) : f32bits;
+}
+
+/* One fp32 operation of the ring's reduction, IEEE round-to-nearest-even. */
+static uint32_t op_f32(uint32_t a_bits, uint32_t b_bits, int op)
+{
+    float a = bits_to_f32(a_bits), b = bits_to_f32(b_bits);
+    uint32_t r;
+    switch (op) {
+    case OR_SUM:
+    case OR_AVG:
+        r = f32_to_bits(a + b);
+        break;
+    case OR_PROD:
+        r = f32_to_bits(a * b);
+        break;
+    case OR_MAX:
+        if (f32_bits_is_nan(a_bits) || f32_bits_is_nan(b_bits))
+            r = 0x7fffffffu;
+        else if (a > b)
+            r = a_bits;
+        else if (b > a)
+            r = b_bits;
+        else
+            r = a_bits & b_bits; /* equal: identical bits, or +0 vs -0 -> +0 */
+        break;
+    default:
+        r = 0x7fffffffu;
+    }
+    if (f32_bits_is_nan(r))
+        r = 0x7fffffffu;
+    return r;
+}
+
+/* x_local (+) x_incoming, rounded to the buffer type: one ring hop
+ * ("add what was received into the matching local chunk"). */
+static uint32_t hop(uint32_t local, uint32_t incoming, int dtype, int op)
+{
+    return narrow_bits(op_f32(widen_bits(local, dtype), widen_bits(incoming, dtype), op), dtype);
+}
+
+/* AVG's single division by N, done once on the finished sum. */
+static uint32_t avg_scale(uint32_t v, int N, int dtype)
+{
+    float x = bits_to_f32(widen_bits(v, dtype));
+    uint32_t r = f32_to_bits(x / (float)N);
+    if (f32_bits_is_nan(r))
+        r = 0x7fffffffu;
+    return narrow_bits(r, dtype);
+}
+
+static size_t esize(int dtype) { return dtype == OR_BF16 ? 2 : 4; }
+
+static uint32_t load(const void *buf, int dtype, uint64_t i)
+{
+    if (dtype == OR_BF16)
+        return ((const uint16_t *)buf)[i];
+    return ((const uint32_t *)buf)[i];
+}
+
+static void store(void *buf, int dtype, uint64_t i, uint32_t v)
+{
+    if (dtype == OR_BF16)
+        ((uint16_t *)buf)[i] = (uint16_t)v;
+    else
+        ((uint32_t *)buf)[i] = v;
+}
+
+static int mod(int64_t a, int n) { int64_t r = a % n; return (int)(r < 0 ? r + n : r); }
+
+static int bad_args(int N, int dtype, int op)
+{
+    return N < 1 || (dtype != OR_FP32 && dtype != OR_BF16) || op < OR_SUM || op > OR_PROD;
+}
+
+/* ------------------------------------------------------------------ */
+/* partition and schedule                                              */
+/* ------------------------------------------------------------------ */
+
+/* Split K elements into N contiguous chunks; the first K mod N chunks get one
+ * extra element.  (The pages require K divisible by N -- Lesson 3 splits each
+ * rank's tensor into N equal blocks -- this is the plainest extension.) */
+void oracle_partition(uint64_t K, int N, uint64_t *off, uint64_t *len)
+{
+    uint64_t q = K / (uint64_t)N, rem = K % (uint64_t)N, o = 0;
+    for (int c = 0; c < N; ++c) {
+        len[c] = q + ((uint64_t)c < rem ? 1 : 0);
+        off[c] = o;
+        o += len[c];
+    }
+}
+
+/* The ring's step table, laid out [phase][s][rank][3] = {send chunk, recv chunk,
+ * source rank}.  ReduceScatter step s: rank i sends chunk (i-s) mod N to its
+ * right neighbour and receives chunk (i-1-s) mod N from its left one.
+ * AllGather step s: rank i forwards chunk (i+1-s) mod N and stores chunk
+ * (i-s) mod N.  (Collectives and sharded matmul, "ring ReduceScatter"; AllReduce
+ * survey, Ring AllReduce phase 1; Lesson 3 reference solution.) */
+void oracle_ring_schedule(int N, int32_t *tab)
+{
+    int steps = N - 1;
+    for (int phase = 0; phase < 2; ++phase)
+        for (int s = 0; s < steps; ++s)
+            for (int i = 0; i < N; ++i) {
+                int32_t *e = tab + (((size_t)phase * steps + s) * N + i) * 3;
+                if (phase == 0) {
+                    e[0] = mod((int64_t)i - s, N);
+                    e[1] = mod((int64_t)i - 1 - s, N);
+                } else {
+                    e[0] = mod((int64_t)i + 1 - s, N);
+                    e[1] = mod((int64_t)i - s, N);
+                }
+                e[2] = mod((int64_t)i - 1, N);
+            }
+}
+
+/* ------------------------------------------------------------------ */
+/* step-faithful ring phases on N in-place rank buffers                */
+/* ------------------------------------------------------------------ */
+
+/* ReduceScatter phase, N-1 steps.  All sends of a step are snapshotted first,
+ * then each rank adds what it received into its matching chunk, operand order
+ * (local, incoming).  Afterwards rank i holds the finished chunk (i+1) mod N. */
+static int rs_phase(void **buf, int N, const uint64_t *off, const uint64_t *len,
+                    int dtype, int op, uint64_t *sent, void *snap, uint64_t stride)
+{
+    size_t es = esize(dtype);
+    for (int s = 0; s < N - 1; ++s) {
+        for (int i = 0; i < N; ++i) {
+            int c = mod((int64_t)i - s, N);
+            memcpy((char *)snap + (size_t)i * stride * es, (char *)buf[i] + off[c] * es, len[c] * es);
+            if (sent)
+                sent[i] += len[c];
+        }
+        for (int i = 0; i < N; ++i) {
+            int c = mod((int64_t)i - 1 - s, N);
+            int src = mod((int64_t)i - 1, N);
+            const void *in = (const char *)snap + (size_t)src * stride * es;
+            for (uint64_t e = 0; e < len[c]; ++e) {
+                uint64_t g = off[c] + e;
+                store(buf[i], dtype, g, hop(load(buf[i], dtype, g), load(in, dtype, e), dtype, op));
+            }
+        }
+    }
+    if (op == OR_AVG)
+        for (int i = 0; i < N; ++i) {
+            int c = mod((int64_t)i + 1, N);
+            for (uint64_t e = 0; e < len[c]; ++e)
+                store(buf[i], dtype, off[c] + e, avg_scale(load(buf[i], dtype, off[c] + e), N, dtype));
+        }
+    return OR_OK;
+}
+
+/* AllGather phase after ReduceScatter, N-1 steps: rank i forwards chunk
+ * (i+1-s) mod N and stores the chunk (i-s) mod N it receives. */
+static void ag_phase_after_rs(void **buf, int N, const uint64_t *off, const uint64_t *len,
+                              int dtype, uint64_t *sent, void *snap, uint64_t stride)
+{
+    size_t es = esize(dtype);
+    for (int s = 0; s < N - 1; ++s) {
+        for (int i = 0; i < N; ++i) {
+            int c = mod((int64_t)i + 1 - s, N);
+            memcpy((char *)snap + (size_t)i * stride * es, (char *)buf[i] + off[c] * es, len[c] * es);
+            if (sent)
+                sent[i] += len[c];
+        }
+        for (int i = 0; i < N; ++i) {
+            int c = mod((int64_t)i - s, N);
+            int src = mod((int64_t)i - 1, N);
+            memcpy((char *)buf[i] + off[c] * es, (char *)snap + (size_t)src * stride * es, len[c] * es);
+        }
+    }
+}
+
+/* Ring AllReduce, step by step, in place on buf[0..N-1] (K elements each).
+ * ReduceScatter phase, AVG scaling at the holders, AllGather phase.
+ * sent[i] (optional) accumulates the number of elements rank i sent, which for
+ * K divisible by N is 2(N-1)K/N (Lesson 3, traffic check). */
+int oracle_ring_allreduce(void **buf, int N, uint64_t K, int dtype, int op, uint64_t *sent)
+{
+    if (bad_args(N, dtype, op))
+        return OR_EINVAL;
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
+    uint64_t stride = K / (uint64_t)N + 1;
+    void *snap = malloc((size_t)N * stride * esize(dtype));
+    if (!off || !len || !snap) {
+        free(off); free(len); free(snap);
+        return OR_ENOMEM;
+    }
+    oracle_partition(K, N, off, len);
+    if (sent)
+        memset(sent, 0, sizeof(uint64_t) * (size_t)N);
+    rs_phase(buf, N, off, len, dtype, op, sent, snap, stride);
+    ag_phase_after_rs(buf, N, off, len, dtype, sent, snap, stride);
+    free(off); free(len); free(snap);
+    return OR_OK;
+}
+
+/* Second, independent formulation (closed form).  Chunk c starts at rank c at
+ * step 0 and collects one contribution per hop, finishing at rank c-1 after N-1
+ * hops, so each of its elements is the left fold
+ *     R = x_{c-1} (+) ( ... (x_{c+2} (+) (x_{c+1} (+) x_c)) ... )
+ * with a round to the buffer type after every (+); AVG divides once; every rank
+ * receives R.  in[] and out[] may alias per rank. */
+int oracle_ring_allreduce_closed(const void **in, void **out, int N, uint64_t K, int dtype, int op)
+{
+    if (bad_args(N, dtype, op))
+        return OR_EINVAL;
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
+    if (!off || !len) {
+        free(off); free(len);
+        return OR_ENOMEM;
+    }
+    oracle_partition(K, N, off, len);
+    for (int c = 0; c < N; ++c)
+        for (uint64_t e = off[c]; e < off[c] + len[c]; ++e) {
+            uint32_t acc = load(in[c], dtype, e);
+            for (int k = 1; k < N; ++k)
+                acc = hop(load(in[(c + k) % N], dtype, e), acc, dtype, op);
+            if (op == OR_AVG)
+                acc = avg_scale(acc, N, dtype);
+            for (int r = 0; r < N; ++r)
+                store(out[r], dtype, e, acc);
+        }
+    free(off); free(len);
+    return OR_OK;
+}
+
+/* Closed form evaluated only at the listed element indices (for spot checks of
+ * buffers too large to reduce in full on the CPU).  out receives one element
+ * per index, in the buffer type. */
+int oracle_ring_allreduce_at(const void **in, int N, uint64_t K, int dtype, int op,
+                             const uint64_t *idx, uint64_t n, void *out)
+{
+    if (bad_args(N, dtype, op))
+        return OR_EINVAL;
+    uint64_t q = K / (uint64_t)N, rem = K % (uint64_t)N;
+    for (uint64_t t = 0; t < n; ++t) {
+        uint64_t e = idx[t];
+        if (e >= K)
+            return OR_EINVAL;
+        /* chunk of e under the front-loaded partition */
+        int c;
+        if (e < rem * (q + 1))
+            c = (int)(e / (q + 1));
+        else
+            c = (int)(rem + (e - rem * (q + 1)) / q);
+        uint32_t acc = load(in[c], dtype, e);
+        for (int k = 1; k < N; ++k)
+            acc = hop(load(in[(c + k) % N], dtype, e), acc, dtype, op);
+        if (op == OR_AVG)
+            acc = avg_scale(acc, N, dtype);
+        store(out, dtype, t, acc);
+    }
+    return OR_OK;
+}
+
+/* ReduceScatter API: rank r receives the finished chunk r (len_r elements).
+ * Runs the ring ReduceScatter phase step by step on copies of the inputs; the
+ * phase leaves chunk r at rank r-1, and the API hands it to rank r
+ * (Collectives and sharded matmul, "Scatter and ReduceScatter": rank r gets the
+ * sum of block r). */
+int oracle_reduce_scatter(const void **in, void **out, int N, uint64_t K, int dtype, int op)
+{
+    if (bad_args(N, dtype, op))
+        return OR_EINVAL;
+    size_t es = esize(dtype);
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
+    uint64_t stride = K / (uint64_t)N + 1;
+    void *snap = malloc((size_t)N * stride * es);
+    void **work = calloc((size_t)N, sizeof(void *));
+    int rc = OR_OK;
+    if (!off || !len || !snap || !work) {
+        rc = OR_ENOMEM;
+        goto done;
+    }
+    for (int r = 0; r < N; ++r) {
+        work[r] = malloc(K * es + 1);
+        if (!work[r]) {
+            rc = OR_ENOMEM;
+            goto done;
+        }
+        memcpy(work[r], in[r], K * es);
+    }
+    oracle_partition(K, N, off, len);
+    rs_phase(work, N, off, len, dtype, op, NULL, snap, stride);
+    for (int r = 0; r < N; ++r)
+        memcpy(out[r], (char *)work[mod((int64_t)r - 1, N)] + off[r] * es, len[r] * es);
+done:
+    if (work)
+        for (int r = 0; r < N; ++r)
+            free(work[r]);
+    free(work); free(off); free(len); free(snap);
+    return rc;
+}
+
+/* AllGather API: rank r contributes chunk r (len_r elements, in[r]); every
+ * rank ends with the concatenation of all chunks in rank order.  Ring steps:
+ * rank i starts holding chunk i; at step s it forwards chunk (i-s) mod N and
+ * stores the chunk (i-1-s) mod N arriving from its left neighbour
+ * (Collectives and sharded matmul, "ring AllGather"). */
+int oracle_allgather(const void **in, void **out, int N, uint64_t K, int dtype)
+{
+    if (bad_args(N, dtype, OR_SUM))
+        return OR_EINVAL;
+    size_t es = esize(dtype);
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
+    uint64_t stride = K / (uint64_t)N + 1;
+    void *snap = malloc((size_t)N * stride * es);
+    if (!off || !len || !snap) {
+        free(off); free(len); free(snap);
+        return OR_ENOMEM;
+    }
+    oracle_partition(K, N, off, len);
+    for (int r = 0; r < N; ++r)
+        memcpy((char *)out[r] + off[r] * es, in[r], len[r] * es);
+    for (int s = 0; s < N - 1; ++s) {
+        for (int i = 0; i < N; ++i) {
+            int c = mod((int64_t)i - s, N);
+            memcpy((char *)snap + (size_t)i * stride * es, (char *)out[i] + off[c] * es, len[c] * es);
+        }
+        for (int i = 0; i < N; ++i) {
+            int c = mod((int64_t)i - 1 - s, N);
+            int src = mod((int64_t)i - 1, N);
+            memcpy((char *)out[i] + off[c] * es, (char *)snap + (size_t)src * stride * es, len[c] * es);
+        }
+    }
+    free(off); free(len); free(snap);
+    return OR_OK;
+}
+
+/* Broadcast: every rank ends with root's K elements.  Chain order root ->
+ * root+1 -> ... around the ring, one hop per step (copies, so the order cannot
+ * change any bit).  in[r] for r != root is not read. */
+int oracle_broadcast(const void **in, void **out, int N, int root, uint64_t K, int dtype)
+{
+    if (bad_args(N, dtype, OR_SUM) || root < 0 || root >= N)
+        return OR_EINVAL;
+    size_t es = esize(dtype);
+    if (out[root] != in[root])
+        memmove(out[root], in[root], K * es);
+    for (int s = 0; s < N - 1; ++s) {
+        int from = (root + s) % N, to = (root + s + 1) % N;
+        memmove(out[to], out[from], K * es);
+    }
+    return OR_OK;
+}
+
+/* AllToAllv: counts[i*N+j] elements go from rank i to rank j.  Rank i's send
+ * buffer holds its blocks ordered by destination, rank j's receive buffer holds
+ * its blocks ordered by source (displacements are prefix sums).  Pairwise steps:
+ * at step k rank i sends to (i+k) mod N, so block (i,j) lands in recv_j at the
+ * position of source i ("rank = row, block = column: a transpose").
+ * (Distributed LLM collectives, "Pairwise algorithm"; Collectives and sharded
+ * matmul, "AllToAll".) */
+int oracle_alltoallv(const void **in, void **out, int N, const uint64_t *counts, int dtype)
+{
+    if (bad_args(N, dtype, OR_SUM))
+        return OR_EINVAL;
+    size_t es = esize(dtype);
+    uint64_t *sd = malloc(sizeof(uint64_t) * (size_t)N * N), *rd = malloc(sizeof(uint64_t) * (size_t)N * N);
+    if (!sd || !rd) {
+        free(sd); free(rd);
+        return OR_ENOMEM;
+    }
+    for (int i = 0; i < N; ++i) {
+        uint64_t o = 0;
+        for (int j = 0; j < N; ++j) {
+            sd[(size_t)i * N + j] = o;
+            o += counts[(size_t)i * N + j];
+        }
+    }
+    for (int j = 0; j < N; ++j) {
+        uint64_t o = 0;
+        for (int i = 0; i < N; ++i) {
+            rd[(size_t)j * N + i] = o;
+            o += counts[(size_t)i * N + j];
+        }
+    }
+    for (int k = 0; k < N; ++k)
+        for (int i = 0; i < N; ++i) {
+            int j = (i + k) % N;
+            memcpy((char *)out[j] + rd[(size_t)j * N + i] * es,
+                   (const char *)in[i] + sd[(size_t)i * N + j] * es,
+                   counts[(size_t)i * N + j] * es);
+        }
+    free(sd); free(rd);
+    return OR_OK;
+}
+
+/* Bucket-fused AllReduce.  Each rank registers T gradient tensors in forward
+ * order (tensors[r*T + t], numels[t] elements).  The tensors are laid end to end
+ * in REVERSE registration order, the stream is cut into buckets of bucket_elems
+ * elements (the last one partial; a tensor may span buckets), and each bucket is
+ * AllReduced on its own with the ring above, its own N-chunk partition included.
+ * (Collective Communication, "Bucket fusion": DDP fills buckets in reverse order
+ * of use in the forward pass.)  In place on the tensors. */
+int oracle_bucket_allreduce(void **tensors, const uint64_t *numels, int T, int N,
+                            uint64_t bucket_elems, int dtype, int op)
+{
+    if (bad_args(N, dtype, op) || T < 0 || bucket_elems == 0)
+        return OR_EINVAL;
+    size_t es = esize(dtype);
+    uint64_t total = 0;
+    for (int t = 0; t < T; ++t)
+        total += numels[t];
+    void **bk = calloc((size_t)N, sizeof(void *));
+    int rc = OR_OK;
+    if (!bk)
+        return OR_ENOMEM;
+    for (int r = 0; r < N; ++r) {
+        bk[r] = malloc(bucket_elems * es + 1);
+        if (!bk[r]) {
+            rc = OR_ENOMEM;
+            goto done;
+        }
+    }
+    for (uint64_t b0 = 0; b0 < total; b0 += bucket_elems) {
+        uint64_t blen = total - b0 < bucket_elems ? total - b0 : bucket_elems;
+        /* gather (pack) stream range [b0, b0+blen) of every rank */
+        for (int dir = 0; dir < 2; ++dir) {
+            uint64_t pos = 0; /* stream position of the current tensor's first element */
+            for (int t = T - 1; t >= 0; --t) {
+                uint64_t lo = pos > b0 ? pos : b0;
+                uint64_t hi = pos + numels[t] < b0 + blen ? pos + numels[t] : b0 + blen;
+                if (lo < hi)
+                    for (int r = 0; r < N; ++r) {
+                        char *tp = (char *)tensors[(size_t)r * T + t] + (lo - pos) * es;
+                        char *bp = (char *)bk[r] + (lo - b0) * es;
+                        if (dir == 0)
+                            memcpy(bp, tp, (hi - lo) * es);
+                        else
+                            memcpy(tp, bp, (hi - lo) * es);
+                    }
+                pos += numels[t];
+            }
+            if (dir == 0) {
+                rc = oracle_ring_allreduce(bk, N, blen, dtype, op, NULL);
+                if (rc != OR_OK)
+                    goto done;
+            }
+        }
+    }
+done:
+    for (int r = 0; r < N; ++r)
+        free(bk[r]);
+    free(bk);
+    return rc;
+}
+
+/* Plain fp64 reference of the reduction (the definition y = sum_r x_r with no
+ * ring and no intermediate rounding), plus sum_r |x_r|, the scale against which
+ * relative error is measured.  SUM/AVG only. */
+int oracle_sum_f64(const void **in, int N, uint64_t K, int dtype, int op, double *y, double *absum)
+{
+    if (bad_args(N, dtype, op) || (op != OR_SUM && op != OR_AVG))
+        return OR_EINVAL;
+    for (uint64_t e = 0; e < K; ++e) {
+        double s = 0.0, a = 0.0;
+        for (int r = 0; r < N; ++r) {
+            double x = (double)bits_to_f32(widen_bits(load(in[r], dtype, e), dtype));
+            s += x;
+            a += x < 0 ? -x : x;
+        }
+        y[e] = op == OR_AVG ? s / (double)N : s;
+        absum[e] = op == OR_AVG ? a / (double)N : a;
+    }
+    return OR_OK;
+}
