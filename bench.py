@@ -1,0 +1,354 @@
+"""Benchmark: fused ring-order AllReduce, N=8 simulated ranks, bf16, AVG,
+64Mi elements (128 MiB) per rank, in place, on one GB300.
+
+One step = one ccl_allreduce call over the whole arena (the ReduceScatter
+phase, the AVG scaling and the AllGather phase, computed in one launch).
+Metric: algorithmic HBM bytes (N*M read + N*M written = 2 GiB per step) per
+second.  Inputs (1 GiB read per step) are larger than the 129 MB L2, so no
+flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--gpus N > 1 runs N independent replicas (one per GPU, launched by
+torch.distributed.run): the path has no cross-GPU exchange.  --impl reference
+times the CPU oracle on the host cores on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "AllReduce HBM GB/s & % of peak, N=8 bf16 128 MB/rank, 1 GB300"
+UNIT = "GB/s"
+NRANKS = 8
+COUNT = 64 * 1024 * 1024  # bf16 elements per rank (128 MiB)
+ELEM = 2
+ALG_BYTES = 2 * NRANKS * COUNT * ELEM  # N*M read + N*M written
+WORKLOAD = "allreduce-avg N=8 bf16 64Mi elements/rank (128 MiB), in place, fused ring order"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_allreduce_bf16_n8_128mib.traffic")
+KERNEL_SOURCES = ["ring_allreduce_rank_gb300/csrc/reduce.cu", "ring_allreduce_rank_gb300/csrc/ccl_device.cuh",
+                  "ring_allreduce_rank_gb300/csrc/ccl_internal.h"]
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style torch copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        kv = dict(line.split("=", 1) for line in open(TRAFFIC_FILE).read().split() if "=" in line)
+        if kv.get("kernel_digest") != kernel_digest():
+            return None
+        return int(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = [l.split(",") for l in open(self.file.name).read().strip().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle timing (CPU)
+
+def oracle_sample_gbs(target_s: float, max_count: int = COUNT):
+    """Time the CPU oracle (step-by-step ring simulation, single thread) on a
+    sample of the workload: N=8 ranks, a prefix length of the per-rank buffer
+    sized to take about target_s seconds.  Returns (GB/s, sample description)."""
+    import oracle
+    from ring_allreduce_rank_gb300 import workloads as W
+
+    oracle.build()
+    k = 1 << 18
+    while True:
+        x = list(W.normal_bf16(NRANKS, k, std=1e-3, seed_base=0))
+        t0 = time.perf_counter()
+        oracle.ring_allreduce(x, "avg")
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4 or k >= max_count:
+            break
+        k = min(max_count, int(k * max(2.0, min(16.0, target_s / max(dt, 1e-3) / 2))))
+    gbs = 2 * NRANKS * k * ELEM / dt / 1e9
+    return gbs, dt, k
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args)
+        return
+
+    import torch
+
+    import ring_allreduce_rank_gb300 as ccl
+    from ring_allreduce_rank_gb300 import workloads as W
+    from ring_allreduce_rank_gb300.arena import RankArena
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    ccl.lib()
+
+    x = W.normal_bf16(NRANKS, COUNT, std=1e-3, seed_base=0)
+    arena = RankArena(NRANKS, COUNT, torch.bfloat16, device=dev)
+    arena.load([r.view(np.int16) for r in x])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ccl.ccl_allreduce(arena.ranks, op="avg", mode="fused", stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = ccl.ccl_launch_count()
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = ccl.ccl_launch_count() - n0
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+
+    total_ms = t_all0.elapsed_time(t_all1)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * ALG_BYTES * args.steps / (total_ms / 1e3) / 1e9
+
+    avg_launch_s = statistics.mean(per_launch_ms) / 1e3
+    achieved = ALG_BYTES / avg_launch_s / 1e9
+    peak, peak_src = measured_peak()
+    traffic = recorded_traffic()
+
+    # end to end through the public API with host buffers: pinned host -> arena,
+    # AllReduce, arena -> pinned host, every step
+    host_in = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    host_out = torch.empty((NRANKS, COUNT), dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        e2e_step(ccl, arena, host_in, host_out, stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step(ccl, arena, host_in, host_out, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = world * ALG_BYTES * args.e2e_steps / (e2e_ms / 1e3) / 1e9
+
+    # alpha: one tiny AllReduce (latency of a launch through the API)
+    tiny = [torch.zeros(8, dtype=torch.bfloat16, device=dev) for _ in range(NRANKS)]
+    for _ in range(5):
+        ccl.ccl_allreduce(tiny, op="sum", stream=stream)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(50):
+        ccl.ccl_allreduce(tiny, op="sum", stream=stream)
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    alpha_s = a0.elapsed_time(a1) / 50 / 1e3
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, dt, k = oracle_sample_gbs(target_s=12.0)
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "N=8 bf16 AVG, first %d of %d elements per rank (%.1f s), step-by-step ring "
+                         "simulation in plain C, one thread" % (k, COUNT, dt)}
+
+    if rank != 0:
+        return
+    M = COUNT * ELEM
+    algbw = M / (ms_per_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "nranks": NRANKS, "count_per_rank": COUNT, "op": "avg",
+                   "mode": "fused", "inputs": "Normal(0, 1e-3) bf16, per-rank seeds",
+                   "l2": "inputs larger than L2 (1 GiB read per step > 129 MB), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ALG_BYTES, "peak_source": peak_src,
+                     "kernel": "fused_reduce_kernel<bf16, AVG, 8 ranks>"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": NRANKS * COUNT * ELEM,
+                "d2h_bytes_per_step": NRANKS * COUNT * ELEM, "steps": args.e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "alpha_beta": {"algbw_GBs": round(algbw, 2), "busbw_GBs": round(algbw * 2 * (NRANKS - 1) / NRANKS, 2),
+                       "alpha_us": round(alpha_s * 1e6, 3), "beta_GBs": peak,
+                       "model_ms": round((2 * (NRANKS - 1) * alpha_s + 2 * (NRANKS - 1) / NRANKS * M /
+                                          (peak * 1e9)) * 1e3, 4),
+                       "formula": "algbw = M/t; busbw = algbw*2(N-1)/N; T = 2(N-1)alpha + 2(N-1)/N * M/beta, "
+                                  "M = bytes per rank, alpha = one tiny AllReduce, beta = HBM peak"},
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def e2e_step(ccl, arena, host_in, host_out, stream):
+    for r in range(NRANKS):
+        arena.ranks[r].copy_(host_in[r], non_blocking=True)
+    ccl.ccl_allreduce(arena.ranks, op="avg", mode="fused", stream=stream)
+    for r in range(NRANKS):
+        host_out[r].copy_(arena.ranks[r], non_blocking=True)
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is one step-by-step ring
+    AllReduce of a bounded sample of the workload on the host cores."""
+    import oracle
+    from ring_allreduce_rank_gb300 import workloads as W
+
+    oracle.build()
+    steps, warm = args.steps, max(args.warmup, 3)
+    budget = 150.0
+    _, dt, k = oracle_sample_gbs(target_s=budget / (steps + warm) * 2, max_count=COUNT)
+    x = list(W.normal_bf16(NRANKS, k, std=1e-3, seed_base=0))
+    for _ in range(warm):
+        oracle.ring_allreduce(x, "avg")
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.ring_allreduce(x, "avg")
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    val = 2 * NRANKS * k * ELEM * steps / tot / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": UNIT, "n_gpus": 1,
+            "steps": steps, "warmup": warm, "ms_per_step": round(tot / steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "nranks": NRANKS, "count_per_rank": COUNT, "op": "avg",
+                       "mode": "fused"},
+            "cpu_baseline": {"value": round(val, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "N=8 bf16 AVG, first %d of %d elements per rank per step, step-by-step "
+                                       "ring simulation in plain C, one thread" % (k, COUNT)},
+            "e2e": {"value": round(val, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

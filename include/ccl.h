@@ -1,0 +1,190 @@
+/*
+ * ccl.h -- C ABI of the single-GPU ring-collective library (libccl.so).
+ *
+ * N "ranks" are simulated on one GPU: each rank is a buffer in device memory
+ * (normally a slice of one arena allocation).  Every collective computes the
+ * exact data semantics of the textbook ring algorithm on the device:
+ *
+ *   ReduceScatter phase, step s = 0..N-2: rank i sends chunk (i-s) mod N to
+ *   rank i+1 and adds the chunk (i-1-s) mod N arriving from rank i-1 into its
+ *   own copy; AllGather phase: rank i forwards chunk (i+1-s) mod N and stores
+ *   chunk (i-s) mod N.  (Collectives and sharded matmul, "ring ReduceScatter"
+ *   and "ring AllGather"; AllReduce survey, "Algorithm 1: Ring AllReduce",
+ *   phase 1 and 2; Collective Communication, Algorithm 1.)
+ *
+ * Chunk c of a K-element buffer holds len_c = K/N + (c < K mod N) elements
+ * starting at off_c = sum_{d<c} len_d (the pages split evenly; the first
+ * K mod N chunks take the remainder).  Chunk c is therefore folded in the order
+ * x_c, x_{c+1}, ..., x_{c-1} (ranks mod N): each hop is one IEEE fp32 operation
+ * rounded to nearest-even, followed by a round to the buffer type (identity for
+ * fp32, round-to-nearest-even for bf16).  A NaN result is the canonical quiet
+ * NaN (fp32 0x7FFFFFFF, bf16 0x7FFF).  AVG sums around the ring, then divides
+ * the finished chunk once by N in fp32 before the gather, so every rank gets
+ * identical bits.  MAX is NaN if either side is NaN, else the larger, and
+ * +0 against -0 gives +0.
+ *
+ * Common conventions
+ *   - Pointer arrays (send[], recv[], ptrs[]) are HOST arrays of nranks DEVICE
+ *     pointers.  The caller owns every buffer; the library never frees them.
+ *   - All entry points that take a stream are asynchronous: they validate
+ *     their arguments on the host, enqueue kernels on `stream` (0 = legacy
+ *     default stream) and return.  Completion is stream completion
+ *     (Collective Communication, section on correctness: a non-blocking return
+ *     means work in flight, not work done).
+ *   - Argument errors are returned before anything is enqueued: NULL pointers,
+ *     nranks outside [1, CCL_MAX_RANKS], counts that overflow, unknown dtype,
+ *     op or mode, root out of range, and buffers that partially overlap
+ *     (CCL_ERR_OVERLAP).  A CUDA launch error is returned as CCL_ERR_CUDA.
+ *     Nothing aborts or traps.
+ *   - count == 0 is a no-op returning CCL_OK; nranks == 1 is a copy (or
+ *     nothing, in place).
+ *   - In-place: send[r] == recv[r] is allowed for every rank.  Any other
+ *     overlap between two buffers that the same call writes and reads is an
+ *     error, except the in-place forms noted per call.
+ *   - CCL_MODE_FUSED computes the ring's end state in one pass over memory (one
+ *     launch).  CCL_MODE_STEP executes the ring's 2(N-1) steps one launch per
+ *     step, in stream order, for validating the schedule; it gives identical
+ *     bits and is slower.
+ */
+#ifndef CCL_H
+#define CCL_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CCL_MAX_RANKS 1024
+#define CCL_DEFAULT_BUCKET_BYTES (25u * 1024u * 1024u)
+
+typedef enum { CCL_FP32 = 0, CCL_BF16 = 1 } ccl_dtype_t;
+typedef enum { CCL_SUM = 0, CCL_AVG = 1, CCL_MAX = 2, CCL_PROD = 3 } ccl_op_t;
+typedef enum { CCL_MODE_FUSED = 0, CCL_MODE_STEP = 1 } ccl_mode_t;
+typedef enum {
+    CCL_OK = 0,
+    CCL_ERR_INVALID_ARG = 1,
+    CCL_ERR_UNSUPPORTED = 2,
+    CCL_ERR_OVERLAP = 3,
+    CCL_ERR_CUDA = 4,
+    CCL_ERR_NO_MEMORY = 5,
+    CCL_ERR_TIMEOUT = 6,
+    CCL_ERR_CHECK_FAILED = 7
+} ccl_status_t;
+
+/* ------------------------------------------------------------------ */
+/* Collectives                                                         */
+/* ------------------------------------------------------------------ */
+
+/* AllReduce: every rank ends with the reduction of all ranks' buffers
+ * (Collectives and sharded matmul, "Reduce and AllReduce"; Collective
+ * Communication, table of the six core primitives: y_i = sum_j x_j for all i).
+ * send[r], recv[r]: `count` elements each.  In place when send[r] == recv[r].
+ * Result: the ring fold of chunk c starting at rank c, on every rank. */
+ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nranks, size_t count,
+                           ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream);
+
+/* ReduceScatter: rank r receives chunk r of the reduction (Collectives and
+ * sharded matmul, "Scatter and ReduceScatter": the sum of block r goes only to
+ * rank r).  send[r]: `count` elements; recv[r]: len_r elements.  The fold
+ * order is the AllReduce's (start at rank r), so ReduceScatter followed by
+ * AllGather is bit-identical to AllReduce.  In place when
+ * recv[r] == send[r] + off_r elements. */
+ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream);
+
+/* AllGather: send[r] holds len_r elements (chunk r of a `count`-element
+ * result); every recv[q] receives all `count` elements, chunks in rank order
+ * (Collectives and sharded matmul, "Gather and AllGather").  In place when
+ * send[r] == recv[r] + off_r elements. */
+ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nranks, size_t count,
+                           ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
+
+/* Broadcast: every recv[q] receives root's `count` elements
+ * (Collectives and sharded matmul, "Broadcast").  Only send[root] is read;
+ * other send[] entries may be NULL.  Step mode chains root -> root+1 -> ...
+ * one hop per launch. */
+ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                           ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
+
+/* AllToAll, uniform blocks: send[i] holds nranks blocks of `count` elements
+ * ordered by destination; recv[j] receives nranks blocks ordered by source:
+ * recv[j][i*count + t] = send[i][j*count + t] ("rank = row, block = column:
+ * a transpose", Collectives and sharded matmul, "AllToAll"; Collective
+ * Communication, Figure 5).  send and recv buffers must not overlap. */
+ccl_status_t ccl_alltoall(const void *const *send, void *const *recv, int nranks, size_t count,
+                          ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
+
+/* AllToAllv: counts is a HOST array of nranks*nranks element counts,
+ * counts[i*nranks + j] = elements rank i sends to rank j.  send[i] holds its
+ * blocks ordered by destination, recv[j] its blocks ordered by source, both at
+ * prefix-sum displacements (explicit per-destination counts and displacements,
+ * Collective Communication, section on correctness).  Step mode follows the
+ * pairwise schedule: at step k rank i sends to (i+k) mod N (Distributed LLM
+ * collectives, "Pairwise algorithm"). */
+ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nranks, const size_t *counts,
+                           ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
+
+/* Bucket-fused gradient AllReduce (Collective Communication, "Bucket fusion").
+ * Each rank registers ntensors gradient tensors in forward order:
+ * ptrs[r*ntensors + t] is rank r's tensor t (numels[t] elements, HOST array).
+ * The tensors are laid end to end in REVERSE registration order, the stream is
+ * cut into buckets of bucket_bytes (0 = CCL_DEFAULT_BUCKET_BYTES, 25 MiB; the
+ * last bucket is partial and a tensor may span buckets) and every bucket is
+ * ring-AllReduced on its own, with its own N-chunk partition.  In place on the
+ * tensors; nothing is copied into a staging bucket (the kernel reads and writes
+ * the pieces where they are). */
+ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int ntensors, int nranks,
+                                  size_t bucket_bytes, ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode,
+                                  cudaStream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Planner (host only; no GPU needed)                                  */
+/* ------------------------------------------------------------------ */
+
+/* Chunk partition of `count` elements over nranks: off[c], len[c] (HOST arrays
+ * of nranks entries, written by the call). */
+ccl_status_t ccl_plan_chunks(size_t count, int nranks, size_t *off, size_t *len);
+
+/* Ring step table, HOST array of 2*(nranks-1)*nranks*3 int32 laid out
+ * [phase][s][rank] = {send chunk, recv chunk, source rank}; phase 0 is the
+ * ReduceScatter phase, phase 1 the AllGather phase. */
+ccl_status_t ccl_plan_ring_schedule(int nranks, int32_t *table);
+
+/* Bucket boundaries of the reversed tensor stream: writes min(nbuckets,
+ * max_buckets)+1 stream offsets into starts (bucket b covers
+ * [starts[b], starts[b+1])) and the bucket count into *nbuckets. */
+ccl_status_t ccl_plan_buckets(const size_t *numels, int ntensors, size_t bucket_elems, size_t *starts,
+                              size_t max_buckets, size_t *nbuckets);
+
+/* AllToAllv displacements: sdispl[i*N+j] = elements before block j in
+ * send[i]; rdispl[j*N+i] = elements before block i in recv[j]. */
+ccl_status_t ccl_plan_alltoallv(int nranks, const size_t *counts, size_t *sdispl, size_t *rdispl);
+
+/* Arena layout: per-rank stride (bytes_per_rank rounded up to `align`, a power
+ * of two >= 256) and total bytes for nranks rank buffers in one allocation. */
+ccl_status_t ccl_arena_layout(int nranks, size_t bytes_per_rank, size_t align, size_t *stride, size_t *total);
+
+/* ------------------------------------------------------------------ */
+/* Misc                                                                */
+/* ------------------------------------------------------------------ */
+
+const char *ccl_status_string(ccl_status_t status);
+int ccl_version(void);
+
+/* Number of kernels this library has enqueued since it was loaded (host-side
+ * counter, for accounting; thread-safe). */
+unsigned long long ccl_launch_count(void);
+
+/* Frees the library's cached device workspace on the current device (used by
+ * step-mode ReduceScatter only).  Safe to call at any time when no call of this
+ * library is in flight. */
+ccl_status_t ccl_finalize(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCL_H */

@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_ring_allreduce.argtypes = [pp, i32, u64, i32, i32, p64]
             L.oracle_ring_allreduce_closed.argtypes = [pp, pp, i32, u64, i32, i32]
             L.oracle_ring_allreduce_at.argtypes = [pp, i32, u64, i32, i32, p64, u64, vp]
+            L.oracle_ring_allreduce_gathered.argtypes = [pp, i32, u64, i32, i32, p64, u64, vp]
             L.oracle_reduce_scatter.argtypes = [pp, pp, i32, u64, i32, i32]
             L.oracle_allgather.argtypes = [pp, pp, i32, u64, i32]
             L.oracle_broadcast.argtypes = [pp, pp, i32, i32, u64, i32]
@@ -71,7 +72,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_bucket_allreduce.argtypes = [pp, p64, i32, i32, u64, i32, i32]
             L.oracle_sum_f64.argtypes = [pp, i32, u64, i32, i32, vp, vp]
             for name in ("oracle_ring_allreduce", "oracle_ring_allreduce_closed", "oracle_ring_allreduce_at",
-                         "oracle_reduce_scatter", "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
+                         "oracle_ring_allreduce_gathered", "oracle_reduce_scatter", "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
                          "oracle_bucket_allreduce", "oracle_sum_f64"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -162,6 +163,17 @@ def ring_allreduce_at(bufs, idx, op="sum") -> np.ndarray:
     _check(lib().oracle_ring_allreduce_at(_ptrs(ins), len(ins), ins[0].size, _dtype_code(ins[0]), _op(op),
                                           idx.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), idx.size,
                                           out.ctypes.data), "oracle_ring_allreduce_at")
+    return out
+
+
+def ring_allreduce_gathered(vals, K: int, idx, op="sum") -> np.ndarray:
+    """vals[r] = rank r's elements at the indices idx (of K-element buffers)."""
+    ins = [np.ascontiguousarray(v) for v in vals]
+    idx = np.ascontiguousarray(idx, dtype=np.uint64)
+    out = np.empty(idx.size, dtype=ins[0].dtype)
+    _check(lib().oracle_ring_allreduce_gathered(_ptrs(ins), len(ins), K, _dtype_code(ins[0]), _op(op),
+                                                idx.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), idx.size,
+                                                out.ctypes.data), "oracle_ring_allreduce_gathered")
     return out
 
 

@@ -340,6 +340,35 @@ int oracle_ring_allreduce_at(const void **in, int N, uint64_t K, int dtype, int 
     return OR_OK;
 }
 
+/* Closed form at listed positions, from the contributions already gathered:
+ * vals[r][t] is rank r's element at index idx[t] of a K-element buffer.  Lets
+ * a caller check huge buffers whose inputs it can regenerate at the sampled
+ * positions without materialising them. */
+int oracle_ring_allreduce_gathered(const void **vals, int N, uint64_t K, int dtype, int op,
+                                   const uint64_t *idx, uint64_t n, void *out)
+{
+    if (bad_args(N, dtype, op))
+        return OR_EINVAL;
+    uint64_t q = K / (uint64_t)N, rem = K % (uint64_t)N;
+    for (uint64_t t = 0; t < n; ++t) {
+        uint64_t e = idx[t];
+        if (e >= K)
+            return OR_EINVAL;
+        int c;
+        if (e < rem * (q + 1))
+            c = (int)(e / (q + 1));
+        else
+            c = (int)(rem + (e - rem * (q + 1)) / q);
+        uint32_t acc = load(vals[c], dtype, t);
+        for (int k = 1; k < N; ++k)
+            acc = hop(load(vals[(c + k) % N], dtype, t), acc, dtype, op);
+        if (op == OR_AVG)
+            acc = avg_scale(acc, N, dtype);
+        store(out, dtype, t, acc);
+    }
+    return OR_OK;
+}
+
 /* ReduceScatter API: rank r receives the finished chunk r (len_r elements).
  * Runs the ring ReduceScatter phase step by step on copies of the inputs; the
  * phase leaves chunk r at rank r-1, and the API hands it to rank r

@@ -1,0 +1,236 @@
+"""Thin Python binding of libccl.so (include/ccl.h).
+
+Argument marshalling only: torch tensors become device pointers, element
+counts and dtype codes, and the call goes straight to the C ABI, which runs
+every step in the library's own CUDA kernels.  There is no fallback: if the
+library is not built, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+FP32, BF16 = 0, 1
+SUM, AVG, MAX, PROD = 0, 1, 2, 3
+FUSED, STEP = 0, 1
+OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD}
+MODES = {"fused": FUSED, "step": STEP}
+STATUS = {0: "CCL_OK", 1: "CCL_ERR_INVALID_ARG", 2: "CCL_ERR_UNSUPPORTED", 3: "CCL_ERR_OVERLAP",
+          4: "CCL_ERR_CUDA", 5: "CCL_ERR_NO_MEMORY", 6: "CCL_ERR_TIMEOUT", 7: "CCL_ERR_CHECK_FAILED"}
+MAX_RANKS = 1024
+DEFAULT_BUCKET_BYTES = 25 * 1024 * 1024
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CclError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s returned %s" % (where, STATUS.get(status, status)))
+
+
+def lib() -> ctypes.CDLL:
+    """Load libccl.so (built in-tree); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError("libccl.so is not built (%s); run `python -m ring_allreduce_rank_gb300.build` "
+                                   "or __graft_entry__.build()" % _LIB_PATH)
+            L = ctypes.CDLL(_LIB_PATH)
+            vp, pp, i32, sz = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_size_t
+            psz = ctypes.POINTER(ctypes.c_size_t)
+            sig = {
+                "ccl_allreduce": [pp, pp, i32, sz, i32, i32, i32, vp],
+                "ccl_reduce_scatter": [pp, pp, i32, sz, i32, i32, i32, vp],
+                "ccl_allgather": [pp, pp, i32, sz, i32, i32, vp],
+                "ccl_broadcast": [pp, pp, i32, i32, sz, i32, i32, vp],
+                "ccl_alltoall": [pp, pp, i32, sz, i32, i32, vp],
+                "ccl_alltoallv": [pp, pp, i32, psz, i32, i32, vp],
+                "ccl_bucket_allreduce": [pp, psz, i32, i32, sz, i32, i32, i32, vp],
+                "ccl_plan_chunks": [sz, i32, psz, psz],
+                "ccl_plan_ring_schedule": [i32, ctypes.POINTER(ctypes.c_int32)],
+                "ccl_plan_buckets": [psz, i32, sz, psz, sz, psz],
+                "ccl_plan_alltoallv": [i32, psz, psz, psz],
+                "ccl_arena_layout": [i32, sz, sz, psz, psz],
+                "ccl_finalize": [],
+            }
+            for name, args in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            L.ccl_status_string.argtypes = [ctypes.c_int]
+            L.ccl_status_string.restype = ctypes.c_char_p
+            L.ccl_version.argtypes = []
+            L.ccl_version.restype = ctypes.c_int
+            L.ccl_launch_count.argtypes = []
+            L.ccl_launch_count.restype = ctypes.c_ulonglong
+            _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise CclError(status, where)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return FP32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("ccl supports float32 and bfloat16 tensors, got %s" % t.dtype)
+
+
+def _ptrs(ts: Sequence[Optional[torch.Tensor]]) -> ctypes.Array:
+    vals = []
+    for t in ts:
+        if t is None:
+            vals.append(None)
+            continue
+        if not t.is_contiguous():
+            raise ValueError("rank buffers must be contiguous")
+        vals.append(t.data_ptr())
+    return (ctypes.c_void_p * max(1, len(vals)))(*vals)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _op(op) -> int:
+    return OPS[op] if isinstance(op, str) else int(op)
+
+
+def _mode(mode) -> int:
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def _sizes(vals) -> ctypes.Array:
+    vals = [int(v) for v in vals]
+    return (ctypes.c_size_t * max(1, len(vals)))(*vals)
+
+
+# ------------------------------------------------------------------ collectives
+
+def ccl_allreduce(send: Sequence[torch.Tensor], recv: Optional[Sequence[torch.Tensor]] = None, op="sum",
+                  mode="fused", stream=None) -> None:
+    """AllReduce over len(send) simulated ranks; recv=None means in place."""
+    recv = send if recv is None else recv
+    n = len(send)
+    _check(lib().ccl_allreduce(_ptrs(send), _ptrs(recv), n, send[0].numel(), _dtype(send[0]), _op(op), _mode(mode),
+                               _stream(stream)), "ccl_allreduce")
+
+
+def ccl_reduce_scatter(send: Sequence[torch.Tensor], recv: Sequence[torch.Tensor], op="sum", mode="fused",
+                       stream=None) -> None:
+    """recv[r] (len_r elements) receives chunk r of the ring reduction of send."""
+    _check(lib().ccl_reduce_scatter(_ptrs(send), _ptrs(recv), len(send), send[0].numel(), _dtype(send[0]), _op(op),
+                                    _mode(mode), _stream(stream)), "ccl_reduce_scatter")
+
+
+def ccl_allgather(send: Sequence[torch.Tensor], recv: Sequence[torch.Tensor], mode="fused", stream=None) -> None:
+    """send[r] is chunk r (len_r elements); every recv[q] gets all chunks."""
+    _check(lib().ccl_allgather(_ptrs(send), _ptrs(recv), len(recv), recv[0].numel(), _dtype(recv[0]), _mode(mode),
+                               _stream(stream)), "ccl_allgather")
+
+
+def ccl_broadcast(send: Sequence[Optional[torch.Tensor]], recv: Sequence[torch.Tensor], root: int = 0,
+                  mode="fused", stream=None) -> None:
+    _check(lib().ccl_broadcast(_ptrs(send), _ptrs(recv), len(recv), int(root), recv[0].numel(), _dtype(recv[0]),
+                               _mode(mode), _stream(stream)), "ccl_broadcast")
+
+
+def ccl_alltoall(send: Sequence[torch.Tensor], recv: Sequence[torch.Tensor], mode="fused", stream=None) -> None:
+    n = len(send)
+    if send[0].numel() % n:
+        raise ValueError("uniform AllToAll needs numel divisible by the number of ranks")
+    _check(lib().ccl_alltoall(_ptrs(send), _ptrs(recv), n, send[0].numel() // n, _dtype(send[0]), _mode(mode),
+                              _stream(stream)), "ccl_alltoall")
+
+
+def ccl_alltoallv(send: Sequence[torch.Tensor], recv: Sequence[torch.Tensor], counts, mode="fused",
+                  stream=None) -> None:
+    """counts[i][j] elements go from rank i to rank j (host data)."""
+    n = len(send)
+    flat = [int(counts[i][j]) for i in range(n) for j in range(n)]
+    dt = _dtype(next(t for t in list(send) + list(recv) if t is not None))
+    _check(lib().ccl_alltoallv(_ptrs(send), _ptrs(recv), n, _sizes(flat), dt, _mode(mode), _stream(stream)),
+           "ccl_alltoallv")
+
+
+def ccl_bucket_allreduce(tensors: Sequence[Sequence[torch.Tensor]], bucket_bytes: int = DEFAULT_BUCKET_BYTES,
+                         op="sum", mode="fused", stream=None) -> None:
+    """tensors[r][t]: rank r's t-th gradient in registration order (in place)."""
+    nranks, nt = len(tensors), len(tensors[0])
+    flat = [tensors[r][t] for r in range(nranks) for t in range(nt)]
+    numels = [tensors[0][t].numel() for t in range(nt)]
+    _check(lib().ccl_bucket_allreduce(_ptrs(flat), _sizes(numels), nt, nranks, int(bucket_bytes),
+                                      _dtype(flat[0]), _op(op), _mode(mode), _stream(stream)),
+           "ccl_bucket_allreduce")
+
+
+# ------------------------------------------------------------------ planner
+
+def ccl_plan_chunks(count: int, nranks: int):
+    off, ln = (ctypes.c_size_t * nranks)(), (ctypes.c_size_t * nranks)()
+    _check(lib().ccl_plan_chunks(count, nranks, off, ln), "ccl_plan_chunks")
+    return list(off), list(ln)
+
+
+def ccl_plan_ring_schedule(nranks: int):
+    steps = max(nranks - 1, 0)
+    n = max(1, 2 * steps * nranks * 3)
+    buf = (ctypes.c_int32 * n)()
+    _check(lib().ccl_plan_ring_schedule(nranks, buf), "ccl_plan_ring_schedule")
+    flat = list(buf)[:2 * steps * nranks * 3]
+    return [[[tuple(flat[((ph * steps + s) * nranks + i) * 3:((ph * steps + s) * nranks + i) * 3 + 3])
+              for i in range(nranks)] for s in range(steps)] for ph in range(2)]
+
+
+def ccl_plan_buckets(numels, bucket_elems: int):
+    nb = ctypes.c_size_t()
+    _check(lib().ccl_plan_buckets(_sizes(numels), len(numels), bucket_elems, None, 0, ctypes.byref(nb)),
+           "ccl_plan_buckets")
+    starts = (ctypes.c_size_t * (nb.value + 1))()
+    _check(lib().ccl_plan_buckets(_sizes(numels), len(numels), bucket_elems, starts, nb.value, ctypes.byref(nb)),
+           "ccl_plan_buckets")
+    return list(starts)
+
+
+def ccl_plan_alltoallv(counts):
+    n = len(counts)
+    flat = [int(counts[i][j]) for i in range(n) for j in range(n)]
+    sd, rd = (ctypes.c_size_t * (n * n))(), (ctypes.c_size_t * (n * n))()
+    _check(lib().ccl_plan_alltoallv(n, _sizes(flat), sd, rd), "ccl_plan_alltoallv")
+    return [list(sd)[i * n:(i + 1) * n] for i in range(n)], [list(rd)[j * n:(j + 1) * n] for j in range(n)]
+
+
+def ccl_arena_layout(nranks: int, bytes_per_rank: int, align: int = 256):
+    stride, total = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().ccl_arena_layout(nranks, bytes_per_rank, align, ctypes.byref(stride), ctypes.byref(total)),
+           "ccl_arena_layout")
+    return stride.value, total.value
+
+
+def ccl_status_string(status: int) -> str:
+    return lib().ccl_status_string(status).decode()
+
+
+def ccl_launch_count() -> int:
+    return int(lib().ccl_launch_count())
+
+
+def ccl_finalize() -> None:
+    _check(lib().ccl_finalize(), "ccl_finalize")

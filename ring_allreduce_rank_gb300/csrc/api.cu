@@ -1,0 +1,606 @@
+// api.cu -- the exported C ABI (include/ccl.h): argument validation, planning
+// (chunk partition, ring steps, bucket segments, all-to-all displacements) and
+// dispatch to the kernels.
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/ccl.h"
+#include "ccl_internal.h"
+
+namespace ccl {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(unsigned long long n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+size_t elem_size(ccl_dtype_t dt) { return dt == CCL_BF16 ? 2 : 4; }
+bool valid_dtype(ccl_dtype_t dt) { return dt == CCL_FP32 || dt == CCL_BF16; }
+bool valid_op(ccl_op_t op) { return op == CCL_SUM || op == CCL_AVG || op == CCL_MAX || op == CCL_PROD; }
+bool valid_mode(ccl_mode_t m) { return m == CCL_MODE_FUSED || m == CCL_MODE_STEP; }
+bool valid_ranks(int n) { return n >= 1 && n <= CCL_MAX_RANKS; }
+
+bool mul_overflows(size_t a, size_t b) { return a != 0 && b > SIZE_MAX / a; }
+
+ccl_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CCL_OK : CCL_ERR_CUDA; }
+
+// A byte range touched by a call: lo/hi, which rank, read or write.
+struct Range {
+    uintptr_t lo, hi;
+    int rank;
+};
+
+// Writes must be pairwise disjoint; a read may overlap a write only in one of
+// the call's in-place forms, decided by `allowed(read, write)`.
+template <class Allowed>
+ccl_status_t check_overlaps(std::vector<Range> writes, const std::vector<Range> &reads, Allowed allowed)
+{
+    writes.erase(std::remove_if(writes.begin(), writes.end(), [](const Range &r) { return r.lo == r.hi; }),
+                 writes.end());
+    std::sort(writes.begin(), writes.end(), [](const Range &a, const Range &b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < writes.size(); ++i)
+        if (writes[i].lo < writes[i - 1].hi)
+            return CCL_ERR_OVERLAP;
+    for (const Range &r : reads) {
+        if (r.lo == r.hi)
+            continue;
+        // first write whose end is past the read's start (ends are sorted too)
+        auto it = std::upper_bound(writes.begin(), writes.end(), r.lo,
+                                   [](uintptr_t v, const Range &w) { return v < w.hi; });
+        for (; it != writes.end() && it->lo < r.hi; ++it)
+            if (!allowed(r, *it))
+                return CCL_ERR_OVERLAP;
+    }
+    return CCL_OK;
+}
+
+Range range_of(const void *p, size_t bytes, int rank)
+{
+    return Range{(uintptr_t)p, (uintptr_t)p + bytes, rank};
+}
+
+Partition make_partition(size_t count, int nranks)
+{
+    Partition p;
+    p.q = count / (uint64_t)nranks;
+    p.rem = (uint32_t)(count % (uint64_t)nranks);
+    return p;
+}
+
+// ------------------------------------------------------------------ workspace
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::unordered_map<int, Workspace> g_ws;
+
+ccl_status_t get_workspace(size_t bytes, void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace &w = g_ws[dev];
+    if (w.bytes < bytes) {
+        if (w.ptr)
+            cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (cudaMalloc(&w.ptr, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            w.ptr = nullptr;
+            return CCL_ERR_NO_MEMORY;
+        }
+        w.bytes = bytes;
+    }
+    *out = w.ptr;
+    return CCL_OK;
+}
+
+// ------------------------------------------------------------------ step-mode helpers
+
+// The ring's two phases, step by step, in place on bufs (full K-element buffers).
+ccl_status_t ring_steps_allreduce(int dt, int op, void *const *bufs, int nranks, size_t count, cudaStream_t st)
+{
+    for (int s = 0; s < nranks - 1; ++s)
+        if (cudaError_t e = launch_ring_step(dt, op, STEP_RS, s, bufs, nranks, count, st))
+            return from_cuda(e);
+    if (op == OP_AVG)
+        if (cudaError_t e = launch_ring_step(dt, op, STEP_SCALE, 0, bufs, nranks, count, st))
+            return from_cuda(e);
+    for (int s = 0; s < nranks - 1; ++s)
+        if (cudaError_t e = launch_ring_step(dt, op, STEP_AG, s, bufs, nranks, count, st))
+            return from_cuda(e);
+    return CCL_OK;
+}
+
+ccl_status_t copy_ranks(const void *const *src, void *const *dst, int nranks, size_t bytes, cudaStream_t st)
+{
+    std::vector<CopySeg> segs;
+    for (int r = 0; r < nranks; ++r)
+        if (src[r] != dst[r])
+            segs.push_back(CopySeg{static_cast<const char *>(src[r]), static_cast<char *>(dst[r]), bytes, 0});
+    return from_cuda(launch_copy_segments(segs.data(), segs.size(), st));
+}
+
+} // namespace
+} // namespace ccl
+
+using namespace ccl;
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char *ccl_status_string(ccl_status_t s)
+{
+    switch (s) {
+    case CCL_OK: return "ok";
+    case CCL_ERR_INVALID_ARG: return "invalid argument";
+    case CCL_ERR_UNSUPPORTED: return "unsupported";
+    case CCL_ERR_OVERLAP: return "buffers overlap";
+    case CCL_ERR_CUDA: return "CUDA error";
+    case CCL_ERR_NO_MEMORY: return "out of device memory";
+    case CCL_ERR_TIMEOUT: return "timeout";
+    case CCL_ERR_CHECK_FAILED: return "result check failed";
+    }
+    return "unknown status";
+}
+
+int ccl_version(void) { return 10000; }
+
+unsigned long long ccl_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+ccl_status_t ccl_finalize(void)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    auto it = g_ws.find(dev);
+    if (it != g_ws.end()) {
+        if (it->second.ptr)
+            cudaFree(it->second.ptr);
+        g_ws.erase(it);
+    }
+    return CCL_OK;
+}
+
+// ------------------------------------------------------------------ planner
+
+ccl_status_t ccl_plan_chunks(size_t count, int nranks, size_t *off, size_t *len)
+{
+    if (!valid_ranks(nranks) || !off || !len)
+        return CCL_ERR_INVALID_ARG;
+    const Partition p = make_partition(count, nranks);
+    for (int c = 0; c < nranks; ++c) {
+        off[c] = (size_t)p.off((uint32_t)c);
+        len[c] = (size_t)p.len((uint32_t)c);
+    }
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_ring_schedule(int nranks, int32_t *table)
+{
+    if (!valid_ranks(nranks) || (!table && nranks > 1))
+        return CCL_ERR_INVALID_ARG;
+    const int steps = nranks - 1;
+    for (int phase = 0; phase < 2; ++phase)
+        for (int s = 0; s < steps; ++s)
+            for (int i = 0; i < nranks; ++i) {
+                int32_t *e = table + (((size_t)phase * steps + s) * nranks + i) * 3;
+                // ReduceScatter: send (i-s), receive (i-1-s); AllGather: send (i+1-s), receive (i-s)
+                e[0] = ring_mod(phase == 0 ? i - s : i + 1 - s, nranks);
+                e[1] = ring_mod(phase == 0 ? i - 1 - s : i - s, nranks);
+                e[2] = ring_mod(i - 1, nranks);
+            }
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_buckets(const size_t *numels, int ntensors, size_t bucket_elems, size_t *starts,
+                              size_t max_buckets, size_t *nbuckets)
+{
+    if (ntensors < 0 || (ntensors > 0 && !numels) || bucket_elems == 0 || !nbuckets)
+        return CCL_ERR_INVALID_ARG;
+    size_t total = 0;
+    for (int t = 0; t < ntensors; ++t) {
+        if (total + numels[t] < total)
+            return CCL_ERR_INVALID_ARG;
+        total += numels[t];
+    }
+    const size_t nb = (total + bucket_elems - 1) / bucket_elems;
+    *nbuckets = nb;
+    if (starts) {
+        const size_t n = std::min(nb, max_buckets);
+        for (size_t b = 0; b < n; ++b)
+            starts[b] = b * bucket_elems;
+        starts[n] = n == nb ? total : n * bucket_elems;
+    }
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_alltoallv(int nranks, const size_t *counts, size_t *sdispl, size_t *rdispl)
+{
+    if (!valid_ranks(nranks) || !counts || !sdispl || !rdispl)
+        return CCL_ERR_INVALID_ARG;
+    const size_t N = (size_t)nranks;
+    for (size_t i = 0; i < N; ++i) {
+        size_t o = 0;
+        for (size_t j = 0; j < N; ++j) {
+            sdispl[i * N + j] = o;
+            o += counts[i * N + j];
+        }
+    }
+    for (size_t j = 0; j < N; ++j) {
+        size_t o = 0;
+        for (size_t i = 0; i < N; ++i) {
+            rdispl[j * N + i] = o;
+            o += counts[i * N + j];
+        }
+    }
+    return CCL_OK;
+}
+
+ccl_status_t ccl_arena_layout(int nranks, size_t bytes_per_rank, size_t align, size_t *stride, size_t *total)
+{
+    if (!valid_ranks(nranks) || !stride || !total || align < 256 || (align & (align - 1)) != 0)
+        return CCL_ERR_INVALID_ARG;
+    if (bytes_per_rank > SIZE_MAX - align)
+        return CCL_ERR_INVALID_ARG;
+    const size_t s = (bytes_per_rank + align - 1) & ~(align - 1);
+    if (mul_overflows(s, (size_t)nranks))
+        return CCL_ERR_INVALID_ARG;
+    *stride = s;
+    *total = s * (size_t)nranks;
+    return CCL_OK;
+}
+
+// ------------------------------------------------------------------ AllReduce
+
+ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+                           ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !valid_mode(mode) || !send || !recv)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const size_t bytes = count * es;
+    std::vector<Range> w, r;
+    bool in_place = true;
+    for (int i = 0; i < nranks; ++i) {
+        if (!send[i] || !recv[i])
+            return CCL_ERR_INVALID_ARG;
+        in_place = in_place && send[i] == recv[i];
+        w.push_back(range_of(recv[i], bytes, i));
+        r.push_back(range_of(send[i], bytes, i));
+    }
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return rd.rank == wr.rank && rd.lo == wr.lo;
+    });
+    if (st != CCL_OK)
+        return st;
+    if (nranks == 1 && in_place && op != CCL_AVG)
+        return CCL_OK;
+    if (mode == CCL_MODE_FUSED)
+        return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, true, stream));
+    if ((st = copy_ranks(send, recv, nranks, bytes, stream)) != CCL_OK)
+        return st;
+    return ring_steps_allreduce((int)dtype, (int)op, recv, nranks, count, stream);
+}
+
+// ------------------------------------------------------------------ ReduceScatter
+
+ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !valid_mode(mode) || !send || !recv)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es) || mul_overflows(count, (size_t)nranks))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const Partition part = make_partition(count, nranks);
+    std::vector<Range> w, r;
+    for (int i = 0; i < nranks; ++i) {
+        if (!send[i] || !recv[i])
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(recv[i], part.len((uint32_t)i) * es, i));
+        r.push_back(range_of(send[i], count * es, i));
+    }
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return rd.rank == wr.rank && wr.lo == rd.lo + part.off((uint32_t)rd.rank) * es;
+    });
+    if (st != CCL_OK)
+        return st;
+    if (mode == CCL_MODE_FUSED)
+        return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, false, stream));
+    // step mode: the ring's ReduceScatter phase on a workspace copy of the inputs
+    void *ws = nullptr;
+    if ((st = get_workspace(count * es * (size_t)nranks, &ws)) != CCL_OK)
+        return st;
+    std::vector<void *> bufs(nranks);
+    for (int i = 0; i < nranks; ++i)
+        bufs[i] = static_cast<char *>(ws) + (size_t)i * count * es;
+    if ((st = copy_ranks(send, bufs.data(), nranks, count * es, stream)) != CCL_OK)
+        return st;
+    for (int s = 0; s < nranks - 1; ++s)
+        if (cudaError_t e = launch_ring_step((int)dtype, (int)op, STEP_RS, s, bufs.data(), nranks, count, stream))
+            return from_cuda(e);
+    if (op == CCL_AVG)
+        if (cudaError_t e = launch_ring_step((int)dtype, (int)op, STEP_SCALE, 0, bufs.data(), nranks, count, stream))
+            return from_cuda(e);
+    // the phase leaves chunk c at rank c-1; hand it to rank c
+    std::vector<CopySeg> segs;
+    for (int c = 0; c < nranks; ++c)
+        segs.push_back(CopySeg{static_cast<const char *>(bufs[ring_mod(c - 1, nranks)]) + part.off((uint32_t)c) * es,
+                               static_cast<char *>(recv[c]), part.len((uint32_t)c) * es, 0});
+    return from_cuda(launch_copy_segments(segs.data(), segs.size(), stream));
+}
+
+// ------------------------------------------------------------------ AllGather
+
+ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+                           ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const Partition part = make_partition(count, nranks);
+    std::vector<Range> w, r;
+    for (int i = 0; i < nranks; ++i) {
+        if (!send[i] || !recv[i])
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(recv[i], count * es, i));
+        r.push_back(range_of(send[i], part.len((uint32_t)i) * es, i));
+    }
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return rd.rank == wr.rank && rd.lo == wr.lo + part.off((uint32_t)rd.rank) * es;
+    });
+    if (st != CCL_OK)
+        return st;
+    if (mode == CCL_MODE_FUSED)
+        return from_cuda(launch_fanout((int)dtype, send, nranks, recv, nranks, count, stream));
+    // step mode: rank i starts with chunk i; ring steps forward the rest
+    std::vector<CopySeg> segs;
+    for (int i = 0; i < nranks; ++i)
+        segs.push_back(CopySeg{static_cast<const char *>(send[i]),
+                               static_cast<char *>(recv[i]) + part.off((uint32_t)i) * es,
+                               part.len((uint32_t)i) * es, 0});
+    if ((st = from_cuda(launch_copy_segments(segs.data(), segs.size(), stream))) != CCL_OK)
+        return st;
+    for (int s = 0; s < nranks - 1; ++s)
+        if (cudaError_t e = launch_ring_step((int)dtype, CCL_SUM, STEP_AG_API, s, recv, nranks, count, stream))
+            return from_cuda(e);
+    return CCL_OK;
+}
+
+// ------------------------------------------------------------------ Broadcast
+
+ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                           ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv || root < 0 ||
+        root >= nranks || !send[root])
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const size_t bytes = count * es;
+    std::vector<Range> w, r;
+    for (int i = 0; i < nranks; ++i) {
+        if (!recv[i])
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(recv[i], bytes, i));
+    }
+    r.push_back(range_of(send[root], bytes, root));
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return wr.rank == root && rd.lo == wr.lo;
+    });
+    if (st != CCL_OK)
+        return st;
+    if (mode == CCL_MODE_FUSED) {
+        const void *src[1] = {send[root]};
+        return from_cuda(launch_fanout((int)dtype, src, 1, recv, nranks, count, stream));
+    }
+    // step mode: a chain around the ring starting at root
+    if (send[root] != recv[root]) {
+        CopySeg s{static_cast<const char *>(send[root]), static_cast<char *>(recv[root]), bytes, 0};
+        if ((st = from_cuda(launch_copy_segments(&s, 1, stream))) != CCL_OK)
+            return st;
+    }
+    for (int s = 0; s < nranks - 1; ++s) {
+        const int from = (root + s) % nranks, to = (root + s + 1) % nranks;
+        CopySeg g{static_cast<const char *>(recv[from]), static_cast<char *>(recv[to]), bytes, 0};
+        if ((st = from_cuda(launch_copy_segments(&g, 1, stream))) != CCL_OK)
+            return st;
+    }
+    return CCL_OK;
+}
+
+// ------------------------------------------------------------------ AllToAll(v)
+
+ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nranks, const size_t *counts,
+                           ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv || !counts)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    const size_t N = (size_t)nranks;
+    std::vector<size_t> sd(N * N), rd(N * N), stot(N, 0), rtot(N, 0);
+    for (size_t i = 0; i < N; ++i)
+        for (size_t j = 0; j < N; ++j) {
+            const size_t c = counts[i * N + j];
+            if (stot[i] + c < stot[i] || rtot[j] + c < rtot[j])
+                return CCL_ERR_INVALID_ARG;
+            stot[i] += c;
+            rtot[j] += c;
+        }
+    for (size_t i = 0; i < N; ++i)
+        if (mul_overflows(stot[i], es) || mul_overflows(rtot[i], es))
+            return CCL_ERR_INVALID_ARG;
+    ccl_plan_alltoallv(nranks, counts, sd.data(), rd.data());
+    std::vector<Range> w, r;
+    for (int i = 0; i < nranks; ++i) {
+        if ((stot[i] && !send[i]) || (rtot[i] && !recv[i]))
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(recv[i], rtot[i] * es, i));
+        r.push_back(range_of(send[i], stot[i] * es, i));
+    }
+    ccl_status_t st = check_overlaps(w, r, [](const Range &, const Range &) { return false; });
+    if (st != CCL_OK)
+        return st;
+    auto seg = [&](size_t i, size_t j) {
+        return CopySeg{static_cast<const char *>(send[i]) + sd[i * N + j] * es,
+                       static_cast<char *>(recv[j]) + rd[j * N + i] * es, counts[i * N + j] * es, 0};
+    };
+    std::vector<CopySeg> segs;
+    if (mode == CCL_MODE_FUSED) {
+        for (size_t i = 0; i < N; ++i)
+            for (size_t j = 0; j < N; ++j)
+                segs.push_back(seg(i, j));
+        return from_cuda(launch_copy_segments(segs.data(), segs.size(), stream));
+    }
+    // pairwise schedule: step k, rank i sends its block for rank (i+k) mod N
+    for (size_t k = 0; k < N; ++k) {
+        segs.clear();
+        for (size_t i = 0; i < N; ++i)
+            segs.push_back(seg(i, (i + k) % N));
+        if ((st = from_cuda(launch_copy_segments(segs.data(), segs.size(), stream))) != CCL_OK)
+            return st;
+    }
+    return CCL_OK;
+}
+
+ccl_status_t ccl_alltoall(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+                          ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks))
+        return CCL_ERR_INVALID_ARG;
+    if (mul_overflows(count, (size_t)nranks))
+        return CCL_ERR_INVALID_ARG;
+    std::vector<size_t> counts((size_t)nranks * nranks, count);
+    return ccl_alltoallv(send, recv, nranks, counts.data(), dtype, mode, stream);
+}
+
+// ------------------------------------------------------------------ bucket AllReduce
+
+ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int ntensors, int nranks,
+                                  size_t bucket_bytes, ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode,
+                                  cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !valid_mode(mode) || ntensors < 0 ||
+        (ntensors > 0 && (!ptrs || !numels)))
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (bucket_bytes == 0)
+        bucket_bytes = CCL_DEFAULT_BUCKET_BYTES;
+    const size_t B = bucket_bytes / es;
+    if (B == 0)
+        return CCL_ERR_INVALID_ARG;
+    const size_t T = (size_t)ntensors, N = (size_t)nranks;
+    // stream layout: reverse registration order
+    std::vector<size_t> pos(T);
+    size_t total = 0;
+    for (size_t k = T; k-- > 0;) {
+        if (mul_overflows(numels[k], es) || total + numels[k] < total)
+            return CCL_ERR_INVALID_ARG;
+        pos[k] = total;
+        total += numels[k];
+    }
+    if (total == 0)
+        return CCL_OK;
+    std::vector<Range> w;
+    std::vector<void *> tp(T * N); // [t][r]
+    for (size_t r = 0; r < N; ++r)
+        for (size_t t = 0; t < T; ++t) {
+            void *p = ptrs[r * T + t];
+            if (numels[t] && !p)
+                return CCL_ERR_INVALID_ARG;
+            tp[t * N + r] = p;
+            w.push_back(range_of(p, numels[t] * es, (int)r));
+        }
+    ccl_status_t st = check_overlaps(w, {}, [](const Range &, const Range &) { return false; });
+    if (st != CCL_OK)
+        return st;
+    // tensors in stream order
+    std::vector<size_t> order;
+    for (size_t k = T; k-- > 0;)
+        if (numels[k])
+            order.push_back(k);
+
+    if (mode == CCL_MODE_FUSED) {
+        // cut each (bucket, chunk) stream range at tensor boundaries
+        std::vector<RedSeg> segs;
+        size_t oi = 0;
+        for (size_t b0 = 0; b0 < total; b0 += B) {
+            const size_t blen = std::min(B, total - b0);
+            const Partition part = make_partition(blen, nranks);
+            for (int c = 0; c < nranks; ++c) {
+                size_t lo = b0 + part.off((uint32_t)c);
+                const size_t hi = lo + part.len((uint32_t)c);
+                while (lo < hi) {
+                    while (pos[order[oi]] + numels[order[oi]] <= lo)
+                        ++oi;
+                    const size_t t = order[oi];
+                    const size_t e = std::min(hi, pos[t] + numels[t]);
+                    segs.push_back(RedSeg{(uint32_t)t, (uint32_t)c, lo - pos[t], e - lo, 0});
+                    lo = e;
+                }
+            }
+        }
+        return from_cuda(launch_bucket_reduce((int)dtype, (int)op, tp.data(), ntensors, nranks, segs.data(),
+                                              segs.size(), stream));
+    }
+    // step mode: explicit pack -> ring steps -> unpack per bucket, through a workspace
+    void *ws = nullptr;
+    if ((st = get_workspace(std::min(B, total) * es * N, &ws)) != CCL_OK)
+        return st;
+    std::vector<void *> bufs(N);
+    for (size_t r = 0; r < N; ++r)
+        bufs[r] = static_cast<char *>(ws) + r * std::min(B, total) * es;
+    size_t oi = 0;
+    for (size_t b0 = 0; b0 < total; b0 += B) {
+        const size_t blen = std::min(B, total - b0);
+        std::vector<CopySeg> pack, unpack;
+        size_t lo = b0;
+        size_t oj = oi;
+        while (lo < b0 + blen) {
+            while (pos[order[oj]] + numels[order[oj]] <= lo)
+                ++oj;
+            const size_t t = order[oj];
+            const size_t e = std::min(b0 + blen, pos[t] + numels[t]);
+            for (size_t r = 0; r < N; ++r) {
+                char *tpr = static_cast<char *>(tp[t * N + r]) + (lo - pos[t]) * es;
+                char *bpr = static_cast<char *>(bufs[r]) + (lo - b0) * es;
+                pack.push_back(CopySeg{tpr, bpr, (e - lo) * es, 0});
+                unpack.push_back(CopySeg{bpr, tpr, (e - lo) * es, 0});
+            }
+            lo = e;
+        }
+        oi = oj;
+        if ((st = from_cuda(launch_copy_segments(pack.data(), pack.size(), stream))) != CCL_OK)
+            return st;
+        if ((st = ring_steps_allreduce((int)dtype, (int)op, bufs.data(), nranks, blen, stream)) != CCL_OK)
+            return st;
+        if ((st = from_cuda(launch_copy_segments(unpack.data(), unpack.size(), stream))) != CCL_OK)
+            return st;
+    }
+    return CCL_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,249 @@
+// ccl_device.cuh -- device-side building blocks shared by the collective kernels:
+// 16-byte streaming loads/stores and the per-hop arithmetic of the ring
+// reduction (one IEEE fp32 operation, round to nearest even, then a round to
+// the buffer type).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ccl {
+
+enum { DT_FP32 = 0, DT_BF16 = 1 };
+enum { OP_SUM = 0, OP_AVG = 1, OP_MAX = 2, OP_PROD = 3 };
+
+constexpr int kThreads = 256;
+
+template <int DT> struct DType;
+template <> struct DType<DT_FP32> { static constexpr int kSize = 4; static constexpr int kVec = 4; };
+template <> struct DType<DT_BF16> { static constexpr int kSize = 2; static constexpr int kVec = 8; };
+
+// ------------------------------------------------------------------ memory
+// Loads bypass L1 (every byte is used once); stores are plain write-back so
+// that in-place writes land on lines the same thread just read.
+
+__device__ __forceinline__ uint4 ld16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st16(void *p, const uint4 &v)
+{
+    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+template <int DT> __device__ __forceinline__ uint32_t ld_elem(const void *base, uint64_t i)
+{
+    if (DT == DT_BF16)
+        return static_cast<const uint16_t *>(base)[i];
+    return static_cast<const uint32_t *>(base)[i];
+}
+
+template <int DT> __device__ __forceinline__ void st_elem(void *base, uint64_t i, uint32_t v)
+{
+    if (DT == DT_BF16)
+        static_cast<uint16_t *>(base)[i] = static_cast<uint16_t>(v);
+    else
+        static_cast<uint32_t *>(base)[i] = v;
+}
+
+// ------------------------------------------------------------------ arithmetic
+
+// MAX on fp32 bit patterns: NaN if either is NaN, else the larger; equal
+// values give the bitwise AND (identical bits, or +0 for +0 vs -0).
+__device__ __forceinline__ uint32_t max_f32_bits(uint32_t a, uint32_t b)
+{
+    const float fa = __uint_as_float(a), fb = __uint_as_float(b);
+    if (fa != fa || fb != fb)
+        return 0x7fffffffu;
+    if (fa > fb)
+        return a;
+    if (fb > fa)
+        return b;
+    return a & b;
+}
+
+template <int OP> __device__ __forceinline__ float op_f32(float local, float acc)
+{
+    if (OP == OP_PROD)
+        return __fmul_rn(local, acc);
+    return __fadd_rn(local, acc); // SUM and AVG
+}
+
+// One ring hop on one fp32 element: local (+) incoming.
+template <int OP> __device__ __forceinline__ uint32_t hop_f32(uint32_t local, uint32_t acc)
+{
+    if (OP == OP_MAX)
+        return max_f32_bits(local, acc);
+    return __float_as_uint(op_f32<OP>(__uint_as_float(local), __uint_as_float(acc)));
+}
+
+// One ring hop on a pair of bf16 elements packed in 32 bits (element 0 in the
+// low half): widen (exact), fp32 operation, round each to bf16 (RNE).
+template <int OP> __device__ __forceinline__ uint32_t hop_bf16x2(uint32_t local, uint32_t acc)
+{
+    if (OP == OP_MAX) {
+        const uint32_t lo = max_f32_bits(local << 16, acc << 16) >> 16;
+        const uint32_t hi = max_f32_bits(local & 0xffff0000u, acc & 0xffff0000u) & 0xffff0000u;
+        return lo | hi;
+    }
+    const float r0 = op_f32<OP>(__uint_as_float(local << 16), __uint_as_float(acc << 16));
+    const float r1 = op_f32<OP>(__uint_as_float(local & 0xffff0000u), __uint_as_float(acc & 0xffff0000u));
+    __nv_bfloat162 p = __floats2bfloat162_rn(r0, r1);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// Scalar hop on a stored element (bf16 in the low 16 bits).
+template <int DT, int OP> __device__ __forceinline__ uint32_t hop_elem(uint32_t local, uint32_t acc)
+{
+    if (DT == DT_FP32)
+        return hop_f32<OP>(local, acc);
+    return hop_bf16x2<OP>(local, acc) & 0xffffu;
+}
+
+template <int DT, int OP> __device__ __forceinline__ uint4 hop_vec(const uint4 &local, const uint4 &acc)
+{
+    uint4 r;
+    if (DT == DT_FP32) {
+        r.x = hop_f32<OP>(local.x, acc.x);
+        r.y = hop_f32<OP>(local.y, acc.y);
+        r.z = hop_f32<OP>(local.z, acc.z);
+        r.w = hop_f32<OP>(local.w, acc.w);
+    } else {
+        r.x = hop_bf16x2<OP>(local.x, acc.x);
+        r.y = hop_bf16x2<OP>(local.y, acc.y);
+        r.z = hop_bf16x2<OP>(local.z, acc.z);
+        r.w = hop_bf16x2<OP>(local.w, acc.w);
+    }
+    return r;
+}
+
+// AVG: one fp32 division of the finished sum by N, rounded to the buffer type.
+__device__ __forceinline__ uint32_t avg_f32(uint32_t v, float n)
+{
+    return __float_as_uint(__fdiv_rn(__uint_as_float(v), n));
+}
+
+__device__ __forceinline__ uint32_t avg_bf16x2(uint32_t v, float n)
+{
+    const float r0 = __fdiv_rn(__uint_as_float(v << 16), n);
+    const float r1 = __fdiv_rn(__uint_as_float(v & 0xffff0000u), n);
+    __nv_bfloat162 p = __floats2bfloat162_rn(r0, r1);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+template <int DT> __device__ __forceinline__ uint32_t avg_elem(uint32_t v, float n)
+{
+    if (DT == DT_FP32)
+        return avg_f32(v, n);
+    return avg_bf16x2(v, n) & 0xffffu;
+}
+
+template <int DT> __device__ __forceinline__ uint4 avg_vec(const uint4 &v, float n)
+{
+    uint4 r;
+    if (DT == DT_FP32) {
+        r.x = avg_f32(v.x, n);
+        r.y = avg_f32(v.y, n);
+        r.z = avg_f32(v.z, n);
+        r.w = avg_f32(v.w, n);
+    } else {
+        r.x = avg_bf16x2(v.x, n);
+        r.y = avg_bf16x2(v.y, n);
+        r.z = avg_bf16x2(v.z, n);
+        r.w = avg_bf16x2(v.w, n);
+    }
+    return r;
+}
+
+// ------------------------------------------------------------------ ring folds over a pointer table
+
+// Fold one 16-byte vector of every rank in ring order starting at rank c:
+// x_c, then x_{c+1} (+) acc, ..., x_{c-1} (+) acc.  ptrs[r] is rank r's base.
+// NR > 0: exactly NR ranks, all loads issued before the first hop.
+// NR == 0: any N, ranks in groups of 8 with the next group's loads in flight.
+template <int DT, int OP, int NR>
+__device__ __forceinline__ uint4 ring_fold_vec(const void *const *ptrs, int N, int c, uint64_t byte_off)
+{
+    if (NR > 0) {
+        uint4 x[NR > 0 ? NR : 1];
+        int r = c;
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+            x[k] = ld16(static_cast<const char *>(ptrs[r]) + byte_off);
+            r = (r + 1 == NR) ? 0 : r + 1;
+        }
+        uint4 acc = x[0];
+#pragma unroll
+        for (int k = 1; k < NR; ++k)
+            acc = hop_vec<DT, OP>(x[k], acc);
+        return acc;
+    }
+    uint4 acc = make_uint4(0, 0, 0, 0);
+    uint4 cur[8], nxt[8];
+    int r = c;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (j < N) {
+            cur[j] = ld16(static_cast<const char *>(ptrs[r]) + byte_off);
+            r = (r + 1 == N) ? 0 : r + 1;
+        }
+    for (int g = 0; g < N; g += 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (g + 8 + j < N) {
+                nxt[j] = ld16(static_cast<const char *>(ptrs[r]) + byte_off);
+                r = (r + 1 == N) ? 0 : r + 1;
+            }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (g + j < N)
+                acc = (g + j == 0) ? cur[0] : hop_vec<DT, OP>(cur[j], acc);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            cur[j] = nxt[j];
+    }
+    return acc;
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t ring_fold_elem(const void *const *ptrs, int N, int c, uint64_t e)
+{
+    int r = c;
+    uint32_t acc = ld_elem<DT>(ptrs[r], e);
+    for (int k = 1; k < N; ++k) {
+        if (++r == N)
+            r = 0;
+        acc = hop_elem<DT, OP>(ld_elem<DT>(ptrs[r], e), acc);
+    }
+    return acc;
+}
+
+__host__ __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+// ------------------------------------------------------------------ chunk partition
+
+// Chunk c of a K-element buffer: len = K/N + (c < K%N), first K%N chunks longer.
+struct Partition {
+    uint64_t q;   // K / N
+    uint32_t rem; // K % N
+    __host__ __device__ __forceinline__ uint64_t off(uint32_t c) const
+    {
+        return (uint64_t)c * q + (c < rem ? c : rem);
+    }
+    __host__ __device__ __forceinline__ uint64_t len(uint32_t c) const { return q + (c < rem ? 1 : 0); }
+};
+
+__host__ __device__ __forceinline__ int ring_mod(int a, int n)
+{
+    int r = a % n;
+    return r < 0 ? r + n : r;
+}
+
+} // namespace ccl

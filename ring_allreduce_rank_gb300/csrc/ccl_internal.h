@@ -1,0 +1,87 @@
+// ccl_internal.h -- host-side declarations shared by the library's translation
+// units: kernel parameter blocks and launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ccl_device.cuh"
+
+namespace ccl {
+
+constexpr int kSmallRanks = 16;
+constexpr int kMaxRanks = 1024;
+
+// ------------------------------------------------------------------ fused reduce
+template <int MAXR> struct FusedParams {
+    const void *send[MAXR];
+    void *recv[MAXR];
+    Partition part;
+    int nranks;
+    int write_all;   // 1: AllReduce (all ranks get the result); 0: ReduceScatter (recv[c], chunk-local)
+    int vec_aligned; // every pointer is 16-byte aligned
+    uint32_t tiles;  // tiles per chunk (gridDim.x)
+    float n_f;       // (float)nranks, the AVG divisor
+};
+
+// Launch the one-pass ring-order reduction: AllReduce (write_all) or ReduceScatter.
+cudaError_t launch_fused_reduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
+                                uint64_t count, bool write_all, cudaStream_t stream);
+
+// ------------------------------------------------------------------ step mode
+enum StepKind {
+    STEP_RS = 0,     // rank i: chunk (i-1-s) += rank (i-1)'s copy
+    STEP_AG = 1,     // rank i: chunk (i-s) = rank (i-1)'s copy (after the RS phase)
+    STEP_AG_API = 2, // rank i: chunk (i-1-s) = rank (i-1)'s copy (AllGather from chunk i at rank i)
+    STEP_SCALE = 3   // rank i: chunk (i+1) /= N (AVG, at the holder)
+};
+
+template <int MAXR> struct StepParams {
+    void *buf[MAXR];
+    Partition part;
+    int nranks;
+    int s;
+    int kind;
+    int vec_aligned;
+    uint32_t tiles;
+    float n_f;
+};
+
+cudaError_t launch_ring_step(int dt, int op, int kind, int s, void *const *bufs, int nranks, uint64_t count,
+                             cudaStream_t stream);
+
+// ------------------------------------------------------------------ copies
+struct CopySeg {
+    const char *src;
+    char *dst;
+    uint64_t nbytes;
+    uint64_t tile_begin; // first tile index of this segment (prefix sum)
+};
+
+// Enqueue byte copies of the given segments (any alignment), split into as
+// many launches as the parameter space requires.
+cudaError_t launch_copy_segments(const CopySeg *segs, size_t nseg, cudaStream_t stream);
+
+// AllGather / Broadcast fan-out: each source element is read once and written
+// to every destination.  AllGather: src[c] is chunk c (partition of count over
+// nchunks = ndst), destination offset off_c.  Broadcast: nchunks = 1.
+cudaError_t launch_fanout(int dt, const void *const *src, int nchunks, void *const *dst, int ndst, uint64_t count,
+                          cudaStream_t stream);
+
+// ------------------------------------------------------------------ buckets
+struct RedSeg {
+    uint32_t tp;     // index of rank 0's pointer of this tensor in the pointer table
+    uint32_t c;      // ring rotation start (chunk index within the bucket)
+    uint64_t off;    // element offset inside the tensor
+    uint64_t len;    // elements
+    uint64_t tile_begin;
+};
+
+cudaError_t launch_bucket_reduce(int dt, int op, void *const *tensor_ptrs /* [t*nranks + r] */, int ntensors,
+                                 int nranks, const RedSeg *segs, size_t nseg, cudaStream_t stream);
+
+// ------------------------------------------------------------------ bookkeeping
+void count_launches(unsigned long long n);
+
+} // namespace ccl

@@ -1,0 +1,240 @@
+// copy.cu -- the data-movement collectives: AllGather and Broadcast fan-out
+// (read each source element once, write it to every rank) and segment copies
+// (AllToAll / AllToAllv blocks, step-mode placement, bucket packing).
+#include <algorithm>
+#include <vector>
+
+#include "ccl_internal.h"
+
+namespace ccl {
+
+// ------------------------------------------------------------------ segment copies
+
+constexpr uint64_t kCopyTileBytes = (uint64_t)kThreads * 4 * 16; // 16 KiB of body per CTA
+
+template <int MAXS> struct CopyParams {
+    uint32_t nseg;
+    uint32_t pad;
+    CopySeg seg[MAXS];
+};
+
+// Alignment class of a segment: the widest power of two (<= 16) dividing the
+// distance between source and destination; the body is moved in words of that
+// width, aligned on the destination.
+__host__ __device__ __forceinline__ uint32_t copy_grain(const char *src, const char *dst)
+{
+    const uintptr_t d = (uintptr_t)src ^ (uintptr_t)dst;
+    if ((d & 15) == 0) return 16;
+    if ((d & 7) == 0) return 8;
+    if ((d & 3) == 0) return 4;
+    if ((d & 1) == 0) return 2;
+    return 1;
+}
+
+__host__ __device__ __forceinline__ void copy_split(const CopySeg &s, uint32_t g, uint64_t &head, uint64_t &body)
+{
+    const uint64_t mis = (uintptr_t)s.dst & (g - 1);
+    head = mis ? umin64(g - mis, s.nbytes) : 0;
+    body = (s.nbytes - head) / g * g;
+}
+
+__host__ __device__ __forceinline__ uint64_t copy_tiles(const CopySeg &s)
+{
+    uint64_t head, body;
+    copy_split(s, copy_grain(s.src, s.dst), head, body);
+    const uint64_t t = (body + kCopyTileBytes - 1) / kCopyTileBytes;
+    return t ? t : 1;
+}
+
+template <typename W>
+__device__ __forceinline__ void copy_body(const char *src, char *dst, uint64_t nbytes)
+{
+    const uint64_t n = nbytes / sizeof(W);
+    const W *s = reinterpret_cast<const W *>(src);
+    W *d = reinterpret_cast<W *>(dst);
+    for (uint64_t i = threadIdx.x; i < n; i += kThreads)
+        d[i] = s[i];
+}
+
+template <int MAXS>
+__global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_constant__ CopyParams<MAXS> p)
+{
+    uint32_t lo = 0, hi = p.nseg - 1;
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi + 1) >> 1;
+        if (p.seg[mid].tile_begin <= blockIdx.x)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const CopySeg s = p.seg[lo];
+    const uint64_t t = blockIdx.x - s.tile_begin;
+    const uint32_t g = copy_grain(s.src, s.dst);
+    uint64_t head, body;
+    copy_split(s, g, head, body);
+    if (t == 0) {
+        for (uint64_t b = threadIdx.x; b < head; b += kThreads)
+            s.dst[b] = s.src[b];
+        for (uint64_t b = head + body + threadIdx.x; b < s.nbytes; b += kThreads)
+            s.dst[b] = s.src[b];
+    }
+    const uint64_t b0 = t * kCopyTileBytes;
+    if (b0 >= body)
+        return;
+    const uint64_t nb = umin64(kCopyTileBytes, body - b0);
+    const char *src = s.src + head + b0;
+    char *dst = s.dst + head + b0;
+    if (g == 16) {
+        const uint64_t n = nb / 16;
+#pragma unroll 4
+        for (uint64_t i = threadIdx.x; i < n; i += kThreads)
+            st16(dst + i * 16, ld16(src + i * 16));
+    } else if (g == 8) {
+        copy_body<uint2>(src, dst, nb);
+    } else if (g == 4) {
+        copy_body<uint32_t>(src, dst, nb);
+    } else if (g == 2) {
+        copy_body<uint16_t>(src, dst, nb);
+    } else {
+        copy_body<uint8_t>(src, dst, nb);
+    }
+}
+
+template <int MAXS>
+static cudaError_t launch_copy_batch(const CopySeg *segs, size_t nseg, cudaStream_t stream)
+{
+    CopyParams<MAXS> p;
+    p.nseg = (uint32_t)nseg;
+    p.pad = 0;
+    uint64_t tiles = 0;
+    for (size_t i = 0; i < nseg; ++i) {
+        p.seg[i] = segs[i];
+        p.seg[i].tile_begin = tiles;
+        tiles += copy_tiles(segs[i]);
+    }
+    if (tiles > 0x7fffffffull)
+        return cudaErrorInvalidValue;
+    copy_segments_kernel<MAXS><<<(unsigned)tiles, kThreads, 0, stream>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+constexpr size_t kCopySegsSmall = 16;
+constexpr size_t kCopySegsLarge = 1000; // 32 KB of kernel parameters
+
+cudaError_t launch_copy_segments(const CopySeg *segs, size_t nseg, cudaStream_t stream)
+{
+    std::vector<CopySeg> live;
+    live.reserve(nseg);
+    for (size_t i = 0; i < nseg; ++i)
+        if (segs[i].nbytes)
+            live.push_back(segs[i]);
+    size_t i = 0;
+    while (i < live.size()) {
+        const size_t n = std::min(kCopySegsLarge, live.size() - i);
+        cudaError_t e = n <= kCopySegsSmall ? launch_copy_batch<kCopySegsSmall>(live.data() + i, n, stream)
+                                            : launch_copy_batch<kCopySegsLarge>(live.data() + i, n, stream);
+        if (e != cudaSuccess)
+            return e;
+        i += n;
+    }
+    return cudaSuccess;
+}
+
+// ------------------------------------------------------------------ fan-out (AllGather, Broadcast)
+
+template <int MAXR> struct FanoutParams {
+    const void *src[MAXR];
+    void *dst[MAXR];
+    Partition part;  // chunking of the destination buffers
+    int nchunks;     // sources (AllGather: N, Broadcast: 1)
+    int ndst;
+    int vec_aligned; // every pointer 16-byte aligned
+};
+
+template <int DT, int MAXR>
+__global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant__ FanoutParams<MAXR> p)
+{
+    constexpr int VEC = DType<DT>::kVec;
+    constexpr int U = 2;
+    constexpr uint64_t TV = (uint64_t)kThreads * U;
+    const uint32_t c = blockIdx.y, t = blockIdx.x;
+    const uint64_t off = p.part.off(c), len = p.part.len(c);
+    const void *src = p.src[c];
+    const int M = p.ndst;
+    if (!(p.vec_aligned && off % VEC == 0)) {
+        const uint64_t e0 = (uint64_t)t * TV * VEC;
+        for (int k = 0; k < U * VEC; ++k) {
+            const uint64_t e = e0 + (uint64_t)k * kThreads + threadIdx.x;
+            if (e < len) {
+                const uint32_t v = ld_elem<DT>(src, e);
+                for (int q = 0; q < M; ++q)
+                    st_elem<DT>(p.dst[q], off + e, v);
+            }
+        }
+        return;
+    }
+    const uint64_t nv = len / VEC;
+    if (t == 0)
+        for (uint64_t e = nv * VEC + threadIdx.x; e < len; e += kThreads) {
+            const uint32_t v = ld_elem<DT>(src, e);
+            for (int q = 0; q < M; ++q)
+                st_elem<DT>(p.dst[q], off + e, v);
+        }
+    uint4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint64_t v = (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
+        if (v < nv)
+            x[u] = ld16(static_cast<const char *>(src) + v * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint64_t v = (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
+        if (v < nv)
+            for (int q = 0; q < M; ++q)
+                st16(static_cast<char *>(p.dst[q]) + (off + v * VEC) * DType<DT>::kSize, x[u]);
+    }
+}
+
+template <int DT, int MAXR>
+static cudaError_t launch_fanout_t(const void *const *src, int nchunks, void *const *dst, int ndst, uint64_t count,
+                                   cudaStream_t stream)
+{
+    constexpr int VEC = DType<DT>::kVec;
+    FanoutParams<MAXR> p;
+    bool aligned = true;
+    for (int i = 0; i < MAXR; ++i) {
+        p.src[i] = i < nchunks ? src[i] : nullptr;
+        p.dst[i] = i < ndst ? dst[i] : nullptr;
+        if (i < nchunks)
+            aligned = aligned && (uintptr_t)src[i] % 16 == 0;
+        if (i < ndst)
+            aligned = aligned && (uintptr_t)dst[i] % 16 == 0;
+    }
+    p.part.q = count / (uint64_t)nchunks;
+    p.part.rem = (uint32_t)(count % (uint64_t)nchunks);
+    p.nchunks = nchunks;
+    p.ndst = ndst;
+    p.vec_aligned = aligned ? 1 : 0;
+    const uint64_t te = (uint64_t)kThreads * 2 * VEC;
+    const uint64_t tiles = (p.part.q + 1 + te - 1) / te;
+    if (tiles > 0x7fffffffull)
+        return cudaErrorInvalidValue;
+    fanout_kernel<DT, MAXR><<<dim3((unsigned)tiles, (unsigned)nchunks), kThreads, 0, stream>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fanout(int dt, const void *const *src, int nchunks, void *const *dst, int ndst, uint64_t count,
+                          cudaStream_t stream)
+{
+    const bool small = nchunks <= kSmallRanks && ndst <= kSmallRanks;
+    if (dt == DT_FP32)
+        return small ? launch_fanout_t<DT_FP32, kSmallRanks>(src, nchunks, dst, ndst, count, stream)
+                     : launch_fanout_t<DT_FP32, kMaxRanks>(src, nchunks, dst, ndst, count, stream);
+    return small ? launch_fanout_t<DT_BF16, kSmallRanks>(src, nchunks, dst, ndst, count, stream)
+                 : launch_fanout_t<DT_BF16, kMaxRanks>(src, nchunks, dst, ndst, count, stream);
+}
+
+} // namespace ccl

@@ -1,0 +1,244 @@
+// reduce.cu -- the fused ring-order reduction: AllReduce and ReduceScatter in
+// one pass over memory.
+//
+// The ring (Collectives and sharded matmul, "ring ReduceScatter": at step s
+// rank i sends chunk (i-s) mod N right and the receiver adds it into its own
+// copy) carries chunk c from rank c through c+1, ..., c-1, adding one
+// contribution per hop.  Its end state is, per element of chunk c, the fold
+//     R = x_{c-1} (+) ( ... (x_{c+1} (+) x_c))
+// rounded to the buffer type after every hop, AVG dividing once by N, and the
+// AllGather phase (AllReduce survey, phase 2) copying R to every rank.  This
+// kernel computes that end state directly: each element's N contributions are
+// read once, folded in ring order in registers, and written once per rank --
+// N*M bytes read and N*M written for AllReduce, the least any implementation
+// can move, instead of the ~5(N-1)M bytes the step-by-step schedule moves.
+//
+// Work decomposition: grid (tiles, N); blockIdx.y is the chunk c, so the ring
+// rotation start is uniform per CTA.  Inside a chunk, threads take 16-byte
+// vectors (4 fp32 / 8 bf16) aligned to the buffers; the unaligned head and tail
+// of each chunk are done element by element by the chunk's first CTA.  When a
+// chunk's output cannot be vector-aligned (unaligned pointers, or a
+// ReduceScatter chunk whose offset is not a multiple of the vector) the CTA
+// walks its tile element by element instead.
+#include "ccl_internal.h"
+
+namespace ccl {
+
+template <int NR> struct Unroll { static constexpr int kU = NR == 2 ? 4 : (NR == 4 ? 2 : 1); };
+
+// Element path: one element at a time, all ranks, ring order.
+template <int DT, int OP, int MAXR>
+__device__ __forceinline__ void reduce_elem(const FusedParams<MAXR> &p, int N, uint32_t c, uint64_t e,
+                                            uint64_t out_base)
+{
+    int r = (int)c;
+    uint32_t acc = ld_elem<DT>(p.send[r], e);
+    for (int k = 1; k < N; ++k) {
+        if (++r == N)
+            r = 0;
+        acc = hop_elem<DT, OP>(ld_elem<DT>(p.send[r], e), acc);
+    }
+    if (OP == OP_AVG)
+        acc = avg_elem<DT>(acc, p.n_f);
+    if (p.write_all) {
+        for (int q = 0; q < N; ++q)
+            st_elem<DT>(p.recv[q], e, acc);
+    } else {
+        st_elem<DT>(p.recv[c], e - out_base, acc);
+    }
+}
+
+template <int DT, int OP, int NR, int MAXR>
+__global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_constant__ FusedParams<MAXR> p)
+{
+    constexpr int VEC = DType<DT>::kVec;
+    constexpr int ES = DType<DT>::kSize;
+    constexpr int U = NR > 0 ? Unroll<NR>::kU : 1;
+    constexpr uint64_t TV = (uint64_t)kThreads * U; // vectors per tile
+    const int N = NR > 0 ? NR : p.nranks;
+    const uint32_t c = blockIdx.y;
+    const uint32_t t = blockIdx.x;
+    const uint64_t off = p.part.off(c), len = p.part.len(c), end = off + len;
+    const uint64_t out_base = p.write_all ? 0 : off;
+    const bool vec_ok = p.vec_aligned && (p.write_all || (off % VEC) == 0);
+
+    if (!vec_ok) {
+        // element path over tile t of the chunk
+        const uint64_t e0 = off + (uint64_t)t * TV * VEC;
+#pragma unroll 4
+        for (int i = 0; i < U * VEC; ++i) {
+            const uint64_t e = e0 + (uint64_t)i * kThreads + threadIdx.x;
+            if (e < end)
+                reduce_elem<DT, OP, MAXR>(p, N, c, e, out_base);
+        }
+        return;
+    }
+
+    const uint64_t vb = (off + VEC - 1) / VEC, ve = end / VEC;
+    if (t == 0) {
+        // unaligned head and tail of the chunk (or all of a chunk shorter than a vector span)
+        const uint64_t hb = vb < ve ? vb * VEC : end;
+        for (uint64_t e = off + threadIdx.x; e < hb; e += kThreads)
+            reduce_elem<DT, OP, MAXR>(p, N, c, e, out_base);
+        if (vb < ve)
+            for (uint64_t e = ve * VEC + threadIdx.x; e < end; e += kThreads)
+                reduce_elem<DT, OP, MAXR>(p, N, c, e, out_base);
+    }
+    if (vb >= ve)
+        return;
+    const uint64_t v0 = vb + (uint64_t)t * TV + threadIdx.x;
+    if (v0 >= ve)
+        return;
+
+    if (NR > 0) {
+        // Exact rank count: every load of every rank for U vectors is issued
+        // before the first hop, so a thread has U*N 16-byte loads in flight.
+        uint4 x[U][NR > 0 ? NR : 1];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = v0 + (uint64_t)u * kThreads;
+            if (v < ve) {
+                int r = (int)c;
+#pragma unroll
+                for (int k = 0; k < NR; ++k) {
+                    x[u][k] = ld16(static_cast<const char *>(p.send[r]) + v * 16);
+                    r = (r + 1 == NR) ? 0 : r + 1;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = v0 + (uint64_t)u * kThreads;
+            if (v < ve) {
+                uint4 acc = x[u][0];
+#pragma unroll
+                for (int k = 1; k < NR; ++k)
+                    acc = hop_vec<DT, OP>(x[u][k], acc);
+                if (OP == OP_AVG)
+                    acc = avg_vec<DT>(acc, p.n_f);
+                if (p.write_all) {
+#pragma unroll
+                    for (int q = 0; q < NR; ++q)
+                        st16(static_cast<char *>(p.recv[q]) + v * 16, acc);
+                } else {
+                    st16(static_cast<char *>(p.recv[c]) + (v * VEC - out_base) * ES, acc);
+                }
+            }
+        }
+    } else {
+        // Any rank count: ranks in groups of 8, the next group's loads issued
+        // before the current group is folded.
+        const uint64_t v = v0;
+        uint4 acc = make_uint4(0, 0, 0, 0);
+        uint4 cur[8], nxt[8];
+        int r = (int)c;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < N) {
+                cur[j] = ld16(static_cast<const char *>(p.send[r]) + v * 16);
+                r = (r + 1 == N) ? 0 : r + 1;
+            }
+        }
+        for (int g = 0; g < N; g += 8) {
+            const int gn = g + 8;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (gn + j < N) {
+                    nxt[j] = ld16(static_cast<const char *>(p.send[r]) + v * 16);
+                    r = (r + 1 == N) ? 0 : r + 1;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (g + j < N)
+                    acc = (g + j == 0) ? cur[0] : hop_vec<DT, OP>(cur[j], acc);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                cur[j] = nxt[j];
+        }
+        if (OP == OP_AVG)
+            acc = avg_vec<DT>(acc, p.n_f);
+        if (p.write_all) {
+            for (int q = 0; q < N; ++q)
+                st16(static_cast<char *>(p.recv[q]) + v * 16, acc);
+        } else {
+            st16(static_cast<char *>(p.recv[c]) + (v * VEC - out_base) * ES, acc);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launch
+
+template <int DT, int OP, int NR, int MAXR>
+static cudaError_t launch_t(const void *const *send, void *const *recv, int nranks, uint64_t count, bool write_all,
+                            cudaStream_t stream)
+{
+    constexpr int VEC = DType<DT>::kVec;
+    constexpr int U = NR > 0 ? Unroll<NR>::kU : 1;
+    FusedParams<MAXR> p;
+    bool aligned = true;
+    for (int r = 0; r < nranks; ++r) {
+        p.send[r] = send[r];
+        p.recv[r] = recv[r];
+        aligned = aligned && ((uintptr_t)send[r] % 16 == 0) && ((uintptr_t)recv[r] % 16 == 0);
+    }
+    for (int r = nranks; r < MAXR; ++r) {
+        p.send[r] = nullptr;
+        p.recv[r] = nullptr;
+    }
+    p.part.q = count / (uint64_t)nranks;
+    p.part.rem = (uint32_t)(count % (uint64_t)nranks);
+    p.nranks = nranks;
+    p.write_all = write_all ? 1 : 0;
+    p.vec_aligned = aligned ? 1 : 0;
+    p.n_f = (float)nranks;
+    const uint64_t te = (uint64_t)kThreads * U * VEC;
+    const uint64_t tiles = (p.part.q + 1 + te - 1) / te;
+    if (tiles > 0x7fffffffull)
+        return cudaErrorInvalidValue;
+    p.tiles = (uint32_t)tiles;
+    dim3 grid((unsigned)tiles, (unsigned)nranks);
+    fused_reduce_kernel<DT, OP, NR, MAXR><<<grid, kThreads, 0, stream>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <int DT, int OP>
+static cudaError_t launch_op(const void *const *send, void *const *recv, int nranks, uint64_t count, bool write_all,
+                             cudaStream_t stream)
+{
+    switch (nranks) {
+    case 2: return launch_t<DT, OP, 2, kSmallRanks>(send, recv, nranks, count, write_all, stream);
+    case 4: return launch_t<DT, OP, 4, kSmallRanks>(send, recv, nranks, count, write_all, stream);
+    case 8: return launch_t<DT, OP, 8, kSmallRanks>(send, recv, nranks, count, write_all, stream);
+    case 16: return launch_t<DT, OP, 16, kSmallRanks>(send, recv, nranks, count, write_all, stream);
+    default:
+        if (nranks <= kSmallRanks)
+            return launch_t<DT, OP, 0, kSmallRanks>(send, recv, nranks, count, write_all, stream);
+        return launch_t<DT, OP, 0, kMaxRanks>(send, recv, nranks, count, write_all, stream);
+    }
+}
+
+template <int DT>
+static cudaError_t launch_dt(int op, const void *const *send, void *const *recv, int nranks, uint64_t count,
+                             bool write_all, cudaStream_t stream)
+{
+    switch (op) {
+    case OP_SUM: return launch_op<DT, OP_SUM>(send, recv, nranks, count, write_all, stream);
+    case OP_AVG: return launch_op<DT, OP_AVG>(send, recv, nranks, count, write_all, stream);
+    case OP_MAX: return launch_op<DT, OP_MAX>(send, recv, nranks, count, write_all, stream);
+    case OP_PROD: return launch_op<DT, OP_PROD>(send, recv, nranks, count, write_all, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fused_reduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
+                                uint64_t count, bool write_all, cudaStream_t stream)
+{
+    if (dt == DT_FP32)
+        return launch_dt<DT_FP32>(op, send, recv, nranks, count, write_all, stream);
+    return launch_dt<DT_BF16>(op, send, recv, nranks, count, write_all, stream);
+}
+
+} // namespace ccl

@@ -1,0 +1,150 @@
+// step.cu -- step-faithful ring: one launch per ring step, for validating the
+// schedule against the fused kernels.
+//
+// ReduceScatter phase, step s (Collectives and sharded matmul, "ring
+// ReduceScatter"; Lesson 3 reference solution): rank i adds the chunk
+// (i-1-s) mod N that rank i-1 sends into its own copy of that chunk.
+// AllGather phase, step s: rank i stores chunk (i-s) mod N from rank i-1.
+// Within one step the chunk a rank receives is never the chunk its right
+// neighbour reads from it, so a step can run in place with no snapshot; the
+// stream order between launches is the step barrier.
+#include "ccl_internal.h"
+
+namespace ccl {
+
+template <int DT, int OP, int MAXR>
+__device__ __forceinline__ void step_elem(const StepParams<MAXR> &p, int kind, int i, int left, uint64_t e)
+{
+    if (kind == STEP_RS) {
+        const uint32_t incoming = ld_elem<DT>(p.buf[left], e);
+        st_elem<DT>(p.buf[i], e, hop_elem<DT, OP>(ld_elem<DT>(p.buf[i], e), incoming));
+    } else if (kind == STEP_SCALE) {
+        st_elem<DT>(p.buf[i], e, avg_elem<DT>(ld_elem<DT>(p.buf[i], e), p.n_f));
+    } else {
+        st_elem<DT>(p.buf[i], e, ld_elem<DT>(p.buf[left], e));
+    }
+}
+
+template <int DT, int OP, int MAXR>
+__device__ __forceinline__ void step_vec(const StepParams<MAXR> &p, int kind, int i, int left, uint64_t v)
+{
+    char *dst = static_cast<char *>(p.buf[i]) + v * 16;
+    if (kind == STEP_RS) {
+        const uint4 incoming = ld16(static_cast<const char *>(p.buf[left]) + v * 16);
+        st16(dst, hop_vec<DT, OP>(ld16(dst), incoming));
+    } else if (kind == STEP_SCALE) {
+        st16(dst, avg_vec<DT>(ld16(dst), p.n_f));
+    } else {
+        st16(dst, ld16(static_cast<const char *>(p.buf[left]) + v * 16));
+    }
+}
+
+template <int DT, int OP, int MAXR>
+__global__ void __launch_bounds__(kThreads) ring_step_kernel(const __grid_constant__ StepParams<MAXR> p)
+{
+    constexpr int VEC = DType<DT>::kVec;
+    constexpr int U = 2;
+    constexpr uint64_t TV = (uint64_t)kThreads * U;
+    const int N = p.nranks;
+    const int i = blockIdx.y;
+    const int left = ring_mod(i - 1, N);
+    const int kind = p.kind;
+    int c;
+    if (kind == STEP_RS || kind == STEP_AG_API)
+        c = ring_mod(i - 1 - p.s, N);
+    else if (kind == STEP_AG)
+        c = ring_mod(i - p.s, N);
+    else
+        c = ring_mod(i + 1, N);
+    const uint64_t off = p.part.off(c), end = off + p.part.len(c);
+    const uint32_t t = blockIdx.x;
+
+    if (!p.vec_aligned) {
+        const uint64_t e0 = off + (uint64_t)t * TV * VEC;
+        for (int k = 0; k < U * VEC; ++k) {
+            const uint64_t e = e0 + (uint64_t)k * kThreads + threadIdx.x;
+            if (e < end)
+                step_elem<DT, OP, MAXR>(p, kind, i, left, e);
+        }
+        return;
+    }
+    const uint64_t vb = (off + VEC - 1) / VEC, ve = end / VEC;
+    if (t == 0) {
+        const uint64_t hb = vb < ve ? vb * VEC : end;
+        for (uint64_t e = off + threadIdx.x; e < hb; e += kThreads)
+            step_elem<DT, OP, MAXR>(p, kind, i, left, e);
+        if (vb < ve)
+            for (uint64_t e = ve * VEC + threadIdx.x; e < end; e += kThreads)
+                step_elem<DT, OP, MAXR>(p, kind, i, left, e);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint64_t v = vb + (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
+        if (v < ve)
+            step_vec<DT, OP, MAXR>(p, kind, i, left, v);
+    }
+}
+
+template <int DT, int OP, int MAXR>
+static cudaError_t launch_step_t(int kind, int s, void *const *bufs, int nranks, uint64_t count, cudaStream_t stream)
+{
+    constexpr int VEC = DType<DT>::kVec;
+    StepParams<MAXR> p;
+    bool aligned = true;
+    for (int r = 0; r < nranks; ++r) {
+        p.buf[r] = bufs[r];
+        aligned = aligned && ((uintptr_t)bufs[r] % 16 == 0);
+    }
+    for (int r = nranks; r < MAXR; ++r)
+        p.buf[r] = nullptr;
+    p.part.q = count / (uint64_t)nranks;
+    p.part.rem = (uint32_t)(count % (uint64_t)nranks);
+    p.nranks = nranks;
+    p.s = s;
+    p.kind = kind;
+    p.vec_aligned = aligned ? 1 : 0;
+    p.n_f = (float)nranks;
+    const uint64_t te = (uint64_t)kThreads * 2 * VEC;
+    const uint64_t tiles = (p.part.q + 1 + te - 1) / te;
+    if (tiles > 0x7fffffffull)
+        return cudaErrorInvalidValue;
+    p.tiles = (uint32_t)tiles;
+    ring_step_kernel<DT, OP, MAXR><<<dim3((unsigned)tiles, (unsigned)nranks), kThreads, 0, stream>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <int DT, int OP>
+static cudaError_t launch_step_op(int kind, int s, void *const *bufs, int nranks, uint64_t count,
+                                  cudaStream_t stream)
+{
+    if (nranks <= kSmallRanks)
+        return launch_step_t<DT, OP, kSmallRanks>(kind, s, bufs, nranks, count, stream);
+    return launch_step_t<DT, OP, kMaxRanks>(kind, s, bufs, nranks, count, stream);
+}
+
+template <int DT>
+static cudaError_t launch_step_dt(int op, int kind, int s, void *const *bufs, int nranks, uint64_t count,
+                                  cudaStream_t stream)
+{
+    switch (op) {
+    case OP_SUM: return launch_step_op<DT, OP_SUM>(kind, s, bufs, nranks, count, stream);
+    case OP_AVG: return launch_step_op<DT, OP_AVG>(kind, s, bufs, nranks, count, stream);
+    case OP_MAX: return launch_step_op<DT, OP_MAX>(kind, s, bufs, nranks, count, stream);
+    case OP_PROD: return launch_step_op<DT, OP_PROD>(kind, s, bufs, nranks, count, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ring_step(int dt, int op, int kind, int s, void *const *bufs, int nranks, uint64_t count,
+                             cudaStream_t stream)
+{
+    // copies do not depend on the op: share one instantiation
+    if (kind == STEP_AG || kind == STEP_AG_API)
+        op = OP_SUM;
+    if (dt == DT_FP32)
+        return launch_step_dt<DT_FP32>(op, kind, s, bufs, nranks, count, stream);
+    return launch_step_dt<DT_BF16>(op, kind, s, bufs, nranks, count, stream);
+}
+
+} // namespace ccl

@@ -1,0 +1,100 @@
+"""Host-side checks of libccl.so that need no GPU: the library loads and exports
+every entry point include/ccl.h declares, the planner agrees with the oracle's
+tables, and argument validation rejects bad calls before anything is launched
+(these calls never reach a kernel, so no device is touched)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import ring_allreduce_rank_gb300 as ccl
+from ring_allreduce_rank_gb300 import ccl as C
+from ring_allreduce_rank_gb300 import workloads as W
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ccl.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ccl_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from ring_allreduce_rank_gb300 import build
+    build.build()
+    return ccl.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version_and_status_strings(L):
+    assert L.ccl_version() >= 10000
+    for s in range(8):
+        assert ccl.ccl_status_string(s)
+
+
+@pytest.mark.parametrize("K,N", [(0, 1), (5, 3), (16777259, 16), (67108864, 8), (3, 8), (1 << 33, 7)])
+def test_planner_partition_matches_oracle(oracle_mod, L, K, N):
+    assert ccl.ccl_plan_chunks(K, N) == oracle_mod.partition(K, N)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 8, 16, 64])
+def test_planner_schedule_matches_oracle(oracle_mod, L, N):
+    tab = np.array(ccl.ccl_plan_ring_schedule(N), dtype=np.int32).reshape(2, max(N - 1, 0), N, 3)
+    np.testing.assert_array_equal(tab, oracle_mod.ring_schedule(N))
+
+
+def test_planner_buckets_c4(L):
+    numels = W.llama_layer_numels(4)
+    starts = ccl.ccl_plan_buckets(numels, W.bucket_elems(25 * W.MiB, 2))
+    assert len(starts) == 63
+    sizes = np.diff(starts)
+    assert list(sizes[:-1]) == [13_107_200] * 61 and sizes[-1] == 9_994_240
+
+
+def test_planner_alltoallv_displacements(L):
+    counts = W.zipf_expert_counts(8, 4096, 64, 1.2, 1000)
+    sd, rd = ccl.ccl_plan_alltoallv(counts.tolist())
+    for i in range(8):
+        assert sd[i] == [int(counts[i, :j].sum()) for j in range(8)]
+    for j in range(8):
+        assert rd[j] == [int(counts[:i, j].sum()) for i in range(8)]
+
+
+def test_zipf_counts_shape():
+    counts = W.zipf_expert_counts(8, 4096, 64, 1.2, 1000)
+    assert counts.shape == (8, 8) and (counts.sum(axis=1) == 4096).all()
+    # experts 0..7 (the most popular) live on rank 0: it receives the most tokens
+    assert counts[:, 0].sum() == counts.sum(axis=0).max()
+
+
+def test_arena_layout(L):
+    assert ccl.ccl_arena_layout(8, 134217728) == (134217728, 8 * 134217728)
+    assert ccl.ccl_arena_layout(3, 1000, 256) == (1024, 3072)
+    with pytest.raises(C.CclError):
+        ccl.ccl_arena_layout(3, 1000, 100)
+
+
+# ------------------------------------------------------------------ validation (no launch)
+# The cases live in tests/validation_cases.py and run in a child process that
+# sees no GPU (CUDA_VISIBLE_DEVICES=""): their pointers are fake, so a case that
+# wrongly passed validation would get "no device" instead of touching memory.
+
+def test_invalid_arguments_and_overlaps_rejected(L):
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    here = os.path.dirname(os.path.abspath(__file__))
+    res = subprocess.run([sys.executable, os.path.join(here, "validation_cases.py")], env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "validation cases ok" in res.stdout
