@@ -43,6 +43,13 @@ KERNEL_SOURCES = ["ring_allreduce_rank_gb300/csrc/reduce.cu", "ring_allreduce_ra
                   "ring_allreduce_rank_gb300/csrc/ccl_internal.h"]
 
 
+def set_count(count: int) -> None:
+    global COUNT, ALG_BYTES, WORKLOAD
+    COUNT = count
+    ALG_BYTES = 2 * NRANKS * COUNT * ELEM
+    WORKLOAD = "allreduce-avg N=8 bf16 %d elements/rank (profiling size), in place, fused ring order" % count
+
+
 def kernel_digest() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -158,7 +165,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--count", type=int, default=COUNT,
+                    help="elements per rank (default: the 64Mi-element workload; smaller values are for profiling)")
     args = ap.parse_args()
+    if args.count != COUNT:
+        set_count(args.count)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -238,25 +249,29 @@ def main():
 
     # end to end through the public API with host buffers: pinned host -> arena,
     # AllReduce, arena -> pinned host, every step
-    host_in = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
-    host_out = torch.empty((NRANKS, COUNT), dtype=torch.bfloat16).pin_memory()
-    for _ in range(2):
-        e2e_step(ccl, arena, host_in, host_out, stream)
-    torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step(ccl, arena, host_in, host_out, stream)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * ALG_BYTES * args.e2e_steps / (e2e_ms / 1e3) / 1e9
+    e2e = None
+    if args.e2e_steps > 0:
+        host_in = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        host_out = torch.empty((NRANKS, COUNT), dtype=torch.bfloat16).pin_memory()
+        for _ in range(2):
+            e2e_step(ccl, arena, host_in, host_out, stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step(ccl, arena, host_in, host_out, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+        if dist:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(world * ALG_BYTES * args.e2e_steps / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": NRANKS * COUNT * ELEM, "d2h_bytes_per_step": NRANKS * COUNT * ELEM,
+               "steps": args.e2e_steps}
 
     # alpha: one tiny AllReduce (latency of a launch through the API)
     tiny = [torch.zeros(8, dtype=torch.bfloat16, device=dev) for _ in range(NRANKS)]
@@ -294,8 +309,7 @@ def main():
                      "algorithmic_bytes_per_launch": ALG_BYTES, "peak_source": peak_src,
                      "kernel": "fused_reduce_kernel<bf16, AVG, 8 ranks>"},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": NRANKS * COUNT * ELEM,
-                "d2h_bytes_per_step": NRANKS * COUNT * ELEM, "steps": args.e2e_steps},
+        "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clk,
         "alpha_beta": {"algbw_GBs": round(algbw, 2), "busbw_GBs": round(algbw * 2 * (NRANKS - 1) / NRANKS, 2),

@@ -311,7 +311,8 @@ ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int 
     const Partition part = make_partition(count, nranks);
     std::vector<Range> w, r;
     for (int i = 0; i < nranks; ++i) {
-        if (!send[i] || !recv[i])
+        // an empty chunk's output may be NULL (K < N leaves chunks empty)
+        if (!send[i] || (!recv[i] && part.len((uint32_t)i) > 0))
             return CCL_ERR_INVALID_ARG;
         w.push_back(range_of(recv[i], part.len((uint32_t)i) * es, i));
         r.push_back(range_of(send[i], count * es, i));
@@ -361,7 +362,8 @@ ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nrank
     const Partition part = make_partition(count, nranks);
     std::vector<Range> w, r;
     for (int i = 0; i < nranks; ++i) {
-        if (!send[i] || !recv[i])
+        // an empty chunk's input may be NULL (K < N leaves chunks empty)
+        if (!recv[i] || (!send[i] && part.len((uint32_t)i) > 0))
             return CCL_ERR_INVALID_ARG;
         w.push_back(range_of(recv[i], count * es, i));
         r.push_back(range_of(send[i], part.len((uint32_t)i) * es, i));
