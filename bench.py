@@ -132,6 +132,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ multi-replica timing
+
+def max_over_ranks(dist, ms: float, device) -> float:
+    """The slowest replica's time (the job finishes when the last one does)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: bytes every replica moved over the slowest replica's time."""
+    return world * bytes_per_step * steps / (ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------------ oracle timing (CPU)
 
 def oracle_sample_gbs(target_s: float, max_count: int = COUNT):
@@ -233,14 +250,10 @@ def main():
         dist.barrier()
     clk = clocks.stop()
 
-    total_ms = t_all0.elapsed_time(t_all1)
+    total_ms = max_over_ranks(dist, t_all0.elapsed_time(t_all1), dev)
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = world * ALG_BYTES * args.steps / (total_ms / 1e3) / 1e9
+    value = job_gbs(world, ALG_BYTES, args.steps, total_ms)
 
     avg_launch_s = statistics.mean(per_launch_ms) / 1e3
     achieved = ALG_BYTES / avg_launch_s / 1e9
@@ -264,12 +277,8 @@ def main():
             e2e_step(ccl, arena, host_in, host_out, stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(world * ALG_BYTES * args.e2e_steps / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+        e2e = {"value": round(job_gbs(world, ALG_BYTES, args.e2e_steps, e2e_ms), 2), "unit": UNIT,
                "h2d_bytes_per_step": NRANKS * COUNT * ELEM, "d2h_bytes_per_step": NRANKS * COUNT * ELEM,
                "steps": args.e2e_steps}
 

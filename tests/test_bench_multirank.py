@@ -1,0 +1,59 @@
+"""The benchmark's multi-replica harness on CPU: two gloo ranks agree on the
+slowest replica's time, the whole-job throughput counts every replica's bytes,
+and the reference arm under torchrun runs on rank 0 only."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank, world_size=world)
+    ms = [10.0, 12.5][rank]
+    got = bench.max_over_ranks(dist, ms, "cpu")
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((rank, got))
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=5) for _ in range(2))
+    assert res == {0: 12.5, 1: 12.5}
+
+
+def test_job_gbs_counts_every_replica():
+    one = bench.job_gbs(1, bench.ALG_BYTES, 10, 5.0)
+    assert bench.job_gbs(4, bench.ALG_BYTES, 10, 5.0) == pytest.approx(4 * one)
+    assert one == pytest.approx(bench.ALG_BYTES * 10 / 5e-3 / 1e9)
+
+
+def test_reference_arm_nonzero_rank_exits_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], env=env, capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0
+    assert res.stdout.strip() == ""
