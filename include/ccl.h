@@ -59,6 +59,8 @@ extern "C" {
 
 #define CCL_MAX_RANKS 1024
 #define CCL_DEFAULT_BUCKET_BYTES (25u * 1024u * 1024u)
+/* Size of the fixed device working space of ccl_reduce_scatter_step_static. */
+#define CCL_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 typedef enum { CCL_FP32 = 0, CCL_BF16 = 1 } ccl_dtype_t;
 typedef enum { CCL_SUM = 0, CCL_AVG = 1, CCL_MAX = 2, CCL_PROD = 3 } ccl_op_t;
@@ -139,6 +141,31 @@ ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nrank
 ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int ntensors, int nranks,
                                   size_t bucket_bytes, ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode,
                                   cudaStream_t stream);
+
+/* Step-by-step ReduceScatter that allocates nothing.  The pages have no
+ * counterpart: this exists for callers that cannot let a library call
+ * cudaMalloc -- a process whose framework has already reserved the GPU's
+ * memory in its own caching pool (a raw cudaMalloc then fails or fragments
+ * what is left), code that must not stall other streams on the device
+ * synchronisation cudaMalloc/cudaFree can imply, or hosts that forbid driver
+ * allocations after start-up.
+ * Same arguments, result and error checks as ccl_reduce_scatter in
+ * CCL_MODE_STEP (identical bits), but the working copies of the N inputs live
+ * in one fixed array of CCL_STATIC_SCRATCH_BYTES (32 MiB) in device memory,
+ * reserved when the library loads and held by every GPU that loads it until
+ * the process exits.  nranks * round_up(count * element size, 256) must not
+ * exceed CCL_STATIC_SCRATCH_BYTES: larger calls return CCL_ERR_INVALID_ARG
+ * before anything is enqueued.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the array and leaves its contents behind.
+ *     Each call overwrites every byte it later reads, so nothing needs
+ *     clearing, but calls whose work overlaps on the GPU (other streams, other
+ *     host threads) race on it: serialise them. */
+ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, void *const *recv, int nranks, size_t count,
+                                            ccl_dtype_t dtype, ccl_op_t op, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* Planner (host only; no GPU needed)                                  */

@@ -1,0 +1,130 @@
+// noalloc.cu -- step-by-step ReduceScatter that never allocates device memory.
+//
+// The regular step-mode ReduceScatter (ccl_reduce_scatter with CCL_MODE_STEP)
+// needs N*count elements of working space, which the library gets with
+// cudaMalloc the first time and keeps.  Some callers cannot let a library do
+// that: a process whose framework has already reserved the GPU's memory in its
+// own caching pool (a raw cudaMalloc then fails or fragments what is left),
+// code that must not stall other streams on the implicit device
+// synchronisation that cudaMalloc/cudaFree can cause, or hosts that forbid
+// driver allocations outside start-up.  This variant runs the same ring steps
+// with its working space in one fixed array in device memory, reserved when
+// the library is loaded.
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+#include <algorithm>
+
+#include "../../include/ccl.h"
+#include "ccl_internal.h"
+
+namespace {
+
+// The working space, CCL_STATIC_SCRATCH_BYTES per device.  Every GPU that loads
+// this library keeps it until the process exits.  All calls on a device share
+// it, so two calls whose work overlaps on that GPU (different streams, or
+// different host threads) race on it.
+static __device__ __align__(256) unsigned char ccl_static_scratch[CCL_STATIC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+std::unordered_map<int, void *> g_scratch_addr; // device -> device address of ccl_static_scratch
+
+// Host code only sees a host-side stand-in for ccl_static_scratch; the device
+// address comes from cudaGetSymbolAddress, once per device, with that device
+// current.
+ccl_status_t scratch_address(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return CCL_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    auto it = g_scratch_addr.find(dev);
+    if (it == g_scratch_addr.end()) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, ccl_static_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return CCL_ERR_CUDA;
+        }
+        it = g_scratch_addr.emplace(dev, p).first;
+    }
+    *out = it->second;
+    return CCL_OK;
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+} // namespace
+
+using namespace ccl;
+
+extern "C" ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, void *const *recv, int nranks,
+                                                       size_t count, ccl_dtype_t dtype, ccl_op_t op,
+                                                       cudaStream_t stream)
+{
+    if (nranks < 1 || nranks > CCL_MAX_RANKS || (dtype != CCL_FP32 && dtype != CCL_BF16) ||
+        (op != CCL_SUM && op != CCL_AVG && op != CCL_MAX && op != CCL_PROD) || !send || !recv)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = dtype == CCL_BF16 ? 2 : 4;
+    if (count > SIZE_MAX / es)
+        return CCL_ERR_INVALID_ARG;
+    // each rank's working copy starts on a 256-byte boundary
+    const size_t stride = (count * es + 255) & ~(size_t)255;
+    if (stride < count * es || stride > CCL_STATIC_SCRATCH_BYTES / (size_t)nranks)
+        return CCL_ERR_INVALID_ARG; // more than the fixed working space holds
+    if (count == 0)
+        return CCL_OK;
+    Partition part;
+    part.q = count / (uint64_t)nranks;
+    part.rem = (uint32_t)(count % (uint64_t)nranks);
+    // outputs pairwise disjoint; an output may sit inside its own rank's input
+    // only at that rank's chunk offset (the in-place form)
+    for (int i = 0; i < nranks; ++i)
+        if (!send[i] || (!recv[i] && part.len((uint32_t)i) > 0))
+            return CCL_ERR_INVALID_ARG;
+    for (int i = 0; i < nranks; ++i) {
+        const uintptr_t w0 = (uintptr_t)recv[i], w1 = w0 + part.len((uint32_t)i) * es;
+        if (w0 == w1)
+            continue;
+        for (int j = 0; j < nranks; ++j) {
+            const uintptr_t r0 = (uintptr_t)send[j], r1 = r0 + count * es;
+            if (overlaps(w0, w1, r0, r1) && !(i == j && w0 == r0 + part.off((uint32_t)i) * es))
+                return CCL_ERR_OVERLAP;
+            if (j != i) {
+                const uintptr_t v0 = (uintptr_t)recv[j], v1 = v0 + part.len((uint32_t)j) * es;
+                if (v0 != v1 && overlaps(w0, w1, v0, v1))
+                    return CCL_ERR_OVERLAP;
+            }
+        }
+    }
+    void *base = nullptr;
+    ccl_status_t st = scratch_address(&base);
+    if (st != CCL_OK)
+        return st;
+    std::vector<void *> bufs(nranks);
+    for (int i = 0; i < nranks; ++i)
+        bufs[i] = static_cast<char *>(base) + (size_t)i * stride;
+    // Every scratch byte the ring reads below is first written by this copy, so
+    // whatever an earlier call left in the array never reaches the result.
+    std::vector<CopySeg> segs;
+    for (int i = 0; i < nranks; ++i)
+        segs.push_back(CopySeg{static_cast<const char *>(send[i]), static_cast<char *>(bufs[i]), count * es, 0});
+    if (launch_copy_segments(segs.data(), segs.size(), stream) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    for (int s = 0; s < nranks - 1; ++s)
+        if (launch_ring_step((int)dtype, (int)op, STEP_RS, s, bufs.data(), nranks, count, stream) != cudaSuccess)
+            return CCL_ERR_CUDA;
+    if (op == CCL_AVG &&
+        launch_ring_step((int)dtype, (int)op, STEP_SCALE, 0, bufs.data(), nranks, count, stream) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    // the ReduceScatter phase leaves chunk c finished at rank c-1; hand it to rank c
+    segs.clear();
+    for (int c = 0; c < nranks; ++c)
+        segs.push_back(CopySeg{static_cast<const char *>(bufs[ring_mod(c - 1, nranks)]) +
+                                   part.off((uint32_t)c) * es,
+                               static_cast<char *>(recv[c]), part.len((uint32_t)c) * es, 0});
+    if (launch_copy_segments(segs.data(), segs.size(), stream) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    return CCL_OK;
+}
