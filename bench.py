@@ -95,7 +95,7 @@ class ClockSampler:
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -153,23 +153,188 @@ def job_gbs(world: int, bytes_per_step: int, steps: int, ms: float) -> float:
 
 def oracle_sample_gbs(target_s: float, max_count: int = COUNT):
     """Time the CPU oracle (step-by-step ring simulation, single thread) on a
-    sample of the workload: N=8 ranks, a prefix length of the per-rank buffer
-    sized to take about target_s seconds.  Returns (GB/s, sample description)."""
+    sample of the workload: N=8 ranks, the first k elements of each rank's
+    buffer, k sized from a short probe to take about target_s seconds.
+    Returns (GB/s, seconds, k)."""
     import oracle
     from ring_allreduce_rank_gb300 import workloads as W
 
     oracle.build()
-    k = 1 << 18
-    while True:
-        x = list(W.normal_bf16(NRANKS, k, std=1e-3, seed_base=0))
-        t0 = time.perf_counter()
-        oracle.ring_allreduce(x, "avg")
-        dt = time.perf_counter() - t0
-        if dt >= target_s / 4 or k >= max_count:
-            break
-        k = min(max_count, int(k * max(2.0, min(16.0, target_s / max(dt, 1e-3) / 2))))
-    gbs = 2 * NRANKS * k * ELEM / dt / 1e9
-    return gbs, dt, k
+    k = min(1 << 18, max_count)
+    x = list(W.normal_bf16(NRANKS, k, std=1e-3, seed_base=0))
+    t0 = time.perf_counter()
+    oracle.ring_allreduce(x, "avg")
+    dt = time.perf_counter() - t0
+    k = int(min(max_count, max(1 << 12, k * target_s / max(dt, 1e-4)))) // 8 * 8
+    x = list(W.normal_bf16(NRANKS, k, std=1e-3, seed_base=0))
+    t0 = time.perf_counter()
+    oracle.ring_allreduce(x, "avg")
+    dt = time.perf_counter() - t0
+    return 2 * NRANKS * k * ELEM / dt / 1e9, dt, k
+
+
+# ------------------------------------------------------------------ the other collectives' workloads
+
+ROWS = {
+    "allreduce-step": "AllReduce AVG, N=8 bf16 64Mi/rank, in place, step mode (2(N-1) launches + 1 AVG scale)",
+    "reduce-scatter": "ReduceScatter SUM, N=16 fp32, 16,777,259 elements/rank (ragged chunks)",
+    "allgather": "AllGather, N=16 fp32, 16,777,259 elements total (ragged chunks)",
+    "broadcast": "Broadcast from rank 0, N=8 bf16 64Mi elements, in place",
+    "alltoallv": "AllToAllv MoE dispatch, N=8, 4096 tokens x 7168 bf16/rank, Zipf(1.2) top-1 over 64 experts",
+    "bucket": "bucket-fused AllReduce SUM, N=8 bf16, 4 Llama layers (809,533,440 elements/rank), 25 MiB buckets",
+    "sweep": "AllReduce SUM bf16, 1 KiB..1 GiB per rank (x4), N in {2,4,8,16,64}",
+}
+
+
+def _timed(torch, ccl, step, steps, warmup, stream, dev):
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    n0 = ccl.ccl_launch_count()
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    per = [a.elapsed_time(b) for a, b in ev]
+    return sum(per), per, ccl.ccl_launch_count() - n0
+
+
+def run_row(args, name, local):
+    """One of the other collectives' workloads, printed as its own JSON line.
+    Inputs come from a seeded torch generator on the device (values do not
+    change the timing; parity at these sizes is covered by the GPU tests)."""
+    import torch
+
+    import ring_allreduce_rank_gb300 as ccl
+    from ring_allreduce_rank_gb300 import workloads as W
+    from ring_allreduce_rank_gb300.arena import RankArena
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ccl.lib()
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    peak, peak_src = measured_peak()
+    clocks = ClockSampler(local)
+
+    def randn_bf16(n):
+        return (torch.randn(n, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+
+    def line(metric, alg, per_ms, launches, kernel, dtype, config, extra=None):
+        tot = sum(per_ms)
+        val = alg * len(per_ms) / (tot / 1e3) / 1e9
+        d = {"metric": metric, "value": round(val, 2), "unit": UNIT, "n_gpus": 1, "steps": len(per_ms),
+             "warmup": max(args.warmup, 3), "ms_per_step": round(tot / len(per_ms), 5), "higher_is_better": True,
+             "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+             "config": dict(config, workload=ROWS[name]),
+             "roofline": {"bound": "hbm", "achieved": round(val, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(val / peak, 4), "traffic": None, "algorithmic_bytes_per_step": alg,
+                          "peak_source": peak_src, "kernel": kernel},
+             "cpu_baseline": None, "e2e": None, "gpu_launches": int(launches)}
+        if extra:
+            d.update(extra)
+        return d
+
+    if name == "sweep":
+        points = []
+        for N in (2, 4, 8, 16, 64):
+            for S in [1 << k for k in range(10, 31, 2)]:
+                K = S // 2
+                arena = RankArena(N, K, torch.bfloat16, device=dev)
+                for r in range(N):
+                    arena.ranks[r].copy_(randn_bf16(K))
+                steps = max(args.steps, min(2000, int(2e9 / max(S * N, 1))))
+                tot, per, launches = _timed(torch, ccl, lambda: ccl.ccl_allreduce(arena.ranks, op="sum",
+                                                                                    stream=stream),
+                                            steps, args.warmup, stream, dev)
+                t = tot / steps / 1e3
+                alg = 2 * N * S
+                points.append({"N": N, "bytes_per_rank": S, "us": round(t * 1e6, 3),
+                               "GBs": round(alg / t / 1e9, 2), "frac": round(alg / t / 1e9 / peak, 4),
+                               "algbw_GBs": round(S / t / 1e9, 3), "busbw_GBs": round(S / t / 1e9 * 2 * (N - 1) / N, 3)})
+                del arena
+                torch.cuda.empty_cache()
+        big = max(points, key=lambda p: p["GBs"])
+        d = line("AllReduce sweep HBM GB/s, bf16, 1 KiB..1 GiB per rank, N in {2,4,8,16,64}, 1 GB300", 2 * big["N"] *
+                 big["bytes_per_rank"], [big["us"] / 1e3], 1, "fused_reduce_kernel<bf16, SUM, N>", "bf16",
+                 {"op": "sum", "mode": "fused"}, {"points": points})
+        print(json.dumps(d))
+        return
+
+    if name in ("allreduce-step", "broadcast"):
+        N, K = 8, 64 * 1024 * 1024
+        arena = RankArena(N, K, torch.bfloat16, device=dev)
+        for r in range(N):
+            arena.ranks[r].copy_(randn_bf16(K))
+        if name == "allreduce-step":
+            step = lambda: ccl.ccl_allreduce(arena.ranks, op="avg", mode="step", stream=stream)
+            alg, kernel = 2 * N * K * 2, "ring_step_kernel<bf16, AVG> x 14 + AVG scale"
+            metric = "AllReduce (step mode) HBM GB/s of the algorithmic 2*N*M bytes, N=8 bf16 128 MB/rank, 1 GB300"
+        else:
+            step = lambda: ccl.ccl_broadcast(arena.ranks, arena.ranks, root=0, stream=stream)
+            alg, kernel = N * K * 2, "fanout_kernel<bf16> (1 source, N-1 destinations)"
+            metric = "Broadcast HBM GB/s, N=8 bf16 128 MB, in place, 1 GB300"
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        print(json.dumps(line(metric, alg, per, launches, kernel, "bf16", {"nranks": N, "count": K},
+                              {"clocks": clk})))
+        return
+
+    if name in ("reduce-scatter", "allgather"):
+        N, K = 16, 16_777_259
+        off, ln = ccl.ccl_plan_chunks(K, N)
+        full = [torch.empty(K, dtype=torch.float32, device=dev).uniform_(-1, 1, generator=g) for _ in range(N)]
+        part = [torch.empty(ln[r], dtype=torch.float32, device=dev).uniform_(-1, 1, generator=g) for r in range(N)]
+        if name == "reduce-scatter":
+            step = lambda: ccl.ccl_reduce_scatter(full, part, op="sum", stream=stream)
+            alg, kernel = N * K * 4 + K * 4, "fused_reduce_kernel<fp32, SUM, 16 ranks> (ReduceScatter)"
+            metric = "ReduceScatter HBM GB/s, N=16 fp32 16,777,259/rank (ragged), 1 GB300"
+        else:
+            step = lambda: ccl.ccl_allgather(part, full, stream=stream)
+            alg, kernel = K * 4 + N * K * 4, "fanout_kernel<fp32> (AllGather)"
+            metric = "AllGather HBM GB/s, N=16 fp32 16,777,259 total (ragged), 1 GB300"
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        print(json.dumps(line(metric, alg, per, launches, kernel, "fp32", {"nranks": N, "count": K},
+                              {"clocks": clk})))
+        return
+
+    if name == "alltoallv":
+        N, T, H = 8, 4096, 7168
+        counts = W.zipf_expert_counts(N, T, 64, 1.2, 1000) * H
+        send = [randn_bf16(T * H) for _ in range(N)]
+        recv = [torch.empty(int(counts[:, j].sum()), dtype=torch.bfloat16, device=dev) for j in range(N)]
+        cl = counts.tolist()
+        step = lambda: ccl.ccl_alltoallv(send, recv, cl, stream=stream)
+        alg = 2 * int(counts.sum()) * 2
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        print(json.dumps(line("AllToAllv HBM GB/s, N=8 MoE dispatch 4096x7168 bf16/rank, 1 GB300", alg, per,
+                              launches, "copy_segments_kernel (64 blocks)", "bf16",
+                              {"nranks": N, "tokens": T, "hidden": H, "max_recv_tokens": int(counts.sum(0).max() // H)},
+                              {"clocks": clk})))
+        return
+
+    if name == "bucket":
+        N = 8
+        numels = W.llama_layer_numels(4)
+        grads = [[randn_bf16(n) for n in numels] for _ in range(N)]
+        step = lambda: ccl.ccl_bucket_allreduce(grads, bucket_bytes=25 * W.MiB, op="sum", stream=stream)
+        alg = 2 * N * sum(numels) * 2
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        print(json.dumps(line("Bucket-fused AllReduce HBM GB/s, N=8 bf16 4 Llama layers (1.62 GB/rank), 25 MiB "
+                              "buckets, 1 GB300", alg, per, launches, "bucket_reduce_kernel<bf16, SUM, 8>", "bf16",
+                              {"nranks": N, "tensors": len(numels), "buckets": 62}, {"clocks": clk})))
+        return
+    raise SystemExit("unknown workload %s" % name)
 
 
 # ------------------------------------------------------------------ main
@@ -177,13 +342,15 @@ def oracle_sample_gbs(target_s: float, max_count: int = COUNT):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--count", type=int, default=COUNT,
                     help="elements per rank (default: the 64Mi-element workload; smaller values are for profiling)")
+    ap.add_argument("--workload", default="allreduce", choices=["allreduce"] + sorted(ROWS),
+                    help="allreduce (the headline) or another collective's workload, each printed as its own line")
     args = ap.parse_args()
     if args.count != COUNT:
         set_count(args.count)
@@ -196,6 +363,9 @@ def main():
         if rank != 0:
             return
         run_reference(args)
+        return
+    if args.workload != "allreduce":
+        run_row(args, args.workload, local)
         return
 
     import torch
@@ -349,8 +519,8 @@ def run_reference(args):
 
     oracle.build()
     steps, warm = args.steps, max(args.warmup, 3)
-    budget = 150.0
-    _, dt, k = oracle_sample_gbs(target_s=budget / (steps + warm) * 2, max_count=COUNT)
+    budget = 120.0  # seconds for the whole run
+    _, dt, k = oracle_sample_gbs(target_s=budget / (steps + warm), max_count=COUNT)
     x = list(W.normal_bf16(NRANKS, k, std=1e-3, seed_base=0))
     for _ in range(warm):
         oracle.ring_allreduce(x, "avg")

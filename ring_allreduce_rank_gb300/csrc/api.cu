@@ -416,8 +416,15 @@ ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nrank
     if (st != CCL_OK)
         return st;
     if (mode == CCL_MODE_FUSED) {
+        // in place, root already holds the data: write only the other ranks
         const void *src[1] = {send[root]};
-        return from_cuda(launch_fanout((int)dtype, src, 1, recv, nranks, count, stream));
+        std::vector<void *> dst;
+        for (int i = 0; i < nranks; ++i)
+            if (recv[i] != send[root])
+                dst.push_back(recv[i]);
+        if (dst.empty())
+            return CCL_OK;
+        return from_cuda(launch_fanout((int)dtype, src, 1, dst.data(), (int)dst.size(), count, stream));
     }
     // step mode: a chain around the ring starting at root
     if (send[root] != recv[root]) {
