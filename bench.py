@@ -182,7 +182,8 @@ ROWS = {
     "broadcast": "Broadcast from rank 0, N=8 bf16 64Mi elements, in place",
     "alltoallv": "AllToAllv MoE dispatch, N=8, 4096 tokens x 7168 bf16/rank, Zipf(1.2) top-1 over 64 experts",
     "bucket": "bucket-fused AllReduce SUM, N=8 bf16, 4 Llama layers (809,533,440 elements/rank), 25 MiB buckets",
-    "sweep": "AllReduce SUM bf16, 1 KiB..1 GiB per rank (x4), N in {2,4,8,16,64}",
+    "sweep": "AllReduce SUM bf16, 1 KiB..1 GiB per rank (x4), N in {2,4,8,16,64}; device time per call from "
+             "CUDA-graph replay; points whose N*S fits in L2 are marked l2_resident (replays hit L2, not HBM)",
 }
 
 
@@ -199,6 +200,35 @@ def _timed(torch, ccl, step, steps, warmup, stream, dev):
     torch.cuda.synchronize(dev)
     per = [a.elapsed_time(b) for a, b in ev]
     return sum(per), per, ccl.ccl_launch_count() - n0
+
+
+def graph_call_seconds(torch, ccl, call, nbytes, dev) -> float:
+    """Device time per call: R calls captured once in a CUDA graph and
+    replayed, so the host's per-call cost (Python, argument checks, launch)
+    is not in the measurement.  R keeps each replay around 20 ms."""
+    R = int(max(1, min(500, 2e10 / max(nbytes, 1) / 1e3)))
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            call(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = torch.cuda.current_stream(dev)
+        for _ in range(R):
+            call(st)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    reps = 5
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize(dev)
+    del g
+    return a.elapsed_time(b) / 1e3 / (R * reps)
 
 
 def run_row(args, name, local):
@@ -246,18 +276,17 @@ def run_row(args, name, local):
                 arena = RankArena(N, K, torch.bfloat16, device=dev)
                 for r in range(N):
                     arena.ranks[r].copy_(randn_bf16(K))
-                steps = max(args.steps, min(2000, int(2e9 / max(S * N, 1))))
-                tot, per, launches = _timed(torch, ccl, lambda: ccl.ccl_allreduce(arena.ranks, op="sum",
-                                                                                    stream=stream),
-                                            steps, args.warmup, stream, dev)
-                t = tot / steps / 1e3
+                t = graph_call_seconds(torch, ccl, lambda st: ccl.ccl_allreduce(arena.ranks, op="sum", stream=st),
+                                       S * N, dev)
                 alg = 2 * N * S
                 points.append({"N": N, "bytes_per_rank": S, "us": round(t * 1e6, 3),
+                               "l2_resident": N * S <= 96 * 1024 * 1024,
                                "GBs": round(alg / t / 1e9, 2), "frac": round(alg / t / 1e9 / peak, 4),
                                "algbw_GBs": round(S / t / 1e9, 3), "busbw_GBs": round(S / t / 1e9 * 2 * (N - 1) / N, 3)})
                 del arena
                 torch.cuda.empty_cache()
-        big = max(points, key=lambda p: p["GBs"])
+        # the line's value: N=8 at 1 GiB per rank (HBM-bound); every point is listed
+        big = [p for p in points if p["N"] == 8 and p["bytes_per_rank"] == 1 << 30][0]
         d = line("AllReduce sweep HBM GB/s, bf16, 1 KiB..1 GiB per rank, N in {2,4,8,16,64}, 1 GB300", 2 * big["N"] *
                  big["bytes_per_rank"], [big["us"] / 1e3], 1, "fused_reduce_kernel<bf16, SUM, N>", "bf16",
                  {"op": "sum", "mode": "fused"}, {"points": points})
@@ -452,17 +481,10 @@ def main():
                "h2d_bytes_per_step": NRANKS * COUNT * ELEM, "d2h_bytes_per_step": NRANKS * COUNT * ELEM,
                "steps": args.e2e_steps}
 
-    # alpha: one tiny AllReduce (latency of a launch through the API)
+    # alpha: device time of one tiny AllReduce (8 elements per rank), from a
+    # CUDA graph of many such calls, so host call overhead is excluded
     tiny = [torch.zeros(8, dtype=torch.bfloat16, device=dev) for _ in range(NRANKS)]
-    for _ in range(5):
-        ccl.ccl_allreduce(tiny, op="sum", stream=stream)
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(50):
-        ccl.ccl_allreduce(tiny, op="sum", stream=stream)
-    a1.record(stream)
-    torch.cuda.synchronize(dev)
-    alpha_s = a0.elapsed_time(a1) / 50 / 1e3
+    alpha_s = graph_call_seconds(torch, ccl, lambda st: ccl.ccl_allreduce(tiny, op="sum", stream=st), 16, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -496,7 +518,7 @@ def main():
                        "model_ms": round((2 * (NRANKS - 1) * alpha_s + 2 * (NRANKS - 1) / NRANKS * M /
                                           (peak * 1e9)) * 1e3, 4),
                        "formula": "algbw = M/t; busbw = algbw*2(N-1)/N; T = 2(N-1)alpha + 2(N-1)/N * M/beta, "
-                                  "M = bytes per rank, alpha = one tiny AllReduce, beta = HBM peak"},
+                                  "M = bytes per rank, alpha = device time of one 8-element AllReduce (CUDA graph replay), beta = HBM peak"},
     }
     print(json.dumps(line))
     if dist:

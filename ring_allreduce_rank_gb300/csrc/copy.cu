@@ -162,6 +162,46 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
     const uint64_t off = p.part.off(c), len = p.part.len(c);
     const void *src = p.src[c];
     const int M = p.ndst;
+    if (p.vec_aligned && off % VEC != 0) {
+        // The chunk lands at an offset that is not a whole vector (ragged
+        // partition): keep the N-fold stores as aligned 16-byte vectors and
+        // gather each vector's source elements one at a time (the source is
+        // only 1/N of the bytes moved).
+        const uint64_t vb = (off + VEC - 1) / VEC, ve = (off + len) / VEC;
+        if (t == 0) {
+            const uint64_t hb = vb < ve ? vb * VEC : off + len;
+            for (uint64_t d = off + threadIdx.x; d < hb; d += kThreads) {
+                const uint32_t v = ld_elem<DT>(src, d - off);
+                for (int q = 0; q < M; ++q)
+                    st_elem<DT>(p.dst[q], d, v);
+            }
+            if (vb < ve)
+                for (uint64_t d = ve * VEC + threadIdx.x; d < off + len; d += kThreads) {
+                    const uint32_t v = ld_elem<DT>(src, d - off);
+                    for (int q = 0; q < M; ++q)
+                        st_elem<DT>(p.dst[q], d, v);
+                }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = vb + (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
+            if (v >= ve)
+                continue;
+            const uint64_t s0 = v * VEC - off; // first source element of this vector
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (DT == DT_FP32)
+                    w[k] = ld_elem<DT>(src, s0 + k);
+                else
+                    w[k] = ld_elem<DT>(src, s0 + 2 * k) | (ld_elem<DT>(src, s0 + 2 * k + 1) << 16);
+            }
+            const uint4 x = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int q = 0; q < M; ++q)
+                st16(static_cast<char *>(p.dst[q]) + v * 16, x);
+        }
+        return;
+    }
     if (!(p.vec_aligned && off % VEC == 0)) {
         const uint64_t e0 = (uint64_t)t * TV * VEC;
         for (int k = 0; k < U * VEC; ++k) {
