@@ -24,8 +24,8 @@ SRC = os.path.join(HERE, "ring_oracle.c")
 LIB = os.path.join(HERE, "_build", "liboracle.so")
 
 FP32, BF16 = 0, 1
-SUM, AVG, MAX, PROD = 0, 1, 2, 3
-OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD}
+SUM, AVG, MAX, PROD, MIN = 0, 1, 2, 3, 4
+OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN}
 
 _lock = threading.Lock()
 _lib = None
@@ -67,12 +67,16 @@ def lib() -> ctypes.CDLL:
             L.oracle_ring_allreduce_gathered.argtypes = [pp, i32, u64, i32, i32, p64, u64, vp]
             L.oracle_reduce_scatter.argtypes = [pp, pp, i32, u64, i32, i32]
             L.oracle_allgather.argtypes = [pp, pp, i32, u64, i32]
+            L.oracle_reduce.argtypes = [pp, pp, i32, i32, u64, i32, i32]
+            L.oracle_gather.argtypes = [pp, vp, i32, u64, i32]
+            L.oracle_scatter.argtypes = [vp, pp, i32, u64, i32]
             L.oracle_broadcast.argtypes = [pp, pp, i32, i32, u64, i32]
             L.oracle_alltoallv.argtypes = [pp, pp, i32, p64, i32]
             L.oracle_bucket_allreduce.argtypes = [pp, p64, i32, i32, u64, i32, i32]
             L.oracle_sum_f64.argtypes = [pp, i32, u64, i32, i32, vp, vp]
             for name in ("oracle_ring_allreduce", "oracle_ring_allreduce_closed", "oracle_ring_allreduce_at",
-                         "oracle_ring_allreduce_gathered", "oracle_reduce_scatter", "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
+                         "oracle_ring_allreduce_gathered", "oracle_reduce_scatter", "oracle_reduce", "oracle_gather",
+                         "oracle_scatter", "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
                          "oracle_bucket_allreduce", "oracle_sum_f64"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -184,6 +188,31 @@ def reduce_scatter(bufs, op="sum"):
     outs = [np.empty(ln[r], dtype=ins[0].dtype) for r in range(N)]
     _check(lib().oracle_reduce_scatter(_ptrs(ins), _ptrs(outs), N, K, _dtype_code(ins[0]), _op(op)),
            "oracle_reduce_scatter")
+    return outs
+
+
+def reduce(bufs, root: int, op="sum"):
+    """Only rank root's buffer changes (to the AllReduce result); returns all N."""
+    ins = [np.ascontiguousarray(b) for b in bufs]
+    outs = [np.array(b, copy=True) for b in ins]
+    _check(lib().oracle_reduce(_ptrs(ins), _ptrs(outs), len(ins), root, ins[0].size, _dtype_code(ins[0]), _op(op)),
+           "oracle_reduce")
+    return outs
+
+
+def gather(chunks, K: int) -> np.ndarray:
+    """chunks[r] = rank r's slice; returns the root's concatenation."""
+    ins = [np.ascontiguousarray(c) for c in chunks]
+    out = np.zeros(K, dtype=ins[0].dtype)
+    _check(lib().oracle_gather(_ptrs(ins), out.ctypes.data, len(ins), K, _dtype_code(ins[0])), "oracle_gather")
+    return out
+
+
+def scatter(root_buf, N: int):
+    src = np.ascontiguousarray(root_buf)
+    _, ln = partition(src.size, N)
+    outs = [np.zeros(ln[r], dtype=src.dtype) for r in range(N)]
+    _check(lib().oracle_scatter(src.ctypes.data, _ptrs(outs), N, src.size, _dtype_code(src)), "oracle_scatter")
     return outs
 
 

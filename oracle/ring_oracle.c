@@ -21,7 +21,8 @@
  *     rounding a NaN to bf16 keeps its sign and top payload bits and sets the
  *     quiet bit;
  *   - MAX: NaN if either operand is NaN, else the larger, and for +0 vs -0 the
- *     bitwise AND of the two (so +0 wins);
+ *     bitwise AND of the two (so +0 wins); MIN: NaN if either is NaN, else the
+ *     smaller, and for +0 vs -0 the bitwise OR (so -0 wins);
  *   - AVG: SUM around the ring, then one fp32 division by N at the rank that
  *     holds the finished chunk, rounded to the buffer type, before the gather.
  *
@@ -39,6 +40,7 @@
 #define OR_AVG 1
 #define OR_MAX 2
 #define OR_PROD 3
+#define OR_MIN 4
 
 #define OR_OK 0
 #define OR_EINVAL 1
@@ -109,6 +111,16 @@ static uint32_t op_f32(uint32_t a_bits, uint32_t b_bits, int op)
         else
             r = a_bits & b_bits; /* equal: identical bits, or +0 vs -0 -> +0 */
         break;
+    case OR_MIN:
+        if (f32_bits_is_nan(a_bits) || f32_bits_is_nan(b_bits))
+            r = 0x7fffffffu;
+        else if (a < b)
+            r = a_bits;
+        else if (b < a)
+            r = b_bits;
+        else
+            r = a_bits | b_bits; /* equal: identical bits, or +0 vs -0 -> -0 */
+        break;
     default:
         r = 0x7fffffffu;
     }
@@ -155,7 +167,7 @@ static int mod(int64_t a, int n) { int64_t r = a % n; return (int)(r < 0 ? r + n
 
 static int bad_args(int N, int dtype, int op)
 {
-    return N < 1 || (dtype != OR_FP32 && dtype != OR_BF16) || op < OR_SUM || op > OR_PROD;
+    return N < 1 || (dtype != OR_FP32 && dtype != OR_BF16) || op < OR_SUM || op > OR_MIN;
 }
 
 /* ------------------------------------------------------------------ */
@@ -406,6 +418,84 @@ done:
             free(work[r]);
     free(work); free(off); free(len); free(snap);
     return rc;
+}
+
+/* Reduce to one rank: only out[root] receives the reduction; every other
+ * out[r] is left untouched.  AllReduce is a Reduce followed by a Broadcast
+ * (Lesson 3, core concepts: "Reduce (many-to-one)" and AllReduce), so the
+ * root receives exactly the AllReduce's bits: the ring's ReduceScatter phase,
+ * then each finished chunk c brought from rank c-1 to the root. */
+int oracle_reduce(const void **in, void **out, int N, int root, uint64_t K, int dtype, int op)
+{
+    if (bad_args(N, dtype, op) || root < 0 || root >= N)
+        return OR_EINVAL;
+    size_t es = esize(dtype);
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
+    uint64_t stride = K / (uint64_t)N + 1;
+    void *snap = malloc((size_t)N * stride * es);
+    void **work = calloc((size_t)N, sizeof(void *));
+    int rc = OR_OK;
+    if (!off || !len || !snap || !work) {
+        rc = OR_ENOMEM;
+        goto done;
+    }
+    for (int r = 0; r < N; ++r) {
+        work[r] = malloc(K * es + 1);
+        if (!work[r]) {
+            rc = OR_ENOMEM;
+            goto done;
+        }
+        memcpy(work[r], in[r], K * es);
+    }
+    oracle_partition(K, N, off, len);
+    rs_phase(work, N, off, len, dtype, op, NULL, snap, stride);
+    for (int c = 0; c < N; ++c)
+        memcpy((char *)out[root] + off[c] * es, (char *)work[mod((int64_t)c - 1, N)] + off[c] * es, len[c] * es);
+done:
+    if (work)
+        for (int r = 0; r < N; ++r)
+            free(work[r]);
+    free(work); free(off); free(len); free(snap);
+    return rc;
+}
+
+/* Gather: the root receives every rank's slice, concatenated in rank order
+ * (Lesson 3, core concepts: "Gather (many-to-one)"); in[r] is chunk r
+ * (len_r elements) of the K-element result. */
+int oracle_gather(const void **in, void *out_root, int N, uint64_t K, int dtype)
+{
+    if (bad_args(N, dtype, OR_SUM))
+        return OR_EINVAL;
+    size_t es = esize(dtype);
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
+    if (!off || !len) {
+        free(off); free(len);
+        return OR_ENOMEM;
+    }
+    oracle_partition(K, N, off, len);
+    for (int r = 0; r < N; ++r)
+        memcpy((char *)out_root + off[r] * es, in[r], len[r] * es);
+    free(off); free(len);
+    return OR_OK;
+}
+
+/* Scatter: the root's K elements split into the N chunks, chunk r to rank r
+ * (Lesson 3, core concepts: "Scatter (one-to-many)", the inverse of Gather). */
+int oracle_scatter(const void *in_root, void **out, int N, uint64_t K, int dtype)
+{
+    if (bad_args(N, dtype, OR_SUM))
+        return OR_EINVAL;
+    size_t es = esize(dtype);
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
+    if (!off || !len) {
+        free(off); free(len);
+        return OR_ENOMEM;
+    }
+    oracle_partition(K, N, off, len);
+    for (int r = 0; r < N; ++r)
+        memcpy(out[r], (const char *)in_root + off[r] * es, len[r] * es);
+    free(off); free(len);
+    return OR_OK;
 }
 
 /* AllGather API: rank r contributes chunk r (len_r elements, in[r]); every

@@ -65,6 +65,13 @@ def test_worked_examples(oracle_mod, case):
         outs = oracle_mod.alltoallv(ins, counts)
         for o, e in zip(outs, exp):
             np.testing.assert_array_equal(o, e)
+    elif kind == "reduce":
+        outs = oracle_mod.reduce(ins, case["root"], case["op"])
+        for o, e in zip(outs, exp):
+            np.testing.assert_array_equal(o, e)
+    elif kind == "gather":
+        out = oracle_mod.gather(ins, exp[0].size)
+        np.testing.assert_array_equal(out, exp[0])
     else:
         raise AssertionError(kind)
 
@@ -213,7 +220,7 @@ def _inputs(dtype, N, K, seed):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min"])
 @pytest.mark.parametrize("N,K", [(1, 7), (2, 9), (3, 3), (3, 0), (4, 37), (5, 3), (7, 101), (8, 1000), (16, 517)])
 def test_step_simulation_equals_closed_form(oracle_mod, dtype, op, N, K):
     """The step-by-step ring simulation and the closed-form fold are written
@@ -285,6 +292,46 @@ def test_max_is_order_free_brute_force(oracle_mod):
         else:
             outs, _ = oracle_mod.ring_allreduce(list(x), "max")
             np.testing.assert_array_equal(outs[0], x.max(axis=0))
+
+
+def test_min_is_order_free_brute_force(oracle_mod):
+    """MIN takes no rounding: it equals numpy's minimum over ranks."""
+    N, K = 6, 401
+    x = W.normal_fp32(N, K, seed_base=8)
+    outs, _ = oracle_mod.ring_allreduce(list(x), "min")
+    np.testing.assert_array_equal(outs[0], x.min(axis=0))
+    xb = [W.to_bf16_bits(r) for r in x]
+    outb, _ = oracle_mod.ring_allreduce(xb, "min")
+    ref = W.to_bf16_bits(np.min(np.stack([W.bf16_bits_to_f32(r) for r in xb]), axis=0))
+    np.testing.assert_array_equal(outb[0], ref)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min"])
+@pytest.mark.parametrize("N,K,root", [(1, 5, 0), (3, 5, 0), (4, 37, 3), (8, 1000, 5), (5, 3, 2)])
+def test_reduce_is_allreduce_at_root_others_unchanged(oracle_mod, dtype, op, N, K, root):
+    """AllReduce = Reduce + Broadcast (Lesson 3, core concepts): the root gets
+    the AllReduce's bits, every other rank keeps its input."""
+    x = _inputs(dtype, N, K, seed=N + K + root)
+    red = oracle_mod.reduce(x, root, op)
+    ar, _ = oracle_mod.ring_allreduce(x, op)
+    bc = oracle_mod.broadcast(red, root)
+    for r in range(N):
+        np.testing.assert_array_equal(_bits(red[r]), _bits(ar[r] if r == root else x[r]))
+        np.testing.assert_array_equal(_bits(bc[r]), _bits(ar[r]))
+
+
+@pytest.mark.parametrize("N,K", [(1, 4), (3, 15), (4, 13), (8, 1000), (5, 3)])
+def test_scatter_inverts_gather(oracle_mod, N, K):
+    """Scatter is the inverse of Gather (Lesson 3, core concepts); both are
+    the chunk partition read or written in rank order."""
+    g = np.random.Generator(np.random.PCG64(K))
+    full = g.integers(0, 1 << 16, size=K).astype(np.uint16)
+    parts = oracle_mod.scatter(full, N)
+    off, ln = oracle_mod.partition(K, N)
+    for r in range(N):
+        np.testing.assert_array_equal(parts[r], full[off[r]:off[r] + ln[r]])
+    np.testing.assert_array_equal(oracle_mod.gather(parts, K), full)
 
 
 def test_prod_exact_on_powers_of_two(oracle_mod):
