@@ -182,6 +182,9 @@ ROWS = {
     "broadcast": "Broadcast from rank 0, N=8 bf16 64Mi elements, in place",
     "alltoallv": "AllToAllv MoE dispatch, N=8, 4096 tokens x 7168 bf16/rank, Zipf(1.2) top-1 over 64 experts",
     "bucket": "bucket-fused AllReduce SUM, N=8 bf16, 4 Llama layers (809,533,440 elements/rank), 25 MiB buckets",
+    "reduce": "Reduce SUM to rank 0, N=8 bf16 64Mi elements/rank, out of place",
+    "gather": "Gather to rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
+    "scatter": "Scatter from rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
     "sweep": "AllReduce SUM bf16, 1 KiB..1 GiB per rank (x4), N in {2,4,8,16,64}; device time per call from "
              "CUDA-graph replay; points whose N*S fits in L2 are marked l2_resident (replays hit L2, not HBM)",
 }
@@ -306,6 +309,35 @@ def run_row(args, name, local):
             step = lambda: ccl.ccl_broadcast(arena.ranks, arena.ranks, root=0, stream=stream)
             alg, kernel = N * K * 2, "fanout_kernel<bf16> (1 source, N-1 destinations)"
             metric = "Broadcast HBM GB/s, N=8 bf16 128 MB, in place, 1 GB300"
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        print(json.dumps(line(metric, alg, per, launches, kernel, "bf16", {"nranks": N, "count": K},
+                              {"clocks": clk})))
+        return
+
+    if name in ("reduce", "gather", "scatter"):
+        N, K = 8, 64 * 1024 * 1024
+        if name == "reduce":
+            send = [randn_bf16(K) for _ in range(N)]
+            recv = [None] * N
+            recv[0] = torch.empty(K, dtype=torch.bfloat16, device=dev)
+            step = lambda: ccl.ccl_reduce(send, recv, root=0, op="sum", stream=stream)
+            alg, kernel = N * K * 2 + K * 2, "fused_reduce_kernel<bf16, SUM, 8 ranks> (root only)"
+            metric = "Reduce HBM GB/s, N=8 bf16 128 MB/rank to one root, 1 GB300"
+        else:
+            _, ln = ccl.ccl_plan_chunks(K, N)
+            parts = [randn_bf16(ln[r]) for r in range(N)]
+            full = [None] * N
+            full[0] = randn_bf16(K)
+            if name == "gather":
+                step = lambda: ccl.ccl_gather(parts, full, root=0, stream=stream)
+                kernel = "fanout_kernel<bf16> (N sources, 1 destination)"
+            else:
+                step = lambda: ccl.ccl_scatter(full, parts, root=0, stream=stream)
+                kernel = "copy_segments_kernel (N segments)"
+            alg = 2 * K * 2
+            metric = "%s HBM GB/s, N=8 bf16 128 MB total, 1 GB300" % name.capitalize()
         clocks.start()
         tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
         clk = clocks.stop()

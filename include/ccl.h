@@ -21,7 +21,9 @@
  * NaN (fp32 0x7FFFFFFF, bf16 0x7FFF).  AVG sums around the ring, then divides
  * the finished chunk once by N in fp32 before the gather, so every rank gets
  * identical bits.  MAX is NaN if either side is NaN, else the larger, and
- * +0 against -0 gives +0.
+ * +0 against -0 gives +0; MIN likewise takes the smaller, and -0 wins the tie
+ * (the pages list sum, min and max as the reductions: Collective
+ * Communication, table of the six core primitives).
  *
  * Common conventions
  *   - Pointer arrays (send[], recv[], ptrs[]) are HOST arrays of nranks DEVICE
@@ -63,7 +65,7 @@ extern "C" {
 #define CCL_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 typedef enum { CCL_FP32 = 0, CCL_BF16 = 1 } ccl_dtype_t;
-typedef enum { CCL_SUM = 0, CCL_AVG = 1, CCL_MAX = 2, CCL_PROD = 3 } ccl_op_t;
+typedef enum { CCL_SUM = 0, CCL_AVG = 1, CCL_MAX = 2, CCL_PROD = 3, CCL_MIN = 4 } ccl_op_t;
 typedef enum { CCL_MODE_FUSED = 0, CCL_MODE_STEP = 1 } ccl_mode_t;
 typedef enum {
     CCL_OK = 0,
@@ -141,6 +143,33 @@ ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nrank
 ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int ntensors, int nranks,
                                   size_t bucket_bytes, ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode,
                                   cudaStream_t stream);
+
+/* Reduce: only recv[root] receives the reduction, the other ranks' buffers
+ * are not touched (Collectives and sharded matmul, "Reduce and AllReduce";
+ * Lesson 3, core concepts: AllReduce equals a Reduce followed by a Broadcast).
+ * The root receives exactly the AllReduce's bits.  send[r]: `count` elements;
+ * recv[root]: `count` elements; recv[r] for r != root is ignored (may be
+ * NULL).  In place when send[root] == recv[root].  Step mode runs the ring's
+ * ReduceScatter phase through a cached workspace, then brings each finished
+ * chunk to the root. */
+ccl_status_t ccl_reduce(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                        ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream);
+
+/* Gather: recv[root] receives every rank's slice concatenated in rank order
+ * (Lesson 3, core concepts: "Gather"; Collectives and sharded matmul, "Gather
+ * and AllGather").  send[r] holds len_r elements (chunk r of `count`);
+ * recv[r] for r != root is ignored.  In place when
+ * send[root] == recv[root] + off_root elements. */
+ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                        ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
+
+/* Scatter: send[root]'s `count` elements are split into the N chunks and
+ * chunk r goes to recv[r] (len_r elements) (Lesson 3, core concepts: "Scatter",
+ * the inverse of Gather; Collectives and sharded matmul, "Scatter and
+ * ReduceScatter").  send[r] for r != root is ignored.  In place when
+ * recv[root] == send[root] + off_root elements. */
+ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                         ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
 
 /* Step-by-step ReduceScatter that allocates nothing.  The pages have no
  * counterpart: this exists for callers that cannot let a library call

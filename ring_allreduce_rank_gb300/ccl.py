@@ -17,9 +17,9 @@ import torch
 from .build import LIB as _LIB_PATH
 
 FP32, BF16 = 0, 1
-SUM, AVG, MAX, PROD = 0, 1, 2, 3
+SUM, AVG, MAX, PROD, MIN = 0, 1, 2, 3, 4
 FUSED, STEP = 0, 1
-OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD}
+OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN}
 MODES = {"fused": FUSED, "step": STEP}
 STATUS = {0: "CCL_OK", 1: "CCL_ERR_INVALID_ARG", 2: "CCL_ERR_UNSUPPORTED", 3: "CCL_ERR_OVERLAP",
           4: "CCL_ERR_CUDA", 5: "CCL_ERR_NO_MEMORY", 6: "CCL_ERR_TIMEOUT", 7: "CCL_ERR_CHECK_FAILED"}
@@ -52,6 +52,9 @@ def lib() -> ctypes.CDLL:
                 "ccl_reduce_scatter": [pp, pp, i32, sz, i32, i32, i32, vp],
                 "ccl_allgather": [pp, pp, i32, sz, i32, i32, vp],
                 "ccl_broadcast": [pp, pp, i32, i32, sz, i32, i32, vp],
+                "ccl_reduce": [pp, pp, i32, i32, sz, i32, i32, i32, vp],
+                "ccl_gather": [pp, pp, i32, i32, sz, i32, i32, vp],
+                "ccl_scatter": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_alltoall": [pp, pp, i32, sz, i32, i32, vp],
                 "ccl_alltoallv": [pp, pp, i32, psz, i32, i32, vp],
                 "ccl_bucket_allreduce": [pp, psz, i32, i32, sz, i32, i32, i32, vp],
@@ -150,6 +153,30 @@ def ccl_broadcast(send: Sequence[Optional[torch.Tensor]], recv: Sequence[torch.T
                   mode="fused", stream=None) -> None:
     _check(lib().ccl_broadcast(_ptrs(send), _ptrs(recv), len(recv), int(root), recv[0].numel(), _dtype(recv[0]),
                                _mode(mode), _stream(stream)), "ccl_broadcast")
+
+
+def ccl_reduce(send: Sequence[torch.Tensor], recv: Sequence[Optional[torch.Tensor]], root: int = 0, op="sum",
+               mode="fused", stream=None) -> None:
+    """Only recv[root] receives the reduction (the AllReduce's bits)."""
+    n = len(send)
+    _check(lib().ccl_reduce(_ptrs(send), _ptrs(recv), n, int(root), send[0].numel(), _dtype(send[0]), _op(op),
+                            _mode(mode), _stream(stream)), "ccl_reduce")
+
+
+def ccl_gather(send: Sequence[torch.Tensor], recv: Sequence[Optional[torch.Tensor]], root: int = 0, mode="fused",
+               stream=None) -> None:
+    """recv[root] receives every rank's slice (chunk r = send[r]) in rank order."""
+    out = recv[root]
+    _check(lib().ccl_gather(_ptrs(send), _ptrs(recv), len(send), int(root), out.numel(), _dtype(out), _mode(mode),
+                            _stream(stream)), "ccl_gather")
+
+
+def ccl_scatter(send: Sequence[Optional[torch.Tensor]], recv: Sequence[torch.Tensor], root: int = 0, mode="fused",
+                stream=None) -> None:
+    """send[root] is split into the N chunks; chunk r goes to recv[r]."""
+    src = send[root]
+    _check(lib().ccl_scatter(_ptrs(send), _ptrs(recv), len(recv), int(root), src.numel(), _dtype(src), _mode(mode),
+                             _stream(stream)), "ccl_scatter")
 
 
 def ccl_alltoall(send: Sequence[torch.Tensor], recv: Sequence[torch.Tensor], mode="fused", stream=None) -> None:

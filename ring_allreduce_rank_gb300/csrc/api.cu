@@ -19,7 +19,10 @@ namespace {
 
 size_t elem_size(ccl_dtype_t dt) { return dt == CCL_BF16 ? 2 : 4; }
 bool valid_dtype(ccl_dtype_t dt) { return dt == CCL_FP32 || dt == CCL_BF16; }
-bool valid_op(ccl_op_t op) { return op == CCL_SUM || op == CCL_AVG || op == CCL_MAX || op == CCL_PROD; }
+bool valid_op(ccl_op_t op)
+{
+    return op == CCL_SUM || op == CCL_AVG || op == CCL_MAX || op == CCL_PROD || op == CCL_MIN;
+}
 bool valid_mode(ccl_mode_t m) { return m == CCL_MODE_FUSED || m == CCL_MODE_STEP; }
 bool valid_ranks(int n) { return n >= 1 && n <= CCL_MAX_RANKS; }
 
@@ -290,7 +293,7 @@ ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nrank
     if (nranks == 1 && in_place && op != CCL_AVG)
         return CCL_OK;
     if (mode == CCL_MODE_FUSED)
-        return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, true, stream));
+        return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_ALL, 0, stream));
     if ((st = copy_ranks(send, recv, nranks, bytes, stream)) != CCL_OK)
         return st;
     return ring_steps_allreduce((int)dtype, (int)op, recv, nranks, count, stream);
@@ -323,7 +326,7 @@ ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int 
     if (st != CCL_OK)
         return st;
     if (mode == CCL_MODE_FUSED)
-        return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, false, stream));
+        return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_CHUNK, 0, stream));
     // step mode: the ring's ReduceScatter phase on a workspace copy of the inputs
     void *ws = nullptr;
     if ((st = get_workspace(count * es * (size_t)nranks, &ws)) != CCL_OK)
@@ -609,6 +612,133 @@ ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int n
         if ((st = from_cuda(launch_copy_segments(unpack.data(), unpack.size(), stream))) != CCL_OK)
             return st;
     }
+    return CCL_OK;
+}
+
+// ------------------------------------------------------------------ Reduce / Gather / Scatter
+
+ccl_status_t ccl_reduce(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                        ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !valid_mode(mode) || !send || !recv ||
+        root < 0 || root >= nranks)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es) || mul_overflows(count, (size_t)nranks))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const size_t bytes = count * es;
+    if (!recv[root])
+        return CCL_ERR_INVALID_ARG;
+    std::vector<Range> w{range_of(recv[root], bytes, root)}, r;
+    for (int i = 0; i < nranks; ++i) {
+        if (!send[i])
+            return CCL_ERR_INVALID_ARG;
+        r.push_back(range_of(send[i], bytes, i));
+    }
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return rd.rank == wr.rank && rd.lo == wr.lo;
+    });
+    if (st != CCL_OK)
+        return st;
+    if (mode == CCL_MODE_FUSED)
+        return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_ROOT, root,
+                                             stream));
+    // step mode: the ring's ReduceScatter phase on a workspace copy, then every
+    // finished chunk c is brought from rank c-1 to the root
+    void *ws = nullptr;
+    if ((st = get_workspace(bytes * (size_t)nranks, &ws)) != CCL_OK)
+        return st;
+    std::vector<void *> bufs(nranks);
+    for (int i = 0; i < nranks; ++i)
+        bufs[i] = static_cast<char *>(ws) + (size_t)i * bytes;
+    if ((st = copy_ranks(send, bufs.data(), nranks, bytes, stream)) != CCL_OK)
+        return st;
+    for (int s = 0; s < nranks - 1; ++s)
+        if (cudaError_t e = launch_ring_step((int)dtype, (int)op, STEP_RS, s, bufs.data(), nranks, count, stream))
+            return from_cuda(e);
+    if (op == CCL_AVG)
+        if (cudaError_t e = launch_ring_step((int)dtype, (int)op, STEP_SCALE, 0, bufs.data(), nranks, count, stream))
+            return from_cuda(e);
+    const Partition part = make_partition(count, nranks);
+    std::vector<CopySeg> segs;
+    for (int c = 0; c < nranks; ++c)
+        segs.push_back(CopySeg{static_cast<const char *>(bufs[ring_mod(c - 1, nranks)]) + part.off((uint32_t)c) * es,
+                               static_cast<char *>(recv[root]) + part.off((uint32_t)c) * es,
+                               part.len((uint32_t)c) * es, 0});
+    return from_cuda(launch_copy_segments(segs.data(), segs.size(), stream));
+}
+
+ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                        ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv || root < 0 ||
+        root >= nranks || !recv[root])
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const Partition part = make_partition(count, nranks);
+    std::vector<Range> w{range_of(recv[root], count * es, root)}, r;
+    for (int i = 0; i < nranks; ++i) {
+        if (!send[i] && part.len((uint32_t)i) > 0)
+            return CCL_ERR_INVALID_ARG;
+        r.push_back(range_of(send[i], part.len((uint32_t)i) * es, i));
+    }
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return rd.lo == wr.lo + part.off((uint32_t)rd.rank) * es;
+    });
+    if (st != CCL_OK)
+        return st;
+    if (mode == CCL_MODE_FUSED) {
+        void *dst[1] = {recv[root]};
+        return from_cuda(launch_fanout((int)dtype, send, nranks, dst, 1, count, stream));
+    }
+    // step mode: one rank's slice per launch, in rank order
+    for (int i = 0; i < nranks; ++i) {
+        CopySeg g{static_cast<const char *>(send[i]), static_cast<char *>(recv[root]) + part.off((uint32_t)i) * es,
+                  part.len((uint32_t)i) * es, 0};
+        if ((st = from_cuda(launch_copy_segments(&g, 1, stream))) != CCL_OK)
+            return st;
+    }
+    return CCL_OK;
+}
+
+ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                         ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv || root < 0 ||
+        root >= nranks || !send[root])
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const Partition part = make_partition(count, nranks);
+    std::vector<Range> w, r{range_of(send[root], count * es, root)};
+    for (int i = 0; i < nranks; ++i) {
+        if (!recv[i] && part.len((uint32_t)i) > 0)
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(recv[i], part.len((uint32_t)i) * es, i));
+    }
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return wr.lo == rd.lo + part.off((uint32_t)wr.rank) * es;
+    });
+    if (st != CCL_OK)
+        return st;
+    std::vector<CopySeg> segs;
+    for (int i = 0; i < nranks; ++i)
+        segs.push_back(CopySeg{static_cast<const char *>(send[root]) + part.off((uint32_t)i) * es,
+                               static_cast<char *>(recv[i]), part.len((uint32_t)i) * es, 0});
+    if (mode == CCL_MODE_FUSED)
+        return from_cuda(launch_copy_segments(segs.data(), segs.size(), stream));
+    for (const CopySeg &g : segs)  // step mode: one destination per launch
+        if ((st = from_cuda(launch_copy_segments(&g, 1, stream))) != CCL_OK)
+            return st;
     return CCL_OK;
 }
 

@@ -188,6 +188,7 @@ static cudaError_t launch_bucket_dt(int op, void *const *tp, int nt, int nr, con
     case OP_AVG: return launch_bucket_t<DT, OP_AVG>(tp, nt, nr, s, ns, st);
     case OP_MAX: return launch_bucket_t<DT, OP_MAX>(tp, nt, nr, s, ns, st);
     case OP_PROD: return launch_bucket_t<DT, OP_PROD>(tp, nt, nr, s, ns, st);
+    case OP_MIN: return launch_bucket_t<DT, OP_MIN>(tp, nt, nr, s, ns, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -10,7 +10,7 @@
 namespace ccl {
 
 enum { DT_FP32 = 0, DT_BF16 = 1 };
-enum { OP_SUM = 0, OP_AVG = 1, OP_MAX = 2, OP_PROD = 3 };
+enum { OP_SUM = 0, OP_AVG = 1, OP_MAX = 2, OP_PROD = 3, OP_MIN = 4 };
 
 constexpr int kThreads = 256;
 
@@ -69,6 +69,25 @@ __device__ __forceinline__ uint32_t max_f32_bits(uint32_t a, uint32_t b)
     return a & b;
 }
 
+// MIN on fp32 bit patterns: NaN if either is NaN, else the smaller; equal
+// values give the bitwise OR (identical bits, or -0 for +0 vs -0).
+__device__ __forceinline__ uint32_t min_f32_bits(uint32_t a, uint32_t b)
+{
+    const float fa = __uint_as_float(a), fb = __uint_as_float(b);
+    if (fa != fa || fb != fb)
+        return 0x7fffffffu;
+    if (fa < fb)
+        return a;
+    if (fb < fa)
+        return b;
+    return a | b;
+}
+
+template <int OP> __device__ __forceinline__ uint32_t minmax_f32_bits(uint32_t a, uint32_t b)
+{
+    return OP == OP_MAX ? max_f32_bits(a, b) : min_f32_bits(a, b);
+}
+
 template <int OP> __device__ __forceinline__ float op_f32(float local, float acc)
 {
     if (OP == OP_PROD)
@@ -79,8 +98,8 @@ template <int OP> __device__ __forceinline__ float op_f32(float local, float acc
 // One ring hop on one fp32 element: local (+) incoming.
 template <int OP> __device__ __forceinline__ uint32_t hop_f32(uint32_t local, uint32_t acc)
 {
-    if (OP == OP_MAX)
-        return max_f32_bits(local, acc);
+    if (OP == OP_MAX || OP == OP_MIN)
+        return minmax_f32_bits<OP>(local, acc);
     return __float_as_uint(op_f32<OP>(__uint_as_float(local), __uint_as_float(acc)));
 }
 
@@ -88,9 +107,10 @@ template <int OP> __device__ __forceinline__ uint32_t hop_f32(uint32_t local, ui
 // low half): widen (exact), fp32 operation, round each to bf16 (RNE).
 template <int OP> __device__ __forceinline__ uint32_t hop_bf16x2(uint32_t local, uint32_t acc)
 {
-    if (OP == OP_MAX) {
-        const uint32_t lo = max_f32_bits(local << 16, acc << 16) >> 16;
-        const uint32_t hi = max_f32_bits(local & 0xffff0000u, acc & 0xffff0000u) & 0xffff0000u;
+    if (OP == OP_MAX || OP == OP_MIN) {
+        // the result is one operand unchanged (or the canonical NaN): no rounding
+        const uint32_t lo = minmax_f32_bits<OP>(local << 16, acc << 16) >> 16;
+        const uint32_t hi = minmax_f32_bits<OP>(local & 0xffff0000u, acc & 0xffff0000u) & 0xffff0000u;
         return lo | hi;
     }
     const float r0 = op_f32<OP>(__uint_as_float(local << 16), __uint_as_float(acc << 16));

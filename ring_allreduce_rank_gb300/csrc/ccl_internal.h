@@ -19,15 +19,22 @@ template <int MAXR> struct FusedParams {
     void *recv[MAXR];
     Partition part;
     int nranks;
-    int write_all;   // 1: AllReduce (all ranks get the result); 0: ReduceScatter (recv[c], chunk-local)
+    int write_mode;  // WRITE_CHUNK, WRITE_ALL or WRITE_ROOT
+    int root;        // WRITE_ROOT: the one rank that receives the result
     int vec_aligned; // every pointer is 16-byte aligned
     uint32_t tiles;  // tiles per chunk (gridDim.x)
     float n_f;       // (float)nranks, the AVG divisor
 };
 
-// Launch the one-pass ring-order reduction: AllReduce (write_all) or ReduceScatter.
+enum WriteMode {
+    WRITE_CHUNK = 0, // ReduceScatter: chunk c goes to recv[c], chunk-local
+    WRITE_ALL = 1,   // AllReduce: every rank receives the whole result
+    WRITE_ROOT = 2   // Reduce: only recv[root] receives the whole result
+};
+
+// Launch the one-pass ring-order reduction (AllReduce, ReduceScatter or Reduce).
 cudaError_t launch_fused_reduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
-                                uint64_t count, bool write_all, cudaStream_t stream);
+                                uint64_t count, int write_mode, int root, cudaStream_t stream);
 
 // ------------------------------------------------------------------ step mode
 enum StepKind {

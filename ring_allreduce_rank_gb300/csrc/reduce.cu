@@ -19,7 +19,8 @@
 // of each chunk are done element by element by the chunk's first CTA.  When a
 // chunk's output cannot be vector-aligned (unaligned pointers, or a
 // ReduceScatter chunk whose offset is not a multiple of the vector) the CTA
-// walks its tile element by element instead.
+// walks its tile element by element instead.  The same kernel serves Reduce:
+// the root receives the AllReduce's result and no other rank is written.
 #include "ccl_internal.h"
 
 namespace ccl {
@@ -40,9 +41,11 @@ __device__ __forceinline__ void reduce_elem(const FusedParams<MAXR> &p, int N, u
     }
     if (OP == OP_AVG)
         acc = avg_elem<DT>(acc, p.n_f);
-    if (p.write_all) {
+    if (p.write_mode == WRITE_ALL) {
         for (int q = 0; q < N; ++q)
             st_elem<DT>(p.recv[q], e, acc);
+    } else if (p.write_mode == WRITE_ROOT) {
+        st_elem<DT>(p.recv[p.root], e, acc);
     } else {
         st_elem<DT>(p.recv[c], e - out_base, acc);
     }
@@ -59,8 +62,8 @@ __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_con
     const uint32_t c = blockIdx.y;
     const uint32_t t = blockIdx.x;
     const uint64_t off = p.part.off(c), len = p.part.len(c), end = off + len;
-    const uint64_t out_base = p.write_all ? 0 : off;
-    const bool vec_ok = p.vec_aligned && (p.write_all || (off % VEC) == 0);
+    const uint64_t out_base = p.write_mode == WRITE_CHUNK ? off : 0;
+    const bool vec_ok = p.vec_aligned && (p.write_mode != WRITE_CHUNK || (off % VEC) == 0);
 
     if (!vec_ok) {
         // element path over tile t of the chunk
@@ -116,10 +119,12 @@ __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_con
                     acc = hop_vec<DT, OP>(x[u][k], acc);
                 if (OP == OP_AVG)
                     acc = avg_vec<DT>(acc, p.n_f);
-                if (p.write_all) {
+                if (p.write_mode == WRITE_ALL) {
 #pragma unroll
                     for (int q = 0; q < NR; ++q)
                         st16(static_cast<char *>(p.recv[q]) + v * 16, acc);
+                } else if (p.write_mode == WRITE_ROOT) {
+                    st16(static_cast<char *>(p.recv[p.root]) + v * 16, acc);
                 } else {
                     st16(static_cast<char *>(p.recv[c]) + (v * VEC - out_base) * ES, acc);
                 }
@@ -159,9 +164,11 @@ __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_con
         }
         if (OP == OP_AVG)
             acc = avg_vec<DT>(acc, p.n_f);
-        if (p.write_all) {
+        if (p.write_mode == WRITE_ALL) {
             for (int q = 0; q < N; ++q)
                 st16(static_cast<char *>(p.recv[q]) + v * 16, acc);
+        } else if (p.write_mode == WRITE_ROOT) {
+            st16(static_cast<char *>(p.recv[p.root]) + v * 16, acc);
         } else {
             st16(static_cast<char *>(p.recv[c]) + (v * VEC - out_base) * ES, acc);
         }
@@ -171,8 +178,8 @@ __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_con
 // ------------------------------------------------------------------ launch
 
 template <int DT, int OP, int NR, int MAXR>
-static cudaError_t launch_t(const void *const *send, void *const *recv, int nranks, uint64_t count, bool write_all,
-                            cudaStream_t stream)
+static cudaError_t launch_t(const void *const *send, void *const *recv, int nranks, uint64_t count, int write_mode,
+                            int root, cudaStream_t stream)
 {
     constexpr int VEC = DType<DT>::kVec;
     constexpr int U = NR > 0 ? Unroll<NR>::kU : 1;
@@ -180,8 +187,9 @@ static cudaError_t launch_t(const void *const *send, void *const *recv, int nran
     bool aligned = true;
     for (int r = 0; r < nranks; ++r) {
         p.send[r] = send[r];
-        p.recv[r] = recv[r];
-        aligned = aligned && ((uintptr_t)send[r] % 16 == 0) && ((uintptr_t)recv[r] % 16 == 0);
+        // Reduce writes only the root's buffer: the others may be NULL
+        p.recv[r] = (write_mode == WRITE_ROOT && r != root) ? nullptr : recv[r];
+        aligned = aligned && ((uintptr_t)send[r] % 16 == 0) && ((uintptr_t)p.recv[r] % 16 == 0);
     }
     for (int r = nranks; r < MAXR; ++r) {
         p.send[r] = nullptr;
@@ -190,7 +198,8 @@ static cudaError_t launch_t(const void *const *send, void *const *recv, int nran
     p.part.q = count / (uint64_t)nranks;
     p.part.rem = (uint32_t)(count % (uint64_t)nranks);
     p.nranks = nranks;
-    p.write_all = write_all ? 1 : 0;
+    p.write_mode = write_mode;
+    p.root = root;
     p.vec_aligned = aligned ? 1 : 0;
     p.n_f = (float)nranks;
     const uint64_t te = (uint64_t)kThreads * U * VEC;
@@ -205,40 +214,41 @@ static cudaError_t launch_t(const void *const *send, void *const *recv, int nran
 }
 
 template <int DT, int OP>
-static cudaError_t launch_op(const void *const *send, void *const *recv, int nranks, uint64_t count, bool write_all,
-                             cudaStream_t stream)
+static cudaError_t launch_op(const void *const *send, void *const *recv, int nranks, uint64_t count, int write_mode,
+                             int root, cudaStream_t stream)
 {
     switch (nranks) {
-    case 2: return launch_t<DT, OP, 2, kSmallRanks>(send, recv, nranks, count, write_all, stream);
-    case 4: return launch_t<DT, OP, 4, kSmallRanks>(send, recv, nranks, count, write_all, stream);
-    case 8: return launch_t<DT, OP, 8, kSmallRanks>(send, recv, nranks, count, write_all, stream);
-    case 16: return launch_t<DT, OP, 16, kSmallRanks>(send, recv, nranks, count, write_all, stream);
+    case 2: return launch_t<DT, OP, 2, kSmallRanks>(send, recv, nranks, count, write_mode, root, stream);
+    case 4: return launch_t<DT, OP, 4, kSmallRanks>(send, recv, nranks, count, write_mode, root, stream);
+    case 8: return launch_t<DT, OP, 8, kSmallRanks>(send, recv, nranks, count, write_mode, root, stream);
+    case 16: return launch_t<DT, OP, 16, kSmallRanks>(send, recv, nranks, count, write_mode, root, stream);
     default:
         if (nranks <= kSmallRanks)
-            return launch_t<DT, OP, 0, kSmallRanks>(send, recv, nranks, count, write_all, stream);
-        return launch_t<DT, OP, 0, kMaxRanks>(send, recv, nranks, count, write_all, stream);
+            return launch_t<DT, OP, 0, kSmallRanks>(send, recv, nranks, count, write_mode, root, stream);
+        return launch_t<DT, OP, 0, kMaxRanks>(send, recv, nranks, count, write_mode, root, stream);
     }
 }
 
 template <int DT>
 static cudaError_t launch_dt(int op, const void *const *send, void *const *recv, int nranks, uint64_t count,
-                             bool write_all, cudaStream_t stream)
+                             int write_mode, int root, cudaStream_t stream)
 {
     switch (op) {
-    case OP_SUM: return launch_op<DT, OP_SUM>(send, recv, nranks, count, write_all, stream);
-    case OP_AVG: return launch_op<DT, OP_AVG>(send, recv, nranks, count, write_all, stream);
-    case OP_MAX: return launch_op<DT, OP_MAX>(send, recv, nranks, count, write_all, stream);
-    case OP_PROD: return launch_op<DT, OP_PROD>(send, recv, nranks, count, write_all, stream);
+    case OP_SUM: return launch_op<DT, OP_SUM>(send, recv, nranks, count, write_mode, root, stream);
+    case OP_AVG: return launch_op<DT, OP_AVG>(send, recv, nranks, count, write_mode, root, stream);
+    case OP_MAX: return launch_op<DT, OP_MAX>(send, recv, nranks, count, write_mode, root, stream);
+    case OP_PROD: return launch_op<DT, OP_PROD>(send, recv, nranks, count, write_mode, root, stream);
+    case OP_MIN: return launch_op<DT, OP_MIN>(send, recv, nranks, count, write_mode, root, stream);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fused_reduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
-                                uint64_t count, bool write_all, cudaStream_t stream)
+                                uint64_t count, int write_mode, int root, cudaStream_t stream)
 {
     if (dt == DT_FP32)
-        return launch_dt<DT_FP32>(op, send, recv, nranks, count, write_all, stream);
-    return launch_dt<DT_BF16>(op, send, recv, nranks, count, write_all, stream);
+        return launch_dt<DT_FP32>(op, send, recv, nranks, count, write_mode, root, stream);
+    return launch_dt<DT_BF16>(op, send, recv, nranks, count, write_mode, root, stream);
 }
 
 } // namespace ccl

@@ -132,6 +132,7 @@ static cudaError_t launch_step_dt(int op, int kind, int s, void *const *bufs, in
     case OP_AVG: return launch_step_op<DT, OP_AVG>(kind, s, bufs, nranks, count, stream);
     case OP_MAX: return launch_step_op<DT, OP_MAX>(kind, s, bufs, nranks, count, stream);
     case OP_PROD: return launch_step_op<DT, OP_PROD>(kind, s, bufs, nranks, count, stream);
+    case OP_MIN: return launch_step_op<DT, OP_MIN>(kind, s, bufs, nranks, count, stream);
     }
     return cudaErrorInvalidValue;
 }

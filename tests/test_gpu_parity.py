@@ -84,10 +84,20 @@ def test_worked_examples_on_gpu(case, mode):
         out = [torch.zeros_like(s) for s in send]
         ccl.ccl_alltoall(send, out, mode=mode)
         got = [bits(t) for t in out]
+    elif kind == "reduce":
+        send = [to_dev(r) for r in ins]
+        ccl.ccl_reduce(send, send, root=case["root"], op=case["op"], mode=mode)
+        got = [bits(t) for t in send]
+    elif kind == "gather":
+        send = [to_dev(r) for r in ins]
+        out = [None] * N
+        out[case["root"]] = torch.zeros(exp[0].size, dtype=torch.float32, device=DEV)
+        ccl.ccl_gather(send, out, root=case["root"], mode=mode)
+        got = [bits(out[case["root"]])]
     else:
         raise AssertionError(kind)
     torch.cuda.synchronize()
-    for r in range(N):
+    for r in range(len(exp)):
         assert_bits_equal(got[r], exp[r], "%s rank %d" % (case["name"], r))
 
 
@@ -112,7 +122,7 @@ AR_SHAPES = [(1, 5), (2, 1), (2, 4099), (3, 5), (3, 2), (4, 4096), (5, 3), (7, 1
 
 @pytest.mark.parametrize("mode", ["fused", "step"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min"])
 @pytest.mark.parametrize("N,K", AR_SHAPES, ids=lambda v: str(v))
 def test_allreduce_matches_oracle(N, K, op, dtype, mode):
     x = inputs(dtype, N, K, seed=17 * N + K)
@@ -226,6 +236,53 @@ def test_allgather_matches_oracle(N, K, dtype, mode):
     want = oracle.allgather(chunks, K)
     for r in range(N):
         assert_bits_equal(bits(out[r]), want[r], "AG rank %d" % r)
+
+
+# ------------------------------------------------------------------ Reduce / Gather / Scatter
+
+@pytest.mark.parametrize("mode", ["fused", "step"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min"])
+@pytest.mark.parametrize("N,K,root", [(1, 9, 0), (3, 5, 0), (4, 4099, 3), (8, 70003, 5), (16, 777, 15),
+                                      (33, 4099, 7)])
+def test_reduce_matches_oracle(N, K, root, op, dtype, mode):
+    """The root receives the AllReduce's bits; no other buffer is written."""
+    x = inputs(dtype, N, K, seed=root * 7 + K)
+    want = oracle.reduce(x, root, op)
+    send = [to_dev(r) for r in x]
+    recv = [None] * N
+    recv[root] = empty_like_host(K, torch_dtype(x), pad_elems=root % 2)
+    ccl.ccl_reduce(send, recv, root=root, op=op, mode=mode)
+    inplace = [to_dev(r) for r in x]
+    ccl.ccl_reduce(inplace, inplace, root=root, op=op, mode=mode)
+    torch.cuda.synchronize()
+    assert_bits_equal(bits(recv[root]), want[root], "reduce root")
+    for r in range(N):
+        assert_bits_equal(bits(send[r]), x[r], "reduce input %d untouched" % r)
+        assert_bits_equal(bits(inplace[r]), want[r], "reduce in place rank %d" % r)
+
+
+@pytest.mark.parametrize("mode", ["fused", "step"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("N,K,root", [(1, 5, 0), (3, 15, 0), (4, 4099, 2), (8, 65536 + 3, 7), (16, 777, 4)])
+def test_gather_and_scatter_match_oracle(N, K, root, dtype, mode):
+    off, ln = ccl.ccl_plan_chunks(K, N)
+    full = inputs(dtype, 1, K, seed=K + root)[0]
+    parts = oracle.scatter(full, N)
+    # Scatter from root
+    send = [None] * N
+    send[root] = to_dev(full)
+    recv = [empty_like_host(ln[r], torch_dtype([full]), pad_elems=r % 3) for r in range(N)]
+    ccl.ccl_scatter(send, recv, root=root, mode=mode)
+    # Gather back to root
+    out = [None] * N
+    out[root] = empty_like_host(K, torch_dtype([full]))
+    ccl.ccl_gather(recv, out, root=root, mode=mode)
+    torch.cuda.synchronize()
+    for r in range(N):
+        assert_bits_equal(bits(recv[r]), parts[r], "scatter rank %d" % r)
+    assert_bits_equal(bits(out[root]), oracle.gather(parts, K), "gather")
+    assert_bits_equal(bits(out[root]), full, "gather(scatter(x)) = x")
 
 
 # ------------------------------------------------------------------ Broadcast
