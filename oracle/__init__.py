@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_reduce_scatter.argtypes = [pp, pp, i32, u64, i32, i32]
             L.oracle_allgather.argtypes = [pp, pp, i32, u64, i32]
             L.oracle_reduce.argtypes = [pp, pp, i32, i32, u64, i32, i32]
+            L.oracle_allreduce_hd.argtypes = [pp, i32, u64, i32, i32]
+            L.oracle_allreduce_tree.argtypes = [pp, i32, u64, i32, i32]
+            L.oracle_allreduce_hier.argtypes = [pp, i32, i32, u64, i32, i32]
+            L.oracle_allreduce_order_at.argtypes = [pp, i32, u64, i32, i32, i32, i32, p64, u64, vp]
             L.oracle_gather.argtypes = [pp, vp, i32, u64, i32]
             L.oracle_scatter.argtypes = [vp, pp, i32, u64, i32]
             L.oracle_broadcast.argtypes = [pp, pp, i32, i32, u64, i32]
@@ -76,7 +80,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_sum_f64.argtypes = [pp, i32, u64, i32, i32, vp, vp]
             for name in ("oracle_ring_allreduce", "oracle_ring_allreduce_closed", "oracle_ring_allreduce_at",
                          "oracle_ring_allreduce_gathered", "oracle_reduce_scatter", "oracle_reduce", "oracle_gather",
-                         "oracle_scatter", "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
+                         "oracle_scatter", "oracle_allreduce_hd", "oracle_allreduce_tree", "oracle_allreduce_hier",
+                         "oracle_allreduce_order_at", "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
                          "oracle_bucket_allreduce", "oracle_sum_f64"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -189,6 +194,40 @@ def reduce_scatter(bufs, op="sum"):
     _check(lib().oracle_reduce_scatter(_ptrs(ins), _ptrs(outs), N, K, _dtype_code(ins[0]), _op(op)),
            "oracle_reduce_scatter")
     return outs
+
+
+ALGOS = {"ring": 0, "halving_doubling": 1, "tree": 2, "hierarchical": 3}
+
+
+def allreduce_algo(bufs, algo: str, op="sum", group: int = 0):
+    """Step-by-step AllReduce under another schedule: halving_doubling, tree or
+    hierarchical (group = ranks per group)."""
+    outs = [np.array(b, copy=True, order="C") for b in bufs]
+    N, K = len(outs), outs[0].size
+    dt = _dtype_code(outs[0])
+    if algo == "ring":
+        return ring_allreduce(outs, op)[0]
+    if algo == "halving_doubling":
+        rc = lib().oracle_allreduce_hd(_ptrs(outs), N, K, dt, _op(op))
+    elif algo == "tree":
+        rc = lib().oracle_allreduce_tree(_ptrs(outs), N, K, dt, _op(op))
+    elif algo == "hierarchical":
+        rc = lib().oracle_allreduce_hier(_ptrs(outs), N, group, K, dt, _op(op))
+    else:
+        raise ValueError(algo)
+    _check(rc, "oracle_allreduce_" + algo)
+    return outs
+
+
+def allreduce_algo_at(bufs, algo: str, idx, op="sum", group: int = 0) -> np.ndarray:
+    """Closed form of another schedule's result at the listed indices."""
+    ins = [np.ascontiguousarray(b) for b in bufs]
+    idx = np.ascontiguousarray(idx, dtype=np.uint64)
+    out = np.empty(idx.size, dtype=ins[0].dtype)
+    _check(lib().oracle_allreduce_order_at(_ptrs(ins), len(ins), ins[0].size, _dtype_code(ins[0]), _op(op),
+                                           ALGOS[algo], group, idx.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                                           idx.size, out.ctypes.data), "oracle_allreduce_order_at")
+    return out
 
 
 def reduce(bufs, root: int, op="sum"):

@@ -652,6 +652,266 @@ done:
     return rc;
 }
 
+/* ------------------------------------------------------------------ */
+/* other schedules: the same reduction, other summation orders          */
+/* ------------------------------------------------------------------ */
+
+static void scale_range(void *buf, uint64_t lo, uint64_t hi, int N, int dtype)
+{
+    for (uint64_t e = lo; e < hi; ++e)
+        store(buf, dtype, e, avg_scale(load(buf, dtype, e), N, dtype));
+}
+
+/* Recursive halving-doubling AllReduce, step by step, in place
+ * (Collective Communication, "Recursive halving-doubling (butterfly)": in
+ * round k rank i pairs with i XOR 2^k, each keeps half of its current range
+ * and adds the partner's copy of that half; the AllGather phase reverses the
+ * rounds.  Distributed LLM collectives, "Recursive Halving-Doubling": for p not
+ * a power of two, r = p - 2^floor(log2 p) and the first 2r ranks are reduced
+ * pairwise into r ranks first, and get the result back at the end.)
+ * Readings fixed here: the pre-fold pairs ranks (2v, 2v+1) and rank 2v+1
+ * keeps the sum; virtual rank v is real rank 2v+1 for v < r, v+r otherwise;
+ * the rank whose bit k is 0 keeps the lower half [lo, lo + ceil((hi-lo)/2)). */
+int oracle_allreduce_hd(void **buf, int N, uint64_t K, int dtype, int op)
+{
+    if (bad_args(N, dtype, op))
+        return OR_EINVAL;
+    int sop = op == OR_AVG ? OR_SUM : op;
+    int pw = 1;
+    while (pw * 2 <= N)
+        pw *= 2;
+    int r = N - pw, m = 0;
+    while ((1 << m) < pw)
+        ++m;
+    uint64_t *lo = malloc(sizeof(uint64_t) * (size_t)pw), *hi = malloc(sizeof(uint64_t) * (size_t)pw);
+    void **vb = malloc(sizeof(void *) * (size_t)pw);
+    if (!lo || !hi || !vb) {
+        free(lo); free(hi); free(vb);
+        return OR_ENOMEM;
+    }
+    /* pre-fold: rank 2v+1 adds rank 2v's buffer */
+    for (int v = 0; v < r; ++v)
+        for (uint64_t e = 0; e < K; ++e)
+            store(buf[2 * v + 1], dtype, e, hop(load(buf[2 * v + 1], dtype, e), load(buf[2 * v], dtype, e), dtype, sop));
+    for (int v = 0; v < pw; ++v) {
+        vb[v] = buf[v < r ? 2 * v + 1 : v + r];
+        lo[v] = 0;
+        hi[v] = K;
+    }
+    /* halving: round k pairs v with v ^ 2^k; both halves are disjoint, so
+     * each rank reads its partner's kept-by-me half before anyone writes it */
+    for (int k = 0; k < m; ++k) {
+        for (int v = 0; v < pw; ++v) {
+            uint64_t mid = lo[v] + (hi[v] - lo[v] + 1) / 2;
+            int upper = (v >> k) & 1;
+            uint64_t a = upper ? mid : lo[v], b = upper ? hi[v] : mid;
+            void *partner = vb[v ^ (1 << k)];
+            for (uint64_t e = a; e < b; ++e)
+                store(vb[v], dtype, e, hop(load(vb[v], dtype, e), load(partner, dtype, e), dtype, sop));
+            lo[v] = a;
+            hi[v] = b;
+        }
+    }
+    if (op == OR_AVG)
+        for (int v = 0; v < pw; ++v)
+            scale_range(vb[v], lo[v], hi[v], N, dtype);
+    /* doubling: reverse rounds, each copies its partner's block */
+    size_t es = esize(dtype);
+    uint64_t *nlo = malloc(sizeof(uint64_t) * (size_t)pw * 2), *nhi;
+    if (!nlo) {
+        free(lo); free(hi); free(vb);
+        return OR_ENOMEM;
+    }
+    nhi = nlo + pw;
+    for (int k = m - 1; k >= 0; --k) {
+        for (int v = 0; v < pw; ++v) {
+            int w = v ^ (1 << k);
+            memcpy((char *)vb[v] + lo[w] * es, (char *)vb[w] + lo[w] * es, (hi[w] - lo[w]) * es);
+            nlo[v] = lo[v] < lo[w] ? lo[v] : lo[w];
+            nhi[v] = hi[v] > hi[w] ? hi[v] : hi[w];
+        }
+        for (int v = 0; v < pw; ++v) {
+            lo[v] = nlo[v];
+            hi[v] = nhi[v];
+        }
+    }
+    /* post: rank 2v gets the result back from rank 2v+1 */
+    for (int v = 0; v < r; ++v)
+        memcpy(buf[2 * v], buf[2 * v + 1], K * es);
+    free(lo); free(hi); free(vb); free(nlo);
+    return OR_OK;
+}
+
+/* Binomial-tree AllReduce, step by step, in place (Collective Communication,
+ * "Tree AllReduce": leaves send to their parent, which adds what it receives
+ * and passes it up, log2 N steps to the root, then the root's result is
+ * broadcast back down).  Reading: at level k, rank i (a multiple of 2^(k+1))
+ * receives from rank i + 2^k when that rank exists; the root is rank 0. */
+int oracle_allreduce_tree(void **buf, int N, uint64_t K, int dtype, int op)
+{
+    if (bad_args(N, dtype, op))
+        return OR_EINVAL;
+    int sop = op == OR_AVG ? OR_SUM : op;
+    size_t es = esize(dtype);
+    int top = 0;
+    while ((1 << top) < N)
+        ++top;
+    for (int k = 0; k < top; ++k)
+        for (int i = 0; i + (1 << k) < N; i += 1 << (k + 1))
+            for (uint64_t e = 0; e < K; ++e)
+                store(buf[i], dtype, e, hop(load(buf[i], dtype, e), load(buf[i + (1 << k)], dtype, e), dtype, sop));
+    if (op == OR_AVG)
+        scale_range(buf[0], 0, K, N, dtype);
+    for (int k = top - 1; k >= 0; --k)
+        for (int i = 0; i + (1 << k) < N; i += 1 << (k + 1))
+            memcpy(buf[i + (1 << k)], buf[i], K * es);
+    return OR_OK;
+}
+
+/* Two-level hierarchical AllReduce, step by step, in place (AllReduce survey,
+ * "multi-dimensional hierarchical AllReduce", two-level table: ReduceScatter
+ * inside each group of L ranks, AllReduce among the G = N/L group
+ * representatives on the M/L shard, AllGather inside each group).  Groups are
+ * consecutive ranks [gL, gL+L); every level is the ring of this file.  The
+ * representative of intra chunk c in group g is the rank that finished it,
+ * local rank (c-1) mod L; the inter ring partitions chunk c into G
+ * sub-chunks.  AVG divides once by N, at the inter ring's holders. */
+int oracle_allreduce_hier(void **buf, int N, int L, uint64_t K, int dtype, int op)
+{
+    if (bad_args(N, dtype, op) || L < 1 || N % L != 0)
+        return OR_EINVAL;
+    int G = N / L;
+    int sop = op == OR_AVG ? OR_SUM : op;
+    size_t es = esize(dtype);
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)(L > G ? L : G) * 2);
+    uint64_t *len = off + (L > G ? L : G);
+    uint64_t *soff = malloc(sizeof(uint64_t) * (size_t)G * 2), *slen;
+    uint64_t stride = K + 1;
+    void *snap = malloc((size_t)(L > G ? L : G) * stride * es);
+    void **grp = malloc(sizeof(void *) * (size_t)(L > G ? L : G));
+    if (!off || !soff || !snap || !grp) {
+        free(off); free(soff); free(snap); free(grp);
+        return OR_ENOMEM;
+    }
+    slen = soff + G;
+    oracle_partition(K, L, off, len);
+    /* 1. ReduceScatter inside every group */
+    for (int g = 0; g < G; ++g) {
+        for (int j = 0; j < L; ++j)
+            grp[j] = buf[g * L + j];
+        rs_phase(grp, L, off, len, dtype, sop, NULL, snap, stride);
+    }
+    /* 2. ring AllReduce of each chunk among the groups' representatives */
+    uint64_t coff[1024], clen[1024];
+    if (L > 1024) {
+        free(off); free(soff); free(snap); free(grp);
+        return OR_EINVAL;
+    }
+    for (int c = 0; c < L; ++c) {
+        coff[c] = off[c];
+        clen[c] = len[c];
+    }
+    for (int c = 0; c < L; ++c) {
+        int rep = mod((int64_t)c - 1, L);
+        for (int g = 0; g < G; ++g)
+            grp[g] = (char *)buf[g * L + rep] + coff[c] * es;
+        oracle_partition(clen[c], G, soff, slen);
+        rs_phase(grp, G, soff, slen, dtype, sop, NULL, snap, stride);
+        if (op == OR_AVG)
+            for (int g = 0; g < G; ++g) {
+                int d = mod((int64_t)g + 1, G);
+                scale_range(grp[g], soff[d], soff[d] + slen[d], N, dtype);
+            }
+        ag_phase_after_rs(grp, G, soff, slen, dtype, NULL, snap, stride);
+    }
+    /* 3. AllGather inside every group */
+    for (int g = 0; g < G; ++g) {
+        for (int j = 0; j < L; ++j)
+            grp[j] = buf[g * L + j];
+        ag_phase_after_rs(grp, L, off, len, dtype, NULL, snap, stride);
+    }
+    free(off); free(soff); free(snap); free(grp);
+    return OR_OK;
+}
+
+/* Closed forms of the three orders for one element (the second formulation):
+ * x[r] is rank r's element (stored bits), e its index, K the buffer length.
+ *   algo 1 halving-doubling: a balanced binary tree over the virtual leaves
+ *          (x_{2v} (+) x_{2v+1} for v < r, then x_{v+r}), adjacent leaves first;
+ *   algo 2 binomial tree: leaves in rank order, a subtree of 2^k ranks rooted
+ *          at i combines with the one rooted at i + 2^k, the root's own
+ *          subtrees folding from the smallest up;
+ *   algo 3 hierarchical (group size L): a ring fold over groups, starting at
+ *          group d, of ring folds inside each group starting at local rank c,
+ *          where c is e's intra chunk and d its sub-chunk within chunk c. */
+static uint32_t tree_fold(const uint32_t *x, int lo, int n, int dtype, int op)
+{
+    /* subtree of n ranks starting at lo in a binomial tree: the node lo
+     * absorbs subtrees of size 1, 2, 4, ... rooted at lo+1, lo+2, lo+4 ... */
+    uint32_t acc = x[lo];
+    for (int s = 1; s < n; s *= 2) {
+        int cnt = (n - s) < s ? (n - s) : s;
+        acc = hop(acc, tree_fold(x, lo + s, cnt, dtype, op), dtype, op);
+    }
+    return acc;
+}
+
+static uint32_t balanced(const uint32_t *leaf, int lo, int n, int dtype, int op)
+{
+    if (n == 1)
+        return leaf[lo];
+    int h = n / 2;
+    return hop(balanced(leaf, lo, h, dtype, op), balanced(leaf, lo + h, n - h, dtype, op), dtype, op);
+}
+
+int oracle_allreduce_order_at(const void **in, int N, uint64_t K, int dtype, int op, int algo, int L,
+                              const uint64_t *idx, uint64_t n, void *out)
+{
+    if (bad_args(N, dtype, op) || algo < 1 || algo > 3 || N > 1024 || (algo == 3 && (L < 1 || N % L)))
+        return OR_EINVAL;
+    int sop = op == OR_AVG ? OR_SUM : op;
+    uint32_t x[1024], leaf[1024];
+    for (uint64_t t = 0; t < n; ++t) {
+        uint64_t e = idx[t];
+        if (e >= K)
+            return OR_EINVAL;
+        for (int r = 0; r < N; ++r)
+            x[r] = load(in[r], dtype, e);
+        uint32_t acc;
+        if (algo == 1) {
+            int pw = 1;
+            while (pw * 2 <= N)
+                pw *= 2;
+            int r = N - pw;
+            for (int v = 0; v < pw; ++v)
+                leaf[v] = v < r ? hop(x[2 * v + 1], x[2 * v], dtype, sop) : x[v + r];
+            acc = balanced(leaf, 0, pw, dtype, sop);
+        } else if (algo == 2) {
+            acc = tree_fold(x, 0, N, dtype, sop);
+        } else {
+            int G = N / L;
+            uint64_t q = K / (uint64_t)L, rem = K % (uint64_t)L;
+            int c = e < rem * (q + 1) ? (int)(e / (q + 1)) : (int)(rem + (e - rem * (q + 1)) / q);
+            uint64_t oc = (uint64_t)c * q + ((uint64_t)c < rem ? (uint64_t)c : rem);
+            uint64_t lc = q + ((uint64_t)c < rem ? 1 : 0);
+            uint64_t ec = e - oc, q2 = lc / (uint64_t)G, rem2 = lc % (uint64_t)G;
+            int d = ec < rem2 * (q2 + 1) ? (int)(ec / (q2 + 1)) : (int)(rem2 + (ec - rem2 * (q2 + 1)) / q2);
+            acc = 0;
+            for (int k = 0; k < G; ++k) {
+                int g = (d + k) % G;
+                uint32_t p = x[g * L + c];
+                for (int j = 1; j < L; ++j)
+                    p = hop(x[g * L + (c + j) % L], p, dtype, sop);
+                acc = k == 0 ? p : hop(p, acc, dtype, sop);
+            }
+        }
+        if (op == OR_AVG)
+            acc = avg_scale(acc, N, dtype);
+        store(out, dtype, t, acc);
+    }
+    return OR_OK;
+}
+
 /* Plain fp64 reference of the reduction (the definition y = sum_r x_r with no
  * ring and no intermediate rounding), plus sum_r |x_r|, the scale against which
  * relative error is measured.  SUM/AVG only. */
