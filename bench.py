@@ -182,6 +182,9 @@ ROWS = {
     "broadcast": "Broadcast from rank 0, N=8 bf16 64Mi elements, in place",
     "alltoallv": "AllToAllv MoE dispatch, N=8, 4096 tokens x 7168 bf16/rank, Zipf(1.2) top-1 over 64 experts",
     "bucket": "bucket-fused AllReduce SUM, N=8 bf16, 4 Llama layers (809,533,440 elements/rank), 25 MiB buckets",
+    "allreduce-hd": "AllReduce AVG in halving-doubling order, N=8 bf16 64Mi/rank, in place, one pass",
+    "allreduce-tree": "AllReduce AVG in binomial-tree order, N=8 bf16 64Mi/rank, in place, one pass",
+    "allreduce-hier": "AllReduce AVG in two-level hierarchical order (2 groups of 4), N=8 bf16 64Mi/rank, in place",
     "reduce": "Reduce SUM to rank 0, N=8 bf16 64Mi elements/rank, out of place",
     "gather": "Gather to rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
     "scatter": "Scatter from rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
@@ -294,6 +297,22 @@ def run_row(args, name, local):
                  big["bytes_per_rank"], [big["us"] / 1e3], 1, "fused_reduce_kernel<bf16, SUM, N>", "bf16",
                  {"op": "sum", "mode": "fused"}, {"points": points})
         print(json.dumps(d))
+        return
+
+    if name in ("allreduce-hd", "allreduce-tree", "allreduce-hier"):
+        N, K = 8, 64 * 1024 * 1024
+        arena = RankArena(N, K, torch.bfloat16, device=dev)
+        for r in range(N):
+            arena.ranks[r].copy_(randn_bf16(K))
+        algo = {"allreduce-hd": "halving_doubling", "allreduce-tree": "tree", "allreduce-hier": "hierarchical"}[name]
+        step = lambda: ccl.ccl_allreduce_algo(arena.ranks, op="avg", algo=algo, group_size=4, stream=stream)
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        kernel = "hier_order_kernel<bf16, AVG, L=4>" if algo == "hierarchical" else "tree_order_kernel<bf16, AVG, 8>"
+        print(json.dumps(line("AllReduce (%s order) HBM GB/s, N=8 bf16 128 MB/rank, 1 GB300" % algo, 2 * N * K * 2,
+                              per, launches, kernel, "bf16", {"nranks": N, "count": K, "algo": algo},
+                              {"clocks": clk})))
         return
 
     if name in ("allreduce-step", "broadcast"):

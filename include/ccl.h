@@ -68,6 +68,12 @@ typedef enum { CCL_FP32 = 0, CCL_BF16 = 1 } ccl_dtype_t;
 typedef enum { CCL_SUM = 0, CCL_AVG = 1, CCL_MAX = 2, CCL_PROD = 3, CCL_MIN = 4 } ccl_op_t;
 typedef enum { CCL_MODE_FUSED = 0, CCL_MODE_STEP = 1 } ccl_mode_t;
 typedef enum {
+    CCL_ALGO_RING = 0,
+    CCL_ALGO_HALVING_DOUBLING = 1,
+    CCL_ALGO_TREE = 2,
+    CCL_ALGO_HIERARCHICAL = 3
+} ccl_algo_t;
+typedef enum {
     CCL_OK = 0,
     CCL_ERR_INVALID_ARG = 1,
     CCL_ERR_UNSUPPORTED = 2,
@@ -170,6 +176,28 @@ ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, 
  * recv[root] == send[root] + off_root elements. */
 ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                          ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
+
+/* AllReduce under another schedule's summation order, in one pass (fused).
+ * Each schedule adds the contributions in its own order, so each gives its own
+ * rounded bits; this call reproduces them exactly.
+ *   CCL_ALGO_RING: the ring of ccl_allreduce (identical result).
+ *   CCL_ALGO_HALVING_DOUBLING: round k pairs rank i with i XOR 2^k, k = 0, 1,
+ *     ... (Collective Communication, "Recursive halving-doubling (butterfly)");
+ *     for N not a power of two the first 2r ranks, r = N - 2^floor(log2 N), are
+ *     first added pairwise (2v, 2v+1) (Distributed LLM collectives, "Recursive
+ *     Halving-Doubling").  Per element: a balanced tree, adjacent leaves first.
+ *   CCL_ALGO_TREE: binomial tree to rank 0, level k adding rank i + 2^k into
+ *     rank i, then broadcast (Collective Communication, "Tree AllReduce").
+ *   CCL_ALGO_HIERARCHICAL: ring ReduceScatter inside groups of group_size
+ *     consecutive ranks, ring AllReduce among the groups' representatives,
+ *     ring AllGather inside the groups (AllReduce survey, two-level table);
+ *     group_size must divide nranks (1 or nranks gives the flat ring).
+ * AVG divides the finished sum once by N.  Buffers as ccl_allreduce (in place
+ * when send[r] == recv[r]).  group_size is ignored except for
+ * CCL_ALGO_HIERARCHICAL. */
+ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, ccl_algo_t algo, int group_size,
+                                cudaStream_t stream);
 
 /* Step-by-step ReduceScatter that allocates nothing.  The pages have no
  * counterpart: this exists for callers that cannot let a library call

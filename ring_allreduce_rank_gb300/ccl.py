@@ -21,6 +21,7 @@ SUM, AVG, MAX, PROD, MIN = 0, 1, 2, 3, 4
 FUSED, STEP = 0, 1
 OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN}
 MODES = {"fused": FUSED, "step": STEP}
+ALGOS = {"ring": 0, "halving_doubling": 1, "tree": 2, "hierarchical": 3}
 STATUS = {0: "CCL_OK", 1: "CCL_ERR_INVALID_ARG", 2: "CCL_ERR_UNSUPPORTED", 3: "CCL_ERR_OVERLAP",
           4: "CCL_ERR_CUDA", 5: "CCL_ERR_NO_MEMORY", 6: "CCL_ERR_TIMEOUT", 7: "CCL_ERR_CHECK_FAILED"}
 MAX_RANKS = 1024
@@ -53,6 +54,7 @@ def lib() -> ctypes.CDLL:
                 "ccl_allgather": [pp, pp, i32, sz, i32, i32, vp],
                 "ccl_broadcast": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_reduce": [pp, pp, i32, i32, sz, i32, i32, i32, vp],
+                "ccl_allreduce_algo": [pp, pp, i32, sz, i32, i32, i32, i32, vp],
                 "ccl_gather": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_scatter": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_alltoall": [pp, pp, i32, sz, i32, i32, vp],
@@ -134,6 +136,15 @@ def ccl_allreduce(send: Sequence[torch.Tensor], recv: Optional[Sequence[torch.Te
     n = len(send)
     _check(lib().ccl_allreduce(_ptrs(send), _ptrs(recv), n, send[0].numel(), _dtype(send[0]), _op(op), _mode(mode),
                                _stream(stream)), "ccl_allreduce")
+
+
+def ccl_allreduce_algo(send: Sequence[torch.Tensor], recv: Optional[Sequence[torch.Tensor]] = None, op="sum",
+                       algo="halving_doubling", group_size: int = 0, stream=None) -> None:
+    """AllReduce under another schedule's summation order (one pass)."""
+    recv = send if recv is None else recv
+    a = ALGOS[algo] if isinstance(algo, str) else int(algo)
+    _check(lib().ccl_allreduce_algo(_ptrs(send), _ptrs(recv), len(send), send[0].numel(), _dtype(send[0]), _op(op),
+                                    a, int(group_size), _stream(stream)), "ccl_allreduce_algo")
 
 
 def ccl_reduce_scatter(send: Sequence[torch.Tensor], recv: Sequence[torch.Tensor], op="sum", mode="fused",

@@ -742,4 +742,39 @@ ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks,
     return CCL_OK;
 }
 
+// ------------------------------------------------------------------ other schedules' orders
+
+ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, ccl_algo_t algo, int group_size,
+                                cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !send || !recv || algo < CCL_ALGO_RING ||
+        algo > CCL_ALGO_HIERARCHICAL)
+        return CCL_ERR_INVALID_ARG;
+    if (algo == CCL_ALGO_HIERARCHICAL && (group_size < 1 || nranks % group_size != 0))
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const size_t bytes = count * es;
+    std::vector<Range> w, r;
+    for (int i = 0; i < nranks; ++i) {
+        if (!send[i] || !recv[i])
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(recv[i], bytes, i));
+        r.push_back(range_of(send[i], bytes, i));
+    }
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return rd.rank == wr.rank && rd.lo == wr.lo;
+    });
+    if (st != CCL_OK)
+        return st;
+    if (algo == CCL_ALGO_RING)
+        return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_ALL, 0, stream));
+    return from_cuda(launch_order_allreduce((int)dtype, (int)op, (int)algo, group_size, send, recv, nranks, count,
+                                           stream));
+}
+
 } // extern "C"

@@ -88,6 +88,14 @@ struct RedSeg {
 cudaError_t launch_bucket_reduce(int dt, int op, void *const *tensor_ptrs /* [t*nranks + r] */, int ntensors,
                                  int nranks, const RedSeg *segs, size_t nseg, cudaStream_t stream);
 
+// ------------------------------------------------------------------ other schedules' orders
+enum Algo { ALGO_RING = 0, ALGO_HD = 1, ALGO_TREE = 2, ALGO_HIER = 3 };
+
+// One-pass AllReduce under halving-doubling, binomial-tree or two-level
+// hierarchical (group = ranks per group) summation order.
+cudaError_t launch_order_allreduce(int dt, int op, int algo, int group, const void *const *send, void *const *recv,
+                                   int nranks, uint64_t count, cudaStream_t stream);
+
 // ------------------------------------------------------------------ bookkeeping
 void count_launches(unsigned long long n);
 
