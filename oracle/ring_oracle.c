@@ -912,6 +912,112 @@ int oracle_allreduce_order_at(const void **in, int N, uint64_t K, int dtype, int
     return OR_OK;
 }
 
+/* ------------------------------------------------------------------ */
+/* compressed AllReduce with error feedback                            */
+/* ------------------------------------------------------------------ */
+
+#define OR_COMP_INT8_BLOCK 0
+#define OR_COMP_THRESHOLD 1
+
+static uint32_t canon(uint32_t r) { return f32_bits_is_nan(r) ? 0x7fffffffu : r; }
+static float fcanon(float x) { return bits_to_f32(canon(f32_to_bits(x))); }
+
+/* Round an fp32 value to the nearest integer, ties to even (the IEEE
+ * roundToIntegralTiesToEven operation), written from its definition. */
+static float round_half_even(float x)
+{
+    if (x != x || x - x != 0.0f) /* NaN or infinity */
+        return fcanon(x);
+    double d = (double)x, f = (double)(int64_t)d; /* |x| < 2^63 here: q is at most ~127 */
+    if (d < 0 && f != d)
+        f -= 1.0; /* floor */
+    double frac = d - f;
+    double r = frac > 0.5 ? f + 1.0 : frac < 0.5 ? f : (((int64_t)f & 1) ? f + 1.0 : f);
+    if (r == 0.0)
+        return d < 0 ? -0.0f : 0.0f;
+    return (float)r;
+}
+
+/* Compress one rank's error-corrected gradient u = g + e (fp32), in place:
+ * u is replaced by the transmitted value v and e by the new residual
+ * e' = u - v (Collective Communication, "Error feedback and residual
+ * accumulation", Definition 1.4: e_{t+1} = g_t + e_t - v_t).
+ *   INT8 block ("Blockwise quantization for gradient communication"): per block
+ *     of `block` consecutive elements, s = max|u| / 127, q = round(u / s) (ties
+ *     to even; q = 0 when s = 0), v = q * s; a NaN anywhere in the block makes
+ *     s NaN.
+ *   THRESHOLD (the greedy 1-bit compressor of Tables 3 and 4): v = 1 when
+ *     u >= threshold, else 0. */
+static void compress(float *u, float *e, uint64_t K, int comp, int block, float threshold)
+{
+    if (comp == OR_COMP_THRESHOLD) {
+        for (uint64_t i = 0; i < K; ++i) {
+            float v = u[i] >= threshold ? 1.0f : 0.0f;
+            e[i] = fcanon(u[i] - v);
+            u[i] = v;
+        }
+        return;
+    }
+    for (uint64_t b0 = 0; b0 < K; b0 += (uint64_t)block) {
+        uint64_t b1 = b0 + (uint64_t)block < K ? b0 + (uint64_t)block : K;
+        float amax = 0.0f;
+        int nan = 0;
+        for (uint64_t i = b0; i < b1; ++i) {
+            float a = u[i] < 0 ? -u[i] : u[i];
+            if (u[i] != u[i])
+                nan = 1;
+            else if (a > amax)
+                amax = a;
+        }
+        float sc = nan ? bits_to_f32(0x7fffffffu) : fcanon(amax / 127.0f);
+        for (uint64_t i = b0; i < b1; ++i) {
+            float q = sc > 0.0f ? round_half_even(fcanon(u[i] / sc)) : (sc == 0.0f ? 0.0f : sc);
+            float v = fcanon(q * sc);
+            e[i] = fcanon(u[i] - v);
+            u[i] = v;
+        }
+    }
+}
+
+/* Compressed AllReduce, in place: grads[r] (K elements of dtype) and the
+ * residuals res[r] (K fp32, start at zero).  Every rank compresses u = g + e,
+ * keeps its residual, and the transmitted values are AllReduced with the ring
+ * of this file in fp32 (SUM, or AVG dividing once by N); the result is rounded
+ * once to the buffer type and written to every rank's grads. */
+int oracle_allreduce_compressed(void **grads, float **res, int N, uint64_t K, int dtype, int op, int comp,
+                                int block, float threshold)
+{
+    if (bad_args(N, dtype, op) || (op != OR_SUM && op != OR_AVG) || (comp != OR_COMP_INT8_BLOCK &&
+        comp != OR_COMP_THRESHOLD) || (comp == OR_COMP_INT8_BLOCK && block < 1))
+        return OR_EINVAL;
+    void **v = calloc((size_t)N, sizeof(void *));
+    int rc = OR_OK;
+    if (!v)
+        return OR_ENOMEM;
+    for (int r = 0; r < N; ++r) {
+        float *u = malloc(K * sizeof(float) + 4);
+        if (!u) {
+            rc = OR_ENOMEM;
+            goto done;
+        }
+        for (uint64_t i = 0; i < K; ++i)
+            u[i] = fcanon(bits_to_f32(widen_bits(load(grads[r], dtype, i), dtype)) + res[r][i]);
+        compress(u, res[r], K, comp, block, threshold);
+        v[r] = u;
+    }
+    rc = oracle_ring_allreduce(v, N, K, OR_FP32, op, NULL);
+    if (rc != OR_OK)
+        goto done;
+    for (int r = 0; r < N; ++r)
+        for (uint64_t i = 0; i < K; ++i)
+            store(grads[r], dtype, i, narrow_bits(((uint32_t *)v[r])[i], dtype));
+done:
+    for (int r = 0; r < N; ++r)
+        free(v[r]);
+    free(v);
+    return rc;
+}
+
 /* Plain fp64 reference of the reduction (the definition y = sum_r x_r with no
  * ring and no intermediate rounding), plus sum_r |x_r|, the scale against which
  * relative error is measured.  SUM/AVG only. */
