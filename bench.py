@@ -185,6 +185,7 @@ ROWS = {
     "allreduce-hd": "AllReduce AVG in halving-doubling order, N=8 bf16 64Mi/rank, in place, one pass",
     "allreduce-tree": "AllReduce AVG in binomial-tree order, N=8 bf16 64Mi/rank, in place, one pass",
     "allreduce-hier": "AllReduce AVG in two-level hierarchical order (2 groups of 4), N=8 bf16 64Mi/rank, in place",
+    "allreduce-int8": "compressed AllReduce AVG with error feedback, blockwise INT8 (b=128), N=8 bf16 64Mi/rank",
     "reduce": "Reduce SUM to rank 0, N=8 bf16 64Mi elements/rank, out of place",
     "gather": "Gather to rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
     "scatter": "Scatter from rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
@@ -313,6 +314,21 @@ def run_row(args, name, local):
         print(json.dumps(line("AllReduce (%s order) HBM GB/s, N=8 bf16 128 MB/rank, 1 GB300" % algo, 2 * N * K * 2,
                               per, launches, kernel, "bf16", {"nranks": N, "count": K, "algo": algo},
                               {"clocks": clk})))
+        return
+
+    if name == "allreduce-int8":
+        N, K = 8, args.count  # 64Mi per rank unless --count picks a profiling size
+        grads = [randn_bf16(K) for _ in range(N)]
+        res = [torch.zeros(K, dtype=torch.float32, device=dev) for _ in range(N)]
+        step = lambda: ccl.ccl_allreduce_compressed(grads, res, op="avg", comp="int8_block", block=128,
+                                                    stream=stream)
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        alg = N * K * (2 + 4 + 4 + 2)  # gradients read and written, residuals read and written
+        print(json.dumps(line("Compressed AllReduce (INT8 blocks + error feedback) HBM GB/s, N=8 bf16 128 MB/rank, "
+                              "1 GB300", alg, per, launches, "compressed_allreduce_kernel<bf16, 4, 8>", "bf16",
+                              {"nranks": N, "count": K, "block": 128}, {"clocks": clk})))
         return
 
     if name in ("allreduce-step", "broadcast"):

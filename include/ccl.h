@@ -73,6 +73,7 @@ typedef enum {
     CCL_ALGO_TREE = 2,
     CCL_ALGO_HIERARCHICAL = 3
 } ccl_algo_t;
+typedef enum { CCL_COMP_INT8_BLOCK = 0, CCL_COMP_THRESHOLD = 1 } ccl_compressor_t;
 typedef enum {
     CCL_OK = 0,
     CCL_ERR_INVALID_ARG = 1,
@@ -199,6 +200,24 @@ ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int 
                                 ccl_dtype_t dtype, ccl_op_t op, ccl_algo_t algo, int group_size,
                                 cudaStream_t stream);
 
+/* Compressed AllReduce with error feedback (Collective Communication,
+ * "Gradient compression": blockwise INT8 quantization, and "Error feedback and
+ * residual accumulation", Definition 1.4).  grads[r]: `count` elements of
+ * dtype, in place; residuals[r]: `count` fp32 per rank, zero before the first
+ * step, carried by the caller from step to step.  Each rank compresses
+ * u = g + e and keeps e' = u - v:
+ *   CCL_COMP_INT8_BLOCK (block = 64 or 128): s = max|u| / 127 over each
+ *     block, q = round(u / s) (ties to even), v = q * s;
+ *   CCL_COMP_THRESHOLD (the greedy 1-bit compressor of the pages' Tables 3
+ *     and 4): v = 1 when u >= threshold, else 0.
+ * The transmitted v are AllReduced in ring order in fp32 (op CCL_SUM, or
+ * CCL_AVG dividing once by N) and rounded once to dtype, written to every
+ * grads[r].  Up to 16 ranks; grads and residuals must not overlap.  One
+ * launch. */
+ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residuals, int nranks, size_t count,
+                                      ccl_dtype_t dtype, ccl_op_t op, ccl_compressor_t comp, int block,
+                                      float threshold, cudaStream_t stream);
+
 /* Step-by-step ReduceScatter that allocates nothing.  The pages have no
  * counterpart: this exists for callers that cannot let a library call
  * cudaMalloc -- a process whose framework has already reserved the GPU's
@@ -246,6 +265,12 @@ ccl_status_t ccl_plan_buckets(const size_t *numels, int ntensors, size_t bucket_
 /* AllToAllv displacements: sdispl[i*N+j] = elements before block j in
  * send[i]; rdispl[j*N+i] = elements before block i in recv[j]. */
 ccl_status_t ccl_plan_alltoallv(int nranks, const size_t *counts, size_t *sdispl, size_t *rdispl);
+
+/* Bytes one rank would put on a link for `count` elements under a
+ * compressor: INT8 block: count + 4 * ceil(count / block) (codes plus fp32
+ * scales, 4b/(b+4) times fewer than fp32: 3.88 at b = 128); THRESHOLD:
+ * ceil(count / 8). */
+ccl_status_t ccl_plan_compressed_bytes(size_t count, ccl_compressor_t comp, int block, size_t *bytes);
 
 /* Arena layout: per-rank stride (bytes_per_rank rounded up to `align`, a power
  * of two >= 256) and total bytes for nranks rank buffers in one allocation. */

@@ -227,7 +227,7 @@ def allreduce_algo_at(bufs, algo: str, idx, op="sum", group: int = 0) -> np.ndar
     out = np.empty(idx.size, dtype=ins[0].dtype)
     _check(lib().oracle_allreduce_order_at(_ptrs(ins), len(ins), ins[0].size, _dtype_code(ins[0]), _op(op),
                                            ALGOS[algo], group, idx.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
-                                           idx.size, out.ctypes.data), "oracle_allreduce_order_at", "oracle_allreduce_compressed")
+                                           idx.size, out.ctypes.data), "oracle_allreduce_order_at")
     return out
 
 

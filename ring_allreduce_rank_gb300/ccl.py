@@ -22,6 +22,7 @@ FUSED, STEP = 0, 1
 OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN}
 MODES = {"fused": FUSED, "step": STEP}
 ALGOS = {"ring": 0, "halving_doubling": 1, "tree": 2, "hierarchical": 3}
+COMPRESSORS = {"int8_block": 0, "threshold": 1}
 STATUS = {0: "CCL_OK", 1: "CCL_ERR_INVALID_ARG", 2: "CCL_ERR_UNSUPPORTED", 3: "CCL_ERR_OVERLAP",
           4: "CCL_ERR_CUDA", 5: "CCL_ERR_NO_MEMORY", 6: "CCL_ERR_TIMEOUT", 7: "CCL_ERR_CHECK_FAILED"}
 MAX_RANKS = 1024
@@ -55,6 +56,8 @@ def lib() -> ctypes.CDLL:
                 "ccl_broadcast": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_reduce": [pp, pp, i32, i32, sz, i32, i32, i32, vp],
                 "ccl_allreduce_algo": [pp, pp, i32, sz, i32, i32, i32, i32, vp],
+                "ccl_allreduce_compressed": [pp, pp, i32, sz, i32, i32, i32, i32, ctypes.c_float, vp],
+                "ccl_plan_compressed_bytes": [sz, i32, i32, psz],
                 "ccl_gather": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_scatter": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_alltoall": [pp, pp, i32, sz, i32, i32, vp],
@@ -145,6 +148,26 @@ def ccl_allreduce_algo(send: Sequence[torch.Tensor], recv: Optional[Sequence[tor
     a = ALGOS[algo] if isinstance(algo, str) else int(algo)
     _check(lib().ccl_allreduce_algo(_ptrs(send), _ptrs(recv), len(send), send[0].numel(), _dtype(send[0]), _op(op),
                                     a, int(group_size), _stream(stream)), "ccl_allreduce_algo")
+
+
+def ccl_allreduce_compressed(grads: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor], op="sum",
+                             comp="int8_block", block: int = 128, threshold: float = 0.5, stream=None) -> None:
+    """One compressed AllReduce step with error feedback, in place on grads
+    and residuals (fp32, one per rank)."""
+    for e in residuals:
+        if e.dtype != torch.float32:
+            raise TypeError("residuals are float32")
+    c = COMPRESSORS[comp] if isinstance(comp, str) else int(comp)
+    _check(lib().ccl_allreduce_compressed(_ptrs(grads), _ptrs(residuals), len(grads), grads[0].numel(),
+                                          _dtype(grads[0]), _op(op), c, int(block), ctypes.c_float(threshold),
+                                          _stream(stream)), "ccl_allreduce_compressed")
+
+
+def ccl_plan_compressed_bytes(count: int, comp="int8_block", block: int = 128) -> int:
+    out = ctypes.c_size_t()
+    c = COMPRESSORS[comp] if isinstance(comp, str) else int(comp)
+    _check(lib().ccl_plan_compressed_bytes(count, c, block, ctypes.byref(out)), "ccl_plan_compressed_bytes")
+    return out.value
 
 
 def ccl_reduce_scatter(send: Sequence[torch.Tensor], recv: Sequence[torch.Tensor], op="sum", mode="fused",

@@ -777,4 +777,45 @@ ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int 
                                            stream));
 }
 
+// ------------------------------------------------------------------ compressed AllReduce
+
+ccl_status_t ccl_plan_compressed_bytes(size_t count, ccl_compressor_t comp, int block, size_t *bytes)
+{
+    if (!bytes || (comp != CCL_COMP_INT8_BLOCK && comp != CCL_COMP_THRESHOLD) ||
+        (comp == CCL_COMP_INT8_BLOCK && block < 1))
+        return CCL_ERR_INVALID_ARG;
+    if (comp == CCL_COMP_THRESHOLD)
+        *bytes = (count + 7) / 8; // one bit per element
+    else
+        *bytes = count + 4 * ((count + (size_t)block - 1) / (size_t)block); // int8 codes + fp32 scales
+    return CCL_OK;
+}
+
+ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residuals, int nranks, size_t count,
+                                      ccl_dtype_t dtype, ccl_op_t op, ccl_compressor_t comp, int block,
+                                      float threshold, cudaStream_t stream)
+{
+    if (nranks < 1 || nranks > 16 || !valid_dtype(dtype) || (op != CCL_SUM && op != CCL_AVG) || !grads ||
+        !residuals || (comp != CCL_COMP_INT8_BLOCK && comp != CCL_COMP_THRESHOLD) ||
+        (comp == CCL_COMP_INT8_BLOCK && block != 64 && block != 128))
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, 4))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    std::vector<Range> w;
+    for (int i = 0; i < nranks; ++i) {
+        if (!grads[i] || !residuals[i])
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(grads[i], count * es, i));
+        w.push_back(range_of(residuals[i], count * 4, i));
+    }
+    ccl_status_t st = check_overlaps(w, {}, [](const Range &, const Range &) { return false; });
+    if (st != CCL_OK)
+        return st;
+    return from_cuda(launch_compressed_allreduce((int)dtype, op == CCL_AVG, (int)comp, block, threshold, grads,
+                                                 residuals, nranks, count, stream));
+}
+
 } // extern "C"

@@ -96,6 +96,15 @@ enum Algo { ALGO_RING = 0, ALGO_HD = 1, ALGO_TREE = 2, ALGO_HIER = 3 };
 cudaError_t launch_order_allreduce(int dt, int op, int algo, int group, const void *const *send, void *const *recv,
                                    int nranks, uint64_t count, cudaStream_t stream);
 
+// ------------------------------------------------------------------ compressed AllReduce
+enum Compressor { COMP_INT8_BLOCK = 0, COMP_THRESHOLD = 1 };
+
+// Error-feedback compression of every rank's gradient, ring-order fp32
+// AllReduce of the transmitted values, one round to the gradients' type.
+cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, float threshold,
+                                        void *const *grads, float *const *res, int nranks, uint64_t count,
+                                        cudaStream_t stream);
+
 // ------------------------------------------------------------------ bookkeeping
 void count_launches(unsigned long long n);
 

@@ -77,6 +77,17 @@ def test_zipf_counts_shape():
     assert counts[:, 0].sum() == counts.sum(axis=0).max()
 
 
+def test_planner_compressed_bytes(L):
+    """Blockwise INT8: codes plus one fp32 scale per block, 4b/(b+4) = 3.88
+    times fewer bytes than fp32 at b = 128 (Collective Communication,
+    blockwise quantization)."""
+    d = 128 * 4096
+    assert ccl.ccl_plan_compressed_bytes(d, "int8_block", 128) == d + 4 * 4096
+    assert round(4 * d / ccl.ccl_plan_compressed_bytes(d, "int8_block", 128), 2) == 3.88
+    assert ccl.ccl_plan_compressed_bytes(1001, "int8_block", 64) == 1001 + 4 * 16
+    assert ccl.ccl_plan_compressed_bytes(1001, "threshold", 0) == 126
+
+
 def test_arena_layout(L):
     assert ccl.ccl_arena_layout(8, 134217728) == (134217728, 8 * 134217728)
     assert ccl.ccl_arena_layout(3, 1000, 256) == (1024, 3072)
