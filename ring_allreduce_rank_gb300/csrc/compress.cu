@@ -14,7 +14,9 @@
 // to the gradients' type and written to every rank.
 //
 // Layout: one warp per compression block (the same block index in every
-// rank); lane l owns elements [l*EPL, (l+1)*EPL) of it.  The warp first issues
+// rank); lane l owns elements [l*EPL, (l+1)*EPL) of it.  Up to 8 ranks with
+// aligned buffers take the pipelined form below (shared-memory double
+// buffering with cp.async); the rest take the direct form.  The warp first issues
 // every rank's g and e loads, then walks the ranks: forms u, reduces the block
 // maximum with shuffles, quantises, writes the new residual, and keeps v in
 // registers.  Then each
@@ -38,6 +40,8 @@ struct CompParams {
     float inv_n; // 1/N, exact when N is a power of two
     int pow2;    // N is a power of two
     int vec_ok;  // grads and residuals aligned for the lane's vector width
+    uint64_t first_block; // the direct kernel starts at this compression block
+    uint64_t nfull;       // the pipelined kernel covers blocks [0, nfull)
 };
 
 template <int DT, int EPL>
@@ -130,34 +134,13 @@ __device__ __forceinline__ uint32_t round_to(float x)
     return *reinterpret_cast<uint32_t *>(&p) & 0xffffu;
 }
 
+// Everything after the loads: u = g + e, compression, residual store, the
+// ring-order fp32 fold and the result store.  v holds g and ee holds e on entry.
 template <int DT, int EPL, int NMAX>
-__global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allreduce_kernel(const __grid_constant__ CompParams p)
+__device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_t i0, int valid, bool vec,
+                                                    float (&v)[NMAX][EPL], float (&ee)[NMAX][EPL])
 {
-    constexpr int B = 32 * EPL; // compression block
-    const int lane = threadIdx.x & 31;
-    const uint64_t blk = ((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const uint64_t b0 = blk * B;
-    if (b0 >= p.K)
-        return; // whole warp leaves together
-    const uint64_t i0 = b0 + (uint64_t)lane * EPL;
-    const int valid = i0 >= p.K ? 0 : (int)umin64(EPL, p.K - i0);
-    const bool vec = p.vec_ok != 0;
     const int N = p.nranks;
-
-    // every rank's gradient and residual loads are issued before any compute,
-    // so a lane has N * EPL * (element + 4) bytes in flight
-    float v[NMAX][EPL], ee[NMAX][EPL];
-#pragma unroll
-    for (int r = 0; r < NMAX; ++r) {
-        if (r < N) {
-            load_g<DT, EPL>(p.grads[r], i0, valid, vec, v[r]);
-            load_f<EPL>(p.res[r], i0, valid, vec, ee[r]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < EPL; ++j)
-                v[r][j] = ee[r][j] = 0.0f; // absent ranks: never stored
-        }
-    }
     // u = g + e (kept in v until it is replaced by the transmitted value)
 #pragma unroll
     for (int r = 0; r < NMAX; ++r)
@@ -175,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allred
                 ee[r][j] = __fsub_rn(u, v[r][j]);
             }
     } else {
-        // block maxima of all ranks, the shuffle chains interleaved
+        // per-rank block maxima (NaN flagged separately)
         float amax[NMAX];
         uint32_t nanmask = 0;
 #pragma unroll
@@ -192,23 +175,59 @@ __global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allred
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int r = 0; r < NMAX; ++r)
-                amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], o));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
             nanmask |= __shfl_xor_sync(0xffffffffu, nanmask, o);
+        float sc[NMAX], inv[NMAX];
+        const int lane = threadIdx.x & 31;
+        if constexpr (NMAX == 8) {
+            // transposing butterfly: after the exchanges at distance 16, 8 and 4
+            // lane l holds rank (l >> 2) & 7's maximum over 8 lanes, and two
+            // more rounds finish it; each lane then computes that one rank's
+            // scale and reciprocal, and the eight values are broadcast
+            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+            float k4[4], k2[2];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float send = b4 ? amax[k] : amax[k + 4];
+                k4[k] = fmaxf(b4 ? amax[k + 4] : amax[k], __shfl_xor_sync(0xffffffffu, send, 16));
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float send = b3 ? k4[k] : k4[k + 2];
+                k2[k] = fmaxf(b3 ? k4[k + 2] : k4[k], __shfl_xor_sync(0xffffffffu, send, 8));
+            }
+            float m = fmaxf(b2 ? k2[1] : k2[0], __shfl_xor_sync(0xffffffffu, b2 ? k2[0] : k2[1], 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const int mine = (lane >> 2) & 7;
+            const float s1 = (nanmask >> mine) & 1u ? __uint_as_float(0x7fffffffu) : __fdiv_rn(m, 127.0f);
+            const float i1 = __frcp_rn(s1);
+#pragma unroll
+            for (int r = 0; r < NMAX; ++r) {
+                sc[r] = __shfl_sync(0xffffffffu, s1, r << 2);
+                inv[r] = __shfl_sync(0xffffffffu, i1, r << 2);
+            }
+        } else {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int r = 0; r < NMAX; ++r)
+                    amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], o));
+#pragma unroll
+            for (int r = 0; r < NMAX; ++r) {
+                sc[r] = (nanmask >> r) & 1u ? __uint_as_float(0x7fffffffu) : __fdiv_rn(amax[r], 127.0f);
+                inv[r] = __frcp_rn(sc[r]);
+            }
+        }
 #pragma unroll
         for (int r = 0; r < NMAX; ++r) {
-            const float s = (nanmask >> r) & 1u ? __uint_as_float(0x7fffffffu) : __fdiv_rn(amax[r], 127.0f);
-            const float inv = __frcp_rn(s);
-            const bool fast = s > 0.0f && inv < __uint_as_float(0x7f800000u); // warp-uniform
+            const float s = sc[r];
+            const bool fast = s > 0.0f && inv[r] < __uint_as_float(0x7f800000u); // warp-uniform
 #pragma unroll
             for (int j = 0; j < EPL; ++j) {
                 const float u = v[r][j];
                 float q;
                 if (fast)
-                    q = quantize_fast(u, s, inv);
+                    q = quantize_fast(u, s, inv[r]);
                 else
                     q = s > 0.0f ? rintf(__fdiv_rn(u, s)) : (s == 0.0f ? 0.0f : s);
                 v[r][j] = __fmul_rn(q, s);
@@ -294,16 +313,203 @@ __global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allred
 }
 
 template <int DT, int EPL, int NMAX>
+__global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allreduce_kernel(const __grid_constant__ CompParams p)
+{
+    constexpr int B = 32 * EPL; // compression block
+    const int lane = threadIdx.x & 31;
+    const uint64_t blk = p.first_block + (((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5);
+    const uint64_t b0 = blk * B;
+    if (b0 >= p.K)
+        return; // whole warp leaves together
+    const uint64_t i0 = b0 + (uint64_t)lane * EPL;
+    const int valid = i0 >= p.K ? 0 : (int)umin64(EPL, p.K - i0);
+    const bool vec = p.vec_ok != 0;
+    const int N = p.nranks;
+
+    // every rank's gradient and residual loads are issued before any compute,
+    // so a lane has N * EPL * (element + 4) bytes in flight
+    float v[NMAX][EPL], ee[NMAX][EPL];
+#pragma unroll
+    for (int r = 0; r < NMAX; ++r) {
+        if (r < N) {
+            load_g<DT, EPL>(p.grads[r], i0, valid, vec, v[r]);
+            load_f<EPL>(p.res[r], i0, valid, vec, ee[r]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < EPL; ++j)
+                v[r][j] = ee[r][j] = 0.0f; // absent ranks: never stored
+        }
+    }
+    compress_fold_store<DT, EPL, NMAX>(p, i0, valid, vec, v, ee);
+}
+
+// ------------------------------------------------------------------ pipelined form (N <= 8)
+//
+// Persistent CTAs walk tiles of 8 compression blocks (one per warp).  While a
+// warp computes tile i from shared memory, cp.async is already copying tile
+// i+1's gradients and residuals into the other stage, so memory latency hides
+// behind the compute.  Each lane copies exactly the words it later reads, so
+// its own cp.async.wait_group is the only synchronisation needed.  Only whole,
+// aligned blocks come here; the tail block goes to the kernel above.
+
+__device__ __forceinline__ void cp_async(void *smem, const void *gmem, int bytes)
+{
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    if (bytes == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+    else if (bytes == 8)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(sa), "l"(gmem) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+template <int DT, int EPL> struct PipeLayout {
+    static constexpr int kWarps = kThreads / 32;
+    static constexpr int kGB = EPL * DType<DT>::kSize; // gradient bytes per lane and rank
+    static constexpr int kEB = EPL * 4;                // residual bytes per lane and rank
+    static constexpr size_t kStageG = (size_t)kWarps * 8 * 32 * kGB;
+    static constexpr size_t kStage = (size_t)kWarps * 8 * 32 * (kGB + kEB);
+    static constexpr size_t kBytes = 2 * kStage;
+};
+
+template <int DT, int EPL>
+__global__ void __launch_bounds__(kThreads) compressed_pipe_kernel(const __grid_constant__ CompParams p)
+{
+    using Lay = PipeLayout<DT, EPL>;
+    constexpr int B = 32 * EPL;
+    constexpr int NMAX = 8;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = p.nranks;
+    const uint64_t ntiles = (p.nfull + Lay::kWarps - 1) / Lay::kWarps;
+
+    auto gslot = [&](int st, int r) {
+        return smem + (size_t)st * Lay::kStage + (((size_t)warp * 8 + r) * 32 + lane) * Lay::kGB;
+    };
+    auto eslot = [&](int st, int r) {
+        return smem + (size_t)st * Lay::kStage + Lay::kStageG + (((size_t)warp * 8 + r) * 32 + lane) * Lay::kEB;
+    };
+    auto issue = [&](uint64_t t, int st) {
+        const uint64_t b = t * Lay::kWarps + warp;
+        if (b < p.nfull) {
+            const uint64_t i0 = b * B + (uint64_t)lane * EPL;
+#pragma unroll
+            for (int r = 0; r < NMAX; ++r)
+                if (r < N) {
+                    cp_async(gslot(st, r), static_cast<const char *>(p.grads[r]) + i0 * DType<DT>::kSize, Lay::kGB);
+                    cp_async(eslot(st, r), p.res[r] + i0, Lay::kEB);
+                }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    uint64_t t = blockIdx.x;
+    if (t >= ntiles)
+        return;
+    issue(t, 0);
+    for (int it = 0; t < ntiles; ++it, t += gridDim.x) {
+        issue(t + gridDim.x, (it + 1) & 1); // an empty group past the end keeps the count uniform
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        const uint64_t b = t * Lay::kWarps + warp;
+        if (b >= p.nfull)
+            continue;
+        const uint64_t i0 = b * B + (uint64_t)lane * EPL;
+        const int st = it & 1;
+        float v[NMAX][EPL], ee[NMAX][EPL];
+#pragma unroll
+        for (int r = 0; r < NMAX; ++r) {
+            if (r < N) {
+                if (DT == DT_FP32) {
+#pragma unroll
+                    for (int j = 0; j < EPL; ++j)
+                        v[r][j] = reinterpret_cast<const float *>(gslot(st, r))[j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < EPL; j += 2) {
+                        const uint32_t w = reinterpret_cast<const uint32_t *>(gslot(st, r))[j / 2];
+                        v[r][j] = __uint_as_float(w << 16);
+                        v[r][j + 1] = __uint_as_float(w & 0xffff0000u);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < EPL; ++j)
+                    ee[r][j] = reinterpret_cast<const float *>(eslot(st, r))[j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < EPL; ++j)
+                    v[r][j] = ee[r][j] = 0.0f;
+            }
+        }
+        compress_fold_store<DT, EPL, NMAX>(p, i0, EPL, true, v, ee);
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+template <int DT, int EPL>
+static cudaError_t launch_pipe_t(const CompParams &p, cudaStream_t stream)
+{
+    using Lay = PipeLayout<DT, EPL>;
+    static bool configured = false; // the attribute is per kernel, set once per process
+    static int per_sm = 1, sms = 0;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(compressed_pipe_kernel<DT, EPL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::kBytes);
+        if (e != cudaSuccess)
+            return e;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compressed_pipe_kernel<DT, EPL>, kThreads,
+                                                      Lay::kBytes);
+        if (per_sm < 1)
+            per_sm = 1;
+        configured = true;
+    }
+    const uint64_t ntiles = (p.nfull + Lay::kWarps - 1) / Lay::kWarps;
+    uint64_t grid = (uint64_t)sms * per_sm;
+    if (grid > ntiles)
+        grid = ntiles;
+    if (grid == 0)
+        return cudaSuccess;
+    compressed_pipe_kernel<DT, EPL><<<(unsigned)grid, kThreads, Lay::kBytes, stream>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <int DT, int EPL, int NMAX>
 static cudaError_t launch_comp_t(const CompParams &p, cudaStream_t stream)
 {
     constexpr int B = 32 * EPL;
-    const uint64_t warps = (p.K + B - 1) / B;
+    const uint64_t nblocks = (p.K + B - 1) / B;
+    if (nblocks <= p.first_block)
+        return cudaSuccess;
+    const uint64_t warps = nblocks - p.first_block;
     const uint64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
     if (blocks > 0x7fffffffull)
         return cudaErrorInvalidValue;
     compressed_allreduce_kernel<DT, EPL, NMAX><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
     count_launches(1);
     return cudaGetLastError();
+}
+
+// N <= 8 with aligned buffers: whole blocks through the pipelined kernel, the
+// last partial block (if any) through the direct one.  Otherwise all direct.
+template <int DT, int EPL>
+static cudaError_t launch_comp_dt(CompParams p, cudaStream_t stream)
+{
+    constexpr int B = 32 * EPL;
+    if (p.nranks <= 8 && p.vec_ok) {
+        p.nfull = p.K / B;
+        if (p.nfull) {
+            cudaError_t e = launch_pipe_t<DT, EPL>(p, stream);
+            if (e != cudaSuccess)
+                return e;
+        }
+        p.first_block = p.nfull;
+        return launch_comp_t<DT, EPL, 8>(p, stream);
+    }
+    p.first_block = 0;
+    return p.nranks <= 8 ? launch_comp_t<DT, EPL, 8>(p, stream) : launch_comp_t<DT, EPL, 16>(p, stream);
 }
 
 cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, float threshold,
@@ -332,15 +538,11 @@ cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, f
     p.pow2 = (nranks & (nranks - 1)) == 0 ? 1 : 0;
     p.inv_n = 1.0f / (float)nranks;
     p.vec_ok = vec ? 1 : 0;
-    const bool small = nranks <= 8;
-    if (dt == DT_FP32) {
-        if (epl == 4)
-            return small ? launch_comp_t<DT_FP32, 4, 8>(p, stream) : launch_comp_t<DT_FP32, 4, 16>(p, stream);
-        return small ? launch_comp_t<DT_FP32, 2, 8>(p, stream) : launch_comp_t<DT_FP32, 2, 16>(p, stream);
-    }
-    if (epl == 4)
-        return small ? launch_comp_t<DT_BF16, 4, 8>(p, stream) : launch_comp_t<DT_BF16, 4, 16>(p, stream);
-    return small ? launch_comp_t<DT_BF16, 2, 8>(p, stream) : launch_comp_t<DT_BF16, 2, 16>(p, stream);
+    p.first_block = 0;
+    p.nfull = 0;
+    if (dt == DT_FP32)
+        return epl == 4 ? launch_comp_dt<DT_FP32, 4>(p, stream) : launch_comp_dt<DT_FP32, 2>(p, stream);
+    return epl == 4 ? launch_comp_dt<DT_BF16, 4>(p, stream) : launch_comp_dt<DT_BF16, 2>(p, stream);
 }
 
 } // namespace ccl
