@@ -186,6 +186,8 @@ ROWS = {
     "allreduce-tree": "AllReduce AVG in binomial-tree order, N=8 bf16 64Mi/rank, in place, one pass",
     "allreduce-hier": "AllReduce AVG in two-level hierarchical order (2 groups of 4), N=8 bf16 64Mi/rank, in place",
     "allreduce-int8": "compressed AllReduce AVG with error feedback, blockwise INT8 (b=128), N=8 bf16 64Mi/rank",
+    "overlap": "bucket AllReduce (4 Llama layers, N=8 bf16, 25 MiB buckets) overlapped with a synthetic backward "
+               "pass of per-rank gradient GEMMs (4096 tokens); bucket kernels on a second stream as gradients finish",
     "reduce": "Reduce SUM to rank 0, N=8 bf16 64Mi elements/rank, out of place",
     "gather": "Gather to rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
     "scatter": "Scatter from rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
@@ -314,6 +316,80 @@ def run_row(args, name, local):
         print(json.dumps(line("AllReduce (%s order) HBM GB/s, N=8 bf16 128 MB/rank, 1 GB300" % algo, 2 * N * K * 2,
                               per, launches, kernel, "bf16", {"nranks": N, "count": K, "algo": algo},
                               {"clocks": clk})))
+        return
+
+    if name == "overlap":
+        N, TOK, H, F = 8, 4096, 4096, 11008
+        numels = W.llama_layer_numels(4)
+        shapes = [(H,), (H, H), (H, H), (H, H), (H, H), (H,), (F, H), (F, H), (H, F)] * 4  # (out, in) per tensor
+        grads = [[torch.empty(n, dtype=torch.bfloat16, device=dev) for n in numels] for _ in range(N)]
+        dYt = {H: torch.randn(H, TOK, generator=g, device=dev).to(torch.bfloat16),
+               F: torch.randn(F, TOK, generator=g, device=dev).to(torch.bfloat16)}
+        X = {H: torch.randn(TOK, H, generator=g, device=dev).to(torch.bfloat16),
+             F: torch.randn(TOK, F, generator=g, device=dev).to(torch.bfloat16)}
+        # the bucket kernels go on a high-priority stream: their CTAs are
+        # scheduled as soon as the backward GEMMs' CTAs free SMs
+        compute, comm = torch.cuda.Stream(dev), torch.cuda.Stream(dev, priority=-1)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        bk = None
+
+        def backward(mark):
+            # gradients in reverse registration order, each computed for every rank
+            for t in range(len(numels) - 1, -1, -1):
+                with torch.cuda.stream(compute):
+                    for r in range(N):
+                        if len(shapes[t]) == 1:
+                            grads[r][t].fill_(1e-3)
+                        else:
+                            o, i = shapes[t]
+                            torch.matmul(dYt[o], X[i], out=grads[r][t].view(o, i))
+                    if mark:
+                        ev = torch.cuda.Event()
+                        ev.record(compute)
+                if mark:
+                    bk.mark_ready(t, ev, comm)
+
+        def run(kind):
+            comm.wait_stream(torch.cuda.current_stream(dev))
+            compute.wait_stream(torch.cuda.current_stream(dev))
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(compute)
+            comm.wait_event(a)
+            if kind == "backward":
+                backward(False)
+            elif kind == "allreduce":
+                ccl.ccl_bucket_allreduce(grads, bucket_bytes=25 * W.MiB, op="sum", stream=comm)
+            else:
+                bk.reset()
+                backward(True)
+            b.record(compute)
+            c.record(comm)
+            torch.cuda.synchronize(dev)
+            return max(a.elapsed_time(b), a.elapsed_time(c))
+
+        def timed(kind):
+            for _ in range(2):
+                run(kind)
+            return statistics.median(run(kind) for _ in range(max(3, min(args.steps, 10))))
+
+        tb, tar = timed("backward"), timed("allreduce")
+        caps = {}
+        for cap in (0, sms // 4, sms // 2, sms):  # CTAs a bucket kernel may hold
+            bk = ccl.CclBucketer(grads, bucket_bytes=25 * W.MiB, op="sum", max_ctas=cap)
+            caps[cap] = timed("overlap")
+            bk.close()
+        best = min(caps, key=caps.get)
+        to = caps[best]
+        alg = 2 * N * sum(numels) * 2
+        d = line("Bucket AllReduce overlapped with a synthetic backward, N=8 bf16 4 Llama layers, 1 GB300", alg,
+                 [tar], 62, "bucket_reduce_kernel<bf16, SUM, 8> per bucket", "bf16",
+                 {"nranks": N, "tokens": TOK, "buckets": 62},
+                 {"overlap": {"backward_ms": round(tb, 3), "allreduce_ms": round(tar, 3), "overlapped_ms": round(to, 3),
+                              "exposed_comm_ms": round(max(to - tb, 0.0), 3),
+                              "hidden_fraction": round(min(1.0, max(0.0, (tb + tar - to) / tar)), 4),
+                              "bucket_kernel_max_ctas": best,
+                              "overlapped_ms_by_max_ctas": {str(k): round(v, 3) for k, v in caps.items()}}})
+        print(json.dumps(d))
         return
 
     if name == "allreduce-int8":

@@ -178,6 +178,35 @@ ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, 
 ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                          ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
 
+/* Bucket AllReduce overlapped with the backward pass (Collective
+ * Communication, "Layer-wise overlap": a gradient hook per parameter starts a
+ * bucket's AllReduce as soon as the bucket is full, while the backward pass
+ * goes on).  ccl_bucketer_create takes the same tensors, layout and bucket
+ * size as ccl_bucket_allreduce and plans the buckets once (the tensors stay
+ * owned by the caller and must outlive the bucketer).  Each step, the caller
+ * calls ccl_bucketer_mark_ready for every tensor once its gradient is final
+ * on every rank, with an event recorded after it on the compute stream (or
+ * NULL if comm_stream is already ordered after that work).  The call makes
+ * comm_stream wait for that event (so the event need only be valid during the
+ * call; mark tensors in the order they are produced, or a later wait delays
+ * an earlier-filled bucket), and when all the tensors a bucket touches are
+ * ready it enqueues the bucket's fused ring reduction on comm_stream.  Results
+ * are bit-identical to ccl_bucket_allreduce.  ccl_bucketer_reset starts the
+ * next step. */
+typedef struct ccl_bucketer ccl_bucketer_t;
+/* max_ctas > 0 caps each bucket kernel's grid so the reduction, which is
+ * bound by memory bandwidth, runs beside the backward pass's compute-bound
+ * kernels on part of the GPU instead of claiming every SM; 0 launches one CTA
+ * per tile.  The bits do not depend on it. */
+ccl_status_t ccl_bucketer_create(void *const *ptrs, const size_t *numels, int ntensors, int nranks,
+                                 size_t bucket_bytes, ccl_dtype_t dtype, ccl_op_t op, int max_ctas,
+                                 ccl_bucketer_t **out);
+ccl_status_t ccl_bucketer_mark_ready(ccl_bucketer_t *b, int tensor, cudaEvent_t ready, cudaStream_t comm_stream);
+ccl_status_t ccl_bucketer_reset(ccl_bucketer_t *b);
+/* Buckets planned and buckets enqueued so far in this step. */
+ccl_status_t ccl_bucketer_status(ccl_bucketer_t *b, size_t *nbuckets, size_t *launched);
+ccl_status_t ccl_bucketer_destroy(ccl_bucketer_t *b);
+
 /* AllReduce under another schedule's summation order, in one pass (fused).
  * Each schedule adds the contributions in its own order, so each gives its own
  * rounded bits; this call reproduces them exactly.

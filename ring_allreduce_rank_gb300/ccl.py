@@ -74,6 +74,14 @@ def lib() -> ctypes.CDLL:
                 fn = getattr(L, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            L.ccl_bucketer_create.argtypes = [pp, psz, i32, i32, sz, i32, i32, i32, ctypes.POINTER(vp)]
+            L.ccl_bucketer_mark_ready.argtypes = [vp, i32, vp, vp]
+            L.ccl_bucketer_reset.argtypes = [vp]
+            L.ccl_bucketer_status.argtypes = [vp, psz, psz]
+            L.ccl_bucketer_destroy.argtypes = [vp]
+            for name in ("ccl_bucketer_create", "ccl_bucketer_mark_ready", "ccl_bucketer_reset",
+                         "ccl_bucketer_status", "ccl_bucketer_destroy"):
+                getattr(L, name).restype = ctypes.c_int
             L.ccl_status_string.argtypes = [ctypes.c_int]
             L.ccl_status_string.restype = ctypes.c_char_p
             L.ccl_version.argtypes = []
@@ -240,6 +248,45 @@ def ccl_bucket_allreduce(tensors: Sequence[Sequence[torch.Tensor]], bucket_bytes
     _check(lib().ccl_bucket_allreduce(_ptrs(flat), _sizes(numels), nt, nranks, int(bucket_bytes),
                                       _dtype(flat[0]), _op(op), _mode(mode), _stream(stream)),
            "ccl_bucket_allreduce")
+
+
+class CclBucketer:
+    """ccl_bucketer_*: per-bucket AllReduce launched as gradients become ready.
+    tensors[r][t] as for ccl_bucket_allreduce; keep them alive while in use."""
+
+    def __init__(self, tensors: Sequence[Sequence[torch.Tensor]], bucket_bytes: int = DEFAULT_BUCKET_BYTES,
+                 op="sum", max_ctas: int = 0):
+        nranks, nt = len(tensors), len(tensors[0])
+        self._tensors = tensors
+        flat = [tensors[r][t] for r in range(nranks) for t in range(nt)]
+        numels = [tensors[0][t].numel() for t in range(nt)]
+        h = ctypes.c_void_p()
+        _check(lib().ccl_bucketer_create(_ptrs(flat), _sizes(numels), nt, nranks, int(bucket_bytes), _dtype(flat[0]),
+                                         _op(op), int(max_ctas), ctypes.byref(h)), "ccl_bucketer_create")
+        self._h = h
+
+    def mark_ready(self, tensor: int, event: Optional[torch.cuda.Event] = None, comm_stream=None) -> None:
+        ev = ctypes.c_void_p(event.cuda_event) if event is not None else ctypes.c_void_p(0)
+        _check(lib().ccl_bucketer_mark_ready(self._h, int(tensor), ev, _stream(comm_stream)), "ccl_bucketer_mark_ready")
+
+    def reset(self) -> None:
+        _check(lib().ccl_bucketer_reset(self._h), "ccl_bucketer_reset")
+
+    def status(self):
+        nb, nl = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().ccl_bucketer_status(self._h, ctypes.byref(nb), ctypes.byref(nl)), "ccl_bucketer_status")
+        return nb.value, nl.value
+
+    def close(self) -> None:
+        if self._h:
+            lib().ccl_bucketer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # ------------------------------------------------------------------ planner

@@ -556,25 +556,12 @@ ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int n
             order.push_back(k);
 
     if (mode == CCL_MODE_FUSED) {
-        // cut each (bucket, chunk) stream range at tensor boundaries
+        // every (bucket, chunk) stream range cut at tensor boundaries, one launch
+        BucketPlan plan;
+        build_bucket_plan(numels, ntensors, nranks, B, plan);
         std::vector<RedSeg> segs;
-        size_t oi = 0;
-        for (size_t b0 = 0; b0 < total; b0 += B) {
-            const size_t blen = std::min(B, total - b0);
-            const Partition part = make_partition(blen, nranks);
-            for (int c = 0; c < nranks; ++c) {
-                size_t lo = b0 + part.off((uint32_t)c);
-                const size_t hi = lo + part.len((uint32_t)c);
-                while (lo < hi) {
-                    while (pos[order[oi]] + numels[order[oi]] <= lo)
-                        ++oi;
-                    const size_t t = order[oi];
-                    const size_t e = std::min(hi, pos[t] + numels[t]);
-                    segs.push_back(RedSeg{(uint32_t)t, (uint32_t)c, lo - pos[t], e - lo, 0});
-                    lo = e;
-                }
-            }
-        }
+        for (const auto &bs : plan.segs)
+            segs.insert(segs.end(), bs.begin(), bs.end());
         return from_cuda(launch_bucket_reduce((int)dtype, (int)op, tp.data(), ntensors, nranks, segs.data(),
                                               segs.size(), stream));
     }

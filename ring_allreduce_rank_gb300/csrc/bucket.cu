@@ -24,27 +24,30 @@ constexpr uint32_t kSegVecFlag = 0x80000000u;
 struct BucketParams {
     void *tp[kBucketPtrs]; // [local tensor][rank]
     RedSeg seg[kBucketSegs];
+    uint64_t ntiles;
     uint32_t nseg;
     int nranks;
     float n_f;
     uint32_t pad;
 };
 
+// One tile of one segment: fold its positions over the ranks in ring order
+// (rotation start c) and write the result to every rank, in place.
 template <int DT, int OP, int NR>
-__global__ void __launch_bounds__(kThreads) bucket_reduce_kernel(const __grid_constant__ BucketParams p)
+__device__ __forceinline__ void bucket_tile(const BucketParams &p, uint64_t tile)
 {
     constexpr int VEC = DType<DT>::kVec;
     constexpr uint64_t TV = kThreads;
     uint32_t lo = 0, hi = p.nseg - 1;
     while (lo < hi) {
         const uint32_t mid = (lo + hi + 1) >> 1;
-        if (p.seg[mid].tile_begin <= blockIdx.x)
+        if (p.seg[mid].tile_begin <= tile)
             lo = mid;
         else
             hi = mid - 1;
     }
     const RedSeg s = p.seg[lo];
-    const uint64_t t = blockIdx.x - s.tile_begin;
+    const uint64_t t = tile - s.tile_begin;
     const int N = NR > 0 ? NR : p.nranks;
     const int c = (int)(s.c & ~kSegVecFlag);
     const bool vec = (s.c & kSegVecFlag) != 0;
@@ -93,6 +96,15 @@ __global__ void __launch_bounds__(kThreads) bucket_reduce_kernel(const __grid_co
     }
 }
 
+// One CTA per tile, or -- with a capped grid, so that the reduction shares the
+// GPU with other kernels instead of claiming every SM -- a grid-stride walk.
+template <int DT, int OP, int NR>
+__global__ void __launch_bounds__(kThreads) bucket_reduce_kernel(const __grid_constant__ BucketParams p)
+{
+    for (uint64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x)
+        bucket_tile<DT, OP, NR>(p, tile);
+}
+
 template <int DT> static uint64_t seg_tiles(const RedSeg &s)
 {
     constexpr int VEC = DType<DT>::kVec;
@@ -108,8 +120,11 @@ template <int DT> static uint64_t seg_tiles(const RedSeg &s)
 }
 
 template <int DT, int OP>
-static cudaError_t launch_batch(BucketParams &p, uint64_t tiles, cudaStream_t stream)
+static cudaError_t launch_batch(BucketParams &p, uint64_t tiles, int max_ctas, cudaStream_t stream)
 {
+    p.ntiles = tiles;
+    if (max_ctas > 0 && tiles > (uint64_t)max_ctas)
+        tiles = (uint64_t)max_ctas;
     if (tiles > 0x7fffffffull)
         return cudaErrorInvalidValue;
     if (p.nranks == 8)
@@ -124,7 +139,7 @@ static cudaError_t launch_batch(BucketParams &p, uint64_t tiles, cudaStream_t st
 
 template <int DT, int OP>
 static cudaError_t launch_bucket_t(void *const *tensor_ptrs, int ntensors, int nranks, const RedSeg *segs,
-                                   size_t nseg, cudaStream_t stream)
+                                   size_t nseg, int max_ctas, cudaStream_t stream)
 {
     (void)ntensors;
     std::vector<char> storage(sizeof(BucketParams));
@@ -146,7 +161,7 @@ static cudaError_t launch_bucket_t(void *const *tensor_ptrs, int ntensors, int n
             continue;
         bool have = local.count(g.tp) != 0;
         if (p.nseg == (uint32_t)kBucketSegs || (!have && nptr + (uint32_t)nranks > (uint32_t)kBucketPtrs)) {
-            cudaError_t e = launch_batch<DT, OP>(p, tiles, stream);
+            cudaError_t e = launch_batch<DT, OP>(p, tiles, max_ctas, stream);
             if (e != cudaSuccess)
                 return e;
             reset();
@@ -175,32 +190,78 @@ static cudaError_t launch_bucket_t(void *const *tensor_ptrs, int ntensors, int n
         p.seg[p.nseg++] = sg;
     }
     if (p.nseg)
-        return launch_batch<DT, OP>(p, tiles, stream);
+        return launch_batch<DT, OP>(p, tiles, max_ctas, stream);
     return cudaSuccess;
 }
 
 template <int DT>
-static cudaError_t launch_bucket_dt(int op, void *const *tp, int nt, int nr, const RedSeg *s, size_t ns,
+static cudaError_t launch_bucket_dt(int op, void *const *tp, int nt, int nr, const RedSeg *s, size_t ns, int mc,
                                     cudaStream_t st)
 {
     switch (op) {
-    case OP_SUM: return launch_bucket_t<DT, OP_SUM>(tp, nt, nr, s, ns, st);
-    case OP_AVG: return launch_bucket_t<DT, OP_AVG>(tp, nt, nr, s, ns, st);
-    case OP_MAX: return launch_bucket_t<DT, OP_MAX>(tp, nt, nr, s, ns, st);
-    case OP_PROD: return launch_bucket_t<DT, OP_PROD>(tp, nt, nr, s, ns, st);
-    case OP_MIN: return launch_bucket_t<DT, OP_MIN>(tp, nt, nr, s, ns, st);
+    case OP_SUM: return launch_bucket_t<DT, OP_SUM>(tp, nt, nr, s, ns, mc, st);
+    case OP_AVG: return launch_bucket_t<DT, OP_AVG>(tp, nt, nr, s, ns, mc, st);
+    case OP_MAX: return launch_bucket_t<DT, OP_MAX>(tp, nt, nr, s, ns, mc, st);
+    case OP_PROD: return launch_bucket_t<DT, OP_PROD>(tp, nt, nr, s, ns, mc, st);
+    case OP_MIN: return launch_bucket_t<DT, OP_MIN>(tp, nt, nr, s, ns, mc, st);
     }
     return cudaErrorInvalidValue;
 }
 
+void build_bucket_plan(const size_t *numels, int ntensors, int nranks, size_t B, BucketPlan &plan)
+{
+    const size_t T = (size_t)ntensors;
+    plan.pos.assign(T, 0);
+    plan.total = 0;
+    for (size_t k = T; k-- > 0;) { // reverse registration order
+        plan.pos[k] = plan.total;
+        plan.total += numels[k];
+    }
+    std::vector<size_t> order; // non-empty tensors in stream order
+    for (size_t k = T; k-- > 0;)
+        if (numels[k])
+            order.push_back(k);
+    plan.start.clear();
+    plan.segs.clear();
+    plan.tensors.clear();
+    size_t oi = 0;
+    for (size_t b0 = 0; b0 < plan.total; b0 += B) {
+        const size_t blen = std::min(B, plan.total - b0);
+        Partition part;
+        part.q = blen / (uint64_t)nranks;
+        part.rem = (uint32_t)(blen % (uint64_t)nranks);
+        std::vector<RedSeg> segs;
+        std::vector<int> ts;
+        for (int c = 0; c < nranks; ++c) {
+            size_t lo = b0 + part.off((uint32_t)c);
+            const size_t hi = lo + part.len((uint32_t)c);
+            while (lo < hi) {
+                while (plan.pos[order[oi]] + numels[order[oi]] <= lo)
+                    ++oi;
+                const size_t t = order[oi];
+                const size_t e = std::min(hi, plan.pos[t] + numels[t]);
+                segs.push_back(RedSeg{(uint32_t)t, (uint32_t)c, lo - plan.pos[t], e - lo, 0});
+                if (ts.empty() || ts.back() != (int)t)
+                    if (std::find(ts.begin(), ts.end(), (int)t) == ts.end())
+                        ts.push_back((int)t);
+                lo = e;
+            }
+        }
+        plan.start.push_back(b0);
+        plan.segs.push_back(std::move(segs));
+        plan.tensors.push_back(std::move(ts));
+    }
+    plan.start.push_back(plan.total);
+}
+
 cudaError_t launch_bucket_reduce(int dt, int op, void *const *tensor_ptrs, int ntensors, int nranks,
-                                 const RedSeg *segs, size_t nseg, cudaStream_t stream)
+                                 const RedSeg *segs, size_t nseg, cudaStream_t stream, int max_ctas)
 {
     if (nranks > kBucketPtrs)
         return cudaErrorInvalidValue;
     if (dt == DT_FP32)
-        return launch_bucket_dt<DT_FP32>(op, tensor_ptrs, ntensors, nranks, segs, nseg, stream);
-    return launch_bucket_dt<DT_BF16>(op, tensor_ptrs, ntensors, nranks, segs, nseg, stream);
+        return launch_bucket_dt<DT_FP32>(op, tensor_ptrs, ntensors, nranks, segs, nseg, max_ctas, stream);
+    return launch_bucket_dt<DT_BF16>(op, tensor_ptrs, ntensors, nranks, segs, nseg, max_ctas, stream);
 }
 
 } // namespace ccl

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "ccl_device.cuh"
 
 namespace ccl {
@@ -85,8 +87,22 @@ struct RedSeg {
     uint64_t tile_begin;
 };
 
+// max_ctas > 0 caps the grid (the CTAs then walk the tiles), so the
+// reduction can run beside other kernels on part of the GPU.
 cudaError_t launch_bucket_reduce(int dt, int op, void *const *tensor_ptrs /* [t*nranks + r] */, int ntensors,
-                                 int nranks, const RedSeg *segs, size_t nseg, cudaStream_t stream);
+                                 int nranks, const RedSeg *segs, size_t nseg, cudaStream_t stream, int max_ctas = 0);
+
+// Bucket layout of a set of gradient tensors: the tensors laid end to end in
+// reverse registration order, cut into buckets of B elements, and every
+// (bucket, chunk) stream range cut at tensor boundaries into segments.
+struct BucketPlan {
+    size_t total = 0;                        // elements in the stream
+    std::vector<size_t> pos;                 // stream position of tensor t
+    std::vector<size_t> start;               // bucket b covers [start[b], start[b+1])
+    std::vector<std::vector<RedSeg>> segs;   // per bucket
+    std::vector<std::vector<int>> tensors;   // per bucket: the tensors it touches
+};
+void build_bucket_plan(const size_t *numels, int ntensors, int nranks, size_t bucket_elems, BucketPlan &plan);
 
 // ------------------------------------------------------------------ other schedules' orders
 enum Algo { ALGO_RING = 0, ALGO_HD = 1, ALGO_TREE = 2, ALGO_HIER = 3 };
