@@ -164,3 +164,70 @@ def test_moe_alltoallv_n8_full():
     torch.cuda.synchronize()
     for j in range(N):
         assert_bits_equal(bits(recv[j]), want[j], "moe a2a rank %d" % j)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_64bit_indexing_over_2_pow_31_elements(dtype):
+    """More than 2^31 elements per rank (N=2, a ragged 2^31 + 4099): every index
+    computation has to be 64-bit.  Inputs are a seeded pattern tiled to full
+    length; outputs are checked at sampled positions on both sides of 2^31
+    and at the chunk boundary."""
+    N, K = 2, (1 << 31) + 4099
+    P = 1 << 20
+    pat = W.normal_bf16(N, P, seed_base=7) if dtype == "bf16" else W.normal_fp32(N, P, seed_base=7)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    arena = RankArena(N, K, td, device=DEV)
+    for r in range(N):
+        p_dev = to_dev(pat[r])
+        arena.ranks[r].copy_(p_dev.repeat((K + P - 1) // P)[:K])
+        del p_dev
+    ccl.ccl_allreduce(arena.ranks, op="sum")
+    torch.cuda.synchronize()
+    off, ln = ccl.ccl_plan_chunks(K, N)
+    g = np.random.Generator(np.random.PCG64(31))
+    idx = set(g.integers(0, K, size=4096).tolist())
+    for e in (0, 1, off[1] - 1, off[1], off[1] + 1, (1 << 31) - 1, 1 << 31, (1 << 31) + 1, K - 8, K - 1):
+        idx.add(int(e))
+    idx = np.array(sorted(idx), dtype=np.int64)
+    vals = [pat[r][idx % P] for r in range(N)]
+    want = oracle.ring_allreduce_gathered(vals, K, idx.astype(np.uint64), "sum")
+    it = torch.from_numpy(idx).to(DEV)
+    for r in range(N):
+        assert_bits_equal(bits(arena.ranks[r].index_select(0, it)), want, "K > 2^31 rank %d" % r)
+    del arena
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("algo", ["ring", "halving_doubling", "tree", "hierarchical"])
+def test_maximum_ranks_1024(algo):
+    """The largest rank count the ABI accepts: 1024 ranks, ragged length."""
+    N, K = 1024, 3001
+    x = list(W.mixed_bf16(N, K, seed_base=11))
+    group = 32 if algo == "hierarchical" else 0
+    if algo == "ring":
+        want, _ = oracle.ring_allreduce(x, "sum")
+    else:
+        want = oracle.allreduce_algo(x, algo, "sum", group)
+    bufs = [to_dev(r) for r in x]
+    ccl.ccl_allreduce_algo(bufs, op="sum", algo=algo, group_size=group)
+    torch.cuda.synchronize()
+    for r in (0, 1, 511, 1023):
+        assert_bits_equal(bits(bufs[r]), want[r], "%s N=1024 rank %d" % (algo, r))
+
+
+def test_maximum_ranks_1024_reduce_scatter_allgather_broadcast():
+    N, K = 1024, 5000
+    x = list(W.normal_bf16(N, K, seed_base=12))
+    off, ln = ccl.ccl_plan_chunks(K, N)
+    send = [to_dev(r) for r in x]
+    rs = [torch.empty(ln[r], dtype=torch.bfloat16, device=DEV) for r in range(N)]
+    ag = [torch.empty(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    ccl.ccl_reduce_scatter(send, rs, op="avg")
+    ccl.ccl_allgather(rs, ag)
+    ccl.ccl_broadcast(send, send, root=1023)
+    torch.cuda.synchronize()
+    want, _ = oracle.ring_allreduce(x, "avg")
+    for r in (0, 7, 1023):
+        assert_bits_equal(bits(ag[r]), want[r], "RS+AG N=1024 rank %d" % r)
+        assert_bits_equal(bits(send[r]), x[1023], "broadcast N=1024 rank %d" % r)
