@@ -273,6 +273,41 @@ ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, void *const
                                             ccl_dtype_t dtype, ccl_op_t op, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* Result checks and tracing                                           */
+/* ------------------------------------------------------------------ */
+
+/* Adds to *mismatches (a DEVICE counter the caller zeroes) the number of
+ * elements, summed over ranks 1..nranks-1, whose bits differ from rank 0's.
+ * After an AllReduce every rank must hold the same bits (Collective
+ * Communication, Definition 1.1); the pages ask that results be checked
+ * against silent corruption (section on pitfalls).  Never traps. */
+ccl_status_t ccl_check_identical(const void *const *bufs, int nranks, size_t count, ccl_dtype_t dtype,
+                                 unsigned long long *mismatches, cudaStream_t stream);
+
+/* One traced call: the collective, its shape, the kernels it enqueued and
+ * the host time it took to validate, plan and enqueue (not GPU time). */
+typedef struct {
+    char collective[24];
+    int nranks;
+    int dtype;
+    int op;   /* -1 where the collective takes none */
+    int mode; /* or the algorithm / compressor of the _algo / _compressed calls */
+    int status;
+    unsigned launches;
+    unsigned long long count;
+    unsigned long long host_ns;
+    unsigned long long seq;
+} ccl_trace_record_t;
+
+/* Tracing is off unless CCL_TRACE is set (to anything but 0) or enabled here.
+ * The last 4096 calls are kept. */
+void ccl_set_trace(int enabled);
+/* Copies up to max_records of the newest records, oldest first, into out
+ * (out == NULL: returns how many are held). */
+size_t ccl_trace_read(ccl_trace_record_t *out, size_t max_records);
+void ccl_trace_clear(void);
+
+/* ------------------------------------------------------------------ */
 /* Planner (host only; no GPU needed)                                  */
 /* ------------------------------------------------------------------ */
 

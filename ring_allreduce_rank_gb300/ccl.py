@@ -82,6 +82,14 @@ def lib() -> ctypes.CDLL:
             for name in ("ccl_bucketer_create", "ccl_bucketer_mark_ready", "ccl_bucketer_reset",
                          "ccl_bucketer_status", "ccl_bucketer_destroy"):
                 getattr(L, name).restype = ctypes.c_int
+            L.ccl_check_identical.argtypes = [pp, i32, sz, i32, vp, vp]
+            L.ccl_check_identical.restype = ctypes.c_int
+            L.ccl_set_trace.argtypes = [i32]
+            L.ccl_set_trace.restype = None
+            L.ccl_trace_read.argtypes = [vp, sz]
+            L.ccl_trace_read.restype = sz
+            L.ccl_trace_clear.argtypes = []
+            L.ccl_trace_clear.restype = None
             L.ccl_status_string.argtypes = [ctypes.c_int]
             L.ccl_status_string.restype = ctypes.c_char_p
             L.ccl_version.argtypes = []
@@ -248,6 +256,40 @@ def ccl_bucket_allreduce(tensors: Sequence[Sequence[torch.Tensor]], bucket_bytes
     _check(lib().ccl_bucket_allreduce(_ptrs(flat), _sizes(numels), nt, nranks, int(bucket_bytes),
                                       _dtype(flat[0]), _op(op), _mode(mode), _stream(stream)),
            "ccl_bucket_allreduce")
+
+
+def ccl_check_identical(bufs: Sequence[torch.Tensor], mismatches: torch.Tensor, stream=None) -> None:
+    """Adds to mismatches (a one-element int64 device tensor) the number of
+    elements whose bits differ from rank 0's, over ranks 1..N-1."""
+    if mismatches.dtype != torch.int64 or mismatches.numel() != 1 or not mismatches.is_cuda:
+        raise TypeError("mismatches must be a one-element int64 CUDA tensor")
+    _check(lib().ccl_check_identical(_ptrs(bufs), len(bufs), bufs[0].numel(), _dtype(bufs[0]),
+                                     ctypes.c_void_p(mismatches.data_ptr()), _stream(stream)), "ccl_check_identical")
+
+
+class TraceRecord(ctypes.Structure):
+    _fields_ = [("collective", ctypes.c_char * 24), ("nranks", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("op", ctypes.c_int), ("mode", ctypes.c_int), ("status", ctypes.c_int), ("launches", ctypes.c_uint),
+                ("count", ctypes.c_ulonglong), ("host_ns", ctypes.c_ulonglong), ("seq", ctypes.c_ulonglong)]
+
+
+def ccl_set_trace(enabled: bool) -> None:
+    lib().ccl_set_trace(1 if enabled else 0)
+
+
+def ccl_trace_read(max_records: int = 4096):
+    """The newest traced calls, oldest first, as dicts."""
+    n = lib().ccl_trace_read(None, 0)
+    n = min(n, max_records)
+    buf = (TraceRecord * max(1, n))()
+    n = lib().ccl_trace_read(ctypes.cast(buf, ctypes.c_void_p), n)
+    return [{"collective": r.collective.decode(), "nranks": r.nranks, "dtype": r.dtype, "op": r.op, "mode": r.mode,
+             "status": r.status, "launches": r.launches, "count": r.count, "host_ns": r.host_ns, "seq": r.seq}
+            for r in buf[:n]]
+
+
+def ccl_trace_clear() -> None:
+    lib().ccl_trace_clear()
 
 
 class CclBucketer:

@@ -265,7 +265,7 @@ ccl_status_t ccl_arena_layout(int nranks, size_t bytes_per_rank, size_t align, s
 
 // ------------------------------------------------------------------ AllReduce
 
-ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+static ccl_status_t ccl_allreduce_impl(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
                            ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !valid_mode(mode) || !send || !recv)
@@ -301,7 +301,7 @@ ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nrank
 
 // ------------------------------------------------------------------ ReduceScatter
 
-ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
+static ccl_status_t ccl_reduce_scatter_impl(const void *const *send, void *const *recv, int nranks, size_t count,
                                 ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !valid_mode(mode) || !send || !recv)
@@ -352,7 +352,7 @@ ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int 
 
 // ------------------------------------------------------------------ AllGather
 
-ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+static ccl_status_t ccl_allgather_impl(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
                            ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv)
@@ -394,7 +394,7 @@ ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nrank
 
 // ------------------------------------------------------------------ Broadcast
 
-ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+static ccl_status_t ccl_broadcast_impl(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                            ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv || root < 0 ||
@@ -446,7 +446,7 @@ ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nrank
 
 // ------------------------------------------------------------------ AllToAll(v)
 
-ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nranks, const size_t *counts,
+static ccl_status_t ccl_alltoallv_impl(const void *const *send, void *const *recv, int nranks, const size_t *counts,
                            ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv || !counts)
@@ -498,7 +498,7 @@ ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nrank
     return CCL_OK;
 }
 
-ccl_status_t ccl_alltoall(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+static ccl_status_t ccl_alltoall_impl(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
                           ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks))
@@ -506,12 +506,12 @@ ccl_status_t ccl_alltoall(const void *const *send, void *const *recv, int nranks
     if (mul_overflows(count, (size_t)nranks))
         return CCL_ERR_INVALID_ARG;
     std::vector<size_t> counts((size_t)nranks * nranks, count);
-    return ccl_alltoallv(send, recv, nranks, counts.data(), dtype, mode, stream);
+    return ccl_alltoallv_impl(send, recv, nranks, counts.data(), dtype, mode, stream);
 }
 
 // ------------------------------------------------------------------ bucket AllReduce
 
-ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int ntensors, int nranks,
+static ccl_status_t ccl_bucket_allreduce_impl(void *const *ptrs, const size_t *numels, int ntensors, int nranks,
                                   size_t bucket_bytes, ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode,
                                   cudaStream_t stream)
 {
@@ -604,7 +604,7 @@ ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int n
 
 // ------------------------------------------------------------------ Reduce / Gather / Scatter
 
-ccl_status_t ccl_reduce(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+static ccl_status_t ccl_reduce_impl(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                         ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !valid_mode(mode) || !send || !recv ||
@@ -657,7 +657,7 @@ ccl_status_t ccl_reduce(const void *const *send, void *const *recv, int nranks, 
     return from_cuda(launch_copy_segments(segs.data(), segs.size(), stream));
 }
 
-ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+static ccl_status_t ccl_gather_impl(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                         ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv || root < 0 ||
@@ -694,7 +694,7 @@ ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, 
     return CCL_OK;
 }
 
-ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+static ccl_status_t ccl_scatter_impl(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                          ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
     if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_mode(mode) || !send || !recv || root < 0 ||
@@ -731,7 +731,7 @@ ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks,
 
 // ------------------------------------------------------------------ other schedules' orders
 
-ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int nranks, size_t count,
+static ccl_status_t ccl_allreduce_algo_impl(const void *const *send, void *const *recv, int nranks, size_t count,
                                 ccl_dtype_t dtype, ccl_op_t op, ccl_algo_t algo, int group_size,
                                 cudaStream_t stream)
 {
@@ -778,7 +778,7 @@ ccl_status_t ccl_plan_compressed_bytes(size_t count, ccl_compressor_t comp, int 
     return CCL_OK;
 }
 
-ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residuals, int nranks, size_t count,
+static ccl_status_t ccl_allreduce_compressed_impl(void *const *grads, float *const *residuals, int nranks, size_t count,
                                       ccl_dtype_t dtype, ccl_op_t op, ccl_compressor_t comp, int block,
                                       float threshold, cudaStream_t stream)
 {
@@ -803,6 +803,95 @@ ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residual
         return st;
     return from_cuda(launch_compressed_allreduce((int)dtype, op == CCL_AVG, (int)comp, block, threshold, grads,
                                                  residuals, nranks, count, stream));
+}
+
+// ------------------------------------------------------------------ traced entry points
+
+ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+                           ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("allreduce", nranks, count, (int)dtype, (int)op, (int)mode);
+    return tr.done(ccl_allreduce_impl(send, recv, nranks, count, dtype, op, mode, stream));
+}
+
+ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("reduce_scatter", nranks, count, (int)dtype, (int)op, (int)mode);
+    return tr.done(ccl_reduce_scatter_impl(send, recv, nranks, count, dtype, op, mode, stream));
+}
+
+ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+                           ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("allgather", nranks, count, (int)dtype, -1, (int)mode);
+    return tr.done(ccl_allgather_impl(send, recv, nranks, count, dtype, mode, stream));
+}
+
+ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                           ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("broadcast", nranks, count, (int)dtype, -1, (int)mode);
+    return tr.done(ccl_broadcast_impl(send, recv, nranks, root, count, dtype, mode, stream));
+}
+
+ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nranks, const size_t *counts,
+                           ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("alltoallv", nranks, 0, (int)dtype, -1, (int)mode);
+    return tr.done(ccl_alltoallv_impl(send, recv, nranks, counts, dtype, mode, stream));
+}
+
+ccl_status_t ccl_alltoall(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
+                          ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("alltoall", nranks, count, (int)dtype, -1, (int)mode);
+    return tr.done(ccl_alltoall_impl(send, recv, nranks, count, dtype, mode, stream));
+}
+
+ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int ntensors, int nranks,
+                                  size_t bucket_bytes, ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode,
+                                  cudaStream_t stream)
+{
+    TraceScope tr("bucket_allreduce", nranks, (size_t)ntensors, (int)dtype, (int)op, (int)mode);
+    return tr.done(ccl_bucket_allreduce_impl(ptrs, numels, ntensors, nranks, bucket_bytes, dtype, op, mode, stream));
+}
+
+ccl_status_t ccl_reduce(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                        ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("reduce", nranks, count, (int)dtype, (int)op, (int)mode);
+    return tr.done(ccl_reduce_impl(send, recv, nranks, root, count, dtype, op, mode, stream));
+}
+
+ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                        ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("gather", nranks, count, (int)dtype, -1, (int)mode);
+    return tr.done(ccl_gather_impl(send, recv, nranks, root, count, dtype, mode, stream));
+}
+
+ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks, int root, size_t count,
+                         ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
+{
+    TraceScope tr("scatter", nranks, count, (int)dtype, -1, (int)mode);
+    return tr.done(ccl_scatter_impl(send, recv, nranks, root, count, dtype, mode, stream));
+}
+
+ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, ccl_algo_t algo, int group_size,
+                                cudaStream_t stream)
+{
+    TraceScope tr("allreduce_algo", nranks, count, (int)dtype, (int)op, (int)algo);
+    return tr.done(ccl_allreduce_algo_impl(send, recv, nranks, count, dtype, op, algo, group_size, stream));
+}
+
+ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residuals, int nranks, size_t count,
+                                      ccl_dtype_t dtype, ccl_op_t op, ccl_compressor_t comp, int block,
+                                      float threshold, cudaStream_t stream)
+{
+    TraceScope tr("allreduce_compressed", nranks, count, (int)dtype, (int)op, (int)comp);
+    return tr.done(ccl_allreduce_compressed_impl(grads, residuals, nranks, count, dtype, op, comp, block, threshold, stream));
 }
 
 } // extern "C"

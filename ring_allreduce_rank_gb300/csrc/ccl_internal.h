@@ -8,6 +8,7 @@
 
 #include <vector>
 
+#include "../../include/ccl.h"
 #include "ccl_device.cuh"
 
 namespace ccl {
@@ -123,5 +124,24 @@ cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, f
 
 // ------------------------------------------------------------------ bookkeeping
 void count_launches(unsigned long long n);
+
+// Records one call in the trace ring buffer when tracing is on (CCL_TRACE or
+// ccl_set_trace): construct at entry, pass the status through done().
+class TraceScope {
+  public:
+    TraceScope(const char *name, int nranks, uint64_t count, int dtype, int op, int mode);
+    ccl_status_t done(ccl_status_t st)
+    {
+        finish((int)st);
+        return st;
+    }
+
+  private:
+    void finish(int status);
+    bool active_;
+    ccl_trace_record_t rec_{};
+    unsigned long long launches0_ = 0;
+    long long t0_ = 0;
+};
 
 } // namespace ccl

@@ -1,0 +1,199 @@
+// check.cu -- result checks and call tracing.
+//
+// After an AllReduce every rank must hold the same bits (Collective
+// Communication, Definition 1.1: gradient synchronisation leaves every replica
+// identical; the section on pitfalls: silent corruption calls for checking
+// results).  ccl_check_identical compares every rank's buffer with rank 0's,
+// bit for bit, and adds the number of differing elements to a device counter;
+// it never traps, so a corrupted result is reported, not fatal.
+//
+// Tracing keeps the last calls' descriptions (collective, ranks, count, type,
+// op, mode, kernels launched, host time to enqueue) in a host ring buffer.
+#include <atomic>
+#include <chrono>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/ccl.h"
+#include "ccl_internal.h"
+
+namespace ccl {
+
+template <int MAXR> struct CheckParams {
+    const void *buf[MAXR];
+    uint64_t K;
+    unsigned long long *mismatches;
+    int nranks;
+    int vec_aligned;
+    int elem_size;
+};
+
+// one element (or 16-byte vector) per thread; differing lanes counted with a
+// warp ballot and added once per warp
+template <int MAXR>
+__global__ void __launch_bounds__(kThreads) check_identical_kernel(const __grid_constant__ CheckParams<MAXR> p)
+{
+    const uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int es = p.elem_size;
+    const uint64_t per_vec = 16 / es;
+    unsigned bad = 0;
+    if (p.vec_aligned) {
+        const uint64_t nv = p.K / per_vec;
+        if (i < nv) {
+            const uint4 a = ld16(static_cast<const char *>(p.buf[0]) + i * 16);
+            for (int r = 1; r < p.nranks; ++r) {
+                const uint4 b = ld16(static_cast<const char *>(p.buf[r]) + i * 16);
+                const uint32_t x[4] = {a.x ^ b.x, a.y ^ b.y, a.z ^ b.z, a.w ^ b.w};
+                for (int w = 0; w < 4; ++w) {
+                    if (es == 4)
+                        bad += x[w] != 0;
+                    else
+                        bad += ((x[w] & 0xffffu) != 0) + ((x[w] >> 16) != 0);
+                }
+            }
+        }
+        // the tail after the last whole vector, one element per thread of block 0
+        if (blockIdx.x == 0)
+            for (uint64_t e = nv * per_vec + threadIdx.x; e < p.K; e += kThreads)
+                for (int r = 1; r < p.nranks; ++r)
+                    bad += es == 4 ? ld_elem<DT_FP32>(p.buf[r], e) != ld_elem<DT_FP32>(p.buf[0], e)
+                                   : ld_elem<DT_BF16>(p.buf[r], e) != ld_elem<DT_BF16>(p.buf[0], e);
+    } else if (i < p.K) {
+        for (int r = 1; r < p.nranks; ++r)
+            bad += es == 4 ? ld_elem<DT_FP32>(p.buf[r], i) != ld_elem<DT_FP32>(p.buf[0], i)
+                           : ld_elem<DT_BF16>(p.buf[r], i) != ld_elem<DT_BF16>(p.buf[0], i);
+    }
+    // warp total: lanes with nothing to add stay out of the atomic
+    const unsigned any = __ballot_sync(0xffffffffu, bad != 0);
+    unsigned total = bad;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        total += __shfl_xor_sync(0xffffffffu, total, o);
+    if (any && (threadIdx.x & 31) == 0)
+        atomicAdd(p.mismatches, (unsigned long long)total);
+}
+
+template <int MAXR>
+static cudaError_t launch_check_t(const void *const *bufs, int nranks, uint64_t count, int es,
+                                  unsigned long long *mismatches, cudaStream_t stream)
+{
+    CheckParams<MAXR> p;
+    bool aligned = true;
+    for (int r = 0; r < MAXR; ++r) {
+        p.buf[r] = r < nranks ? bufs[r] : nullptr;
+        if (r < nranks)
+            aligned = aligned && (uintptr_t)bufs[r] % 16 == 0;
+    }
+    p.K = count;
+    p.mismatches = mismatches;
+    p.nranks = nranks;
+    p.vec_aligned = aligned ? 1 : 0;
+    p.elem_size = es;
+    const uint64_t work = aligned ? count / (16 / es) : count;
+    uint64_t blocks = (work + kThreads - 1) / kThreads;
+    if (blocks == 0)
+        blocks = 1;
+    if (blocks > 0x7fffffffull)
+        return cudaErrorInvalidValue;
+    check_identical_kernel<MAXR><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ tracing
+
+namespace {
+constexpr size_t kTraceCap = 4096;
+std::mutex g_trace_mu;
+ccl_trace_record_t g_trace[kTraceCap];
+size_t g_trace_next = 0, g_trace_count = 0;
+std::atomic<int> g_trace_on{-1}; // -1: read CCL_TRACE on first use
+
+bool trace_enabled()
+{
+    int v = g_trace_on.load(std::memory_order_relaxed);
+    if (v < 0) {
+        const char *env = std::getenv("CCL_TRACE");
+        v = (env && env[0] && std::strcmp(env, "0") != 0) ? 1 : 0;
+        g_trace_on.store(v, std::memory_order_relaxed);
+    }
+    return v > 0;
+}
+} // namespace
+
+TraceScope::TraceScope(const char *name, int nranks, uint64_t count, int dtype, int op, int mode)
+    : active_(trace_enabled())
+{
+    if (!active_)
+        return;
+    std::memset(&rec_, 0, sizeof rec_);
+    std::strncpy(rec_.collective, name, sizeof rec_.collective - 1);
+    rec_.nranks = nranks;
+    rec_.count = count;
+    rec_.dtype = dtype;
+    rec_.op = op;
+    rec_.mode = mode;
+    launches0_ = ccl_launch_count();
+    t0_ = std::chrono::steady_clock::now().time_since_epoch().count();
+}
+
+void TraceScope::finish(int status)
+{
+    if (!active_)
+        return;
+    active_ = false;
+    const long long t1 = std::chrono::steady_clock::now().time_since_epoch().count();
+    rec_.status = status;
+    rec_.launches = (unsigned)(ccl_launch_count() - launches0_);
+    rec_.host_ns = (unsigned long long)(t1 - t0_);
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    rec_.seq = g_trace_count;
+    g_trace[g_trace_next] = rec_;
+    g_trace_next = (g_trace_next + 1) % kTraceCap;
+    ++g_trace_count;
+}
+
+} // namespace ccl
+
+using namespace ccl;
+
+extern "C" {
+
+ccl_status_t ccl_check_identical(const void *const *bufs, int nranks, size_t count, ccl_dtype_t dtype,
+                                 unsigned long long *mismatches, cudaStream_t stream)
+{
+    if (nranks < 1 || nranks > CCL_MAX_RANKS || (dtype != CCL_FP32 && dtype != CCL_BF16) || !bufs || !mismatches)
+        return CCL_ERR_INVALID_ARG;
+    for (int r = 0; r < nranks; ++r)
+        if (!bufs[r] && count)
+            return CCL_ERR_INVALID_ARG;
+    if (count == 0 || nranks == 1)
+        return CCL_OK;
+    const int es = dtype == CCL_BF16 ? 2 : 4;
+    const cudaError_t e = nranks <= kSmallRanks ? launch_check_t<kSmallRanks>(bufs, nranks, count, es, mismatches, stream)
+                                                : launch_check_t<kMaxRanks>(bufs, nranks, count, es, mismatches, stream);
+    return e == cudaSuccess ? CCL_OK : CCL_ERR_CUDA;
+}
+
+void ccl_set_trace(int enabled) { g_trace_on.store(enabled ? 1 : 0, std::memory_order_relaxed); }
+
+size_t ccl_trace_read(ccl_trace_record_t *out, size_t max_records)
+{
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    const size_t have = g_trace_count < kTraceCap ? g_trace_count : kTraceCap;
+    const size_t n = out ? (max_records < have ? max_records : have) : have;
+    if (out)
+        for (size_t k = 0; k < n; ++k) // oldest first, the newest n records
+            out[k] = g_trace[(g_trace_next + kTraceCap - n + k) % kTraceCap];
+    return n;
+}
+
+void ccl_trace_clear(void)
+{
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace_next = 0;
+    g_trace_count = 0;
+}
+
+} // extern "C"

@@ -1,0 +1,62 @@
+"""Result checks and tracing on the device: ccl_check_identical counts, bit
+for bit, the elements where a rank differs from rank 0 (0 after every
+AllReduce, exactly the planted differences otherwise), and traced calls
+record their shape and the kernels they launched."""
+import numpy as np
+import pytest
+import torch
+
+import ring_allreduce_rank_gb300 as ccl
+from ring_allreduce_rank_gb300 import workloads as W
+
+from gpu_util import DEV, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available()
+    ccl.lib()
+    torch.cuda.set_device(0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("N,K,pad", [(8, 70001, 0), (3, 1000, 1), (33, 4099, 0)])
+def test_check_identical_counts_planted_differences(N, K, pad, dtype):
+    x = W.mixed_bf16(N, K, seed_base=N) if dtype == "bf16" else W.mixed_fp32(N, K, seed_base=N)
+    bufs = [to_dev(r, pad_elems=pad) for r in x]
+    ccl.ccl_allreduce(bufs, op="sum")
+    cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+    ccl.ccl_check_identical(bufs, cnt)
+    torch.cuda.synchronize()
+    assert int(cnt.item()) == 0
+    g = np.random.Generator(np.random.PCG64(K))
+    planted = 0
+    for r in (1, N - 1):
+        for e in sorted(set(g.integers(0, K, size=5).tolist()) | {0, K - 1}):
+            v = bufs[r][e:e + 1]
+            v.view(torch.int16 if dtype == "bf16" else torch.int32).bitwise_xor_(1)
+            planted += 1
+    cnt.zero_()
+    ccl.ccl_check_identical(bufs, cnt)
+    torch.cuda.synchronize()
+    assert int(cnt.item()) == planted
+
+
+def test_trace_records_calls():
+    ccl.ccl_trace_clear()
+    ccl.ccl_set_trace(True)
+    try:
+        N, K = 4, 4099
+        bufs = [torch.zeros(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+        ccl.ccl_allreduce(bufs, op="avg")
+        ccl.ccl_allreduce(bufs, op="sum", mode="step")
+        torch.cuda.synchronize()
+        recs = ccl.ccl_trace_read()
+    finally:
+        ccl.ccl_set_trace(False)
+    assert [r["collective"] for r in recs] == ["allreduce", "allreduce"]
+    assert recs[0]["launches"] == 1 and recs[1]["launches"] == 2 * (N - 1)
+    assert all(r["status"] == 0 and r["nranks"] == N and r["count"] == K and r["dtype"] == 1 for r in recs)
+    assert recs[0]["op"] == 1 and recs[1]["mode"] == 1 and recs[1]["seq"] == recs[0]["seq"] + 1

@@ -53,9 +53,26 @@ def overlaps(L):
     assert L.ccl_bucket_allreduce(_pp([FAKE, FAKE + 32]), nums, 2, 1, 0, 0, 0, 0, ok) == 3
 
 
+def traced_rejections(L):
+    """Rejected calls are traced with their status; nothing is launched."""
+    ccl.ccl_trace_clear()
+    ccl.ccl_set_trace(True)
+    s = _pp([FAKE, FAKE + 4096])
+    assert L.ccl_allreduce(s, s, 0, 16, 0, 0, 0, ctypes.c_void_p(0)) == 1
+    assert L.ccl_broadcast(s, s, 2, 5, 16, 1, 0, ctypes.c_void_p(0)) == 1
+    recs = ccl.ccl_trace_read()
+    assert [r["collective"] for r in recs] == ["allreduce", "broadcast"]
+    assert [r["status"] for r in recs] == [1, 1] and all(r["launches"] == 0 for r in recs)
+    assert recs[0]["count"] == 16 and recs[1]["dtype"] == 1
+    ccl.ccl_set_trace(False)
+    assert L.ccl_allreduce(s, s, 0, 16, 0, 0, 0, ctypes.c_void_p(0)) == 1
+    assert len(ccl.ccl_trace_read()) == 2
+
+
 if __name__ == "__main__":
     assert os.environ.get("CUDA_VISIBLE_DEVICES") == "", "run with CUDA_VISIBLE_DEVICES=''"
     L = ccl.lib()
     invalid_arguments(L)
     overlaps(L)
+    traced_rejections(L)
     print("validation cases ok")
