@@ -247,6 +247,37 @@ __device__ __forceinline__ uint32_t ring_fold_elem(const void *const *ptrs, int 
 
 __host__ __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
+// Output window of `d` elements into (lo, hi): the vector made of lo's
+// elements d..VEC-1 followed by hi's elements 0..d-1 (0 < d < VEC).
+template <int DT> __device__ __forceinline__ uint4 shift_window(const uint4 &lo, const uint4 &hi, int d)
+{
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t o[4];
+    if (DT == DT_FP32) {
+        switch (d) {
+        case 1: o[0] = w[1]; o[1] = w[2]; o[2] = w[3]; o[3] = w[4]; break;
+        case 2: o[0] = w[2]; o[1] = w[3]; o[2] = w[4]; o[3] = w[5]; break;
+        default: o[0] = w[3]; o[1] = w[4]; o[2] = w[5]; o[3] = w[6]; break;
+        }
+    } else {
+        // d halfwords: whole words k = d/2, then half a word if d is odd
+#define CCL_SHIFT_CASE(D)                                                                                              \
+    case D:                                                                                                            \
+        _Pragma("unroll") for (int i = 0; i < 4; ++i) o[i] =                                                           \
+            (D & 1) ? __funnelshift_r(w[(D >> 1) + i], w[(D >> 1) + i + 1], 16) : w[(D >> 1) + i];                     \
+        break;
+        switch (d) {
+            CCL_SHIFT_CASE(1) CCL_SHIFT_CASE(2) CCL_SHIFT_CASE(3) CCL_SHIFT_CASE(4) CCL_SHIFT_CASE(5)
+            CCL_SHIFT_CASE(6)
+        default:
+            _Pragma("unroll") for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[3 + i], w[4 + i], 16);
+        }
+#undef CCL_SHIFT_CASE
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+
 // ------------------------------------------------------------------ chunk partition
 
 // Chunk c of a K-element buffer: len = K/N + (c < K%N), first K%N chunks longer.

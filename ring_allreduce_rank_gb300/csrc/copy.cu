@@ -164,10 +164,14 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
     const int M = p.ndst;
     if (p.vec_aligned && off % VEC != 0) {
         // The chunk lands at an offset that is not a whole vector (ragged
-        // partition): keep the N-fold stores as aligned 16-byte vectors and
-        // gather each vector's source elements one at a time (the source is
-        // only 1/N of the bytes moved).
+        // partition).  Lanes load aligned source vectors; each aligned
+        // destination vector is the window s0 elements into two neighbouring
+        // lanes' vectors, exchanged with a shuffle.  A warp loads 32 source
+        // vectors and writes 31 destination vectors to every rank.
+        constexpr int WARPS = kThreads / 32;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const uint64_t vb = (off + VEC - 1) / VEC, ve = (off + len) / VEC;
+        const int s0 = (int)(vb * VEC - off); // 0 < s0 < VEC
         if (t == 0) {
             const uint64_t hb = vb < ve ? vb * VEC : off + len;
             for (uint64_t d = off + threadIdx.x; d < hb; d += kThreads) {
@@ -182,23 +186,33 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
                         st_elem<DT>(p.dst[q], d, v);
                 }
         }
+        const uint64_t i0 = ((uint64_t)t * WARPS + warp) * 31; // this warp's first destination vector (from vb)
+        if (vb >= ve || i0 >= ve - vb)
+            return; // whole warp
+        const uint64_t b = i0 + lane; // source vector
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if ((b + 1) * VEC <= len) {
+            x = ld16(static_cast<const char *>(src) + b * 16);
+        } else {
+            uint32_t h[VEC];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint64_t v = vb + (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
-            if (v >= ve)
-                continue;
-            const uint64_t s0 = v * VEC - off; // first source element of this vector
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (DT == DT_FP32)
-                    w[k] = ld_elem<DT>(src, s0 + k);
-                else
-                    w[k] = ld_elem<DT>(src, s0 + 2 * k) | (ld_elem<DT>(src, s0 + 2 * k + 1) << 16);
-            }
-            const uint4 x = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int k = 0; k < VEC; ++k)
+                h[k] = b * VEC + k < len ? ld_elem<DT>(src, b * VEC + k) : 0u;
+            if (DT == DT_FP32)
+                x = make_uint4(h[0], h[1], h[2], h[3]);
+            else
+                x = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+        }
+        uint4 nx;
+        nx.x = __shfl_down_sync(0xffffffffu, x.x, 1);
+        nx.y = __shfl_down_sync(0xffffffffu, x.y, 1);
+        nx.z = __shfl_down_sync(0xffffffffu, x.z, 1);
+        nx.w = __shfl_down_sync(0xffffffffu, x.w, 1);
+        const uint64_t v = vb + i0 + lane; // destination vector
+        if (lane < 31 && v < ve) {
+            const uint4 w = shift_window<DT>(x, nx, s0);
             for (int q = 0; q < M; ++q)
-                st16(static_cast<char *>(p.dst[q]) + v * 16, x);
+                st16(static_cast<char *>(p.dst[q]) + v * 16, w);
         }
         return;
     }
@@ -258,7 +272,11 @@ static cudaError_t launch_fanout_t(const void *const *src, int nchunks, void *co
     p.ndst = ndst;
     p.vec_aligned = aligned ? 1 : 0;
     const uint64_t te = (uint64_t)kThreads * 2 * VEC;
-    const uint64_t tiles = (p.part.q + 1 + te - 1) / te;
+    uint64_t tiles = (p.part.q + 1 + te - 1) / te;
+    const uint64_t per_tile = (uint64_t)(kThreads / 32) * 31; // ragged chunks: 31 vectors per warp
+    const uint64_t shifted = ((p.part.q + 1) / VEC + per_tile) / per_tile + 1;
+    if (nchunks > 1 && shifted > tiles)
+        tiles = shifted;
     if (tiles > 0x7fffffffull)
         return cudaErrorInvalidValue;
     fanout_kernel<DT, MAXR><<<dim3((unsigned)tiles, (unsigned)nchunks), kThreads, 0, stream>>>(p);

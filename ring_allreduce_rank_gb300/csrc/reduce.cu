@@ -53,6 +53,61 @@ __device__ __forceinline__ void reduce_elem(const FusedParams<MAXR> &p, int N, u
     }
 }
 
+// ReduceScatter chunk whose offset is not a whole vector: fold aligned input
+// vectors, then build each (aligned) output vector from two neighbouring
+// lanes' results.  A warp folds 32 input vectors and stores 31 output vectors.
+template <int DT, int OP, int NR, int MAXR>
+__device__ __forceinline__ void reduce_scatter_shifted(const FusedParams<MAXR> &p, int N, uint32_t c, uint64_t off,
+                                                       uint64_t len, uint32_t t)
+{
+    constexpr int VEC = DType<DT>::kVec;
+    constexpr int WARPS = kThreads / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t nout = len / VEC;            // whole output vectors
+    const int d = (int)(off % VEC);             // misalignment in elements
+    const uint64_t a0 = off / VEC;              // input vector holding the chunk's first element
+    const uint64_t K = (uint64_t)p.part.q * (uint64_t)N + p.part.rem;
+    const uint64_t j0 = ((uint64_t)t * WARPS + warp) * 31; // this warp's first output vector
+    if (t == 0)  // the last, partial output vector
+        for (uint64_t e = off + nout * VEC + threadIdx.x; e < off + len; e += kThreads)
+            reduce_elem<DT, OP, MAXR>(p, N, c, e, off);
+    if (j0 >= nout)
+        return; // whole warp
+    const uint64_t a = a0 + j0 + lane;
+    uint4 r = make_uint4(0, 0, 0, 0);
+    if ((a + 1) * VEC <= K) {
+        r = ring_fold_vec<DT, OP, NR>(p.send, N, (int)c, a * 16);
+        if (OP == OP_AVG)
+            r = avg_vec<DT>(r, p.n_f);
+    } else {
+        // the buffer's last, partial vector: elements past K stay zero (never stored)
+        uint32_t h[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+            const uint64_t e = a * VEC + k;
+            uint32_t v = 0;
+            if (e < K) {
+                v = ring_fold_elem<DT, OP>(p.send, N, (int)c, e);
+                if (OP == OP_AVG)
+                    v = avg_elem<DT>(v, p.n_f);
+            }
+            h[k] = v;
+        }
+        if (DT == DT_FP32)
+            r = make_uint4(h[0], h[1], h[2], h[3]);
+        else
+            r = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+    }
+    uint4 nx;
+    nx.x = __shfl_down_sync(0xffffffffu, r.x, 1);
+    nx.y = __shfl_down_sync(0xffffffffu, r.y, 1);
+    nx.z = __shfl_down_sync(0xffffffffu, r.z, 1);
+    nx.w = __shfl_down_sync(0xffffffffu, r.w, 1);
+    const uint64_t j = j0 + lane;
+    if (lane < 31 && j < nout)
+        st16(static_cast<char *>(p.recv[c]) + j * 16, shift_window<DT>(r, nx, d));
+}
+
 template <int DT, int OP, int NR, int MAXR>
 __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_constant__ FusedParams<MAXR> p)
 {
@@ -67,6 +122,10 @@ __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_con
     const uint64_t out_base = p.write_mode == WRITE_CHUNK ? off : 0;
     const bool vec_ok = p.vec_aligned && (p.write_mode != WRITE_CHUNK || (off % VEC) == 0);
 
+    if (p.vec_aligned && p.write_mode == WRITE_CHUNK && (off % VEC) != 0) {
+        reduce_scatter_shifted<DT, OP, NR, MAXR>(p, N, c, off, len, t);
+        return;
+    }
     if (!vec_ok) {
         // element path over tile t of the chunk
         const uint64_t e0 = off + (uint64_t)t * TV * VEC;
@@ -205,7 +264,13 @@ static cudaError_t launch_t(const void *const *send, void *const *recv, int nran
     p.vec_aligned = aligned ? 1 : 0;
     p.n_f = (float)nranks;
     const uint64_t te = (uint64_t)kThreads * U * VEC;
-    const uint64_t tiles = (p.part.q + 1 + te - 1) / te;
+    uint64_t tiles = (p.part.q + 1 + te - 1) / te;
+    if (write_mode == WRITE_CHUNK) { // ragged chunks may take the shifted path: 31 vectors per warp
+        const uint64_t per_tile = (uint64_t)(kThreads / 32) * 31;
+        const uint64_t shifted = ((p.part.q + 1) / VEC + per_tile) / per_tile + 1;
+        if (shifted > tiles)
+            tiles = shifted;
+    }
     if (tiles > 0x7fffffffull)
         return cudaErrorInvalidValue;
     p.tiles = (uint32_t)tiles;
