@@ -85,10 +85,26 @@ __global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_co
     const char *src = s.src + head + b0;
     char *dst = s.dst + head + b0;
     if (g == 16) {
+        // four 16-byte loads in flight per thread before the stores (the
+        // volatile loads and stores keep program order, so they are batched
+        // by hand)
+        constexpr int B = 4;
         const uint64_t n = nb / 16;
-#pragma unroll 4
-        for (uint64_t i = threadIdx.x; i < n; i += kThreads)
-            st16(dst + i * 16, ld16(src + i * 16));
+        for (uint64_t i0 = threadIdx.x; i0 < n; i0 += (uint64_t)B * kThreads) {
+            uint4 x[B];
+#pragma unroll
+            for (int k = 0; k < B; ++k) {
+                const uint64_t i = i0 + (uint64_t)k * kThreads;
+                if (i < n)
+                    x[k] = ld16(src + i * 16);
+            }
+#pragma unroll
+            for (int k = 0; k < B; ++k) {
+                const uint64_t i = i0 + (uint64_t)k * kThreads;
+                if (i < n)
+                    st16(dst + i * 16, x[k]);
+            }
+        }
     } else if (g == 8) {
         copy_body<uint2>(src, dst, nb);
     } else if (g == 4) {

@@ -26,20 +26,6 @@ __device__ __forceinline__ void step_elem(const StepParams<MAXR> &p, int kind, i
 }
 
 template <int DT, int OP, int MAXR>
-__device__ __forceinline__ void step_vec(const StepParams<MAXR> &p, int kind, int i, int left, uint64_t v)
-{
-    char *dst = static_cast<char *>(p.buf[i]) + v * 16;
-    if (kind == STEP_RS) {
-        const uint4 incoming = ld16(static_cast<const char *>(p.buf[left]) + v * 16);
-        st16(dst, hop_vec<DT, OP>(ld16(dst), incoming));
-    } else if (kind == STEP_SCALE) {
-        st16(dst, avg_vec<DT>(ld16(dst), p.n_f));
-    } else {
-        st16(dst, ld16(static_cast<const char *>(p.buf[left]) + v * 16));
-    }
-}
-
-template <int DT, int OP, int MAXR>
 __global__ void __launch_bounds__(kThreads) ring_step_kernel(const __grid_constant__ StepParams<MAXR> p)
 {
     constexpr int VEC = DType<DT>::kVec;
@@ -77,11 +63,32 @@ __global__ void __launch_bounds__(kThreads) ring_step_kernel(const __grid_consta
             for (uint64_t e = ve * VEC + threadIdx.x; e < end; e += kThreads)
                 step_elem<DT, OP, MAXR>(p, kind, i, left, e);
     }
+    // all of this thread's loads first, then the hops and stores (the volatile
+    // loads and stores keep program order, so they are batched by hand)
+    uint4 mine[U], theirs[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const uint64_t v = vb + (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
-        if (v < ve)
-            step_vec<DT, OP, MAXR>(p, kind, i, left, v);
+        if (v < ve) {
+            if (kind == STEP_RS || kind == STEP_SCALE)
+                mine[u] = ld16(static_cast<const char *>(p.buf[i]) + v * 16);
+            if (kind != STEP_SCALE)
+                theirs[u] = ld16(static_cast<const char *>(p.buf[left]) + v * 16);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint64_t v = vb + (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
+        if (v < ve) {
+            uint4 out;
+            if (kind == STEP_RS)
+                out = hop_vec<DT, OP>(mine[u], theirs[u]);
+            else if (kind == STEP_SCALE)
+                out = avg_vec<DT>(mine[u], p.n_f);
+            else
+                out = theirs[u];
+            st16(static_cast<char *>(p.buf[i]) + v * 16, out);
+        }
     }
 }
 
