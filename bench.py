@@ -214,8 +214,8 @@ def _timed(torch, ccl, step, steps, warmup, stream, dev):
 def graph_call_seconds(torch, ccl, call, nbytes, dev) -> float:
     """Device time per call: R calls captured once in a CUDA graph and
     replayed, so the host's per-call cost (Python, argument checks, launch)
-    is not in the measurement.  R keeps each replay around 20 ms."""
-    R = int(max(1, min(500, 2e10 / max(nbytes, 1) / 1e3)))
+    is not in the measurement.  R (at most 100) keeps each replay short."""
+    R = int(max(1, min(100, 2e10 / max(nbytes, 1) / 1e3)))
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
