@@ -272,6 +272,33 @@ ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residual
 ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, void *const *recv, int nranks, size_t count,
                                             ccl_dtype_t dtype, ccl_op_t op, cudaStream_t stream);
 
+/* Device working space that lets ccl_allreduce_host run at the host link's
+ * speed: three stages of 64 MiB. */
+#define CCL_HOST_WORK_BYTES_DEFAULT (192u * 1024u * 1024u)
+
+/* AllReduce of rank buffers that live in HOST memory: the same result, bit for
+ * bit, as ccl_allreduce on the same data (the ring fold of chunk c starting at
+ * rank c of the count-element partition).  send[r], recv[r]: `count` elements
+ * each, any memory the GPU can copy from and to (cudaMemcpyDefault); page-
+ * locked host memory (cudaHostAlloc, cudaHostRegister) is what makes the
+ * copies asynchronous and overlapped.  In place when send[r] == recv[r].
+ * The vector moves through `work` (DEVICE memory, caller-owned, 16-byte
+ * aligned, work_bytes >= 3 * nranks * 256 * element size; larger is faster,
+ * up to CCL_HOST_WORK_BYTES_DEFAULT) in slices: copies in and out run on two
+ * library-owned streams so that both directions of the host link are busy at
+ * once, and each slice is reduced on `stream` (the link is the bottleneck:
+ * Collective Communication, Table 1, GPU<->CPU row; the overlap is the
+ * pipelining of the section on NCCL).  Ordering: the call starts after the
+ * work already enqueued on `stream`, and work enqueued on `stream` afterwards
+ * sees every result in recv[].  Calls that share `work` must be ordered (one
+ * stream, or events); the library orders its own stage reuse across calls.
+ * Returns CCL_ERR_UNSUPPORTED while `stream` is being captured into a CUDA
+ * graph, CCL_ERR_INVALID_ARG for a work buffer that is too small or
+ * misaligned, and the common argument errors otherwise. */
+ccl_status_t ccl_allreduce_host(const void *const *send, void *const *recv, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, void *work, size_t work_bytes,
+                                cudaStream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* Result checks and tracing                                           */
 /* ------------------------------------------------------------------ */
@@ -335,6 +362,16 @@ ccl_status_t ccl_plan_alltoallv(int nranks, const size_t *counts, size_t *sdispl
  * scales, 4b/(b+4) times fewer than fp32: 3.88 at b = 128); THRESHOLD:
  * ceil(count / 8). */
 ccl_status_t ccl_plan_compressed_bytes(size_t count, ccl_compressor_t comp, int block, size_t *bytes);
+
+/* Slices of ccl_allreduce_host for these arguments: writes up to max_slices
+ * (off, len) pairs, in elements of every rank's buffer, and the total number
+ * into *nslices (off/len may be NULL to ask for the number only).  The slices
+ * tile [0, count) in order; each is at most the stage length
+ * floor(work_bytes / (3 * nranks * element size)) rounded down to a multiple
+ * of 256 elements, starts on a multiple of 256, and they grow from 1/16 of the
+ * stage length at the start and shrink the same way at the end. */
+ccl_status_t ccl_plan_host_slices(size_t count, int nranks, ccl_dtype_t dtype, size_t work_bytes, size_t *off,
+                                  size_t *len, size_t max_slices, size_t *nslices);
 
 /* Arena layout: per-rank stride (bytes_per_rank rounded up to `align`, a power
  * of two >= 256) and total bytes for nranks rank buffers in one allocation. */

@@ -27,6 +27,7 @@ STATUS = {0: "CCL_OK", 1: "CCL_ERR_INVALID_ARG", 2: "CCL_ERR_UNSUPPORTED", 3: "C
           4: "CCL_ERR_CUDA", 5: "CCL_ERR_NO_MEMORY", 6: "CCL_ERR_TIMEOUT", 7: "CCL_ERR_CHECK_FAILED"}
 MAX_RANKS = 1024
 DEFAULT_BUCKET_BYTES = 25 * 1024 * 1024
+HOST_WORK_BYTES_DEFAULT = 192 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
                 "ccl_plan_buckets": [psz, i32, sz, psz, sz, psz],
                 "ccl_plan_alltoallv": [i32, psz, psz, psz],
                 "ccl_arena_layout": [i32, sz, sz, psz, psz],
+                "ccl_allreduce_host": [pp, pp, i32, sz, i32, i32, vp, sz, vp],
+                "ccl_plan_host_slices": [sz, i32, i32, sz, psz, psz, sz, psz],
                 "ccl_finalize": [],
             }
             for name, args in sig.items():
@@ -155,6 +158,19 @@ def ccl_allreduce(send: Sequence[torch.Tensor], recv: Optional[Sequence[torch.Te
     n = len(send)
     _check(lib().ccl_allreduce(_ptrs(send), _ptrs(recv), n, send[0].numel(), _dtype(send[0]), _op(op), _mode(mode),
                                _stream(stream)), "ccl_allreduce")
+
+
+def ccl_allreduce_host(send: Sequence[torch.Tensor], recv: Optional[Sequence[torch.Tensor]] = None, op="sum",
+                       work: Optional[torch.Tensor] = None, stream=None) -> None:
+    """AllReduce of rank buffers in host memory (CPU tensors; pinned ones let
+    the copies overlap), staged through `work`, a contiguous CUDA tensor the
+    caller owns (HOST_WORK_BYTES_DEFAULT bytes run at the link's speed)."""
+    if work is None or not work.is_cuda or not work.is_contiguous():
+        raise ValueError("ccl_allreduce_host needs a contiguous CUDA work tensor")
+    recv = send if recv is None else recv
+    _check(lib().ccl_allreduce_host(_ptrs(send), _ptrs(recv), len(send), send[0].numel(), _dtype(send[0]), _op(op),
+                                    ctypes.c_void_p(work.data_ptr()), work.numel() * work.element_size(),
+                                    _stream(stream)), "ccl_allreduce_host")
 
 
 def ccl_allreduce_algo(send: Sequence[torch.Tensor], recv: Optional[Sequence[torch.Tensor]] = None, op="sum",
@@ -365,6 +381,18 @@ def ccl_plan_alltoallv(counts):
     sd, rd = (ctypes.c_size_t * (n * n))(), (ctypes.c_size_t * (n * n))()
     _check(lib().ccl_plan_alltoallv(n, _sizes(flat), sd, rd), "ccl_plan_alltoallv")
     return [list(sd)[i * n:(i + 1) * n] for i in range(n)], [list(rd)[j * n:(j + 1) * n] for j in range(n)]
+
+
+def ccl_plan_host_slices(count: int, nranks: int, dtype: str = "bf16", work_bytes: int = HOST_WORK_BYTES_DEFAULT):
+    """[(off, len)] slices of ccl_allreduce_host, in elements per rank."""
+    dt = {"fp32": FP32, "bf16": BF16}[dtype]
+    n = ctypes.c_size_t()
+    _check(lib().ccl_plan_host_slices(count, nranks, dt, work_bytes, None, None, 0, ctypes.byref(n)),
+           "ccl_plan_host_slices")
+    off, ln = (ctypes.c_size_t * max(1, n.value))(), (ctypes.c_size_t * max(1, n.value))()
+    _check(lib().ccl_plan_host_slices(count, nranks, dt, work_bytes, off, ln, n.value, ctypes.byref(n)),
+           "ccl_plan_host_slices")
+    return list(zip(list(off)[:n.value], list(ln)[:n.value]))
 
 
 def ccl_arena_layout(nranks: int, bytes_per_rank: int, align: int = 256):

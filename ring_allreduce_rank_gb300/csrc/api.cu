@@ -805,6 +805,66 @@ static ccl_status_t ccl_allreduce_compressed_impl(void *const *grads, float *con
                                                  residuals, nranks, count, stream));
 }
 
+// ------------------------------------------------------------------ host-buffer AllReduce
+
+ccl_status_t ccl_plan_host_slices(size_t count, int nranks, ccl_dtype_t dtype, size_t work_bytes, size_t *off,
+                                  size_t *len, size_t max_slices, size_t *nslices)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !nslices)
+        return CCL_ERR_INVALID_ARG;
+    const uint64_t L = host_stage_elems(nranks, elem_size(dtype), work_bytes);
+    if (count > 0 && L == 0)
+        return CCL_ERR_INVALID_ARG;
+    std::vector<HostSlice> sl;
+    plan_host_slices(count, L, sl);
+    *nslices = sl.size();
+    if (off && len)
+        for (size_t k = 0; k < sl.size() && k < max_slices; ++k) {
+            off[k] = sl[k].off;
+            len[k] = sl[k].len;
+        }
+    return CCL_OK;
+}
+
+static ccl_status_t ccl_allreduce_host_impl(const void *const *send, void *const *recv, int nranks, size_t count,
+                                            ccl_dtype_t dtype, ccl_op_t op, void *work, size_t work_bytes,
+                                            cudaStream_t stream)
+{
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !send || !recv)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    if (!work || (uintptr_t)work % 16 != 0 || host_stage_elems(nranks, es, work_bytes) == 0)
+        return CCL_ERR_INVALID_ARG;
+    const size_t bytes = count * es;
+    std::vector<Range> w, r;
+    bool in_place = true;
+    for (int i = 0; i < nranks; ++i) {
+        if (!send[i] || !recv[i])
+            return CCL_ERR_INVALID_ARG;
+        in_place = in_place && send[i] == recv[i];
+        w.push_back(range_of(recv[i], bytes, i));
+        r.push_back(range_of(send[i], bytes, i));
+    }
+    w.push_back(range_of(work, work_bytes, -1));
+    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return rd.rank == wr.rank && rd.lo == wr.lo;
+    });
+    if (st != CCL_OK)
+        return st;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone)
+        return CCL_ERR_UNSUPPORTED;
+    if (nranks == 1 && in_place && op != CCL_AVG)
+        return CCL_OK;
+    return from_cuda(run_host_allreduce((int)dtype, (int)op, send, recv, nranks, count, work, work_bytes, stream));
+}
+
 // ------------------------------------------------------------------ traced entry points
 
 ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
@@ -812,6 +872,14 @@ ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nrank
 {
     TraceScope tr("allreduce", nranks, count, (int)dtype, (int)op, (int)mode);
     return tr.done(ccl_allreduce_impl(send, recv, nranks, count, dtype, op, mode, stream));
+}
+
+ccl_status_t ccl_allreduce_host(const void *const *send, void *const *recv, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, void *work, size_t work_bytes,
+                                cudaStream_t stream)
+{
+    TraceScope tr("allreduce_host", nranks, count, (int)dtype, (int)op, 0);
+    return tr.done(ccl_allreduce_host_impl(send, recv, nranks, count, dtype, op, work, work_bytes, stream));
 }
 
 ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,

@@ -10,34 +10,9 @@
 
 #include "../../include/ccl.h"
 #include "ccl_device.cuh"
+#include "fused.h"
 
 namespace ccl {
-
-constexpr int kSmallRanks = 16;
-constexpr int kMaxRanks = 1024;
-
-// ------------------------------------------------------------------ fused reduce
-template <int MAXR> struct FusedParams {
-    const void *send[MAXR];
-    void *recv[MAXR];
-    Partition part;
-    int nranks;
-    int write_mode;  // WRITE_CHUNK, WRITE_ALL or WRITE_ROOT
-    int root;        // WRITE_ROOT: the one rank that receives the result
-    int vec_aligned; // every pointer is 16-byte aligned
-    uint32_t tiles;  // tiles per chunk (gridDim.x)
-    float n_f;       // (float)nranks, the AVG divisor
-};
-
-enum WriteMode {
-    WRITE_CHUNK = 0, // ReduceScatter: chunk c goes to recv[c], chunk-local
-    WRITE_ALL = 1,   // AllReduce: every rank receives the whole result
-    WRITE_ROOT = 2   // Reduce: only recv[root] receives the whole result
-};
-
-// Launch the one-pass ring-order reduction (AllReduce, ReduceScatter or Reduce).
-cudaError_t launch_fused_reduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
-                                uint64_t count, int write_mode, int root, cudaStream_t stream);
 
 // ------------------------------------------------------------------ step mode
 enum StepKind {
@@ -122,8 +97,26 @@ cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, f
                                         void *const *grads, float *const *res, int nranks, uint64_t count,
                                         cudaStream_t stream);
 
+// ------------------------------------------------------------------ host-buffer AllReduce
+constexpr int kHostStages = 3;            // device stages in flight: copy-in, reduce, copy-out
+constexpr uint64_t kHostSliceUnit = 256;  // slice starts and stage lengths are multiples of this (elements)
+
+struct HostSlice {
+    uint64_t off, len; // elements of every rank's buffer
+};
+
+// Elements per rank in one stage of a work buffer of work_bytes (a multiple of
+// kHostSliceUnit; 0 if the buffer is too small).
+uint64_t host_stage_elems(int nranks, size_t elem_size, size_t work_bytes);
+// Slices of [0, count): growing from stage_elems/16 to stage_elems, then
+// shrinking again towards the end; every one at most stage_elems long.
+void plan_host_slices(uint64_t count, uint64_t stage_elems, std::vector<HostSlice> &slices);
+// Pipelined copy-in / reduce / copy-out through `work`; validated arguments.
+cudaError_t run_host_allreduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
+                               uint64_t count, void *work, size_t work_bytes, cudaStream_t stream);
+
 // ------------------------------------------------------------------ bookkeeping
-void count_launches(unsigned long long n);
+// (count_launches is declared in fused.h)
 
 // Records one call in the trace ring buffer when tracing is on (CCL_TRACE or
 // ccl_set_trace): construct at entry, pass the status through done().

@@ -21,7 +21,7 @@
 // ReduceScatter chunk whose offset is not a multiple of the vector) the CTA
 // walks its tile element by element instead.  The same kernel serves Reduce:
 // the root receives the AllReduce's result and no other rank is written.
-#include "ccl_internal.h"
+#include "fused.h"
 
 namespace ccl {
 

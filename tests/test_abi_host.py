@@ -95,6 +95,37 @@ def test_arena_layout(L):
         ccl.ccl_arena_layout(3, 1000, 100)
 
 
+@pytest.mark.parametrize("K,N,dt,work", [(64 << 20, 8, "bf16", 192 << 20), (12_345_678, 16, "fp32", 1 << 20),
+                                         (100_000, 8, "bf16", 3 * 8 * 256 * 2), (1000, 3, "fp32", 192 << 20),
+                                         (3 * 1024 * 1024 + 7, 5, "bf16", 3 * 5 * 4096 * 2 + 100)])
+def test_planner_host_slices(L, K, N, dt, work):
+    """Slices of the host-buffer AllReduce tile [0, K) in order, fit a stage,
+    start on 256-element boundaries, and ramp up (and down) by doubling."""
+    es = 2 if dt == "bf16" else 4
+    stage = work // (3 * N * es) // 256 * 256
+    sl = ccl.ccl_plan_host_slices(K, N, dt, work)
+    pos = 0
+    for off, ln in sl:
+        assert off == pos and 0 < ln <= stage and off % 256 == 0
+        pos += ln
+    assert pos == K
+    lens = [ln for _, ln in sl]
+    first = max(256, stage // 16 // 256 * 256)
+    if K >= 4 * stage:
+        assert lens[0] == first and lens[-1] <= first
+        k = 0
+        while lens[k] < stage:  # head: doubling up to the stage length
+            assert lens[k + 1] == min(2 * lens[k], stage)
+            k += 1
+        assert max(lens) == stage
+
+
+def test_planner_host_slices_rejects_small_work(L):
+    with pytest.raises(C.CclError):
+        ccl.ccl_plan_host_slices(1000, 8, "fp32", 3 * 8 * 256 * 4 - 1)
+    assert ccl.ccl_plan_host_slices(0, 8, "fp32", 0) == []
+
+
 # ------------------------------------------------------------------ validation (no launch)
 # The cases live in tests/validation_cases.py and run in a child process that
 # sees no GPU (CUDA_VISIBLE_DEVICES=""): their pointers are fake, so a case that

@@ -53,6 +53,27 @@ def overlaps(L):
     assert L.ccl_bucket_allreduce(_pp([FAKE, FAKE + 32]), nums, 2, 1, 0, 0, 0, 0, ok) == 3
 
 
+def host_allreduce(L):
+    """ccl_allreduce_host: work buffer checks and overlaps, before any launch."""
+    ok = ctypes.c_void_p(0)
+    s, r = _pp([FAKE, FAKE + 4096]), _pp([FAKE + 8192, FAKE + 12288])
+    W = FAKE + (1 << 30)
+    need = 3 * 2 * 256 * 4  # three stages of 256 fp32 elements per rank
+    f = L.ccl_allreduce_host
+    assert f(s, r, 2, 16, 0, 0, None, need, ok) == 1              # no work buffer
+    assert f(s, r, 2, 16, 0, 0, ctypes.c_void_p(W + 8), need, ok) == 1  # misaligned
+    assert f(s, r, 2, 16, 0, 0, ctypes.c_void_p(W), need - 1, ok) == 1  # too small for one unit
+    assert f(s, r, 2, 16, 7, 0, ctypes.c_void_p(W), need, ok) == 1      # dtype
+    assert f(s, r, 0, 16, 0, 0, ctypes.c_void_p(W), need, ok) == 1      # nranks
+    assert f(s, r, 2, 1 << 62, 0, 0, ctypes.c_void_p(W), need, ok) == 1  # bytes overflow
+    # the work buffer overlaps an output, or an input
+    assert f(s, r, 2, 16, 0, 0, ctypes.c_void_p(FAKE + 12288), need, ok) == 3
+    assert f(s, r, 2, 16, 0, 0, ctypes.c_void_p(FAKE), need, ok) == 3
+    # two outputs overlap
+    assert f(s, _pp([FAKE + 8192, FAKE + 8192 + 32]), 2, 16, 0, 0, ctypes.c_void_p(W), need, ok) == 3
+    assert f(s, r, 2, 0, 0, 0, None, 0, ok) == 0                   # count 0: no-op, nothing checked further
+
+
 def traced_rejections(L):
     """Rejected calls are traced with their status; nothing is launched."""
     ccl.ccl_trace_clear()
@@ -74,5 +95,6 @@ if __name__ == "__main__":
     L = ccl.lib()
     invalid_arguments(L)
     overlaps(L)
+    host_allreduce(L)
     traced_rejections(L)
     print("validation cases ok")
