@@ -34,6 +34,7 @@ METRIC = "AllReduce HBM GB/s & % of peak, N=8 bf16 128 MB/rank, 1 GB300"
 UNIT = "GB/s"
 NRANKS = 8
 COUNT = 64 * 1024 * 1024  # bf16 elements per rank (128 MiB)
+DEFAULT_COUNT = COUNT
 ELEM = 2
 ALG_BYTES = 2 * NRANKS * COUNT * ELEM  # N*M read + N*M written
 HOST_WORK_BYTES = 192 * 1024 * 1024  # device stages of the end-to-end (host-buffer) leg
@@ -190,8 +191,8 @@ ROWS = {
     "overlap": "bucket AllReduce (4 Llama layers, N=8 bf16, 25 MiB buckets) overlapped with a synthetic backward "
                "pass of per-rank gradient GEMMs (4096 tokens); bucket kernels on a second stream as gradients finish",
     "reduce": "Reduce SUM to rank 0, N=8 bf16 64Mi elements/rank, out of place",
-    "gather": "Gather to rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
-    "scatter": "Scatter from rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi)",
+    "gather": "Gather to rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi; --count sets the total)",
+    "scatter": "Scatter from rank 0, N=8 bf16, 64Mi elements total (8 slices of 8Mi; --count sets the total)",
     "sweep": "AllReduce SUM bf16, 1 KiB..1 GiB per rank (x4), N in {2,4,8,16,64}; device time per call from "
              "CUDA-graph replay; points whose N*S fits in L2 are marked l2_resident (replays hit L2, not HBM)",
 }
@@ -215,8 +216,8 @@ def _timed(torch, ccl, step, steps, warmup, stream, dev):
 def graph_call_seconds(torch, ccl, call, nbytes, dev) -> float:
     """Device time per call: R calls captured once in a CUDA graph and
     replayed, so the host's per-call cost (Python, argument checks, launch)
-    is not in the measurement.  R (at most 100) keeps each replay short."""
-    R = int(max(1, min(100, 2e10 / max(nbytes, 1) / 1e3)))
+    is not in the measurement.  R (at most 20) keeps each replay short."""
+    R = int(max(1, min(20, 2e10 / max(nbytes, 1) / 1e3)))
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
@@ -429,7 +430,11 @@ def run_row(args, name, local):
         return
 
     if name in ("reduce", "gather", "scatter"):
+        # Reduce: 64Mi elements per rank.  Gather / Scatter: 64Mi elements in
+        # total unless --count sets the total (e.g. 8x that, 128 MiB per rank)
         N, K = 8, 64 * 1024 * 1024
+        if name != "reduce" and args.count != DEFAULT_COUNT:
+            K = args.count
         if name == "reduce":
             send = [randn_bf16(K) for _ in range(N)]
             recv = [None] * N
@@ -449,7 +454,7 @@ def run_row(args, name, local):
                 step = lambda: ccl.ccl_scatter(full, parts, root=0, stream=stream)
                 kernel = "copy_segments_kernel (N segments)"
             alg = 2 * K * 2
-            metric = "%s HBM GB/s, N=8 bf16 128 MB total, 1 GB300" % name.capitalize()
+            metric = "%s HBM GB/s, N=8 bf16 %d MB total, 1 GB300" % (name.capitalize(), K * 2 // 2**20)
         clocks.start()
         tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
         clk = clocks.stop()
