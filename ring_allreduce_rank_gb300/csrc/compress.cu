@@ -42,7 +42,28 @@ struct CompParams {
     int vec_ok;  // grads and residuals aligned for the lane's vector width
     uint64_t first_block; // the direct kernel starts at this compression block
     uint64_t nfull;       // the pipelined kernel covers blocks [0, nfull)
+    uint64_t coff[kCompMaxRanks + 1]; // chunk c starts at coff[c]; entries from N on hold K
 };
+
+// max that returns NaN when either side is NaN (PTX max.NaN), so a block's
+// maximum of |u| also says whether the block holds a NaN
+__device__ __forceinline__ float fmax_nan(float a, float b)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// chunk holding element e: the number of chunk starts after chunk 0 at or below e
+template <int NMAX>
+__device__ __forceinline__ uint32_t chunk_of(const CompParams &p, uint64_t e)
+{
+    uint32_t c = 0;
+#pragma unroll
+    for (int k = 1; k < NMAX; ++k)
+        c += e >= p.coff[k] ? 1u : 0u;
+    return c;
+}
 
 template <int DT, int EPL>
 __device__ __forceinline__ void load_g(const void *base, uint64_t i, int valid, bool vec, float (&out)[EPL])
@@ -158,24 +179,17 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
                 ee[r][j] = __fsub_rn(u, v[r][j]);
             }
     } else {
-        // per-rank block maxima (NaN flagged separately)
+        // per-rank block maxima of |u|; a NaN anywhere in the block makes the
+        // maximum NaN, and the scale with it
         float amax[NMAX];
-        uint32_t nanmask = 0;
 #pragma unroll
         for (int r = 0; r < NMAX; ++r) {
             amax[r] = 0.0f;
 #pragma unroll
             for (int j = 0; j < EPL; ++j)
-                if (j < valid) {
-                    if (v[r][j] != v[r][j])
-                        nanmask |= 1u << r;
-                    else
-                        amax[r] = fmaxf(amax[r], fabsf(v[r][j]));
-                }
+                if (j < valid)
+                    amax[r] = fmax_nan(amax[r], fabsf(v[r][j]));
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            nanmask |= __shfl_xor_sync(0xffffffffu, nanmask, o);
         float sc[NMAX], inv[NMAX];
         const int lane = threadIdx.x & 31;
         if constexpr (NMAX == 8) {
@@ -188,18 +202,17 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float send = b4 ? amax[k] : amax[k + 4];
-                k4[k] = fmaxf(b4 ? amax[k + 4] : amax[k], __shfl_xor_sync(0xffffffffu, send, 16));
+                k4[k] = fmax_nan(b4 ? amax[k + 4] : amax[k], __shfl_xor_sync(0xffffffffu, send, 16));
             }
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const float send = b3 ? k4[k] : k4[k + 2];
-                k2[k] = fmaxf(b3 ? k4[k + 2] : k4[k], __shfl_xor_sync(0xffffffffu, send, 8));
+                k2[k] = fmax_nan(b3 ? k4[k + 2] : k4[k], __shfl_xor_sync(0xffffffffu, send, 8));
             }
-            float m = fmaxf(b2 ? k2[1] : k2[0], __shfl_xor_sync(0xffffffffu, b2 ? k2[0] : k2[1], 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            const int mine = (lane >> 2) & 7;
-            const float s1 = (nanmask >> mine) & 1u ? __uint_as_float(0x7fffffffu) : __fdiv_rn(m, 127.0f);
+            float m = fmax_nan(b2 ? k2[1] : k2[0], __shfl_xor_sync(0xffffffffu, b2 ? k2[0] : k2[1], 4));
+            m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const float s1 = m != m ? __uint_as_float(0x7fffffffu) : __fdiv_rn(m, 127.0f);
             const float i1 = __frcp_rn(s1);
 #pragma unroll
             for (int r = 0; r < NMAX; ++r) {
@@ -211,10 +224,10 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
             for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
                 for (int r = 0; r < NMAX; ++r)
-                    amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], o));
+                    amax[r] = fmax_nan(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], o));
 #pragma unroll
             for (int r = 0; r < NMAX; ++r) {
-                sc[r] = (nanmask >> r) & 1u ? __uint_as_float(0x7fffffffu) : __fdiv_rn(amax[r], 127.0f);
+                sc[r] = amax[r] != amax[r] ? __uint_as_float(0x7fffffffu) : __fdiv_rn(amax[r], 127.0f);
                 inv[r] = __frcp_rn(sc[r]);
             }
         }
@@ -241,15 +254,11 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
             store_f<EPL>(p.res[r], i0, valid, vec, ee[r]);
 
     // ring-order fold in fp32: chunk c from rank c, then c+1, ..., c-1
-    uint32_t c = 0;
-    if (valid > 0) {
-        const uint64_t q1 = p.part.q + 1, head = (uint64_t)p.part.rem * q1;
-        c = i0 < head ? (uint32_t)(i0 / q1) : (uint32_t)(p.part.rem + (p.part.q ? (i0 - head) / p.part.q : 0));
-    }
+    uint32_t c = valid > 0 ? chunk_of<NMAX>(p, i0) : 0u;
     uint32_t outb[EPL];
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
-        while (c + 1 < (uint32_t)N && i0 + j >= p.part.off(c + 1))
+        while (c + 1 < (uint32_t)N && i0 + j >= p.coff[c + 1])
             ++c;
         float acc;
         if (N == NMAX) {
@@ -530,6 +539,8 @@ cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, f
     }
     p.part.q = count / (uint64_t)nranks;
     p.part.rem = (uint32_t)(count % (uint64_t)nranks);
+    for (int c = 0; c <= kCompMaxRanks; ++c)
+        p.coff[c] = c < nranks ? p.part.off((uint32_t)c) : count;
     p.K = count;
     p.nranks = nranks;
     p.comp = comp;
