@@ -21,7 +21,11 @@ import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "ring_oracle.c")
-LIB = os.path.join(HERE, "_build", "liboracle.so")
+# ORACLE_LIB: a prebuilt copy to load instead (the mutation tests point it at
+# copies of ring_oracle.c with one planted mistake each)
+OVERRIDE = os.environ.get("ORACLE_LIB") or None
+LIB = OVERRIDE or os.path.join(HERE, "_build", "liboracle.so")
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall", "-Wextra"]
 
 FP32, BF16 = 0, 1
 SUM, AVG, MAX, PROD, MIN = 0, 1, 2, 3, 4
@@ -33,12 +37,13 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile ring_oracle.c into oracle/_build/liboracle.so (gcc, no fast-math)."""
+    if OVERRIDE:
+        return LIB
     os.makedirs(os.path.dirname(LIB), exist_ok=True)
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
         return LIB
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-           "-Wall", "-Wextra", "-o", tmp, SRC]
+    cmd = ["gcc"] + CFLAGS + ["-o", tmp, SRC]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

@@ -109,3 +109,51 @@ def test_exact_when_every_block_spans_127(oracle_mod, dtype, op):
     for r in range(N):
         np.testing.assert_array_equal(out[r], want)
         assert not np.any(e[r])
+
+
+def test_threshold_error_feedback_cycle_constant_gradient(oracle_mod):
+    """The error accumulator under a constant gradient (the pages' exercise on
+    e_t's steady state, with g = 0.25 so every value is exact in binary).  The
+    greedy compressor sends 1 when g + e >= 0.5 (Collective Communication,
+    Table 3: only values >= 0.5 are sent), so by hand: u = 0.25, 0.5, -0.25, 0,
+    then the cycle repeats -- one 1 every four steps, the long-run average of
+    what is sent equals g, and the residual stays in [-0.5, 0.5)."""
+    e = [np.zeros(1, np.float32)]
+    sent, res = [], []
+    for _ in range(12):
+        out, e = oracle_mod.allreduce_compressed([np.array([0.25], np.float32)], e, "sum", "threshold", 0, 0.5)
+        sent.append(float(out[0][0]))
+        res.append(float(e[0][0]))
+    assert sent == [0.0, 1.0, 0.0, 0.0] * 3
+    assert res == [0.25, -0.5, -0.25, 0.0] * 3
+    assert sum(sent) / len(sent) == 0.25
+
+
+def test_int8_rounds_ties_to_even(oracle_mod):
+    """Blockwise INT8 takes q = round(u / s) with ties to even (the IEEE
+    default rounding).  With max|u| = 127 the scale is exactly 1, so each
+    u = k + 1/2 sits on a tie and v must be numpy's rint(u)."""
+    halves = np.array([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 10.5, 11.5, -126.5, 125.5], np.float32)
+    u = np.zeros(128, np.float32)
+    u[0] = 127.0
+    u[1:1 + halves.size] = halves
+    out, e = oracle_mod.allreduce_compressed([u], [np.zeros(128, np.float32)], "sum", "int8_block", 128, 0.0)
+    v = out[0]
+    np.testing.assert_array_equal(v[1:1 + halves.size], np.rint(halves))
+    np.testing.assert_array_equal(np.signbit(v[1:1 + halves.size]), np.signbit(np.rint(halves)))
+    np.testing.assert_array_equal(e[0], u - v)
+    assert v[0] == 127.0
+
+
+def test_int8_nan_in_a_block_poisons_only_that_block(oracle_mod):
+    """A NaN anywhere in a block makes that block's scale NaN, so every value
+    it sends and every residual it keeps is NaN; the next block is untouched
+    (the reading of s = max|u| / 127 when the block holds a NaN)."""
+    g = W.normal_fp32(1, 256, seed_base=3)[0]
+    g[5] = np.float32("nan")
+    out, e = oracle_mod.allreduce_compressed([g], [np.zeros(256, np.float32)], "sum", "int8_block", 128, 0.0)
+    assert np.isnan(out[0][:128]).all() and np.isnan(e[0][:128]).all()
+    assert not np.isnan(out[0][128:]).any() and not np.isnan(e[0][128:]).any()
+    clean, _ = oracle_mod.allreduce_compressed([g[128:].copy()], [np.zeros(128, np.float32)], "sum", "int8_block",
+                                               128, 0.0)
+    np.testing.assert_array_equal(out[0][128:], clean[0])

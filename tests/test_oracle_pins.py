@@ -348,6 +348,23 @@ def test_prod_exact_on_powers_of_two(oracle_mod):
     np.testing.assert_array_equal(outb[0], W.to_bf16_bits(np.prod(x.astype(np.float64), axis=0).astype(np.float32)))
 
 
+@pytest.mark.parametrize("N", [3, 5, 6, 7])
+def test_avg_is_the_correctly_rounded_quotient(oracle_mod, N):
+    """AVG divides the finished sum once by N.  With integer inputs every ring
+    partial sum is exact, so the result must be the IEEE quotient S / N of the
+    exact sum, computed here by numpy's float32 division.  For N not a power
+    of two that differs from S * (1/N) for many S; the inputs include such S."""
+    K = 4000
+    x = [np.random.Generator(np.random.PCG64(N * 100 + r)).integers(-300, 300, size=K).astype(np.float32)
+         for r in range(N)]
+    S = np.sum(np.stack(x).astype(np.float64), axis=0).astype(np.float32)  # exact: |S| < 2^24
+    want = S / np.float32(N)
+    assert (want != S * (np.float32(1) / np.float32(N))).any()
+    outs, _ = oracle_mod.ring_allreduce(x, "avg")
+    for r in range(N):
+        np.testing.assert_array_equal(outs[r].view(np.uint32), want.view(np.uint32))
+
+
 def test_avg_power_of_two_is_scaled_sum(oracle_mod):
     """For N = 8, dividing by 8 is an exact exponent shift (barring
     subnormals), so AVG equals the SUM result times 2^-3."""
