@@ -95,12 +95,27 @@ def _run_pins(so):
                           + PINS, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
 
 
-def test_unmutated_copy_passes_every_pin(tmp_path):
-    res = _run_pins(_build_copy(tmp_path, "clean"))
+@pytest.fixture(scope="module")
+def runs(tmp_path_factory):
+    """Build every copy, then run the pin suites against all of them at once
+    (independent child processes); each test below reads its own result."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    tmp = tmp_path_factory.mktemp("mutants")
+    libs = {"clean": _build_copy(tmp, "clean")}
+    for name, snippet, repl in MUTANTS:
+        libs[name] = _build_copy(tmp, name, snippet, repl)
+    with ThreadPoolExecutor(max_workers=max(2, min(8, os.cpu_count() or 2))) as ex:
+        futs = {name: ex.submit(_run_pins, so) for name, so in libs.items()}
+        return {name: f.result() for name, f in futs.items()}
+
+
+def test_unmutated_copy_passes_every_pin(runs):
+    res = runs["clean"]
     assert res.returncode == 0, res.stdout[-3000:] + res.stderr[-2000:]
 
 
-@pytest.mark.parametrize("name,snippet,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_planted_mistake_is_caught(tmp_path, name, snippet, repl):
-    res = _run_pins(_build_copy(tmp_path, name, snippet, repl))
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(runs, name):
+    res = runs[name]
     assert res.returncode == 1, "mutant %s passed every pin:\n%s" % (name, res.stdout[-2000:])
