@@ -289,9 +289,16 @@ static cudaError_t launch_fanout_t(const void *const *src, int nchunks, void *co
     p.vec_aligned = aligned ? 1 : 0;
     const uint64_t te = (uint64_t)kThreads * 2 * VEC;
     uint64_t tiles = (p.part.q + 1 + te - 1) / te;
-    const uint64_t per_tile = (uint64_t)(kThreads / 32) * 31; // ragged chunks: 31 vectors per warp
+    // A chunk whose offset is not a whole vector takes the shuffle path (31
+    // vectors per warp) and needs about twice as many tiles; size the grid for
+    // it only when such a chunk exists, or the aligned chunks launch as many
+    // empty CTAs as working ones.
+    bool ragged = false;
+    for (int c = 1; c < nchunks && aligned && !ragged; ++c)
+        ragged = p.part.off((uint32_t)c) % VEC != 0;
+    const uint64_t per_tile = (uint64_t)(kThreads / 32) * 31;
     const uint64_t shifted = ((p.part.q + 1) / VEC + per_tile) / per_tile + 1;
-    if (nchunks > 1 && shifted > tiles)
+    if (ragged && shifted > tiles)
         tiles = shifted;
     if (tiles > 0x7fffffffull)
         return cudaErrorInvalidValue;
