@@ -265,7 +265,13 @@ static cudaError_t launch_t(const void *const *send, void *const *recv, int nran
     p.n_f = (float)nranks;
     const uint64_t te = (uint64_t)kThreads * U * VEC;
     uint64_t tiles = (p.part.q + 1 + te - 1) / te;
-    if (write_mode == WRITE_CHUNK) { // ragged chunks may take the shifted path: 31 vectors per warp
+    // ReduceScatter chunks at offsets that are not whole vectors take the
+    // shifted path (31 vectors per warp, about twice the tiles); size the grid
+    // for it only when such a chunk exists
+    bool ragged = false;
+    for (int c = 1; c < nranks && write_mode == WRITE_CHUNK && aligned && !ragged; ++c)
+        ragged = p.part.off((uint32_t)c) % VEC != 0;
+    if (ragged) {
         const uint64_t per_tile = (uint64_t)(kThreads / 32) * 31;
         const uint64_t shifted = ((p.part.q + 1) / VEC + per_tile) / per_tile + 1;
         if (shifted > tiles)
