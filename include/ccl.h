@@ -47,6 +47,15 @@
  *     launch).  CCL_MODE_STEP executes the ring's 2(N-1) steps one launch per
  *     step, in stream order, for validating the schedule; it gives identical
  *     bits and is slower.
+ *   - CUDA graphs.  Fused-mode collectives, ccl_allreduce_algo,
+ *     ccl_allreduce_compressed and ccl_check_identical enqueue only kernels
+ *     whose arguments travel by value and allocate nothing, so they may be
+ *     captured; a graph replays them on the pointers it was captured with.
+ *     ccl_allreduce_compressed sets up its kernel (shared-memory opt-in) on
+ *     its first call on a device: make that call before capturing.  Step
+ *     mode is not capturable: step-mode ReduceScatter and bucket AllReduce
+ *     use a library-cached device workspace that a first or larger call
+ *     allocates (and frees the old one).  ccl_allreduce_host refuses capture.
  */
 #ifndef CCL_H
 #define CCL_H

@@ -22,6 +22,9 @@
 // registers.  Then each
 // lane folds its elements over the ranks in ring order with two statically
 // unrolled passes (ranks c..N-1, then 0..c-1).  Up to 16 ranks.
+#include <mutex>
+#include <unordered_map>
+
 #include "ccl_internal.h"
 
 namespace ccl {
@@ -454,28 +457,50 @@ __global__ void __launch_bounds__(kThreads) compressed_pipe_kernel(const __grid_
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// The pipelined kernel needs more than 48 KB of dynamic shared memory, which
+// is opted into per kernel and per device; the persistent grid is one full
+// wave on that device.  Both are worked out once per (kernel, device).
+struct PipeConfig {
+    bool ready = false;
+    int ctas = 0; // SMs x resident CTAs per SM
+};
+static std::mutex g_pipe_cfg_mu;
+
+template <int DT, int EPL>
+static cudaError_t pipe_grid(int *ctas)
+{
+    using Lay = PipeLayout<DT, EPL>;
+    static std::unordered_map<int, PipeConfig> cfg; // per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_pipe_cfg_mu);
+    PipeConfig &c = cfg[dev];
+    if (!c.ready) {
+        int sms = 0, per_sm = 0;
+        if ((e = cudaFuncSetAttribute(compressed_pipe_kernel<DT, EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)Lay::kBytes)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compressed_pipe_kernel<DT, EPL>, kThreads,
+                                                               Lay::kBytes)) != cudaSuccess)
+            return e;
+        c.ctas = sms * (per_sm > 0 ? per_sm : 1);
+        c.ready = true;
+    }
+    *ctas = c.ctas;
+    return cudaSuccess;
+}
+
 template <int DT, int EPL>
 static cudaError_t launch_pipe_t(const CompParams &p, cudaStream_t stream)
 {
     using Lay = PipeLayout<DT, EPL>;
-    static bool configured = false; // the attribute is per kernel, set once per process
-    static int per_sm = 1, sms = 0;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(compressed_pipe_kernel<DT, EPL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::kBytes);
-        if (e != cudaSuccess)
-            return e;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compressed_pipe_kernel<DT, EPL>, kThreads,
-                                                      Lay::kBytes);
-        if (per_sm < 1)
-            per_sm = 1;
-        configured = true;
-    }
+    int ctas = 0;
+    if (cudaError_t e = pipe_grid<DT, EPL>(&ctas))
+        return e;
     const uint64_t ntiles = (p.nfull + Lay::kWarps - 1) / Lay::kWarps;
-    uint64_t grid = (uint64_t)sms * per_sm;
+    uint64_t grid = (uint64_t)ctas;
     if (grid > ntiles)
         grid = ntiles;
     if (grid == 0)

@@ -68,3 +68,58 @@ def test_graph_replay_alltoallv_and_buckets():
     for r in range(N):
         for t in range(len(numels)):
             assert_bits_equal(bits(grads[r][t]), wantb[r][t], "graph bucket r%d t%d" % (r, t))
+
+
+def test_graph_replay_rooted_collectives_orders_compressed_and_check():
+    """Reduce, Gather, Scatter, Broadcast, the other schedules' orders, the
+    compressed AllReduce (after one call outside the capture) and the result
+    check, all captured in one graph and replayed once."""
+    N, K, root = 6, 40_009, 4
+    x = list(W.mixed_bf16(N, K, seed_base=21))
+    _, ln = ccl.ccl_plan_chunks(K, N)
+    send = [to_dev(r) for r in x]
+    red = [None] * N
+    red[root] = torch.empty(K, dtype=torch.bfloat16, device=DEV)
+    parts = [send[r][:ln[r]].clone() for r in range(N)]
+    parts_h = [x[r][:ln[r]] for r in range(N)]
+    gat = [None] * N
+    gat[root] = torch.empty(K, dtype=torch.bfloat16, device=DEV)
+    sca = [torch.empty(ln[r], dtype=torch.bfloat16, device=DEV) for r in range(N)]
+    bc = [torch.empty(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    algo = {a: [to_dev(r) for r in x] for a in ("halving_doubling", "tree", "hierarchical")}
+    gq = W.normal_bf16(N, 8192 + 77, std=1e-2, seed_base=31)
+    grads = [to_dev(r) for r in gq]
+    res = [torch.zeros(gq.shape[1], dtype=torch.float32, device=DEV) for _ in range(N)]
+    warm_g = [to_dev(r) for r in gq]
+    warm_e = [torch.zeros(gq.shape[1], dtype=torch.float32, device=DEV) for _ in range(N)]
+    ccl.ccl_allreduce_compressed(warm_g, warm_e, op="avg", comp="int8_block", block=128)
+    mism = torch.zeros(1, dtype=torch.int64, device=DEV)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ccl.ccl_reduce(send, red, root=root, op="sum")
+        ccl.ccl_gather(parts, gat, root=root)
+        ccl.ccl_scatter(gat, sca, root=root)
+        ccl.ccl_broadcast(send, bc, root=root)
+        for a, bufs in algo.items():
+            ccl.ccl_allreduce_algo(bufs, op="sum", algo=a, group_size=3 if a == "hierarchical" else 0)
+        ccl.ccl_allreduce_compressed(grads, res, op="avg", comp="int8_block", block=128)
+        ccl.ccl_check_identical(algo["tree"], mism)
+    g.replay()
+    torch.cuda.synchronize()
+    want_red = oracle.reduce(x, root, "sum")
+    assert_bits_equal(bits(red[root]), want_red[root], "graph reduce")
+    want_g = oracle.gather(parts_h, K)
+    assert_bits_equal(bits(gat[root]), want_g, "graph gather")
+    for r in range(N):
+        assert_bits_equal(bits(sca[r]), parts_h[r], "graph scatter %d" % r)
+        assert_bits_equal(bits(bc[r]), x[root], "graph broadcast %d" % r)
+    for a, bufs in algo.items():
+        want = oracle.allreduce_algo(x, a, "sum", 3 if a == "hierarchical" else 0)
+        for r in (0, N - 1):
+            assert_bits_equal(bits(bufs[r]), want[r], "graph %s rank %d" % (a, r))
+    wq, we = oracle.allreduce_compressed(list(gq), [np.zeros(gq.shape[1], np.float32)] * N, "avg", "int8_block", 128)
+    for r in range(N):
+        assert_bits_equal(bits(grads[r]), wq[r], "graph compressed grads %d" % r)
+        assert_bits_equal(res[r].cpu().numpy().view(np.uint32), we[r].view(np.uint32), "graph residual %d" % r)
+    assert int(mism.item()) == 0
