@@ -56,6 +56,10 @@
  *     mode is not capturable: step-mode ReduceScatter and bucket AllReduce
  *     use a library-cached device workspace that a first or larger call
  *     allocates (and frees the old one).  ccl_allreduce_host refuses capture.
+ *   - That step-mode workspace is one per device, shared by every call:
+ *     step-mode ReduceScatter or bucket AllReduce calls whose work overlaps
+ *     on the GPU (different streams, different host threads) race on it and
+ *     must be serialised.  Fused calls share nothing.
  */
 #ifndef CCL_H
 #define CCL_H
