@@ -365,6 +365,30 @@ def test_avg_is_the_correctly_rounded_quotient(oracle_mod, N):
         np.testing.assert_array_equal(outs[r].view(np.uint32), want.view(np.uint32))
 
 
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "prod", "avg"])
+@pytest.mark.parametrize("N,L", [(3, 7), (4, 16), (5, 3), (8, 9)])
+def test_ring_order_is_rotation_equivariant(oracle_mod, dtype, op, N, L):
+    """Chunk c is folded starting at rank c, so relabelling ranks and chunks by
+    one step moves the result by one chunk: with x'_r[chunk c] =
+    x_{r+1}[chunk c+1], AR(x')[chunk c] = AR(x)[chunk c+1] bit for bit (equal
+    chunks of L elements, indices mod N).  An order whose start does not
+    follow the chunk index breaks this for rounded, non-associative sums."""
+    K = N * L
+    x = _inputs(dtype, N, K, seed=N * 31 + L)
+    xp = []
+    for r in range(N):
+        row = np.empty_like(x[r])
+        for c in range(N):
+            row[c * L:(c + 1) * L] = x[(r + 1) % N][((c + 1) % N) * L:((c + 1) % N + 1) * L]
+        xp.append(row)
+    y, _ = oracle_mod.ring_allreduce(x, op)
+    yp, _ = oracle_mod.ring_allreduce(xp, op)
+    for c in range(N):
+        d = (c + 1) % N
+        np.testing.assert_array_equal(_bits(yp[0][c * L:(c + 1) * L]), _bits(y[0][d * L:(d + 1) * L]))
+
+
 def test_avg_power_of_two_is_scaled_sum(oracle_mod):
     """For N = 8, dividing by 8 is an exact exponent shift (barring
     subnormals), so AVG equals the SUM result times 2^-3."""
