@@ -182,9 +182,10 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
         // The chunk lands at an offset that is not a whole vector (ragged
         // partition).  Lanes load aligned source vectors; each aligned
         // destination vector is the window s0 elements into two neighbouring
-        // lanes' vectors, exchanged with a shuffle.  A warp loads 32 source
-        // vectors and writes 31 destination vectors to every rank.
-        constexpr int WARPS = kThreads / 32;
+        // source vectors, exchanged with a shuffle (lane 31 loads the one
+        // after its own).  A warp writes 32 destination vectors that start on
+        // a multiple of 32 vectors, so every warp store covers whole 512-byte
+        // blocks (3 % faster than windows at arbitrary starts).
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const uint64_t vb = (off + VEC - 1) / VEC, ve = (off + len) / VEC;
         const int s0 = (int)(vb * VEC - off); // 0 < s0 < VEC
@@ -202,30 +203,37 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
                         st_elem<DT>(p.dst[q], d, v);
                 }
         }
-        const uint64_t i0 = ((uint64_t)t * WARPS + warp) * 31; // this warp's first destination vector (from vb)
-        if (vb >= ve || i0 >= ve - vb)
-            return; // whole warp
-        const uint64_t b = i0 + lane; // source vector
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if ((b + 1) * VEC <= len) {
-            x = ld16(static_cast<const char *>(src) + b * 16);
-        } else {
+        if (vb >= ve)
+            return;
+        // this lane's destination vector; whole warps past the end leave together
+        const uint64_t v = (vb / 32 + (uint64_t)t * (kThreads / 32) + warp) * 32 + lane;
+        if (v - lane >= ve)
+            return;
+        // source vector b feeds destination vectors vb + b - 1 and vb + b
+        auto load_src = [&](int64_t b) -> uint4 {
+            if (b < 0)
+                return make_uint4(0, 0, 0, 0);
+            if ((uint64_t)(b + 1) * VEC <= len)
+                return ld16(static_cast<const char *>(src) + (uint64_t)b * 16);
             uint32_t h[VEC];
 #pragma unroll
             for (int k = 0; k < VEC; ++k)
-                h[k] = b * VEC + k < len ? ld_elem<DT>(src, b * VEC + k) : 0u;
+                h[k] = (uint64_t)b * VEC + k < len ? ld_elem<DT>(src, (uint64_t)b * VEC + k) : 0u;
             if (DT == DT_FP32)
-                x = make_uint4(h[0], h[1], h[2], h[3]);
-            else
-                x = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
-        }
+                return make_uint4(h[0], h[1], h[2], h[3]);
+            return make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+        };
+        const int64_t b = (int64_t)v - (int64_t)vb;
+        const uint4 x = load_src(b);
+        const uint4 next = lane == 31 ? load_src(b + 1) : make_uint4(0, 0, 0, 0);
         uint4 nx;
         nx.x = __shfl_down_sync(0xffffffffu, x.x, 1);
         nx.y = __shfl_down_sync(0xffffffffu, x.y, 1);
         nx.z = __shfl_down_sync(0xffffffffu, x.z, 1);
         nx.w = __shfl_down_sync(0xffffffffu, x.w, 1);
-        const uint64_t v = vb + i0 + lane; // destination vector
-        if (lane < 31 && v < ve) {
+        if (lane == 31)
+            nx = next;
+        if (v >= vb && v < ve) {
             const uint4 w = shift_window<DT>(x, nx, s0);
             for (int q = 0; q < M; ++q)
                 st16(static_cast<char *>(p.dst[q]) + v * 16, w);
@@ -289,15 +297,17 @@ static cudaError_t launch_fanout_t(const void *const *src, int nchunks, void *co
     p.vec_aligned = aligned ? 1 : 0;
     const uint64_t te = (uint64_t)kThreads * 2 * VEC;
     uint64_t tiles = (p.part.q + 1 + te - 1) / te;
-    // A chunk whose offset is not a whole vector takes the shuffle path (31
-    // vectors per warp) and needs about twice as many tiles; size the grid for
+    // A chunk whose offset is not a whole vector takes the shuffle path (one
+    // vector per thread) and needs about twice as many tiles; size the grid for
     // it only when such a chunk exists, or the aligned chunks launch as many
     // empty CTAs as working ones.
     bool ragged = false;
     for (int c = 1; c < nchunks && aligned && !ragged; ++c)
         ragged = p.part.off((uint32_t)c) % VEC != 0;
-    const uint64_t per_tile = (uint64_t)(kThreads / 32) * 31;
-    const uint64_t shifted = ((p.part.q + 1) / VEC + per_tile) / per_tile + 1;
+    // ragged path: kThreads destination vectors per tile, the first block
+    // starting up to 31 vectors before the chunk
+    const uint64_t per_tile = (uint64_t)kThreads;
+    const uint64_t shifted = ((p.part.q + 1) / VEC + 31 + per_tile) / per_tile + 1;
     if (ragged && shifted > tiles)
         tiles = shifted;
     if (tiles > 0x7fffffffull)
