@@ -108,6 +108,61 @@ __device__ __forceinline__ void reduce_scatter_shifted(const FusedParams<MAXR> &
         st16(static_cast<char *>(p.recv[c]) + j * 16, shift_window<DT>(r, nx, d));
 }
 
+// Many ranks, short chunks.  The paths below walk the ranks in groups, one
+// round trip to memory per group, so a call's time grows with N even for a
+// few elements per chunk.  Here one CTA per chunk first loads every rank's
+// copy of its chunk into shared memory -- all N x len loads in flight at once --
+// then folds each element from shared memory in ring order (the same hops,
+// the same bits) and writes the results with independent stores.
+constexpr uint64_t kSmallChunkMax = 64;           // elements per chunk
+constexpr size_t kSmallChunkSmem = 48 * 1024;     // the default dynamic shared-memory limit
+
+template <int DT, int OP, int MAXR>
+__global__ void __launch_bounds__(kThreads) small_chunk_kernel(const __grid_constant__ FusedParams<MAXR> p)
+{
+    extern __shared__ uint32_t sx[]; // [N][L] input bits, then [L] results
+    const int N = p.nranks;
+    const uint32_t c = blockIdx.x;
+    const uint64_t off = p.part.off(c);
+    const int L = (int)p.part.len(c);
+    if (L == 0)
+        return;
+    for (int i = threadIdx.x; i < N * L; i += kThreads) {
+        const int r = i / L;
+        sx[i] = ld_elem<DT>(p.send[r], off + (uint64_t)(i - r * L));
+    }
+    __syncthreads();
+    uint32_t *res = sx + (size_t)N * L;
+    for (int e = threadIdx.x; e < L; e += kThreads) {
+        // the ring order c, c+1, ..., N-1, 0, ..., c-1 as two linear runs, so
+        // that unrolled reads of shared memory run ahead of the dependent hops
+        uint32_t acc = sx[(int)c * L + e];
+#pragma unroll 8
+        for (int r = (int)c + 1; r < N; ++r)
+            acc = hop_elem<DT, OP>(sx[r * L + e], acc);
+#pragma unroll 8
+        for (int r = 0; r < (int)c; ++r)
+            acc = hop_elem<DT, OP>(sx[r * L + e], acc);
+        if (OP == OP_AVG)
+            acc = avg_elem<DT>(acc, p.n_f);
+        res[e] = acc;
+    }
+    __syncthreads();
+    if (p.write_mode == WRITE_ALL) {
+        for (int i = threadIdx.x; i < N * L; i += kThreads) {
+            const int r = i / L, e = i - r * L;
+            st_elem<DT>(p.recv[r], off + (uint64_t)e, res[e]);
+        }
+    } else {
+        for (int e = threadIdx.x; e < L; e += kThreads) {
+            if (p.write_mode == WRITE_ROOT)
+                st_elem<DT>(p.recv[p.root], off + (uint64_t)e, res[e]);
+            else
+                st_elem<DT>(p.recv[c], (uint64_t)e, res[e]);
+        }
+    }
+}
+
 template <int DT, int OP, int NR, int MAXR>
 __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_constant__ FusedParams<MAXR> p)
 {
@@ -263,6 +318,16 @@ static cudaError_t launch_t(const void *const *send, void *const *recv, int nran
     p.root = root;
     p.vec_aligned = aligned ? 1 : 0;
     p.n_f = (float)nranks;
+    if (NR == 0 && nranks > kSmallRanks) {
+        const uint64_t lmax = p.part.q + (p.part.rem ? 1 : 0);
+        const size_t smem = ((size_t)nranks + 1) * (size_t)lmax * sizeof(uint32_t);
+        if (lmax <= kSmallChunkMax && smem <= kSmallChunkSmem) {
+            p.tiles = 1;
+            small_chunk_kernel<DT, OP, MAXR><<<(unsigned)nranks, kThreads, smem, stream>>>(p);
+            count_launches(1);
+            return cudaGetLastError();
+        }
+    }
     const uint64_t te = (uint64_t)kThreads * U * VEC;
     uint64_t tiles = (p.part.q + 1 + te - 1) / te;
     // ReduceScatter chunks at offsets that are not whole vectors take the
