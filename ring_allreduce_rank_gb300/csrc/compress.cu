@@ -238,15 +238,31 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
         for (int r = 0; r < NMAX; ++r) {
             const float s = sc[r];
             const bool fast = s > 0.0f && inv[r] < __uint_as_float(0x7f800000u); // warp-uniform
+            float q[EPL];
+            if (fast) {
+                // q = round(u * (1/s)) unless some element of the lane lies
+                // within 2^-14 of a tie; then the lane takes the exact
+                // quotient for all of them (see quantize_fast)
+                float worst = 0.0f;
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) {
+                    const float t = __fmul_rn(v[r][j], inv[r]);
+                    q[j] = rintf(t);
+                    worst = fmaxf(worst, fabsf(t - q[j]));
+                }
+                if (worst > 0.49993896484375f)
+#pragma unroll
+                    for (int j = 0; j < EPL; ++j)
+                        q[j] = rintf(__fdiv_rn(v[r][j], s));
+            } else {
+#pragma unroll
+                for (int j = 0; j < EPL; ++j)
+                    q[j] = s > 0.0f ? rintf(__fdiv_rn(v[r][j], s)) : (s == 0.0f ? 0.0f : s);
+            }
 #pragma unroll
             for (int j = 0; j < EPL; ++j) {
                 const float u = v[r][j];
-                float q;
-                if (fast)
-                    q = quantize_fast(u, s, inv[r]);
-                else
-                    q = s > 0.0f ? rintf(__fdiv_rn(u, s)) : (s == 0.0f ? 0.0f : s);
-                v[r][j] = __fmul_rn(q, s);
+                v[r][j] = __fmul_rn(q[j], s);
                 ee[r][j] = __fsub_rn(u, v[r][j]);
             }
         }
@@ -257,32 +273,40 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
             store_f<EPL>(p.res[r], i0, valid, vec, ee[r]);
 
     // ring-order fold in fp32: chunk c from rank c, then c+1, ..., c-1
-    uint32_t c = valid > 0 ? chunk_of<NMAX>(p, i0) : 0u;
-    uint32_t outb[EPL];
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-        while (c + 1 < (uint32_t)N && i0 + j >= p.coff[c + 1])
-            ++c;
-        float acc;
-        if (N == NMAX) {
-            // every rank present: one static fold per rotation start (the start
-            // is the same across the warp except at a chunk boundary)
-            switch (c) {
+    const uint32_t c0 = valid > 0 ? chunk_of<NMAX>(p, i0) : 0u;
+    // all of the lane's elements in chunk c0 (the rule; a chunk boundary inside
+    // a lane is the exception)
+    const bool one_chunk = valid == 0 || c0 + 1 >= (uint32_t)N || i0 + (uint64_t)(valid - 1) < p.coff[c0 + 1];
+    float accv[EPL];
+    if (N == NMAX && one_chunk) {
+        // every rank present: one static fold per rotation start, for all of
+        // the lane's elements at once
+        switch (c0) {
 #define CCL_FOLD_CASE(C)                                                                                           \
     case C:                                                                                                            \
-        acc = v[C % NMAX][j];                                                                                          \
-        _Pragma("unroll") for (int k = 1; k < NMAX; ++k) acc = __fadd_rn(v[(C + k) % NMAX][j], acc);                   \
+        _Pragma("unroll") for (int j = 0; j < EPL; ++j) {                                                              \
+            float a = v[C % NMAX][j];                                                                                  \
+            _Pragma("unroll") for (int k = 1; k < NMAX; ++k) a = __fadd_rn(v[(C + k) % NMAX][j], a);                  \
+            accv[j] = a;                                                                                               \
+        }                                                                                                              \
         break;
-                CCL_FOLD_CASE(0) CCL_FOLD_CASE(1) CCL_FOLD_CASE(2) CCL_FOLD_CASE(3)
-                CCL_FOLD_CASE(4) CCL_FOLD_CASE(5) CCL_FOLD_CASE(6) CCL_FOLD_CASE(7)
-                CCL_FOLD_CASE(8) CCL_FOLD_CASE(9) CCL_FOLD_CASE(10) CCL_FOLD_CASE(11)
-                CCL_FOLD_CASE(12) CCL_FOLD_CASE(13) CCL_FOLD_CASE(14) CCL_FOLD_CASE(15)
+            CCL_FOLD_CASE(0) CCL_FOLD_CASE(1) CCL_FOLD_CASE(2) CCL_FOLD_CASE(3)
+            CCL_FOLD_CASE(4) CCL_FOLD_CASE(5) CCL_FOLD_CASE(6) CCL_FOLD_CASE(7)
+            CCL_FOLD_CASE(8) CCL_FOLD_CASE(9) CCL_FOLD_CASE(10) CCL_FOLD_CASE(11)
+            CCL_FOLD_CASE(12) CCL_FOLD_CASE(13) CCL_FOLD_CASE(14) CCL_FOLD_CASE(15)
 #undef CCL_FOLD_CASE
-            default:
-                acc = 0.0f;
-            }
-        } else {
-            acc = 0.0f;
+        default:
+#pragma unroll
+            for (int j = 0; j < EPL; ++j)
+                accv[j] = 0.0f;
+        }
+    } else {
+        uint32_t c = c0;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            while (c + 1 < (uint32_t)N && i0 + j >= p.coff[c + 1])
+                ++c;
+            float acc = 0.0f;
 #pragma unroll
             for (int r = 0; r < NMAX; ++r)
                 if (r < N && r >= (int)c)
@@ -291,7 +315,13 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
             for (int r = 0; r < NMAX; ++r)
                 if (r < (int)c)
                     acc = __fadd_rn(v[r][j], acc);
+            accv[j] = acc;
         }
+    }
+    uint32_t outb[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        float acc = accv[j];
         if (p.n_f > 0.0f) // AVG: x / N, or x * (1/N) when N is a power of two (the same rounded value)
             acc = p.pow2 ? __fmul_rn(acc, p.inv_n) : __fdiv_rn(acc, p.n_f);
         outb[j] = round_to<DT>(acc);

@@ -81,3 +81,52 @@ def test_compressed_special_values_and_unaligned(dtype):
     for r in range(N):
         assert_bits_equal(bits(grads[r]), want_g[r], "special grads rank %d" % r)
         assert_bits_equal(bits(res[r]), want_e[r], "special residual rank %d" % r)
+
+
+def _tie_blocks(dtype, n_blocks, seed):
+    """Gradients and residuals whose u = g + e sit exactly on, or within a few
+    ulps of, the half-integer ties of u / s (INT8, blocks of 128): the cases
+    where rounding u * (1/s) could differ from rounding the exact quotient."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    grads = np.zeros(n_blocks * 128, np.float32)
+    res = np.zeros(n_blocks * 128, np.float32)
+    for b in range(n_blocks):
+        blk = slice(b * 128, (b + 1) * 128)
+        k = g.integers(-126, 126, size=128).astype(np.float32)
+        if dtype == "bf16" or b % 2 == 0:
+            # max |u| = 127: the scale is exactly 1, k + 1/2 is a tie
+            vals = k + np.float32(0.5)
+            vals[0] = np.float32(127.0)
+            jitter = g.choice(np.array([0.0, 2.0 ** -12, -2.0 ** -12, 2.0 ** -20, -2.0 ** -20, 2.0 ** -16],
+                                       np.float32), size=128)
+            jitter[0] = 0.0
+            grads[blk] = vals
+            res[blk] = jitter
+        else:
+            top = np.float32(g.uniform(20.0, 300.0))
+            s = np.float32(top / np.float32(127.0))
+            vals = ((k + np.float32(0.5)) * s).astype(np.float32)
+            step = g.choice(np.array([-2, -1, 0, 1, 2]), size=128)
+            vals = np.nextafter(vals, np.where(step > 0, np.inf, -np.inf).astype(np.float32)) * (step != 0) + \
+                vals * (step == 0)
+            vals = vals.astype(np.float32)
+            vals[0] = top
+            grads[blk] = vals
+    if dtype == "bf16":
+        return W.to_bf16_bits(grads), res
+    return grads, res
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("N", [1, 3, 8])
+def test_compressed_ties_and_near_ties(dtype, N):
+    nb = 96
+    gs, rs = zip(*[_tie_blocks(dtype, nb, seed=17 * N + r) for r in range(N)])
+    want_g, want_e = oracle.allreduce_compressed(list(gs), list(rs), "sum", "int8_block", 128)
+    grads = [to_dev(x) for x in gs]
+    res = [torch.from_numpy(e.copy()).to(DEV) for e in rs]
+    ccl.ccl_allreduce_compressed(grads, res, op="sum", comp="int8_block", block=128)
+    torch.cuda.synchronize()
+    for r in range(N):
+        assert_bits_equal(bits(grads[r]), want_g[r], "ties grads rank %d" % r)
+        assert_bits_equal(bits(res[r]), want_e[r], "ties residual rank %d" % r)
