@@ -203,14 +203,19 @@ def _timed(torch, ccl, step, steps, warmup, stream, dev):
         step()
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n0 = ccl.ccl_launch_count()
+    t0.record(stream)
     for a, b in ev:
         a.record(stream)
         step()
         b.record(stream)
+    t1.record(stream)
     torch.cuda.synchronize(dev)
     per = [a.elapsed_time(b) for a, b in ev]
-    return sum(per), per, ccl.ccl_launch_count() - n0
+    # whole-run time of the back-to-back steps (the line's value), and each
+    # launch's own duration (the roofline's achieved bandwidth)
+    return t0.elapsed_time(t1), per, ccl.ccl_launch_count() - n0
 
 
 def graph_call_seconds(torch, ccl, call, nbytes, dev) -> float:
@@ -264,15 +269,19 @@ def run_row(args, name, local):
     def randn_bf16(n):
         return (torch.randn(n, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
 
-    def line(metric, alg, per_ms, launches, kernel, dtype, config, extra=None):
-        tot = sum(per_ms)
+    def line(metric, alg, per_ms, launches, kernel, dtype, config, extra=None, total_ms=None):
+        """value: whole-run throughput (total_ms over the back-to-back steps,
+        else the sum of the per-launch times); roofline.achieved: algorithmic
+        bytes over the average per-launch time."""
+        tot = total_ms if total_ms is not None else sum(per_ms)
         val = alg * len(per_ms) / (tot / 1e3) / 1e9
+        ach = alg * len(per_ms) / (sum(per_ms) / 1e3) / 1e9
         d = {"metric": metric, "value": round(val, 2), "unit": UNIT, "n_gpus": 1, "steps": len(per_ms),
              "warmup": max(args.warmup, 3), "ms_per_step": round(tot / len(per_ms), 5), "higher_is_better": True,
              "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
              "config": dict(config, workload=ROWS[name]),
-             "roofline": {"bound": "hbm", "achieved": round(val, 1), "peak": peak, "unit": "GB/s",
-                          "frac": round(val / peak, 4), "traffic": None, "algorithmic_bytes_per_step": alg,
+             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(ach / peak, 4), "traffic": None, "algorithmic_bytes_per_step": alg,
                           "peak_source": peak_src, "kernel": kernel},
              "cpu_baseline": None, "e2e": None, "gpu_launches": int(launches)}
         if extra:
@@ -317,7 +326,7 @@ def run_row(args, name, local):
         kernel = "hier_order_kernel<bf16, AVG, L=4>" if algo == "hierarchical" else "tree_order_kernel<bf16, AVG, 8>"
         print(json.dumps(line("AllReduce (%s order) HBM GB/s, N=8 bf16 128 MB/rank, 1 GB300" % algo, 2 * N * K * 2,
                               per, launches, kernel, "bf16", {"nranks": N, "count": K, "algo": algo},
-                              {"clocks": clk})))
+                              {"clocks": clk}, total_ms=tot)))
         return
 
     if name == "overlap":
@@ -406,7 +415,7 @@ def run_row(args, name, local):
         alg = N * K * (2 + 4 + 4 + 2)  # gradients read and written, residuals read and written
         print(json.dumps(line("Compressed AllReduce (INT8 blocks + error feedback) HBM GB/s, N=8 bf16 128 MB/rank, "
                               "1 GB300", alg, per, launches, "compressed_allreduce_kernel<bf16, 4, 8>", "bf16",
-                              {"nranks": N, "count": K, "block": 128}, {"clocks": clk})))
+                              {"nranks": N, "count": K, "block": 128}, {"clocks": clk}, total_ms=tot)))
         return
 
     if name in ("allreduce-step", "broadcast"):
@@ -426,7 +435,7 @@ def run_row(args, name, local):
         tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
         clk = clocks.stop()
         print(json.dumps(line(metric, alg, per, launches, kernel, "bf16", {"nranks": N, "count": K},
-                              {"clocks": clk})))
+                              {"clocks": clk}, total_ms=tot)))
         return
 
     if name in ("reduce", "gather", "scatter"):
@@ -459,7 +468,7 @@ def run_row(args, name, local):
         tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
         clk = clocks.stop()
         print(json.dumps(line(metric, alg, per, launches, kernel, "bf16", {"nranks": N, "count": K},
-                              {"clocks": clk})))
+                              {"clocks": clk}, total_ms=tot)))
         return
 
     if name in ("reduce-scatter", "allgather"):
@@ -479,7 +488,7 @@ def run_row(args, name, local):
         tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
         clk = clocks.stop()
         print(json.dumps(line(metric, alg, per, launches, kernel, "fp32", {"nranks": N, "count": K},
-                              {"clocks": clk})))
+                              {"clocks": clk}, total_ms=tot)))
         return
 
     if name == "alltoallv":
@@ -496,7 +505,7 @@ def run_row(args, name, local):
         print(json.dumps(line("AllToAllv HBM GB/s, N=8 MoE dispatch 4096x7168 bf16/rank, 1 GB300", alg, per,
                               launches, "copy_segments_kernel (64 blocks)", "bf16",
                               {"nranks": N, "tokens": T, "hidden": H, "max_recv_tokens": int(counts.sum(0).max() // H)},
-                              {"clocks": clk})))
+                              {"clocks": clk}, total_ms=tot)))
         return
 
     if name == "bucket":
@@ -510,7 +519,7 @@ def run_row(args, name, local):
         clk = clocks.stop()
         print(json.dumps(line("Bucket-fused AllReduce HBM GB/s, N=8 bf16 4 Llama layers (1.62 GB/rank), 25 MiB "
                               "buckets, 1 GB300", alg, per, launches, "bucket_reduce_kernel<bf16, SUM, 8>", "bf16",
-                              {"nranks": N, "tensors": len(numels), "buckets": 62}, {"clocks": clk})))
+                              {"nranks": N, "tensors": len(numels), "buckets": 62}, {"clocks": clk}, total_ms=tot)))
         return
     raise SystemExit("unknown workload %s" % name)
 

@@ -135,7 +135,11 @@ static cudaError_t launch_copy_batch(const CopySeg *segs, size_t nseg, cudaStrea
     return cudaGetLastError();
 }
 
+// Parameter-block tiers: every launch carries its segment table, and a 32 KB
+// block costs the GPU's front end microseconds per launch (AllToAllv over 8
+// ranks, 64 segments: 140 us per call with the large block, 135 in a graph)
 constexpr size_t kCopySegsSmall = 16;
+constexpr size_t kCopySegsMid = 128;    // 4 KB: AllToAll(v) up to 11 ranks
 constexpr size_t kCopySegsLarge = 1000; // 32 KB of kernel parameters
 
 cudaError_t launch_copy_segments(const CopySeg *segs, size_t nseg, cudaStream_t stream)
@@ -149,6 +153,7 @@ cudaError_t launch_copy_segments(const CopySeg *segs, size_t nseg, cudaStream_t 
     while (i < live.size()) {
         const size_t n = std::min(kCopySegsLarge, live.size() - i);
         cudaError_t e = n <= kCopySegsSmall ? launch_copy_batch<kCopySegsSmall>(live.data() + i, n, stream)
+                        : n <= kCopySegsMid ? launch_copy_batch<kCopySegsMid>(live.data() + i, n, stream)
                                             : launch_copy_batch<kCopySegsLarge>(live.data() + i, n, stream);
         if (e != cudaSuccess)
             return e;
