@@ -153,26 +153,54 @@ def job_gbs(world: int, bytes_per_step: int, steps: int, ms: float) -> float:
 
 # ------------------------------------------------------------------ oracle timing (CPU)
 
-def oracle_sample_gbs(target_s: float, max_count: int = COUNT):
-    """Time the CPU oracle (step-by-step ring simulation, single thread) on a
-    sample of the workload: N=8 ranks, the first k elements of each rank's
-    buffer, k sized from a short probe to take about target_s seconds.
-    Returns (GB/s, seconds, k)."""
+def oracle_sample_gbs(target_s: float, max_count: int = COUNT, threads: int = 1):
+    """Time the CPU oracle (step-by-step ring simulation) on a sample of the
+    workload: N=8 ranks, the first k elements of each rank's buffer, k sized
+    from a short probe to take about target_s seconds.  threads = 1: the
+    one-thread simulation; more: the ranks spread over that many threads with
+    a barrier per step (the same bits).  Returns (GB/s, seconds, k)."""
     import oracle
     from ring_allreduce_rank_gb300 import workloads as W
 
     oracle.build()
+
+    def run(x):
+        if threads > 1:
+            oracle.ring_allreduce_threads(x, "avg", threads)
+        else:
+            oracle.ring_allreduce(x, "avg")
+
     k = min(1 << 18, max_count)
     x = list(W.normal_bf16(NRANKS, k, std=1e-3, seed_base=0))
     t0 = time.perf_counter()
-    oracle.ring_allreduce(x, "avg")
+    run(x)
     dt = time.perf_counter() - t0
     k = int(min(max_count, max(1 << 12, k * target_s / max(dt, 1e-4)))) // 8 * 8
     x = list(W.normal_bf16(NRANKS, k, std=1e-3, seed_base=0))
     t0 = time.perf_counter()
-    oracle.ring_allreduce(x, "avg")
+    run(x)
     dt = time.perf_counter() - t0
     return 2 * NRANKS * k * ELEM / dt / 1e9, dt, k
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
 
 # ------------------------------------------------------------------ the other collectives' workloads
@@ -653,9 +681,15 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, dt, k = oracle_sample_gbs(target_s=12.0)
+        nt = max(1, min(NRANKS, os.cpu_count() or 1))
+        gbs_t, dt_t, k_t = oracle_sample_gbs(target_s=6.0, threads=nt)
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "N=8 bf16 AVG, first %d of %d elements per rank (%.1f s), step-by-step ring "
-                         "simulation in plain C, one thread" % (k, COUNT, dt)}
+                         "simulation in plain C, one thread" % (k, COUNT, dt),
+               "threaded": {"value": round(gbs_t, 4), "unit": UNIT, "cores": nt,
+                            "sample": "the same simulation with one thread per rank and a barrier per step, "
+                                      "first %d elements per rank (%.1f s)" % (k_t, dt_t)},
+               "cpu_model": cpu_model(), "host_cores": os.cpu_count()}
 
     if rank != 0:
         return

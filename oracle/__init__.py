@@ -25,7 +25,7 @@ SRC = os.path.join(HERE, "ring_oracle.c")
 # copies of ring_oracle.c with one planted mistake each)
 OVERRIDE = os.environ.get("ORACLE_LIB") or None
 LIB = OVERRIDE or os.path.join(HERE, "_build", "liboracle.so")
-CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall", "-Wextra"]
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread", "-Wall", "-Wextra"]
 
 FP32, BF16 = 0, 1
 SUM, AVG, MAX, PROD, MIN = 0, 1, 2, 3, 4
@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_ring_schedule.argtypes = [i32, ctypes.POINTER(ctypes.c_int32)]
             L.oracle_ring_schedule.restype = None
             L.oracle_ring_allreduce.argtypes = [pp, i32, u64, i32, i32, p64]
+            L.oracle_ring_allreduce_threads.argtypes = [pp, i32, u64, i32, i32, i32]
             L.oracle_ring_allreduce_closed.argtypes = [pp, pp, i32, u64, i32, i32]
             L.oracle_ring_allreduce_at.argtypes = [pp, i32, u64, i32, i32, p64, u64, vp]
             L.oracle_ring_allreduce_gathered.argtypes = [pp, i32, u64, i32, i32, p64, u64, vp]
@@ -161,6 +162,16 @@ def ring_allreduce(bufs, op="sum"):
     _check(lib().oracle_ring_allreduce(_ptrs(outs), N, K, _dtype_code(outs[0]), _op(op), sent),
            "oracle_ring_allreduce")
     return outs, list(sent)
+
+
+def ring_allreduce_threads(bufs, op="sum", threads: int = 0):
+    """The step-by-step ring with the ranks spread over `threads` threads (0:
+    one per rank) and a barrier per step; the same bits as ring_allreduce."""
+    outs = [np.array(b, copy=True, order="C") for b in bufs]
+    N, K = len(outs), outs[0].size
+    _check(lib().oracle_ring_allreduce_threads(_ptrs(outs), N, K, _dtype_code(outs[0]), _op(op), threads or N),
+           "oracle_ring_allreduce_threads")
+    return outs
 
 
 def ring_allreduce_closed(bufs, op="sum"):

@@ -29,6 +29,8 @@
  * Parity pins live in tests/test_oracle_*.py; see each function's comment for
  * which passage it follows.
  */
+#define _POSIX_C_SOURCE 200809L /* pthread barriers */
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -291,6 +293,133 @@ int oracle_ring_allreduce(void **buf, int N, uint64_t K, int dtype, int op, uint
     ag_phase_after_rs(buf, N, off, len, dtype, sent, snap, stride);
     free(off); free(len); free(snap);
     return OR_OK;
+}
+
+/* The same ring with the ranks spread over threads, for timing the CPU
+ * baseline on several cores (N rank-threads with a barrier per step).  Thread
+ * t owns ranks [r0, r1).  Every step is: all threads snapshot what their ranks
+ * send, a barrier, all threads apply what their ranks receive, a barrier --
+ * the operations of oracle_ring_allreduce in the same order for every
+ * element, so the bits are the same (pinned by a test). */
+typedef struct {
+    pthread_mutex_t mu;
+    pthread_cond_t cv;
+    int go; /* 0: wait, 1: run, -1: leave without running */
+} start_gate;
+
+typedef struct {
+    void **buf;
+    int N, dtype, op, r0, r1;
+    const uint64_t *off, *len;
+    char *snap;
+    uint64_t stride;
+    pthread_barrier_t *bar;
+    start_gate *gate;
+} ring_part;
+
+static void *ring_part_run(void *arg)
+{
+    const ring_part *p = (const ring_part *)arg;
+    const int N = p->N;
+    const size_t es = esize(p->dtype);
+    for (int s = 0; s < N - 1; ++s) { /* ReduceScatter phase */
+        for (int i = p->r0; i < p->r1; ++i) {
+            int c = mod((int64_t)i - s, N);
+            memcpy(p->snap + (size_t)i * p->stride * es, (char *)p->buf[i] + p->off[c] * es, p->len[c] * es);
+        }
+        pthread_barrier_wait(p->bar);
+        for (int i = p->r0; i < p->r1; ++i) {
+            int c = mod((int64_t)i - 1 - s, N);
+            const void *in = p->snap + (size_t)mod((int64_t)i - 1, N) * p->stride * es;
+            for (uint64_t e = 0; e < p->len[c]; ++e) {
+                uint64_t g = p->off[c] + e;
+                store(p->buf[i], p->dtype, g,
+                      hop(load(p->buf[i], p->dtype, g), load(in, p->dtype, e), p->dtype, p->op));
+            }
+        }
+        pthread_barrier_wait(p->bar);
+    }
+    if (p->op == OR_AVG)
+        for (int i = p->r0; i < p->r1; ++i) {
+            int c = mod((int64_t)i + 1, N);
+            for (uint64_t e = 0; e < p->len[c]; ++e)
+                store(p->buf[i], p->dtype, p->off[c] + e,
+                      avg_scale(load(p->buf[i], p->dtype, p->off[c] + e), N, p->dtype));
+        }
+    pthread_barrier_wait(p->bar);
+    for (int s = 0; s < N - 1; ++s) { /* AllGather phase */
+        for (int i = p->r0; i < p->r1; ++i) {
+            int c = mod((int64_t)i + 1 - s, N);
+            memcpy(p->snap + (size_t)i * p->stride * es, (char *)p->buf[i] + p->off[c] * es, p->len[c] * es);
+        }
+        pthread_barrier_wait(p->bar);
+        for (int i = p->r0; i < p->r1; ++i) {
+            int c = mod((int64_t)i - s, N);
+            memcpy((char *)p->buf[i] + p->off[c] * es, p->snap + (size_t)mod((int64_t)i - 1, N) * p->stride * es,
+                   p->len[c] * es);
+        }
+        pthread_barrier_wait(p->bar);
+    }
+    return NULL;
+}
+
+/* Helper threads wait at the gate until every thread exists, so that a failed
+ * pthread_create never leaves some of them waiting at the barrier. */
+static void *ring_part_gated(void *arg)
+{
+    const ring_part *p = (const ring_part *)arg;
+    pthread_mutex_lock(&p->gate->mu);
+    while (p->gate->go == 0)
+        pthread_cond_wait(&p->gate->cv, &p->gate->mu);
+    const int go = p->gate->go;
+    pthread_mutex_unlock(&p->gate->mu);
+    return go > 0 ? ring_part_run(arg) : NULL;
+}
+
+static void open_gate(start_gate *g, int go)
+{
+    pthread_mutex_lock(&g->mu);
+    g->go = go;
+    pthread_cond_broadcast(&g->cv);
+    pthread_mutex_unlock(&g->mu);
+}
+
+int oracle_ring_allreduce_threads(void **buf, int N, uint64_t K, int dtype, int op, int nthreads)
+{
+    if (bad_args(N, dtype, op) || nthreads < 1)
+        return OR_EINVAL;
+    if (nthreads > N)
+        nthreads = N;
+    uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
+    uint64_t stride = K / (uint64_t)N + 1;
+    char *snap = malloc((size_t)N * stride * esize(dtype));
+    ring_part *parts = malloc(sizeof(ring_part) * (size_t)nthreads);
+    pthread_t *th = malloc(sizeof(pthread_t) * (size_t)nthreads);
+    pthread_barrier_t bar;
+    start_gate gate = {PTHREAD_MUTEX_INITIALIZER, PTHREAD_COND_INITIALIZER, 0};
+    int started = 1;
+    if (!off || !len || !snap || !parts || !th || pthread_barrier_init(&bar, NULL, (unsigned)nthreads) != 0) {
+        free(off); free(len); free(snap); free(parts); free(th);
+        return OR_ENOMEM;
+    }
+    oracle_partition(K, N, off, len);
+    for (int t = 0; t < nthreads; ++t) {
+        ring_part q = {buf, N, dtype, op, (int)((int64_t)N * t / nthreads), (int)((int64_t)N * (t + 1) / nthreads),
+                       off, len, snap, stride, &bar, &gate};
+        parts[t] = q;
+    }
+    while (started < nthreads && pthread_create(&th[started], NULL, ring_part_gated, &parts[started]) == 0)
+        ++started;
+    const int all = started == nthreads;
+    open_gate(&gate, all ? 1 : -1);
+    if (all)
+        ring_part_run(&parts[0]); /* the calling thread is thread 0 */
+    for (int t = 1; t < started; ++t)
+        pthread_join(th[t], NULL);
+    pthread_barrier_destroy(&bar);
+    free(off); free(len); free(snap); free(parts); free(th);
+    /* not every thread could be started: the one-thread ring, the same bits */
+    return all ? OR_OK : oracle_ring_allreduce(buf, N, K, dtype, op, NULL);
 }
 
 /* Second, independent formulation (closed form).  Chunk c starts at rank c at

@@ -389,6 +389,19 @@ def test_ring_order_is_rotation_equivariant(oracle_mod, dtype, op, N, L):
         np.testing.assert_array_equal(_bits(yp[0][c * L:(c + 1) * L]), _bits(y[0][d * L:(d + 1) * L]))
 
 
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min"])
+@pytest.mark.parametrize("N,K,threads", [(8, 1000, 8), (8, 1001, 3), (5, 37, 2), (16, 517, 16), (3, 2, 3), (1, 9, 1)])
+def test_threaded_ring_equals_single_thread(oracle_mod, dtype, op, N, K, threads):
+    """The CPU baseline's multi-core form (ranks on threads, a barrier per
+    step) is the same computation: identical bits to the one-thread ring."""
+    x = _inputs(dtype, N, K, seed=N * 7 + K)
+    a, _ = oracle_mod.ring_allreduce(x, op)
+    b = oracle_mod.ring_allreduce_threads(x, op, threads)
+    for r in range(N):
+        np.testing.assert_array_equal(_bits(b[r]), _bits(a[r]))
+
+
 def test_avg_power_of_two_is_scaled_sum(oracle_mod):
     """For N = 8, dividing by 8 is an exact exponent shift (barring
     subnormals), so AVG equals the SUM result times 2^-3."""
