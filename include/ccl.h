@@ -324,6 +324,18 @@ ccl_status_t ccl_allreduce_host(const void *const *send, void *const *recv, int 
 ccl_status_t ccl_check_identical(const void *const *bufs, int nranks, size_t count, ccl_dtype_t dtype,
                                  unsigned long long *mismatches, cudaStream_t stream);
 
+/* Automatic result checks, off unless CCL_CHECK is set (to anything but 0)
+ * or enabled here.  While on, every AllReduce (fused or step, any order, the
+ * compressed one), AllGather and Broadcast that succeeds also enqueues
+ * ccl_check_identical over its outputs on the call's stream, adding to a
+ * per-device counter the library owns (one cudaMalloc on the first checked
+ * call on a device: make it before any stream capture).  Never traps. */
+void ccl_set_check(int enabled);
+/* Waits for the whole device, stores the current device's counter in
+ * *mismatches (0 if nothing was checked yet) and, when reset != 0, sets the
+ * counter back to 0. */
+ccl_status_t ccl_check_read(unsigned long long *mismatches, int reset);
+
 /* One traced call: the collective, its shape, the kernels it enqueued and
  * the host time it took to validate, plan and enqueue (not GPU time). */
 typedef struct {

@@ -87,6 +87,10 @@ def lib() -> ctypes.CDLL:
                 getattr(L, name).restype = ctypes.c_int
             L.ccl_check_identical.argtypes = [pp, i32, sz, i32, vp, vp]
             L.ccl_check_identical.restype = ctypes.c_int
+            L.ccl_set_check.argtypes = [i32]
+            L.ccl_set_check.restype = None
+            L.ccl_check_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
+            L.ccl_check_read.restype = ctypes.c_int
             L.ccl_set_trace.argtypes = [i32]
             L.ccl_set_trace.restype = None
             L.ccl_trace_read.argtypes = [vp, sz]
@@ -287,6 +291,18 @@ class TraceRecord(ctypes.Structure):
     _fields_ = [("collective", ctypes.c_char * 24), ("nranks", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("op", ctypes.c_int), ("mode", ctypes.c_int), ("status", ctypes.c_int), ("launches", ctypes.c_uint),
                 ("count", ctypes.c_ulonglong), ("host_ns", ctypes.c_ulonglong), ("seq", ctypes.c_ulonglong)]
+
+
+def ccl_set_check(enabled: bool) -> None:
+    """Automatic result checks after AllReduce, AllGather and Broadcast."""
+    lib().ccl_set_check(1 if enabled else 0)
+
+
+def ccl_check_read(reset: bool = True) -> int:
+    """Mismatches counted by the automatic checks on the current device."""
+    n = ctypes.c_ulonglong()
+    _check(lib().ccl_check_read(ctypes.byref(n), 1 if reset else 0), "ccl_check_read")
+    return int(n.value)
 
 
 def ccl_set_trace(enabled: bool) -> None:

@@ -867,11 +867,22 @@ static ccl_status_t ccl_allreduce_host_impl(const void *const *send, void *const
 
 // ------------------------------------------------------------------ traced entry points
 
+// after a successful call whose outputs must be identical on every rank: the
+// automatic result check (a no-op unless checks are on)
+static ccl_status_t then_check(ccl_status_t st, const void *const *outs, int nranks, size_t count,
+                               ccl_dtype_t dtype, cudaStream_t stream)
+{
+    if (st != CCL_OK)
+        return st;
+    return from_cuda(auto_check(outs, nranks, count, (int)elem_size(dtype), stream));
+}
+
 ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
                            ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
 {
     TraceScope tr("allreduce", nranks, count, (int)dtype, (int)op, (int)mode);
-    return tr.done(ccl_allreduce_impl(send, recv, nranks, count, dtype, op, mode, stream));
+    return tr.done(then_check(ccl_allreduce_impl(send, recv, nranks, count, dtype, op, mode, stream), recv, nranks,
+                              count, dtype, stream));
 }
 
 ccl_status_t ccl_allreduce_host(const void *const *send, void *const *recv, int nranks, size_t count,
@@ -893,14 +904,16 @@ ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nrank
                            ccl_mode_t mode, cudaStream_t stream)
 {
     TraceScope tr("allgather", nranks, count, (int)dtype, -1, (int)mode);
-    return tr.done(ccl_allgather_impl(send, recv, nranks, count, dtype, mode, stream));
+    return tr.done(then_check(ccl_allgather_impl(send, recv, nranks, count, dtype, mode, stream), recv, nranks, count,
+                              dtype, stream));
 }
 
 ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                            ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
     TraceScope tr("broadcast", nranks, count, (int)dtype, -1, (int)mode);
-    return tr.done(ccl_broadcast_impl(send, recv, nranks, root, count, dtype, mode, stream));
+    return tr.done(then_check(ccl_broadcast_impl(send, recv, nranks, root, count, dtype, mode, stream), recv, nranks,
+                              count, dtype, stream));
 }
 
 ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nranks, const size_t *counts,
@@ -951,7 +964,8 @@ ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int 
                                 cudaStream_t stream)
 {
     TraceScope tr("allreduce_algo", nranks, count, (int)dtype, (int)op, (int)algo);
-    return tr.done(ccl_allreduce_algo_impl(send, recv, nranks, count, dtype, op, algo, group_size, stream));
+    return tr.done(then_check(ccl_allreduce_algo_impl(send, recv, nranks, count, dtype, op, algo, group_size, stream),
+                              recv, nranks, count, dtype, stream));
 }
 
 ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residuals, int nranks, size_t count,
@@ -959,7 +973,9 @@ ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residual
                                       float threshold, cudaStream_t stream)
 {
     TraceScope tr("allreduce_compressed", nranks, count, (int)dtype, (int)op, (int)comp);
-    return tr.done(ccl_allreduce_compressed_impl(grads, residuals, nranks, count, dtype, op, comp, block, threshold, stream));
+    return tr.done(then_check(ccl_allreduce_compressed_impl(grads, residuals, nranks, count, dtype, op, comp, block,
+                                                            threshold, stream),
+                              grads, nranks, count, dtype, stream));
 }
 
 } // extern "C"

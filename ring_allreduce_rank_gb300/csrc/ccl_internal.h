@@ -115,6 +115,12 @@ void plan_host_slices(uint64_t count, uint64_t stage_elems, std::vector<HostSlic
 cudaError_t run_host_allreduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
                                uint64_t count, void *work, size_t work_bytes, cudaStream_t stream);
 
+// ------------------------------------------------------------------ automatic result checks
+// With checks on (CCL_CHECK or ccl_set_check), enqueue the bit comparison of
+// nranks outputs of `count` elements on `stream`, adding to the device's
+// counter; a no-op otherwise.
+cudaError_t auto_check(const void *const *bufs, int nranks, uint64_t count, int elem_size, cudaStream_t stream);
+
 // ------------------------------------------------------------------ bookkeeping
 // (count_launches is declared in fused.h)
 

@@ -14,6 +14,9 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/ccl.h"
 #include "ccl_internal.h"
@@ -101,6 +104,49 @@ static cudaError_t launch_check_t(const void *const *bufs, int nranks, uint64_t 
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ automatic checks
+
+namespace {
+std::atomic<int> g_check_on{-1}; // -1: read CCL_CHECK on first use
+std::mutex g_chk_mu;
+std::unordered_map<int, unsigned long long *> g_chk_ctr; // per device
+
+bool check_enabled()
+{
+    int v = g_check_on.load(std::memory_order_relaxed);
+    if (v < 0) {
+        const char *env = std::getenv("CCL_CHECK");
+        v = (env && env[0] && std::strcmp(env, "0") != 0) ? 1 : 0;
+        g_check_on.store(v, std::memory_order_relaxed);
+    }
+    return v > 0;
+}
+} // namespace
+
+cudaError_t auto_check(const void *const *bufs, int nranks, uint64_t count, int elem_size, cudaStream_t stream)
+{
+    if (!check_enabled() || nranks < 2 || count == 0)
+        return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    unsigned long long *ctr = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_chk_mu);
+        auto it = g_chk_ctr.find(dev);
+        if (it == g_chk_ctr.end()) {
+            if ((e = cudaMalloc(&ctr, sizeof *ctr)) != cudaSuccess || (e = cudaMemset(ctr, 0, sizeof *ctr)) != cudaSuccess)
+                return e;
+            g_chk_ctr[dev] = ctr;
+        } else {
+            ctr = it->second;
+        }
+    }
+    return nranks <= kSmallRanks ? launch_check_t<kSmallRanks>(bufs, nranks, count, elem_size, ctr, stream)
+                                 : launch_check_t<kMaxRanks>(bufs, nranks, count, elem_size, ctr, stream);
+}
+
 // ------------------------------------------------------------------ tracing
 
 namespace {
@@ -125,6 +171,9 @@ bool trace_enabled()
 TraceScope::TraceScope(const char *name, int nranks, uint64_t count, int dtype, int op, int mode)
     : active_(trace_enabled())
 {
+    // an NVTX range per call, so that profiler timelines name the collective
+    // (no cost beyond a check when no tool is attached)
+    nvtxRangePushA(name);
     if (!active_)
         return;
     std::memset(&rec_, 0, sizeof rec_);
@@ -140,6 +189,7 @@ TraceScope::TraceScope(const char *name, int nranks, uint64_t count, int dtype, 
 
 void TraceScope::finish(int status)
 {
+    nvtxRangePop();
     if (!active_)
         return;
     active_ = false;
@@ -177,6 +227,33 @@ ccl_status_t ccl_check_identical(const void *const *bufs, int nranks, size_t cou
 }
 
 void ccl_set_trace(int enabled) { g_trace_on.store(enabled ? 1 : 0, std::memory_order_relaxed); }
+
+void ccl_set_check(int enabled) { g_check_on.store(enabled ? 1 : 0, std::memory_order_relaxed); }
+
+ccl_status_t ccl_check_read(unsigned long long *mismatches, int reset)
+{
+    if (!mismatches)
+        return CCL_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    unsigned long long *ctr = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_chk_mu);
+        auto it = g_chk_ctr.find(dev);
+        if (it != g_chk_ctr.end())
+            ctr = it->second;
+    }
+    *mismatches = 0;
+    if (!ctr)
+        return CCL_OK; // nothing checked on this device yet
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(mismatches, ctr, sizeof *ctr, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    if (reset && cudaMemset(ctr, 0, sizeof *ctr) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    return CCL_OK;
+}
 
 size_t ccl_trace_read(ccl_trace_record_t *out, size_t max_records)
 {

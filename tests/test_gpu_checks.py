@@ -60,3 +60,47 @@ def test_trace_records_calls():
     assert recs[0]["launches"] == 1 and recs[1]["launches"] == 2 * (N - 1)
     assert all(r["status"] == 0 and r["nranks"] == N and r["count"] == K and r["dtype"] == 1 for r in recs)
     assert recs[0]["op"] == 1 and recs[1]["mode"] == 1 and recs[1]["seq"] == recs[0]["seq"] + 1
+
+
+def test_automatic_checks_follow_each_collective():
+    """With checks on, every AllReduce (fused, step, another order, the
+    compressed one), AllGather and Broadcast enqueues one comparison of its
+    outputs: one extra launch each, and no mismatch on correct results.  Off,
+    nothing extra is launched."""
+    N, K = 6, 20_011
+    x = list(W.mixed_bf16(N, K, seed_base=41))
+    bufs = [to_dev(r) for r in x]
+    _, ln = ccl.ccl_plan_chunks(K, N)
+    parts = [torch.empty(ln[r], dtype=torch.bfloat16, device=DEV) for r in range(N)]
+    full = [torch.empty(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    grads = [to_dev(r) for r in W.normal_bf16(N, K, std=1e-2, seed_base=3)]
+    res = [torch.zeros(K, dtype=torch.float32, device=DEV) for _ in range(N)]
+    ccl.ccl_allreduce_compressed(grads, res, op="avg")  # its one-time set-up, outside the counted region
+    torch.cuda.synchronize()
+    ccl.ccl_set_check(True)
+    try:
+        ccl.ccl_check_read(reset=True)
+        n0 = ccl.ccl_launch_count()
+        ccl.ccl_allreduce(bufs, op="sum")
+        ccl.ccl_allreduce_algo(bufs, op="max", algo="tree")
+        ccl.ccl_reduce_scatter(bufs, parts, op="sum")          # not checked: outputs differ by design
+        ccl.ccl_allgather(parts, full)
+        ccl.ccl_broadcast(bufs, full, root=2)
+        ccl.ccl_allreduce_compressed(grads, res, op="avg")
+        fused = ccl.ccl_launch_count() - n0
+        assert ccl.ccl_check_read() == 0
+        n1 = ccl.ccl_launch_count()
+        ccl.ccl_allreduce(bufs, op="avg", mode="step")
+        step = ccl.ccl_launch_count() - n1
+        assert ccl.ccl_check_read() == 0
+    finally:
+        ccl.ccl_set_check(False)
+    n2 = ccl.ccl_launch_count()
+    ccl.ccl_allreduce(bufs, op="sum")
+    ccl.ccl_allreduce_compressed(grads, res, op="avg")
+    plain = ccl.ccl_launch_count() - n2
+    # checked: AR 1+1, tree 1+1, RS 1, AG 1+1, broadcast 1+1, compressed (pipe + tail) 2+1
+    assert fused == 2 + 2 + 1 + 2 + 2 + 3
+    assert step == 2 * (N - 1) + 1 + 1  # in place: 2(N-1) steps, the AVG scale, the check
+    assert plain == 1 + 2
+    torch.cuda.synchronize()
