@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_ring_schedule.restype = None
             L.oracle_ring_allreduce.argtypes = [pp, i32, u64, i32, i32, p64]
             L.oracle_ring_allreduce_threads.argtypes = [pp, i32, u64, i32, i32, i32]
+            L.oracle_ring_allreduce_threads_ex.argtypes = [pp, i32, u64, i32, i32, i32, i32, ctypes.c_long]
             L.oracle_ring_allreduce_closed.argtypes = [pp, pp, i32, u64, i32, i32]
             L.oracle_ring_allreduce_at.argtypes = [pp, i32, u64, i32, i32, p64, u64, vp]
             L.oracle_ring_allreduce_gathered.argtypes = [pp, i32, u64, i32, i32, p64, u64, vp]
@@ -172,6 +173,22 @@ def ring_allreduce_threads(bufs, op="sum", threads: int = 0):
     _check(lib().oracle_ring_allreduce_threads(_ptrs(outs), N, K, _dtype_code(outs[0]), _op(op), threads or N),
            "oracle_ring_allreduce_threads")
     return outs
+
+
+TIMED_OUT = 3
+
+
+def ring_allreduce_threads_status(bufs, op="sum", threads: int = 0, withhold: int = -1, timeout_ms: int = 60000):
+    """As ring_allreduce_threads, with the thread owning rank `withhold` leaving
+    before its first send (a failed rank).  Returns (outputs, code): 0, or
+    TIMED_OUT when the others' bounded waits ran out."""
+    outs = [np.array(b, copy=True, order="C") for b in bufs]
+    N, K = len(outs), outs[0].size
+    rc = lib().oracle_ring_allreduce_threads_ex(_ptrs(outs), N, K, _dtype_code(outs[0]), _op(op), threads or N,
+                                                withhold, timeout_ms)
+    if rc not in (0, TIMED_OUT):
+        _check(rc, "oracle_ring_allreduce_threads_ex")
+    return outs, rc
 
 
 def ring_allreduce_closed(bufs, op="sum"):

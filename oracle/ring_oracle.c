@@ -30,8 +30,10 @@
  * which passage it follows.
  */
 #define _POSIX_C_SOURCE 200809L /* pthread barriers */
+#include <errno.h>
 #include <pthread.h>
 #include <stdint.h>
+#include <time.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -47,6 +49,7 @@
 #define OR_OK 0
 #define OR_EINVAL 1
 #define OR_ENOMEM 2
+#define OR_ETIMEDOUT 3
 
 /* ------------------------------------------------------------------ */
 /* scalar arithmetic                                                   */
@@ -307,27 +310,83 @@ typedef struct {
     int go; /* 0: wait, 1: run, -1: leave without running */
 } start_gate;
 
+/* A barrier whose wait gives up after a deadline.  A rank that never arrives
+ * (it left, or failed) breaks the barrier for everyone: every wait from then
+ * on returns at once with an error, so no thread hangs (the pages: a rank that
+ * exits early hangs the others until a timeout; Lesson 3, pitfalls). */
+typedef struct {
+    pthread_mutex_t mu;
+    pthread_cond_t cv;
+    unsigned n, arrived, generation;
+    int broken;
+    long timeout_ms;
+} timed_barrier;
+
+static int timed_barrier_wait(timed_barrier *b)
+{
+    pthread_mutex_lock(&b->mu);
+    if (b->broken) {
+        pthread_mutex_unlock(&b->mu);
+        return -1;
+    }
+    const unsigned gen = b->generation;
+    if (++b->arrived == b->n) {
+        b->arrived = 0;
+        ++b->generation;
+        pthread_cond_broadcast(&b->cv);
+        pthread_mutex_unlock(&b->mu);
+        return 0;
+    }
+    struct timespec until;
+    clock_gettime(CLOCK_REALTIME, &until);
+    until.tv_sec += b->timeout_ms / 1000;
+    until.tv_nsec += (b->timeout_ms % 1000) * 1000000L;
+    if (until.tv_nsec >= 1000000000L) {
+        until.tv_sec += 1;
+        until.tv_nsec -= 1000000000L;
+    }
+    int rc = 0;
+    while (b->generation == gen && !b->broken && rc != ETIMEDOUT)
+        rc = pthread_cond_timedwait(&b->cv, &b->mu, &until);
+    const int ok = b->generation != gen;
+    if (!ok && !b->broken) {
+        b->broken = 1; /* this wait ran out: release everyone */
+        pthread_cond_broadcast(&b->cv);
+    }
+    pthread_mutex_unlock(&b->mu);
+    return ok ? 0 : -1;
+}
+
 typedef struct {
     void **buf;
     int N, dtype, op, r0, r1;
     const uint64_t *off, *len;
     char *snap;
     uint64_t stride;
-    pthread_barrier_t *bar;
+    timed_barrier *bar;
     start_gate *gate;
+    int withhold; /* this thread leaves before its first send (a failed rank) */
 } ring_part;
+
+#define RING_SYNC(p)                                                                                          \
+    do {                                                                                                               \
+        if (timed_barrier_wait((p)->bar) != 0)                                                                          \
+            return NULL;                                                                                               \
+    } while (0)
 
 static void *ring_part_run(void *arg)
 {
     const ring_part *p = (const ring_part *)arg;
     const int N = p->N;
     const size_t es = esize(p->dtype);
+    if (p->withhold)
+        return NULL;
     for (int s = 0; s < N - 1; ++s) { /* ReduceScatter phase */
         for (int i = p->r0; i < p->r1; ++i) {
             int c = mod((int64_t)i - s, N);
             memcpy(p->snap + (size_t)i * p->stride * es, (char *)p->buf[i] + p->off[c] * es, p->len[c] * es);
         }
-        pthread_barrier_wait(p->bar);
+        RING_SYNC(p);
         for (int i = p->r0; i < p->r1; ++i) {
             int c = mod((int64_t)i - 1 - s, N);
             const void *in = p->snap + (size_t)mod((int64_t)i - 1, N) * p->stride * es;
@@ -337,7 +396,7 @@ static void *ring_part_run(void *arg)
                       hop(load(p->buf[i], p->dtype, g), load(in, p->dtype, e), p->dtype, p->op));
             }
         }
-        pthread_barrier_wait(p->bar);
+        RING_SYNC(p);
     }
     if (p->op == OR_AVG)
         for (int i = p->r0; i < p->r1; ++i) {
@@ -346,19 +405,19 @@ static void *ring_part_run(void *arg)
                 store(p->buf[i], p->dtype, p->off[c] + e,
                       avg_scale(load(p->buf[i], p->dtype, p->off[c] + e), N, p->dtype));
         }
-    pthread_barrier_wait(p->bar);
+    RING_SYNC(p);
     for (int s = 0; s < N - 1; ++s) { /* AllGather phase */
         for (int i = p->r0; i < p->r1; ++i) {
             int c = mod((int64_t)i + 1 - s, N);
             memcpy(p->snap + (size_t)i * p->stride * es, (char *)p->buf[i] + p->off[c] * es, p->len[c] * es);
         }
-        pthread_barrier_wait(p->bar);
+        RING_SYNC(p);
         for (int i = p->r0; i < p->r1; ++i) {
             int c = mod((int64_t)i - s, N);
             memcpy((char *)p->buf[i] + p->off[c] * es, p->snap + (size_t)mod((int64_t)i - 1, N) * p->stride * es,
                    p->len[c] * es);
         }
-        pthread_barrier_wait(p->bar);
+        RING_SYNC(p);
     }
     return NULL;
 }
@@ -384,10 +443,17 @@ static void open_gate(start_gate *g, int go)
     pthread_mutex_unlock(&g->mu);
 }
 
-int oracle_ring_allreduce_threads(void **buf, int N, uint64_t K, int dtype, int op, int nthreads)
+/* withhold_rank >= 0: the thread that owns that rank leaves before its first
+ * send, as a failed rank would; the others' waits then run out after
+ * timeout_ms and the call returns OR_ETIMEDOUT (the buffers are left
+ * partly updated).  The plain call waits up to a minute per step. */
+int oracle_ring_allreduce_threads_ex(void **buf, int N, uint64_t K, int dtype, int op, int nthreads,
+                                     int withhold_rank, long timeout_ms)
 {
-    if (bad_args(N, dtype, op) || nthreads < 1)
+    if (bad_args(N, dtype, op) || nthreads < 1 || timeout_ms < 1 || withhold_rank >= N)
         return OR_EINVAL;
+    if (withhold_rank >= 0 && (nthreads < 2 || N < 2))
+        return OR_EINVAL; /* a failure needs another thread to notice it */
     if (nthreads > N)
         nthreads = N;
     uint64_t *off = malloc(sizeof(uint64_t) * (size_t)N), *len = malloc(sizeof(uint64_t) * (size_t)N);
@@ -395,17 +461,18 @@ int oracle_ring_allreduce_threads(void **buf, int N, uint64_t K, int dtype, int 
     char *snap = malloc((size_t)N * stride * esize(dtype));
     ring_part *parts = malloc(sizeof(ring_part) * (size_t)nthreads);
     pthread_t *th = malloc(sizeof(pthread_t) * (size_t)nthreads);
-    pthread_barrier_t bar;
+    timed_barrier bar = {PTHREAD_MUTEX_INITIALIZER, PTHREAD_COND_INITIALIZER, (unsigned)nthreads, 0, 0, 0, timeout_ms};
     start_gate gate = {PTHREAD_MUTEX_INITIALIZER, PTHREAD_COND_INITIALIZER, 0};
     int started = 1;
-    if (!off || !len || !snap || !parts || !th || pthread_barrier_init(&bar, NULL, (unsigned)nthreads) != 0) {
+    if (!off || !len || !snap || !parts || !th) {
         free(off); free(len); free(snap); free(parts); free(th);
         return OR_ENOMEM;
     }
     oracle_partition(K, N, off, len);
     for (int t = 0; t < nthreads; ++t) {
-        ring_part q = {buf, N, dtype, op, (int)((int64_t)N * t / nthreads), (int)((int64_t)N * (t + 1) / nthreads),
-                       off, len, snap, stride, &bar, &gate};
+        const int r0 = (int)((int64_t)N * t / nthreads), r1 = (int)((int64_t)N * (t + 1) / nthreads);
+        ring_part q = {buf, N, dtype, op, r0, r1, off, len, snap, stride, &bar, &gate,
+                       withhold_rank >= r0 && withhold_rank < r1};
         parts[t] = q;
     }
     while (started < nthreads && pthread_create(&th[started], NULL, ring_part_gated, &parts[started]) == 0)
@@ -416,10 +483,16 @@ int oracle_ring_allreduce_threads(void **buf, int N, uint64_t K, int dtype, int 
         ring_part_run(&parts[0]); /* the calling thread is thread 0 */
     for (int t = 1; t < started; ++t)
         pthread_join(th[t], NULL);
-    pthread_barrier_destroy(&bar);
+    const int broken = bar.broken;
     free(off); free(len); free(snap); free(parts); free(th);
-    /* not every thread could be started: the one-thread ring, the same bits */
-    return all ? OR_OK : oracle_ring_allreduce(buf, N, K, dtype, op, NULL);
+    if (!all) /* not every thread could be started: the one-thread ring, the same bits */
+        return withhold_rank >= 0 ? OR_ENOMEM : oracle_ring_allreduce(buf, N, K, dtype, op, NULL);
+    return broken ? OR_ETIMEDOUT : OR_OK;
+}
+
+int oracle_ring_allreduce_threads(void **buf, int N, uint64_t K, int dtype, int op, int nthreads)
+{
+    return oracle_ring_allreduce_threads_ex(buf, N, K, dtype, op, nthreads, -1, 60000);
 }
 
 /* Second, independent formulation (closed form).  Chunk c starts at rank c at

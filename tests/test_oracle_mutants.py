@@ -49,6 +49,9 @@ MUTANTS = [
     ("rs_adds_into_wrong_chunk",
      "int c = mod((int64_t)i - 1 - s, N);\n            int src = mod((int64_t)i - 1, N);\n            const void *in",
      "int c = mod((int64_t)i - s, N);\n            int src = mod((int64_t)i - 1, N);\n            const void *in"),
+    ("threaded_rs_adds_into_wrong_chunk",
+     "int c = mod((int64_t)i - 1 - s, N);\n            const void *in = p->snap",
+     "int c = mod((int64_t)i - s, N);\n            const void *in = p->snap"),
     ("ag_stores_wrong_chunk",
      "int c = mod((int64_t)i - s, N);\n            int src = mod((int64_t)i - 1, N);\n            memcpy((char *)buf[i]",
      "int c = mod((int64_t)i + 1 - s, N);\n            int src = mod((int64_t)i - 1, N);\n            memcpy((char *)buf[i]"),
