@@ -336,6 +336,15 @@ void ccl_set_check(int enabled);
  * counter back to 0. */
 ccl_status_t ccl_check_read(unsigned long long *mismatches, int reset);
 
+/* Debug builds (libccl_debug.so, compiled with CCL_DEBUG_BOUNDS) check every
+ * global load and store of every kernel against the byte ranges of the
+ * call's own buffers, library workspace included; an access outside them is
+ * skipped, never performed, and counted.  Waits for the device and returns
+ * the count and the first offending address.  Release builds return
+ * CCL_ERR_UNSUPPORTED.  Calls whose work overlaps on the GPU share the range
+ * table in debug builds: run them one at a time there. */
+ccl_status_t ccl_debug_faults(unsigned long long *faults, unsigned long long *first_address);
+
 /* One traced call: the collective, its shape, the kernels it enqueued and
  * the host time it took to validate, plan and enqueue (not GPU time). */
 typedef struct {

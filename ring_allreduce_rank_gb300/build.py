@@ -19,6 +19,11 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(BUILD, "libccl.so")
+# the bounds-checking debug build: every global access of every kernel is
+# checked against the call's buffers (CCL_DEBUG_BOUNDS; device globals shared
+# across translation units, hence relocatable device code)
+DEBUG_LIB = os.path.join(BUILD, "libccl_debug.so")
+DEBUG_FLAGS = ["-DCCL_DEBUG_BOUNDS", "-rdc=true"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false", "-ftz=false",
@@ -45,20 +50,24 @@ def _digest(paths: list[str], extra: list[str]) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, debug_bounds: bool = False) -> str:
+    """Build libccl.so (or, with debug_bounds, libccl_debug.so) unless the
+    sources and flags are unchanged since the last build."""
     os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
     deps = srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))] + \
         [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
-    flags = ARCH + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_verbose else [])
-    stamp = os.path.join(BUILD, "libccl.stamp")
+    flags = ARCH + NVCC_FLAGS + (DEBUG_FLAGS if debug_bounds else []) + (["-Xptxas", "-v"] if ptxas_verbose else [])
+    lib = DEBUG_LIB if debug_bounds else LIB
+    tag = "debug." if debug_bounds else ""
+    stamp = os.path.join(BUILD, "libccl.%sstamp" % tag)
     digest = _digest(deps, flags)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == digest:
-        return LIB
+    if not force and os.path.exists(lib) and os.path.exists(stamp) and open(stamp).read() == digest:
+        return lib
     exe = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(BUILD, os.path.basename(src) + "." + tag + "o")
         cmd = [exe, *flags, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
@@ -69,17 +78,18 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = [exe, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    tmp = lib + ".tmp.%d" % os.getpid()
+    cmd = [exe, *ARCH, *(["-rdc=true"] if debug_bounds else []), "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), res.stderr))
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="--ptxas" in sys.argv,
+                debug_bounds="--debug-bounds" in sys.argv))

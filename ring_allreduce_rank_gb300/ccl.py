@@ -44,10 +44,13 @@ def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(_LIB_PATH):
+            # CCL_LIBRARY: another build of this library to load (the
+            # bounds-checking debug build, libccl_debug.so)
+            path = os.environ.get("CCL_LIBRARY") or _LIB_PATH
+            if not os.path.exists(path):
                 raise RuntimeError("libccl.so is not built (%s); run `python -m ring_allreduce_rank_gb300.build` "
-                                   "or __graft_entry__.build()" % _LIB_PATH)
-            L = ctypes.CDLL(_LIB_PATH)
+                                   "or __graft_entry__.build()" % path)
+            L = ctypes.CDLL(path)
             vp, pp, i32, sz = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_size_t
             psz = ctypes.POINTER(ctypes.c_size_t)
             sig = {
@@ -87,6 +90,8 @@ def lib() -> ctypes.CDLL:
                 getattr(L, name).restype = ctypes.c_int
             L.ccl_check_identical.argtypes = [pp, i32, sz, i32, vp, vp]
             L.ccl_check_identical.restype = ctypes.c_int
+            L.ccl_debug_faults.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.POINTER(ctypes.c_ulonglong)]
+            L.ccl_debug_faults.restype = ctypes.c_int
             L.ccl_set_check.argtypes = [i32]
             L.ccl_set_check.restype = None
             L.ccl_check_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
@@ -291,6 +296,14 @@ class TraceRecord(ctypes.Structure):
     _fields_ = [("collective", ctypes.c_char * 24), ("nranks", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("op", ctypes.c_int), ("mode", ctypes.c_int), ("status", ctypes.c_int), ("launches", ctypes.c_uint),
                 ("count", ctypes.c_ulonglong), ("host_ns", ctypes.c_ulonglong), ("seq", ctypes.c_ulonglong)]
+
+
+def ccl_debug_faults():
+    """(accesses skipped, first address) in a bounds-checking debug build;
+    raises CclError (CCL_ERR_UNSUPPORTED) in a release build."""
+    n, a = ctypes.c_ulonglong(), ctypes.c_ulonglong()
+    _check(lib().ccl_debug_faults(ctypes.byref(n), ctypes.byref(a)), "ccl_debug_faults")
+    return int(n.value), int(a.value)
 
 
 def ccl_set_check(enabled: bool) -> None:

@@ -131,6 +131,32 @@ ccl_status_t copy_ranks(const void *const *src, void *const *dst, int nranks, si
     return from_cuda(launch_copy_segments(segs.data(), segs.size(), st));
 }
 
+#ifdef CCL_DEBUG_BOUNDS
+// debug builds: upload the byte ranges this call's kernels may touch
+ccl_status_t dbg_call(const std::vector<Range> &a, const std::vector<Range> &b, std::initializer_list<DbgRange> extra,
+                      cudaStream_t st)
+{
+    std::vector<DbgRange> v;
+    for (const Range &x : a)
+        v.push_back(DbgRange{reinterpret_cast<const void *>(x.lo), (size_t)(x.hi - x.lo)});
+    for (const Range &x : b)
+        v.push_back(DbgRange{reinterpret_cast<const void *>(x.lo), (size_t)(x.hi - x.lo)});
+    for (const DbgRange &x : extra)
+        v.push_back(x);
+    return from_cuda(dbg_set_ranges(v, st));
+}
+#define CCL_DBG(...)                                                                                                   \
+    do {                                                                                                               \
+        ccl_status_t s_ = dbg_call(__VA_ARGS__);                                                                       \
+        if (s_ != CCL_OK)                                                                                              \
+            return s_;                                                                                                 \
+    } while (0)
+#else
+#define CCL_DBG(...)                                                                                                   \
+    do {                                                                                                               \
+    } while (0)
+#endif
+
 } // namespace
 } // namespace ccl
 
@@ -290,6 +316,7 @@ static ccl_status_t ccl_allreduce_impl(const void *const *send, void *const *rec
     });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     if (nranks == 1 && in_place && op != CCL_AVG)
         return CCL_OK;
     if (mode == CCL_MODE_FUSED)
@@ -325,12 +352,14 @@ static ccl_status_t ccl_reduce_scatter_impl(const void *const *send, void *const
     });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     if (mode == CCL_MODE_FUSED)
         return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_CHUNK, 0, stream));
     // step mode: the ring's ReduceScatter phase on a workspace copy of the inputs
     void *ws = nullptr;
     if ((st = get_workspace(count * es * (size_t)nranks, &ws)) != CCL_OK)
         return st;
+    CCL_DBG(w, r, {DbgRange{ws, count * es * (size_t)nranks}}, stream);
     std::vector<void *> bufs(nranks);
     for (int i = 0; i < nranks; ++i)
         bufs[i] = static_cast<char *>(ws) + (size_t)i * count * es;
@@ -376,6 +405,7 @@ static ccl_status_t ccl_allgather_impl(const void *const *send, void *const *rec
     });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     if (mode == CCL_MODE_FUSED)
         return from_cuda(launch_fanout((int)dtype, send, nranks, recv, nranks, count, stream));
     // step mode: rank i starts with chunk i; ring steps forward the rest
@@ -418,6 +448,7 @@ static ccl_status_t ccl_broadcast_impl(const void *const *send, void *const *rec
     });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     if (mode == CCL_MODE_FUSED) {
         // in place, root already holds the data: write only the other ranks
         const void *src[1] = {send[root]};
@@ -476,6 +507,7 @@ static ccl_status_t ccl_alltoallv_impl(const void *const *send, void *const *rec
     ccl_status_t st = check_overlaps(w, r, [](const Range &, const Range &) { return false; });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     auto seg = [&](size_t i, size_t j) {
         return CopySeg{static_cast<const char *>(send[i]) + sd[i * N + j] * es,
                        static_cast<char *>(recv[j]) + rd[j * N + i] * es, counts[i * N + j] * es, 0};
@@ -549,6 +581,7 @@ static ccl_status_t ccl_bucket_allreduce_impl(void *const *ptrs, const size_t *n
     ccl_status_t st = check_overlaps(w, {}, [](const Range &, const Range &) { return false; });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, {}, {}, stream);
     // tensors in stream order
     std::vector<size_t> order;
     for (size_t k = T; k-- > 0;)
@@ -569,6 +602,7 @@ static ccl_status_t ccl_bucket_allreduce_impl(void *const *ptrs, const size_t *n
     void *ws = nullptr;
     if ((st = get_workspace(std::min(B, total) * es * N, &ws)) != CCL_OK)
         return st;
+    CCL_DBG(w, {}, {DbgRange{ws, std::min(B, total) * es * N}}, stream);
     std::vector<void *> bufs(N);
     for (size_t r = 0; r < N; ++r)
         bufs[r] = static_cast<char *>(ws) + r * std::min(B, total) * es;
@@ -629,6 +663,7 @@ static ccl_status_t ccl_reduce_impl(const void *const *send, void *const *recv, 
     });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     if (mode == CCL_MODE_FUSED)
         return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_ROOT, root,
                                              stream));
@@ -637,6 +672,7 @@ static ccl_status_t ccl_reduce_impl(const void *const *send, void *const *recv, 
     void *ws = nullptr;
     if ((st = get_workspace(bytes * (size_t)nranks, &ws)) != CCL_OK)
         return st;
+    CCL_DBG(w, r, {DbgRange{ws, bytes * (size_t)nranks}}, stream);
     std::vector<void *> bufs(nranks);
     for (int i = 0; i < nranks; ++i)
         bufs[i] = static_cast<char *>(ws) + (size_t)i * bytes;
@@ -680,6 +716,7 @@ static ccl_status_t ccl_gather_impl(const void *const *send, void *const *recv, 
     });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     if (mode == CCL_MODE_FUSED) {
         void *dst[1] = {recv[root]};
         return from_cuda(launch_fanout((int)dtype, send, nranks, dst, 1, count, stream));
@@ -717,6 +754,7 @@ static ccl_status_t ccl_scatter_impl(const void *const *send, void *const *recv,
     });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     std::vector<CopySeg> segs;
     for (int i = 0; i < nranks; ++i)
         segs.push_back(CopySeg{static_cast<const char *>(send[root]) + part.off((uint32_t)i) * es,
@@ -758,6 +796,7 @@ static ccl_status_t ccl_allreduce_algo_impl(const void *const *send, void *const
     });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, r, {}, stream);
     if (algo == CCL_ALGO_RING)
         return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_ALL, 0, stream));
     return from_cuda(launch_order_allreduce((int)dtype, (int)op, (int)algo, group_size, send, recv, nranks, count,
@@ -801,6 +840,7 @@ static ccl_status_t ccl_allreduce_compressed_impl(void *const *grads, float *con
     ccl_status_t st = check_overlaps(w, {}, [](const Range &, const Range &) { return false; });
     if (st != CCL_OK)
         return st;
+    CCL_DBG(w, {}, {}, stream);
     return from_cuda(launch_compressed_allreduce((int)dtype, op == CCL_AVG, (int)comp, block, threshold, grads,
                                                  residuals, nranks, count, stream));
 }
@@ -860,6 +900,7 @@ static ccl_status_t ccl_allreduce_host_impl(const void *const *send, void *const
         return CCL_ERR_CUDA;
     if (cap != cudaStreamCaptureStatusNone)
         return CCL_ERR_UNSUPPORTED;
+    CCL_DBG(w, r, {}, stream);
     if (nranks == 1 && in_place && op != CCL_AVG)
         return CCL_OK;
     return from_cuda(run_host_allreduce((int)dtype, (int)op, send, recv, nranks, count, work, work_bytes, stream));

@@ -22,6 +22,7 @@ struct ccl_bucketer {
     int T = 0, N = 0;
     int dt = 0, op = 0;
     std::vector<void *> tp;                 // [t][r]
+    std::vector<ccl::DbgRange> ranges;      // every (tensor, rank) buffer, for debug builds
     ccl::BucketPlan plan;
     std::vector<std::vector<int>> buckets_of; // per tensor: the buckets it touches
     std::vector<int> remaining;             // per bucket: tensors not yet ready
@@ -84,6 +85,9 @@ ccl_status_t ccl_bucketer_create(void *const *ptrs, const size_t *numels, int nt
     for (int r = 0; r < nranks; ++r)
         for (int t = 0; t < ntensors; ++t)
             b->tp[(size_t)t * nranks + r] = ptrs[(size_t)r * ntensors + t];
+    for (int r = 0; r < nranks; ++r)
+        for (int t = 0; t < ntensors; ++t)
+            b->ranges.push_back(DbgRange{ptrs[(size_t)r * ntensors + t], numels[t] * es});
     build_bucket_plan(numels, ntensors, nranks, B, b->plan);
     const size_t nb = b->plan.segs.size();
     b->buckets_of.assign(ntensors, {});
@@ -117,6 +121,8 @@ ccl_status_t ccl_bucketer_mark_ready(ccl_bucketer_t *b, int tensor, cudaEvent_t 
             continue;
         // the whole bucket is ready (its waits are already on comm_stream)
         const auto &segs = b->plan.segs[k];
+        if (dbg_set_ranges(b->ranges, comm_stream) != cudaSuccess)
+            return CCL_ERR_CUDA;
         if (launch_bucket_reduce(b->dt, b->op, b->tp.data(), b->T, b->N, segs.data(), segs.size(), comm_stream,
                                  b->max_ctas) != cudaSuccess)
             return CCL_ERR_CUDA;

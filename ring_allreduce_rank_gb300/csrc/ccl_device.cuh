@@ -18,39 +18,86 @@ template <int DT> struct DType;
 template <> struct DType<DT_FP32> { static constexpr int kSize = 4; static constexpr int kVec = 4; };
 template <> struct DType<DT_BF16> { static constexpr int kSize = 2; static constexpr int kVec = 8; };
 
+// ------------------------------------------------------------------ bounds checks (debug builds)
+// Built with CCL_DEBUG_BOUNDS, every global access below is checked against
+// the byte ranges of the current call's buffers, which the host sets on the
+// call's stream before its kernels (dbg_set_ranges).  An access outside all of
+// them is counted, its address recorded, and skipped -- never performed, so a
+// wrong index cannot fault the device.  Release builds compile the check to
+// `true`.
+
+#ifdef CCL_DEBUG_BOUNDS
+constexpr int kDbgMaxRanges = 4096;
+extern __device__ unsigned g_dbg_n;                          // ranges in use
+extern __device__ unsigned long long g_dbg_r[kDbgMaxRanges][2]; // [lo, hi) byte addresses
+extern __device__ unsigned g_dbg_faults;
+extern __device__ unsigned long long g_dbg_first_fault;
+
+__device__ __forceinline__ bool dbg_ok(const void *p, size_t bytes)
+{
+    const unsigned long long a = (unsigned long long)(uintptr_t)p, b = a + bytes;
+    const unsigned n = g_dbg_n;
+    for (unsigned i = 0; i < n; ++i)
+        if (a >= g_dbg_r[i][0] && b <= g_dbg_r[i][1])
+            return true;
+    if (atomicAdd(&g_dbg_faults, 1u) == 0)
+        g_dbg_first_fault = a;
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool dbg_ok(const void *, size_t) { return true; }
+#endif
+
 // ------------------------------------------------------------------ memory
 // Loads bypass L1 (every byte is used once); stores are plain write-back so
 // that in-place writes land on lines the same thread just read.
 
 __device__ __forceinline__ uint4 ld16(const void *p)
 {
-    uint4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (dbg_ok(p, 16))
+        asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p));
     return v;
 }
 
 __device__ __forceinline__ void st16(void *p, const uint4 &v)
 {
-    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
+    if (dbg_ok(p, 16))
+        asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                     "r"(v.w)
+                     : "memory");
+}
+
+// plain global load / store of a T (vector widths the kernels use directly)
+template <class T> __device__ __forceinline__ T gload(const void *p)
+{
+    T v{};
+    if (dbg_ok(p, sizeof(T)))
+        v = *static_cast<const T *>(p);
+    return v;
+}
+
+template <class T> __device__ __forceinline__ void gstore(void *p, const T &v)
+{
+    if (dbg_ok(p, sizeof(T)))
+        *static_cast<T *>(p) = v;
 }
 
 template <int DT> __device__ __forceinline__ uint32_t ld_elem(const void *base, uint64_t i)
 {
     if (DT == DT_BF16)
-        return static_cast<const uint16_t *>(base)[i];
-    return static_cast<const uint32_t *>(base)[i];
+        return gload<uint16_t>(static_cast<const uint16_t *>(base) + i);
+    return gload<uint32_t>(static_cast<const uint32_t *>(base) + i);
 }
 
 template <int DT> __device__ __forceinline__ void st_elem(void *base, uint64_t i, uint32_t v)
 {
     if (DT == DT_BF16)
-        static_cast<uint16_t *>(base)[i] = static_cast<uint16_t>(v);
+        gstore<uint16_t>(static_cast<uint16_t *>(base) + i, static_cast<uint16_t>(v));
     else
-        static_cast<uint32_t *>(base)[i] = v;
+        gstore<uint32_t>(static_cast<uint32_t *>(base) + i, v);
 }
 
 // ------------------------------------------------------------------ arithmetic

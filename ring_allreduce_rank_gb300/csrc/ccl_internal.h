@@ -115,6 +115,15 @@ void plan_host_slices(uint64_t count, uint64_t stage_elems, std::vector<HostSlic
 cudaError_t run_host_allreduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
                                uint64_t count, void *work, size_t work_bytes, cudaStream_t stream);
 
+// ------------------------------------------------------------------ bounds checks (debug builds)
+// The byte ranges a call's kernels may touch.  Debug builds upload them on the
+// call's stream before its kernels; release builds do nothing.
+struct DbgRange {
+    const void *lo;
+    size_t bytes;
+};
+cudaError_t dbg_set_ranges(const std::vector<DbgRange> &ranges, cudaStream_t stream);
+
 // ------------------------------------------------------------------ automatic result checks
 // With checks on (CCL_CHECK or ccl_set_check), enqueue the bit comparison of
 // nranks outputs of `count` elements on `stream`, adding to the device's

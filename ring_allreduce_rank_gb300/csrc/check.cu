@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kThreads) check_identical_kernel(const __grid_
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         total += __shfl_xor_sync(0xffffffffu, total, o);
-    if (any && (threadIdx.x & 31) == 0)
+    if (any && (threadIdx.x & 31) == 0 && dbg_ok(p.mismatches, sizeof *p.mismatches))
         atomicAdd(p.mismatches, (unsigned long long)total);
 }
 
@@ -102,6 +102,49 @@ static cudaError_t launch_check_t(const void *const *bufs, int nranks, uint64_t 
     check_identical_kernel<MAXR><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
     count_launches(1);
     return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ bounds checks (debug builds)
+
+#ifdef CCL_DEBUG_BOUNDS
+__device__ unsigned g_dbg_n = 0;
+__device__ unsigned long long g_dbg_r[kDbgMaxRanges][2];
+__device__ unsigned g_dbg_faults = 0;
+__device__ unsigned long long g_dbg_first_fault = 0;
+#endif
+
+cudaError_t dbg_set_ranges(const std::vector<DbgRange> &ranges, cudaStream_t stream)
+{
+#ifdef CCL_DEBUG_BOUNDS
+    // CCL_DEBUG_SHRINK (tests of the checker only): register the first half
+    // of every range, so that the second half's accesses are counted and
+    // skipped -- nothing outside the buffers is touched either way
+    static const bool shrink = [] {
+        const char *e = std::getenv("CCL_DEBUG_SHRINK");
+        return e && e[0] && std::strcmp(e, "0") != 0;
+    }();
+    std::vector<unsigned long long> r;
+    r.reserve(ranges.size() * 2);
+    for (const DbgRange &g : ranges) {
+        if (r.size() / 2 == (size_t)kDbgMaxRanges || !g.lo || !g.bytes)
+            continue;
+        const unsigned long long lo = (unsigned long long)(uintptr_t)g.lo;
+        r.push_back(lo);
+        r.push_back(lo + (shrink ? g.bytes / 2 : g.bytes));
+    }
+    const unsigned n = (unsigned)(r.size() / 2);
+    cudaError_t e = cudaSuccess;
+    if (n)
+        e = cudaMemcpyToSymbolAsync(g_dbg_r, r.data(), r.size() * sizeof(unsigned long long), 0,
+                                    cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_dbg_n, &n, sizeof n, 0, cudaMemcpyHostToDevice, stream);
+    return e;
+#else
+    (void)ranges;
+    (void)stream;
+    return cudaSuccess;
+#endif
 }
 
 // ------------------------------------------------------------------ automatic checks
@@ -143,6 +186,12 @@ cudaError_t auto_check(const void *const *bufs, int nranks, uint64_t count, int 
             ctr = it->second;
         }
     }
+    std::vector<DbgRange> rg; // debug builds: the outputs and the counter
+    for (int r = 0; r < nranks; ++r)
+        rg.push_back(DbgRange{bufs[r], (size_t)count * (size_t)elem_size});
+    rg.push_back(DbgRange{ctr, sizeof *ctr});
+    if ((e = dbg_set_ranges(rg, stream)) != cudaSuccess)
+        return e;
     return nranks <= kSmallRanks ? launch_check_t<kSmallRanks>(bufs, nranks, count, elem_size, ctr, stream)
                                  : launch_check_t<kMaxRanks>(bufs, nranks, count, elem_size, ctr, stream);
 }
@@ -221,6 +270,12 @@ ccl_status_t ccl_check_identical(const void *const *bufs, int nranks, size_t cou
     if (count == 0 || nranks == 1)
         return CCL_OK;
     const int es = dtype == CCL_BF16 ? 2 : 4;
+    std::vector<DbgRange> rg; // debug builds: the buffers and the counter
+    for (int r = 0; r < nranks; ++r)
+        rg.push_back(DbgRange{bufs[r], count * (size_t)es});
+    rg.push_back(DbgRange{mismatches, sizeof *mismatches});
+    if (dbg_set_ranges(rg, stream) != cudaSuccess)
+        return CCL_ERR_CUDA;
     const cudaError_t e = nranks <= kSmallRanks ? launch_check_t<kSmallRanks>(bufs, nranks, count, es, mismatches, stream)
                                                 : launch_check_t<kMaxRanks>(bufs, nranks, count, es, mismatches, stream);
     return e == cudaSuccess ? CCL_OK : CCL_ERR_CUDA;
@@ -229,6 +284,24 @@ ccl_status_t ccl_check_identical(const void *const *bufs, int nranks, size_t cou
 void ccl_set_trace(int enabled) { g_trace_on.store(enabled ? 1 : 0, std::memory_order_relaxed); }
 
 void ccl_set_check(int enabled) { g_check_on.store(enabled ? 1 : 0, std::memory_order_relaxed); }
+
+ccl_status_t ccl_debug_faults(unsigned long long *faults, unsigned long long *first_address)
+{
+#ifdef CCL_DEBUG_BOUNDS
+    if (!faults || !first_address)
+        return CCL_ERR_INVALID_ARG;
+    unsigned n = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpyFromSymbol(&n, g_dbg_faults, sizeof n) != cudaSuccess ||
+        cudaMemcpyFromSymbol(first_address, g_dbg_first_fault, sizeof *first_address) != cudaSuccess)
+        return CCL_ERR_CUDA;
+    *faults = n;
+    return CCL_OK;
+#else
+    (void)faults;
+    (void)first_address;
+    return CCL_ERR_UNSUPPORTED;
+#endif
+}
 
 ccl_status_t ccl_check_read(unsigned long long *mismatches, int reset)
 {

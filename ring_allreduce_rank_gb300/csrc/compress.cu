@@ -74,22 +74,22 @@ __device__ __forceinline__ void load_g(const void *base, uint64_t i, int valid, 
     if (vec && valid == EPL) {
         if (DT == DT_FP32) {
             if (EPL == 4) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(static_cast<const float *>(base) + i);
+                const uint4 w = gload<uint4>(static_cast<const float *>(base) + i);
                 out[0] = __uint_as_float(w.x); out[1] = __uint_as_float(w.y);
                 out[2] = __uint_as_float(w.z); out[3] = __uint_as_float(w.w);
                 return;
             }
-            const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const float *>(base) + i);
+            const uint2 w = gload<uint2>(static_cast<const float *>(base) + i);
             out[0] = __uint_as_float(w.x); out[1] = __uint_as_float(w.y);
             return;
         }
         if (EPL == 4) {
-            const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(base) + i);
+            const uint2 w = gload<uint2>(static_cast<const uint16_t *>(base) + i);
             out[0] = __uint_as_float(w.x << 16); out[1] = __uint_as_float(w.x & 0xffff0000u);
             out[2] = __uint_as_float(w.y << 16); out[3] = __uint_as_float(w.y & 0xffff0000u);
             return;
         }
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(base) + i);
+        const uint32_t w = gload<uint32_t>(static_cast<const uint16_t *>(base) + i);
         out[0] = __uint_as_float(w << 16); out[1] = __uint_as_float(w & 0xffff0000u);
         return;
     }
@@ -105,17 +105,17 @@ __device__ __forceinline__ void load_f(const float *base, uint64_t i, int valid,
 {
     if (vec && valid == EPL) {
         if (EPL == 4) {
-            const float4 w = *reinterpret_cast<const float4 *>(base + i);
+            const float4 w = gload<float4>(base + i);
             out[0] = w.x; out[1] = w.y; out[2] = w.z; out[3] = w.w;
         } else {
-            const float2 w = *reinterpret_cast<const float2 *>(base + i);
+            const float2 w = gload<float2>(base + i);
             out[0] = w.x; out[1] = w.y;
         }
         return;
     }
 #pragma unroll
     for (int j = 0; j < EPL; ++j)
-        out[j] = j < valid ? base[i + j] : 0.0f;
+        out[j] = j < valid ? gload<float>(base + i + j) : 0.0f;
 }
 
 template <int EPL>
@@ -123,15 +123,15 @@ __device__ __forceinline__ void store_f(float *base, uint64_t i, int valid, bool
 {
     if (vec && valid == EPL) {
         if (EPL == 4)
-            *reinterpret_cast<float4 *>(base + i) = make_float4(v[0], v[1], v[2], v[3]);
+            gstore<float4>(base + i, make_float4(v[0], v[1], v[2], v[3]));
         else
-            *reinterpret_cast<float2 *>(base + i) = make_float2(v[0], v[1]);
+            gstore<float2>(base + i, make_float2(v[0], v[1]));
         return;
     }
 #pragma unroll
     for (int j = 0; j < EPL; ++j)
         if (j < valid)
-            base[i + j] = v[j];
+            gstore<float>(base + i + j, v[j]);
 }
 
 // q = round(u / s), ties to even, with u / s the correctly rounded fp32
@@ -338,13 +338,13 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
             break;
         if (packed) {
             if (DT == DT_FP32 && EPL == 4)
-                *reinterpret_cast<uint4 *>(static_cast<uint32_t *>(p.grads[r]) + i0) = make_uint4(w[0], w[1], w[2], w[3]);
+                gstore<uint4>(static_cast<uint32_t *>(p.grads[r]) + i0, make_uint4(w[0], w[1], w[2], w[3]));
             else if (DT == DT_FP32)
-                *reinterpret_cast<uint2 *>(static_cast<uint32_t *>(p.grads[r]) + i0) = make_uint2(w[0], w[1]);
+                gstore<uint2>(static_cast<uint32_t *>(p.grads[r]) + i0, make_uint2(w[0], w[1]));
             else if (EPL == 4)
-                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.grads[r]) + i0) = make_uint2(w[0], w[2]);
+                gstore<uint2>(static_cast<uint16_t *>(p.grads[r]) + i0, make_uint2(w[0], w[2]));
             else
-                *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(p.grads[r]) + i0) = w[0];
+                gstore<uint32_t>(static_cast<uint16_t *>(p.grads[r]) + i0, w[0]);
         } else {
 #pragma unroll
             for (int j = 0; j < EPL; ++j)
@@ -396,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allred
 
 __device__ __forceinline__ void cp_async(void *smem, const void *gmem, int bytes)
 {
+    if (!dbg_ok(gmem, (size_t)bytes))
+        return; // debug builds: outside the call's buffers
     const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
     if (bytes == 16)
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");

@@ -53,7 +53,7 @@ __device__ __forceinline__ void copy_body(const char *src, char *dst, uint64_t n
     const W *s = reinterpret_cast<const W *>(src);
     W *d = reinterpret_cast<W *>(dst);
     for (uint64_t i = threadIdx.x; i < n; i += kThreads)
-        d[i] = s[i];
+        gstore<W>(d + i, gload<W>(s + i));
 }
 
 template <int MAXS>
@@ -74,9 +74,9 @@ __global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_co
     copy_split(s, g, head, body);
     if (t == 0) {
         for (uint64_t b = threadIdx.x; b < head; b += kThreads)
-            s.dst[b] = s.src[b];
+            gstore<char>(s.dst + b, gload<char>(s.src + b));
         for (uint64_t b = head + body + threadIdx.x; b < s.nbytes; b += kThreads)
-            s.dst[b] = s.src[b];
+            gstore<char>(s.dst + b, gload<char>(s.src + b));
     }
     const uint64_t b0 = t * kCopyTileBytes;
     if (b0 >= body)

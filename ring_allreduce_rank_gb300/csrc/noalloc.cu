@@ -105,6 +105,18 @@ extern "C" ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, 
     std::vector<void *> bufs(nranks);
     for (int i = 0; i < nranks; ++i)
         bufs[i] = static_cast<char *>(base) + (size_t)i * stride;
+    {   // debug builds: the scratch rows and the call's buffers
+        std::vector<DbgRange> rg;
+        for (int i = 0; i < nranks; ++i) {
+            rg.push_back(DbgRange{send[i], count * es});
+            rg.push_back(DbgRange{bufs[i], count * es});
+        }
+        const uint64_t q = count / (uint64_t)nranks, rem = count % (uint64_t)nranks;
+        for (int i = 0; i < nranks; ++i)
+            rg.push_back(DbgRange{recv[i], (size_t)(q + ((uint64_t)i < rem ? 1 : 0)) * es});
+        if (dbg_set_ranges(rg, stream) != cudaSuccess)
+            return CCL_ERR_CUDA;
+    }
     // Every scratch byte the ring reads below is first written by this copy, so
     // whatever an earlier call left in the array never reaches the result.
     std::vector<CopySeg> segs;
