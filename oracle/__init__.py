@@ -28,8 +28,8 @@ LIB = OVERRIDE or os.path.join(HERE, "_build", "liboracle.so")
 CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread", "-Wall", "-Wextra"]
 
 FP32, BF16 = 0, 1
-SUM, AVG, MAX, PROD, MIN = 0, 1, 2, 3, 4
-OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN}
+SUM, AVG, MAX, PROD, MIN, AVG_PREMUL = 0, 1, 2, 3, 4, 5
+OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN, "avg_premul": AVG_PREMUL}
 
 _lock = threading.Lock()
 _lib = None

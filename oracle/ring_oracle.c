@@ -24,7 +24,12 @@
  *     bitwise AND of the two (so +0 wins); MIN: NaN if either is NaN, else the
  *     smaller, and for +0 vs -0 the bitwise OR (so -0 wins);
  *   - AVG: SUM around the ring, then one fp32 division by N at the rank that
- *     holds the finished chunk, rounded to the buffer type, before the gather.
+ *     holds the finished chunk, rounded to the buffer type, before the gather;
+ *   - AVG_PREMUL (NCCL's pre-multiplied sum, Collective Communication,
+ *     libraries section): every rank first multiplies each of its values by
+ *     the fp32 reciprocal of N (correctly rounded), rounds the product to the
+ *     buffer type, and the ring then SUMs those; nothing is divided at the end.
+ *     Only the ring order takes it; the other orders reject it.
  *
  * Parity pins live in tests/test_oracle_*.py; see each function's comment for
  * which passage it follows.
@@ -45,6 +50,7 @@
 #define OR_MAX 2
 #define OR_PROD 3
 #define OR_MIN 4
+#define OR_AVGP 5 /* AVG by pre-multiplication: every contribution times rn(1/N), then SUM */
 
 #define OR_OK 0
 #define OR_EINVAL 1
@@ -101,6 +107,7 @@ static uint32_t op_f32(uint32_t a_bits, uint32_t b_bits, int op)
     switch (op) {
     case OR_SUM:
     case OR_AVG:
+    case OR_AVGP:
         r = f32_to_bits(a + b);
         break;
     case OR_PROD:
@@ -151,6 +158,26 @@ static uint32_t avg_scale(uint32_t v, int N, int dtype)
     return narrow_bits(r, dtype);
 }
 
+/* AVG by pre-multiplication (NCCL's pre-multiplied sum, Collective
+ * Communication, libraries section): each contribution x becomes
+ * round_T(x * rn(1/N)) -- one fp32 multiply by the correctly rounded
+ * reciprocal -- and the scaled contributions are summed around the ring with
+ * no division at the end. */
+static uint32_t premul(uint32_t v, int N, int dtype)
+{
+    const float inv = 1.0f / (float)N;
+    uint32_t r = f32_to_bits(bits_to_f32(widen_bits(v, dtype)) * inv);
+    if (f32_bits_is_nan(r))
+        r = 0x7fffffffu;
+    return narrow_bits(r, dtype);
+}
+
+/* what a rank puts into the ring for operator op */
+static uint32_t contrib(uint32_t v, int N, int dtype, int op)
+{
+    return op == OR_AVGP ? premul(v, N, dtype) : v;
+}
+
 static size_t esize(int dtype) { return dtype == OR_BF16 ? 2 : 4; }
 
 static uint32_t load(const void *buf, int dtype, uint64_t i)
@@ -172,7 +199,7 @@ static int mod(int64_t a, int n) { int64_t r = a % n; return (int)(r < 0 ? r + n
 
 static int bad_args(int N, int dtype, int op)
 {
-    return N < 1 || (dtype != OR_FP32 && dtype != OR_BF16) || op < OR_SUM || op > OR_MIN;
+    return N < 1 || (dtype != OR_FP32 && dtype != OR_BF16) || op < OR_SUM || op > OR_AVGP;
 }
 
 /* ------------------------------------------------------------------ */
@@ -227,6 +254,11 @@ static int rs_phase(void **buf, int N, const uint64_t *off, const uint64_t *len,
                     int dtype, int op, uint64_t *sent, void *snap, uint64_t stride)
 {
     size_t es = esize(dtype);
+    if (op == OR_AVGP) /* every rank scales its own contribution before it enters the ring */
+        for (int i = 0; i < N; ++i)
+            for (int c = 0; c < N; ++c)
+                for (uint64_t e = off[c]; e < off[c] + len[c]; ++e)
+                    store(buf[i], dtype, e, premul(load(buf[i], dtype, e), N, dtype));
     for (int s = 0; s < N - 1; ++s) {
         for (int i = 0; i < N; ++i) {
             int c = mod((int64_t)i - s, N);
@@ -381,6 +413,11 @@ static void *ring_part_run(void *arg)
     const size_t es = esize(p->dtype);
     if (p->withhold)
         return NULL;
+    if (p->op == OR_AVGP) /* each thread scales its own ranks' contributions */
+        for (int i = p->r0; i < p->r1; ++i)
+            for (int c = 0; c < N; ++c)
+                for (uint64_t e = p->off[c]; e < p->off[c] + p->len[c]; ++e)
+                    store(p->buf[i], p->dtype, e, premul(load(p->buf[i], p->dtype, e), N, p->dtype));
     for (int s = 0; s < N - 1; ++s) { /* ReduceScatter phase */
         for (int i = p->r0; i < p->r1; ++i) {
             int c = mod((int64_t)i - s, N);
@@ -499,8 +536,9 @@ int oracle_ring_allreduce_threads(void **buf, int N, uint64_t K, int dtype, int 
  * step 0 and collects one contribution per hop, finishing at rank c-1 after N-1
  * hops, so each of its elements is the left fold
  *     R = x_{c-1} (+) ( ... (x_{c+2} (+) (x_{c+1} (+) x_c)) ... )
- * with a round to the buffer type after every (+); AVG divides once; every rank
- * receives R.  in[] and out[] may alias per rank. */
+ * with a round to the buffer type after every (+); AVG divides once, while
+ * AVG_PREMUL scales each x_r before it enters the fold; every rank receives R.
+ * in[] and out[] may alias per rank. */
 int oracle_ring_allreduce_closed(const void **in, void **out, int N, uint64_t K, int dtype, int op)
 {
     if (bad_args(N, dtype, op))
@@ -513,9 +551,9 @@ int oracle_ring_allreduce_closed(const void **in, void **out, int N, uint64_t K,
     oracle_partition(K, N, off, len);
     for (int c = 0; c < N; ++c)
         for (uint64_t e = off[c]; e < off[c] + len[c]; ++e) {
-            uint32_t acc = load(in[c], dtype, e);
+            uint32_t acc = contrib(load(in[c], dtype, e), N, dtype, op);
             for (int k = 1; k < N; ++k)
-                acc = hop(load(in[(c + k) % N], dtype, e), acc, dtype, op);
+                acc = hop(contrib(load(in[(c + k) % N], dtype, e), N, dtype, op), acc, dtype, op);
             if (op == OR_AVG)
                 acc = avg_scale(acc, N, dtype);
             for (int r = 0; r < N; ++r)
@@ -544,9 +582,9 @@ int oracle_ring_allreduce_at(const void **in, int N, uint64_t K, int dtype, int 
             c = (int)(e / (q + 1));
         else
             c = (int)(rem + (e - rem * (q + 1)) / q);
-        uint32_t acc = load(in[c], dtype, e);
+        uint32_t acc = contrib(load(in[c], dtype, e), N, dtype, op);
         for (int k = 1; k < N; ++k)
-            acc = hop(load(in[(c + k) % N], dtype, e), acc, dtype, op);
+            acc = hop(contrib(load(in[(c + k) % N], dtype, e), N, dtype, op), acc, dtype, op);
         if (op == OR_AVG)
             acc = avg_scale(acc, N, dtype);
         store(out, dtype, t, acc);
@@ -573,9 +611,9 @@ int oracle_ring_allreduce_gathered(const void **vals, int N, uint64_t K, int dty
             c = (int)(e / (q + 1));
         else
             c = (int)(rem + (e - rem * (q + 1)) / q);
-        uint32_t acc = load(vals[c], dtype, t);
+        uint32_t acc = contrib(load(vals[c], dtype, t), N, dtype, op);
         for (int k = 1; k < N; ++k)
-            acc = hop(load(vals[(c + k) % N], dtype, t), acc, dtype, op);
+            acc = hop(contrib(load(vals[(c + k) % N], dtype, t), N, dtype, op), acc, dtype, op);
         if (op == OR_AVG)
             acc = avg_scale(acc, N, dtype);
         store(out, dtype, t, acc);
@@ -876,7 +914,7 @@ static void scale_range(void *buf, uint64_t lo, uint64_t hi, int N, int dtype)
  * the rank whose bit k is 0 keeps the lower half [lo, lo + ceil((hi-lo)/2)). */
 int oracle_allreduce_hd(void **buf, int N, uint64_t K, int dtype, int op)
 {
-    if (bad_args(N, dtype, op))
+    if (bad_args(N, dtype, op) || op == OR_AVGP)
         return OR_EINVAL;
     int sop = op == OR_AVG ? OR_SUM : op;
     int pw = 1;
@@ -951,7 +989,7 @@ int oracle_allreduce_hd(void **buf, int N, uint64_t K, int dtype, int op)
  * receives from rank i + 2^k when that rank exists; the root is rank 0. */
 int oracle_allreduce_tree(void **buf, int N, uint64_t K, int dtype, int op)
 {
-    if (bad_args(N, dtype, op))
+    if (bad_args(N, dtype, op) || op == OR_AVGP)
         return OR_EINVAL;
     int sop = op == OR_AVG ? OR_SUM : op;
     size_t es = esize(dtype);
@@ -980,7 +1018,7 @@ int oracle_allreduce_tree(void **buf, int N, uint64_t K, int dtype, int op)
  * sub-chunks.  AVG divides once by N, at the inter ring's holders. */
 int oracle_allreduce_hier(void **buf, int N, int L, uint64_t K, int dtype, int op)
 {
-    if (bad_args(N, dtype, op) || L < 1 || N % L != 0)
+    if (bad_args(N, dtype, op) || op == OR_AVGP || L < 1 || N % L != 0)
         return OR_EINVAL;
     int G = N / L;
     int sop = op == OR_AVG ? OR_SUM : op;
@@ -1069,7 +1107,7 @@ static uint32_t balanced(const uint32_t *leaf, int lo, int n, int dtype, int op)
 int oracle_allreduce_order_at(const void **in, int N, uint64_t K, int dtype, int op, int algo, int L,
                               const uint64_t *idx, uint64_t n, void *out)
 {
-    if (bad_args(N, dtype, op) || algo < 1 || algo > 3 || N > 1024 || (algo == 3 && (L < 1 || N % L)))
+    if (bad_args(N, dtype, op) || op == OR_AVGP || algo < 1 || algo > 3 || N > 1024 || (algo == 3 && (L < 1 || N % L)))
         return OR_EINVAL;
     int sop = op == OR_AVG ? OR_SUM : op;
     uint32_t x[1024], leaf[1024];
@@ -1225,8 +1263,10 @@ done:
  * relative error is measured.  SUM/AVG only. */
 int oracle_sum_f64(const void **in, int N, uint64_t K, int dtype, int op, double *y, double *absum)
 {
-    if (bad_args(N, dtype, op) || (op != OR_SUM && op != OR_AVG))
+    if (bad_args(N, dtype, op) || (op != OR_SUM && op != OR_AVG && op != OR_AVGP))
         return OR_EINVAL;
+    if (op == OR_AVGP)
+        op = OR_AVG; /* the same mean */
     for (uint64_t e = 0; e < K; ++e) {
         double s = 0.0, a = 0.0;
         for (int r = 0; r < N; ++r) {

@@ -56,8 +56,14 @@ MUTANTS = [
      "int c = mod((int64_t)i - s, N);\n            int src = mod((int64_t)i - 1, N);\n            memcpy((char *)buf[i]",
      "int c = mod((int64_t)i + 1 - s, N);\n            int src = mod((int64_t)i - 1, N);\n            memcpy((char *)buf[i]"),
     ("closed_form_rotation_off_by_one",
-     "            uint32_t acc = load(in[c], dtype, e);\n            for (int k = 1; k < N; ++k)",
-     "            uint32_t acc = load(in[(c + 1) % N], dtype, e);\n            for (int k = 2; k <= N; ++k)"),
+     "            uint32_t acc = contrib(load(in[c], dtype, e), N, dtype, op);\n            for (int k = 1; k < N; ++k)",
+     "            uint32_t acc = contrib(load(in[(c + 1) % N], dtype, e), N, dtype, op);\n"
+     "            for (int k = 2; k <= N; ++k)"),
+    # the pre-multiplied AVG
+    ("premul_skipped_in_closed_form", "return op == OR_AVGP ? premul(v, N, dtype) : v;", "return v;"),
+    ("premul_divides_instead_of_multiplying",
+     "uint32_t r = f32_to_bits(bits_to_f32(widen_bits(v, dtype)) * inv);",
+     "uint32_t r = f32_to_bits(bits_to_f32(widen_bits(v, dtype)) / (float)N);"),
     # other schedules' orders
     ("hd_partner_not_xor", "void *partner = vb[v ^ (1 << k)];", "void *partner = vb[(v + (1 << k)) % pw];"),
     ("tree_levels_top_down",

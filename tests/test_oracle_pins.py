@@ -220,7 +220,7 @@ def _inputs(dtype, N, K, seed):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min", "avg_premul"])
 @pytest.mark.parametrize("N,K", [(1, 7), (2, 9), (3, 3), (3, 0), (4, 37), (5, 3), (7, 101), (8, 1000), (16, 517)])
 def test_step_simulation_equals_closed_form(oracle_mod, dtype, op, N, K):
     """The step-by-step ring simulation and the closed-form fold are written
@@ -307,7 +307,7 @@ def test_min_is_order_free_brute_force(oracle_mod):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min", "avg_premul"])
 @pytest.mark.parametrize("N,K,root", [(1, 5, 0), (3, 5, 0), (4, 37, 3), (8, 1000, 5), (5, 3, 2)])
 def test_reduce_is_allreduce_at_root_others_unchanged(oracle_mod, dtype, op, N, K, root):
     """AllReduce = Reduce + Broadcast (Lesson 3, core concepts): the root gets
@@ -366,7 +366,7 @@ def test_avg_is_the_correctly_rounded_quotient(oracle_mod, N):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("op", ["sum", "prod", "avg"])
+@pytest.mark.parametrize("op", ["sum", "prod", "avg", "avg_premul"])
 @pytest.mark.parametrize("N,L", [(3, 7), (4, 16), (5, 3), (8, 9)])
 def test_ring_order_is_rotation_equivariant(oracle_mod, dtype, op, N, L):
     """Chunk c is folded starting at rank c, so relabelling ranks and chunks by
@@ -390,7 +390,7 @@ def test_ring_order_is_rotation_equivariant(oracle_mod, dtype, op, N, L):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "min", "avg_premul"])
 @pytest.mark.parametrize("N,K,threads", [(8, 1000, 8), (8, 1001, 3), (5, 37, 2), (16, 517, 16), (3, 2, 3), (1, 9, 1)])
 def test_threaded_ring_equals_single_thread(oracle_mod, dtype, op, N, K, threads):
     """The CPU baseline's multi-core form (ranks on threads, a barrier per
@@ -438,10 +438,81 @@ def test_error_bound_against_fp64(oracle_mod, dtype, op, N, K, rtol):
     assert np.linalg.norm(err) <= rtol * np.linalg.norm(y64)
 
 
+# ---------------------------------------------------------------- pre-multiplied AVG
+
+def _prescaled(x, dtype, N):
+    """Each contribution times the float32 reciprocal of N, rounded to the
+    buffer type: numpy's float32 division and multiplication (IEEE, round to
+    nearest even) and torch's bf16 conversion."""
+    inv = np.float32(1) / np.float32(N)
+    with np.errstate(invalid="ignore", over="ignore", under="ignore"):
+        if dtype == "bf16":
+            return [W.to_bf16_bits(W.bf16_bits_to_f32(r) * inv) for r in x]
+        return [(np.asarray(r, dtype=np.float32) * inv).astype(np.float32) for r in x]
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("N", [3, 5, 6, 7, 12])
+def test_avg_premul_is_the_sum_of_prescaled_contributions(oracle_mod, dtype, N):
+    """NCCL's pre-multiplied AVG (Collective Communication, libraries section)
+    scales every contribution by 1/N before the ring sums them and divides
+    nothing at the end: the result must be the ring SUM of the contributions
+    scaled here independently, special values included.  For N not a power of
+    two it must differ from AVG's single division somewhere."""
+    K = 3001
+    x = _inputs(dtype, N, K, seed=N * 17)
+    p, _ = oracle_mod.ring_allreduce(x, "avg_premul")
+    s, _ = oracle_mod.ring_allreduce(_prescaled(x, dtype, N), "sum")
+    a, _ = oracle_mod.ring_allreduce(x, "avg")
+    for r in range(N):
+        np.testing.assert_array_equal(_bits(p[r]), _bits(s[r]))
+    assert (_bits(p[0]) != _bits(a[0])).any()
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
+def test_avg_premul_power_of_two_equals_avg(oracle_mod, dtype, N):
+    """For N a power of two, 1/N is exact and multiplying by it only shifts
+    the exponent; rounding commutes with that shift away from the subnormal
+    range, so scaling before the sum and dividing after it give the same bits.
+    N = 1 leaves every value unchanged."""
+    K = 4099
+    x = list(W.normal_bf16(N, K, std=1e-3, seed_base=N)) if dtype == "bf16" else \
+        list(W.normal_fp32(N, K, seed_base=N))
+    p, _ = oracle_mod.ring_allreduce(x, "avg_premul")
+    a, _ = oracle_mod.ring_allreduce(x, "avg")
+    for r in range(N):
+        np.testing.assert_array_equal(_bits(p[r]), _bits(a[r]))
+    if N == 1:
+        np.testing.assert_array_equal(_bits(p[0]), _bits(x[0]))
+
+
+@pytest.mark.parametrize("dtype,N,K", [("bf16", 8, 20000), ("bf16", 6, 20000), ("fp32", 5, 9999),
+                                       ("fp32", 16, 5000)])
+def test_avg_premul_error_bound_against_fp64(oracle_mod, dtype, N, K):
+    """Against the fp64 mean m = sum_r x_r / N: each scaled contribution
+    carries the reciprocal's and the product's fp32 roundings (and, for bf16,
+    one rounding to bf16); the N-1 hops add one rounding each.  So
+    |y - m| <= gamma_(N+1) * sum_r |x_r| / N, with gamma_n = n u / (1 - n u)
+    and u the per-rounding unit (2^-8 + 2^-24 for bf16, 2^-24 for fp32)."""
+    if dtype == "bf16":
+        x = list(W.normal_bf16(N, K, std=1e-3, seed_base=3))
+        u = 2.0 ** -8 + 2.0 ** -24
+    else:
+        x = list(W.uniform_fp32(N, K, seed_base=3))
+        u = 2.0 ** -24
+    outs, _ = oracle_mod.ring_allreduce(x, "avg_premul")
+    y = W.bf16_bits_to_f32(outs[0]) if dtype == "bf16" else outs[0]
+    m, absum = oracle_mod.sum_f64(x, "avg_premul")
+    n = N + 1
+    bound = n * u / (1 - n * u) * absum * (1 + 1e-9) + 1e-300
+    assert np.all(np.abs(y.astype(np.float64) - m) <= bound)
+
+
 # ---------------------------------------------------------------- composition invariants
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "prod", "avg_premul"])
 @pytest.mark.parametrize("N,K", [(3, 10), (4, 4), (5, 2), (8, 77), (16, 259)])
 def test_allreduce_equals_reducescatter_then_allgather(oracle_mod, dtype, op, N, K):
     """AllReduce = AllGather o ReduceScatter (Collectives and sharded matmul,
@@ -524,22 +595,22 @@ def test_c4_bucket_count(oracle_mod):
     assert (n_full, last) == (61, 9_994_240)
 
 
-def test_bucket_allreduce_matches_flatten_and_ring(oracle_mod):
+@pytest.mark.parametrize("op,N", [("sum", 4), ("avg", 3), ("avg_premul", 3)])
+def test_bucket_allreduce_matches_flatten_and_ring(oracle_mod, op, N):
     """Bucket fusion (Collective Communication, 'Bucket fusion'): tensors are
     laid out in reverse registration order, cut into fixed-size buckets, and
     each bucket is an independent ring AllReduce.  The packing is re-done here
     with numpy (concatenate reversed, split) and compared."""
-    N = 4
     numels = [5, 17, 3, 40, 1, 26]
     be = 13
     grads = [[W.to_bf16_bits(W.normal_fp32(1, n, seed_base=100 * r + t)[0]) for t, n in enumerate(numels)]
              for r in range(N)]
-    got = oracle_mod.bucket_allreduce(grads, be, "sum")
+    got = oracle_mod.bucket_allreduce(grads, be, op)
     streams = [np.concatenate(grads[r][::-1]) for r in range(N)]
     total = streams[0].size
     res = [np.empty_like(s) for s in streams]
     for b0 in range(0, total, be):
-        outs, _ = oracle_mod.ring_allreduce([s[b0:b0 + be] for s in streams], "sum")
+        outs, _ = oracle_mod.ring_allreduce([s[b0:b0 + be] for s in streams], op)
         for r in range(N):
             res[r][b0:b0 + be] = outs[r]
     for r in range(N):
