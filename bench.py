@@ -215,6 +215,8 @@ ROWS = {
     "allreduce-hd": "AllReduce AVG in halving-doubling order, N=8 bf16 64Mi/rank, in place, one pass",
     "allreduce-tree": "AllReduce AVG in binomial-tree order, N=8 bf16 64Mi/rank, in place, one pass",
     "allreduce-hier": "AllReduce AVG in two-level hierarchical order (2 groups of 4), N=8 bf16 64Mi/rank, in place",
+    "allreduce-premul": "AllReduce AVG by pre-multiplication (each contribution times 1/N, then SUM), N=8 bf16 "
+                        "64Mi/rank, in place, fused ring order",
     "allreduce-int8": "compressed AllReduce AVG with error feedback, blockwise INT8 (b=128), N=8 bf16 64Mi/rank",
     "overlap": "bucket AllReduce (4 Llama layers, N=8 bf16, 25 MiB buckets) overlapped with a synthetic backward "
                "pass of per-rank gradient GEMMs (4096 tokens); bucket kernels on a second stream as gradients finish",
@@ -355,6 +357,20 @@ def run_row(args, name, local):
         print(json.dumps(line("AllReduce (%s order) HBM GB/s, N=8 bf16 128 MB/rank, 1 GB300" % algo, 2 * N * K * 2,
                               per, launches, kernel, "bf16", {"nranks": N, "count": K, "algo": algo},
                               {"clocks": clk}, total_ms=tot)))
+        return
+
+    if name == "allreduce-premul":
+        N, K = 8, 64 * 1024 * 1024
+        arena = RankArena(N, K, torch.bfloat16, device=dev)
+        for r in range(N):
+            arena.ranks[r].copy_(randn_bf16(K))
+        step = lambda: ccl.ccl_allreduce(arena.ranks, op="avg_premul", stream=stream)
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        print(json.dumps(line("AllReduce (pre-multiplied AVG) HBM GB/s, N=8 bf16 128 MB/rank, 1 GB300", 2 * N * K * 2,
+                              per, launches, "fused_reduce_kernel<bf16, AVG_PREMUL, 8 ranks>", "bf16",
+                              {"nranks": N, "count": K, "op": "avg_premul"}, {"clocks": clk}, total_ms=tot)))
         return
 
     if name == "overlap":

@@ -20,7 +20,15 @@
  * fp32, round-to-nearest-even for bf16).  A NaN result is the canonical quiet
  * NaN (fp32 0x7FFFFFFF, bf16 0x7FFF).  AVG sums around the ring, then divides
  * the finished chunk once by N in fp32 before the gather, so every rank gets
- * identical bits.  MAX is NaN if either side is NaN, else the larger, and
+ * identical bits.  AVG_PREMUL is NCCL's pre-multiplied average (Collective
+ * Communication, libraries section on NCCL): every contribution is first
+ * multiplied in fp32 by the correctly rounded reciprocal of N and rounded to
+ * the buffer type, the scaled values are summed around the ring as SUM does,
+ * and nothing is divided at the end.  It differs from AVG in the last bits for
+ * N not a power of two (the same bits for N a power of two, barring
+ * subnormals); its partial sums stay near the inputs' magnitude, where the
+ * plain sum that AVG divides can overflow first.  MAX is NaN if
+ * either side is NaN, else the larger, and
  * +0 against -0 gives +0; MIN likewise takes the smaller, and -0 wins the tie
  * (the pages list sum, min and max as the reductions: Collective
  * Communication, table of the six core primitives).
@@ -78,7 +86,14 @@ extern "C" {
 #define CCL_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 typedef enum { CCL_FP32 = 0, CCL_BF16 = 1 } ccl_dtype_t;
-typedef enum { CCL_SUM = 0, CCL_AVG = 1, CCL_MAX = 2, CCL_PROD = 3, CCL_MIN = 4 } ccl_op_t;
+typedef enum {
+    CCL_SUM = 0,
+    CCL_AVG = 1,
+    CCL_MAX = 2,
+    CCL_PROD = 3,
+    CCL_MIN = 4,
+    CCL_AVG_PREMUL = 5 /* AllReduce, ReduceScatter, Reduce, bucket and host-buffer calls; ring order only */
+} ccl_op_t;
 typedef enum { CCL_MODE_FUSED = 0, CCL_MODE_STEP = 1 } ccl_mode_t;
 typedef enum {
     CCL_ALGO_RING = 0,
@@ -235,9 +250,10 @@ ccl_status_t ccl_bucketer_destroy(ccl_bucketer_t *b);
  *     consecutive ranks, ring AllReduce among the groups' representatives,
  *     ring AllGather inside the groups (AllReduce survey, two-level table);
  *     group_size must divide nranks (1 or nranks gives the flat ring).
- * AVG divides the finished sum once by N.  Buffers as ccl_allreduce (in place
- * when send[r] == recv[r]).  group_size is ignored except for
- * CCL_ALGO_HIERARCHICAL. */
+ * AVG divides the finished sum once by N; CCL_AVG_PREMUL is accepted with
+ * CCL_ALGO_RING only (CCL_ERR_UNSUPPORTED otherwise).  Buffers as
+ * ccl_allreduce (in place when send[r] == recv[r]).  group_size is ignored
+ * except for CCL_ALGO_HIERARCHICAL. */
 ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int nranks, size_t count,
                                 ccl_dtype_t dtype, ccl_op_t op, ccl_algo_t algo, int group_size,
                                 cudaStream_t stream);
@@ -253,9 +269,9 @@ ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int 
  *   CCL_COMP_THRESHOLD (the greedy 1-bit compressor of the pages' Tables 3
  *     and 4): v = 1 when u >= threshold, else 0.
  * The transmitted v are AllReduced in ring order in fp32 (op CCL_SUM, or
- * CCL_AVG dividing once by N) and rounded once to dtype, written to every
- * grads[r].  Up to 16 ranks; grads and residuals must not overlap.  One
- * launch. */
+ * CCL_AVG dividing once by N; CCL_AVG_PREMUL returns CCL_ERR_UNSUPPORTED) and
+ * rounded once to dtype, written to every grads[r].  Up to 16 ranks; grads
+ * and residuals must not overlap.  One launch. */
 ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residuals, int nranks, size_t count,
                                       ccl_dtype_t dtype, ccl_op_t op, ccl_compressor_t comp, int block,
                                       float threshold, cudaStream_t stream);

@@ -17,9 +17,9 @@ import torch
 from .build import LIB as _LIB_PATH
 
 FP32, BF16 = 0, 1
-SUM, AVG, MAX, PROD, MIN = 0, 1, 2, 3, 4
+SUM, AVG, MAX, PROD, MIN, AVG_PREMUL = 0, 1, 2, 3, 4, 5
 FUSED, STEP = 0, 1
-OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN}
+OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN, "avg_premul": AVG_PREMUL}
 MODES = {"fused": FUSED, "step": STEP}
 ALGOS = {"ring": 0, "halving_doubling": 1, "tree": 2, "hierarchical": 3}
 COMPRESSORS = {"int8_block": 0, "threshold": 1}

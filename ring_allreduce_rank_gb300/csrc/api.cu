@@ -21,8 +21,15 @@ size_t elem_size(ccl_dtype_t dt) { return dt == CCL_BF16 ? 2 : 4; }
 bool valid_dtype(ccl_dtype_t dt) { return dt == CCL_FP32 || dt == CCL_BF16; }
 bool valid_op(ccl_op_t op)
 {
-    return op == CCL_SUM || op == CCL_AVG || op == CCL_MAX || op == CCL_PROD || op == CCL_MIN;
+    return op == CCL_SUM || op == CCL_AVG || op == CCL_MAX || op == CCL_PROD || op == CCL_MIN ||
+           op == CCL_AVG_PREMUL;
 }
+// Operators that change a value even with one rank (x / 1 or x * 1 turns a
+// NaN into the canonical NaN), so N = 1 in place is not a no-op for them.
+bool scales(int op) { return op == CCL_AVG || op == CCL_AVG_PREMUL; }
+// Step mode: a separate scaling launch after the ReduceScatter phase -- AVG's
+// division, or the pre-multiplied AVG's scaling when N = 1 gives it no hop.
+bool step_scale(int op, int nranks) { return op == CCL_AVG || (op == CCL_AVG_PREMUL && nranks == 1); }
 bool valid_mode(ccl_mode_t m) { return m == CCL_MODE_FUSED || m == CCL_MODE_STEP; }
 bool valid_ranks(int n) { return n >= 1 && n <= CCL_MAX_RANKS; }
 
@@ -113,7 +120,7 @@ ccl_status_t ring_steps_allreduce(int dt, int op, void *const *bufs, int nranks,
     for (int s = 0; s < nranks - 1; ++s)
         if (cudaError_t e = launch_ring_step(dt, op, STEP_RS, s, bufs, nranks, count, st))
             return from_cuda(e);
-    if (op == OP_AVG)
+    if (step_scale(op, nranks))
         if (cudaError_t e = launch_ring_step(dt, op, STEP_SCALE, 0, bufs, nranks, count, st))
             return from_cuda(e);
     for (int s = 0; s < nranks - 1; ++s)
@@ -317,7 +324,7 @@ static ccl_status_t ccl_allreduce_impl(const void *const *send, void *const *rec
     if (st != CCL_OK)
         return st;
     CCL_DBG(w, r, {}, stream);
-    if (nranks == 1 && in_place && op != CCL_AVG)
+    if (nranks == 1 && in_place && !scales(op))
         return CCL_OK;
     if (mode == CCL_MODE_FUSED)
         return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_ALL, 0, stream));
@@ -368,7 +375,7 @@ static ccl_status_t ccl_reduce_scatter_impl(const void *const *send, void *const
     for (int s = 0; s < nranks - 1; ++s)
         if (cudaError_t e = launch_ring_step((int)dtype, (int)op, STEP_RS, s, bufs.data(), nranks, count, stream))
             return from_cuda(e);
-    if (op == CCL_AVG)
+    if (step_scale(op, nranks))
         if (cudaError_t e = launch_ring_step((int)dtype, (int)op, STEP_SCALE, 0, bufs.data(), nranks, count, stream))
             return from_cuda(e);
     // the phase leaves chunk c at rank c-1; hand it to rank c
@@ -681,7 +688,7 @@ static ccl_status_t ccl_reduce_impl(const void *const *send, void *const *recv, 
     for (int s = 0; s < nranks - 1; ++s)
         if (cudaError_t e = launch_ring_step((int)dtype, (int)op, STEP_RS, s, bufs.data(), nranks, count, stream))
             return from_cuda(e);
-    if (op == CCL_AVG)
+    if (step_scale(op, nranks))
         if (cudaError_t e = launch_ring_step((int)dtype, (int)op, STEP_SCALE, 0, bufs.data(), nranks, count, stream))
             return from_cuda(e);
     const Partition part = make_partition(count, nranks);
@@ -778,6 +785,8 @@ static ccl_status_t ccl_allreduce_algo_impl(const void *const *send, void *const
         return CCL_ERR_INVALID_ARG;
     if (algo == CCL_ALGO_HIERARCHICAL && (group_size < 1 || nranks % group_size != 0))
         return CCL_ERR_INVALID_ARG;
+    if (op == CCL_AVG_PREMUL && algo != CCL_ALGO_RING)
+        return CCL_ERR_UNSUPPORTED; // the other orders divide once, at the end
     const size_t es = elem_size(dtype);
     if (mul_overflows(count, es))
         return CCL_ERR_INVALID_ARG;
@@ -821,6 +830,8 @@ static ccl_status_t ccl_allreduce_compressed_impl(void *const *grads, float *con
                                       ccl_dtype_t dtype, ccl_op_t op, ccl_compressor_t comp, int block,
                                       float threshold, cudaStream_t stream)
 {
+    if (op == CCL_AVG_PREMUL)
+        return CCL_ERR_UNSUPPORTED; // the compressed AllReduce divides once, at the end
     if (nranks < 1 || nranks > 16 || !valid_dtype(dtype) || (op != CCL_SUM && op != CCL_AVG) || !grads ||
         !residuals || (comp != CCL_COMP_INT8_BLOCK && comp != CCL_COMP_THRESHOLD) ||
         (comp == CCL_COMP_INT8_BLOCK && block != 64 && block != 128))
@@ -901,7 +912,7 @@ static ccl_status_t ccl_allreduce_host_impl(const void *const *send, void *const
     if (cap != cudaStreamCaptureStatusNone)
         return CCL_ERR_UNSUPPORTED;
     CCL_DBG(w, r, {}, stream);
-    if (nranks == 1 && in_place && op != CCL_AVG)
+    if (nranks == 1 && in_place && !scales(op))
         return CCL_OK;
     return from_cuda(run_host_allreduce((int)dtype, (int)op, send, recv, nranks, count, work, work_bytes, stream));
 }

@@ -28,7 +28,7 @@ struct BucketParams {
     uint32_t nseg;
     int nranks;
     float n_f;
-    uint32_t pad;
+    float inv_n; // 1/nranks correctly rounded (pre-multiplied AVG)
 };
 
 // One tile of one segment: fold its positions over the ranks in ring order
@@ -55,7 +55,7 @@ __device__ __forceinline__ void bucket_tile(const BucketParams &p, uint64_t tile
     const uint64_t off = s.off, end = s.off + s.len;
 
     auto do_elem = [&](uint64_t e) {
-        uint32_t acc = ring_fold_elem<DT, OP>(ptrs, N, c, e);
+        uint32_t acc = ring_fold_elem<DT, OP>(ptrs, N, c, e, p.inv_n);
         if (OP == OP_AVG)
             acc = avg_elem<DT>(acc, p.n_f);
         for (int q = 0; q < N; ++q)
@@ -83,7 +83,7 @@ __device__ __forceinline__ void bucket_tile(const BucketParams &p, uint64_t tile
     const uint64_t v = vb + t * TV + threadIdx.x;
     if (v >= ve)
         return;
-    uint4 acc = ring_fold_vec<DT, OP, NR>(ptrs, N, c, v * 16);
+    uint4 acc = ring_fold_vec<DT, OP, NR>(ptrs, N, c, v * 16, p.inv_n);
     if (OP == OP_AVG)
         acc = avg_vec<DT>(acc, p.n_f);
     if (NR > 0) {
@@ -150,7 +150,7 @@ static cudaError_t launch_bucket_t(void *const *tensor_ptrs, int ntensors, int n
         p.nseg = 0;
         p.nranks = nranks;
         p.n_f = (float)nranks;
-        p.pad = 0;
+        p.inv_n = 1.0f / (float)nranks;
     };
     reset();
     uint32_t nptr = 0;
@@ -204,6 +204,7 @@ static cudaError_t launch_bucket_dt(int op, void *const *tp, int nt, int nr, con
     case OP_MAX: return launch_bucket_t<DT, OP_MAX>(tp, nt, nr, s, ns, mc, st);
     case OP_PROD: return launch_bucket_t<DT, OP_PROD>(tp, nt, nr, s, ns, mc, st);
     case OP_MIN: return launch_bucket_t<DT, OP_MIN>(tp, nt, nr, s, ns, mc, st);
+    case OP_AVGP: return launch_bucket_t<DT, OP_AVGP>(tp, nt, nr, s, ns, mc, st);
     }
     return cudaErrorInvalidValue;
 }

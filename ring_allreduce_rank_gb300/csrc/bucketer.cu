@@ -41,7 +41,8 @@ ccl_status_t ccl_bucketer_create(void *const *ptrs, const size_t *numels, int nt
                                  ccl_bucketer_t **out)
 {
     if (!out || max_ctas < 0 || nranks < 1 || nranks > CCL_MAX_RANKS || (dtype != CCL_FP32 && dtype != CCL_BF16) ||
-        (op != CCL_SUM && op != CCL_AVG && op != CCL_MAX && op != CCL_PROD && op != CCL_MIN) || ntensors < 1 ||
+        (op != CCL_SUM && op != CCL_AVG && op != CCL_MAX && op != CCL_PROD && op != CCL_MIN &&
+         op != CCL_AVG_PREMUL) || ntensors < 1 ||
         !ptrs || !numels)
         return CCL_ERR_INVALID_ARG;
     *out = nullptr;

@@ -10,7 +10,7 @@
 namespace ccl {
 
 enum { DT_FP32 = 0, DT_BF16 = 1 };
-enum { OP_SUM = 0, OP_AVG = 1, OP_MAX = 2, OP_PROD = 3, OP_MIN = 4 };
+enum { OP_SUM = 0, OP_AVG = 1, OP_MAX = 2, OP_PROD = 3, OP_MIN = 4, OP_AVGP = 5 };
 
 constexpr int kThreads = 256;
 
@@ -139,7 +139,7 @@ template <int OP> __device__ __forceinline__ float op_f32(float local, float acc
 {
     if (OP == OP_PROD)
         return __fmul_rn(local, acc);
-    return __fadd_rn(local, acc); // SUM and AVG
+    return __fadd_rn(local, acc); // SUM, AVG and pre-multiplied AVG
 }
 
 // One ring hop on one fp32 element: local (+) incoming.
@@ -229,14 +229,56 @@ template <int DT> __device__ __forceinline__ uint4 avg_vec(const uint4 &v, float
     return r;
 }
 
+// AVG by pre-multiplication (NCCL's pre-multiplied sum, Collective
+// Communication, libraries section): a contribution x enters the ring as
+// x * inv rounded to the buffer type, inv being the correctly rounded fp32
+// reciprocal of N, and the ring then sums; nothing is divided at the end.
+// Every other operator takes its contributions unchanged.
+__device__ __forceinline__ uint32_t premul_bf16x2(uint32_t v, float inv)
+{
+    const float r0 = __fmul_rn(__uint_as_float(v << 16), inv);
+    const float r1 = __fmul_rn(__uint_as_float(v & 0xffff0000u), inv);
+    __nv_bfloat162 p = __floats2bfloat162_rn(r0, r1);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+template <int DT, int OP> __device__ __forceinline__ uint32_t pre_elem(uint32_t v, float inv)
+{
+    if (OP != OP_AVGP)
+        return v;
+    if (DT == DT_FP32)
+        return __float_as_uint(__fmul_rn(__uint_as_float(v), inv));
+    return premul_bf16x2(v, inv) & 0xffffu;
+}
+
+template <int DT, int OP> __device__ __forceinline__ uint4 pre_vec(const uint4 &v, float inv)
+{
+    if (OP != OP_AVGP)
+        return v;
+    uint4 r;
+    if (DT == DT_FP32) {
+        r.x = __float_as_uint(__fmul_rn(__uint_as_float(v.x), inv));
+        r.y = __float_as_uint(__fmul_rn(__uint_as_float(v.y), inv));
+        r.z = __float_as_uint(__fmul_rn(__uint_as_float(v.z), inv));
+        r.w = __float_as_uint(__fmul_rn(__uint_as_float(v.w), inv));
+    } else {
+        r.x = premul_bf16x2(v.x, inv);
+        r.y = premul_bf16x2(v.y, inv);
+        r.z = premul_bf16x2(v.z, inv);
+        r.w = premul_bf16x2(v.w, inv);
+    }
+    return r;
+}
+
 // ------------------------------------------------------------------ ring folds over a pointer table
 
 // Fold one 16-byte vector of every rank in ring order starting at rank c:
 // x_c, then x_{c+1} (+) acc, ..., x_{c-1} (+) acc.  ptrs[r] is rank r's base.
 // NR > 0: exactly NR ranks, all loads issued before the first hop.
 // NR == 0: any N, ranks in groups of 8 with the next group's loads in flight.
+// inv: the reciprocal of N for the pre-multiplied AVG (unused otherwise).
 template <int DT, int OP, int NR>
-__device__ __forceinline__ uint4 ring_fold_vec(const void *const *ptrs, int N, int c, uint64_t byte_off)
+__device__ __forceinline__ uint4 ring_fold_vec(const void *const *ptrs, int N, int c, uint64_t byte_off, float inv)
 {
     if (NR > 0) {
         uint4 x[NR > 0 ? NR : 1];
@@ -246,10 +288,10 @@ __device__ __forceinline__ uint4 ring_fold_vec(const void *const *ptrs, int N, i
             x[k] = ld16(static_cast<const char *>(ptrs[r]) + byte_off);
             r = (r + 1 == NR) ? 0 : r + 1;
         }
-        uint4 acc = x[0];
+        uint4 acc = pre_vec<DT, OP>(x[0], inv);
 #pragma unroll
         for (int k = 1; k < NR; ++k)
-            acc = hop_vec<DT, OP>(x[k], acc);
+            acc = hop_vec<DT, OP>(pre_vec<DT, OP>(x[k], inv), acc);
         return acc;
     }
     uint4 acc = make_uint4(0, 0, 0, 0);
@@ -271,7 +313,7 @@ __device__ __forceinline__ uint4 ring_fold_vec(const void *const *ptrs, int N, i
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (g + j < N)
-                acc = (g + j == 0) ? cur[0] : hop_vec<DT, OP>(cur[j], acc);
+                acc = (g + j == 0) ? pre_vec<DT, OP>(cur[0], inv) : hop_vec<DT, OP>(pre_vec<DT, OP>(cur[j], inv), acc);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             cur[j] = nxt[j];
@@ -280,14 +322,14 @@ __device__ __forceinline__ uint4 ring_fold_vec(const void *const *ptrs, int N, i
 }
 
 template <int DT, int OP>
-__device__ __forceinline__ uint32_t ring_fold_elem(const void *const *ptrs, int N, int c, uint64_t e)
+__device__ __forceinline__ uint32_t ring_fold_elem(const void *const *ptrs, int N, int c, uint64_t e, float inv)
 {
     int r = c;
-    uint32_t acc = ld_elem<DT>(ptrs[r], e);
+    uint32_t acc = pre_elem<DT, OP>(ld_elem<DT>(ptrs[r], e), inv);
     for (int k = 1; k < N; ++k) {
         if (++r == N)
             r = 0;
-        acc = hop_elem<DT, OP>(ld_elem<DT>(ptrs[r], e), acc);
+        acc = hop_elem<DT, OP>(pre_elem<DT, OP>(ld_elem<DT>(ptrs[r], e), inv), acc);
     }
     return acc;
 }

@@ -19,7 +19,7 @@ enum StepKind {
     STEP_RS = 0,     // rank i: chunk (i-1-s) += rank (i-1)'s copy
     STEP_AG = 1,     // rank i: chunk (i-s) = rank (i-1)'s copy (after the RS phase)
     STEP_AG_API = 2, // rank i: chunk (i-1-s) = rank (i-1)'s copy (AllGather from chunk i at rank i)
-    STEP_SCALE = 3   // rank i: chunk (i+1) /= N (AVG, at the holder)
+    STEP_SCALE = 3   // rank i: chunk (i+1) /= N (AVG, at the holder); pre-multiplied AVG: *= 1/N
 };
 
 template <int MAXR> struct StepParams {
@@ -31,6 +31,7 @@ template <int MAXR> struct StepParams {
     int vec_aligned;
     uint32_t tiles;
     float n_f;
+    float inv_n; // 1/nranks correctly rounded (pre-multiplied AVG)
 };
 
 cudaError_t launch_ring_step(int dt, int op, int kind, int s, void *const *bufs, int nranks, uint64_t count,

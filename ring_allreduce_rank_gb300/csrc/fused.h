@@ -25,6 +25,7 @@ template <int MAXR> struct FusedParams {
     int vec_aligned; // every pointer is 16-byte aligned
     uint32_t tiles;  // tiles per chunk (gridDim.x)
     float n_f;       // (float)nranks, the AVG divisor
+    float inv_n;     // 1/nranks correctly rounded, the pre-multiplied AVG's scale
 };
 
 enum WriteMode {

@@ -6,7 +6,8 @@
 // copy) carries chunk c from rank c through c+1, ..., c-1, adding one
 // contribution per hop.  Its end state is, per element of chunk c, the fold
 //     R = x_{c-1} (+) ( ... (x_{c+1} (+) x_c))
-// rounded to the buffer type after every hop, AVG dividing once by N, and the
+// rounded to the buffer type after every hop, AVG dividing once by N (the
+// pre-multiplied AVG instead scales every x_r by 1/N as it is loaded), and the
 // AllGather phase (AllReduce survey, phase 2) copying R to every rank.  This
 // kernel computes that end state directly: each element's N contributions are
 // read once, folded in ring order in registers, and written once per rank --
@@ -35,11 +36,11 @@ __device__ __forceinline__ void reduce_elem(const FusedParams<MAXR> &p, int N, u
                                             uint64_t out_base)
 {
     int r = (int)c;
-    uint32_t acc = ld_elem<DT>(p.send[r], e);
+    uint32_t acc = pre_elem<DT, OP>(ld_elem<DT>(p.send[r], e), p.inv_n);
     for (int k = 1; k < N; ++k) {
         if (++r == N)
             r = 0;
-        acc = hop_elem<DT, OP>(ld_elem<DT>(p.send[r], e), acc);
+        acc = hop_elem<DT, OP>(pre_elem<DT, OP>(ld_elem<DT>(p.send[r], e), p.inv_n), acc);
     }
     if (OP == OP_AVG)
         acc = avg_elem<DT>(acc, p.n_f);
@@ -76,7 +77,7 @@ __device__ __forceinline__ void reduce_scatter_shifted(const FusedParams<MAXR> &
     const uint64_t a = a0 + j0 + lane;
     uint4 r = make_uint4(0, 0, 0, 0);
     if ((a + 1) * VEC <= K) {
-        r = ring_fold_vec<DT, OP, NR>(p.send, N, (int)c, a * 16);
+        r = ring_fold_vec<DT, OP, NR>(p.send, N, (int)c, a * 16, p.inv_n);
         if (OP == OP_AVG)
             r = avg_vec<DT>(r, p.n_f);
     } else {
@@ -87,7 +88,7 @@ __device__ __forceinline__ void reduce_scatter_shifted(const FusedParams<MAXR> &
             const uint64_t e = a * VEC + k;
             uint32_t v = 0;
             if (e < K) {
-                v = ring_fold_elem<DT, OP>(p.send, N, (int)c, e);
+                v = ring_fold_elem<DT, OP>(p.send, N, (int)c, e, p.inv_n);
                 if (OP == OP_AVG)
                     v = avg_elem<DT>(v, p.n_f);
             }
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) small_chunk_kernel(const __grid_cons
         return;
     for (int i = threadIdx.x; i < N * L; i += kThreads) {
         const int r = i / L;
-        sx[i] = ld_elem<DT>(p.send[r], off + (uint64_t)(i - r * L));
+        sx[i] = pre_elem<DT, OP>(ld_elem<DT>(p.send[r], off + (uint64_t)(i - r * L)), p.inv_n);
     }
     __syncthreads();
     uint32_t *res = sx + (size_t)N * L;
@@ -229,10 +230,10 @@ __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_con
         for (int u = 0; u < U; ++u) {
             const uint64_t v = v0 + (uint64_t)u * kThreads;
             if (v < ve) {
-                uint4 acc = x[u][0];
+                uint4 acc = pre_vec<DT, OP>(x[u][0], p.inv_n);
 #pragma unroll
                 for (int k = 1; k < NR; ++k)
-                    acc = hop_vec<DT, OP>(x[u][k], acc);
+                    acc = hop_vec<DT, OP>(pre_vec<DT, OP>(x[u][k], p.inv_n), acc);
                 if (OP == OP_AVG)
                     acc = avg_vec<DT>(acc, p.n_f);
                 if (p.write_mode == WRITE_ALL) {
@@ -272,7 +273,8 @@ __global__ void __launch_bounds__(kThreads) fused_reduce_kernel(const __grid_con
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (g + j < N)
-                    acc = (g + j == 0) ? cur[0] : hop_vec<DT, OP>(cur[j], acc);
+                    acc = (g + j == 0) ? pre_vec<DT, OP>(cur[0], p.inv_n)
+                                       : hop_vec<DT, OP>(pre_vec<DT, OP>(cur[j], p.inv_n), acc);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -318,6 +320,7 @@ static cudaError_t launch_t(const void *const *send, void *const *recv, int nran
     p.root = root;
     p.vec_aligned = aligned ? 1 : 0;
     p.n_f = (float)nranks;
+    p.inv_n = 1.0f / (float)nranks;
     if (NR == 0 && nranks > kSmallRanks) {
         const uint64_t lmax = p.part.q + (p.part.rem ? 1 : 0);
         const size_t smem = ((size_t)nranks + 1) * (size_t)lmax * sizeof(uint32_t);
@@ -377,6 +380,7 @@ static cudaError_t launch_dt(int op, const void *const *send, void *const *recv,
     case OP_MAX: return launch_op<DT, OP_MAX>(send, recv, nranks, count, write_mode, root, stream);
     case OP_PROD: return launch_op<DT, OP_PROD>(send, recv, nranks, count, write_mode, root, stream);
     case OP_MIN: return launch_op<DT, OP_MIN>(send, recv, nranks, count, write_mode, root, stream);
+    case OP_AVGP: return launch_op<DT, OP_AVGP>(send, recv, nranks, count, write_mode, root, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -8,18 +8,38 @@
 // Within one step the chunk a rank receives is never the chunk its right
 // neighbour reads from it, so a step can run in place with no snapshot; the
 // stream order between launches is the step barrier.
+//
+// Pre-multiplied AVG: rank i adds into chunk (i-1-s) only at step s, so its
+// own copy is still the unscaled input then and is scaled as it is read; what
+// arrives was scaled by its sender, except at step 0, where rank i-1 sends an
+// untouched input chunk.  That scales every contribution exactly once without
+// a separate pass over the buffers (N = 1, which has no steps, scales with
+// one STEP_SCALE launch).
+
 #include "ccl_internal.h"
 
 namespace ccl {
+
+// Incoming operand of a ReduceScatter hop: only at step 0 is it an input.
+template <int DT, int OP> __device__ __forceinline__ uint32_t incoming_elem(uint32_t v, int s, float inv)
+{
+    return (OP == OP_AVGP && s == 0) ? pre_elem<DT, OP>(v, inv) : v;
+}
+
+template <int DT, int OP> __device__ __forceinline__ uint4 incoming_vec(const uint4 &v, int s, float inv)
+{
+    return (OP == OP_AVGP && s == 0) ? pre_vec<DT, OP>(v, inv) : v;
+}
 
 template <int DT, int OP, int MAXR>
 __device__ __forceinline__ void step_elem(const StepParams<MAXR> &p, int kind, int i, int left, uint64_t e)
 {
     if (kind == STEP_RS) {
-        const uint32_t incoming = ld_elem<DT>(p.buf[left], e);
-        st_elem<DT>(p.buf[i], e, hop_elem<DT, OP>(ld_elem<DT>(p.buf[i], e), incoming));
+        const uint32_t incoming = incoming_elem<DT, OP>(ld_elem<DT>(p.buf[left], e), p.s, p.inv_n);
+        st_elem<DT>(p.buf[i], e, hop_elem<DT, OP>(pre_elem<DT, OP>(ld_elem<DT>(p.buf[i], e), p.inv_n), incoming));
     } else if (kind == STEP_SCALE) {
-        st_elem<DT>(p.buf[i], e, avg_elem<DT>(ld_elem<DT>(p.buf[i], e), p.n_f));
+        const uint32_t v = ld_elem<DT>(p.buf[i], e);
+        st_elem<DT>(p.buf[i], e, OP == OP_AVGP ? pre_elem<DT, OP>(v, p.inv_n) : avg_elem<DT>(v, p.n_f));
     } else {
         st_elem<DT>(p.buf[i], e, ld_elem<DT>(p.buf[left], e));
     }
@@ -82,9 +102,9 @@ __global__ void __launch_bounds__(kThreads) ring_step_kernel(const __grid_consta
         if (v < ve) {
             uint4 out;
             if (kind == STEP_RS)
-                out = hop_vec<DT, OP>(mine[u], theirs[u]);
+                out = hop_vec<DT, OP>(pre_vec<DT, OP>(mine[u], p.inv_n), incoming_vec<DT, OP>(theirs[u], p.s, p.inv_n));
             else if (kind == STEP_SCALE)
-                out = avg_vec<DT>(mine[u], p.n_f);
+                out = OP == OP_AVGP ? pre_vec<DT, OP>(mine[u], p.inv_n) : avg_vec<DT>(mine[u], p.n_f);
             else
                 out = theirs[u];
             st16(static_cast<char *>(p.buf[i]) + v * 16, out);
@@ -111,6 +131,7 @@ static cudaError_t launch_step_t(int kind, int s, void *const *bufs, int nranks,
     p.kind = kind;
     p.vec_aligned = aligned ? 1 : 0;
     p.n_f = (float)nranks;
+    p.inv_n = 1.0f / (float)nranks;
     const uint64_t te = (uint64_t)kThreads * 2 * VEC;
     const uint64_t tiles = (p.part.q + 1 + te - 1) / te;
     if (tiles > 0x7fffffffull)
@@ -140,6 +161,7 @@ static cudaError_t launch_step_dt(int op, int kind, int s, void *const *bufs, in
     case OP_MAX: return launch_step_op<DT, OP_MAX>(kind, s, bufs, nranks, count, stream);
     case OP_PROD: return launch_step_op<DT, OP_PROD>(kind, s, bufs, nranks, count, stream);
     case OP_MIN: return launch_step_op<DT, OP_MIN>(kind, s, bufs, nranks, count, stream);
+    case OP_AVGP: return launch_step_op<DT, OP_AVGP>(kind, s, bufs, nranks, count, stream);
     }
     return cudaErrorInvalidValue;
 }

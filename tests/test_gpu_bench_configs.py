@@ -6,6 +6,7 @@ rank (the headline's shape).
               hierarchical order (sampled closed-form values of each order)
   compressed  INT8 blocks of 128 + error feedback, AVG (the whole result and
               every residual, against the full oracle run)
+  premul      AllReduce with the pre-multiplied AVG (sampled closed-form values)
   reduce      Reduce SUM to rank 0 (sampled closed-form values)
   gather      Gather to rank 0, Scatter back, Broadcast from rank 0 (copies,
               compared in full)
@@ -84,6 +85,17 @@ def test_compressed_full_size(x):
     for r in range(N):
         assert_bits_equal(got_g[r], want_g[r], "compressed grads rank %d" % r)
         assert_bits_equal(got_e[r], want_e[r].view(np.uint32), "compressed residual rank %d" % r)
+
+
+def test_premul_full_size(x):
+    a = _arena(x)
+    ccl.ccl_allreduce(a.ranks, op="avg_premul")
+    torch.cuda.synchronize()
+    idx = _sample([N], seed=6)
+    want = oracle.ring_allreduce_at(list(x), idx.astype(np.uint64), "avg_premul")
+    it = torch.from_numpy(idx).to(DEV)
+    for r in range(N):
+        assert_bits_equal(bits(a.ranks[r].index_select(0, it)), want, "premul rank %d" % r)
 
 
 def test_reduce_full_size(x):
