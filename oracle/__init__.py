@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_allgather.argtypes = [pp, pp, i32, u64, i32]
             L.oracle_reduce.argtypes = [pp, pp, i32, i32, u64, i32, i32]
             L.oracle_allreduce_compressed.argtypes = [pp, pp, i32, u64, i32, i32, i32, i32, ctypes.c_float]
+            L.oracle_allreduce_compressed_k.argtypes = [pp, pp, i32, u64, i32, i32, i32, i32, ctypes.c_float, u64]
             L.oracle_allreduce_hd.argtypes = [pp, i32, u64, i32, i32]
             L.oracle_allreduce_tree.argtypes = [pp, i32, u64, i32, i32]
             L.oracle_allreduce_hier.argtypes = [pp, i32, i32, u64, i32, i32]
@@ -89,7 +90,8 @@ def lib() -> ctypes.CDLL:
             for name in ("oracle_ring_allreduce", "oracle_ring_allreduce_closed", "oracle_ring_allreduce_at",
                          "oracle_ring_allreduce_gathered", "oracle_reduce_scatter", "oracle_reduce", "oracle_gather",
                          "oracle_scatter", "oracle_allreduce_hd", "oracle_allreduce_tree", "oracle_allreduce_hier",
-                         "oracle_allreduce_order_at", "oracle_allreduce_compressed", "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
+                         "oracle_allreduce_order_at", "oracle_allreduce_compressed", "oracle_allreduce_compressed_k",
+                         "oracle_allgather", "oracle_broadcast", "oracle_alltoallv",
                          "oracle_bucket_allreduce", "oracle_sum_f64"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -264,18 +266,19 @@ def allreduce_algo_at(bufs, algo: str, idx, op="sum", group: int = 0) -> np.ndar
     return out
 
 
-COMPRESSORS = {"int8_block": 0, "threshold": 1}
+COMPRESSORS = {"int8_block": 0, "threshold": 1, "topk": 2}
 
 
-def allreduce_compressed(grads, residuals, op="sum", comp="int8_block", block=128, threshold=0.5):
+def allreduce_compressed(grads, residuals, op="sum", comp="int8_block", block=128, threshold=0.5, k=0):
     """One compressed AllReduce step with error feedback.  Returns (new grads,
-    new residuals); inputs are not modified."""
+    new residuals); inputs are not modified.  k: elements kept per rank by the
+    "topk" compressor."""
     g = [np.array(x, copy=True, order="C") for x in grads]
     e = [np.array(x, dtype=np.float32, copy=True, order="C") for x in residuals]
     N, K = len(g), g[0].size
-    _check(lib().oracle_allreduce_compressed(_ptrs(g), _ptrs(e), N, K, _dtype_code(g[0]), _op(op),
-                                             COMPRESSORS[comp], int(block), ctypes.c_float(threshold)),
-           "oracle_allreduce_compressed")
+    _check(lib().oracle_allreduce_compressed_k(_ptrs(g), _ptrs(e), N, K, _dtype_code(g[0]), _op(op),
+                                               COMPRESSORS[comp], int(block), ctypes.c_float(threshold), int(k)),
+           "oracle_allreduce_compressed_k")
     return g, e
 
 

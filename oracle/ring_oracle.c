@@ -1158,6 +1158,7 @@ int oracle_allreduce_order_at(const void **in, int N, uint64_t K, int dtype, int
 
 #define OR_COMP_INT8_BLOCK 0
 #define OR_COMP_THRESHOLD 1
+#define OR_COMP_TOPK 2
 
 static uint32_t canon(uint32_t r) { return f32_bits_is_nan(r) ? 0x7fffffffu : r; }
 static float fcanon(float x) { return bits_to_f32(canon(f32_to_bits(x))); }
@@ -1187,7 +1188,39 @@ static float round_half_even(float x)
  *     to even; q = 0 when s = 0), v = q * s; a NaN anywhere in the block makes
  *     s NaN.
  *   THRESHOLD (the greedy 1-bit compressor of Tables 3 and 4): v = 1 when
- *     u >= threshold, else 0. */
+ *     u >= threshold, else 0.
+ *   TOPK ("Top-k sparsification"): v = u where |u| >= |u|_(k), the k-th
+ *     largest magnitude, else 0 -- every element tied with the k-th is kept.
+ *     Magnitudes are ordered as the bit patterns of |u|, so a NaN counts as
+ *     larger than any number and is always kept (it reaches the result, as a
+ *     NaN in an INT8 block does).  k = 0 keeps nothing; k >= K keeps all. */
+static int cmp_desc_u32(const void *a, const void *b)
+{
+    const uint32_t x = *(const uint32_t *)a, y = *(const uint32_t *)b;
+    return x < y ? 1 : (x > y ? -1 : 0);
+}
+
+static int compress_topk(float *u, float *e, uint64_t K, uint64_t k)
+{
+    uint32_t tau = 0xffffffffu; /* k = 0: no magnitude reaches it */
+    if (k > 0 && K > 0) {
+        uint32_t *mag = malloc(K * sizeof(uint32_t));
+        if (!mag)
+            return OR_ENOMEM;
+        for (uint64_t i = 0; i < K; ++i)
+            mag[i] = f32_to_bits(u[i]) & 0x7fffffffu;
+        qsort(mag, K, sizeof(uint32_t), cmp_desc_u32); /* largest first */
+        tau = mag[(k < K ? k : K) - 1];
+        free(mag);
+    }
+    for (uint64_t i = 0; i < K; ++i) {
+        float v = (f32_to_bits(u[i]) & 0x7fffffffu) >= tau ? u[i] : 0.0f;
+        e[i] = fcanon(u[i] - v);
+        u[i] = v;
+    }
+    return OR_OK;
+}
+
 static void compress(float *u, float *e, uint64_t K, int comp, int block, float threshold)
 {
     if (comp == OR_COMP_THRESHOLD) {
@@ -1224,11 +1257,11 @@ static void compress(float *u, float *e, uint64_t K, int comp, int block, float 
  * keeps its residual, and the transmitted values are AllReduced with the ring
  * of this file in fp32 (SUM, or AVG dividing once by N); the result is rounded
  * once to the buffer type and written to every rank's grads. */
-int oracle_allreduce_compressed(void **grads, float **res, int N, uint64_t K, int dtype, int op, int comp,
-                                int block, float threshold)
+int oracle_allreduce_compressed_k(void **grads, float **res, int N, uint64_t K, int dtype, int op, int comp,
+                                  int block, float threshold, uint64_t topk)
 {
     if (bad_args(N, dtype, op) || (op != OR_SUM && op != OR_AVG) || (comp != OR_COMP_INT8_BLOCK &&
-        comp != OR_COMP_THRESHOLD) || (comp == OR_COMP_INT8_BLOCK && block < 1))
+        comp != OR_COMP_THRESHOLD && comp != OR_COMP_TOPK) || (comp == OR_COMP_INT8_BLOCK && block < 1))
         return OR_EINVAL;
     void **v = calloc((size_t)N, sizeof(void *));
     int rc = OR_OK;
@@ -1242,8 +1275,13 @@ int oracle_allreduce_compressed(void **grads, float **res, int N, uint64_t K, in
         }
         for (uint64_t i = 0; i < K; ++i)
             u[i] = fcanon(bits_to_f32(widen_bits(load(grads[r], dtype, i), dtype)) + res[r][i]);
-        compress(u, res[r], K, comp, block, threshold);
         v[r] = u;
+        if (comp == OR_COMP_TOPK) {
+            if ((rc = compress_topk(u, res[r], K, topk)) != OR_OK)
+                goto done;
+        } else {
+            compress(u, res[r], K, comp, block, threshold);
+        }
     }
     rc = oracle_ring_allreduce(v, N, K, OR_FP32, op, NULL);
     if (rc != OR_OK)
@@ -1256,6 +1294,15 @@ done:
         free(v[r]);
     free(v);
     return rc;
+}
+
+/* The INT8 block and threshold compressors (no k). */
+int oracle_allreduce_compressed(void **grads, float **res, int N, uint64_t K, int dtype, int op, int comp,
+                                int block, float threshold)
+{
+    if (comp == OR_COMP_TOPK)
+        return OR_EINVAL;
+    return oracle_allreduce_compressed_k(grads, res, N, K, dtype, op, comp, block, threshold, 0);
 }
 
 /* Plain fp64 reference of the reduction (the definition y = sum_r x_r with no

@@ -13,6 +13,11 @@ from ring_allreduce_rank_gb300 import workloads as W
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
 
+def _bits(a):
+    a = np.asarray(a)
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
 def _table():
     with open(os.path.join(GOLD, "error_feedback_table4.json")) as f:
         return json.load(f)
@@ -157,3 +162,117 @@ def test_int8_nan_in_a_block_poisons_only_that_block(oracle_mod):
     clean, _ = oracle_mod.allreduce_compressed([g[128:].copy()], [np.zeros(128, np.float32)], "sum", "int8_block",
                                                128, 0.0)
     np.testing.assert_array_equal(out[0][128:], clean[0])
+
+
+# ---------------------------------------------------------------- Top-k sparsification
+
+def test_topk_ratio_closed_form():
+    """Top-k with fp32 values and int32 indices sends 8 bytes per kept
+    element: ratio 4d / (8 K_top) = d / (2 K_top), printed as 500x (not 1000x)
+    for K_top = 0.001 d."""
+    t = _table()
+    d = 1_000_000
+    k = int(round(t["topk_kept_fraction"] * d))
+    assert d // k == t["topk_kept_fraction_naive_ratio"]
+    assert 4 * d / (8 * k) == t["topk_ratio"]
+
+
+def _topk_numpy(u, k):
+    """TopK(u) = u * 1[|u| >= |u|_(k)] with numpy's sort (every value tied
+    with the k-th largest magnitude is kept); k = 0 keeps nothing."""
+    a = np.abs(u.astype(np.float64))
+    if k == 0:
+        return np.zeros_like(u)
+    kth = np.sort(a)[::-1][min(k, a.size) - 1]
+    return np.where(a >= kth, u, np.float32(0)).astype(np.float32)
+
+
+def _int_grads(dtype, N, K, seed, lo=-20, hi=20):
+    g = W.integers_fp32(N, K, seed=seed, lo=lo, hi=hi)
+    grads = [W.to_bf16_bits(r) for r in g] if dtype == "bf16" else list(g)
+    return g, grads
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "avg"])
+@pytest.mark.parametrize("N,K,k", [(1, 50, 7), (3, 1000, 10), (4, 4096, 41), (5, 333, 333), (2, 100, 1),
+                                   (3, 64, 500)])
+def test_topk_matches_the_definition_on_integers(oracle_mod, dtype, op, N, K, k):
+    """Integer gradients and residuals, with many equal magnitudes so that the
+    k-th largest is tied: every sum is exact, so the result must be the
+    brute-force sum of numpy's TopK of each rank's u = g + e (AVG: numpy's
+    float32 quotient by N), rounded to the gradient type, and each residual
+    must be u minus what that rank sent.  At least k values are sent per rank."""
+    g, grads = _int_grads(dtype, N, K, seed=N * 1000 + K + k)
+    e0 = list(W.integers_fp32(N, K, seed=7 + k, lo=-3, hi=3))
+    out, e1 = oracle_mod.allreduce_compressed(grads, e0, op, "topk", k=k)
+    u = [g[r] + e0[r] for r in range(N)]
+    v = [_topk_numpy(u[r], k) for r in range(N)]
+    S = np.sum(np.stack(v).astype(np.float64), axis=0).astype(np.float32)
+    want = S / np.float32(N) if op == "avg" else S
+    want = W.to_bf16_bits(want) if dtype == "bf16" else want
+    for r in range(N):
+        np.testing.assert_array_equal(_bits(out[r]), _bits(want))
+        np.testing.assert_array_equal(_bits(e1[r]), _bits((u[r] - v[r]).astype(np.float32)))
+        assert np.count_nonzero(np.abs(u[r]) >= np.sort(np.abs(u[r]))[::-1][min(k, K) - 1]) >= min(k, K)
+
+
+def test_topk_keeps_exactly_k_distinct_magnitudes(oracle_mod):
+    """Distinct magnitudes: exactly k values leave each rank, the k largest."""
+    N, K, k = 3, 5000, 37
+    x = W.normal_fp32(N, K, seed_base=21)
+    out, e1 = oracle_mod.allreduce_compressed(list(x), [np.zeros(K, np.float32)] * N, "sum", "topk", k=k)
+    for r in range(N):
+        sent = x[r] - e1[r]
+        assert np.count_nonzero(sent) == k
+        top = np.argsort(-np.abs(x[r]), kind="stable")[:k]
+        np.testing.assert_array_equal(np.sort(np.nonzero(sent)[0]), np.sort(top))
+
+
+def test_topk_k_zero_sends_nothing_and_k_all_sends_everything(oracle_mod):
+    N, K = 4, 999
+    g, grads = _int_grads("fp32", N, K, seed=3)
+    e0 = [np.zeros(K, np.float32) for _ in range(N)]
+    out, e1 = oracle_mod.allreduce_compressed(grads, e0, "sum", "topk", k=0)
+    for r in range(N):
+        np.testing.assert_array_equal(_bits(out[r]), np.zeros(K, np.uint32))  # +0 everywhere
+        np.testing.assert_array_equal(_bits(e1[r]), _bits(g[r]))
+    for k in (K, K + 5):
+        out, e1 = oracle_mod.allreduce_compressed(grads, e0, "sum", "topk", k=k)
+        S = np.sum(g.astype(np.float64), axis=0).astype(np.float32)
+        for r in range(N):
+            np.testing.assert_array_equal(out[r], S)
+            assert not np.any(e1[r])
+
+
+def test_topk_nan_counts_as_the_largest_magnitude(oracle_mod):
+    """A NaN in u is ordered above every number, so with k = 1 it is the one
+    value its rank sends: the result is NaN there on every rank, that rank
+    keeps every other value as residual, and the residual at the NaN is NaN."""
+    N, K = 3, 300
+    x = W.normal_fp32(N, K, seed_base=5)
+    x[1][17] = np.float32("nan")
+    out, e1 = oracle_mod.allreduce_compressed(list(x), [np.zeros(K, np.float32)] * N, "sum", "topk", k=1)
+    for r in range(N):
+        assert np.isnan(out[r][17])
+        assert out[r].view(np.uint32)[17] == 0x7FFFFFFF
+    assert np.isnan(e1[1][17])
+    rest = np.arange(K) != 17
+    np.testing.assert_array_equal(e1[1][rest], x[1][rest])
+
+
+def test_topk_error_feedback_telescopes_exactly(oracle_mod):
+    """sum_t v_t = sum_t g_t + e_1 - e_{T+1} (Collective Communication, the
+    telescoping sum under Definition 1.4).  Gradients on a 1/8 grid keep every
+    value exact, so the identity holds with equality."""
+    K, T, k = 512, 40, 32
+    e = [np.zeros(K, np.float32)]
+    sv = np.zeros(K)
+    sg = np.zeros(K)
+    g0 = np.random.Generator(np.random.PCG64(11))
+    for t in range(T):
+        g = (g0.integers(-16, 17, size=K) / 8.0).astype(np.float32)
+        out, e = oracle_mod.allreduce_compressed([g], e, "sum", "topk", k=k)
+        sv += out[0]
+        sg += g
+    np.testing.assert_array_equal(sv, sg - e[0].astype(np.float64))

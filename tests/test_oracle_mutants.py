@@ -79,6 +79,12 @@ MUTANTS = [
     ("residual_sign_flipped", "e[i] = fcanon(u[i] - v);\n            u[i] = v;\n        }\n    }",
      "e[i] = fcanon(v - u[i]);\n            u[i] = v;\n        }\n    }"),
     ("threshold_strict", "float v = u[i] >= threshold ? 1.0f : 0.0f;", "float v = u[i] > threshold ? 1.0f : 0.0f;"),
+    ("topk_strict_threshold", "float v = (f32_to_bits(u[i]) & 0x7fffffffu) >= tau ? u[i] : 0.0f;",
+     "float v = (f32_to_bits(u[i]) & 0x7fffffffu) > tau ? u[i] : 0.0f;"),
+    ("topk_keeps_the_smallest", "return x < y ? 1 : (x > y ? -1 : 0);", "return x < y ? -1 : (x > y ? 1 : 0);"),
+    ("topk_kth_off_by_one", "tau = mag[(k < K ? k : K) - 1];", "tau = mag[(k < K ? k : K - 1)];"),
+    ("topk_residual_zeroed", "e[i] = fcanon(u[i] - v);\n        u[i] = v;\n    }\n    return OR_OK;",
+     "e[i] = 0.0f;\n        u[i] = v;\n    }\n    return OR_OK;"),
     ("error_feedback_dropped",
      "u[i] = fcanon(bits_to_f32(widen_bits(load(grads[r], dtype, i), dtype)) + res[r][i]);",
      "u[i] = fcanon(bits_to_f32(widen_bits(load(grads[r], dtype, i), dtype)));"),
