@@ -217,6 +217,8 @@ ROWS = {
     "allreduce-hier": "AllReduce AVG in two-level hierarchical order (2 groups of 4), N=8 bf16 64Mi/rank, in place",
     "allreduce-premul": "AllReduce AVG by pre-multiplication (each contribution times 1/N, then SUM), N=8 bf16 "
                         "64Mi/rank, in place, fused ring order",
+    "allreduce-topk": "Top-k sparsified AllReduce AVG with error feedback, k = 1% of each rank's 64Mi bf16 "
+                      "elements (671,089), N=8; threshold by on-device radix select",
     "allreduce-int8": "compressed AllReduce AVG with error feedback, blockwise INT8 (b=128), N=8 bf16 64Mi/rank",
     "overlap": "bucket AllReduce (4 Llama layers, N=8 bf16, 25 MiB buckets) overlapped with a synthetic backward "
                "pass of per-rank gradient GEMMs (4096 tokens); bucket kernels on a second stream as gradients finish",
@@ -460,6 +462,26 @@ def run_row(args, name, local):
         print(json.dumps(line("Compressed AllReduce (INT8 blocks + error feedback) HBM GB/s, N=8 bf16 128 MB/rank, "
                               "1 GB300", alg, per, launches, "compressed_allreduce_kernel<bf16, 4, 8>", "bf16",
                               {"nranks": N, "count": K, "block": 128}, {"clocks": clk}, total_ms=tot)))
+        return
+
+    if name == "allreduce-topk":
+        N, K = 8, args.count
+        kk = K // 100
+        grads = [randn_bf16(K) for _ in range(N)]
+        res = [torch.zeros(K, dtype=torch.float32, device=dev) for _ in range(N)]
+        work = torch.empty(ccl.ccl_plan_topk_work_bytes(N), dtype=torch.uint8, device=dev)
+        step = lambda: ccl.ccl_allreduce_topk(grads, res, kk, op="avg", work=work, stream=stream)
+        clocks.start()
+        tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
+        clk = clocks.stop()
+        # the least any exact Top-k must move: g and e read once to find the
+        # threshold, then gradients and residuals read and written once
+        alg = N * K * (2 + 4) + N * K * (2 + 4 + 4 + 2)
+        print(json.dumps(line("Top-k AllReduce (1%% kept + error feedback) HBM GB/s of the %d-byte minimum, N=8 bf16 "
+                              "128 MB/rank, 1 GB300" % alg, alg, per, launches,
+                              "whole step: topk_init + 3 x (topk_hist_kernel + topk_scan_kernel) + "
+                              "compressed_pipe_kernel<bf16, 4>", "bf16",
+                              {"nranks": N, "count": K, "k": kk}, {"clocks": clk}, total_ms=tot)))
         return
 
     if name in ("allreduce-step", "broadcast"):

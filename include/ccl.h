@@ -101,7 +101,7 @@ typedef enum {
     CCL_ALGO_TREE = 2,
     CCL_ALGO_HIERARCHICAL = 3
 } ccl_algo_t;
-typedef enum { CCL_COMP_INT8_BLOCK = 0, CCL_COMP_THRESHOLD = 1 } ccl_compressor_t;
+typedef enum { CCL_COMP_INT8_BLOCK = 0, CCL_COMP_THRESHOLD = 1, CCL_COMP_TOPK = 2 } ccl_compressor_t;
 typedef enum {
     CCL_OK = 0,
     CCL_ERR_INVALID_ARG = 1,
@@ -271,10 +271,45 @@ ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int 
  * The transmitted v are AllReduced in ring order in fp32 (op CCL_SUM, or
  * CCL_AVG dividing once by N; CCL_AVG_PREMUL returns CCL_ERR_UNSUPPORTED) and
  * rounded once to dtype, written to every grads[r].  Up to 16 ranks; grads
- * and residuals must not overlap.  One launch. */
+ * and residuals must not overlap.  CCL_COMP_TOPK needs k and a work buffer:
+ * it is ccl_allreduce_topk's (CCL_ERR_INVALID_ARG here).  One launch, two
+ * with a partial last block. */
 ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residuals, int nranks, size_t count,
                                       ccl_dtype_t dtype, ccl_op_t op, ccl_compressor_t comp, int block,
                                       float threshold, cudaStream_t stream);
+
+/* Top-k sparsified AllReduce with error feedback (Collective Communication,
+ * "Top-k sparsification", and "Error feedback and residual accumulation",
+ * Definition 1.4).  grads[r]: `count` elements of dtype, in place;
+ * residuals[r]: `count` fp32 per rank, zero before the first step, carried by
+ * the caller.  Each rank forms u = g + e (fp32) and sends v = u where |u| is
+ * at least its k-th largest magnitude |u|_(k), else 0 -- every value tied
+ * with the k-th is sent, so a rank may send more than k -- and keeps
+ * e' = u - v.  Magnitudes are ordered as the bit patterns of |u|, so a NaN
+ * counts as the largest and is always sent.  k = 0 sends nothing; k >= count
+ * sends everything.  The sent values are AllReduced in ring order in fp32
+ * (CCL_SUM, or CCL_AVG dividing once by N; CCL_AVG_PREMUL returns
+ * CCL_ERR_UNSUPPORTED) and rounded once to dtype, written to every grads[r].
+ * The threshold is found on the device by a radix select (three histogram
+ * passes over g and e, no host round trip), then one pass sends, keeps the
+ * residuals and reduces.  work: device memory of ccl_plan_topk_work_bytes
+ * bytes, 16-byte aligned, owned by the caller, not shared with a concurrent
+ * call; its contents need no initialisation.  Up to 16 ranks; grads,
+ * residuals and work must not overlap (CCL_ERR_OVERLAP).  Launches: one to
+ * reset the work buffer, three histogram-and-scan pairs when 0 < k < count,
+ * and the compressed pass (one launch, two with a partial last block of 128). */
+ccl_status_t ccl_allreduce_topk(void *const *grads, float *const *residuals, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, size_t k, void *work, size_t work_bytes,
+                                cudaStream_t stream);
+
+/* Bytes of the work buffer ccl_allreduce_topk needs for nranks ranks. */
+ccl_status_t ccl_plan_topk_work_bytes(int nranks, size_t *bytes);
+
+/* Bytes one rank would put on a link for Top-k with fp32 values and int32
+ * indices: 8 * min(k, count), a ratio of 4 count / bytes = count / (2k) over
+ * dense fp32 (Collective Communication, "Top-k sparsification": 500x, not
+ * 1000x, for k = 0.001 count).  Host only. */
+ccl_status_t ccl_plan_topk_bytes(size_t count, size_t k, size_t *bytes);
 
 /* Step-by-step ReduceScatter that allocates nothing.  The pages have no
  * counterpart: this exists for callers that cannot let a library call
@@ -410,7 +445,8 @@ ccl_status_t ccl_plan_alltoallv(int nranks, const size_t *counts, size_t *sdispl
 /* Bytes one rank would put on a link for `count` elements under a
  * compressor: INT8 block: count + 4 * ceil(count / block) (codes plus fp32
  * scales, 4b/(b+4) times fewer than fp32: 3.88 at b = 128); THRESHOLD:
- * ceil(count / 8). */
+ * ceil(count / 8).  TOPK depends on k: ccl_plan_topk_bytes (CCL_ERR_INVALID_ARG
+ * here). */
 ccl_status_t ccl_plan_compressed_bytes(size_t count, ccl_compressor_t comp, int block, size_t *bytes);
 
 /* Slices of ccl_allreduce_host for these arguments: writes up to max_slices

@@ -22,7 +22,7 @@ FUSED, STEP = 0, 1
 OPS = {"sum": SUM, "avg": AVG, "max": MAX, "prod": PROD, "min": MIN, "avg_premul": AVG_PREMUL}
 MODES = {"fused": FUSED, "step": STEP}
 ALGOS = {"ring": 0, "halving_doubling": 1, "tree": 2, "hierarchical": 3}
-COMPRESSORS = {"int8_block": 0, "threshold": 1}
+COMPRESSORS = {"int8_block": 0, "threshold": 1, "topk": 2}
 STATUS = {0: "CCL_OK", 1: "CCL_ERR_INVALID_ARG", 2: "CCL_ERR_UNSUPPORTED", 3: "CCL_ERR_OVERLAP",
           4: "CCL_ERR_CUDA", 5: "CCL_ERR_NO_MEMORY", 6: "CCL_ERR_TIMEOUT", 7: "CCL_ERR_CHECK_FAILED"}
 MAX_RANKS = 1024
@@ -62,6 +62,9 @@ def lib() -> ctypes.CDLL:
                 "ccl_allreduce_algo": [pp, pp, i32, sz, i32, i32, i32, i32, vp],
                 "ccl_allreduce_compressed": [pp, pp, i32, sz, i32, i32, i32, i32, ctypes.c_float, vp],
                 "ccl_plan_compressed_bytes": [sz, i32, i32, psz],
+                "ccl_allreduce_topk": [pp, pp, i32, sz, i32, i32, sz, vp, sz, vp],
+                "ccl_plan_topk_work_bytes": [i32, psz],
+                "ccl_plan_topk_bytes": [sz, sz, psz],
                 "ccl_gather": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_scatter": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_alltoall": [pp, pp, i32, sz, i32, i32, vp],
@@ -202,6 +205,33 @@ def ccl_allreduce_compressed(grads: Sequence[torch.Tensor], residuals: Sequence[
     _check(lib().ccl_allreduce_compressed(_ptrs(grads), _ptrs(residuals), len(grads), grads[0].numel(),
                                           _dtype(grads[0]), _op(op), c, int(block), ctypes.c_float(threshold),
                                           _stream(stream)), "ccl_allreduce_compressed")
+
+
+def ccl_allreduce_topk(grads: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor], k: int, op="sum",
+                       work: Optional[torch.Tensor] = None, stream=None) -> None:
+    """One Top-k sparsified AllReduce step with error feedback, in place on
+    grads and residuals (fp32, one per rank).  work: a device buffer of at
+    least ccl_plan_topk_work_bytes(N) bytes (allocated here when omitted)."""
+    for e in residuals:
+        if e.dtype != torch.float32:
+            raise TypeError("residuals are float32")
+    if work is None:
+        work = torch.empty(ccl_plan_topk_work_bytes(len(grads)), dtype=torch.uint8, device=grads[0].device)
+    _check(lib().ccl_allreduce_topk(_ptrs(grads), _ptrs(residuals), len(grads), grads[0].numel(), _dtype(grads[0]),
+                                    _op(op), int(k), ctypes.c_void_p(work.data_ptr()), work.numel() * work.element_size(),
+                                    _stream(stream)), "ccl_allreduce_topk")
+
+
+def ccl_plan_topk_work_bytes(nranks: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().ccl_plan_topk_work_bytes(int(nranks), ctypes.byref(out)), "ccl_plan_topk_work_bytes")
+    return out.value
+
+
+def ccl_plan_topk_bytes(count: int, k: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().ccl_plan_topk_bytes(int(count), int(k), ctypes.byref(out)), "ccl_plan_topk_bytes")
+    return out.value
 
 
 def ccl_plan_compressed_bytes(count: int, comp="int8_block", block: int = 128) -> int:

@@ -853,7 +853,62 @@ static ccl_status_t ccl_allreduce_compressed_impl(void *const *grads, float *con
         return st;
     CCL_DBG(w, {}, {}, stream);
     return from_cuda(launch_compressed_allreduce((int)dtype, op == CCL_AVG, (int)comp, block, threshold, grads,
-                                                 residuals, nranks, count, stream));
+                                                 residuals, nranks, count, nullptr, stream));
+}
+
+ccl_status_t ccl_plan_topk_bytes(size_t count, size_t k, size_t *bytes)
+{
+    if (!bytes)
+        return CCL_ERR_INVALID_ARG;
+    const size_t kept = k < count ? k : count;
+    if (mul_overflows(kept, 8))
+        return CCL_ERR_INVALID_ARG;
+    *bytes = kept * 8; // an fp32 value and an int32 index per kept element
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_topk_work_bytes(int nranks, size_t *bytes)
+{
+    if (nranks < 1 || nranks > kTopkMaxRanks || !bytes)
+        return CCL_ERR_INVALID_ARG;
+    *bytes = topk_work_bytes(nranks);
+    return CCL_OK;
+}
+
+static ccl_status_t ccl_allreduce_topk_impl(void *const *grads, float *const *residuals, int nranks, size_t count,
+                                            ccl_dtype_t dtype, ccl_op_t op, size_t k, void *work, size_t work_bytes,
+                                            cudaStream_t stream)
+{
+    if (op == CCL_AVG_PREMUL)
+        return CCL_ERR_UNSUPPORTED; // the compressed AllReduce divides once, at the end
+    if (nranks < 1 || nranks > kTopkMaxRanks || !valid_dtype(dtype) || (op != CCL_SUM && op != CCL_AVG) || !grads ||
+        !residuals)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, 4))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const size_t wb = topk_work_bytes(nranks);
+    if (!work || work_bytes < wb || (uintptr_t)work % 16 != 0)
+        return CCL_ERR_INVALID_ARG;
+    std::vector<Range> w;
+    for (int i = 0; i < nranks; ++i) {
+        if (!grads[i] || !residuals[i])
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(grads[i], count * es, i));
+        w.push_back(range_of(residuals[i], count * 4, i));
+    }
+    w.push_back(range_of(work, wb, nranks));
+    ccl_status_t st = check_overlaps(w, {}, [](const Range &, const Range &) { return false; });
+    if (st != CCL_OK)
+        return st;
+    CCL_DBG(w, {}, {}, stream);
+    const uint32_t *tau = nullptr;
+    if (cudaError_t e = launch_topk_select((int)dtype, grads, residuals, nranks, count, k, work, &tau, stream))
+        return from_cuda(e);
+    return from_cuda(launch_compressed_allreduce((int)dtype, op == CCL_AVG, COMP_TOPK, 0, 0.0f, grads, residuals,
+                                                 nranks, count, tau, stream));
 }
 
 // ------------------------------------------------------------------ host-buffer AllReduce
@@ -1027,6 +1082,16 @@ ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residual
     TraceScope tr("allreduce_compressed", nranks, count, (int)dtype, (int)op, (int)comp);
     return tr.done(then_check(ccl_allreduce_compressed_impl(grads, residuals, nranks, count, dtype, op, comp, block,
                                                             threshold, stream),
+                              grads, nranks, count, dtype, stream));
+}
+
+ccl_status_t ccl_allreduce_topk(void *const *grads, float *const *residuals, int nranks, size_t count,
+                                ccl_dtype_t dtype, ccl_op_t op, size_t k, void *work, size_t work_bytes,
+                                cudaStream_t stream)
+{
+    TraceScope tr("allreduce_topk", nranks, count, (int)dtype, (int)op, (int)CCL_COMP_TOPK);
+    return tr.done(then_check(ccl_allreduce_topk_impl(grads, residuals, nranks, count, dtype, op, k, work,
+                                                      work_bytes, stream),
                               grads, nranks, count, dtype, stream));
 }
 

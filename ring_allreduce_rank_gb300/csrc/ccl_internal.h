@@ -90,13 +90,21 @@ cudaError_t launch_order_allreduce(int dt, int op, int algo, int group, const vo
                                    int nranks, uint64_t count, cudaStream_t stream);
 
 // ------------------------------------------------------------------ compressed AllReduce
-enum Compressor { COMP_INT8_BLOCK = 0, COMP_THRESHOLD = 1 };
+enum Compressor { COMP_INT8_BLOCK = 0, COMP_THRESHOLD = 1, COMP_TOPK = 2 };
 
 // Error-feedback compression of every rank's gradient, ring-order fp32
 // AllReduce of the transmitted values, one round to the gradients' type.
+// COMP_TOPK reads each rank's threshold key from tau[rank] (device memory).
 cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, float threshold,
                                         void *const *grads, float *const *res, int nranks, uint64_t count,
-                                        cudaStream_t stream);
+                                        const uint32_t *tau, cudaStream_t stream);
+
+// Top-k threshold per rank: the k-th largest key |u| (bits, sign cleared) of
+// u = g + e, written to *tau_out[rank] in `work` (topk_work_bytes(nranks)).
+constexpr int kTopkMaxRanks = 16;
+size_t topk_work_bytes(int nranks);
+cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, int nranks, uint64_t count,
+                               uint64_t k, void *work, const uint32_t **tau_out, cudaStream_t stream);
 
 // ------------------------------------------------------------------ host-buffer AllReduce
 constexpr int kHostStages = 3;            // device stages in flight: copy-in, reduce, copy-out

@@ -8,7 +8,10 @@
 //     q = round(u / s) (ties to even), v = q * s -- 4b/(b+4) fewer bytes than
 //     fp32 on a real link;
 //   THRESHOLD (the greedy 1-bit compressor of the pages' Tables 3 and 4):
-//     v = 1 when u >= threshold, else 0.
+//     v = 1 when u >= threshold, else 0;
+//   TOPK ("Top-k sparsification"): v = u when the magnitude key of u (its
+//     bits with the sign cleared) reaches the rank's k-th largest key tau,
+//     found beforehand by the radix select in topk.cu, else 0.
 // The transmitted values are then AllReduced in ring order in fp32 (chunk c
 // folded from rank c), AVG divides once by N, and the result is rounded once
 // to the gradients' type and written to every rank.
@@ -37,7 +40,7 @@ struct CompParams {
     Partition part;
     uint64_t K;
     int nranks;
-    int comp;  // COMP_INT8_BLOCK or COMP_THRESHOLD
+    int comp;  // COMP_INT8_BLOCK, COMP_THRESHOLD or COMP_TOPK
     float threshold;
     float n_f;   // AVG: N (0 for SUM)
     float inv_n; // 1/N, exact when N is a power of two
@@ -46,6 +49,7 @@ struct CompParams {
     uint64_t first_block; // the direct kernel starts at this compression block
     uint64_t nfull;       // the pipelined kernel covers blocks [0, nfull)
     uint64_t coff[kCompMaxRanks + 1]; // chunk c starts at coff[c]; entries from N on hold K
+    const uint32_t *tau;              // COMP_TOPK: each rank's threshold key (device memory)
 };
 
 // max that returns NaN when either side is NaN (PTX max.NaN), so a block's
@@ -181,6 +185,17 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
                 v[r][j] = u >= p.threshold ? 1.0f : 0.0f;
                 ee[r][j] = __fsub_rn(u, v[r][j]);
             }
+    } else if (p.comp == COMP_TOPK) {
+#pragma unroll
+        for (int r = 0; r < NMAX; ++r) {
+            const uint32_t tau = r < N ? gload<uint32_t>(p.tau + r) : 0xffffffffu;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) {
+                const float u = v[r][j];
+                v[r][j] = (__float_as_uint(u) & 0x7fffffffu) >= tau ? u : 0.0f;
+                ee[r][j] = __fsub_rn(u, v[r][j]);
+            }
+        }
     } else {
         // per-rank block maxima of |u|; a NaN anywhere in the block makes the
         // maximum NaN, and the scale with it
@@ -590,12 +605,12 @@ static cudaError_t launch_comp_dt(CompParams p, cudaStream_t stream)
 
 cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, float threshold,
                                         void *const *grads, float *const *res, int nranks, uint64_t count,
-                                        cudaStream_t stream)
+                                        const uint32_t *tau, cudaStream_t stream)
 {
     if (nranks > kCompMaxRanks)
         return cudaErrorInvalidValue;
     CompParams p;
-    const int epl = comp == COMP_THRESHOLD ? 4 : block / 32;
+    const int epl = (comp == COMP_THRESHOLD || comp == COMP_TOPK) ? 4 : block / 32;
     const int es = dt == DT_BF16 ? 2 : 4;
     bool vec = true;
     for (int r = 0; r < kCompMaxRanks; ++r) {
@@ -618,6 +633,7 @@ cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, f
     p.vec_ok = vec ? 1 : 0;
     p.first_block = 0;
     p.nfull = 0;
+    p.tau = tau;
     if (dt == DT_FP32)
         return epl == 4 ? launch_comp_dt<DT_FP32, 4>(p, stream) : launch_comp_dt<DT_FP32, 2>(p, stream);
     return epl == 4 ? launch_comp_dt<DT_BF16, 4>(p, stream) : launch_comp_dt<DT_BF16, 2>(p, stream);

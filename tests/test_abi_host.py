@@ -88,6 +88,23 @@ def test_planner_compressed_bytes(L):
     assert ccl.ccl_plan_compressed_bytes(1001, "threshold", 0) == 126
 
 
+def test_planner_topk_bytes(L):
+    """Top-k with fp32 values and int32 indices: 8 bytes per kept element,
+    ratio d / (2k) over dense fp32 -- 500x for k = 0.001 d (Collective
+    Communication, "Top-k sparsification")."""
+    d = 1_000_000
+    assert ccl.ccl_plan_topk_bytes(d, d // 1000) == 8000
+    assert 4 * d / ccl.ccl_plan_topk_bytes(d, d // 1000) == 500
+    assert ccl.ccl_plan_topk_bytes(10, 50) == 80  # k beyond count keeps count
+    assert ccl.ccl_plan_topk_bytes(10, 0) == 0
+    assert ccl.ccl_plan_topk_work_bytes(8) == 8 * 2048 * 8 + 8 * 16 + 8 * 4
+    for n in (0, 17):
+        with pytest.raises(C.CclError):
+            ccl.ccl_plan_topk_work_bytes(n)
+    with pytest.raises(C.CclError):
+        ccl.ccl_plan_compressed_bytes(1000, "topk", 10)
+
+
 def test_arena_layout(L):
     assert ccl.ccl_arena_layout(8, 134217728) == (134217728, 8 * 134217728)
     assert ccl.ccl_arena_layout(3, 1000, 256) == (1024, 3072)

@@ -7,6 +7,9 @@ rank (the headline's shape).
   compressed  INT8 blocks of 128 + error feedback, AVG (the whole result and
               every residual, against the full oracle run)
   premul      AllReduce with the pre-multiplied AVG (sampled closed-form values)
+  topk        Top-k AllReduce AVG, k = 1%, with error feedback (the definition
+              checked as properties of the whole result, sums at sampled
+              positions against the oracle's closed form)
   reduce      Reduce SUM to rank 0 (sampled closed-form values)
   gather      Gather to rank 0, Scatter back, Broadcast from rank 0 (copies,
               compared in full)
@@ -96,6 +99,38 @@ def test_premul_full_size(x):
     it = torch.from_numpy(idx).to(DEV)
     for r in range(N):
         assert_bits_equal(bits(a.ranks[r].index_select(0, it)), want, "premul rank %d" % r)
+
+
+def test_topk_full_size(x):
+    """Per rank, the sent set S must be exactly the definition's: every value
+    of S has a magnitude at least that of every value outside it, S holds at
+    least k values, and without the values tied at its smallest magnitude it
+    would hold fewer than k.  The result at sampled positions is then the
+    oracle's fp32 ring-order AVG of the sent values, rounded to bf16."""
+    k = K // 100
+    g = [to_dev(r) for r in x]
+    u = [gr.float() for gr in g]  # u = g + e with e = 0
+    e = [torch.zeros(K, dtype=torch.float32, device=DEV) for _ in range(N)]
+    ccl.ccl_allreduce_topk(g, e, k, op="avg")
+    torch.cuda.synchronize()
+    sent = []
+    for r in range(N):
+        m = (e[r] == 0) & (u[r] != 0)  # sent values leave no residual (finite inputs)
+        mag = u[r].abs()
+        lo = mag[m].min()
+        assert int(m.sum()) >= k
+        assert bool((mag[~m] <= lo).all())
+        assert int((m & (mag > lo)).sum()) < k
+        assert int(((mag == lo) & ~m).sum()) == 0  # every tie at the threshold is sent
+        assert torch.equal(e[r][~m], u[r][~m])
+        sent.append(torch.where(m, u[r], torch.zeros_like(u[r])))
+    idx = _sample([N], seed=8)
+    it = torch.from_numpy(idx).to(DEV)
+    vals = [s.index_select(0, it).cpu().numpy() for s in sent]
+    want = oracle.ring_allreduce_gathered(vals, K, idx.astype(np.uint64), "avg")
+    want = W.to_bf16_bits(want)
+    for r in range(N):
+        assert_bits_equal(bits(g[r].index_select(0, it)), want, "topk rank %d" % r)
 
 
 def test_reduce_full_size(x):

@@ -1,0 +1,168 @@
+"""Top-k sparsified AllReduce with error feedback on the device
+(ccl_allreduce_topk), bit for bit against the oracle: gradients and residuals
+after one or several steps, ties at the k-th magnitude, special values (a NaN
+counts as the largest magnitude), unaligned buffers (the element paths), the
+degenerate k, CUDA-graph capture, and the argument checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ring_allreduce_rank_gb300 as ccl
+from ring_allreduce_rank_gb300 import ccl as C
+from ring_allreduce_rank_gb300 import workloads as W
+
+from gpu_util import DEV, assert_bits_equal, bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    ccl.lib()
+    oracle.build()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def _grads(dtype, N, K, seed):
+    return list(W.mixed_bf16(N, K, seed_base=seed)) if dtype == "bf16" else list(W.mixed_fp32(N, K, seed_base=seed))
+
+
+def _res(N, K, seed):
+    return [W.normal_fp32(1, K, std=1e-3, seed_base=seed + r)[0] for r in range(N)]
+
+
+def _run(g_host, e_host, k, op, pad=0):
+    g = [to_dev(x, pad_elems=pad) for x in g_host]
+    e = [to_dev(x, pad_elems=pad) for x in e_host]
+    ccl.ccl_allreduce_topk(g, e, k, op=op)
+    torch.cuda.synchronize()
+    return [bits(x) for x in g], [bits(x) for x in e]
+
+
+def _check(got_g, got_e, want_g, want_e, what):
+    for r in range(len(got_g)):
+        assert_bits_equal(got_g[r], want_g[r], "%s grads rank %d" % (what, r))
+        assert_bits_equal(got_e[r], np.asarray(want_e[r]).view(np.uint32), "%s residual rank %d" % (what, r))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "avg"])
+@pytest.mark.parametrize("N,K,k", [(1, 1000, 7), (3, 10_007, 100), (8, 65_536 + 13, 655), (16, 40_001, 1),
+                                   (5, 4, 2), (4, 5000, 0), (4, 5000, 5000), (4, 5000, 6000), (2, 300_001, 299_999),
+                                   (8, 1 << 20, 10_486)])
+def test_matches_oracle(dtype, op, N, K, k):
+    g = _grads(dtype, N, K, seed=N * 100 + K % 89)
+    e = _res(N, K, seed=K % 1000)
+    want_g, want_e = oracle.allreduce_compressed(g, e, op, "topk", k=k)
+    got_g, got_e = _run(g, e, k, op)
+    _check(got_g, got_e, want_g, want_e, "topk %s %s N=%d K=%d k=%d" % (dtype, op, N, K, k))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("k", [1, 50, 333, 1000, 3999])
+def test_ties_at_the_kth_magnitude(dtype, k):
+    """Integers in [-6, 6] with zero residuals: thousands of equal magnitudes,
+    so the k-th falls inside a tie group and every tied value is sent."""
+    N, K = 4, 4000
+    x = W.integers_fp32(N, K, seed=k, lo=-6, hi=6)
+    g = [W.to_bf16_bits(r) for r in x] if dtype == "bf16" else list(x)
+    e = [np.zeros(K, np.float32) for _ in range(N)]
+    want_g, want_e = oracle.allreduce_compressed(g, e, "sum", "topk", k=k)
+    got_g, got_e = _run(g, e, k, "sum")
+    _check(got_g, got_e, want_g, want_e, "ties k=%d" % k)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_three_steps_carry_the_residual(dtype):
+    N, K, k = 6, 50_003, 500
+    e_host = [np.zeros(K, np.float32) for _ in range(N)]
+    e_dev = [to_dev(x) for x in e_host]
+    for step in range(3):
+        g = _grads(dtype, N, K, seed=1000 * step + 1)
+        gd = [to_dev(x) for x in g]
+        ccl.ccl_allreduce_topk(gd, e_dev, k, op="avg")
+        want_g, e_host = oracle.allreduce_compressed(g, e_host, "avg", "topk", k=k)
+        torch.cuda.synchronize()
+        _check([bits(x) for x in gd], [bits(x) for x in e_dev], want_g, e_host, "step %d" % step)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("pad", [1, 3])
+def test_unaligned_buffers(dtype, pad):
+    N, K, k = 3, 20_011, 77
+    g = _grads(dtype, N, K, seed=pad)
+    e = _res(N, K, seed=pad + 50)
+    want_g, want_e = oracle.allreduce_compressed(g, e, "sum", "topk", k=k)
+    got_g, got_e = _run(g, e, k, "sum", pad=pad)
+    _check(got_g, got_e, want_g, want_e, "unaligned pad %d" % pad)
+
+
+def test_nan_is_sent_first():
+    N, K = 3, 4096
+    g = list(W.normal_fp32(N, K, seed_base=8))
+    g[2][100] = np.float32("nan")
+    e = [np.zeros(K, np.float32) for _ in range(N)]
+    want_g, want_e = oracle.allreduce_compressed(g, e, "sum", "topk", k=1)
+    got_g, got_e = _run(g, e, 1, "sum")
+    _check(got_g, got_e, want_g, want_e, "nan")
+    assert got_g[0][100] == 0x7FFFFFFF
+
+
+def test_graph_capture_and_replay():
+    """The whole call -- work reset, selection passes, compressed pass -- is
+    device-only work: captured once, replayed twice, it equals two oracle
+    steps (the residual carries from the first replay into the second)."""
+    N, K, k = 4, 100_000, 1000
+    x = _grads("bf16", N, K, seed=77)
+    g = [to_dev(r) for r in x]
+    e = [torch.zeros(K, dtype=torch.float32, device=DEV) for _ in range(N)]
+    work = torch.empty(ccl.ccl_plan_topk_work_bytes(N), dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        gr.capture_begin()
+        ccl.ccl_allreduce_topk(g, e, k, op="sum", work=work, stream=s)
+        gr.capture_end()
+    torch.cuda.synchronize()
+    want_g, want_e = list(x), [np.zeros(K, np.float32) for _ in range(N)]
+    for step in range(2):
+        for r in range(N):
+            g[r].copy_(to_dev(x[r]))
+        gr.replay()
+        torch.cuda.synchronize()
+        want_g, want_e = oracle.allreduce_compressed(list(x), want_e, "sum", "topk", k=k)
+        _check([bits(t) for t in g], [bits(t) for t in e], want_g, want_e, "graph replay %d" % step)
+
+
+def test_argument_errors():
+    N, K = 4, 1000
+    g = [torch.zeros(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    e = [torch.zeros(K, dtype=torch.float32, device=DEV) for _ in range(N)]
+    wb = ccl.ccl_plan_topk_work_bytes(N)
+    work = torch.empty(wb + 64, dtype=torch.uint8, device=DEV)
+
+    def status(fn):
+        with pytest.raises(C.CclError) as ei:
+            fn()
+        return ei.value.status
+
+    assert status(lambda: ccl.ccl_allreduce_topk(g, e, 10, op="avg_premul", work=work)) == 2  # unsupported
+    assert status(lambda: ccl.ccl_allreduce_topk(g, e, 10, op="max", work=work)) == 1
+    assert status(lambda: ccl.ccl_allreduce_topk(g, e, 10, work=work[:wb - 1])) == 1  # too small
+    assert status(lambda: ccl.ccl_allreduce_topk(g, e, 10, work=work[1:])) == 1  # not 16-byte aligned
+    big = [torch.zeros(K, dtype=torch.bfloat16, device=DEV) for _ in range(17)]
+    bige = [torch.zeros(K, dtype=torch.float32, device=DEV) for _ in range(17)]
+    assert status(lambda: ccl.ccl_allreduce_topk(big, bige, 10)) == 1  # more than 16 ranks
+    # the work buffer inside a residual
+    K2 = 40_000
+    g2 = [torch.zeros(K2, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    e2 = [torch.zeros(K2, dtype=torch.float32, device=DEV) for _ in range(N)]
+    assert status(lambda: ccl.ccl_allreduce_topk(g2, e2, 10, work=e2[1].view(torch.uint8)[:wb])) == 3
+    assert status(lambda: ccl.ccl_allreduce_compressed(g, e, comp="topk")) == 1
+    ccl.ccl_allreduce_topk([t[:0] for t in g], [t[:0] for t in e], 10, work=work)  # count 0: nothing to do
+    torch.cuda.synchronize()
