@@ -218,7 +218,7 @@ ROWS = {
     "allreduce-premul": "AllReduce AVG by pre-multiplication (each contribution times 1/N, then SUM), N=8 bf16 "
                         "64Mi/rank, in place, fused ring order",
     "allreduce-topk": "Top-k sparsified AllReduce AVG with error feedback, k = 1% of each rank's 64Mi bf16 "
-                      "elements (671,089), N=8; threshold by on-device radix select",
+                      "elements (671,088), N=8; threshold by on-device radix select",
     "allreduce-int8": "compressed AllReduce AVG with error feedback, blockwise INT8 (b=128), N=8 bf16 64Mi/rank",
     "overlap": "bucket AllReduce (4 Llama layers, N=8 bf16, 25 MiB buckets) overlapped with a synthetic backward "
                "pass of per-rank gradient GEMMs (4096 tokens); bucket kernels on a second stream as gradients finish",
@@ -479,7 +479,7 @@ def run_row(args, name, local):
         alg = N * K * (2 + 4) + N * K * (2 + 4 + 4 + 2)
         print(json.dumps(line("Top-k AllReduce (1%% kept + error feedback) HBM GB/s of the %d-byte minimum, N=8 bf16 "
                               "128 MB/rank, 1 GB300" % alg, alg, per, launches,
-                              "whole step: topk_init + 3 x (topk_hist_kernel + topk_scan_kernel) + "
+                              "whole step: topk_init, topk_top_kernel + scan, topk_low_kernel + 2 scans, "
                               "compressed_pipe_kernel<bf16, 4>", "bf16",
                               {"nranks": N, "count": K, "k": kk}, {"clocks": clk}, total_ms=tot)))
         return

@@ -290,14 +290,20 @@ ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residual
  * sends everything.  The sent values are AllReduced in ring order in fp32
  * (CCL_SUM, or CCL_AVG dividing once by N; CCL_AVG_PREMUL returns
  * CCL_ERR_UNSUPPORTED) and rounded once to dtype, written to every grads[r].
- * The threshold is found on the device by a radix select (three histogram
- * passes over g and e, no host round trip), then one pass sends, keeps the
+ * The threshold is found on the device by a radix select, with no host round
+ * trip: a 1/16 sample places a window of two top-11-bit bins, one full pass
+ * over g and e counts every key's top bits and the low 20 bits of the keys
+ * in the window, and a second full pass runs only when the k-th key's top
+ * bin fell outside the window.  One more pass then sends, keeps the
  * residuals and reduces.  work: device memory of ccl_plan_topk_work_bytes
- * bytes, 16-byte aligned, owned by the caller, not shared with a concurrent
- * call; its contents need no initialisation.  Up to 16 ranks; grads,
- * residuals and work must not overlap (CCL_ERR_OVERLAP).  Launches: one to
- * reset the work buffer, three histogram-and-scan pairs when 0 < k < count,
- * and the compressed pass (one launch, two with a partial last block of 128). */
+ * bytes (about 12 MiB per rank), 16-byte aligned,
+ * owned by the caller, not shared with a concurrent call; its contents need
+ * no initialisation.  Up to 16 ranks and count < 2^32; grads, residuals and
+ * work must not overlap (CCL_ERR_OVERLAP).  Launches: one to reset the work
+ * buffer; when 0 < k < count the sample and its scan (large aligned inputs),
+ * the full pass and its scan, the two fallback launches (which return at once
+ * when the window held the bin), and the low histogram's two scans; and the
+ * compressed pass (one launch, two with a partial last block of 128). */
 ccl_status_t ccl_allreduce_topk(void *const *grads, float *const *residuals, int nranks, size_t count,
                                 ccl_dtype_t dtype, ccl_op_t op, size_t k, void *work, size_t work_bytes,
                                 cudaStream_t stream);

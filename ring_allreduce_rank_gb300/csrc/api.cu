@@ -885,7 +885,7 @@ static ccl_status_t ccl_allreduce_topk_impl(void *const *grads, float *const *re
         !residuals)
         return CCL_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
-    if (mul_overflows(count, 4))
+    if (mul_overflows(count, 4) || (uint64_t)count > 0xffffffffull) // 32-bit histogram bins
         return CCL_ERR_INVALID_ARG;
     if (count == 0)
         return CCL_OK;

@@ -5,148 +5,124 @@
 // |u|_(k), every tie included, and keeps the rest as residual.  Magnitudes are
 // ordered as the bit patterns of |u| (the sign bit cleared): for numbers that
 // is the order of |u|, and a NaN lands above every number.  The k-th largest
-// 31-bit key tau is found by a radix select in three digit passes (11, 11 and
-// 9 bits, most significant first).  Each pass re-forms u from g and e, counts
-// the keys that agree with the digits fixed so far in a 2048-bin histogram
-// (shared-memory atomics per CTA, merged into a 64-bit histogram per rank),
-// and a one-CTA-per-rank scan walks the bins from the top to the bin holding
-// the k-th key, fixing the next digit and the rank of the key within it.
-// After the third pass tau is exact.  The compressed AllReduce kernel then
-// sends u where key(u) >= tau, in the same pass that writes the residuals and
-// folds the sent values in ring order.
+// 31-bit key tau is found by a radix select on the top 11 key bits (bits
+// 30..20, a 2048-bin histogram) and then the low 20 bits of the keys in the
+// top bin that holds the k-th key (a 2^20-bin histogram, 4 MB per rank,
+// resident in L2).  Both histograms come out of ONE full pass over g and e:
+//   1. a sample (one run of 256 elements in every 16) histograms its top
+//      bits, and a scan picks a window of two top bins that holds the k-th
+//      key with high probability (the sample's order statistics k f -+ m,
+//      f the sampled fraction, m five standard deviations of the count);
+//   2. the full pass counts every key's top bits exactly (shared-memory
+//      atomics per CTA, merged into a 64-bit histogram per rank) and the low
+//      bits of the keys inside the window (global atomics);
+//   3. a scan of the exact top histogram fixes the top bin of the k-th key;
+//      if the window missed it, a second full pass counts that bin's low bits
+//      (its launches return at once when the window held the bin);
+//   4. block sums and a last scan of the low histogram give the exact key.
+// The sample only decides how much work the select does, never its result.
+// The compressed AllReduce kernel then sends u where key(u) >= tau, in the
+// same pass that writes the residuals and folds the sent values in ring order.
 //
 // Everything stays on the device and in the caller's work buffer, so a call
 // never waits for the host and can be captured in a CUDA graph.
+#include <cmath>
+
 #include "ccl_internal.h"
 
 namespace ccl {
 
-constexpr int kTopkBins = 2048;
+constexpr int kTopBins = 2048;          // key bits 30..20
+constexpr int kLowBits = 20;            // key bits 19..0
+constexpr uint32_t kLowBins = 1u << kLowBits;
+constexpr int kLowBlocks = 256;         // a low histogram in blocks of 4096 bins
+constexpr int kLowPerBlock = (int)(kLowBins / kLowBlocks);
+constexpr int kWindow = 2;              // top bins whose low bits the full pass counts
+constexpr int kRegions = kWindow + 1;   // low histograms per rank: the window's, then the fallback's
+constexpr int kRun = 32;                // groups of 8 elements in a sampled run (one group per lane)
+constexpr int kSampleEvery = 16;        // one run in every 16 is sampled
+constexpr int kInitCtas = 64;           // CTAs per rank that clear low histograms
+constexpr uint32_t kNoWindow = 0xffffffffu;
 
 struct TopkState {
-    uint32_t prefix;        // digits fixed so far
-    uint32_t tau;           // the k-th largest key, once all digits are fixed
-    unsigned long long kr;  // rank (1-based) of the k-th key among keys that match prefix
+    uint32_t prefix;        // top digit of the k-th key, once fixed
+    uint32_t tau;           // the k-th largest key, once found
+    unsigned long long kr;  // rank (1-based) of the k-th key among the keys with that top digit
+    uint32_t wlo;           // first top digit of the window, or kNoWindow
+    uint32_t region;        // low histogram that counts the k-th key's top bin
+    uint32_t hit;           // the window held that bin: no second pass
+    uint32_t pad;
 };
 
+// Work buffer, for n ranks: top[n][kTopBins] (u64), stop[n][kTopBins] (u32,
+// the sample's), low[n][kRegions][kLowBins] (u32), blk[n][kLowBlocks] (u64),
+// state[n], tau[n].
 struct TopkParams {
     const void *grads[kTopkMaxRanks];
     const float *res[kTopkMaxRanks];
-    unsigned long long *hist; // [nranks][kTopkBins]
-    TopkState *state;         // [nranks]
-    uint32_t *tau;            // [nranks], read by the compressed kernel
+    unsigned long long *top;
+    uint32_t *stop;
+    uint32_t *low;
+    unsigned long long *blk;
+    TopkState *state;
+    uint32_t *tau; // read by the compressed kernel
     uint64_t K;
     unsigned long long k;
+    unsigned long long qa, qb; // the sample's order statistics that bound the window (qa < qb)
     int nranks;
-    int pass;   // 0, 1, 2
     int vec_ok; // every gradient and residual 16-byte aligned
 };
 
-// Digit layout of the 31-bit key: pass 0 takes bits 30..20, pass 1 bits
-// 19..9, pass 2 bits 8..0.  Keys enter a pass's histogram only when the bits
-// above its digit equal the prefix fixed by the earlier passes.
-__host__ __device__ __forceinline__ int topk_shift(int pass) { return pass == 0 ? 20 : (pass == 1 ? 9 : 0); }
-__host__ __device__ __forceinline__ int topk_bits(int pass) { return pass == 2 ? 9 : 11; }
-
 __device__ __forceinline__ uint32_t topk_key(float g, float e) { return __float_as_uint(__fadd_rn(g, e)) & 0x7fffffffu; }
 
-__device__ __forceinline__ void topk_count(uint32_t *h, uint32_t key, int pass, uint32_t prefix)
+// u = g + e for the 8 elements of group gi (16-byte loads; vec_ok buffers).
+template <int DT, class F> __device__ __forceinline__ void group_keys(const void *g, const float *e, uint64_t gi, F &&f)
 {
-    const int sh = topk_shift(pass);
-    const uint32_t above = pass == 0 ? 0u : key >> (sh + topk_bits(pass));
-    if (above == prefix)
-        atomicAdd(&h[(key >> sh) & ((1u << topk_bits(pass)) - 1u)], 1u);
-}
-
-__global__ void __launch_bounds__(kThreads) topk_init_kernel(const __grid_constant__ TopkParams p)
-{
-    const int r = blockIdx.x;
-    for (int i = threadIdx.x; i < kTopkBins; i += kThreads)
-        gstore<unsigned long long>(p.hist + (size_t)r * kTopkBins + i, 0ull);
-    if (threadIdx.x == 0) {
-        TopkState s;
-        s.prefix = 0;
-        s.kr = p.k;
-        // k = 0: no key reaches tau, nothing is sent; k >= K: every key does
-        s.tau = p.k == 0 ? 0xffffffffu : 0u;
-        gstore<TopkState>(p.state + r, s);
-        gstore<uint32_t>(p.tau + r, s.tau);
+    float gv[8];
+    if (DT == DT_BF16) {
+        const uint4 w = gload<uint4>(static_cast<const uint16_t *>(g) + gi * 8);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            gv[2 * j] = __uint_as_float(ws[j] << 16);
+            gv[2 * j + 1] = __uint_as_float(ws[j] & 0xffff0000u);
+        }
+    } else {
+        const float4 a = gload<float4>(static_cast<const float *>(g) + gi * 8);
+        const float4 b = gload<float4>(static_cast<const float *>(g) + gi * 8 + 4);
+        gv[0] = a.x; gv[1] = a.y; gv[2] = a.z; gv[3] = a.w;
+        gv[4] = b.x; gv[5] = b.y; gv[6] = b.z; gv[7] = b.w;
     }
+    const float4 ea = gload<float4>(e + gi * 8), eb = gload<float4>(e + gi * 8 + 4);
+    const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        f(topk_key(gv[j], ev[j]));
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads) topk_hist_kernel(const __grid_constant__ TopkParams p)
+// Calls f(key) for every element of rank r that this CTA covers: groups of 8
+// elements with 16-byte loads, the rest (all of it when a buffer is
+// unaligned) one element at a time.
+template <int DT, class F> __device__ __forceinline__ void for_each_key(const TopkParams &p, int r, F &&f)
 {
-    __shared__ uint32_t h[kTopkBins];
-    for (int i = threadIdx.x; i < kTopkBins; i += kThreads)
-        h[i] = 0u;
-    __syncthreads();
-    const int r = blockIdx.y, pass = p.pass;
-    const uint32_t prefix = pass == 0 ? 0u : gload<TopkState>(p.state + r).prefix;
     const void *g = p.grads[r];
     const float *e = p.res[r];
     const uint64_t K = p.K;
-    const uint64_t ng = p.vec_ok ? K / 8 : 0; // whole groups of 8 elements
-    for (uint64_t gi = (uint64_t)blockIdx.x * kThreads + threadIdx.x; gi < ng; gi += (uint64_t)gridDim.x * kThreads) {
-        float gv[8];
-        if (DT == DT_BF16) {
-            const uint4 w = gload<uint4>(static_cast<const uint16_t *>(g) + gi * 8);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                gv[2 * j] = __uint_as_float(ws[j] << 16);
-                gv[2 * j + 1] = __uint_as_float(ws[j] & 0xffff0000u);
-            }
-        } else {
-            const float4 a = gload<float4>(static_cast<const float *>(g) + gi * 8);
-            const float4 b = gload<float4>(static_cast<const float *>(g) + gi * 8 + 4);
-            gv[0] = a.x; gv[1] = a.y; gv[2] = a.z; gv[3] = a.w;
-            gv[4] = b.x; gv[5] = b.y; gv[6] = b.z; gv[7] = b.w;
-        }
-        const float4 ea = gload<float4>(e + gi * 8), eb = gload<float4>(e + gi * 8 + 4);
-        const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            topk_count(h, topk_key(gv[j], ev[j]), pass, prefix);
-    }
-    // the elements no whole group covers (all of them when a buffer is unaligned)
-    for (uint64_t i = ng * 8 + (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < K; i += (uint64_t)gridDim.x * kThreads) {
+    const uint64_t ng = p.vec_ok ? K / 8 : 0;
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+    for (uint64_t gi = (uint64_t)blockIdx.x * kThreads + threadIdx.x; gi < ng; gi += stride)
+        group_keys<DT>(g, e, gi, f);
+    for (uint64_t i = ng * 8 + (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < K; i += stride) {
         const uint32_t b = ld_elem<DT>(g, i);
-        topk_count(h, topk_key(__uint_as_float(DT == DT_BF16 ? b << 16 : b), gload<float>(e + i)), pass, prefix);
+        f(topk_key(__uint_as_float(DT == DT_BF16 ? b << 16 : b), gload<float>(e + i)));
     }
-    __syncthreads();
-    unsigned long long *gh = p.hist + (size_t)r * kTopkBins;
-    for (int i = threadIdx.x; i < kTopkBins; i += kThreads)
-        if (h[i] && dbg_ok(gh + i, sizeof(unsigned long long)))
-            atomicAdd(gh + i, (unsigned long long)h[i]);
 }
 
-// One CTA per rank: walk this pass's bins from the largest digit down to the
-// one where the running count reaches kr; fix that digit, take the counts
-// above it off kr, and clear the histogram for the next pass.
-__global__ void __launch_bounds__(kThreads) topk_scan_kernel(const __grid_constant__ TopkParams p)
+// Exclusive prefix sum of one value per thread, in thread order.  Every
+// thread of the CTA calls it; ws holds kThreads / 32 values of shared memory.
+__device__ __forceinline__ unsigned long long cta_exclusive_scan(unsigned long long s, unsigned long long *ws)
 {
-    constexpr int kPer = kTopkBins / kThreads; // bins per thread (pass 2 uses the first quarter of them)
-    __shared__ unsigned long long warp_sum[kThreads / 32];
-    const int r = blockIdx.x, pass = p.pass, t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int nb = 1 << topk_bits(pass), per = nb / kThreads;
-    unsigned long long *gh = p.hist + (size_t)r * kTopkBins;
-    // read before the barriers below: one thread rewrites it after them
-    const TopkState st = gload<TopkState>(p.state + r);
-    // thread t holds bins nb-1-t*per ... nb-per-t*per (descending)
-    unsigned long long c[kPer];
-    unsigned long long s = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        c[j] = j < per ? gload<unsigned long long>(gh + (nb - 1 - (t * per + j))) : 0ull;
-        s += c[j];
-    }
-    __syncthreads(); // every count is read before any is cleared
-#pragma unroll
-    for (int j = 0; j < kPer; ++j)
-        if (j < per)
-            gstore<unsigned long long>(gh + (nb - 1 - (t * per + j)), 0ull);
-    // exclusive scan of s in thread order (descending bins)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned long long incl = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -154,26 +130,266 @@ __global__ void __launch_bounds__(kThreads) topk_scan_kernel(const __grid_consta
         if (lane >= o)
             incl += y;
     }
+    __syncthreads(); // ws may still be read by an earlier call
     if (lane == 31)
-        warp_sum[warp] = incl;
+        ws[warp] = incl;
     __syncthreads();
     unsigned long long base = 0;
     for (int w = 0; w < warp; ++w)
-        base += warp_sum[w];
-    const unsigned long long excl = base + incl - s;
-    if (excl < st.kr && st.kr <= excl + s) {
-        unsigned long long acc = excl;
+        base += ws[w];
+    return base + incl - s;
+}
+
+// Merge a CTA's shared-memory histogram into a global one.
+template <class T> __device__ __forceinline__ void merge_hist(const uint32_t *h, T *gh)
+{
+    for (int i = threadIdx.x; i < kTopBins; i += kThreads)
+        if (h[i] && dbg_ok(gh + i, sizeof(T)))
+            atomicAdd(gh + i, (T)h[i]);
+}
+
+__device__ __forceinline__ uint32_t *low_region(const TopkParams &p, int r, uint32_t region)
+{
+    return p.low + ((size_t)r * kRegions + region) * kLowBins;
+}
+
+__global__ void __launch_bounds__(kThreads) topk_init_kernel(const __grid_constant__ TopkParams p)
+{
+    const int r = blockIdx.y;
+    uint4 *low = reinterpret_cast<uint4 *>(low_region(p, r, 0)); // the window's regions
+    for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < kWindow * kLowBins / 4; i += gridDim.x * kThreads)
+        gstore<uint4>(low + i, make_uint4(0, 0, 0, 0));
+    if (blockIdx.x != 0)
+        return;
+    for (int i = threadIdx.x; i < kTopBins; i += kThreads) {
+        gstore<unsigned long long>(p.top + (size_t)r * kTopBins + i, 0ull);
+        gstore<uint32_t>(p.stop + (size_t)r * kTopBins + i, 0u);
+    }
+    if (threadIdx.x == 0) {
+        TopkState s;
+        s.prefix = 0;
+        s.kr = p.k;
+        // k = 0: no key reaches tau, nothing is sent; k >= K: every key does
+        s.tau = p.k == 0 ? 0xffffffffu : 0u;
+        s.wlo = kNoWindow;
+        s.region = kWindow;
+        s.hit = 0;
+        s.pad = 0;
+        gstore<TopkState>(p.state + r, s);
+        gstore<uint32_t>(p.tau + r, s.tau);
+    }
+}
+
+// 1. The sample: run q of 32 groups (one per lane of a warp) for q = 0, 16,
+// 32, ...: whole 512-byte (bf16) or 1 KB (fp32, residuals) spans, so the
+// sample reads about 1/16 of the bytes.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) topk_sample_kernel(const __grid_constant__ TopkParams p)
+{
+    __shared__ uint32_t h[kTopBins];
+    for (int i = threadIdx.x; i < kTopBins; i += kThreads)
+        h[i] = 0u;
+    __syncthreads();
+    const int r = blockIdx.y, lane = threadIdx.x & 31;
+    const uint64_t ng = p.K / 8, nruns = (ng + kRun - 1) / kRun;
+    const uint64_t nsampled = (nruns + kSampleEvery - 1) / kSampleEvery;
+    const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
+    for (uint64_t w = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); w < nsampled; w += warps) {
+        const uint64_t gi = w * kSampleEvery * kRun + (uint64_t)lane;
+        if (gi < ng)
+            group_keys<DT>(p.grads[r], p.res[r], gi, [&](uint32_t key) { atomicAdd(&h[key >> kLowBits], 1u); });
+    }
+    __syncthreads();
+    merge_hist<uint32_t>(h, p.stop + (size_t)r * kTopBins);
+}
+
+// The window: the top digits of the sample's qa-th and qb-th largest keys
+// (dA >= dB); two bins cover them when dA - dB < 2.
+__global__ void __launch_bounds__(kThreads) topk_window_kernel(const __grid_constant__ TopkParams p)
+{
+    constexpr int kPer = kTopBins / kThreads;
+    __shared__ unsigned long long ws[kThreads / 32];
+    __shared__ int dA, dB;
+    const int r = blockIdx.x, t = threadIdx.x;
+    if (t == 0)
+        dA = dB = -1;
+    const uint32_t *gh = p.stop + (size_t)r * kTopBins;
+    unsigned long long c[kPer], s = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        c[j] = gload<uint32_t>(gh + (kTopBins - 1 - (t * kPer + j)));
+        s += c[j];
+    }
+    const unsigned long long excl = cta_exclusive_scan(s, ws); // its barriers order dA, dB's reset
+    unsigned long long acc = excl;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int d = kTopBins - 1 - (t * kPer + j);
+        if (acc < p.qa && p.qa <= acc + c[j])
+            dA = d;
+        if (acc < p.qb && p.qb <= acc + c[j])
+            dB = d;
+        acc += c[j];
+    }
+    __syncthreads();
+    if (t == 0 && dA >= 0 && dB >= 0 && dA - dB < kWindow) {
+        TopkState st = gload<TopkState>(p.state + r);
+        st.wlo = (uint32_t)(dB + kWindow <= kTopBins ? dB : kTopBins - kWindow);
+        gstore<TopkState>(p.state + r, st);
+    }
+}
+
+// 2. The full pass: exact top histogram, and the low bits of the keys whose
+// top bin lies in the window.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) topk_main_kernel(const __grid_constant__ TopkParams p)
+{
+    __shared__ uint32_t h[kTopBins];
+    for (int i = threadIdx.x; i < kTopBins; i += kThreads)
+        h[i] = 0u;
+    __syncthreads();
+    const int r = blockIdx.y;
+    const uint32_t wlo = gload<TopkState>(p.state + r).wlo;
+    uint32_t *low = low_region(p, r, 0);
+    for_each_key<DT>(p, r, [&](uint32_t key) {
+        const uint32_t d = key >> kLowBits;
+        atomicAdd(&h[d], 1u);
+        const uint32_t w = d - wlo; // wraps past kWindow below the window
+        if (wlo != kNoWindow && w < (uint32_t)kWindow) {
+            uint32_t *b = low + (size_t)w * kLowBins + (key & (kLowBins - 1u));
+            if (dbg_ok(b, sizeof(uint32_t)))
+                atomicAdd(b, 1u);
+        }
+    });
+    __syncthreads();
+    merge_hist<unsigned long long>(h, p.top + (size_t)r * kTopBins);
+}
+
+// 3. One CTA per rank: the top bin of the k-th key, walking from the top;
+// whether the window counted its low bits.
+__global__ void __launch_bounds__(kThreads) topk_top_scan_kernel(const __grid_constant__ TopkParams p)
+{
+    constexpr int kPer = kTopBins / kThreads;
+    __shared__ unsigned long long ws[kThreads / 32];
+    const int r = blockIdx.x, t = threadIdx.x;
+    const unsigned long long *gh = p.top + (size_t)r * kTopBins;
+    const TopkState st = gload<TopkState>(p.state + r); // read before the one write below
+    unsigned long long c[kPer], s = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) { // thread t: bins kTopBins-1-t*kPer downwards
+        c[j] = gload<unsigned long long>(gh + (kTopBins - 1 - (t * kPer + j)));
+        s += c[j];
+    }
+    unsigned long long acc = cta_exclusive_scan(s, ws);
+    if (acc < st.kr && st.kr <= acc + s) {
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
-            if (j < per && acc + c[j] >= st.kr) {
-                const uint32_t digit = (uint32_t)(nb - 1 - (t * per + j));
-                TopkState n;
-                n.prefix = (st.prefix << topk_bits(pass)) | digit;
+            if (acc + c[j] >= st.kr) {
+                TopkState n = st;
+                n.prefix = (uint32_t)(kTopBins - 1 - (t * kPer + j));
                 n.kr = st.kr - acc;
-                n.tau = pass == 2 ? n.prefix : st.tau;
+                const uint32_t w = n.prefix - st.wlo;
+                n.hit = (st.wlo != kNoWindow && w < (uint32_t)kWindow) ? 1u : 0u;
+                n.region = n.hit ? w : (uint32_t)kWindow;
                 gstore<TopkState>(p.state + r, n);
-                if (pass == 2)
-                    gstore<uint32_t>(p.tau + r, n.prefix);
+                break;
+            }
+            acc += c[j];
+        }
+    }
+}
+
+// The fallback when the window missed: clear the fallback histogram, then a
+// second full pass counts the low bits of the chosen top bin into it.
+__global__ void __launch_bounds__(kThreads) topk_fallback_clear_kernel(const __grid_constant__ TopkParams p)
+{
+    const int r = blockIdx.y;
+    if (gload<TopkState>(p.state + r).hit)
+        return;
+    uint4 *low = reinterpret_cast<uint4 *>(low_region(p, r, kWindow));
+    for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < kLowBins / 4; i += gridDim.x * kThreads)
+        gstore<uint4>(low + i, make_uint4(0, 0, 0, 0));
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) topk_fallback_kernel(const __grid_constant__ TopkParams p)
+{
+    const int r = blockIdx.y;
+    const TopkState st = gload<TopkState>(p.state + r);
+    if (st.hit)
+        return;
+    uint32_t *low = low_region(p, r, kWindow);
+    for_each_key<DT>(p, r, [&](uint32_t key) {
+        if ((key >> kLowBits) == st.prefix) {
+            uint32_t *b = low + (key & (kLowBins - 1u));
+            if (dbg_ok(b, sizeof(uint32_t)))
+                atomicAdd(b, 1u);
+        }
+    });
+}
+
+// 4. Sum of each 4096-bin block of the low histogram that holds the k-th key.
+__global__ void __launch_bounds__(kThreads) topk_low_sum_kernel(const __grid_constant__ TopkParams p)
+{
+    __shared__ unsigned long long ws[kThreads / 32];
+    const int r = blockIdx.y, b = blockIdx.x;
+    const uint32_t region = gload<TopkState>(p.state + r).region;
+    const uint4 *q = reinterpret_cast<const uint4 *>(low_region(p, r, region) + (size_t)b * kLowPerBlock);
+    unsigned long long s = 0;
+    for (int i = threadIdx.x; i < kLowPerBlock / 4; i += kThreads) {
+        const uint4 v = gload<uint4>(q + i);
+        s += (unsigned long long)v.x + v.y + v.z + v.w;
+    }
+    const unsigned long long before = cta_exclusive_scan(s, ws);
+    if (threadIdx.x == kThreads - 1)
+        gstore<unsigned long long>(p.blk + (size_t)r * kLowBlocks + b, before + s);
+}
+
+// One CTA per rank: the block, then the bin within it, that holds the k-th
+// key among the keys of the chosen top bin; tau = top digit : low bits.
+__global__ void __launch_bounds__(kThreads) topk_low_scan_kernel(const __grid_constant__ TopkParams p)
+{
+    static_assert(kLowBlocks == kThreads, "one block sum per thread");
+    constexpr int kPer = kLowPerBlock / kThreads;
+    __shared__ unsigned long long ws[kThreads / 32];
+    __shared__ int sel_block;
+    __shared__ unsigned long long sel_kr;
+    const int r = blockIdx.x, t = threadIdx.x;
+    const TopkState st = gload<TopkState>(p.state + r);
+    if (t == 0) {
+        sel_block = -1;
+        sel_kr = 0;
+    }
+    // blocks from the top: thread t takes block kLowBlocks-1-t
+    const unsigned long long bs = gload<unsigned long long>(p.blk + (size_t)r * kLowBlocks + (kLowBlocks - 1 - t));
+    const unsigned long long before = cta_exclusive_scan(bs, ws); // its barriers also order the stores above
+    if (before < st.kr && st.kr <= before + bs) {
+        sel_block = kLowBlocks - 1 - t;
+        sel_kr = st.kr - before;
+    }
+    __syncthreads();
+    const int B = sel_block;
+    if (B < 0)
+        return; // cannot happen when the histograms are consistent; tau keeps its initial value
+    const uint32_t *low = low_region(p, r, st.region) + (size_t)B * kLowPerBlock;
+    unsigned long long c[kPer], s = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        c[j] = gload<uint32_t>(low + (kLowPerBlock - 1 - (t * kPer + j)));
+        s += c[j];
+    }
+    const unsigned long long kr = sel_kr;
+    unsigned long long acc = cta_exclusive_scan(s, ws);
+    if (acc < kr && kr <= acc + s) {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            if (acc + c[j] >= kr) {
+                const uint32_t bin = (uint32_t)B * kLowPerBlock + (uint32_t)(kLowPerBlock - 1 - (t * kPer + j));
+                TopkState n = st;
+                n.tau = (st.prefix << kLowBits) | bin;
+                n.kr = kr - acc;
+                gstore<TopkState>(p.state + r, n);
+                gstore<uint32_t>(p.tau + r, n.tau);
                 break;
             }
             acc += c[j];
@@ -184,7 +400,29 @@ __global__ void __launch_bounds__(kThreads) topk_scan_kernel(const __grid_consta
 size_t topk_work_bytes(int nranks)
 {
     const size_t n = (size_t)nranks;
-    return n * kTopkBins * sizeof(unsigned long long) + n * sizeof(TopkState) + n * sizeof(uint32_t);
+    return n * (kTopBins * sizeof(unsigned long long) + kTopBins * sizeof(uint32_t) +
+                (size_t)kRegions * kLowBins * sizeof(uint32_t) + kLowBlocks * sizeof(unsigned long long) +
+                sizeof(TopkState) + sizeof(uint32_t));
+}
+
+// The sample's size, and the order statistics that bound the window: the
+// number of sampled keys at or above the k-th key is about k f (f the
+// sampled fraction), with a standard deviation below sqrt(k f); five of them
+// on each side.  false when the sample is too small to place a window.
+static bool sample_bounds(uint64_t count, uint64_t k, unsigned long long *qa, unsigned long long *qb)
+{
+    const uint64_t ng = count / 8, nruns = (ng + kRun - 1) / kRun;
+    uint64_t groups = 0;
+    for (uint64_t q = 0; q < nruns; q += kSampleEvery)
+        groups += ng - q * kRun < (uint64_t)kRun ? ng - q * kRun : (uint64_t)kRun;
+    const double nsamp = 8.0 * (double)groups;
+    const double mean = (double)k * nsamp / (double)count;
+    const double m = 5.0 * sqrt(mean) + 2.0;
+    if (mean - m < 1.0 || mean + m > nsamp)
+        return false;
+    *qa = (unsigned long long)(mean - m);
+    *qb = (unsigned long long)ceil(mean + m);
+    return true;
 }
 
 cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, int nranks, uint64_t count,
@@ -200,21 +438,31 @@ cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, in
         if (r < nranks)
             vec = vec && (uintptr_t)grads[r] % 16 == 0 && (uintptr_t)res[r] % 16 == 0;
     }
+    const size_t n = (size_t)nranks;
     char *w = static_cast<char *>(work);
-    p.hist = reinterpret_cast<unsigned long long *>(w);
-    p.state = reinterpret_cast<TopkState *>(w + (size_t)nranks * kTopkBins * sizeof(unsigned long long));
-    p.tau = reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(p.state) + (size_t)nranks * sizeof(TopkState));
+    p.top = reinterpret_cast<unsigned long long *>(w);
+    w += n * kTopBins * sizeof(unsigned long long);
+    p.stop = reinterpret_cast<uint32_t *>(w);
+    w += n * kTopBins * sizeof(uint32_t);
+    p.low = reinterpret_cast<uint32_t *>(w);
+    w += n * kRegions * kLowBins * sizeof(uint32_t);
+    p.blk = reinterpret_cast<unsigned long long *>(w);
+    w += n * kLowBlocks * sizeof(unsigned long long);
+    p.state = reinterpret_cast<TopkState *>(w);
+    w += n * sizeof(TopkState);
+    p.tau = reinterpret_cast<uint32_t *>(w);
     p.K = count;
     p.k = k;
+    p.qa = p.qb = 0;
     p.nranks = nranks;
-    p.pass = 0;
     p.vec_ok = vec ? 1 : 0;
     *tau_out = p.tau;
-    topk_init_kernel<<<(unsigned)nranks, kThreads, 0, stream>>>(p);
+    const bool select = k > 0 && k < count;
+    topk_init_kernel<<<dim3(select ? kInitCtas : 1, (unsigned)nranks), kThreads, 0, stream>>>(p);
     count_launches(1);
     if (cudaError_t e = cudaGetLastError())
         return e;
-    if (k == 0 || k >= count)
+    if (!select)
         return cudaSuccess; // tau is already final
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -223,24 +471,41 @@ cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, in
     if (e != cudaSuccess)
         return e;
     // about eight resident CTAs per SM over all ranks, no more than the elements need
-    const uint64_t groups = (count / (vec ? 8 : 1) + kThreads - 1) / kThreads;
+    const uint64_t items = (count / (vec ? 8 : 1) + kThreads - 1) / kThreads;
     uint64_t per_rank = (uint64_t)sms * 8 / (uint64_t)nranks;
     if (per_rank < 1)
         per_rank = 1;
-    if (per_rank > groups)
-        per_rank = groups > 0 ? groups : 1;
-    for (int pass = 0; pass < 3; ++pass) {
-        p.pass = pass;
+    if (per_rank > items)
+        per_rank = items > 0 ? items : 1;
+    const dim3 grid((unsigned)per_rank, (unsigned)nranks);
+    unsigned long long launches = 0;
+    if (vec && sample_bounds(count, k, &p.qa, &p.qb)) {
+        const uint64_t nruns = (count / 8 + kRun - 1) / kRun;
+        const uint64_t swarps = (nruns + kSampleEvery - 1) / kSampleEvery;
+        uint64_t sctas = (swarps + kThreads / 32 - 1) / (kThreads / 32);
+        if (sctas > per_rank)
+            sctas = per_rank;
         if (dt == DT_FP32)
-            topk_hist_kernel<DT_FP32><<<dim3((unsigned)per_rank, (unsigned)nranks), kThreads, 0, stream>>>(p);
+            topk_sample_kernel<DT_FP32><<<dim3((unsigned)sctas, (unsigned)nranks), kThreads, 0, stream>>>(p);
         else
-            topk_hist_kernel<DT_BF16><<<dim3((unsigned)per_rank, (unsigned)nranks), kThreads, 0, stream>>>(p);
-        topk_scan_kernel<<<(unsigned)nranks, kThreads, 0, stream>>>(p);
-        count_launches(2);
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return e;
+            topk_sample_kernel<DT_BF16><<<dim3((unsigned)sctas, (unsigned)nranks), kThreads, 0, stream>>>(p);
+        topk_window_kernel<<<(unsigned)nranks, kThreads, 0, stream>>>(p);
+        launches += 2;
     }
-    return cudaSuccess;
+    if (dt == DT_FP32)
+        topk_main_kernel<DT_FP32><<<grid, kThreads, 0, stream>>>(p);
+    else
+        topk_main_kernel<DT_BF16><<<grid, kThreads, 0, stream>>>(p);
+    topk_top_scan_kernel<<<(unsigned)nranks, kThreads, 0, stream>>>(p);
+    topk_fallback_clear_kernel<<<dim3(kInitCtas, (unsigned)nranks), kThreads, 0, stream>>>(p);
+    if (dt == DT_FP32)
+        topk_fallback_kernel<DT_FP32><<<grid, kThreads, 0, stream>>>(p);
+    else
+        topk_fallback_kernel<DT_BF16><<<grid, kThreads, 0, stream>>>(p);
+    topk_low_sum_kernel<<<dim3(kLowBlocks, (unsigned)nranks), kThreads, 0, stream>>>(p);
+    topk_low_scan_kernel<<<(unsigned)nranks, kThreads, 0, stream>>>(p);
+    count_launches(launches + 6);
+    return cudaGetLastError();
 }
 
 } // namespace ccl

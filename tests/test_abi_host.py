@@ -97,7 +97,7 @@ def test_planner_topk_bytes(L):
     assert 4 * d / ccl.ccl_plan_topk_bytes(d, d // 1000) == 500
     assert ccl.ccl_plan_topk_bytes(10, 50) == 80  # k beyond count keeps count
     assert ccl.ccl_plan_topk_bytes(10, 0) == 0
-    assert ccl.ccl_plan_topk_work_bytes(8) == 8 * 2048 * 8 + 8 * 16 + 8 * 4
+    assert ccl.ccl_plan_topk_work_bytes(8) == 8 * (2048 * 8 + 2048 * 4 + 3 * (1 << 20) * 4 + 256 * 8 + 32 + 4)
     for n in (0, 17):
         with pytest.raises(C.CclError):
             ccl.ccl_plan_topk_work_bytes(n)

@@ -101,6 +101,47 @@ def test_unaligned_buffers(dtype, pad):
     _check(got_g, got_e, want_g, want_e, "unaligned pad %d" % pad)
 
 
+def _window_hits(work, N):
+    """The select's per-rank record in the work buffer (the layout of
+    topk.cu: top u64[N][2048], sample u32[N][2048], low u32[N][3][2^20],
+    block sums u64[N][256], then one 32-byte record per rank whose 7th word
+    says whether the sampled window held the k-th key's top bin)."""
+    off = N * (2048 * 8 + 2048 * 4 + 3 * (1 << 20) * 4 + 256 * 8)
+    rec = work[off:off + 32 * N].cpu().numpy().view(np.uint32).reshape(N, 8)
+    return rec[:, 6].tolist()
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_sampled_window_hit_and_miss(dtype):
+    """Both ways through the select give the oracle's bits.  Normal data: the
+    1/16 sample places the window on the k-th key's top bin (one full pass).
+    Data whose sampled runs (the first 256 elements of every 4096) hold tiny
+    values: the window lands far below the k-th key and the fallback pass
+    counts the right bin."""
+    N, K, k = 4, 1 << 20, 10_486
+    base = _grads(dtype, N, K, seed=123)
+    if dtype == "bf16":
+        base = [W.to_bf16_bits(W.bf16_bits_to_f32(r)) for r in base]
+    rigged = []
+    idx = np.arange(K)
+    sampled = (idx // 256) % 16 == 0
+    for r in range(N):
+        x = (W.bf16_bits_to_f32(base[r]) if dtype == "bf16" else base[r]).copy()
+        x[sampled] = np.float32(1e-6) * np.sign(x[sampled])
+        rigged.append(W.to_bf16_bits(x) if dtype == "bf16" else x.astype(np.float32))
+    work = torch.empty(ccl.ccl_plan_topk_work_bytes(N), dtype=torch.uint8, device=DEV)
+    for data, expect_hit in ((list(W.normal_bf16(N, K, seed_base=5)) if dtype == "bf16"
+                              else list(W.normal_fp32(N, K, seed_base=5)), 1), (rigged, 0)):
+        e = _res(N, K, seed=9)
+        want_g, want_e = oracle.allreduce_compressed(data, e, "avg", "topk", k=k)
+        g = [to_dev(x) for x in data]
+        ed = [to_dev(x) for x in e]
+        ccl.ccl_allreduce_topk(g, ed, k, op="avg", work=work)
+        torch.cuda.synchronize()
+        assert _window_hits(work, N) == [expect_hit] * N
+        _check([bits(x) for x in g], [bits(x) for x in ed], want_g, want_e, "window hit=%d" % expect_hit)
+
+
 def test_nan_is_sent_first():
     N, K = 3, 4096
     g = list(W.normal_fp32(N, K, seed_base=8))
@@ -159,7 +200,7 @@ def test_argument_errors():
     bige = [torch.zeros(K, dtype=torch.float32, device=DEV) for _ in range(17)]
     assert status(lambda: ccl.ccl_allreduce_topk(big, bige, 10)) == 1  # more than 16 ranks
     # the work buffer inside a residual
-    K2 = 40_000
+    K2 = wb // 4 + 16  # a residual large enough to hold the whole work buffer
     g2 = [torch.zeros(K2, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
     e2 = [torch.zeros(K2, dtype=torch.float32, device=DEV) for _ in range(N)]
     assert status(lambda: ccl.ccl_allreduce_topk(g2, e2, 10, work=e2[1].view(torch.uint8)[:wb])) == 3
