@@ -460,7 +460,7 @@ def run_row(args, name, local):
         clk = clocks.stop()
         alg = N * K * (2 + 4 + 4 + 2)  # gradients read and written, residuals read and written
         print(json.dumps(line("Compressed AllReduce (INT8 blocks + error feedback) HBM GB/s, N=8 bf16 128 MB/rank, "
-                              "1 GB300", alg, per, launches, "compressed_allreduce_kernel<bf16, 4, 8>", "bf16",
+                              "1 GB300", alg, per, launches, "compressed_pipe_kernel<bf16, 4, INT8>", "bf16",
                               {"nranks": N, "count": K, "block": 128}, {"clocks": clk}, total_ms=tot)))
         return
 
@@ -480,7 +480,7 @@ def run_row(args, name, local):
         print(json.dumps(line("Top-k AllReduce (1%% kept + error feedback) HBM GB/s of the %d-byte minimum, N=8 bf16 "
                               "128 MB/rank, 1 GB300" % alg, alg, per, launches,
                               "whole step: topk_init, topk_top_kernel + scan, topk_low_kernel + 2 scans, "
-                              "compressed_pipe_kernel<bf16, 4>", "bf16",
+                              "compressed_pipe_kernel<bf16, 4, TOPK>", "bf16",
                               {"nranks": N, "count": K, "k": kk}, {"clocks": clk}, total_ms=tot)))
         return
 

@@ -164,7 +164,7 @@ __device__ __forceinline__ uint32_t round_to(float x)
 
 // Everything after the loads: u = g + e, compression, residual store, the
 // ring-order fp32 fold and the result store.  v holds g and ee holds e on entry.
-template <int DT, int EPL, int NMAX>
+template <int DT, int EPL, int NMAX, int COMP>
 __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_t i0, int valid, bool vec,
                                                     float (&v)[NMAX][EPL], float (&ee)[NMAX][EPL])
 {
@@ -176,7 +176,7 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
         for (int j = 0; j < EPL; ++j)
             v[r][j] = __fadd_rn(v[r][j], ee[r][j]);
 
-    if (p.comp == COMP_THRESHOLD) {
+    if constexpr (COMP == COMP_THRESHOLD) {
 #pragma unroll
         for (int r = 0; r < NMAX; ++r)
 #pragma unroll
@@ -185,7 +185,7 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
                 v[r][j] = u >= p.threshold ? 1.0f : 0.0f;
                 ee[r][j] = __fsub_rn(u, v[r][j]);
             }
-    } else if (p.comp == COMP_TOPK) {
+    } else if constexpr (COMP == COMP_TOPK) {
 #pragma unroll
         for (int r = 0; r < NMAX; ++r) {
             const uint32_t tau = r < N ? gload<uint32_t>(p.tau + r) : 0xffffffffu;
@@ -369,7 +369,7 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
     }
 }
 
-template <int DT, int EPL, int NMAX>
+template <int DT, int EPL, int NMAX, int COMP>
 __global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allreduce_kernel(const __grid_constant__ CompParams p)
 {
     constexpr int B = 32 * EPL; // compression block
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allred
                 v[r][j] = ee[r][j] = 0.0f; // absent ranks: never stored
         }
     }
-    compress_fold_store<DT, EPL, NMAX>(p, i0, valid, vec, v, ee);
+    compress_fold_store<DT, EPL, NMAX, COMP>(p, i0, valid, vec, v, ee);
 }
 
 // ------------------------------------------------------------------ pipelined form (N <= 8)
@@ -439,7 +439,7 @@ template <int DT, int EPL> struct PipeLayout {
     static constexpr size_t kBytes = kPipeStages * kStage;
 };
 
-template <int DT, int EPL>
+template <int DT, int EPL, int COMP>
 __global__ void __launch_bounds__(kPipeThreads) compressed_pipe_kernel(const __grid_constant__ CompParams p)
 {
     using Lay = PipeLayout<DT, EPL>;
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kPipeThreads) compressed_pipe_kernel(const __g
                     v[r][j] = ee[r][j] = 0.0f;
             }
         }
-        compress_fold_store<DT, EPL, NMAX>(p, i0, EPL, true, v, ee);
+        compress_fold_store<DT, EPL, NMAX, COMP>(p, i0, EPL, true, v, ee);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
@@ -523,7 +523,7 @@ struct PipeConfig {
 };
 static std::mutex g_pipe_cfg_mu;
 
-template <int DT, int EPL>
+template <int DT, int EPL, int COMP>
 static cudaError_t pipe_grid(int *ctas)
 {
     using Lay = PipeLayout<DT, EPL>;
@@ -536,10 +536,10 @@ static cudaError_t pipe_grid(int *ctas)
     PipeConfig &c = cfg[dev];
     if (!c.ready) {
         int sms = 0, per_sm = 0;
-        if ((e = cudaFuncSetAttribute(compressed_pipe_kernel<DT, EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((e = cudaFuncSetAttribute(compressed_pipe_kernel<DT, EPL, COMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)Lay::kBytes)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
-            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compressed_pipe_kernel<DT, EPL>, kPipeThreads,
+            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compressed_pipe_kernel<DT, EPL, COMP>, kPipeThreads,
                                                                Lay::kBytes)) != cudaSuccess)
             return e;
         c.ctas = sms * (per_sm > 0 ? per_sm : 1);
@@ -549,12 +549,12 @@ static cudaError_t pipe_grid(int *ctas)
     return cudaSuccess;
 }
 
-template <int DT, int EPL>
+template <int DT, int EPL, int COMP>
 static cudaError_t launch_pipe_t(const CompParams &p, cudaStream_t stream)
 {
     using Lay = PipeLayout<DT, EPL>;
     int ctas = 0;
-    if (cudaError_t e = pipe_grid<DT, EPL>(&ctas))
+    if (cudaError_t e = pipe_grid<DT, EPL, COMP>(&ctas))
         return e;
     const uint64_t ntiles = (p.nfull + Lay::kWarps - 1) / Lay::kWarps;
     uint64_t grid = (uint64_t)ctas;
@@ -562,12 +562,12 @@ static cudaError_t launch_pipe_t(const CompParams &p, cudaStream_t stream)
         grid = ntiles;
     if (grid == 0)
         return cudaSuccess;
-    compressed_pipe_kernel<DT, EPL><<<(unsigned)grid, kPipeThreads, Lay::kBytes, stream>>>(p);
+    compressed_pipe_kernel<DT, EPL, COMP><<<(unsigned)grid, kPipeThreads, Lay::kBytes, stream>>>(p);
     count_launches(1);
     return cudaGetLastError();
 }
 
-template <int DT, int EPL, int NMAX>
+template <int DT, int EPL, int NMAX, int COMP>
 static cudaError_t launch_comp_t(const CompParams &p, cudaStream_t stream)
 {
     constexpr int B = 32 * EPL;
@@ -578,29 +578,29 @@ static cudaError_t launch_comp_t(const CompParams &p, cudaStream_t stream)
     const uint64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
     if (blocks > 0x7fffffffull)
         return cudaErrorInvalidValue;
-    compressed_allreduce_kernel<DT, EPL, NMAX><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    compressed_allreduce_kernel<DT, EPL, NMAX, COMP><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
     count_launches(1);
     return cudaGetLastError();
 }
 
 // N <= 8 with aligned buffers: whole blocks through the pipelined kernel, the
 // last partial block (if any) through the direct one.  Otherwise all direct.
-template <int DT, int EPL>
+template <int DT, int EPL, int COMP>
 static cudaError_t launch_comp_dt(CompParams p, cudaStream_t stream)
 {
     constexpr int B = 32 * EPL;
     if (p.nranks <= 8 && p.vec_ok) {
         p.nfull = p.K / B;
         if (p.nfull) {
-            cudaError_t e = launch_pipe_t<DT, EPL>(p, stream);
+            cudaError_t e = launch_pipe_t<DT, EPL, COMP>(p, stream);
             if (e != cudaSuccess)
                 return e;
         }
         p.first_block = p.nfull;
-        return launch_comp_t<DT, EPL, 8>(p, stream);
+        return launch_comp_t<DT, EPL, 8, COMP>(p, stream);
     }
     p.first_block = 0;
-    return p.nranks <= 8 ? launch_comp_t<DT, EPL, 8>(p, stream) : launch_comp_t<DT, EPL, 16>(p, stream);
+    return p.nranks <= 8 ? launch_comp_t<DT, EPL, 8, COMP>(p, stream) : launch_comp_t<DT, EPL, 16, COMP>(p, stream);
 }
 
 cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, float threshold,
@@ -634,9 +634,18 @@ cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, f
     p.first_block = 0;
     p.nfull = 0;
     p.tau = tau;
+    // one instantiation per compressor: each kernel carries only its own arithmetic
+    if (comp == COMP_THRESHOLD)
+        return dt == DT_FP32 ? launch_comp_dt<DT_FP32, 4, COMP_THRESHOLD>(p, stream)
+                             : launch_comp_dt<DT_BF16, 4, COMP_THRESHOLD>(p, stream);
+    if (comp == COMP_TOPK)
+        return dt == DT_FP32 ? launch_comp_dt<DT_FP32, 4, COMP_TOPK>(p, stream)
+                             : launch_comp_dt<DT_BF16, 4, COMP_TOPK>(p, stream);
     if (dt == DT_FP32)
-        return epl == 4 ? launch_comp_dt<DT_FP32, 4>(p, stream) : launch_comp_dt<DT_FP32, 2>(p, stream);
-    return epl == 4 ? launch_comp_dt<DT_BF16, 4>(p, stream) : launch_comp_dt<DT_BF16, 2>(p, stream);
+        return epl == 4 ? launch_comp_dt<DT_FP32, 4, COMP_INT8_BLOCK>(p, stream)
+                        : launch_comp_dt<DT_FP32, 2, COMP_INT8_BLOCK>(p, stream);
+    return epl == 4 ? launch_comp_dt<DT_BF16, 4, COMP_INT8_BLOCK>(p, stream)
+                    : launch_comp_dt<DT_BF16, 2, COMP_INT8_BLOCK>(p, stream);
 }
 
 } // namespace ccl

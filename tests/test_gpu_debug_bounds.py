@@ -23,7 +23,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 # not the C example (it links the release library)
 FILES = ["tests/test_gpu_parity.py", "tests/test_gpu_small_chunks.py", "tests/test_gpu_orders.py",
          "tests/test_gpu_compressed.py", "tests/test_gpu_host.py", "tests/test_gpu_checks.py",
-         "tests/test_zz_no_alloc.py"]
+         "tests/test_gpu_premul.py", "tests/test_gpu_topk.py", "tests/test_zz_no_alloc.py"]
 
 
 @pytest.fixture(scope="module")
@@ -41,7 +41,7 @@ def _run(lib, args, extra_env=None):
 
 
 def test_every_kernel_access_stays_inside_the_calls_buffers(debug_lib):
-    res, faults = _run(debug_lib, ["-m", "gpu and not slow", "-k", "not 1024", *FILES])
+    res, faults = _run(debug_lib, ["-m", "gpu and not slow", "-k", "not 1024 and not graph_capture", *FILES])
     assert res.returncode == 0, res.stdout[-4000:] + res.stderr[-2000:]
     assert faults == 0, res.stdout[-2000:]
 
