@@ -64,7 +64,8 @@ extern "C" ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, 
                                                        cudaStream_t stream)
 {
     if (nranks < 1 || nranks > CCL_MAX_RANKS || (dtype != CCL_FP32 && dtype != CCL_BF16) ||
-        (op != CCL_SUM && op != CCL_AVG && op != CCL_MAX && op != CCL_PROD) || !send || !recv)
+        (op != CCL_SUM && op != CCL_AVG && op != CCL_MAX && op != CCL_PROD && op != CCL_MIN &&
+         op != CCL_AVG_PREMUL) || !send || !recv)
         return CCL_ERR_INVALID_ARG;
     const size_t es = dtype == CCL_BF16 ? 2 : 4;
     if (count > SIZE_MAX / es)
@@ -127,7 +128,9 @@ extern "C" ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, 
     for (int s = 0; s < nranks - 1; ++s)
         if (launch_ring_step((int)dtype, (int)op, STEP_RS, s, bufs.data(), nranks, count, stream) != cudaSuccess)
             return CCL_ERR_CUDA;
-    if (op == CCL_AVG &&
+    // AVG divides once at the end; the pre-multiplied AVG scales inside the
+    // steps, and needs this launch only when N = 1 gives it no step
+    if ((op == CCL_AVG || (op == CCL_AVG_PREMUL && nranks == 1)) &&
         launch_ring_step((int)dtype, (int)op, STEP_SCALE, 0, bufs.data(), nranks, count, stream) != cudaSuccess)
         return CCL_ERR_CUDA;
     // the ReduceScatter phase leaves chunk c finished at rank c-1; hand it to rank c

@@ -179,3 +179,28 @@ def test_refused_by_other_orders_and_compression():
         ccl.ccl_allreduce_compressed(x, res, op=OP, comp="int8_block", block=128)
     assert ei.value.status == 2
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("op", ["avg_premul", "min"])
+@pytest.mark.parametrize("N", [1, 5])
+def test_static_scratch_reduce_scatter(op, N):
+    """The allocation-free step-by-step ReduceScatter takes every op the
+    step mode takes, the pre-multiplied AVG included (N = 1: one scaling
+    launch and no steps)."""
+    import ctypes
+    fn = ccl.lib().ccl_reduce_scatter_step_static
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    fn.argtypes = [pp, pp, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    K = 50_003
+    x = inputs("bf16", N, K, seed=N + 40)
+    want = oracle.reduce_scatter(x, op)
+    send = [to_dev(r) for r in x]
+    _, ln = ccl.ccl_plan_chunks(K, N)
+    recv = [empty_like_host(int(ln[r]), torch.bfloat16) for r in range(N)]
+    ptrs = lambda ts: (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    rc = fn(ptrs(send), ptrs(recv), N, K, 1, C.OPS[op], ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, ccl.ccl_status_string(rc)
+    torch.cuda.synchronize()
+    for r in range(N):
+        assert_bits_equal(bits(recv[r]), want[r], "static scratch %s N=%d rank %d" % (op, N, r))
