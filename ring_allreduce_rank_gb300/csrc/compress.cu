@@ -162,11 +162,21 @@ __device__ __forceinline__ uint32_t round_to(float x)
     return *reinterpret_cast<uint32_t *>(&p) & 0xffffu;
 }
 
+// Each rank's Top-k threshold key, read once per kernel (all-ones, which no
+// key reaches, for the other compressors and absent ranks).
+template <int NMAX, int COMP> __device__ __forceinline__ void load_tau(const CompParams &p, uint32_t (&tau)[NMAX])
+{
+#pragma unroll
+    for (int r = 0; r < NMAX; ++r)
+        tau[r] = (COMP == COMP_TOPK && r < p.nranks) ? gload<uint32_t>(p.tau + r) : 0xffffffffu;
+}
+
 // Everything after the loads: u = g + e, compression, residual store, the
 // ring-order fp32 fold and the result store.  v holds g and ee holds e on entry.
 template <int DT, int EPL, int NMAX, int COMP>
 __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_t i0, int valid, bool vec,
-                                                    float (&v)[NMAX][EPL], float (&ee)[NMAX][EPL])
+                                                    float (&v)[NMAX][EPL], float (&ee)[NMAX][EPL],
+                                                    const uint32_t (&tau)[NMAX])
 {
     const int N = p.nranks;
     // u = g + e (kept in v until it is replaced by the transmitted value)
@@ -188,11 +198,10 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
     } else if constexpr (COMP == COMP_TOPK) {
 #pragma unroll
         for (int r = 0; r < NMAX; ++r) {
-            const uint32_t tau = r < N ? gload<uint32_t>(p.tau + r) : 0xffffffffu;
 #pragma unroll
             for (int j = 0; j < EPL; ++j) {
                 const float u = v[r][j];
-                v[r][j] = (__float_as_uint(u) & 0x7fffffffu) >= tau ? u : 0.0f;
+                v[r][j] = (__float_as_uint(u) & 0x7fffffffu) >= tau[r] ? u : 0.0f;
                 ee[r][j] = __fsub_rn(u, v[r][j]);
             }
         }
@@ -397,7 +406,9 @@ __global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allred
                 v[r][j] = ee[r][j] = 0.0f; // absent ranks: never stored
         }
     }
-    compress_fold_store<DT, EPL, NMAX, COMP>(p, i0, valid, vec, v, ee);
+    uint32_t tau[NMAX];
+    load_tau<NMAX, COMP>(p, tau);
+    compress_fold_store<DT, EPL, NMAX, COMP>(p, i0, valid, vec, v, ee, tau);
 }
 
 // ------------------------------------------------------------------ pipelined form (N <= 8)
@@ -473,6 +484,8 @@ __global__ void __launch_bounds__(kPipeThreads) compressed_pipe_kernel(const __g
     uint64_t t = blockIdx.x;
     if (t >= ntiles)
         return;
+    uint32_t tau[NMAX];
+    load_tau<NMAX, COMP>(p, tau);
     for (int k = 0; k < kPipeStages - 1; ++k)
         issue(t + (uint64_t)k * gridDim.x, k);
     for (int it = 0; t < ntiles; ++it, t += gridDim.x) {
@@ -509,7 +522,7 @@ __global__ void __launch_bounds__(kPipeThreads) compressed_pipe_kernel(const __g
                     v[r][j] = ee[r][j] = 0.0f;
             }
         }
-        compress_fold_store<DT, EPL, NMAX, COMP>(p, i0, EPL, true, v, ee);
+        compress_fold_store<DT, EPL, NMAX, COMP>(p, i0, EPL, true, v, ee, tau);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }

@@ -156,9 +156,11 @@ __device__ __forceinline__ uint32_t *low_region(const TopkParams &p, int r, uint
 __global__ void __launch_bounds__(kThreads) topk_init_kernel(const __grid_constant__ TopkParams p)
 {
     const int r = blockIdx.y;
-    uint4 *low = reinterpret_cast<uint4 *>(low_region(p, r, 0)); // the window's regions
-    for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < kWindow * kLowBins / 4; i += gridDim.x * kThreads)
-        gstore<uint4>(low + i, make_uint4(0, 0, 0, 0));
+    if (p.k > 0 && p.k < p.K) { // the window's low histograms, only when a select follows
+        uint4 *low = reinterpret_cast<uint4 *>(low_region(p, r, 0));
+        for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < kWindow * kLowBins / 4; i += gridDim.x * kThreads)
+            gstore<uint4>(low + i, make_uint4(0, 0, 0, 0));
+    }
     if (blockIdx.x != 0)
         return;
     for (int i = threadIdx.x; i < kTopBins; i += kThreads) {
