@@ -68,6 +68,9 @@
  *     step-mode ReduceScatter or bucket AllReduce calls whose work overlaps
  *     on the GPU (different streams, different host threads) race on it and
  *     must be serialised.  Fused calls share nothing.
+ *   - The environment variable CCL_MODE (or ccl_set_mode_override) can force
+ *     one mode on every call that takes a mode argument; a forced step mode
+ *     brings the step-mode rules above with it.  See "Settings" below.
  */
 #ifndef CCL_H
 #define CCL_H
@@ -170,8 +173,10 @@ ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nrank
  * Each rank registers ntensors gradient tensors in forward order:
  * ptrs[r*ntensors + t] is rank r's tensor t (numels[t] elements, HOST array).
  * The tensors are laid end to end in REVERSE registration order, the stream is
- * cut into buckets of bucket_bytes (0 = CCL_DEFAULT_BUCKET_BYTES, 25 MiB; the
- * last bucket is partial and a tensor may span buckets) and every bucket is
+ * cut into buckets of bucket_bytes (0 = the default bucket size: 25 MiB,
+ * CCL_DEFAULT_BUCKET_BYTES, unless CCL_BUCKET_MB or
+ * ccl_set_default_bucket_bytes changed it; the last bucket is partial and a
+ * tensor may span buckets) and every bucket is
  * ring-AllReduced on its own, with its own N-chunk partition.  In place on the
  * tensors; nothing is copied into a staging bucket (the kernel reads and writes
  * the pieces where they are). */
@@ -402,8 +407,8 @@ ccl_status_t ccl_check_read(unsigned long long *mismatches, int reset);
  * table in debug builds: run them one at a time there. */
 ccl_status_t ccl_debug_faults(unsigned long long *faults, unsigned long long *first_address);
 
-/* One traced call: the collective, its shape, the kernels it enqueued and
- * the host time it took to validate, plan and enqueue (not GPU time). */
+/* One traced call: the collective, its shape, the kernels it enqueued, the
+ * host time it took to validate, plan and enqueue, and its device time. */
 typedef struct {
     char collective[24];
     int nranks;
@@ -415,6 +420,14 @@ typedef struct {
     unsigned long long count;
     unsigned long long host_ns;
     unsigned long long seq;
+    /* Device time from the start to the end of the call's work on its stream
+     * (two events recorded around it; Collective Communication, libraries
+     * section: time a collective against a bare baseline with a profiler
+     * before tuning it).  0 until that work has completed on the device --
+     * ccl_trace_read fills it in once it has -- and 0 for calls not timed:
+     * made while the stream was being captured into a CUDA graph, or in a
+     * process without a device. */
+    unsigned long long gpu_ns;
 } ccl_trace_record_t;
 
 /* Tracing is off unless CCL_TRACE is set (to anything but 0) or enabled here.
@@ -424,6 +437,46 @@ void ccl_set_trace(int enabled);
  * (out == NULL: returns how many are held). */
 size_t ccl_trace_read(ccl_trace_record_t *out, size_t max_records);
 void ccl_trace_clear(void);
+
+/* ------------------------------------------------------------------ */
+/* Settings (host only; no GPU needed)                                 */
+/* ------------------------------------------------------------------ */
+
+/* Library-wide settings, read from the environment once, on first use, and
+ * replaced by the setters below (Collective Communication, libraries section:
+ * NCCL is steered by environment variables such as NCCL_ALGO; bucket fusion
+ * section: DDP's bucket_cap_mb, 25 MB by default).
+ *   CCL_MODE=fused | step (any case): every call that takes a mode argument
+ *     (AllReduce, ReduceScatter, AllGather, Broadcast, Reduce, Gather,
+ *     Scatter, AllToAll(v), bucket AllReduce) runs in that mode whatever it
+ *     passes, so that a whole program can be re-run with the ring executed
+ *     step by step (same bits, slower) without changing its calls.  Unset or
+ *     empty: each call's own argument.  A mode argument that is not a valid
+ *     ccl_mode_t is still rejected.  Trace records show the mode that ran.
+ *   CCL_BUCKET_MB=<MiB>, a positive decimal number (e.g. 25 or 0.5): the
+ *     bucket size of ccl_bucket_allreduce and ccl_bucketer_create calls that
+ *     pass bucket_bytes = 0; at least 4 bytes, at most 1 TiB.
+ *   CCL_TRACE, CCL_CHECK: ccl_set_trace, ccl_set_check.
+ * A value that cannot be read is ignored (the default stays) with one line on
+ * stderr.  The settings are process-wide and may be changed at any time; a
+ * call uses the values current when it is made. */
+typedef struct {
+    int mode_override;           /* -1: none; else CCL_MODE_FUSED or CCL_MODE_STEP */
+    int trace;                   /* 1 when call tracing is on */
+    int check;                   /* 1 when automatic result checks are on */
+    int reserved;                /* 0 */
+    size_t default_bucket_bytes; /* the bucket size that bucket_bytes = 0 selects */
+} ccl_config_t;
+
+/* The current settings (CCL_ERR_INVALID_ARG for a NULL out). */
+ccl_status_t ccl_get_config(ccl_config_t *out);
+/* mode: CCL_MODE_FUSED or CCL_MODE_STEP forces that mode; -1 removes the
+ * override (CCL_MODE is then no longer consulted).  Anything else:
+ * CCL_ERR_INVALID_ARG, nothing changed. */
+ccl_status_t ccl_set_mode_override(int mode);
+/* bytes >= 4 sets the default bucket size; 0 restores 25 MiB
+ * (CCL_DEFAULT_BUCKET_BYTES); 1 to 3: CCL_ERR_INVALID_ARG, nothing changed. */
+ccl_status_t ccl_set_default_bucket_bytes(size_t bytes);
 
 /* ------------------------------------------------------------------ */
 /* Planner (host only; no GPU needed)                                  */

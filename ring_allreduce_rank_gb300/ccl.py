@@ -33,6 +33,12 @@ _lock = threading.Lock()
 _lib = None
 
 
+class Config(ctypes.Structure):
+    """ccl_config_t."""
+    _fields_ = [("mode_override", ctypes.c_int), ("trace", ctypes.c_int), ("check", ctypes.c_int),
+                ("reserved", ctypes.c_int), ("default_bucket_bytes", ctypes.c_size_t)]
+
+
 class CclError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -105,6 +111,12 @@ def lib() -> ctypes.CDLL:
             L.ccl_trace_read.restype = sz
             L.ccl_trace_clear.argtypes = []
             L.ccl_trace_clear.restype = None
+            L.ccl_get_config.argtypes = [ctypes.POINTER(Config)]
+            L.ccl_get_config.restype = ctypes.c_int
+            L.ccl_set_mode_override.argtypes = [i32]
+            L.ccl_set_mode_override.restype = ctypes.c_int
+            L.ccl_set_default_bucket_bytes.argtypes = [sz]
+            L.ccl_set_default_bucket_bytes.restype = ctypes.c_int
             L.ccl_status_string.argtypes = [ctypes.c_int]
             L.ccl_status_string.restype = ctypes.c_char_p
             L.ccl_version.argtypes = []
@@ -302,9 +314,11 @@ def ccl_alltoallv(send: Sequence[torch.Tensor], recv: Sequence[torch.Tensor], co
            "ccl_alltoallv")
 
 
-def ccl_bucket_allreduce(tensors: Sequence[Sequence[torch.Tensor]], bucket_bytes: int = DEFAULT_BUCKET_BYTES,
+def ccl_bucket_allreduce(tensors: Sequence[Sequence[torch.Tensor]], bucket_bytes: int = 0,
                          op="sum", mode="fused", stream=None) -> None:
-    """tensors[r][t]: rank r's t-th gradient in registration order (in place)."""
+    """tensors[r][t]: rank r's t-th gradient in registration order (in place).
+    bucket_bytes = 0 takes the library's default bucket size (25 MiB, or
+    CCL_BUCKET_MB / ccl_set_default_bucket_bytes)."""
     nranks, nt = len(tensors), len(tensors[0])
     flat = [tensors[r][t] for r in range(nranks) for t in range(nt)]
     numels = [tensors[0][t].numel() for t in range(nt)]
@@ -325,7 +339,8 @@ def ccl_check_identical(bufs: Sequence[torch.Tensor], mismatches: torch.Tensor, 
 class TraceRecord(ctypes.Structure):
     _fields_ = [("collective", ctypes.c_char * 24), ("nranks", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("op", ctypes.c_int), ("mode", ctypes.c_int), ("status", ctypes.c_int), ("launches", ctypes.c_uint),
-                ("count", ctypes.c_ulonglong), ("host_ns", ctypes.c_ulonglong), ("seq", ctypes.c_ulonglong)]
+                ("count", ctypes.c_ulonglong), ("host_ns", ctypes.c_ulonglong), ("seq", ctypes.c_ulonglong),
+                ("gpu_ns", ctypes.c_ulonglong)]
 
 
 def ccl_debug_faults():
@@ -359,7 +374,8 @@ def ccl_trace_read(max_records: int = 4096):
     buf = (TraceRecord * max(1, n))()
     n = lib().ccl_trace_read(ctypes.cast(buf, ctypes.c_void_p), n)
     return [{"collective": r.collective.decode(), "nranks": r.nranks, "dtype": r.dtype, "op": r.op, "mode": r.mode,
-             "status": r.status, "launches": r.launches, "count": r.count, "host_ns": r.host_ns, "seq": r.seq}
+             "status": r.status, "launches": r.launches, "count": r.count, "host_ns": r.host_ns, "seq": r.seq,
+             "gpu_ns": r.gpu_ns}
             for r in buf[:n]]
 
 
@@ -367,11 +383,32 @@ def ccl_trace_clear() -> None:
     lib().ccl_trace_clear()
 
 
+def ccl_get_config() -> dict:
+    """The library's settings: mode override ("fused", "step" or None),
+    trace, check, default bucket bytes."""
+    c = Config()
+    _check(lib().ccl_get_config(ctypes.byref(c)), "ccl_get_config")
+    names = {v: k for k, v in MODES.items()}
+    return {"mode_override": names.get(c.mode_override), "trace": bool(c.trace), "check": bool(c.check),
+            "default_bucket_bytes": int(c.default_bucket_bytes)}
+
+
+def ccl_set_mode_override(mode: Optional[str]) -> None:
+    """Force "fused" or "step" on every call that takes a mode; None removes
+    the override."""
+    _check(lib().ccl_set_mode_override(-1 if mode is None else _mode(mode)), "ccl_set_mode_override")
+
+
+def ccl_set_default_bucket_bytes(nbytes: int) -> None:
+    """Bucket size for bucket_bytes = 0 (0 restores 25 MiB)."""
+    _check(lib().ccl_set_default_bucket_bytes(int(nbytes)), "ccl_set_default_bucket_bytes")
+
+
 class CclBucketer:
     """ccl_bucketer_*: per-bucket AllReduce launched as gradients become ready.
     tensors[r][t] as for ccl_bucket_allreduce; keep them alive while in use."""
 
-    def __init__(self, tensors: Sequence[Sequence[torch.Tensor]], bucket_bytes: int = DEFAULT_BUCKET_BYTES,
+    def __init__(self, tensors: Sequence[Sequence[torch.Tensor]], bucket_bytes: int = 0,
                  op="sum", max_ctas: int = 0):
         nranks, nt = len(tensors), len(tensors[0])
         self._tensors = tensors

@@ -188,7 +188,7 @@ const char *ccl_status_string(ccl_status_t s)
     return "unknown status";
 }
 
-int ccl_version(void) { return 10000; }
+int ccl_version(void) { return 10100; }
 
 unsigned long long ccl_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -559,7 +559,7 @@ static ccl_status_t ccl_bucket_allreduce_impl(void *const *ptrs, const size_t *n
         return CCL_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     if (bucket_bytes == 0)
-        bucket_bytes = CCL_DEFAULT_BUCKET_BYTES;
+        bucket_bytes = default_bucket_bytes();
     const size_t B = bucket_bytes / es;
     if (B == 0)
         return CCL_ERR_INVALID_ARG;
@@ -987,7 +987,8 @@ static ccl_status_t then_check(ccl_status_t st, const void *const *outs, int nra
 ccl_status_t ccl_allreduce(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
                            ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("allreduce", nranks, count, (int)dtype, (int)op, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("allreduce", nranks, count, (int)dtype, (int)op, (int)mode, stream);
     return tr.done(then_check(ccl_allreduce_impl(send, recv, nranks, count, dtype, op, mode, stream), recv, nranks,
                               count, dtype, stream));
 }
@@ -996,21 +997,23 @@ ccl_status_t ccl_allreduce_host(const void *const *send, void *const *recv, int 
                                 ccl_dtype_t dtype, ccl_op_t op, void *work, size_t work_bytes,
                                 cudaStream_t stream)
 {
-    TraceScope tr("allreduce_host", nranks, count, (int)dtype, (int)op, 0);
+    TraceScope tr("allreduce_host", nranks, count, (int)dtype, (int)op, 0, stream);
     return tr.done(ccl_allreduce_host_impl(send, recv, nranks, count, dtype, op, work, work_bytes, stream));
 }
 
 ccl_status_t ccl_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
                                 ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("reduce_scatter", nranks, count, (int)dtype, (int)op, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("reduce_scatter", nranks, count, (int)dtype, (int)op, (int)mode, stream);
     return tr.done(ccl_reduce_scatter_impl(send, recv, nranks, count, dtype, op, mode, stream));
 }
 
 ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
                            ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("allgather", nranks, count, (int)dtype, -1, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("allgather", nranks, count, (int)dtype, -1, (int)mode, stream);
     return tr.done(then_check(ccl_allgather_impl(send, recv, nranks, count, dtype, mode, stream), recv, nranks, count,
                               dtype, stream));
 }
@@ -1018,7 +1021,8 @@ ccl_status_t ccl_allgather(const void *const *send, void *const *recv, int nrank
 ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                            ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("broadcast", nranks, count, (int)dtype, -1, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("broadcast", nranks, count, (int)dtype, -1, (int)mode, stream);
     return tr.done(then_check(ccl_broadcast_impl(send, recv, nranks, root, count, dtype, mode, stream), recv, nranks,
                               count, dtype, stream));
 }
@@ -1026,14 +1030,16 @@ ccl_status_t ccl_broadcast(const void *const *send, void *const *recv, int nrank
 ccl_status_t ccl_alltoallv(const void *const *send, void *const *recv, int nranks, const size_t *counts,
                            ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("alltoallv", nranks, 0, (int)dtype, -1, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("alltoallv", nranks, 0, (int)dtype, -1, (int)mode, stream);
     return tr.done(ccl_alltoallv_impl(send, recv, nranks, counts, dtype, mode, stream));
 }
 
 ccl_status_t ccl_alltoall(const void *const *send, void *const *recv, int nranks, size_t count, ccl_dtype_t dtype,
                           ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("alltoall", nranks, count, (int)dtype, -1, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("alltoall", nranks, count, (int)dtype, -1, (int)mode, stream);
     return tr.done(ccl_alltoall_impl(send, recv, nranks, count, dtype, mode, stream));
 }
 
@@ -1041,28 +1047,32 @@ ccl_status_t ccl_bucket_allreduce(void *const *ptrs, const size_t *numels, int n
                                   size_t bucket_bytes, ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode,
                                   cudaStream_t stream)
 {
-    TraceScope tr("bucket_allreduce", nranks, (size_t)ntensors, (int)dtype, (int)op, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("bucket_allreduce", nranks, (size_t)ntensors, (int)dtype, (int)op, (int)mode, stream);
     return tr.done(ccl_bucket_allreduce_impl(ptrs, numels, ntensors, nranks, bucket_bytes, dtype, op, mode, stream));
 }
 
 ccl_status_t ccl_reduce(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                         ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("reduce", nranks, count, (int)dtype, (int)op, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("reduce", nranks, count, (int)dtype, (int)op, (int)mode, stream);
     return tr.done(ccl_reduce_impl(send, recv, nranks, root, count, dtype, op, mode, stream));
 }
 
 ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                         ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("gather", nranks, count, (int)dtype, -1, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("gather", nranks, count, (int)dtype, -1, (int)mode, stream);
     return tr.done(ccl_gather_impl(send, recv, nranks, root, count, dtype, mode, stream));
 }
 
 ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                          ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream)
 {
-    TraceScope tr("scatter", nranks, count, (int)dtype, -1, (int)mode);
+    mode = effective_mode(mode);
+    TraceScope tr("scatter", nranks, count, (int)dtype, -1, (int)mode, stream);
     return tr.done(ccl_scatter_impl(send, recv, nranks, root, count, dtype, mode, stream));
 }
 
@@ -1070,7 +1080,7 @@ ccl_status_t ccl_allreduce_algo(const void *const *send, void *const *recv, int 
                                 ccl_dtype_t dtype, ccl_op_t op, ccl_algo_t algo, int group_size,
                                 cudaStream_t stream)
 {
-    TraceScope tr("allreduce_algo", nranks, count, (int)dtype, (int)op, (int)algo);
+    TraceScope tr("allreduce_algo", nranks, count, (int)dtype, (int)op, (int)algo, stream);
     return tr.done(then_check(ccl_allreduce_algo_impl(send, recv, nranks, count, dtype, op, algo, group_size, stream),
                               recv, nranks, count, dtype, stream));
 }
@@ -1079,7 +1089,7 @@ ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residual
                                       ccl_dtype_t dtype, ccl_op_t op, ccl_compressor_t comp, int block,
                                       float threshold, cudaStream_t stream)
 {
-    TraceScope tr("allreduce_compressed", nranks, count, (int)dtype, (int)op, (int)comp);
+    TraceScope tr("allreduce_compressed", nranks, count, (int)dtype, (int)op, (int)comp, stream);
     return tr.done(then_check(ccl_allreduce_compressed_impl(grads, residuals, nranks, count, dtype, op, comp, block,
                                                             threshold, stream),
                               grads, nranks, count, dtype, stream));
@@ -1089,7 +1099,7 @@ ccl_status_t ccl_allreduce_topk(void *const *grads, float *const *residuals, int
                                 ccl_dtype_t dtype, ccl_op_t op, size_t k, void *work, size_t work_bytes,
                                 cudaStream_t stream)
 {
-    TraceScope tr("allreduce_topk", nranks, count, (int)dtype, (int)op, (int)CCL_COMP_TOPK);
+    TraceScope tr("allreduce_topk", nranks, count, (int)dtype, (int)op, (int)CCL_COMP_TOPK, stream);
     return tr.done(then_check(ccl_allreduce_topk_impl(grads, residuals, nranks, count, dtype, op, k, work,
                                                       work_bytes, stream),
                               grads, nranks, count, dtype, stream));

@@ -48,7 +48,7 @@ ccl_status_t ccl_bucketer_create(void *const *ptrs, const size_t *numels, int nt
     *out = nullptr;
     const size_t es = dtype == CCL_BF16 ? 2 : 4;
     if (bucket_bytes == 0)
-        bucket_bytes = CCL_DEFAULT_BUCKET_BYTES;
+        bucket_bytes = default_bucket_bytes();
     const size_t B = bucket_bytes / es;
     if (B == 0)
         return CCL_ERR_INVALID_ARG;

@@ -139,14 +139,27 @@ cudaError_t dbg_set_ranges(const std::vector<DbgRange> &ranges, cudaStream_t str
 // counter; a no-op otherwise.
 cudaError_t auto_check(const void *const *bufs, int nranks, uint64_t count, int elem_size, cudaStream_t stream);
 
+// ------------------------------------------------------------------ settings
+// The mode a call runs in: its own argument, or the one CCL_MODE /
+// ccl_set_mode_override forces (invalid arguments are returned unchanged).
+ccl_mode_t effective_mode(ccl_mode_t requested);
+// Bucket size used when a call passes bucket_bytes = 0 (CCL_BUCKET_MB /
+// ccl_set_default_bucket_bytes, else CCL_DEFAULT_BUCKET_BYTES).
+size_t default_bucket_bytes();
+// Whether automatic result checks and call tracing are on.
+bool check_enabled();
+bool trace_enabled();
+
 // ------------------------------------------------------------------ bookkeeping
 // (count_launches is declared in fused.h)
 
 // Records one call in the trace ring buffer when tracing is on (CCL_TRACE or
-// ccl_set_trace): construct at entry, pass the status through done().
+// ccl_set_trace): construct at entry, pass the status through done().  The
+// call's device time is taken with two events recorded on `stream` around it
+// (not while the stream is being captured into a graph).
 class TraceScope {
   public:
-    TraceScope(const char *name, int nranks, uint64_t count, int dtype, int op, int mode);
+    TraceScope(const char *name, int nranks, uint64_t count, int dtype, int op, int mode, cudaStream_t stream);
     ccl_status_t done(ccl_status_t st)
     {
         finish((int)st);
@@ -156,6 +169,8 @@ class TraceScope {
   private:
     void finish(int status);
     bool active_;
+    cudaStream_t stream_ = nullptr;
+    cudaEvent_t ev0_ = nullptr, ev1_ = nullptr;
     ccl_trace_record_t rec_{};
     unsigned long long launches0_ = 0;
     long long t0_ = 0;

@@ -8,7 +8,8 @@
 // it never traps, so a corrupted result is reported, not fatal.
 //
 // Tracing keeps the last calls' descriptions (collective, ranks, count, type,
-// op, mode, kernels launched, host time to enqueue) in a host ring buffer.
+// op, mode, kernels launched, host time to enqueue, and device time from two
+// events around the call's work on its stream) in a host ring buffer.
 #include <atomic>
 #include <chrono>
 #include <cstdlib>
@@ -153,6 +154,7 @@ namespace {
 std::atomic<int> g_check_on{-1}; // -1: read CCL_CHECK on first use
 std::mutex g_chk_mu;
 std::unordered_map<int, unsigned long long *> g_chk_ctr; // per device
+} // namespace
 
 bool check_enabled()
 {
@@ -164,7 +166,6 @@ bool check_enabled()
     }
     return v > 0;
 }
-} // namespace
 
 cudaError_t auto_check(const void *const *bufs, int nranks, uint64_t count, int elem_size, cudaStream_t stream)
 {
@@ -202,8 +203,36 @@ namespace {
 constexpr size_t kTraceCap = 4096;
 std::mutex g_trace_mu;
 ccl_trace_record_t g_trace[kTraceCap];
+// the events around each held call, until its device time has been read
+struct EventPair {
+    cudaEvent_t start, end;
+};
+EventPair g_trace_ev[kTraceCap];
 size_t g_trace_next = 0, g_trace_count = 0;
+
+void release(EventPair &p)
+{
+    // an event still pending is released by the runtime once it completes
+    if (p.start)
+        cudaEventDestroy(p.start);
+    if (p.end)
+        cudaEventDestroy(p.end);
+    p.start = p.end = nullptr;
+}
+
+// Fills in the device time of a held call whose events have completed.
+void resolve(size_t slot)
+{
+    EventPair &p = g_trace_ev[slot];
+    if (!p.end || cudaEventQuery(p.end) != cudaSuccess)
+        return;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, p.start, p.end) == cudaSuccess && ms >= 0.0f)
+        g_trace[slot].gpu_ns = (unsigned long long)((double)ms * 1e6 + 0.5);
+    release(p);
+}
 std::atomic<int> g_trace_on{-1}; // -1: read CCL_TRACE on first use
+} // namespace
 
 bool trace_enabled()
 {
@@ -215,10 +244,10 @@ bool trace_enabled()
     }
     return v > 0;
 }
-} // namespace
 
-TraceScope::TraceScope(const char *name, int nranks, uint64_t count, int dtype, int op, int mode)
-    : active_(trace_enabled())
+TraceScope::TraceScope(const char *name, int nranks, uint64_t count, int dtype, int op, int mode,
+                       cudaStream_t stream)
+    : active_(trace_enabled()), stream_(stream)
 {
     // an NVTX range per call, so that profiler timelines name the collective
     // (no cost beyond a check when no tool is attached)
@@ -234,6 +263,20 @@ TraceScope::TraceScope(const char *name, int nranks, uint64_t count, int dtype, 
     rec_.mode = mode;
     launches0_ = ccl_launch_count();
     t0_ = std::chrono::steady_clock::now().time_since_epoch().count();
+    // device time: an event before the call's work on its stream (none while
+    // the stream is being captured, where events would become graph nodes)
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return;
+    }
+    if (cudaEventCreate(&ev0_) != cudaSuccess || cudaEventCreate(&ev1_) != cudaSuccess ||
+        cudaEventRecord(ev0_, stream) != cudaSuccess) {
+        cudaGetLastError();
+        EventPair p{ev0_, ev1_};
+        release(p);
+        ev0_ = ev1_ = nullptr;
+    }
 }
 
 void TraceScope::finish(int status)
@@ -246,9 +289,17 @@ void TraceScope::finish(int status)
     rec_.status = status;
     rec_.launches = (unsigned)(ccl_launch_count() - launches0_);
     rec_.host_ns = (unsigned long long)(t1 - t0_);
+    rec_.gpu_ns = 0;
+    EventPair ev{ev0_, ev1_};
+    if (ev.end && cudaEventRecord(ev.end, stream_) != cudaSuccess) {
+        cudaGetLastError();
+        release(ev);
+    }
     std::lock_guard<std::mutex> lk(g_trace_mu);
     rec_.seq = g_trace_count;
+    release(g_trace_ev[g_trace_next]); // the overwritten call's events, if unread
     g_trace[g_trace_next] = rec_;
+    g_trace_ev[g_trace_next] = ev;
     g_trace_next = (g_trace_next + 1) % kTraceCap;
     ++g_trace_count;
 }
@@ -334,14 +385,19 @@ size_t ccl_trace_read(ccl_trace_record_t *out, size_t max_records)
     const size_t have = g_trace_count < kTraceCap ? g_trace_count : kTraceCap;
     const size_t n = out ? (max_records < have ? max_records : have) : have;
     if (out)
-        for (size_t k = 0; k < n; ++k) // oldest first, the newest n records
-            out[k] = g_trace[(g_trace_next + kTraceCap - n + k) % kTraceCap];
+        for (size_t k = 0; k < n; ++k) { // oldest first, the newest n records
+            const size_t slot = (g_trace_next + kTraceCap - n + k) % kTraceCap;
+            resolve(slot);
+            out[k] = g_trace[slot];
+        }
     return n;
 }
 
 void ccl_trace_clear(void)
 {
     std::lock_guard<std::mutex> lk(g_trace_mu);
+    for (size_t k = 0; k < kTraceCap; ++k)
+        release(g_trace_ev[k]);
     g_trace_next = 0;
     g_trace_count = 0;
 }

@@ -60,6 +60,49 @@ def test_trace_records_calls():
     assert recs[0]["launches"] == 1 and recs[1]["launches"] == 2 * (N - 1)
     assert all(r["status"] == 0 and r["nranks"] == N and r["count"] == K and r["dtype"] == 1 for r in recs)
     assert recs[0]["op"] == 1 and recs[1]["mode"] == 1 and recs[1]["seq"] == recs[0]["seq"] + 1
+    assert all(r["gpu_ns"] > 0 for r in recs)
+
+
+def test_trace_device_time_agrees_with_events_and_skips_capture():
+    """A traced call's device time is that of its work on its stream: it
+    agrees with CUDA events taken around the same call by the caller.  Calls
+    made during graph capture are traced untimed and the capture still
+    works."""
+    N, K = 8, 1 << 24  # 32 MiB per rank: about 80 us per AllReduce
+    bufs = [torch.zeros(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    ccl.ccl_allreduce(bufs, op="sum")  # warm-up
+    torch.cuda.synchronize()
+    ccl.ccl_trace_clear()
+    ccl.ccl_set_trace(True)
+    try:
+        times = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            # keep the GPU busy while the host enqueues, so that the caller's
+            # events time the call's work and not the host's enqueue gap
+            torch.cuda._sleep(2_000_000)
+            e0.record()
+            ccl.ccl_allreduce(bufs, op="sum")
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e6)
+        recs = ccl.ccl_trace_read()
+        assert len(recs) == 3
+        for r, t in zip(recs, times):
+            assert r["gpu_ns"] > 0
+            assert abs(r["gpu_ns"] - t) <= 0.25 * t + 10_000, (r["gpu_ns"], t)
+
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                ccl.ccl_allreduce(bufs, op="sum")
+        g.replay()
+        torch.cuda.synchronize()
+        rec = ccl.ccl_trace_read()[-1]
+        assert rec["collective"] == "allreduce" and rec["status"] == 0 and rec["gpu_ns"] == 0
+    finally:
+        ccl.ccl_set_trace(False)
 
 
 def test_automatic_checks_follow_each_collective():
