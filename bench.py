@@ -575,17 +575,20 @@ def run_row(args, name, local):
         return
 
     if name == "bucket":
-        N = 8
-        numels = W.llama_layer_numels(4)
+        N, L = 8, args.layers
+        numels = W.llama_layer_numels(L)
+        nbuckets = len(ccl.ccl_plan_buckets(numels, W.bucket_elems(25 * W.MiB, 2))) - 1
         grads = [[randn_bf16(n) for n in numels] for _ in range(N)]
         step = lambda: ccl.ccl_bucket_allreduce(grads, bucket_bytes=25 * W.MiB, op="sum", stream=stream)
         alg = 2 * N * sum(numels) * 2
         clocks.start()
         tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
         clk = clocks.stop()
-        print(json.dumps(line("Bucket-fused AllReduce HBM GB/s, N=8 bf16 4 Llama layers (1.62 GB/rank), 25 MiB "
-                              "buckets, 1 GB300", alg, per, launches, "bucket_reduce_kernel<bf16, SUM, 8>", "bf16",
-                              {"nranks": N, "tensors": len(numels), "buckets": 62}, {"clocks": clk}, total_ms=tot)))
+        print(json.dumps(line("Bucket-fused AllReduce HBM GB/s, N=8 bf16 %d Llama layer%s (%.2f GB/rank), 25 MiB "
+                              "buckets, 1 GB300" % (L, "s" if L != 1 else "", sum(numels) * 2 / 1e9), alg, per,
+                              launches, "bucket_reduce_kernel<bf16, SUM, 8>", "bf16",
+                              {"nranks": N, "layers": L, "tensors": len(numels), "buckets": nbuckets},
+                              {"clocks": clk}, total_ms=tot)))
         return
     raise SystemExit("unknown workload %s" % name)
 
@@ -600,6 +603,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=4,
+                    help="bucket workload: Llama layers per rank (4 is the benchmark; 1 is a profiling size)")
     ap.add_argument("--count", type=int, default=COUNT,
                     help="elements per rank (default: the 64Mi-element workload; smaller values are for profiling)")
     ap.add_argument("--workload", default="allreduce", choices=["allreduce"] + sorted(ROWS),
