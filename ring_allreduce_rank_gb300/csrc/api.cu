@@ -13,7 +13,17 @@
 namespace ccl {
 
 static std::atomic<unsigned long long> g_launches{0};
-void count_launches(unsigned long long n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+// Every kernel of a call is launched from the calling thread, so a per-thread
+// count gives a traced call its own launches even while other threads call in.
+static thread_local unsigned long long t_launches = 0;
+
+void count_launches(unsigned long long n)
+{
+    g_launches.fetch_add(n, std::memory_order_relaxed);
+    t_launches += n;
+}
+
+unsigned long long thread_launch_count() { return t_launches; }
 
 namespace {
 

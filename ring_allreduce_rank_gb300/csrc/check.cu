@@ -261,7 +261,7 @@ TraceScope::TraceScope(const char *name, int nranks, uint64_t count, int dtype, 
     rec_.dtype = dtype;
     rec_.op = op;
     rec_.mode = mode;
-    launches0_ = ccl_launch_count();
+    launches0_ = thread_launch_count();
     t0_ = std::chrono::steady_clock::now().time_since_epoch().count();
     // device time: an event before the call's work on its stream (none while
     // the stream is being captured, where events would become graph nodes)
@@ -287,7 +287,7 @@ void TraceScope::finish(int status)
     active_ = false;
     const long long t1 = std::chrono::steady_clock::now().time_since_epoch().count();
     rec_.status = status;
-    rec_.launches = (unsigned)(ccl_launch_count() - launches0_);
+    rec_.launches = (unsigned)(thread_launch_count() - launches0_);
     rec_.host_ns = (unsigned long long)(t1 - t0_);
     rec_.gpu_ns = 0;
     EventPair ev{ev0_, ev1_};
