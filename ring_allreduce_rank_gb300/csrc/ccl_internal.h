@@ -152,6 +152,8 @@ bool trace_enabled();
 
 // ------------------------------------------------------------------ bookkeeping
 // (count_launches is declared in fused.h)
+// kernels launched so far by the calling thread
+unsigned long long thread_launch_count();
 
 // Records one call in the trace ring buffer when tracing is on (CCL_TRACE or
 // ccl_set_trace): construct at entry, pass the status through done().  The

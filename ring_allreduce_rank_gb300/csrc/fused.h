@@ -39,7 +39,5 @@ cudaError_t launch_fused_reduce(int dt, int op, const void *const *send, void *c
                                 uint64_t count, int write_mode, int root, cudaStream_t stream);
 
 void count_launches(unsigned long long n);
-// kernels launched so far by the calling thread
-unsigned long long thread_launch_count();
 
 } // namespace ccl
