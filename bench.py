@@ -314,7 +314,8 @@ def run_row(args, name, local):
              "config": dict(config, workload=ROWS[name]),
              "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                           "frac": round(ach / peak, 4), "traffic": None, "algorithmic_bytes_per_step": alg,
-                          "peak_source": peak_src, "kernel": kernel},
+                          "peak_source": peak_src, "kernel": kernel,
+                          "achieved_median": round(alg / (statistics.median(per_ms) / 1e3) / 1e9, 1)},
              "cpu_baseline": None, "e2e": None, "gpu_launches": int(launches)}
         if extra:
             d.update(extra)
@@ -749,7 +750,12 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": ALG_BYTES, "peak_source": peak_src,
-                     "kernel": "fused_reduce_kernel<bf16, AVG, 8 ranks>"},
+                     "kernel": "fused_reduce_kernel<bf16, AVG, 8 ranks>",
+                     "achieved_median": round(ALG_BYTES / (statistics.median(per_launch_ms) / 1e3) / 1e9, 1),
+                     "launch_us": {"mean": round(statistics.mean(per_launch_ms) * 1e3, 2),
+                                   "median": round(statistics.median(per_launch_ms) * 1e3, 2),
+                                   "min": round(min(per_launch_ms) * 1e3, 2),
+                                   "max": round(max(per_launch_ms) * 1e3, 2)}},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(launches),
