@@ -187,8 +187,8 @@ def test_bf16_rne_against_torch_random(oracle_mod):
 
 
 def test_bf16_nan_rule(oracle_mod):
-    """NaN keeps its sign and top payload bits and becomes quiet (this build's
-    reading; the pages do not mention NaN)."""
+    """NaN keeps its sign and top payload bits and becomes quiet (the
+    library's reading; the pages do not mention NaN)."""
     assert oracle_mod.round_bf16(0x7fffffff) == 0x7fff
     assert oracle_mod.round_bf16(0x7fc00000) == 0x7fc0
     assert oracle_mod.round_bf16(0x7f800001) == 0x7fc0
@@ -517,7 +517,8 @@ def test_avg_premul_error_bound_against_fp64(oracle_mod, dtype, N, K):
 def test_allreduce_equals_reducescatter_then_allgather(oracle_mod, dtype, op, N, K):
     """AllReduce = AllGather o ReduceScatter (Collectives and sharded matmul,
     'where 2(N-1)/N comes from'; AllReduce survey, semantics and decomposition),
-    bit for bit under this build's placement reading."""
+    bit for bit when ReduceScatter gives rank r chunk r folded from rank r (the
+    library's placement reading)."""
     x = _inputs(dtype, N, K, seed=N + 7 * K)
     ar, _ = oracle_mod.ring_allreduce(x, op)
     rs = oracle_mod.reduce_scatter(x, op)
