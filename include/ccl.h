@@ -533,6 +533,22 @@ int ccl_version(void);
  * counter, for accounting; thread-safe). */
 unsigned long long ccl_launch_count(void);
 
+/* Per-rank traffic of the step-by-step mode (Lesson 3, reference solution:
+ * every rank counts what it sends, and an AllReduce moves 2(N-1)K/N elements
+ * per rank when N divides K).  sent[j] (HOST array of nranks entries) receives
+ * the elements rank j has sent in the ring steps that this host thread's
+ * step-mode calls launched since the last reset: the ReduceScatter and
+ * AllGather steps of AllReduce, ReduceScatter, AllGather, Reduce and bucket
+ * AllReduce, and ccl_reduce_scatter_step_static.  At ReduceScatter step s
+ * rank j sends chunk (j - s) mod N, at the AllReduce's AllGather step s chunk
+ * (j + 1 - s) mod N, and at the AllGather entry point's step s chunk
+ * (j - s) mod N (the lengths of the call's chunk partition).  Copies outside
+ * the ring (placing ReduceScatter's results, Broadcast's chain, the pairwise
+ * AllToAll) are not counted, nor is anything in fused mode.  reset != 0 zeroes
+ * the counters after reading.  Host only; CCL_ERR_INVALID_ARG for nranks
+ * outside [1, CCL_MAX_RANKS] or a NULL sent. */
+ccl_status_t ccl_step_sent(int nranks, unsigned long long *sent, int reset);
+
 /* Frees the library's cached device workspace on the current device (used by
  * step-mode ReduceScatter only).  Safe to call at any time when no call of this
  * library is in flight. */

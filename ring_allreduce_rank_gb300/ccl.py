@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
             L.ccl_trace_read.restype = sz
             L.ccl_trace_clear.argtypes = []
             L.ccl_trace_clear.restype = None
+            L.ccl_step_sent.argtypes = [i32, ctypes.POINTER(ctypes.c_ulonglong), i32]
+            L.ccl_step_sent.restype = ctypes.c_int
             L.ccl_get_config.argtypes = [ctypes.POINTER(Config)]
             L.ccl_get_config.restype = ctypes.c_int
             L.ccl_set_mode_override.argtypes = [i32]
@@ -381,6 +383,14 @@ def ccl_trace_read(max_records: int = 4096):
 
 def ccl_trace_clear() -> None:
     lib().ccl_trace_clear()
+
+
+def ccl_step_sent(nranks: int, reset: bool = True) -> list:
+    """Elements each rank sent in the ring steps of this thread's step-mode
+    calls since the last reset."""
+    buf = (ctypes.c_ulonglong * nranks)()
+    _check(lib().ccl_step_sent(int(nranks), buf, 1 if reset else 0), "ccl_step_sent")
+    return [int(v) for v in buf]
 
 
 def ccl_get_config() -> dict:

@@ -166,15 +166,50 @@ static cudaError_t launch_step_dt(int op, int kind, int s, void *const *bufs, in
     return cudaErrorInvalidValue;
 }
 
+// Elements each rank has sent in ring steps launched by this thread (Lesson 3's
+// per-rank traffic counter): at ReduceScatter step s rank j sends chunk
+// (j - s) mod N, at AllGather step s chunk (j + 1 - s) mod N, and in the
+// AllGather entry point's steps (which start from chunk j at rank j) chunk
+// (j - s) mod N.
+static thread_local std::vector<unsigned long long> t_sent;
+
+static void count_sent(int kind, int s, int nranks, uint64_t count)
+{
+    if (kind == STEP_SCALE)
+        return;
+    if (t_sent.size() < (size_t)nranks)
+        t_sent.resize((size_t)nranks, 0ull);
+    const uint64_t q = count / (uint64_t)nranks, rem = count % (uint64_t)nranks;
+    const int shift = kind == STEP_AG ? 1 - s : -s;
+    for (int j = 0; j < nranks; ++j) {
+        const int c = ((j + shift) % nranks + nranks) % nranks;
+        t_sent[(size_t)j] += q + ((uint64_t)c < rem ? 1 : 0);
+    }
+}
+
 cudaError_t launch_ring_step(int dt, int op, int kind, int s, void *const *bufs, int nranks, uint64_t count,
                              cudaStream_t stream)
 {
     // copies do not depend on the op: share one instantiation
     if (kind == STEP_AG || kind == STEP_AG_API)
         op = OP_SUM;
-    if (dt == DT_FP32)
-        return launch_step_dt<DT_FP32>(op, kind, s, bufs, nranks, count, stream);
-    return launch_step_dt<DT_BF16>(op, kind, s, bufs, nranks, count, stream);
+    const cudaError_t e = dt == DT_FP32 ? launch_step_dt<DT_FP32>(op, kind, s, bufs, nranks, count, stream)
+                                        : launch_step_dt<DT_BF16>(op, kind, s, bufs, nranks, count, stream);
+    if (e == cudaSuccess)
+        count_sent(kind, s, nranks, count);
+    return e;
 }
 
 } // namespace ccl
+
+extern "C" ccl_status_t ccl_step_sent(int nranks, unsigned long long *sent, int reset)
+{
+    using ccl::t_sent;
+    if (nranks < 1 || nranks > CCL_MAX_RANKS || !sent)
+        return CCL_ERR_INVALID_ARG;
+    for (int j = 0; j < nranks; ++j)
+        sent[j] = (size_t)j < t_sent.size() ? t_sent[(size_t)j] : 0ull;
+    if (reset)
+        t_sent.assign(t_sent.size(), 0ull);
+    return CCL_OK;
+}

@@ -157,3 +157,14 @@ def test_invalid_arguments_and_overlaps_rejected(L):
                          capture_output=True, text=True, timeout=300)
     assert res.returncode == 0, res.stdout + res.stderr
     assert "validation cases ok" in res.stdout
+
+
+def test_step_sent_counter_without_a_device(L):
+    """The step-mode traffic counter is host state: zero before any step-mode
+    launch, and its arguments are validated."""
+    assert ccl.ccl_step_sent(8) == [0] * 8
+    assert ccl.ccl_step_sent(C.MAX_RANKS, reset=False) == [0] * C.MAX_RANKS
+    buf = (ctypes.c_ulonglong * 1)()
+    assert L.ccl_step_sent(0, buf, 1) == 1
+    assert L.ccl_step_sent(C.MAX_RANKS + 1, buf, 1) == 1
+    assert L.ccl_step_sent(4, None, 1) == 1
