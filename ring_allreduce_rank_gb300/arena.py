@@ -38,6 +38,15 @@ class RankArena:
     def guards_intact(self) -> bool:
         return all(bool((self.guard(r) == POISON).all()) for r in range(self.nranks))
 
+    def first_damage(self):
+        """(rank, byte offset into that rank's guard band) of the first guard
+        byte that no longer holds the poison value, or None."""
+        for r in range(self.nranks):
+            bad = torch.nonzero(self.guard(r) != POISON)
+            if bad.numel():
+                return r, int(bad[0, 0])
+        return None
+
     def load(self, host_rows) -> None:
         """Copy host rows (one per rank; numpy or torch, matching bytes) into the arena."""
         for r in range(self.nranks):
