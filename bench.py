@@ -479,7 +479,7 @@ def run_row(args, name, local):
         # threshold, then gradients and residuals read and written once
         alg = N * K * (2 + 4) + N * K * (2 + 4 + 4 + 2)
         print(json.dumps(line("Top-k AllReduce (1%% kept + error feedback) HBM GB/s of the %d-byte minimum, N=8 bf16 "
-                              "128 MB/rank, 1 GB300" % alg, alg, per, launches,
+                              "%d MB/rank, 1 GB300" % (alg, K * 2 // 2**20), alg, per, launches,
                               "whole step: topk_init, topk_top_kernel + scan, topk_low_kernel + 2 scans, "
                               "compressed_pipe_kernel<bf16, 4, TOPK>", "bf16",
                               {"nranks": N, "count": K, "k": kk}, {"clocks": clk}, total_ms=tot)))
