@@ -1,7 +1,8 @@
 """The boundary is a C ABI: include/ccl.h compiles as strict C and C++, and a
 plain C program (tests/c_abi_example.c) builds against it and libccl.so with
 gcc alone -- no Python, no torch -- and, on a GPU, runs collectives through it
-with exact integer results."""
+with exact integer results.  A second program (tests/c_abi_host_example.c)
+uses the host-only entry points from C on a machine without a GPU."""
 import os
 import shutil
 import subprocess
@@ -11,6 +12,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 INCLUDE = os.path.join(ROOT, "include")
 EXAMPLE = os.path.join(ROOT, "tests", "c_abi_example.c")
+HOST_EXAMPLE = os.path.join(ROOT, "tests", "c_abi_host_example.c")
 CUDA = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 
 
@@ -31,15 +33,28 @@ def test_header_compiles_strictly(lang, std, tmp_path):
                     "-isystem", _cuda_include(), str(src)], check=True)
 
 
-def _build_example(out):
+def _build_example(out, src=EXAMPLE):
     from ring_allreduce_rank_gb300 import build
     lib = build.build()
     libdir = os.path.dirname(lib)
     cudalib = os.path.join(CUDA, "lib64")
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-O1", "-I", INCLUDE, "-isystem", _cuda_include(),
-                    EXAMPLE, "-o", out, "-L", libdir, "-lccl", "-Wl,-rpath," + libdir, "-L", cudalib, "-lcudart",
+                    src, "-o", out, "-L", libdir, "-lccl", "-Wl,-rpath," + libdir, "-L", cudalib, "-lcudart",
                     "-Wl,-rpath," + cudalib], check=True)
     return out
+
+
+def test_host_example_runs_without_a_gpu(tmp_path):
+    """The planner, the settings (ccl_config_t read from C), the step-mode
+    traffic counter and argument validation, from plain C with no device."""
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    exe = _build_example(str(tmp_path / "c_abi_host_example"), HOST_EXAMPLE)
+    env = {k: v for k, v in os.environ.items() if not k.startswith("CCL_")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    res = subprocess.run([exe], capture_output=True, text=True, timeout=120, env=env)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "c abi host ok" in res.stdout
 
 
 def test_example_builds_with_gcc_alone(tmp_path):
