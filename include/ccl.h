@@ -61,13 +61,14 @@
  *     captured; a graph replays them on the pointers it was captured with.
  *     ccl_allreduce_compressed sets up its kernel (shared-memory opt-in) on
  *     its first call on a device: make that call before capturing.  Step
- *     mode is not capturable: step-mode ReduceScatter and bucket AllReduce
- *     use a library-cached device workspace that a first or larger call
- *     allocates (and frees the old one).  ccl_allreduce_host refuses capture.
+ *     mode is not capturable: step-mode ReduceScatter, Reduce and bucket
+ *     AllReduce use a library-cached device workspace that a first or larger
+ *     call allocates (and frees the old one).  ccl_allreduce_host refuses
+ *     capture.
  *   - That step-mode workspace is one per device, shared by every call:
- *     step-mode ReduceScatter or bucket AllReduce calls whose work overlaps
- *     on the GPU (different streams, different host threads) race on it and
- *     must be serialised.  Fused calls share nothing.
+ *     step-mode ReduceScatter, Reduce or bucket AllReduce calls whose work
+ *     overlaps on the GPU (different streams, different host threads) race on
+ *     it and must be serialised.  Fused calls share nothing.
  *   - The environment variable CCL_MODE (or ccl_set_mode_override) can force
  *     one mode on every call that takes a mode argument; a forced step mode
  *     brings the step-mode rules above with it.  See "Settings" below.
@@ -550,8 +551,8 @@ unsigned long long ccl_launch_count(void);
 ccl_status_t ccl_step_sent(int nranks, unsigned long long *sent, int reset);
 
 /* Frees the library's cached device workspace on the current device (used by
- * step-mode ReduceScatter only).  Safe to call at any time when no call of this
- * library is in flight. */
+ * step-mode ReduceScatter, Reduce and bucket AllReduce).  Safe to call at any
+ * time when no call of this library is in flight. */
 ccl_status_t ccl_finalize(void);
 
 #ifdef __cplusplus
