@@ -1,0 +1,150 @@
+"""Tiny pure-Python ring AllReduce -- TEST INFRASTRUCTURE ONLY, small cases.
+
+A second statement of the ring AllReduce, in Python loops over Python
+integers (bit patterns), written independently of ``ring_oracle.c``.  The tests
+compare the two bit for bit on small inputs and check this one against the
+pages' worked examples.  Like the rest of ``oracle/`` it may be used only by
+``tests/``.
+
+The schedule (Collectives and sharded matmul, slides "ring ReduceScatter" and
+"ring AllGather"; Lesson 3, reference solution, which snapshots every send of a
+step before any receive is applied):
+
+  ReduceScatter step s = 0..N-2: rank i sends its current chunk (i-s) mod N to
+  rank i+1; rank i combines the chunk (i-1-s) mod N arriving from rank i-1
+  into its own copy (local first, then incoming).
+  AllGather step s = 0..N-2: rank i sends chunk (i+1-s) mod N; rank i stores
+  the chunk (i-s) mod N arriving from rank i-1.
+
+Chunk c of K elements holds K // N + (c < K % N) elements.  Each combination
+is one IEEE binary32 operation rounded to nearest-even, then a round to the
+buffer type.  A binary32 sum, product or quotient of two binary32 values is
+taken here in binary64 and rounded once to binary32; 53 >= 2 * 24 + 2, so that
+double rounding gives the correctly rounded binary32 result.  Readings where
+the pages are silent: a NaN result is the quiet NaN 0x7FFFFFFF; MAX and MIN
+return NaN if either side is NaN, else the larger (smaller) value, with +0
+beating -0 in MAX and -0 beating +0 in MIN; AVG divides the finished chunk once
+by N at the rank that holds it; the pre-multiplied AVG scales every
+contribution by the binary32 reciprocal of N first, rounds it to the buffer
+type, and sums.
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+import numpy as np
+
+NAN32 = 0x7FFFFFFF
+
+
+def f32_value(bits: int) -> float:
+    return struct.unpack("<f", struct.pack("<I", bits & 0xFFFFFFFF))[0]
+
+
+def f32_bits(x: float) -> int:
+    """Round a binary64 value to binary32 (nearest-even, overflow to infinity)."""
+    if math.isnan(x):
+        return NAN32
+    if math.isinf(x):
+        return 0x7F800000 if x > 0 else 0xFF800000
+    with np.errstate(over="ignore"):
+        y = np.float32(x)  # IEEE conversion, round to nearest-even
+    return int(np.array([y], dtype=np.float32).view(np.uint32)[0])
+
+
+def bf16_from_f32(bits: int) -> int:
+    """Round a binary32 bit pattern to bfloat16, nearest-even; a NaN keeps its
+    sign and top payload bits and becomes quiet."""
+    if (bits & 0x7F800000) == 0x7F800000 and (bits & 0x007FFFFF):
+        return ((bits >> 16) | 0x0040) & 0xFFFF
+    upper, lower = bits >> 16, bits & 0xFFFF
+    if lower > 0x8000 or (lower == 0x8000 and (upper & 1)):
+        upper += 1
+    return upper & 0xFFFF
+
+
+def _is_nan(bits: int) -> bool:
+    return (bits & 0x7F800000) == 0x7F800000 and (bits & 0x007FFFFF) != 0
+
+
+def _binop(a: int, b: int, op: str) -> int:
+    """One binary32 operation on binary32 bit patterns."""
+    if op in ("max", "min"):
+        if _is_nan(a) or _is_nan(b):
+            return NAN32
+        x, y = f32_value(a), f32_value(b)
+        if x == y:  # equal values: only +0 / -0 can differ in bits
+            return (a & b) if op == "max" else (a | b)
+        return a if (x > y) == (op == "max") else b
+    x, y = f32_value(a), f32_value(b)
+    r = x * y if op == "prod" else x + y
+    return f32_bits(r)
+
+
+def _canon(bits: int) -> int:
+    return NAN32 if _is_nan(bits) else bits
+
+
+class _Type:
+    def __init__(self, bf16: bool):
+        self.bf16 = bf16
+
+    def widen(self, v: int) -> int:
+        return (v << 16) if self.bf16 else v
+
+    def narrow(self, bits: int) -> int:
+        return bf16_from_f32(bits) if self.bf16 else bits
+
+
+def partition(K: int, N: int):
+    lens = [K // N + (1 if c < K % N else 0) for c in range(N)]
+    offs = [sum(lens[:c]) for c in range(N)]
+    return offs, lens
+
+
+def ring_allreduce(bufs, op: str = "sum"):
+    """bufs: N equal-length numpy arrays (float32, or uint16 bf16 bit patterns).
+    Returns (outputs as arrays of the same kind, elements sent per rank)."""
+    arrs = [np.ascontiguousarray(b) for b in bufs]
+    bf16 = arrs[0].dtype == np.uint16
+    T = _Type(bf16)
+    N, K = len(arrs), arrs[0].size
+    buf = [[int(v) for v in (a if bf16 else a.view(np.uint32))] for a in arrs]
+    offs, lens = partition(K, N)
+    sent = [0] * N
+    ring_op = "sum" if op in ("avg", "avg_premul") else op
+
+    if op == "avg_premul":  # every contribution scaled by rn(1/N) and rounded to the type
+        inv = f32_value(f32_bits(1.0 / N))
+        buf = [[T.narrow(_canon(f32_bits(f32_value(T.widen(v)) * inv))) for v in row] for row in buf]
+
+    def chunk(c):
+        return range(offs[c], offs[c] + lens[c])
+
+    for s in range(N - 1):  # ReduceScatter phase
+        msgs = [[buf[i][e] for e in chunk((i - s) % N)] for i in range(N)]
+        for i in range(N):
+            c = (i - 1 - s) % N
+            incoming = msgs[(i - 1) % N]
+            for k, e in enumerate(chunk(c)):
+                buf[i][e] = T.narrow(_canon(_binop(T.widen(buf[i][e]), T.widen(incoming[k]), ring_op)))
+            sent[(i - 1) % N] += lens[c]
+    if op == "avg":  # once, at the rank holding the finished chunk (i+1) mod N
+        for i in range(N):
+            for e in chunk((i + 1) % N):
+                buf[i][e] = T.narrow(_canon(f32_bits(f32_value(T.widen(buf[i][e])) / N)))
+    for s in range(N - 1):  # AllGather phase
+        msgs = [[buf[i][e] for e in chunk((i + 1 - s) % N)] for i in range(N)]
+        for i in range(N):
+            c = (i - s) % N
+            incoming = msgs[(i - 1) % N]
+            for k, e in enumerate(chunk(c)):
+                buf[i][e] = incoming[k]
+            sent[(i - 1) % N] += lens[c]
+
+    if bf16:
+        outs = [np.array(row, dtype=np.uint16) for row in buf]
+    else:
+        outs = [np.array(row, dtype=np.uint32).view(np.float32) for row in buf]
+    return outs, sent
