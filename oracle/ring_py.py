@@ -103,9 +103,23 @@ def partition(K: int, N: int):
     return offs, lens
 
 
-def ring_allreduce(bufs, op: str = "sum"):
-    """bufs: N equal-length numpy arrays (float32, or uint16 bf16 bit patterns).
-    Returns (outputs as arrays of the same kind, elements sent per rank)."""
+def reduce_scatter(bufs, op: str = "sum"):
+    """ReduceScatter as the ring computes it: the ReduceScatter phase leaves
+    chunk c finished at rank c-1, which hands it to rank c.  Returns one
+    array per rank (chunk r for rank r)."""
+    buf, T, offs, lens, _ = _reduce_scatter_phase(bufs, op)
+    N = len(buf)
+    out = []
+    for r in range(N):
+        row = buf[(r - 1) % N][offs[r]:offs[r] + lens[r]]
+        out.append(np.array(row, dtype=np.uint16) if T.bf16 else np.array(row, dtype=np.uint32).view(np.float32))
+    return out
+
+
+def _reduce_scatter_phase(bufs, op):
+    """The N-1 ReduceScatter steps (and AVG's one division at each holder) on
+    copies of bufs.  Returns (buffers as bit patterns, type, offsets, lengths,
+    elements sent per rank)."""
     arrs = [np.ascontiguousarray(b) for b in bufs]
     bf16 = arrs[0].dtype == np.uint16
     T = _Type(bf16)
@@ -122,7 +136,7 @@ def ring_allreduce(bufs, op: str = "sum"):
     def chunk(c):
         return range(offs[c], offs[c] + lens[c])
 
-    for s in range(N - 1):  # ReduceScatter phase
+    for s in range(N - 1):
         msgs = [[buf[i][e] for e in chunk((i - s) % N)] for i in range(N)]
         for i in range(N):
             c = (i - 1 - s) % N
@@ -134,6 +148,19 @@ def ring_allreduce(bufs, op: str = "sum"):
         for i in range(N):
             for e in chunk((i + 1) % N):
                 buf[i][e] = T.narrow(_canon(f32_bits(f32_value(T.widen(buf[i][e])) / N)))
+    return buf, T, offs, lens, sent
+
+
+def ring_allreduce(bufs, op: str = "sum"):
+    """bufs: N equal-length numpy arrays (float32, or uint16 bf16 bit patterns).
+    Returns (outputs as arrays of the same kind, elements sent per rank)."""
+    buf, T, offs, lens, sent = _reduce_scatter_phase(bufs, op)
+    N = len(buf)
+    bf16 = T.bf16
+
+    def chunk(c):
+        return range(offs[c], offs[c] + lens[c])
+
     for s in range(N - 1):  # AllGather phase
         msgs = [[buf[i][e] for e in chunk((i + 1 - s) % N)] for i in range(N)]
         for i in range(N):

@@ -51,3 +51,23 @@ def test_bf16_rounding_agrees_with_the_c_oracle_on_deciding_patterns(oracle_mod)
     want = [oracle_mod.round_bf16(int(p)) for p in pats]
     got = [ring_py.bf16_from_f32(int(p)) for p in pats]
     assert got == want
+
+
+def test_printed_reduce_scatter_example():
+    case = [c for c in json.load(open(GOLD))["cases"] if c["collective"] == "reduce_scatter"][0]
+    ins = [np.asarray(r, dtype=np.float32) for r in case["inputs"]]
+    out = ring_py.reduce_scatter(ins, case["op"])
+    for r, want in enumerate(case["expected"]):
+        np.testing.assert_array_equal(out[r], np.asarray(want, dtype=np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "min", "prod", "avg_premul"])
+@pytest.mark.parametrize("N,K", [(1, 5), (3, 17), (4, 3), (6, 50)])
+def test_reduce_scatter_agrees_with_the_c_oracle(oracle_mod, dtype, op, N, K):
+    seed = 2000 + 13 * N + K
+    x = list(W.mixed_bf16(N, K, seed_base=seed) if dtype == "bf16" else W.mixed_fp32(N, K, seed_base=seed))
+    want = oracle_mod.reduce_scatter(x, op)
+    got = ring_py.reduce_scatter(x, op)
+    for r in range(N):
+        np.testing.assert_array_equal(_bits(got[r]), _bits(want[r]), err_msg="rank %d" % r)
