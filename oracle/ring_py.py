@@ -175,3 +175,82 @@ def ring_allreduce(bufs, op: str = "sum"):
     else:
         outs = [np.array(row, dtype=np.uint32).view(np.float32) for row in buf]
     return outs, sent
+
+
+# ------------------------------------------------------------------ compressed AllReduce with error feedback
+# (Collective Communication: "Blockwise quantization for gradient
+# communication", the greedy 1-bit compressor of Tables 3 and 4, "Top-k
+# sparsification", and error feedback, Definition 1.4: e_{t+1} = g_t + e_t - v_t.)
+# Each rank compresses u = g + e (binary32) to the transmitted v and keeps
+# e' = u - v; the v's are AllReduced by the ring above in binary32 (SUM, or AVG
+# dividing once by N) and the result is rounded once to the gradient type.
+# numpy binary32 array operations are single IEEE operations (round to
+# nearest-even, no contraction); NaN results are made the quiet NaN 0x7FFFFFFF.
+
+def _canon_f32(a: np.ndarray) -> np.ndarray:
+    a = np.asarray(a, dtype=np.float32).copy()
+    a.view(np.uint32)[np.isnan(a)] = NAN32
+    return a
+
+
+def _int8_block(u: np.ndarray, block: int) -> np.ndarray:
+    """v for one rank: per block of `block` elements s = max|u| / 127 (NaN if
+    the block holds a NaN), q = u / s rounded to an integer with ties to even
+    (0 when s = 0), v = q * s."""
+    v = np.empty_like(u)
+    with np.errstate(all="ignore"):
+        for b0 in range(0, u.size, block):
+            blk = u[b0:b0 + block]
+            if np.isnan(blk).any():
+                s = np.float32(np.nan)
+            else:
+                s = _canon_f32(np.abs(blk).max(initial=np.float32(0)) / np.float32(127))[()]
+            if s > 0:
+                q = np.rint(_canon_f32(blk / s))  # IEEE roundToIntegralTiesToEven
+            elif s == 0:
+                q = np.zeros_like(blk)
+            else:  # NaN scale
+                q = np.full_like(blk, s)
+            v[b0:b0 + block] = _canon_f32(_canon_f32(q) * s)
+    return v
+
+
+def _top_k(u: np.ndarray, k: int) -> np.ndarray:
+    """v = u where the magnitude key (the bit pattern of |u|, so NaN ranks
+    above every number) reaches the k-th largest key, else 0."""
+    keys = u.view(np.uint32) & np.uint32(0x7FFFFFFF)
+    if k <= 0 or u.size == 0:
+        return np.zeros_like(u)
+    tau = np.sort(keys)[::-1][min(k, u.size) - 1]
+    return np.where(keys >= tau, u, np.float32(0)).astype(np.float32)
+
+
+def allreduce_compressed(grads, residuals, op: str = "sum", comp: str = "int8_block", block: int = 128,
+                         threshold: float = 0.5, k: int = 0):
+    """One step.  grads: N arrays (float32, or uint16 bf16 patterns); residuals:
+    N float32 arrays.  Returns (new grads, new residuals); inputs untouched."""
+    if op not in ("sum", "avg"):
+        raise ValueError("compressed AllReduce takes SUM or AVG")
+    bf16 = np.asarray(grads[0]).dtype == np.uint16
+    sent, res = [], []
+    with np.errstate(all="ignore"):
+        for g, e in zip(grads, residuals):
+            g32 = (np.asarray(g, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32) if bf16 \
+                else np.asarray(g, dtype=np.float32)
+            u = _canon_f32(g32 + np.asarray(e, dtype=np.float32))
+            if comp == "int8_block":
+                v = _int8_block(u, block)
+            elif comp == "threshold":
+                v = np.where(u >= np.float32(threshold), np.float32(1), np.float32(0)).astype(np.float32)
+            elif comp == "topk":
+                v = _top_k(u, k)
+            else:
+                raise ValueError(comp)
+            res.append(_canon_f32(u - v))
+            sent.append(v)
+    total, _ = ring_allreduce(sent, op)
+    if bf16:
+        out = [np.array([bf16_from_f32(int(b)) for b in t.view(np.uint32)], dtype=np.uint16) for t in total]
+    else:
+        out = [t.copy() for t in total]
+    return out, res

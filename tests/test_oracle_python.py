@@ -1,5 +1,6 @@
 """The pure-Python ring (oracle/ring_py.py) against the C oracle and the pages
-(no GPU).  Two independent statements of the same schedule, in two languages,
+(no GPU): AllReduce, ReduceScatter and the compressed AllReduce with error
+feedback.  Two independent statements of the same schedule, in two languages,
 must agree bit for bit -- results and the elements each rank sends -- on small
 inputs that mix signed zeros, subnormals, infinities and NaNs into values of
 widely varying magnitude, for every operator and both buffer types; and the
@@ -71,3 +72,25 @@ def test_reduce_scatter_agrees_with_the_c_oracle(oracle_mod, dtype, op, N, K):
     got = ring_py.reduce_scatter(x, op)
     for r in range(N):
         np.testing.assert_array_equal(_bits(got[r]), _bits(want[r]), err_msg="rank %d" % r)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "avg"])
+@pytest.mark.parametrize("comp,block,k", [("int8_block", 128, 0), ("int8_block", 7, 0), ("threshold", 0, 0),
+                                          ("topk", 0, 1), ("topk", 0, 13), ("topk", 0, 0), ("topk", 0, 10_000)])
+@pytest.mark.parametrize("N,K", [(1, 40), (3, 300), (5, 129)])
+def test_compressed_allreduce_agrees_with_the_c_oracle(oracle_mod, dtype, op, comp, block, k, N, K):
+    seed = 3000 + 7 * N + K
+    g = list(W.mixed_bf16(N, K, seed_base=seed) if dtype == "bf16" else W.mixed_fp32(N, K, seed_base=seed))
+    with np.errstate(invalid="ignore"):
+        e = list(W.mixed_fp32(N, K, seed_base=seed + 100, special_frac=0.01) * np.float32(1e-3))
+    # two steps, the second carrying the first's residuals (error feedback)
+    for _ in range(2):
+        want_g, want_e = oracle_mod.allreduce_compressed(g, e, op=op, comp=comp, block=block or 128,
+                                                         threshold=0.5, k=k)
+        got_g, got_e = ring_py.allreduce_compressed(g, e, op=op, comp=comp, block=block or 128,
+                                                    threshold=0.5, k=k)
+        for r in range(N):
+            np.testing.assert_array_equal(_bits(got_g[r]), _bits(want_g[r]), err_msg="grads rank %d" % r)
+            np.testing.assert_array_equal(_bits(got_e[r]), _bits(want_e[r]), err_msg="residual rank %d" % r)
+        g, e = want_g, want_e
