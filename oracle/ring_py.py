@@ -1,4 +1,4 @@
-"""Tiny pure-Python ring AllReduce -- TEST INFRASTRUCTURE ONLY, small cases.
+"""Tiny pure-Python ring collectives -- TEST INFRASTRUCTURE ONLY, small cases.
 
 A second statement of the ring AllReduce, in Python loops over Python
 integers (bit patterns), written independently of ``ring_oracle.c``.  The tests
@@ -254,3 +254,140 @@ def allreduce_compressed(grads, residuals, op: str = "sum", comp: str = "int8_bl
     else:
         out = [t.copy() for t in total]
     return out, res
+
+
+# ------------------------------------------------------------------ other schedules, step by step
+# The fold orders of the other AllReduce schedules the pages describe, each
+# simulated step by step on whole buffers (the C oracle has its own step
+# simulations and per-element closed forms; this is a third statement).
+
+def _load(bufs):
+    arrs = [np.ascontiguousarray(b) for b in bufs]
+    bf16 = arrs[0].dtype == np.uint16
+    return [[int(v) for v in (a if bf16 else a.view(np.uint32))] for a in arrs], _Type(bf16)
+
+
+def _store(buf, T):
+    if T.bf16:
+        return [np.array(row, dtype=np.uint16) for row in buf]
+    return [np.array(row, dtype=np.uint32).view(np.float32) for row in buf]
+
+
+def _combine(T, a, b, op):
+    return T.narrow(_canon(_binop(T.widen(a), T.widen(b), op)))
+
+
+def _divide(T, a, n):
+    return T.narrow(_canon(f32_bits(f32_value(T.widen(a)) / n)))
+
+
+def allreduce_halving_doubling(bufs, op: str = "sum"):
+    """Recursive halving then doubling (Collective Communication, "Recursive
+    halving-doubling"; distance doubling: round k pairs rank v with v XOR 2^k,
+    and the rank whose bit k is 0 keeps the lower half of its current range,
+    rounded up).  N not a power of two: with P the largest power of two <= N
+    and r = N - P, rank 2v+1 first adds rank 2v's buffer (v < r) and stands in
+    for both; the virtual ranks are 2v+1 (v < r) and v + r (v >= r); rank 2v
+    receives the result at the end.  AVG divides once by N."""
+    if op not in ("sum", "avg", "max", "min", "prod"):
+        raise ValueError(op)
+    buf, T = _load(bufs)
+    N, K = len(buf), len(buf[0])
+    sop = "sum" if op == "avg" else op
+    P = 1
+    while P * 2 <= N:
+        P *= 2
+    r = N - P
+    for v in range(r):
+        buf[2 * v + 1] = [_combine(T, a, b, sop) for a, b in zip(buf[2 * v + 1], buf[2 * v])]
+    real = [2 * v + 1 if v < r else v + r for v in range(P)]
+    lo, hi = [0] * P, [K] * P
+    rounds = P.bit_length() - 1
+    for k in range(rounds):  # halving: exchange and combine half of the current range
+        snap = [list(buf[real[v]]) for v in range(P)]
+        for v in range(P):
+            p = v ^ (1 << k)
+            mid = lo[v] + (hi[v] - lo[v] + 1) // 2
+            keep = (lo[v], mid) if not v & (1 << k) else (mid, hi[v])
+            row = buf[real[v]]
+            for e in range(*keep):
+                row[e] = _combine(T, row[e], snap[p][e], sop)
+            lo[v], hi[v] = keep
+    if op == "avg":
+        for v in range(P):
+            row = buf[real[v]]
+            for e in range(lo[v], hi[v]):
+                row[e] = _divide(T, row[e], N)
+    for k in reversed(range(rounds)):  # doubling: exchange the finished ranges
+        snap = [list(buf[real[v]]) for v in range(P)]
+        rng = list(zip(lo, hi))
+        for v in range(P):
+            p = v ^ (1 << k)
+            row = buf[real[v]]
+            for e in range(*rng[p]):
+                row[e] = snap[p][e]
+            lo[v], hi[v] = min(rng[v][0], rng[p][0]), max(rng[v][1], rng[p][1])
+    for v in range(r):
+        buf[2 * v] = list(buf[2 * v + 1])
+    return _store(buf, T)
+
+
+def allreduce_binomial_tree(bufs, op: str = "sum"):
+    """Reduce up a binomial tree rooted at rank 0, then broadcast down
+    (Collective Communication, "Tree AllReduce"): at level k every rank i that
+    is a multiple of 2^(k+1) adds rank i + 2^k's buffer, if that rank exists.
+    AVG divides once by N at the root."""
+    if op not in ("sum", "avg", "max", "min", "prod"):
+        raise ValueError(op)
+    buf, T = _load(bufs)
+    N = len(buf)
+    sop = "sum" if op == "avg" else op
+    step = 1
+    while step < N:
+        for i in range(0, N, 2 * step):
+            if i + step < N:
+                buf[i] = [_combine(T, a, b, sop) for a, b in zip(buf[i], buf[i + step])]
+        step *= 2
+    if op == "avg":
+        buf[0] = [_divide(T, a, N) for a in buf[0]]
+    return _store([list(buf[0]) for _ in range(N)], T)
+
+
+def allreduce_hierarchical(bufs, L: int, op: str = "sum"):
+    """Two-level AllReduce (AllReduce survey, two-level table): groups of L
+    consecutive ranks; a ring ReduceScatter inside every group over L chunks
+    (chunk c finished at local rank c-1); a ring AllReduce of chunk c across
+    the groups' holders, chunk c cut into G = N / L sub-chunks; then a ring
+    AllGather inside every group.  AVG divides once by N."""
+    if op not in ("sum", "avg", "max", "min", "prod"):
+        raise ValueError(op)
+    arrs = [np.ascontiguousarray(b) for b in bufs]
+    N, K = len(arrs), arrs[0].size
+    if L < 1 or N % L:
+        raise ValueError("group size must divide the rank count")
+    G = N // L
+    sop = "sum" if op == "avg" else op
+    offs, lens = partition(K, L)
+    T = _Type(arrs[0].dtype == np.uint16)
+    out = [None] * N
+    # 1. ring ReduceScatter inside every group
+    grp = []
+    for g in range(G):
+        b, _, _, _, _ = _reduce_scatter_phase(arrs[g * L:(g + 1) * L], sop)
+        grp.append(b)
+    result = [0] * K
+    # 2. ring AllReduce of every chunk across the groups' holders
+    for c in range(L):
+        holder = (c - 1) % L
+        rows = [grp[g][holder][offs[c]:offs[c] + lens[c]] for g in range(G)]
+        rows = [np.array(rw, dtype=np.uint16) if T.bf16 else np.array(rw, dtype=np.uint32).view(np.float32)
+                for rw in rows]
+        red, _ = ring_allreduce(rows, sop)
+        vals = [int(v) for v in (red[0] if T.bf16 else red[0].view(np.uint32))]
+        if op == "avg":
+            vals = [_divide(T, a, N) for a in vals]
+        result[offs[c]:offs[c] + lens[c]] = vals
+    # 3. ring AllGather inside every group: every rank receives every chunk
+    for i in range(N):
+        out[i] = list(result)
+    return _store(out, T)

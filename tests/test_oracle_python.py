@@ -94,3 +94,39 @@ def test_compressed_allreduce_agrees_with_the_c_oracle(oracle_mod, dtype, op, co
             np.testing.assert_array_equal(_bits(got_g[r]), _bits(want_g[r]), err_msg="grads rank %d" % r)
             np.testing.assert_array_equal(_bits(got_e[r]), _bits(want_e[r]), err_msg="residual rank %d" % r)
         g, e = want_g, want_e
+
+
+ORDERS = {"halving_doubling": lambda x, op, L: ring_py.allreduce_halving_doubling(x, op),
+          "tree": lambda x, op, L: ring_py.allreduce_binomial_tree(x, op),
+          "hierarchical": lambda x, op, L: ring_py.allreduce_hierarchical(x, L, op)}
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "min", "prod"])
+@pytest.mark.parametrize("algo,N,L", [("halving_doubling", 1, 0), ("halving_doubling", 2, 0),
+                                      ("halving_doubling", 5, 0), ("halving_doubling", 6, 0),
+                                      ("halving_doubling", 8, 0), ("halving_doubling", 11, 0),
+                                      ("tree", 3, 0), ("tree", 7, 0), ("tree", 8, 0), ("tree", 13, 0),
+                                      ("hierarchical", 6, 3), ("hierarchical", 6, 2), ("hierarchical", 8, 4),
+                                      ("hierarchical", 9, 3), ("hierarchical", 4, 1), ("hierarchical", 4, 4)])
+@pytest.mark.parametrize("K", [1, 29])
+def test_other_orders_agree_with_the_c_oracle(oracle_mod, dtype, op, algo, N, L, K):
+    seed = 4000 + 31 * N + K + L
+    x = list(W.mixed_bf16(N, K, seed_base=seed) if dtype == "bf16" else W.mixed_fp32(N, K, seed_base=seed))
+    want = oracle_mod.allreduce_algo(x, algo, op, group=L)
+    got = ORDERS[algo](x, op, L)
+    for r in range(N):
+        np.testing.assert_array_equal(_bits(got[r]), _bits(want[r]), err_msg="%s rank %d" % (algo, r))
+
+
+@pytest.mark.parametrize("case", json.load(open(os.path.join(os.path.dirname(__file__), "golden", "order_cases.json")))
+                         ["cases"], ids=lambda c: c["name"])
+def test_other_orders_reproduce_the_hand_derived_cases(case):
+    ins = [np.array([int(v, 16) for v in row], dtype=np.uint16 if case["dtype"] == "bf16" else np.uint32)
+           for row in case["inputs_bits"]]
+    if case["dtype"] == "fp32":
+        ins = [a.view(np.float32) for a in ins]
+    got = ORDERS[case["algo"]](ins, case["op"], case.get("group", 0))
+    want = [int(v, 16) for v in case["expected_bits"]]
+    for r in range(len(ins)):
+        assert [int(v) for v in _bits(got[r])] == want, "rank %d" % r
