@@ -391,3 +391,79 @@ def allreduce_hierarchical(bufs, L: int, op: str = "sum"):
     for i in range(N):
         out[i] = list(result)
     return _store(out, T)
+
+
+# ------------------------------------------------------------------ the other collectives
+
+def reduce(bufs, root: int, op: str = "sum"):
+    """Reduce(root): the root receives the AllReduce's bits, the other ranks
+    keep their buffers (Lesson 3, core concepts: AllReduce = Reduce followed by
+    Broadcast)."""
+    out = [np.array(b, copy=True) for b in bufs]
+    out[root] = ring_allreduce(bufs, op)[0][root]
+    return out
+
+
+def allgather(chunks, K: int):
+    """Every rank receives the concatenation, in rank order, of the ranks'
+    chunks (chunk r of the K-element partition comes from rank r)."""
+    offs, lens = partition(K, len(chunks))
+    full = np.concatenate([np.asarray(c)[:lens[r]] for r, c in enumerate(chunks)]) if K else \
+        np.zeros(0, dtype=np.asarray(chunks[0]).dtype)
+    return [full.copy() for _ in chunks]
+
+
+def gather(chunks, K: int) -> np.ndarray:
+    """The root's concatenation of the ranks' chunks."""
+    return allgather(chunks, K)[0]
+
+
+def scatter(root_buf, N: int):
+    """Rank r receives chunk r of the root's buffer."""
+    src = np.asarray(root_buf)
+    offs, lens = partition(src.size, N)
+    return [src[offs[r]:offs[r] + lens[r]].copy() for r in range(N)]
+
+
+def broadcast(bufs, root: int):
+    return [np.array(bufs[root], copy=True) for _ in bufs]
+
+
+def alltoallv(sends, counts):
+    """recv_j holds, in source order, the counts[i][j] elements rank i sends to
+    rank j; send_i holds its blocks in destination order."""
+    counts = np.asarray(counts, dtype=np.int64)
+    N = len(sends)
+    recv = []
+    for j in range(N):
+        parts = []
+        for i in range(N):
+            start = int(counts[i, :j].sum())
+            parts.append(np.asarray(sends[i])[start:start + int(counts[i, j])])
+        recv.append(np.concatenate(parts) if parts else np.zeros(0, dtype=np.asarray(sends[0]).dtype))
+    return recv
+
+
+def bucket_allreduce(tensors, bucket_elems: int, op: str = "sum"):
+    """Bucket fusion (Collective Communication, "Bucket fusion"): every rank's
+    tensors are laid end to end in reverse registration order, the stream is
+    cut into buckets of bucket_elems (the last one partial; a tensor may span
+    buckets) and every bucket is ring-AllReduced on its own, with its own chunk
+    partition.  tensors[r][t]; returns new arrays."""
+    N, T = len(tensors), len(tensors[0])
+    streams = [np.concatenate([np.asarray(tensors[r][t]) for t in reversed(range(T))]) for r in range(N)]
+    total = streams[0].size
+    for b0 in range(0, total, bucket_elems):
+        b1 = min(b0 + bucket_elems, total)
+        red, _ = ring_allreduce([s[b0:b1] for s in streams], op)
+        for r in range(N):
+            streams[r][b0:b1] = red[r]
+    out = []
+    for r in range(N):
+        row, pos = [None] * T, 0
+        for t in reversed(range(T)):
+            n = np.asarray(tensors[r][t]).size
+            row[t] = streams[r][pos:pos + n].copy()
+            pos += n
+        out.append(row)
+    return out

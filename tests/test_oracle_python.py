@@ -130,3 +130,45 @@ def test_other_orders_reproduce_the_hand_derived_cases(case):
     want = [int(v, 16) for v in case["expected_bits"]]
     for r in range(len(ins)):
         assert [int(v) for v in _bits(got[r])] == want, "rank %d" % r
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("N,K", [(1, 6), (3, 10), (4, 2), (5, 37)])
+def test_other_collectives_agree_with_the_c_oracle(oracle_mod, dtype, N, K):
+    seed = 5000 + 3 * N + K
+    x = list(W.mixed_bf16(N, K, seed_base=seed) if dtype == "bf16" else W.mixed_fp32(N, K, seed_base=seed))
+    eq = np.testing.assert_array_equal
+    for op in ("sum", "avg", "max", "avg_premul"):
+        for root in {0, N - 1}:
+            for a, b in zip(ring_py.reduce(x, root, op), oracle_mod.reduce(x, root, op)):
+                eq(_bits(a), _bits(b))
+    _, ln = ring_py.partition(K, N)
+    chunks = [x[r][:ln[r]] for r in range(N)]
+    for a, b in zip(ring_py.allgather(chunks, K), oracle_mod.allgather(chunks, K)):
+        eq(_bits(a), _bits(b))
+    eq(_bits(ring_py.gather(chunks, K)), _bits(oracle_mod.gather(chunks, K)))
+    for a, b in zip(ring_py.scatter(x[0], N), oracle_mod.scatter(x[0], N)):
+        eq(_bits(a), _bits(b))
+    for root in {0, N - 1}:
+        for a, b in zip(ring_py.broadcast(x, root), oracle_mod.broadcast(x, root)):
+            eq(_bits(a), _bits(b))
+    g = np.random.default_rng(seed)
+    counts = g.integers(0, 5, size=(N, N))
+    sends = [np.asarray(x[i])[:0] if counts[i].sum() == 0 else
+             np.resize(np.asarray(x[i]), int(counts[i].sum())) for i in range(N)]
+    for a, b in zip(ring_py.alltoallv(sends, counts), oracle_mod.alltoallv(sends, counts)):
+        eq(_bits(a), _bits(b))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "avg", "max", "avg_premul"])
+@pytest.mark.parametrize("B", [1, 7, 64, 1000])
+def test_bucket_allreduce_agrees_with_the_c_oracle(oracle_mod, dtype, op, B):
+    N, numels = 3, [5, 40, 1, 0, 23]
+    gen = W.mixed_bf16 if dtype == "bf16" else W.mixed_fp32
+    tensors = [[gen(1, n, seed_base=600 + 10 * r + t)[0] for t, n in enumerate(numels)] for r in range(N)]
+    got = ring_py.bucket_allreduce(tensors, B, op)
+    want = oracle_mod.bucket_allreduce(tensors, B, op)
+    for r in range(N):
+        for t in range(len(numels)):
+            np.testing.assert_array_equal(_bits(got[r][t]), _bits(want[r][t]), err_msg="rank %d tensor %d" % (r, t))
