@@ -7,9 +7,10 @@ every parity claim.
 
 The arithmetic lives in ``ring_oracle.c`` (plain C, built here with gcc
 ``-O2 -ffp-contract=off``); this module only compiles it and marshals numpy
-arrays.  ``ring_py.py`` is a second, pure-Python statement of every function
-here, for small inputs, written apart from the C code; the tests require the
-two to agree bit for bit.  Buffers are numpy arrays: ``np.float32`` for fp32, ``np.uint16`` bit
+arrays.  ``ring_py.py`` is a second, pure-Python statement of every collective
+here (not of the alternative formulations -- threaded ring, closed forms, the
+fp64 sum), for small inputs, written apart from the C code; the tests require
+the two to agree bit for bit.  Buffers are numpy arrays: ``np.float32`` for fp32, ``np.uint16`` bit
 patterns for bf16 (the oracle never needs a bf16 numpy type).
 """
 from __future__ import annotations
