@@ -35,6 +35,28 @@ struct HostPipe {
 std::mutex g_pipe_mu; // held for a whole call: the streams and events are shared
 std::unordered_map<int, HostPipe> g_pipe;
 
+// Releases whatever make_pipe created (null handles are skipped).
+void destroy_pipe(HostPipe &p)
+{
+    for (cudaStream_t *st : {&p.h2d, &p.d2h})
+        if (*st) {
+            cudaStreamDestroy(*st);
+            *st = nullptr;
+        }
+    cudaEvent_t *evs[] = {&p.start, &p.h2d_end, &p.d2h_end};
+    for (cudaEvent_t *ev : evs)
+        if (*ev) {
+            cudaEventDestroy(*ev);
+            *ev = nullptr;
+        }
+    for (int s = 0; s < kHostStages; ++s)
+        for (cudaEvent_t *ev : {&p.in[s], &p.red[s], &p.out[s]})
+            if (*ev) {
+                cudaEventDestroy(*ev);
+                *ev = nullptr;
+            }
+}
+
 cudaError_t make_pipe(int dev, HostPipe &p)
 {
     int pitch = 0;
@@ -147,8 +169,10 @@ cudaError_t run_host_allreduce(int dt, int op, const void *const *send, void *co
     auto it = g_pipe.find(dev);
     if (it == g_pipe.end()) {
         HostPipe p;
-        if ((e = make_pipe(dev, p)) != cudaSuccess)
+        if ((e = make_pipe(dev, p)) != cudaSuccess) {
+            destroy_pipe(p); // nothing half-built is kept or leaked; the next call tries again
             return e;
+        }
         it = g_pipe.emplace(dev, p).first;
     }
     HostPipe &P = it->second;
