@@ -88,6 +88,18 @@ MUTANTS = [
     ("error_feedback_dropped",
      "u[i] = fcanon(bits_to_f32(widen_bits(load(grads[r], dtype, i), dtype)) + res[r][i]);",
      "u[i] = fcanon(bits_to_f32(widen_bits(load(grads[r], dtype, i), dtype)));"),
+    # bucket fusion, AllToAllv, the halving-doubling pre-fold, hierarchical AVG, Reduce
+    ("bucket_forward_order", "            for (int t = T - 1; t >= 0; --t) {", "            for (int t = 0; t < T; ++t) {"),
+    ("alltoallv_recv_displacements_from_transposed_counts",
+     "rd[(size_t)j * N + i] = o;\n            o += counts[(size_t)i * N + j];",
+     "rd[(size_t)j * N + i] = o;\n            o += counts[(size_t)j * N + i];"),
+    ("hd_prefold_adds_the_wrong_neighbour",
+     "hop(load(buf[2 * v + 1], dtype, e), load(buf[2 * v], dtype, e), dtype, sop));",
+     "hop(load(buf[2 * v + 1], dtype, e), load(buf[2 * v + 2], dtype, e), dtype, sop));"),
+    ("hier_avg_divides_by_group_count", "scale_range(grp[g], soff[d], soff[d] + slen[d], N, dtype);",
+     "scale_range(grp[g], soff[d], soff[d] + slen[d], G, dtype);"),
+    ("reduce_takes_chunk_from_its_own_rank", "(char *)work[mod((int64_t)c - 1, N)] + off[c] * es, len[c] * es);",
+     "(char *)work[c] + off[c] * es, len[c] * es);"),
 ]
 
 
