@@ -100,6 +100,17 @@ MUTANTS = [
      "scale_range(grp[g], soff[d], soff[d] + slen[d], G, dtype);"),
     ("reduce_takes_chunk_from_its_own_rank", "(char *)work[mod((int64_t)c - 1, N)] + off[c] * es, len[c] * es);",
      "(char *)work[c] + off[c] * es, len[c] * es);"),
+    # the copy collectives and the compressors' edges
+    ("gather_drops_the_last_rank",
+     "    for (int r = 0; r < N; ++r)\n        memcpy((char *)out_root + off[r] * es, in[r], len[r] * es);",
+     "    for (int r = 0; r < N - 1; ++r)\n        memcpy((char *)out_root + off[r] * es, in[r], len[r] * es);"),
+    ("allgather_stores_from_the_right_neighbour",
+     "int src = mod((int64_t)i - 1, N);\n            memcpy((char *)out[i] + off[c] * es, (char *)snap",
+     "int src = mod((int64_t)i + 1, N);\n            memcpy((char *)out[i] + off[c] * es, (char *)snap"),
+    ("int8_blocks_one_longer", "for (uint64_t b0 = 0; b0 < K; b0 += (uint64_t)block) {",
+     "for (uint64_t b0 = 0; b0 < K; b0 += (uint64_t)block + 1) {"),
+    ("topk_nan_ranked_lowest", "mag[i] = f32_to_bits(u[i]) & 0x7fffffffu;",
+     "mag[i] = u[i] != u[i] ? 0u : f32_to_bits(u[i]) & 0x7fffffffu;"),
 ]
 
 
