@@ -111,6 +111,8 @@ MUTANTS = [
      "for (uint64_t b0 = 0; b0 < K; b0 += (uint64_t)block + 1) {"),
     ("topk_nan_ranked_lowest", "mag[i] = f32_to_bits(u[i]) & 0x7fffffffu;",
      "mag[i] = u[i] != u[i] ? 0u : f32_to_bits(u[i]) & 0x7fffffffu;"),
+    ("chunk_offsets_ignore_the_remainder", "        off[c] = o;\n        o += len[c];",
+     "        off[c] = (uint64_t)c * q;\n        o += len[c];"),
 ]
 
 
