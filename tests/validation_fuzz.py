@@ -1,0 +1,103 @@
+"""Randomised overlap validation, run by test_validation_fuzz.py in a child
+process with CUDA_VISIBLE_DEVICES="": the pointers are fake, so a call that
+passed validation can only fail its launch (no device), never touch memory.
+
+The expected outcome comes from the header's contract, restated here: the
+buffers a call writes must not overlap one another, and a buffer it reads may
+overlap a buffer it writes only in that call's documented in-place form
+(AllReduce: send[r] == recv[r]; ReduceScatter: recv[r] == send[r] + off_r
+elements; AllGather: send[r] == recv[r] + off_r elements)."""
+import ctypes
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import ring_allreduce_rank_gb300 as ccl  # noqa: E402
+
+FAKE = 0x7f0000000000
+OVERLAP, CUDA_ERR = 3, 4
+
+
+def _pp(vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def _meets(a, b):
+    return a[0] < b[1] and b[0] < a[1] and a[0] < a[1] and b[0] < b[1]
+
+
+def expected_overlap(kind, send, recv, K, es):
+    N = len(send)
+    q, rem = K // N, K % N
+    ln = [q + (1 if c < rem else 0) for c in range(N)]
+    off = [sum(ln[:c]) for c in range(N)]
+    if kind == "allreduce":
+        W = [(recv[r], recv[r] + K * es) for r in range(N)]
+        R = [(send[r], send[r] + K * es) for r in range(N)]
+        in_place = lambda r: send[r] == recv[r]
+    elif kind == "reduce_scatter":
+        W = [(recv[r], recv[r] + ln[r] * es) for r in range(N)]
+        R = [(send[r], send[r] + K * es) for r in range(N)]
+        in_place = lambda r: recv[r] == send[r] + off[r] * es
+    else:  # allgather
+        W = [(recv[r], recv[r] + K * es) for r in range(N)]
+        R = [(send[r], send[r] + ln[r] * es) for r in range(N)]
+        in_place = lambda r: send[r] == recv[r] + off[r] * es
+    for i in range(N):
+        for j in range(i + 1, N):
+            if _meets(W[i], W[j]):
+                return True
+    for i in range(N):  # read i against write j
+        for j in range(N):
+            if _meets(R[i], W[j]) and not (i == j and in_place(i)):
+                return True
+    return False
+
+
+def main(iters=3000):
+    L = ccl.lib()
+    g = np.random.default_rng(20261202)
+    seen = {OVERLAP: 0, "accepted": 0}
+    stream = ctypes.c_void_p(0)
+    for it in range(iters):
+        kind = ["allreduce", "reduce_scatter", "allgather"][it % 3]
+        N = int(g.integers(1, 7))
+        K = int(g.integers(1, 40))
+        dt = int(g.integers(0, 2))
+        es = 4 if dt == 0 else 2
+        window = int(g.choice([64, 512, 4096]))
+        send = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+        recv = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+        q, rem = K // N, K % N
+        off = [c * q + min(c, rem) for c in range(N)]
+        for r in range(N):  # often take the call's in-place form for some ranks
+            if g.random() < 0.3:
+                if kind == "allreduce":
+                    recv[r] = send[r]
+                elif kind == "reduce_scatter":
+                    recv[r] = send[r] + off[r] * es
+                else:
+                    send[r] = recv[r] + off[r] * es
+        want = expected_overlap(kind, send, recv, K, es)
+        fn = {"allreduce": lambda: L.ccl_allreduce(_pp(send), _pp(recv), N, K, dt, 0, 0, stream),
+              "reduce_scatter": lambda: L.ccl_reduce_scatter(_pp(send), _pp(recv), N, K, dt, 0, 0, stream),
+              "allgather": lambda: L.ccl_allgather(_pp(send), _pp(recv), N, K, dt, 0, stream)}[kind]
+        got = fn()
+        if want:
+            assert got == OVERLAP, (kind, N, K, es, send, recv, got)
+            seen[OVERLAP] += 1
+        else:
+            # accepted: nothing to do (0) or a launch that fails without a device
+            assert got in (0, CUDA_ERR), (kind, N, K, es, send, recv, got)
+            seen["accepted"] += 1
+    assert seen[OVERLAP] > iters // 10 and seen["accepted"] > iters // 10, seen
+    print("validation fuzz ok", seen)
+
+
+if __name__ == "__main__":
+    assert os.environ.get("CUDA_VISIBLE_DEVICES") == "", "run with CUDA_VISIBLE_DEVICES=''"
+    main()
