@@ -200,7 +200,9 @@ ccl_status_t ccl_reduce(const void *const *send, void *const *recv, int nranks, 
  * (Lesson 3, core concepts: "Gather"; Collectives and sharded matmul, "Gather
  * and AllGather").  send[r] holds len_r elements (chunk r of `count`);
  * recv[r] for r != root is ignored.  In place when
- * send[root] == recv[root] + off_root elements. */
+ * send[root] == recv[root] + off_root elements; more generally, any send[r]
+ * may already sit at its own place, recv[root] + off_r elements (its chunk is
+ * then copied onto itself). */
 ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                         ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
 
@@ -208,7 +210,9 @@ ccl_status_t ccl_gather(const void *const *send, void *const *recv, int nranks, 
  * chunk r goes to recv[r] (len_r elements) (Lesson 3, core concepts: "Scatter",
  * the inverse of Gather; Collectives and sharded matmul, "Scatter and
  * ReduceScatter").  send[r] for r != root is ignored.  In place when
- * recv[root] == send[root] + off_root elements. */
+ * recv[root] == send[root] + off_root elements; more generally, any recv[r]
+ * may already sit at its own place, send[root] + off_r elements (its chunk is
+ * then copied onto itself). */
 ccl_status_t ccl_scatter(const void *const *send, void *const *recv, int nranks, int root, size_t count,
                          ccl_dtype_t dtype, ccl_mode_t mode, cudaStream_t stream);
 

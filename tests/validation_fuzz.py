@@ -47,15 +47,49 @@ def expected_overlap(kind, send, recv, K, es):
         W = [(recv[r], recv[r] + K * es) for r in range(N)]
         R = [(send[r], send[r] + ln[r] * es) for r in range(N)]
         in_place = lambda r: send[r] == recv[r] + off[r] * es
-    for i in range(N):
-        for j in range(i + 1, N):
+    return _violates(W, R, lambda i, j: i == j and in_place(i))
+
+
+def _violates(W, R, allowed):
+    """W, R: lists of (lo, hi) write / read ranges; allowed(i, j): read i may
+    overlap write j."""
+    for i in range(len(W)):
+        for j in range(i + 1, len(W)):
             if _meets(W[i], W[j]):
                 return True
-    for i in range(N):  # read i against write j
-        for j in range(N):
-            if _meets(R[i], W[j]) and not (i == j and in_place(i)):
+    for i in range(len(R)):
+        for j in range(len(W)):
+            if _meets(R[i], W[j]) and not allowed(i, j):
                 return True
     return False
+
+
+def expected_overlap_rooted(kind, send, recv, root, K, es):
+    """Reduce: writes recv[root], reads every send[r], in place when
+    send[root] == recv[root].  Broadcast: writes every recv[r], reads
+    send[root], in place when recv[root] == send[root].  Gather: writes
+    recv[root], reads every send[r] (len_r), which may sit at recv[root] +
+    off_r.  Scatter: writes every recv[r] (len_r), reads send[root], and recv[r]
+    may sit at send[root] + off_r."""
+    N = len(send)
+    q, rem = K // N, K % N
+    ln = [q + (1 if c < rem else 0) for c in range(N)]
+    off = [sum(ln[:c]) for c in range(N)]
+    if kind == "reduce":
+        W = [(recv[root], recv[root] + K * es)]
+        R = [(send[r], send[r] + K * es) for r in range(N)]
+        return _violates(W, R, lambda i, j: i == root and send[root] == recv[root])
+    if kind == "broadcast":
+        W = [(recv[r], recv[r] + K * es) for r in range(N)]
+        R = [(send[root], send[root] + K * es)]
+        return _violates(W, R, lambda i, j: j == root and send[root] == recv[root])
+    if kind == "gather":
+        W = [(recv[root], recv[root] + K * es)]
+        R = [(send[r], send[r] + ln[r] * es) for r in range(N)]
+        return _violates(W, R, lambda i, j: send[i] == recv[root] + off[i] * es)
+    W = [(recv[r], recv[r] + ln[r] * es) for r in range(N)]  # scatter
+    R = [(send[root], send[root] + K * es)]
+    return _violates(W, R, lambda i, j: recv[j] == send[root] + off[j] * es)
 
 
 def main(iters=3000):
@@ -95,7 +129,41 @@ def main(iters=3000):
             assert got in (0, CUDA_ERR), (kind, N, K, es, send, recv, got)
             seen["accepted"] += 1
     assert seen[OVERLAP] > iters // 10 and seen["accepted"] > iters // 10, seen
-    print("validation fuzz ok", seen)
+    rooted = {OVERLAP: 0, "accepted": 0}
+    for it in range(iters):
+        kind = ["reduce", "broadcast", "gather", "scatter"][it % 4]
+        N = int(g.integers(1, 7))
+        K = int(g.integers(1, 40))
+        root = int(g.integers(0, N))
+        dt = int(g.integers(0, 2))
+        es = 4 if dt == 0 else 2
+        window = int(g.choice([64, 512, 4096]))
+        send = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+        recv = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+        q, rem = K // N, K % N
+        off = [c * q + min(c, rem) for c in range(N)]
+        for r in range(N):  # the documented in-place forms, often
+            if g.random() < 0.3:
+                if kind in ("reduce", "broadcast") and r == root:
+                    recv[root] = send[root]
+                elif kind == "gather":
+                    send[r] = recv[root] + off[r] * es
+                elif kind == "scatter":
+                    recv[r] = send[root] + off[r] * es
+        want = expected_overlap_rooted(kind, send, recv, root, K, es)
+        fn = {"reduce": lambda: L.ccl_reduce(_pp(send), _pp(recv), N, root, K, dt, 0, 0, stream),
+              "broadcast": lambda: L.ccl_broadcast(_pp(send), _pp(recv), N, root, K, dt, 0, stream),
+              "gather": lambda: L.ccl_gather(_pp(send), _pp(recv), N, root, K, dt, 0, stream),
+              "scatter": lambda: L.ccl_scatter(_pp(send), _pp(recv), N, root, K, dt, 0, stream)}[kind]
+        got = fn()
+        if want:
+            assert got == OVERLAP, (kind, N, root, K, es, send, recv, got)
+            rooted[OVERLAP] += 1
+        else:
+            assert got in (0, CUDA_ERR), (kind, N, root, K, es, send, recv, got)
+            rooted["accepted"] += 1
+    assert rooted[OVERLAP] > iters // 10 and rooted["accepted"] > iters // 10, rooted
+    print("validation fuzz ok", seen, rooted)
 
 
 if __name__ == "__main__":
