@@ -1,7 +1,7 @@
 """Overlap validation of seven collectives over thousands of random pointer
-layouts (no GPU): the
-cases run in a child process that sees no device (tests/validation_fuzz.py),
-where every call the library accepts can only fail its launch."""
+layouts (no GPU): the cases run in a child process that sees no device
+(tests/validation_fuzz.py), where every call the library accepts can only
+fail its launch."""
 import os
 import subprocess
 import sys
