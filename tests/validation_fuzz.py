@@ -163,7 +163,42 @@ def main(iters=3000):
             assert got in (0, CUDA_ERR), (kind, N, root, K, es, send, recv, got)
             rooted["accepted"] += 1
     assert rooted[OVERLAP] > iters // 10 and rooted["accepted"] > iters // 10, rooted
-    print("validation fuzz ok", seen, rooted)
+    # AllToAllv: no in-place form (every read disjoint from every write);
+    # bucket AllReduce: in place on the tensors, which must all be disjoint
+    other = {OVERLAP: 0, "accepted": 0}
+    for it in range(iters):
+        N = int(g.integers(1, 6))
+        dt = int(g.integers(0, 2))
+        es = 4 if dt == 0 else 2
+        window = int(g.choice([64, 512, 4096]))
+        if it % 2 == 0:
+            counts = g.integers(0, 6, size=(N, N))
+            stot, rtot = counts.sum(axis=1), counts.sum(axis=0)
+            send = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+            recv = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+            W = [(recv[j], recv[j] + int(rtot[j]) * es) for j in range(N)]
+            R = [(send[i], send[i] + int(stot[i]) * es) for i in range(N)]
+            want = _violates(W, R, lambda i, j: False)
+            cts = (ctypes.c_size_t * (N * N))(*[int(c) for c in counts.ravel()])
+            got = L.ccl_alltoallv(_pp(send), _pp(recv), N, cts, dt, 0, stream)
+            what = ("alltoallv", N, counts.tolist(), send, recv, got)
+        else:
+            T = int(g.integers(1, 5))
+            numels = [int(v) for v in g.integers(0, 20, size=T)]
+            ptrs = [FAKE + es * int(g.integers(0, window)) for _ in range(N * T)]
+            W = [(ptrs[r * T + t], ptrs[r * T + t] + numels[t] * es) for r in range(N) for t in range(T)]
+            want = _violates(W, [], lambda i, j: False)
+            nums = (ctypes.c_size_t * T)(*numels)
+            got = L.ccl_bucket_allreduce(_pp(ptrs), nums, T, N, 0, dt, 0, 0, stream)
+            what = ("bucket", N, numels, ptrs, got)
+        if want:
+            assert got == OVERLAP, what
+            other[OVERLAP] += 1
+        else:
+            assert got in (0, CUDA_ERR), what
+            other["accepted"] += 1
+    assert other[OVERLAP] > iters // 10 and other["accepted"] > iters // 10, other
+    print("validation fuzz ok", seen, rooted, other)
 
 
 if __name__ == "__main__":
