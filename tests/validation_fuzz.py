@@ -198,7 +198,55 @@ def main(iters=3000):
             assert got in (0, CUDA_ERR), what
             other["accepted"] += 1
     assert other[OVERLAP] > iters // 10 and other["accepted"] > iters // 10, other
-    print("validation fuzz ok", seen, rooted, other)
+    # compressed and Top-k AllReduce: gradients, residuals (and Top-k's work
+    # buffer) all disjoint; host-buffer AllReduce: outputs and the work buffer
+    # disjoint, an input overlapping an output only as send[r] == recv[r]
+    comp = {OVERLAP: 0, "accepted": 0}
+    topk_wb = ctypes.c_size_t()
+    for it in range(iters):
+        N = int(g.integers(1, 6))
+        K = int(g.integers(1, 40))
+        dt = int(g.integers(0, 2))
+        es = 4 if dt == 0 else 2
+        window = int(g.choice([64, 512, 4096]))
+        far = FAKE + (1 << 32)
+        kind = ["compressed", "topk", "host"][it % 3]
+        if kind in ("compressed", "topk"):
+            grads = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+            res = [FAKE + 4 * int(g.integers(0, window)) for _ in range(N)]
+            W = [(p, p + K * es) for p in grads] + [(p, p + K * 4) for p in res]
+            if kind == "compressed":
+                got = L.ccl_allreduce_compressed(_pp(grads), _pp(res), N, K, dt, 0, 0, 128, ctypes.c_float(0.5),
+                                                 stream)
+            else:
+                assert L.ccl_plan_topk_work_bytes(N, ctypes.byref(topk_wb)) == 0
+                work = far if g.random() < 0.7 else FAKE + 16 * int(g.integers(0, window))
+                W.append((work, work + topk_wb.value))
+                got = L.ccl_allreduce_topk(_pp(grads), _pp(res), N, K, dt, 0, 3, ctypes.c_void_p(work),
+                                           topk_wb.value, stream)
+            want = _violates(W, [], lambda i, j: False)
+            what = (kind, N, K, es, grads, res, got)
+        else:
+            send = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+            recv = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+            for r in range(N):
+                if g.random() < 0.3:
+                    recv[r] = send[r]
+            wbytes = 3 * N * 256 * es
+            work = far if g.random() < 0.7 else FAKE + 16 * int(g.integers(0, window))
+            W = [(recv[r], recv[r] + K * es) for r in range(N)] + [(work, work + wbytes)]
+            R = [(send[r], send[r] + K * es) for r in range(N)]
+            want = _violates(W, R, lambda i, j: j == i and send[i] == recv[i])
+            got = L.ccl_allreduce_host(_pp(send), _pp(recv), N, K, dt, 0, ctypes.c_void_p(work), wbytes, stream)
+            what = (kind, N, K, es, send, recv, work, got)
+        if want:
+            assert got == OVERLAP, what
+            comp[OVERLAP] += 1
+        else:
+            assert got in (0, CUDA_ERR), what
+            comp["accepted"] += 1
+    assert comp[OVERLAP] > iters // 10 and comp["accepted"] > iters // 10, comp
+    print("validation fuzz ok", seen, rooted, other, comp)
 
 
 if __name__ == "__main__":
