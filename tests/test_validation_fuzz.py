@@ -1,4 +1,4 @@
-"""Overlap validation of twelve entry points over thousands of random pointer
+"""Overlap validation of thirteen entry points over thousands of random pointer
 layouts (no GPU): the cases run in a child process that sees no device
 (tests/validation_fuzz.py), where every call the library accepts can only
 fail its launch."""

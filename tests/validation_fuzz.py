@@ -246,7 +246,28 @@ def main(iters=3000):
             assert got in (0, CUDA_ERR), what
             comp["accepted"] += 1
     assert comp[OVERLAP] > iters // 10 and comp["accepted"] > iters // 10, comp
-    print("validation fuzz ok", seen, rooted, other, comp)
+    # the ReduceScatter that allocates nothing promises ccl_reduce_scatter's
+    # error checks: both must answer every layout the same way
+    same = {OVERLAP: 0, "accepted": 0}
+    for it in range(iters):
+        N = int(g.integers(1, 7))
+        K = int(g.integers(1, 40))
+        dt = int(g.integers(0, 2))
+        es = 4 if dt == 0 else 2
+        window = int(g.choice([64, 512, 4096]))
+        send = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+        recv = [FAKE + es * int(g.integers(0, window)) for _ in range(N)]
+        q, rem = K // N, K % N
+        for r in range(N):
+            if g.random() < 0.3:
+                recv[r] = send[r] + (r * q + min(r, rem)) * es
+        want = expected_overlap("reduce_scatter", send, recv, K, es)
+        a = L.ccl_reduce_scatter(_pp(send), _pp(recv), N, K, dt, 0, 1, stream)
+        b = L.ccl_reduce_scatter_step_static(_pp(send), _pp(recv), N, K, dt, 0, stream)
+        assert (a == OVERLAP) == want and (b == OVERLAP) == want, (N, K, es, send, recv, a, b)
+        same[OVERLAP if want else "accepted"] += 1
+    assert same[OVERLAP] > iters // 10 and same["accepted"] > iters // 10, same
+    print("validation fuzz ok", seen, rooted, other, comp, same)
 
 
 if __name__ == "__main__":
