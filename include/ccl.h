@@ -36,6 +36,11 @@
  * Common conventions
  *   - Pointer arrays (send[], recv[], ptrs[]) are HOST arrays of nranks DEVICE
  *     pointers.  The caller owns every buffer; the library never frees them.
+ *     A pointer to zero elements may be NULL (a ReduceScatter or Scatter
+ *     output, or an AllGather or Gather input, for an empty chunk when
+ *     count < nranks; a zero-length bucket tensor; an empty AllToAllv
+ *     buffer), as may the entries a call ignores (noted per call); every other
+ *     pointer a call uses must not be NULL (CCL_ERR_INVALID_ARG).
  *   - All entry points that take a stream are asynchronous: they validate
  *     their arguments on the host, enqueue kernels on `stream` (0 = legacy
  *     default stream) and return.  Completion is stream completion

@@ -267,7 +267,50 @@ def main(iters=3000):
         assert (a == OVERLAP) == want and (b == OVERLAP) == want, (N, K, es, send, recv, a, b)
         same[OVERLAP if want else "accepted"] += 1
     assert same[OVERLAP] > iters // 10 and same["accepted"] > iters // 10, same
-    print("validation fuzz ok", seen, rooted, other, comp, same)
+    # NULL entries: allowed for zero-element buffers and for the entries a
+    # call ignores, rejected (CCL_ERR_INVALID_ARG) everywhere else.  Buffers
+    # sit far apart here, so no layout overlaps.
+    nulls = {"rejected": 0, "accepted": 0}
+    for it in range(iters):
+        kind = ["reduce_scatter", "allgather", "gather", "scatter", "broadcast", "reduce", "allreduce"][it % 7]
+        N = int(g.integers(1, 7))
+        K = int(g.integers(1, 9))  # often fewer elements than ranks: empty chunks
+        root = int(g.integers(0, N))
+        q, rem = K // N, K % N
+        ln = [q + (1 if c < rem else 0) for c in range(N)]
+        send = [FAKE + (2 * r) * (1 << 20) for r in range(N)]
+        recv = [FAKE + (2 * r + 1) * (1 << 20) for r in range(N)]
+        for r in range(N):
+            if g.random() < 0.25:
+                send[r] = None
+            if g.random() < 0.25:
+                recv[r] = None
+        need_send = {"reduce_scatter": [True] * N, "allgather": [ln[r] > 0 for r in range(N)],
+                     "gather": [ln[r] > 0 for r in range(N)], "scatter": [r == root for r in range(N)],
+                     "broadcast": [r == root for r in range(N)], "reduce": [True] * N,
+                     "allreduce": [True] * N}[kind]
+        need_recv = {"reduce_scatter": [ln[r] > 0 for r in range(N)], "allgather": [True] * N,
+                     "gather": [r == root for r in range(N)], "scatter": [ln[r] > 0 for r in range(N)],
+                     "broadcast": [True] * N, "reduce": [r == root for r in range(N)],
+                     "allreduce": [True] * N}[kind]
+        want_reject = any(need_send[r] and send[r] is None for r in range(N)) or \
+            any(need_recv[r] and recv[r] is None for r in range(N))
+        fn = {"reduce_scatter": lambda: L.ccl_reduce_scatter(_pp(send), _pp(recv), N, K, 0, 0, 0, stream),
+              "allgather": lambda: L.ccl_allgather(_pp(send), _pp(recv), N, K, 0, 0, stream),
+              "gather": lambda: L.ccl_gather(_pp(send), _pp(recv), N, root, K, 0, 0, stream),
+              "scatter": lambda: L.ccl_scatter(_pp(send), _pp(recv), N, root, K, 0, 0, stream),
+              "broadcast": lambda: L.ccl_broadcast(_pp(send), _pp(recv), N, root, K, 0, 0, stream),
+              "reduce": lambda: L.ccl_reduce(_pp(send), _pp(recv), N, root, K, 0, 0, 0, stream),
+              "allreduce": lambda: L.ccl_allreduce(_pp(send), _pp(recv), N, K, 0, 0, 0, stream)}[kind]
+        got = fn()
+        if want_reject:
+            assert got == 1, (kind, N, K, root, send, recv, got)
+            nulls["rejected"] += 1
+        else:
+            assert got in (0, CUDA_ERR), (kind, N, K, root, send, recv, got)
+            nulls["accepted"] += 1
+    assert nulls["rejected"] > iters // 10 and nulls["accepted"] > iters // 10, nulls
+    print("validation fuzz ok", seen, rooted, other, comp, same, nulls)
 
 
 if __name__ == "__main__":
