@@ -28,7 +28,7 @@ def test_header_compiles_strictly(lang, std, tmp_path):
     src = tmp_path / ("h." + ("c" if lang == "c" else "cpp"))
     src.write_text('#include "ccl.h"\nint main(void) { return ccl_version() > 0 ? 0 : 1; }\n')
     cc = "gcc" if lang == "c" else "g++"
-    # CUDA's own headers are system headers here: the strict flags judge ccl.h
+    # CUDA's own headers are system headers here: the strict flags apply to ccl.h alone
     subprocess.run([cc, "-std=" + std, "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only", "-I", INCLUDE,
                     "-isystem", _cuda_include(), str(src)], check=True)
 
