@@ -17,6 +17,7 @@ import ring_allreduce_rank_gb300 as ccl
 from ring_allreduce_rank_gb300 import workloads as W
 from ring_allreduce_rank_gb300.arena import RankArena
 
+from accuracy import error_figures, report
 from gpu_util import DEV, assert_bits_equal, bits, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -33,11 +34,15 @@ def _device():
     torch.cuda.empty_cache()
 
 
-def _normwise_ok(y_bits_bf16, x, op, rtol):
+def _normwise_ok(y_bits_bf16, x, op, rtol, tag):
+    """The relative tolerance, normwise; the elementwise figure is printed
+    beside it (tests/accuracy.py)."""
     y = W.bf16_bits_to_f32(y_bits_bf16).astype(np.float64) if y_bits_bf16.dtype == np.uint16 else \
         y_bits_bf16.astype(np.float64)
-    y64, _ = oracle.sum_f64(x, op)
-    return np.linalg.norm(y - y64) <= rtol * np.linalg.norm(y64)
+    y64, absum = oracle.sum_f64(x, op)
+    fig = error_figures(y, y64, absum)
+    report(tag, fig)
+    return fig["normwise"] <= rtol
 
 
 def test_integers_fp32_n4_exact():
@@ -63,7 +68,7 @@ def test_grad_avg_bf16_n8_128mib_full():
     want, _ = oracle.ring_allreduce(list(x), "avg")
     for r in range(N):
         assert_bits_equal(got[r].view(np.uint16), want[r], "grad-avg rank %d" % r)
-    assert _normwise_ok(want[0], list(x), "avg", 1e-2)
+    assert _normwise_ok(want[0], list(x), "avg", 1e-2, "grad-avg N=8 bf16 64Mi")
 
 
 @pytest.mark.parametrize("op", ["sum", "max"])
@@ -85,7 +90,7 @@ def test_ragged_fp32_n16_rs_ag_equals_ar(op):
         assert_bits_equal(g, a, "RS+AG vs AR rank %d" % r)
         assert_bits_equal(a, want[r], "ragged AR rank %d" % r)
     if op == "sum":
-        assert _normwise_ok(want[0], list(x), "sum", 1e-5)
+        assert _normwise_ok(want[0], list(x), "sum", 1e-5, "ragged N=16 fp32 SUM")
     else:
         np.testing.assert_array_equal(want[0], x.max(axis=0))
 
@@ -148,6 +153,9 @@ def test_sweep_allreduce_bf16_sampled(N):
             assert_bits_equal(got, want, "sweep N=%d S=%d rank %d" % (N, S, r))
         for r in range(1, N):
             assert torch.equal(arena.ranks[r].view(torch.int16), arena.ranks[0].view(torch.int16))
+        y64, absum = oracle.sum_f64(vals, "sum")
+        fig = error_figures(W.bf16_bits_to_f32(want), y64, absum)
+        report("sweep N=%d S=%d (sampled)" % (N, S), fig)
         del arena
         torch.cuda.empty_cache()
 

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 from ring_allreduce_rank_gb300 import workloads as W
+from accuracy import error_figures, report
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -415,6 +416,7 @@ def test_avg_power_of_two_is_scaled_sum(oracle_mod):
 
 
 @pytest.mark.parametrize("dtype,op,N,K,rtol", [("bf16", "avg", 8, 65536, 1e-2), ("bf16", "sum", 16, 20000, 1e-2),
+                                                ("bf16", "sum", 64, 65536, 1e-2),
                                                 ("fp32", "sum", 16, 20011, 1e-5), ("fp32", "avg", 5, 9999, 1e-5)])
 def test_error_bound_against_fp64(oracle_mod, dtype, op, N, K, rtol):
     """Accuracy against the plain definition y = sum_r x_r in fp64.
@@ -436,6 +438,9 @@ def test_error_bound_against_fp64(oracle_mod, dtype, op, N, K, rtol):
     bound = (N - 1 + (1 if op == "avg" else 0)) * u * absum * (1 + 1e-6) + 1e-300
     assert np.all(err <= bound)
     assert np.linalg.norm(err) <= rtol * np.linalg.norm(y64)
+    fig = error_figures(y, y64, absum)
+    report("oracle %s %s N=%d K=%d" % (dtype, op, N, K), fig)
+    assert fig["elementwise"] <= (N - 1 + (1 if op == "avg" else 0)) * u * (1 + 1e-6)
 
 
 # ---------------------------------------------------------------- pre-multiplied AVG
