@@ -340,20 +340,28 @@ ccl_status_t ccl_plan_topk_bytes(size_t count, size_t k, size_t *bytes);
  * synchronisation cudaMalloc/cudaFree can imply, or hosts that forbid driver
  * allocations after start-up.
  * Same arguments, result and error checks as ccl_reduce_scatter in
- * CCL_MODE_STEP (identical bits), but the working copies of the N inputs live
- * in one fixed array of CCL_STATIC_SCRATCH_BYTES (32 MiB) in device memory,
- * reserved when the library loads and held by every GPU that loads it until
- * the process exits.  nranks * round_up(count * element size, 256) must not
- * exceed CCL_STATIC_SCRATCH_BYTES: larger calls return CCL_ERR_INVALID_ARG
- * before anything is enqueued.  It calls no cudaMalloc, cudaFree or other
- * allocating routine.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ * CCL_MODE_STEP (identical bits; the checks are the same code), but the
+ * working copies of the N inputs live in one fixed array of
+ * CCL_STATIC_SCRATCH_BYTES (32 MiB) in device memory, held by every GPU that
+ * reserves it until the process exits.  nranks * round_up(count * element
+ * size, 256) must not exceed CCL_STATIC_SCRATCH_BYTES: larger calls return
+ * CCL_ERR_INVALID_ARG before anything is enqueued.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   - Set-up, once per device: a call with count = 0 (valid nranks, dtype and
+ *     op, non-NULL pointer arrays whose entries are not read) looks up the
+ *     array's device address (cudaGetSymbolAddress, with that device current),
+ *     loads every kernel this entry launches, caches the address and enqueues
+ *     nothing; it returns CCL_ERR_CUDA if that fails.  Under CUDA's lazy module
+ *     loading (the default since CUDA 12.2) this lookup is when the driver
+ *     reserves the array, so make this call at start-up, before a caching
+ *     pool takes the GPU's memory and before any stream capture.  A first
+ *     call with count > 0 does the same set-up itself.
  *   - Every call on a device shares the array and leaves its contents behind.
  *     Each call overwrites every byte it later reads, so nothing needs
  *     clearing, but calls whose work overlaps on the GPU (other streams, other
- *     host threads) race on it: serialise them. */
+ *     host threads) race on it: serialise them.
+ *   - ccl_finalize forgets the cached address of the current device; call it
+ *     after a cudaDeviceReset, before the next call on that device. */
 ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, void *const *recv, int nranks, size_t count,
                                             ccl_dtype_t dtype, ccl_op_t op, cudaStream_t stream);
 
@@ -560,8 +568,11 @@ unsigned long long ccl_launch_count(void);
 ccl_status_t ccl_step_sent(int nranks, unsigned long long *sent, int reset);
 
 /* Frees the library's cached device workspace on the current device (used by
- * step-mode ReduceScatter, Reduce and bucket AllReduce).  Safe to call at any
- * time when no call of this library is in flight. */
+ * step-mode ReduceScatter, Reduce and bucket AllReduce) and forgets the cached
+ * address of ccl_reduce_scatter_step_static's fixed array there (the array
+ * itself stays).  Safe to call at any time when no call of this library is in
+ * flight; call it after a cudaDeviceReset, before the next call on that
+ * device, since the reset invalidates both. */
 ccl_status_t ccl_finalize(void);
 
 #ifdef __cplusplus

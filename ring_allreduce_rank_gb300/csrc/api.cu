@@ -27,69 +27,6 @@ unsigned long long thread_launch_count() { return t_launches; }
 
 namespace {
 
-size_t elem_size(ccl_dtype_t dt) { return dt == CCL_BF16 ? 2 : 4; }
-bool valid_dtype(ccl_dtype_t dt) { return dt == CCL_FP32 || dt == CCL_BF16; }
-bool valid_op(ccl_op_t op)
-{
-    return op == CCL_SUM || op == CCL_AVG || op == CCL_MAX || op == CCL_PROD || op == CCL_MIN ||
-           op == CCL_AVG_PREMUL;
-}
-// Operators that change a value even with one rank (x / 1 or x * 1 turns a
-// NaN into the canonical NaN), so N = 1 in place is not a no-op for them.
-bool scales(int op) { return op == CCL_AVG || op == CCL_AVG_PREMUL; }
-// Step mode: a separate scaling launch after the ReduceScatter phase -- AVG's
-// division, or the pre-multiplied AVG's scaling when N = 1 gives it no hop.
-bool step_scale(int op, int nranks) { return op == CCL_AVG || (op == CCL_AVG_PREMUL && nranks == 1); }
-bool valid_mode(ccl_mode_t m) { return m == CCL_MODE_FUSED || m == CCL_MODE_STEP; }
-bool valid_ranks(int n) { return n >= 1 && n <= CCL_MAX_RANKS; }
-
-bool mul_overflows(size_t a, size_t b) { return a != 0 && b > SIZE_MAX / a; }
-
-ccl_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CCL_OK : CCL_ERR_CUDA; }
-
-// A byte range touched by a call: lo/hi, which rank, read or write.
-struct Range {
-    uintptr_t lo, hi;
-    int rank;
-};
-
-// Writes must be pairwise disjoint; a read may overlap a write only in one of
-// the call's in-place forms, decided by `allowed(read, write)`.
-template <class Allowed>
-ccl_status_t check_overlaps(std::vector<Range> writes, const std::vector<Range> &reads, Allowed allowed)
-{
-    writes.erase(std::remove_if(writes.begin(), writes.end(), [](const Range &r) { return r.lo == r.hi; }),
-                 writes.end());
-    std::sort(writes.begin(), writes.end(), [](const Range &a, const Range &b) { return a.lo < b.lo; });
-    for (size_t i = 1; i < writes.size(); ++i)
-        if (writes[i].lo < writes[i - 1].hi)
-            return CCL_ERR_OVERLAP;
-    for (const Range &r : reads) {
-        if (r.lo == r.hi)
-            continue;
-        // first write whose end is past the read's start (ends are sorted too)
-        auto it = std::upper_bound(writes.begin(), writes.end(), r.lo,
-                                   [](uintptr_t v, const Range &w) { return v < w.hi; });
-        for (; it != writes.end() && it->lo < r.hi; ++it)
-            if (!allowed(r, *it))
-                return CCL_ERR_OVERLAP;
-    }
-    return CCL_OK;
-}
-
-Range range_of(const void *p, size_t bytes, int rank)
-{
-    return Range{(uintptr_t)p, (uintptr_t)p + bytes, rank};
-}
-
-Partition make_partition(size_t count, int nranks)
-{
-    Partition p;
-    p.q = count / (uint64_t)nranks;
-    p.rem = (uint32_t)(count % (uint64_t)nranks);
-    return p;
-}
-
 // ------------------------------------------------------------------ workspace
 
 struct Workspace {
@@ -175,6 +112,32 @@ ccl_status_t dbg_call(const std::vector<Range> &a, const std::vector<Range> &b, 
 #endif
 
 } // namespace
+
+ccl_status_t check_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
+                                  ccl_dtype_t dtype, ccl_op_t op, std::vector<Range> &w, std::vector<Range> &r)
+{
+    w.clear();
+    r.clear();
+    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !send || !recv)
+        return CCL_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (mul_overflows(count, es) || mul_overflows(count, (size_t)nranks))
+        return CCL_ERR_INVALID_ARG;
+    if (count == 0)
+        return CCL_OK;
+    const Partition part = make_partition(count, nranks);
+    for (int i = 0; i < nranks; ++i) {
+        // an empty chunk's output may be NULL (K < N leaves chunks empty)
+        if (!send[i] || (!recv[i] && part.len((uint32_t)i) > 0))
+            return CCL_ERR_INVALID_ARG;
+        w.push_back(range_of(recv[i], part.len((uint32_t)i) * es, i));
+        r.push_back(range_of(send[i], count * es, i));
+    }
+    return check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
+        return rd.rank == wr.rank && wr.lo == rd.lo + part.off((uint32_t)rd.rank) * es;
+    });
+}
+
 } // namespace ccl
 
 using namespace ccl;
@@ -214,6 +177,7 @@ ccl_status_t ccl_finalize(void)
             cudaFree(it->second.ptr);
         g_ws.erase(it);
     }
+    forget_static_scratch(dev);
     return CCL_OK;
 }
 
@@ -348,27 +312,14 @@ static ccl_status_t ccl_allreduce_impl(const void *const *send, void *const *rec
 static ccl_status_t ccl_reduce_scatter_impl(const void *const *send, void *const *recv, int nranks, size_t count,
                                 ccl_dtype_t dtype, ccl_op_t op, ccl_mode_t mode, cudaStream_t stream)
 {
-    if (!valid_ranks(nranks) || !valid_dtype(dtype) || !valid_op(op) || !valid_mode(mode) || !send || !recv)
+    if (!valid_mode(mode))
         return CCL_ERR_INVALID_ARG;
-    const size_t es = elem_size(dtype);
-    if (mul_overflows(count, es) || mul_overflows(count, (size_t)nranks))
-        return CCL_ERR_INVALID_ARG;
-    if (count == 0)
-        return CCL_OK;
-    const Partition part = make_partition(count, nranks);
     std::vector<Range> w, r;
-    for (int i = 0; i < nranks; ++i) {
-        // an empty chunk's output may be NULL (K < N leaves chunks empty)
-        if (!send[i] || (!recv[i] && part.len((uint32_t)i) > 0))
-            return CCL_ERR_INVALID_ARG;
-        w.push_back(range_of(recv[i], part.len((uint32_t)i) * es, i));
-        r.push_back(range_of(send[i], count * es, i));
-    }
-    ccl_status_t st = check_overlaps(w, r, [&](const Range &rd, const Range &wr) {
-        return rd.rank == wr.rank && wr.lo == rd.lo + part.off((uint32_t)rd.rank) * es;
-    });
-    if (st != CCL_OK)
+    ccl_status_t st = check_reduce_scatter(send, recv, nranks, count, dtype, op, w, r);
+    if (st != CCL_OK || count == 0)
         return st;
+    const size_t es = elem_size(dtype);
+    const Partition part = make_partition(count, nranks);
     CCL_DBG(w, r, {}, stream);
     if (mode == CCL_MODE_FUSED)
         return from_cuda(launch_fused_reduce((int)dtype, (int)op, send, recv, nranks, count, WRITE_CHUNK, 0, stream));

@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "../../include/ccl.h"
@@ -13,6 +14,81 @@
 #include "fused.h"
 
 namespace ccl {
+
+// ------------------------------------------------------------------ argument checks
+inline size_t elem_size(ccl_dtype_t dt) { return dt == CCL_BF16 ? 2 : 4; }
+inline bool valid_dtype(ccl_dtype_t dt) { return dt == CCL_FP32 || dt == CCL_BF16; }
+inline bool valid_op(ccl_op_t op)
+{
+    return op == CCL_SUM || op == CCL_AVG || op == CCL_MAX || op == CCL_PROD || op == CCL_MIN ||
+           op == CCL_AVG_PREMUL;
+}
+// Operators that change a value even with one rank (x / 1 or x * 1 turns a
+// NaN into the canonical NaN), so N = 1 in place is not a no-op for them.
+inline bool scales(int op) { return op == CCL_AVG || op == CCL_AVG_PREMUL; }
+// Step mode: a separate scaling launch after the ReduceScatter phase -- AVG's
+// division, or the pre-multiplied AVG's scaling when N = 1 gives it no hop.
+inline bool step_scale(int op, int nranks) { return op == CCL_AVG || (op == CCL_AVG_PREMUL && nranks == 1); }
+inline bool valid_mode(ccl_mode_t m) { return m == CCL_MODE_FUSED || m == CCL_MODE_STEP; }
+inline bool valid_ranks(int n) { return n >= 1 && n <= CCL_MAX_RANKS; }
+
+inline bool mul_overflows(size_t a, size_t b) { return a != 0 && b > SIZE_MAX / a; }
+
+inline ccl_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CCL_OK : CCL_ERR_CUDA; }
+
+// A byte range touched by a call: lo/hi, which rank, read or write.
+struct Range {
+    uintptr_t lo, hi;
+    int rank;
+};
+
+// Writes must be pairwise disjoint; a read may overlap a write only in one of
+// the call's in-place forms, decided by `allowed(read, write)`.
+template <class Allowed>
+inline ccl_status_t check_overlaps(std::vector<Range> writes, const std::vector<Range> &reads, Allowed allowed)
+{
+    writes.erase(std::remove_if(writes.begin(), writes.end(), [](const Range &r) { return r.lo == r.hi; }),
+                 writes.end());
+    std::sort(writes.begin(), writes.end(), [](const Range &a, const Range &b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < writes.size(); ++i)
+        if (writes[i].lo < writes[i - 1].hi)
+            return CCL_ERR_OVERLAP;
+    for (const Range &r : reads) {
+        if (r.lo == r.hi)
+            continue;
+        // first write whose end is past the read's start (ends are sorted too)
+        auto it = std::upper_bound(writes.begin(), writes.end(), r.lo,
+                                   [](uintptr_t v, const Range &w) { return v < w.hi; });
+        for (; it != writes.end() && it->lo < r.hi; ++it)
+            if (!allowed(r, *it))
+                return CCL_ERR_OVERLAP;
+    }
+    return CCL_OK;
+}
+
+inline Range range_of(const void *p, size_t bytes, int rank)
+{
+    return Range{(uintptr_t)p, (uintptr_t)p + bytes, rank};
+}
+
+inline Partition make_partition(size_t count, int nranks)
+{
+    Partition p;
+    p.q = count / (uint64_t)nranks;
+    p.rem = (uint32_t)(count % (uint64_t)nranks);
+    return p;
+}
+
+// ReduceScatter's argument checks (all but the mode), shared by
+// ccl_reduce_scatter and ccl_reduce_scatter_step_static so that both answer
+// every call alike: enums, NULL pointers (an empty chunk's output may be NULL),
+// byte-count overflow, and overlaps (outputs pairwise disjoint; an output may
+// sit inside its own rank's input only at that rank's chunk offset).  On
+// CCL_OK, w and r hold the call's written and read ranges (empty for
+// count = 0).
+ccl_status_t check_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
+                                  ccl_dtype_t dtype, ccl_op_t op, std::vector<Range> &w, std::vector<Range> &r);
+
 
 // ------------------------------------------------------------------ step mode
 enum StepKind {
@@ -37,6 +113,10 @@ template <int MAXR> struct StepParams {
 cudaError_t launch_ring_step(int dt, int op, int kind, int s, void *const *bufs, int nranks, uint64_t count,
                              cudaStream_t stream);
 
+// Loads every ring-step kernel into the current device's context (CUDA loads
+// kernels lazily, at first launch, by default).
+cudaError_t preload_ring_step_kernels();
+
 // ------------------------------------------------------------------ copies
 struct CopySeg {
     const char *src;
@@ -48,6 +128,9 @@ struct CopySeg {
 // Enqueue byte copies of the given segments (any alignment), split into as
 // many launches as the parameter space requires.
 cudaError_t launch_copy_segments(const CopySeg *segs, size_t nseg, cudaStream_t stream);
+
+// Loads every segment-copy kernel into the current device's context.
+cudaError_t preload_copy_kernels();
 
 // AllGather / Broadcast fan-out: each source element is read once and written
 // to every destination.  AllGather: src[c] is chunk c (partition of count over
@@ -123,6 +206,11 @@ void plan_host_slices(uint64_t count, uint64_t stage_elems, std::vector<HostSlic
 // Pipelined copy-in / reduce / copy-out through `work`; validated arguments.
 cudaError_t run_host_allreduce(int dt, int op, const void *const *send, void *const *recv, int nranks,
                                uint64_t count, void *work, size_t work_bytes, cudaStream_t stream);
+
+// ------------------------------------------------------------------ fixed working space
+// Drops the cached device address of ccl_reduce_scatter_step_static's array on
+// device `dev` (ccl_finalize), so that the next call resolves it again.
+void forget_static_scratch(int dev);
 
 // ------------------------------------------------------------------ bounds checks (debug builds)
 // The byte ranges a call's kernels may touch.  Debug builds upload them on the

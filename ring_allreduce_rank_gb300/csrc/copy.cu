@@ -162,6 +162,15 @@ cudaError_t launch_copy_segments(const CopySeg *segs, size_t nseg, cudaStream_t 
     return cudaSuccess;
 }
 
+cudaError_t preload_copy_kernels()
+{
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, copy_segments_kernel<kCopySegsSmall>);
+    if (e == cudaSuccess)
+        e = cudaFuncGetAttributes(&a, copy_segments_kernel<kCopySegsMid>);
+    return e != cudaSuccess ? e : cudaFuncGetAttributes(&a, copy_segments_kernel<kCopySegsLarge>);
+}
+
 // ------------------------------------------------------------------ fan-out (AllGather, Broadcast)
 
 template <int MAXR> struct FanoutParams {

@@ -8,20 +8,25 @@
 // code that must not stall other streams on the implicit device
 // synchronisation that cudaMalloc/cudaFree can cause, or hosts that forbid
 // driver allocations outside start-up.  This variant runs the same ring steps
-// with its working space in one fixed array in device memory, reserved when
-// the library is loaded.
+// with its working space in one fixed array in device memory.
+//
+// When that array is reserved depends on how CUDA loads this library's device
+// code.  Under lazy loading (the default since CUDA 12.2) it is reserved the
+// first time a device resolves its address, not when the library is loaded.
+// A call with count = 0 does exactly that set-up on the current device: it
+// resolves the address (reserving the array) and loads every kernel the entry
+// launches, so that later calls need no device memory at all.
 #include <mutex>
 #include <unordered_map>
 #include <vector>
-#include <algorithm>
 
 #include "../../include/ccl.h"
 #include "ccl_internal.h"
 
 namespace {
 
-// The working space, CCL_STATIC_SCRATCH_BYTES per device.  Every GPU that loads
-// this library keeps it until the process exits.  All calls on a device share
+// The working space, CCL_STATIC_SCRATCH_BYTES per device.  Every GPU that
+// reserves it keeps it until the process exits.  All calls on a device share
 // it, so two calls whose work overlaps on that GPU (different streams, or
 // different host threads) race on it.
 static __device__ __align__(256) unsigned char ccl_static_scratch[CCL_STATIC_SCRATCH_BYTES];
@@ -31,7 +36,8 @@ std::unordered_map<int, void *> g_scratch_addr; // device -> device address of c
 
 // Host code only sees a host-side stand-in for ccl_static_scratch; the device
 // address comes from cudaGetSymbolAddress, once per device, with that device
-// current.
+// current.  The first lookup on a device also loads the kernels this entry
+// launches.
 ccl_status_t scratch_address(void **out)
 {
     int dev = 0;
@@ -43,7 +49,8 @@ ccl_status_t scratch_address(void **out)
     auto it = g_scratch_addr.find(dev);
     if (it == g_scratch_addr.end()) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, ccl_static_scratch) != cudaSuccess || p == nullptr) {
+        if (cudaGetSymbolAddress(&p, ccl_static_scratch) != cudaSuccess || p == nullptr ||
+            ccl::preload_ring_step_kernels() != cudaSuccess || ccl::preload_copy_kernels() != cudaSuccess) {
             cudaGetLastError();
             return CCL_ERR_CUDA;
         }
@@ -53,9 +60,13 @@ ccl_status_t scratch_address(void **out)
     return CCL_OK;
 }
 
-bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
-
 } // namespace
+
+void ccl::forget_static_scratch(int dev)
+{
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    g_scratch_addr.erase(dev);
+}
 
 using namespace ccl;
 
@@ -63,46 +74,22 @@ extern "C" ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, 
                                                        size_t count, ccl_dtype_t dtype, ccl_op_t op,
                                                        cudaStream_t stream)
 {
-    if (nranks < 1 || nranks > CCL_MAX_RANKS || (dtype != CCL_FP32 && dtype != CCL_BF16) ||
-        (op != CCL_SUM && op != CCL_AVG && op != CCL_MAX && op != CCL_PROD && op != CCL_MIN &&
-         op != CCL_AVG_PREMUL) || !send || !recv)
-        return CCL_ERR_INVALID_ARG;
-    const size_t es = dtype == CCL_BF16 ? 2 : 4;
-    if (count > SIZE_MAX / es)
-        return CCL_ERR_INVALID_ARG;
+    // the same checks, in the same order, as ccl_reduce_scatter
+    std::vector<Range> w, r;
+    ccl_status_t st = check_reduce_scatter(send, recv, nranks, count, dtype, op, w, r);
+    if (st != CCL_OK)
+        return st;
+    const size_t es = elem_size(dtype);
     // each rank's working copy starts on a 256-byte boundary
     const size_t stride = (count * es + 255) & ~(size_t)255;
     if (stride < count * es || stride > CCL_STATIC_SCRATCH_BYTES / (size_t)nranks)
         return CCL_ERR_INVALID_ARG; // more than the fixed working space holds
-    if (count == 0)
-        return CCL_OK;
-    Partition part;
-    part.q = count / (uint64_t)nranks;
-    part.rem = (uint32_t)(count % (uint64_t)nranks);
-    // outputs pairwise disjoint; an output may sit inside its own rank's input
-    // only at that rank's chunk offset (the in-place form)
-    for (int i = 0; i < nranks; ++i)
-        if (!send[i] || (!recv[i] && part.len((uint32_t)i) > 0))
-            return CCL_ERR_INVALID_ARG;
-    for (int i = 0; i < nranks; ++i) {
-        const uintptr_t w0 = (uintptr_t)recv[i], w1 = w0 + part.len((uint32_t)i) * es;
-        if (w0 == w1)
-            continue;
-        for (int j = 0; j < nranks; ++j) {
-            const uintptr_t r0 = (uintptr_t)send[j], r1 = r0 + count * es;
-            if (overlaps(w0, w1, r0, r1) && !(i == j && w0 == r0 + part.off((uint32_t)i) * es))
-                return CCL_ERR_OVERLAP;
-            if (j != i) {
-                const uintptr_t v0 = (uintptr_t)recv[j], v1 = v0 + part.len((uint32_t)j) * es;
-                if (v0 != v1 && overlaps(w0, w1, v0, v1))
-                    return CCL_ERR_OVERLAP;
-            }
-        }
-    }
     void *base = nullptr;
-    ccl_status_t st = scratch_address(&base);
-    if (st != CCL_OK)
+    if ((st = scratch_address(&base)) != CCL_OK)
         return st;
+    if (count == 0)
+        return CCL_OK; // the set-up call: array reserved, kernels loaded, nothing enqueued
+    const Partition part = make_partition(count, nranks);
     std::vector<void *> bufs(nranks);
     for (int i = 0; i < nranks; ++i)
         bufs[i] = static_cast<char *>(base) + (size_t)i * stride;
@@ -111,10 +98,8 @@ extern "C" ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, 
         for (int i = 0; i < nranks; ++i) {
             rg.push_back(DbgRange{send[i], count * es});
             rg.push_back(DbgRange{bufs[i], count * es});
+            rg.push_back(DbgRange{recv[i], part.len((uint32_t)i) * es});
         }
-        const uint64_t q = count / (uint64_t)nranks, rem = count % (uint64_t)nranks;
-        for (int i = 0; i < nranks; ++i)
-            rg.push_back(DbgRange{recv[i], (size_t)(q + ((uint64_t)i < rem ? 1 : 0)) * es});
         if (dbg_set_ranges(rg, stream) != cudaSuccess)
             return CCL_ERR_CUDA;
     }
@@ -130,7 +115,7 @@ extern "C" ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, 
             return CCL_ERR_CUDA;
     // AVG divides once at the end; the pre-multiplied AVG scales inside the
     // steps, and needs this launch only when N = 1 gives it no step
-    if ((op == CCL_AVG || (op == CCL_AVG_PREMUL && nranks == 1)) &&
+    if (step_scale((int)op, nranks) &&
         launch_ring_step((int)dtype, (int)op, STEP_SCALE, 0, bufs.data(), nranks, count, stream) != cudaSuccess)
         return CCL_ERR_CUDA;
     // the ReduceScatter phase leaves chunk c finished at rank c-1; hand it to rank c

@@ -166,6 +166,33 @@ static cudaError_t launch_step_dt(int op, int kind, int s, void *const *bufs, in
     return cudaErrorInvalidValue;
 }
 
+// Loads every ring-step kernel into the current device's context now rather
+// than at its first launch (CUDA's default lazy loading), so that a later
+// launch needs no device memory for code.
+template <int DT, int OP> static cudaError_t preload_step_op()
+{
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, ring_step_kernel<DT, OP, kSmallRanks>);
+    return e != cudaSuccess ? e : cudaFuncGetAttributes(&a, ring_step_kernel<DT, OP, kMaxRanks>);
+}
+
+template <int DT> static cudaError_t preload_step_dt()
+{
+    const cudaError_t e[] = {preload_step_op<DT, OP_SUM>(), preload_step_op<DT, OP_AVG>(),
+                             preload_step_op<DT, OP_MAX>(), preload_step_op<DT, OP_PROD>(),
+                             preload_step_op<DT, OP_MIN>(), preload_step_op<DT, OP_AVGP>()};
+    for (cudaError_t x : e)
+        if (x != cudaSuccess)
+            return x;
+    return cudaSuccess;
+}
+
+cudaError_t preload_ring_step_kernels()
+{
+    const cudaError_t e = preload_step_dt<DT_FP32>();
+    return e != cudaSuccess ? e : preload_step_dt<DT_BF16>();
+}
+
 // Elements each rank has sent in ring steps launched by this thread (Lesson 3's
 // per-rank traffic counter): at ReduceScatter step s rank j sends chunk
 // (j - s) mod N, at AllGather step s chunk (j + 1 - s) mod N, and in the
