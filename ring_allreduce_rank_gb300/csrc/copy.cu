@@ -173,6 +173,24 @@ cudaError_t preload_copy_kernels()
 
 // ------------------------------------------------------------------ fan-out (AllGather, Broadcast)
 
+// 32-byte vector load / store (sm_100 and later); p must be 32-byte aligned
+__device__ __forceinline__ void ld32(const void *p, uint4 &a, uint4 &b)
+{
+    a = b = make_uint4(0, 0, 0, 0);
+    if (dbg_ok(p, 32))
+        asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                     : "l"(p));
+}
+
+__device__ __forceinline__ void st32(void *p, const uint4 &a, const uint4 &b)
+{
+    if (dbg_ok(p, 32))
+        asm volatile("st.global.L1::no_allocate.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x),
+                     "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                     : "memory");
+}
+
 template <int MAXR> struct FanoutParams {
     const void *src[MAXR];
     void *dst[MAXR];
@@ -180,6 +198,7 @@ template <int MAXR> struct FanoutParams {
     int nchunks;     // sources (AllGather: N, Broadcast: 1)
     int ndst;
     int vec_aligned; // every pointer 16-byte aligned
+    int vec32;       // every pointer 32-byte aligned
 };
 
 template <int DT, int MAXR>
@@ -266,6 +285,24 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
         }
         return;
     }
+    if (p.vec32 && off % (2 * VEC) == 0) {
+        // 32-byte vectors: one per thread, a warp covering 1 KiB contiguous
+        const uint64_t nw = len / (2 * VEC);
+        if (t == 0)
+            for (uint64_t e = nw * 2 * VEC + threadIdx.x; e < len; e += kThreads) {
+                const uint32_t v = ld_elem<DT>(src, e);
+                for (int q = 0; q < M; ++q)
+                    st_elem<DT>(p.dst[q], off + e, v);
+            }
+        const uint64_t w = (uint64_t)t * kThreads + threadIdx.x;
+        if (w < nw) {
+            uint4 a, b;
+            ld32(static_cast<const char *>(src) + w * 32, a, b);
+            for (int q = 0; q < M; ++q)
+                st32(static_cast<char *>(p.dst[q]) + off * DType<DT>::kSize + w * 32, a, b);
+        }
+        return;
+    }
     const uint64_t nv = len / VEC;
     if (t == 0)
         for (uint64_t e = nv * VEC + threadIdx.x; e < len; e += kThreads) {
@@ -295,20 +332,26 @@ static cudaError_t launch_fanout_t(const void *const *src, int nchunks, void *co
 {
     constexpr int VEC = DType<DT>::kVec;
     FanoutParams<MAXR> p;
-    bool aligned = true;
+    bool aligned = true, aligned32 = true;
     for (int i = 0; i < MAXR; ++i) {
         p.src[i] = i < nchunks ? src[i] : nullptr;
         p.dst[i] = i < ndst ? dst[i] : nullptr;
-        if (i < nchunks)
+        if (i < nchunks) {
             aligned = aligned && (uintptr_t)src[i] % 16 == 0;
-        if (i < ndst)
+            aligned32 = aligned32 && (uintptr_t)src[i] % 32 == 0;
+        }
+        if (i < ndst) {
             aligned = aligned && (uintptr_t)dst[i] % 16 == 0;
+            aligned32 = aligned32 && (uintptr_t)dst[i] % 32 == 0;
+        }
     }
     p.part.q = count / (uint64_t)nchunks;
     p.part.rem = (uint32_t)(count % (uint64_t)nchunks);
     p.nchunks = nchunks;
     p.ndst = ndst;
     p.vec_aligned = aligned ? 1 : 0;
+    p.vec32 = aligned32 ? 1 : 0;
+    // a tile: kThreads x 32 bytes (two 16-byte vectors per thread, or one 32-byte one)
     const uint64_t te = (uint64_t)kThreads * 2 * VEC;
     uint64_t tiles = (p.part.q + 1 + te - 1) / te;
     // A chunk whose offset is not a whole vector takes the shuffle path (one

@@ -305,6 +305,48 @@ def test_broadcast_matches_oracle(N, K, root, dtype, mode):
         assert_bits_equal(bits(out[r]), want[r], "bcast rank %d" % r)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("shift", [0, 16, 32, 4])
+@pytest.mark.parametrize("kind", ["whole32", "whole16", "ragged"])
+def test_fanout_vector_widths(kind, shift, dtype):
+    """The fan-out kernel (Broadcast, AllGather, Gather) moves 32-byte vectors
+    when every buffer starts on a 32-byte boundary and the chunk starts on a
+    whole 32-byte vector, 16-byte vectors when only 16-byte alignment holds,
+    and elements or shifted windows otherwise.  Buffers start `shift` bytes
+    past a 512-byte boundary; the chunk length makes chunk offsets whole
+    32-byte vectors, whole 16-byte vectors only (odd multiples), or ragged."""
+    es = 2 if dtype == "bf16" else 4
+    vec = 16 // es
+    N = 8
+    per = {"whole32": 2 * vec * 300, "whole16": 2 * vec * 300 + vec, "ragged": 2 * vec * 300 + 3}[kind]
+    K = N * per + (5 if kind == "ragged" else 0)
+    pad = shift // es
+    x = inputs(dtype, N, K, seed=K + shift)
+    tdt = torch_dtype(x)
+    # Broadcast from rank 3, out of place
+    send = [None] * N
+    send[3] = to_dev(x[3], pad_elems=pad)
+    out = [empty_like_host(K, tdt, pad_elems=pad) for _ in range(N)]
+    ccl.ccl_broadcast(send, out, root=3)
+    # AllGather of each rank's chunk
+    off, ln = ccl.ccl_plan_chunks(K, N)
+    chunks = [x[r][off[r]:off[r] + ln[r]].copy() for r in range(N)]
+    cs = [to_dev(c, pad_elems=pad) for c in chunks]
+    ag = [empty_like_host(K, tdt, pad_elems=pad) for _ in range(N)]
+    ccl.ccl_allgather(cs, ag)
+    # Gather to rank 5
+    g = [None] * N
+    g[5] = empty_like_host(K, tdt, pad_elems=pad)
+    ccl.ccl_gather(cs, g, root=5)
+    torch.cuda.synchronize()
+    want_b = oracle.broadcast(x, 3)
+    want_ag = oracle.allgather(chunks, K)
+    for r in range(N):
+        assert_bits_equal(bits(out[r]), want_b[r], "bcast rank %d" % r)
+        assert_bits_equal(bits(ag[r]), want_ag[r], "allgather rank %d" % r)
+    assert_bits_equal(bits(g[5]), oracle.gather(chunks, K), "gather")
+
+
 # ------------------------------------------------------------------ AllToAll(v)
 
 @pytest.mark.parametrize("mode", ["fused", "step"])
