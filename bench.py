@@ -425,33 +425,49 @@ def run_row(args, name, local):
             else:
                 bk.reset()
                 backward(True)
+            # b: the last gradient is ready; c: the last bucket is reduced
             b.record(compute)
             c.record(comm)
             torch.cuda.synchronize(dev)
-            return max(a.elapsed_time(b), a.elapsed_time(c))
+            tb_, tc_ = a.elapsed_time(b), a.elapsed_time(c)
+            return max(tb_, tc_), max(0.0, tc_ - tb_)
 
         def timed(kind):
             for _ in range(2):
                 run(kind)
-            return statistics.median(run(kind) for _ in range(max(3, min(args.steps, 10))))
+            rs = [run(kind) for _ in range(max(3, min(args.steps, 10)))]
+            return statistics.median(r[0] for r in rs), statistics.median(r[1] for r in rs)
 
-        tb, tar = timed("backward"), timed("allreduce")
-        caps = {}
-        for cap in (0, sms // 4, sms // 2, sms):  # CTAs a bucket kernel may hold
-            bk = ccl.CclBucketer(grads, bucket_bytes=25 * W.MiB, op="sum", max_ctas=cap)
-            caps[cap] = timed("overlap")
-            bk.close()
-        best = min(caps, key=caps.get)
-        to = caps[best]
+        tb, tar = timed("backward")[0], timed("allreduce")[0]
+        # bucket-size policies (Collective Communication, "Bucket fusion": 5-10 MB
+        # start communicating earlier, 50-100 MB amortise the per-bucket cost, 25 MB
+        # is PyTorch's reference point), each with the bucket kernels' CTA cap that
+        # gives the shortest step
+        policies = {}
+        for mib in (5, 10, 25, 50, 100):
+            res = {}
+            for cap in (0, sms // 2, sms):  # CTAs a bucket kernel may hold (0: no cap)
+                bk = ccl.CclBucketer(grads, bucket_bytes=mib * W.MiB, op="sum", max_ctas=cap)
+                nb = bk.status()[0]
+                res[cap] = timed("overlap")
+                bk.close()
+            best = min(res, key=lambda c_: res[c_][0])
+            policies[mib] = {"buckets": nb, "bucket_kernel_max_ctas": best,
+                             "overlapped_ms": round(res[best][0], 3), "exposed_tail_ms": round(res[best][1], 3),
+                             "overlapped_ms_by_max_ctas": {str(k_): round(v[0], 3) for k_, v in res.items()}}
+        to = policies[25]["overlapped_ms"]
         alg = 2 * N * sum(numels) * 2
         d = line("Bucket AllReduce overlapped with a synthetic backward, N=8 bf16 4 Llama layers, 1 GB300", alg,
                  [tar], 62, "bucket_reduce_kernel<bf16, SUM, 8> per bucket", "bf16",
                  {"nranks": N, "tokens": TOK, "buckets": 62},
-                 {"overlap": {"backward_ms": round(tb, 3), "allreduce_ms": round(tar, 3), "overlapped_ms": round(to, 3),
+                 {"overlap": {"backward_ms": round(tb, 3), "allreduce_ms": round(tar, 3), "overlapped_ms": to,
                               "exposed_comm_ms": round(max(to - tb, 0.0), 3),
+                              "exposed_tail_ms": policies[25]["exposed_tail_ms"],
                               "hidden_fraction": round(min(1.0, max(0.0, (tb + tar - to) / tar)), 4),
-                              "bucket_kernel_max_ctas": best,
-                              "overlapped_ms_by_max_ctas": {str(k): round(v, 3) for k, v in caps.items()}}})
+                              "bucket_kernel_max_ctas": policies[25]["bucket_kernel_max_ctas"],
+                              "exposed_tail": "time from the last gradient's ready event to the last bucket's "
+                                              "completion (the optimizer's wait)",
+                              "policies_by_bucket_mib": {str(k_): v for k_, v in policies.items()}}})
         print(json.dumps(d))
         return
 
@@ -485,7 +501,8 @@ def run_row(args, name, local):
         alg = N * K * (2 + 4) + N * K * (2 + 4 + 4 + 2)
         print(json.dumps(line("Top-k AllReduce (1%% kept + error feedback) HBM GB/s of the %d-byte minimum, N=8 bf16 "
                               "%d MB/rank, 1 GB300" % (alg, K * 2 // 2**20), alg, per, launches,
-                              "whole step: topk_init, topk_top_kernel + scan, topk_low_kernel + 2 scans, "
+                              "whole step: topk_init, topk_sample (+ window), topk_main (+ window check), two "
+                              "fallback passes (return at once after a hit), topk_low_sum (+ scan), "
                               "compressed_pipe_kernel<bf16, 4, TOPK>", "bf16",
                               {"nranks": N, "count": K, "k": kk}, {"clocks": clk}, total_ms=tot)))
         return
@@ -539,8 +556,22 @@ def run_row(args, name, local):
         clocks.start()
         tot, per, launches = _timed(torch, ccl, step, args.steps, args.warmup, stream, dev)
         clk = clocks.stop()
+        extra = {"clocks": clk}
+        if name != "reduce":
+            # a short call pays a fixed ramp and drain: the runtime's own device
+            # copy of the same bytes (cudaMemcpyAsync), timed the same way, is the
+            # roofline a call of this size can reach
+            src = torch.empty(K, dtype=torch.bfloat16, device=dev)
+            dst = torch.empty(K, dtype=torch.bfloat16, device=dev)
+            _, cper, _ = _timed(torch, ccl, lambda: dst.copy_(src), args.steps, args.warmup, stream, dev)
+            cgbs = alg * len(cper) / (sum(cper) / 1e3) / 1e9
+            ach = alg * len(per) / (sum(per) / 1e3) / 1e9
+            extra["same_size_copy"] = {"GBs": round(cgbs, 1), "frac": round(ach / cgbs, 4),
+                                       "what": "torch copy_ (cudaMemcpyAsync device to device) of the same %d bytes, "
+                                               "per-launch CUDA-event time" % (K * 2)}
+            del src, dst
         print(json.dumps(line(metric, alg, per, launches, kernel, "bf16", {"nranks": N, "count": K},
-                              {"clocks": clk}, total_ms=tot)))
+                              extra, total_ms=tot)))
         return
 
     if name in ("reduce-scatter", "allgather"):

@@ -27,13 +27,16 @@ def _grads(N, numels, seed):
     return [[W.normal_bf16(1, n, seed_base=seed + 97 * r + t)[0] for t, n in enumerate(numels)] for r in range(N)]
 
 
+@pytest.mark.parametrize("be", [10000, 2500, 60000])
 @pytest.mark.parametrize("max_ctas", [0, 3])
 @pytest.mark.parametrize("order", ["backward", "forward", "shuffled"])
 @pytest.mark.parametrize("op", ["sum", "avg"])
-def test_bucketer_matches_oracle_over_two_steps(order, op, max_ctas):
+def test_bucketer_matches_oracle_over_two_steps(order, op, max_ctas, be):
+    """Bucket sizes from many small buckets (a bucket per few thousand
+    elements) to few large ones, the bucket-size policies the overlap
+    benchmark compares."""
     N = 4
     numels = [5000, 20000, 3, 70001, 4096, 1]
-    be = 10000
     dev_grads = [[torch.empty(n, dtype=torch.bfloat16, device=DEV) for n in numels] for _ in range(N)]
     bk = ccl.CclBucketer(dev_grads, bucket_bytes=be * 2, op=op, max_ctas=max_ctas)
     nb, _ = bk.status()
