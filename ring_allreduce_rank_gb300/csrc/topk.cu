@@ -75,12 +75,22 @@ struct TopkParams {
 
 __device__ __forceinline__ uint32_t topk_key(float g, float e) { return __float_as_uint(__fadd_rn(g, e)) & 0x7fffffffu; }
 
+// g and e stream through L2 once: streaming loads (evict first) leave the
+// low histograms, which the window's keys count into, resident in L2.
+template <class T> __device__ __forceinline__ T gload_stream(const T *p)
+{
+    T v{};
+    if (dbg_ok(p, sizeof(T)))
+        v = __ldcs(p);
+    return v;
+}
+
 // u = g + e for the 8 elements of group gi (16-byte loads; vec_ok buffers).
 template <int DT, class F> __device__ __forceinline__ void group_keys(const void *g, const float *e, uint64_t gi, F &&f)
 {
     float gv[8];
     if (DT == DT_BF16) {
-        const uint4 w = gload<uint4>(static_cast<const uint16_t *>(g) + gi * 8);
+        const uint4 w = gload_stream(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g) + gi * 8));
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -88,12 +98,13 @@ template <int DT, class F> __device__ __forceinline__ void group_keys(const void
             gv[2 * j + 1] = __uint_as_float(ws[j] & 0xffff0000u);
         }
     } else {
-        const float4 a = gload<float4>(static_cast<const float *>(g) + gi * 8);
-        const float4 b = gload<float4>(static_cast<const float *>(g) + gi * 8 + 4);
+        const float4 a = gload_stream(reinterpret_cast<const float4 *>(static_cast<const float *>(g) + gi * 8));
+        const float4 b = gload_stream(reinterpret_cast<const float4 *>(static_cast<const float *>(g) + gi * 8 + 4));
         gv[0] = a.x; gv[1] = a.y; gv[2] = a.z; gv[3] = a.w;
         gv[4] = b.x; gv[5] = b.y; gv[6] = b.z; gv[7] = b.w;
     }
-    const float4 ea = gload<float4>(e + gi * 8), eb = gload<float4>(e + gi * 8 + 4);
+    const float4 ea = gload_stream(reinterpret_cast<const float4 *>(e + gi * 8)),
+                 eb = gload_stream(reinterpret_cast<const float4 *>(e + gi * 8 + 4));
     const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j)

@@ -101,45 +101,58 @@ def test_unaligned_buffers(dtype, pad):
     _check(got_g, got_e, want_g, want_e, "unaligned pad %d" % pad)
 
 
-def _window_hits(work, N):
+def _window_record(work, N):
     """The select's per-rank record in the work buffer (the layout of
     topk.cu: top u64[N][2048], sample u32[N][2048], low u32[N][3][2^20],
-    block sums u64[N][256], then one 32-byte record per rank whose 7th word
-    says whether the sampled window held the k-th key's top bin)."""
+    block sums u64[N][256], then one 32-byte record per rank whose 5th word
+    is the window's first top digit (all ones when the sample placed none)
+    and whose 7th says whether the window held the k-th key's top digit).
+    Returns (hit, window placed) per rank."""
     off = N * (2048 * 8 + 2048 * 4 + 3 * (1 << 20) * 4 + 256 * 8)
     rec = work[off:off + 32 * N].cpu().numpy().view(np.uint32).reshape(N, 8)
-    return rec[:, 6].tolist()
+    return rec[:, 6].tolist(), [int(w != 0xFFFFFFFF) for w in rec[:, 4].tolist()]
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-def test_sampled_window_hit_and_miss(dtype):
-    """Both ways through the select give the oracle's bits.  Normal data: the
-    1/16 sample places the window on the k-th key's top bin (one full pass).
-    Data whose sampled runs (the first 256 elements of every 4096) hold tiny
-    values: the window lands far below the k-th key and the fallback pass
-    counts the right bin."""
+def test_sampled_window_hit_miss_and_none(dtype):
+    """Every way through the select gives the oracle's bits.
+    - Normal data: the 1/16 sample places a window of two top digits on the
+      k-th key's (one full pass; hit).
+    - Zero residuals and sampled runs (the first 256 elements of every 4096)
+      that all hold +-1e-6: the sample puts the window on that one digit, far
+      below the k-th key; the fallback pass counts the right digit (miss).
+    - Sampled runs whose values spread over many binades: the sample's bounds
+      fall more than one digit apart, no window is placed, and the fallback
+      pass counts the k-th key's digit."""
     N, K, k = 4, 1 << 20, 10_486
     base = _grads(dtype, N, K, seed=123)
-    if dtype == "bf16":
-        base = [W.to_bf16_bits(W.bf16_bits_to_f32(r)) for r in base]
-    rigged = []
     idx = np.arange(K)
     sampled = (idx // 256) % 16 == 0
-    for r in range(N):
-        x = (W.bf16_bits_to_f32(base[r]) if dtype == "bf16" else base[r]).copy()
-        x[sampled] = np.float32(1e-6) * np.sign(x[sampled])
-        rigged.append(W.to_bf16_bits(x) if dtype == "bf16" else x.astype(np.float32))
+    g = np.random.Generator(np.random.PCG64(77))
+
+    def rig(fill):
+        out = []
+        for r in range(N):
+            x = (W.bf16_bits_to_f32(base[r]) if dtype == "bf16" else base[r]).copy()
+            x[sampled] = fill(int(sampled.sum()))
+            out.append(W.to_bf16_bits(x) if dtype == "bf16" else x.astype(np.float32))
+        return out
+
+    normal = list(W.normal_bf16(N, K, seed_base=5)) if dtype == "bf16" else list(W.normal_fp32(N, K, seed_base=5))
+    tiny = rig(lambda n: np.where(g.random(n) < 0.5, -1e-6, 1e-6).astype(np.float32))
+    spread = rig(lambda n: (np.exp2(g.uniform(-60, 60, n)) * np.where(g.random(n) < 0.5, -1, 1)).astype(np.float32))
+    zeros = [np.zeros(K, np.float32) for _ in range(N)]
     work = torch.empty(ccl.ccl_plan_topk_work_bytes(N), dtype=torch.uint8, device=DEV)
-    for data, expect_hit in ((list(W.normal_bf16(N, K, seed_base=5)) if dtype == "bf16"
-                              else list(W.normal_fp32(N, K, seed_base=5)), 1), (rigged, 0)):
-        e = _res(N, K, seed=9)
+    for name, data, e, want_rec in (("hit", normal, _res(N, K, seed=9), (1, 1)), ("miss", tiny, zeros, (0, 1)),
+                                    ("no window", spread, zeros, (0, 0))):
         want_g, want_e = oracle.allreduce_compressed(data, e, "avg", "topk", k=k)
-        g = [to_dev(x) for x in data]
+        gd = [to_dev(x) for x in data]
         ed = [to_dev(x) for x in e]
-        ccl.ccl_allreduce_topk(g, ed, k, op="avg", work=work)
+        ccl.ccl_allreduce_topk(gd, ed, k, op="avg", work=work)
         torch.cuda.synchronize()
-        assert _window_hits(work, N) == [expect_hit] * N
-        _check([bits(x) for x in g], [bits(x) for x in ed], want_g, want_e, "window hit=%d" % expect_hit)
+        hit, placed = _window_record(work, N)
+        assert (hit, placed) == ([want_rec[0]] * N, [want_rec[1]] * N), name
+        _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, name)
 
 
 def test_nan_is_sent_first():
