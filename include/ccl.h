@@ -375,7 +375,15 @@ ccl_status_t ccl_reduce_scatter_step_static(const void *const *send, void *const
  * each, any memory the GPU can copy from and to (cudaMemcpyDefault); page-
  * locked host memory (cudaHostAlloc, cudaHostRegister) is what makes the
  * copies asynchronous and overlapped.  In place when send[r] == recv[r].
- * The vector moves through `work` (DEVICE memory, caller-owned, 16-byte
+ * Two paths give the same bits:
+ *   - in place over the host link, when CCL_HOST_PATH=direct (or
+ *     ccl_set_host_path(CCL_HOST_PATH_DIRECT)) and every send[r] and recv[r]
+ *     is page-locked host memory that the current device can address: one
+ *     fused AllReduce launch on `stream` reads and writes them directly
+ *     (both link directions busy at once, nothing staged; `work` is
+ *     validated but not used);
+ *   - staged, the default, and for any other memory:
+ * the vector moves through `work` (DEVICE memory, caller-owned, 16-byte
  * aligned, work_bytes >= 3 * nranks * 256 * element size; larger is faster,
  * up to CCL_HOST_WORK_BYTES_DEFAULT) in slices: copies in and out run on two
  * library-owned streams so that both directions of the host link are busy at
@@ -474,6 +482,12 @@ void ccl_trace_clear(void);
  *   CCL_BUCKET_MB=<MiB>, a positive decimal number (e.g. 25 or 0.5): the
  *     bucket size of ccl_bucket_allreduce and ccl_bucketer_create calls that
  *     pass bucket_bytes = 0; at least 4 bytes, at most 1 TiB.
+ *   CCL_HOST_PATH=staged|direct: how ccl_allreduce_host moves its buffers.
+ *     staged (the default): slices go through the caller's work buffer.
+ *     direct: when every buffer is page-locked host memory that the device
+ *     can address (cudaHostAlloc, cudaHostRegister), one fused launch reads
+ *     and writes them in place over the host link; other memory is staged.
+ *     ccl_set_host_path replaces it.
  *   CCL_TRACE, CCL_CHECK: ccl_set_trace, ccl_set_check.
  * A value that cannot be read is ignored (the default stays) with one line on
  * stderr.  The settings are process-wide and may be changed at any time; a
@@ -482,7 +496,7 @@ typedef struct {
     int mode_override;           /* -1: none; else CCL_MODE_FUSED or CCL_MODE_STEP */
     int trace;                   /* 1 when call tracing is on */
     int check;                   /* 1 when automatic result checks are on */
-    int reserved;                /* 0 */
+    int host_path;               /* CCL_HOST_PATH_STAGED or CCL_HOST_PATH_DIRECT */
     size_t default_bucket_bytes; /* the bucket size that bucket_bytes = 0 selects */
 } ccl_config_t;
 
@@ -495,6 +509,13 @@ ccl_status_t ccl_set_mode_override(int mode);
 /* bytes >= 4 sets the default bucket size; 0 restores 25 MiB
  * (CCL_DEFAULT_BUCKET_BYTES); 1 to 3: CCL_ERR_INVALID_ARG, nothing changed. */
 ccl_status_t ccl_set_default_bucket_bytes(size_t bytes);
+/* ccl_allreduce_host's path: CCL_HOST_PATH_STAGED (through the work buffer)
+ * or CCL_HOST_PATH_DIRECT (in place over the host link when every buffer
+ * allows it, else staged).  Anything else: CCL_ERR_INVALID_ARG, nothing
+ * changed. */
+#define CCL_HOST_PATH_STAGED 0
+#define CCL_HOST_PATH_DIRECT 1
+ccl_status_t ccl_set_host_path(int path);
 
 /* ------------------------------------------------------------------ */
 /* Planner (host only; no GPU needed)                                  */

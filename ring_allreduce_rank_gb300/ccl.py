@@ -36,7 +36,7 @@ _lib = None
 class Config(ctypes.Structure):
     """ccl_config_t."""
     _fields_ = [("mode_override", ctypes.c_int), ("trace", ctypes.c_int), ("check", ctypes.c_int),
-                ("reserved", ctypes.c_int), ("default_bucket_bytes", ctypes.c_size_t)]
+                ("host_path", ctypes.c_int), ("default_bucket_bytes", ctypes.c_size_t)]
 
 
 class CclError(RuntimeError):
@@ -119,6 +119,8 @@ def lib() -> ctypes.CDLL:
             L.ccl_set_mode_override.restype = ctypes.c_int
             L.ccl_set_default_bucket_bytes.argtypes = [sz]
             L.ccl_set_default_bucket_bytes.restype = ctypes.c_int
+            L.ccl_set_host_path.argtypes = [i32]
+            L.ccl_set_host_path.restype = ctypes.c_int
             L.ccl_status_string.argtypes = [ctypes.c_int]
             L.ccl_status_string.restype = ctypes.c_char_p
             L.ccl_version.argtypes = []
@@ -395,18 +397,32 @@ def ccl_step_sent(nranks: int, reset: bool = True) -> list:
 
 def ccl_get_config() -> dict:
     """The library's settings: mode override ("fused", "step" or None),
-    trace, check, default bucket bytes."""
+    trace, check, default bucket bytes, the host-buffer AllReduce's path
+    ("staged" or "direct")."""
     c = Config()
     _check(lib().ccl_get_config(ctypes.byref(c)), "ccl_get_config")
     names = {v: k for k, v in MODES.items()}
     return {"mode_override": names.get(c.mode_override), "trace": bool(c.trace), "check": bool(c.check),
-            "default_bucket_bytes": int(c.default_bucket_bytes)}
+            "default_bucket_bytes": int(c.default_bucket_bytes),
+            "host_path": {v: k for k, v in HOST_PATHS.items()}.get(c.host_path, c.host_path)}
 
 
 def ccl_set_mode_override(mode: Optional[str]) -> None:
     """Force "fused" or "step" on every call that takes a mode; None removes
     the override."""
     _check(lib().ccl_set_mode_override(-1 if mode is None else _mode(mode)), "ccl_set_mode_override")
+
+
+HOST_PATHS = {"staged": 0, "direct": 1}
+
+
+def ccl_set_host_path(path: str) -> None:
+    """ccl_allreduce_host's path: "staged" (the default) or "direct" (in
+    place over the host link when every buffer is page-locked host memory,
+    else staged)."""
+    if path not in HOST_PATHS:
+        raise ValueError("host path must be 'staged' or 'direct', not %r" % (path,))
+    _check(lib().ccl_set_host_path(HOST_PATHS[path]), "ccl_set_host_path")
 
 
 def ccl_set_default_bucket_bytes(nbytes: int) -> None:

@@ -111,6 +111,32 @@ ccl_status_t dbg_call(const std::vector<Range> &a, const std::vector<Range> &b, 
     } while (0)
 #endif
 
+// The device's addresses of page-locked host buffers (cudaHostAlloc,
+// cudaHostRegister) on the current device; false if any buffer is other
+// memory (pageable, device, managed) or has no such address.
+bool device_views(const void *const *send, void *const *recv, int nranks, const void **ds, void **dr)
+{
+    auto view = [](const void *p, void **out) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        *out = a.devicePointer;
+        return a.type == cudaMemoryTypeHost && a.devicePointer != nullptr;
+    };
+    for (int i = 0; i < nranks; ++i) {
+        void *v = nullptr;
+        if (!view(send[i], &v))
+            return false;
+        ds[i] = v;
+        if (!view(recv[i], &v))
+            return false;
+        dr[i] = v;
+    }
+    return true;
+}
+
 } // namespace
 
 ccl_status_t check_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
@@ -927,9 +953,26 @@ static ccl_status_t ccl_allreduce_host_impl(const void *const *send, void *const
         return CCL_ERR_CUDA;
     if (cap != cudaStreamCaptureStatusNone)
         return CCL_ERR_UNSUPPORTED;
-    CCL_DBG(w, r, {}, stream);
     if (nranks == 1 && in_place && !scales(op))
         return CCL_OK;
+    // On request, page-locked host buffers that the device can address: the
+    // fused kernel reads and writes them in place over the host link, both
+    // directions at once, with no staging memory.  Other memory is staged.
+    std::vector<const void *> ds(nranks);
+    std::vector<void *> dr(nranks);
+    if (host_path() == CCL_HOST_PATH_DIRECT && device_views(send, recv, nranks, ds.data(), dr.data())) {
+#ifdef CCL_DEBUG_BOUNDS
+        std::vector<Range> dw, drd; // the kernel touches the device's addresses of the buffers
+        for (int i = 0; i < nranks; ++i) {
+            dw.push_back(range_of(dr[i], bytes, i));
+            drd.push_back(range_of(ds[i], bytes, i));
+        }
+        CCL_DBG(dw, drd, {}, stream);
+#endif
+        return from_cuda(launch_fused_reduce((int)dtype, (int)op, ds.data(), dr.data(), nranks, count, WRITE_ALL, 0,
+                                             stream));
+    }
+    CCL_DBG(w, r, {}, stream);
     return from_cuda(run_host_allreduce((int)dtype, (int)op, send, recv, nranks, count, work, work_bytes, stream));
 }
 

@@ -234,6 +234,9 @@ ccl_mode_t effective_mode(ccl_mode_t requested);
 // Bucket size used when a call passes bucket_bytes = 0 (CCL_BUCKET_MB /
 // ccl_set_default_bucket_bytes, else CCL_DEFAULT_BUCKET_BYTES).
 size_t default_bucket_bytes();
+// ccl_allreduce_host's path: CCL_HOST_PATH_STAGED or CCL_HOST_PATH_DIRECT
+// (CCL_HOST_PATH / ccl_set_host_path).
+int host_path();
 // Whether automatic result checks and call tracing are on.
 bool check_enabled();
 bool trace_enabled();

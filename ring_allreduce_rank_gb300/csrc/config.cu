@@ -11,6 +11,9 @@
 //                        by step, without changing its calls;
 //   CCL_BUCKET_MB=<MiB>  the bucket size of bucket AllReduce calls that pass
 //                        bucket_bytes = 0;
+//   CCL_HOST_PATH=staged|direct  whether the host-buffer AllReduce stages
+//                        slices through device memory (staged) or may work on
+//                        page-locked host buffers in place (direct);
 //   CCL_TRACE, CCL_CHECK (check.cu).
 // Each is read once, on first use; the setters replace what was read.
 #include <atomic>
@@ -34,7 +37,9 @@ constexpr unsigned long long kBucketUnread = 0;
 // the whole gradient stream behaves like one bucket anyway).
 constexpr double kMaxBucketMiB = 1024.0 * 1024.0;
 
+constexpr int kHostPathUnread = -1;
 std::atomic<int> g_mode{kModeUnread};
+std::atomic<int> g_host_path{kHostPathUnread};
 std::atomic<unsigned long long> g_bucket{kBucketUnread};
 
 int mode_from_env()
@@ -67,6 +72,17 @@ unsigned long long bucket_from_env()
     return (unsigned long long)bytes;
 }
 
+int host_path_from_env()
+{
+    const char *e = std::getenv("CCL_HOST_PATH");
+    if (!e || !e[0] || strcasecmp(e, "staged") == 0)
+        return CCL_HOST_PATH_STAGED;
+    if (strcasecmp(e, "direct") == 0)
+        return CCL_HOST_PATH_DIRECT;
+    std::fprintf(stderr, "ccl: ignoring CCL_HOST_PATH=%s (expected staged or direct)\n", e);
+    return CCL_HOST_PATH_STAGED;
+}
+
 int mode_override()
 {
     int v = g_mode.load(std::memory_order_relaxed);
@@ -86,6 +102,17 @@ ccl_mode_t effective_mode(ccl_mode_t requested)
         return requested;
     const int v = mode_override();
     return v == kModeNone ? requested : (ccl_mode_t)v;
+}
+
+int host_path()
+{
+    int v = g_host_path.load(std::memory_order_relaxed);
+    if (v == kHostPathUnread) {
+        int expected = kHostPathUnread;
+        g_host_path.compare_exchange_strong(expected, host_path_from_env(), std::memory_order_relaxed);
+        v = g_host_path.load(std::memory_order_relaxed);
+    }
+    return v;
 }
 
 size_t default_bucket_bytes()
@@ -114,6 +141,15 @@ ccl_status_t ccl_get_config(ccl_config_t *out)
     out->trace = trace_enabled() ? 1 : 0;
     out->check = check_enabled() ? 1 : 0;
     out->default_bucket_bytes = default_bucket_bytes();
+    out->host_path = host_path();
+    return CCL_OK;
+}
+
+ccl_status_t ccl_set_host_path(int path)
+{
+    if (path != CCL_HOST_PATH_STAGED && path != CCL_HOST_PATH_DIRECT)
+        return CCL_ERR_INVALID_ARG;
+    g_host_path.store(path, std::memory_order_relaxed);
     return CCL_OK;
 }
 

@@ -4,7 +4,7 @@
  * every expected value is a plain integer sum computed here.
  *   1. AllReduce SUM (fused) on device buffers, in place.
  *   2. ReduceScatter then AllGather, out of place: the same bits as 1.
- *   3. The host-buffer AllReduce on page-locked host buffers.
+ *   3. The host-buffer AllReduce on page-locked host buffers, on both paths.
  *   4. Argument errors come back as status codes, before any launch.
  * Prints "c abi ok" and exits 0 when every check holds.
  */
@@ -67,24 +67,30 @@ int main(void)
             return fail("ReduceScatter + AllGather result");
     }
 
-    /* 3: page-locked host rank buffers, staged through a small work buffer */
+    /* 3: page-locked host rank buffers, staged through a small work buffer
+     * (the default path), then in place over the host link */
     void *hs[NR], *work = NULL;
     const size_t work_bytes = (size_t)3 * NR * 1024 * sizeof(float);
     CUDA_OK(cudaMalloc(&work, work_bytes));
-    for (int r = 0; r < NR; ++r) {
+    for (int r = 0; r < NR; ++r)
         CUDA_OK(cudaHostAlloc(&hs[r], K * sizeof(float), cudaHostAllocDefault));
-        for (int i = 0; i < K; ++i)
-            ((float *)hs[r])[i] = value(r, i);
-    }
     size_t nslices = 0;
     CCL_OK_(ccl_plan_host_slices(K, NR, CCL_FP32, work_bytes, NULL, NULL, 0, &nslices));
     if (nslices < 2)
         return fail("expected several slices");
-    CCL_OK_(ccl_allreduce_host((const void *const *)hs, hs, NR, K, CCL_FP32, CCL_SUM, work, work_bytes, 0));
-    CUDA_OK(cudaDeviceSynchronize());
-    for (int r = 0; r < NR; ++r)
-        if (memcmp(hs[r], want, K * sizeof(float)) != 0)
-            return fail("host-buffer AllReduce result");
+    for (int path = CCL_HOST_PATH_STAGED; path <= CCL_HOST_PATH_DIRECT; ++path) {
+        for (int r = 0; r < NR; ++r)
+            for (int i = 0; i < K; ++i)
+                ((float *)hs[r])[i] = value(r, i);
+        CCL_OK_(ccl_set_host_path(path));
+        CCL_OK_(ccl_allreduce_host((const void *const *)hs, hs, NR, K, CCL_FP32, CCL_SUM, work, work_bytes, 0));
+        CUDA_OK(cudaDeviceSynchronize());
+        for (int r = 0; r < NR; ++r)
+            if (memcmp(hs[r], want, K * sizeof(float)) != 0)
+                return fail(path == CCL_HOST_PATH_DIRECT ? "host-buffer AllReduce result (in place)"
+                                                         : "host-buffer AllReduce result (staged)");
+    }
+    CCL_OK_(ccl_set_host_path(CCL_HOST_PATH_STAGED));
 
     /* 4: errors are status codes */
     if (ccl_allreduce((const void *const *)dev, dev, 0, K, CCL_FP32, CCL_SUM, CCL_MODE_FUSED, 0) != CCL_ERR_INVALID_ARG)

@@ -38,9 +38,14 @@ int main(void)
 
     memset(&cfg, 0xff, sizeof cfg);
     check(ccl_get_config(&cfg) == CCL_OK, "get_config");
-    check(cfg.mode_override == -1 && cfg.trace == 0 && cfg.check == 0 && cfg.reserved == 0 &&
+    check(cfg.mode_override == -1 && cfg.trace == 0 && cfg.check == 0 && cfg.host_path == CCL_HOST_PATH_STAGED &&
               cfg.default_bucket_bytes == CCL_DEFAULT_BUCKET_BYTES,
           "default settings");
+    check(ccl_set_host_path(CCL_HOST_PATH_DIRECT) == CCL_OK && ccl_get_config(&cfg) == CCL_OK &&
+              cfg.host_path == CCL_HOST_PATH_DIRECT,
+          "direct host path");
+    check(ccl_set_host_path(7) == CCL_ERR_INVALID_ARG && ccl_set_host_path(CCL_HOST_PATH_STAGED) == CCL_OK,
+          "host path setter validates");
     check(ccl_set_mode_override(CCL_MODE_STEP) == CCL_OK, "force step mode");
     check(ccl_set_default_bucket_bytes(1u << 20) == CCL_OK, "bucket size");
     check(ccl_get_config(&cfg) == CCL_OK && cfg.mode_override == CCL_MODE_STEP &&

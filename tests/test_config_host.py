@@ -1,5 +1,5 @@
-"""Library settings on the host (no GPU): CCL_MODE, CCL_BUCKET_MB, CCL_TRACE
-and CCL_CHECK as read from the environment, the warnings for values that
+"""Library settings on the host (no GPU): CCL_MODE, CCL_BUCKET_MB,
+CCL_HOST_PATH, CCL_TRACE and CCL_CHECK as read from the environment, the warnings for values that
 cannot be read, and the setters that replace them.  Each case runs in a child
 process, because the environment is read once per process; the children see no
 GPU and make no collective call."""
@@ -23,6 +23,12 @@ for step in json.loads(sys.argv[1]):
     try:
         if kind == "mode":
             ccl.ccl_set_mode_override(arg)
+        elif kind == "host":
+            ccl.ccl_set_host_path(arg)
+        elif kind == "host_raw":  # the C setter itself, with any int
+            rc = ccl.lib().ccl_set_host_path(arg)
+            if rc:
+                raise ccl.CclError(rc, "ccl_set_host_path")
         else:
             ccl.ccl_set_default_bucket_bytes(arg)
         out.setdefault("rc", []).append("ok")
@@ -51,7 +57,8 @@ def run_child(env_extra, steps=()):
 
 def test_defaults_without_environment(built):
     out, err = run_child({})
-    assert out["env"] == {"mode_override": None, "trace": False, "check": False, "default_bucket_bytes": 25 * MiB}
+    assert out["env"] == {"mode_override": None, "trace": False, "check": False, "default_bucket_bytes": 25 * MiB,
+                          "host_path": "staged"}
     assert "ignoring" not in err
 
 
@@ -107,3 +114,26 @@ def test_setters_reject_bad_values_and_change_nothing(built):
     out, _ = run_child({"CCL_MODE": "step"}, [["mode", 2], ["mode", -2], ["bucket", 3], ["bucket", 1]])
     assert out["rc"] == [1, 1, 1, 1]  # CCL_ERR_INVALID_ARG each time
     assert out["after"] == out["env"]
+
+
+@pytest.mark.parametrize("value,want", [("staged", "staged"), ("STAGED", "staged"), ("direct", "direct"),
+                                        ("Direct", "direct"), ("", "staged")])
+def test_host_path_from_environment(built, value, want):
+    out, err = run_child({"CCL_HOST_PATH": value})
+    assert out["env"]["host_path"] == want
+    assert "ignoring" not in err
+
+
+@pytest.mark.parametrize("value", ["auto", "1", "stage", " direct"])
+def test_unreadable_host_path_is_ignored_with_a_warning(built, value):
+    out, err = run_child({"CCL_HOST_PATH": value})
+    assert out["env"]["host_path"] == "staged"
+    assert err.count("ignoring CCL_HOST_PATH") == 1
+
+
+def test_host_path_setter(built):
+    out, _ = run_child({"CCL_HOST_PATH": "direct"}, [["host", "staged"]])
+    assert out["env"]["host_path"] == "direct" and out["after"]["host_path"] == "staged"
+    out, _ = run_child({}, [["host_raw", 1], ["host_raw", 2], ["host_raw", -1]])
+    assert out["rc"] == ["ok", 1, 1]  # CCL_ERR_INVALID_ARG, nothing changed
+    assert out["after"]["host_path"] == "direct"

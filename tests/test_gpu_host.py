@@ -1,7 +1,10 @@
 """AllReduce of rank buffers in host memory (ccl_allreduce_host), checked bit
-for bit against the oracle: slices of the vector are copied in, reduced with
-the whole vector's chunk rotation and copied out, so the result must be the
-ring AllReduce of the whole vector, whatever the slicing."""
+for bit against the oracle, on both of its paths: in place over the host link
+(page-locked buffers read and written by the fused kernel) and staged (slices
+copied in, reduced with the whole vector's chunk rotation and copied out, so
+the result must be the ring AllReduce of the whole vector, whatever the
+slicing).  Every test runs with the library's host path set to "staged" (the
+default) and to "direct"."""
 import numpy as np
 import pytest
 import torch
@@ -25,6 +28,13 @@ def _device():
     yield
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
+
+
+@pytest.fixture(autouse=True, params=["staged", "direct"])
+def host_path(request):
+    ccl.ccl_set_host_path(request.param)
+    yield request.param
+    ccl.ccl_set_host_path("staged")
 
 
 def _host(rows, pinned=True):
@@ -187,3 +197,26 @@ def test_host_allreduce_headline_size():
     want, _ = oracle.ring_allreduce(list(x), "avg")
     for r in range(N):
         assert_bits_equal(_host_bits(recv[r]), want[r], "headline host AR rank %d" % r)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_allreduce_path_taken(host_path, pinned):
+    """Page-locked buffers take one fused launch on the "direct" path;
+    pageable buffers, or the "staged" path, take the staged pipeline (many
+    launches: one reduction per slice).  The bits are the oracle's either way."""
+    N, K = 4, 3 * 65_536 + 11
+    x = W.normal_bf16(N, K, std=1e-3, seed_base=17)
+    send = _host(x, pinned=pinned)
+    recv = [torch.empty_like(t).pin_memory() if pinned else torch.empty_like(t) for t in send]
+    work = _stage_work(N, 2, 4096)
+    n0 = ccl.ccl_launch_count()
+    ccl.ccl_allreduce_host(send, recv, op="avg", work=work)
+    torch.cuda.synchronize()
+    launches = ccl.ccl_launch_count() - n0
+    if pinned and host_path == "direct":
+        assert launches == 1
+    else:
+        assert launches > 1
+    want, _ = oracle.ring_allreduce(list(x), "avg")
+    for r in range(N):
+        assert_bits_equal(_host_bits(recv[r]), want[r], "%s pinned=%s rank %d" % (host_path, pinned, r))
