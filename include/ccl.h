@@ -306,12 +306,12 @@ ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residual
  * (CCL_SUM, or CCL_AVG dividing once by N; CCL_AVG_PREMUL returns
  * CCL_ERR_UNSUPPORTED) and rounded once to dtype, written to every grads[r].
  * The threshold is found on the device by a radix select, with no host round
- * trip: a 1/16 sample places a window of two top-11-bit bins, one full pass
- * over g and e counts every key's top bits and the low 20 bits of the keys
+ * trip: a 1/16 sample places a window of one to four top-12-bit bins, one full pass
+ * over g and e counts every key's top bits and the low 19 bits of the keys
  * in the window, and a second full pass runs only when the k-th key's top
  * bin fell outside the window.  One more pass then sends, keeps the
  * residuals and reduces.  work: device memory of ccl_plan_topk_work_bytes
- * bytes (about 12 MiB per rank), 16-byte aligned,
+ * bytes (about 10 MiB per rank), 16-byte aligned,
  * owned by the caller, not shared with a concurrent call; its contents need
  * no initialisation.  Up to 16 ranks and count < 2^32; grads, residuals and
  * work must not overlap (CCL_ERR_OVERLAP).  Launches: one to reset the work

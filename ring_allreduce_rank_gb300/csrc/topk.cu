@@ -5,14 +5,15 @@
 // |u|_(k), every tie included, and keeps the rest as residual.  Magnitudes are
 // ordered as the bit patterns of |u| (the sign bit cleared): for numbers that
 // is the order of |u|, and a NaN lands above every number.  The k-th largest
-// 31-bit key tau is found by a radix select on the top 11 key bits (bits
-// 30..20, a 2048-bin histogram) and then the low 20 bits of the keys in the
-// top bin that holds the k-th key (a 2^20-bin histogram, 4 MB per rank,
+// 31-bit key tau is found by a radix select on the top 12 key bits (bits
+// 30..19, a 4096-bin histogram) and then the low 19 bits of the keys in the
+// top bin that holds the k-th key (a 2^19-bin histogram, 2 MB per rank,
 // resident in L2).  Both histograms come out of ONE full pass over g and e:
 //   1. a sample (one run of 256 elements in every 16) histograms its top
-//      bits, and a scan picks a window of two top bins that holds the k-th
-//      key with high probability (the sample's order statistics k f -+ m,
-//      f the sampled fraction, m five standard deviations of the count);
+//      bits, and a scan picks a window of top bins that holds the k-th key
+//      with high probability: the bins between the sample's order statistics
+//      k f -+ m (f the sampled fraction, m five standard deviations of the
+//      count), at most kWindowMax of them;
 //   2. the full pass counts every key's top bits exactly (shared-memory
 //      atomics per CTA, merged into a 64-bit histogram per rank) and the low
 //      bits of the keys inside the window (global atomics);
@@ -32,13 +33,18 @@
 
 namespace ccl {
 
-constexpr int kTopBins = 2048;          // key bits 30..20
-constexpr int kLowBits = 20;            // key bits 19..0
+// A top digit is 1/16 of a binade: the window's two digits hold few keys (one
+// histogram increment each) and their low histograms stay small, 4 MB per rank.
+constexpr int kTopBins = 4096;          // key bits 30..19
+constexpr int kLowBits = 19;            // key bits 18..0
 constexpr uint32_t kLowBins = 1u << kLowBits;
-constexpr int kLowBlocks = 256;         // a low histogram in blocks of 4096 bins
+constexpr int kLowBlocks = 256;         // a low histogram in blocks of 2048 bins
 constexpr int kLowPerBlock = (int)(kLowBins / kLowBlocks);
-constexpr int kWindow = 2;              // top bins whose low bits the full pass counts
-constexpr int kRegions = kWindow + 1;   // low histograms per rank: the window's, then the fallback's
+// The window covers the top digits between the sample's two bounds, at most
+// this many (a quarter of a binade): narrow when the sample pins the k-th key
+// down, as wide as it needs to be otherwise.
+constexpr int kWindowMax = 4;
+constexpr int kRegions = kWindowMax + 1; // low histograms per rank: the window's, then the fallback's
 constexpr int kRun = 32;                // groups of 8 elements in a sampled run (one group per lane)
 constexpr int kSampleEvery = 16;        // one run in every 16 is sampled
 constexpr int kInitCtas = 64;           // CTAs per rank that clear low histograms
@@ -51,7 +57,7 @@ struct TopkState {
     uint32_t wlo;           // first top digit of the window, or kNoWindow
     uint32_t region;        // low histogram that counts the k-th key's top bin
     uint32_t hit;           // the window held that bin: no second pass
-    uint32_t pad;
+    uint32_t nwin;          // top digits in the window (0: none)
 };
 
 // Work buffer, for n ranks: top[n][kTopBins] (u64), stop[n][kTopBins] (u32,
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) topk_init_kernel(const __grid_consta
     const int r = blockIdx.y;
     if (p.k > 0 && p.k < p.K) { // the window's low histograms, only when a select follows
         uint4 *low = reinterpret_cast<uint4 *>(low_region(p, r, 0));
-        for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < kWindow * kLowBins / 4; i += gridDim.x * kThreads)
+        for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < kWindowMax * kLowBins / 4; i += gridDim.x * kThreads)
             gstore<uint4>(low + i, make_uint4(0, 0, 0, 0));
     }
     if (blockIdx.x != 0)
@@ -185,9 +191,9 @@ __global__ void __launch_bounds__(kThreads) topk_init_kernel(const __grid_consta
         // k = 0: no key reaches tau, nothing is sent; k >= K: every key does
         s.tau = p.k == 0 ? 0xffffffffu : 0u;
         s.wlo = kNoWindow;
-        s.region = kWindow;
+        s.region = kWindowMax;
         s.hit = 0;
-        s.pad = 0;
+        s.nwin = 0;
         gstore<TopkState>(p.state + r, s);
         gstore<uint32_t>(p.tau + r, s.tau);
     }
@@ -245,9 +251,10 @@ __global__ void __launch_bounds__(kThreads) topk_window_kernel(const __grid_cons
         acc += c[j];
     }
     __syncthreads();
-    if (t == 0 && dA >= 0 && dB >= 0 && dA - dB < kWindow) {
+    if (t == 0 && dA >= 0 && dB >= 0 && dA - dB < kWindowMax) {
         TopkState st = gload<TopkState>(p.state + r);
-        st.wlo = (uint32_t)(dB + kWindow <= kTopBins ? dB : kTopBins - kWindow);
+        st.wlo = (uint32_t)dB;
+        st.nwin = (uint32_t)(dA - dB + 1);
         gstore<TopkState>(p.state + r, st);
     }
 }
@@ -262,13 +269,14 @@ __global__ void __launch_bounds__(kThreads) topk_main_kernel(const __grid_consta
         h[i] = 0u;
     __syncthreads();
     const int r = blockIdx.y;
-    const uint32_t wlo = gload<TopkState>(p.state + r).wlo;
+    const TopkState st = gload<TopkState>(p.state + r);
+    const uint32_t wlo = st.wlo, nwin = st.nwin;
     uint32_t *low = low_region(p, r, 0);
     for_each_key<DT>(p, r, [&](uint32_t key) {
         const uint32_t d = key >> kLowBits;
         atomicAdd(&h[d], 1u);
-        const uint32_t w = d - wlo; // wraps past kWindow below the window
-        if (wlo != kNoWindow && w < (uint32_t)kWindow) {
+        const uint32_t w = d - wlo; // wraps past nwin below the window
+        if (w < nwin) {
             uint32_t *b = low + (size_t)w * kLowBins + (key & (kLowBins - 1u));
             if (dbg_ok(b, sizeof(uint32_t)))
                 atomicAdd(b, 1u);
@@ -302,8 +310,8 @@ __global__ void __launch_bounds__(kThreads) topk_top_scan_kernel(const __grid_co
                 n.prefix = (uint32_t)(kTopBins - 1 - (t * kPer + j));
                 n.kr = st.kr - acc;
                 const uint32_t w = n.prefix - st.wlo;
-                n.hit = (st.wlo != kNoWindow && w < (uint32_t)kWindow) ? 1u : 0u;
-                n.region = n.hit ? w : (uint32_t)kWindow;
+                n.hit = w < st.nwin ? 1u : 0u;
+                n.region = n.hit ? w : (uint32_t)kWindowMax;
                 gstore<TopkState>(p.state + r, n);
                 break;
             }
@@ -319,7 +327,7 @@ __global__ void __launch_bounds__(kThreads) topk_fallback_clear_kernel(const __g
     const int r = blockIdx.y;
     if (gload<TopkState>(p.state + r).hit)
         return;
-    uint4 *low = reinterpret_cast<uint4 *>(low_region(p, r, kWindow));
+    uint4 *low = reinterpret_cast<uint4 *>(low_region(p, r, kWindowMax));
     for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < kLowBins / 4; i += gridDim.x * kThreads)
         gstore<uint4>(low + i, make_uint4(0, 0, 0, 0));
 }
@@ -331,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) topk_fallback_kernel(const __grid_co
     const TopkState st = gload<TopkState>(p.state + r);
     if (st.hit)
         return;
-    uint32_t *low = low_region(p, r, kWindow);
+    uint32_t *low = low_region(p, r, kWindowMax);
     for_each_key<DT>(p, r, [&](uint32_t key) {
         if ((key >> kLowBits) == st.prefix) {
             uint32_t *b = low + (key & (kLowBins - 1u));
@@ -341,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) topk_fallback_kernel(const __grid_co
     });
 }
 
-// 4. Sum of each 4096-bin block of the low histogram that holds the k-th key.
+// 4. Sum of each 2048-bin block of the low histogram that holds the k-th key.
 __global__ void __launch_bounds__(kThreads) topk_low_sum_kernel(const __grid_constant__ TopkParams p)
 {
     __shared__ unsigned long long ws[kThreads / 32];

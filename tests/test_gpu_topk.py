@@ -103,12 +103,12 @@ def test_unaligned_buffers(dtype, pad):
 
 def _window_record(work, N):
     """The select's per-rank record in the work buffer (the layout of
-    topk.cu: top u64[N][2048], sample u32[N][2048], low u32[N][3][2^20],
+    topk.cu: top u64[N][4096], sample u32[N][4096], low u32[N][5][2^19],
     block sums u64[N][256], then one 32-byte record per rank whose 5th word
     is the window's first top digit (all ones when the sample placed none)
     and whose 7th says whether the window held the k-th key's top digit).
     Returns (hit, window placed) per rank."""
-    off = N * (2048 * 8 + 2048 * 4 + 3 * (1 << 20) * 4 + 256 * 8)
+    off = N * (4096 * 8 + 4096 * 4 + 5 * (1 << 19) * 4 + 256 * 8)
     rec = work[off:off + 32 * N].cpu().numpy().view(np.uint32).reshape(N, 8)
     return rec[:, 6].tolist(), [int(w != 0xFFFFFFFF) for w in rec[:, 4].tolist()]
 
@@ -116,7 +116,7 @@ def _window_record(work, N):
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 def test_sampled_window_hit_miss_and_none(dtype):
     """Every way through the select gives the oracle's bits.
-    - Normal data: the 1/16 sample places a window of two top digits on the
+    - Normal data: the 1/16 sample places a window of top digits around the
       k-th key's (one full pass; hit).
     - Zero residuals and sampled runs (the first 256 elements of every 4096)
       that all hold +-1e-6: the sample puts the window on that one digit, far
