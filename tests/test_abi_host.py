@@ -97,7 +97,10 @@ def test_planner_topk_bytes(L):
     assert 4 * d / ccl.ccl_plan_topk_bytes(d, d // 1000) == 500
     assert ccl.ccl_plan_topk_bytes(10, 50) == 80  # k beyond count keeps count
     assert ccl.ccl_plan_topk_bytes(10, 0) == 0
-    assert ccl.ccl_plan_topk_work_bytes(8) == 8 * (2048 * 8 + 2048 * 4 + 3 * (1 << 20) * 4 + 256 * 8 + 32 + 4)
+    # per rank: 4096-bin top histograms (u64 exact, u32 sampled), four window
+    # low histograms and the fallback's (2^19 u32 bins each), 256 block sums,
+    # a 32-byte state record and the threshold
+    assert ccl.ccl_plan_topk_work_bytes(8) == 8 * (4096 * 8 + 4096 * 4 + 5 * (1 << 19) * 4 + 256 * 8 + 32 + 4)
     for n in (0, 17):
         with pytest.raises(C.CclError):
             ccl.ccl_plan_topk_work_bytes(n)
