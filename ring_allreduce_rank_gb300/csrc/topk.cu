@@ -259,14 +259,28 @@ __global__ void __launch_bounds__(kThreads) topk_window_kernel(const __grid_cons
     }
 }
 
+// A CTA's cache of window bins in shared memory: a slot holds one bin (its
+// index into the window's low histograms) and that bin's count so far.  When
+// the window's keys fall on few bins -- residuals of bf16-valued numbers leave
+// only a few low bits free -- counting them here spares L2 a stream of
+// reductions into the same few addresses; keys whose slot another bin holds go
+// to L2 directly.  Each slot is flushed once, when the CTA ends.
+constexpr int kBinCache = 256;
+constexpr uint32_t kEmptySlot = 0xffffffffu;
+
 // 2. The full pass: exact top histogram, and the low bits of the keys whose
 // top bin lies in the window.
 template <int DT>
 __global__ void __launch_bounds__(kThreads) topk_main_kernel(const __grid_constant__ TopkParams p)
 {
     __shared__ uint32_t h[kTopBins];
+    __shared__ uint32_t cache_bin[kBinCache], cache_cnt[kBinCache];
     for (int i = threadIdx.x; i < kTopBins; i += kThreads)
         h[i] = 0u;
+    for (int i = threadIdx.x; i < kBinCache; i += kThreads) {
+        cache_bin[i] = kEmptySlot;
+        cache_cnt[i] = 0u;
+    }
     __syncthreads();
     const int r = blockIdx.y;
     const TopkState st = gload<TopkState>(p.state + r);
@@ -277,13 +291,28 @@ __global__ void __launch_bounds__(kThreads) topk_main_kernel(const __grid_consta
         atomicAdd(&h[d], 1u);
         const uint32_t w = d - wlo; // wraps past nwin below the window
         if (w < nwin) {
-            uint32_t *b = low + (size_t)w * kLowBins + (key & (kLowBins - 1u));
-            if (dbg_ok(b, sizeof(uint32_t)))
-                atomicAdd(b, 1u);
+            const uint32_t bin = w * kLowBins + (key & (kLowBins - 1u)); // < kWindowMax * kLowBins
+            const uint32_t slot = (bin * 2654435761u) >> 24;            // Fibonacci hash, 256 slots
+            const uint32_t held = atomicCAS(&cache_bin[slot], kEmptySlot, bin);
+            if (held == kEmptySlot || held == bin) {
+                atomicAdd(&cache_cnt[slot], 1u);
+            } else {
+                uint32_t *b = low + bin;
+                if (dbg_ok(b, sizeof(uint32_t)))
+                    atomicAdd(b, 1u);
+            }
         }
     });
     __syncthreads();
     merge_hist<unsigned long long>(h, p.top + (size_t)r * kTopBins);
+    for (int i = threadIdx.x; i < kBinCache; i += kThreads) {
+        const uint32_t bin = cache_bin[i], n = cache_cnt[i];
+        if (bin != kEmptySlot && n) {
+            uint32_t *b = low + bin;
+            if (dbg_ok(b, sizeof(uint32_t)))
+                atomicAdd(b, n);
+        }
+    }
 }
 
 // 3. One CTA per rank: the top bin of the k-th key, walking from the top;
