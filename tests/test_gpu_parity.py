@@ -305,10 +305,11 @@ def test_broadcast_matches_oracle(N, K, root, dtype, mode):
         assert_bits_equal(bits(out[r]), want[r], "bcast rank %d" % r)
 
 
+@pytest.mark.parametrize("N", [8, 20])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("shift", [0, 16, 32, 4])
 @pytest.mark.parametrize("kind", ["whole32", "whole16", "ragged"])
-def test_fanout_vector_widths(kind, shift, dtype):
+def test_fanout_vector_widths(kind, shift, dtype, N):
     """The fan-out kernel (Broadcast, AllGather, Gather) moves 32-byte vectors
     when every buffer starts on a 32-byte boundary and the chunk starts on a
     whole 32-byte vector, 16-byte vectors when only 16-byte alignment holds,
@@ -317,13 +318,12 @@ def test_fanout_vector_widths(kind, shift, dtype):
     32-byte vectors, whole 16-byte vectors only (odd multiples), or ragged."""
     es = 2 if dtype == "bf16" else 4
     vec = 16 // es
-    N = 8
     per = {"whole32": 2 * vec * 300, "whole16": 2 * vec * 300 + vec, "ragged": 2 * vec * 300 + 3}[kind]
     K = N * per + (5 if kind == "ragged" else 0)
     pad = shift // es
     x = inputs(dtype, N, K, seed=K + shift)
     tdt = torch_dtype(x)
-    # Broadcast from rank 3, out of place
+    # Broadcast from rank 3, out of place (N = 20: the large parameter block)
     send = [None] * N
     send[3] = to_dev(x[3], pad_elems=pad)
     out = [empty_like_host(K, tdt, pad_elems=pad) for _ in range(N)]
