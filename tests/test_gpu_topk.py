@@ -155,6 +155,31 @@ def test_sampled_window_hit_miss_and_none(dtype):
         _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, name)
 
 
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_window_widths(dtype):
+    """The sample's window covers the top digits between its two bounds, one
+    to four of them: narrow where the sample pins the k-th key down (many
+    elements), wider where it cannot (few).  Every width gives the oracle's
+    bits, and the sizes below produce windows of one or two digits and of
+    three or four."""
+    N = 4
+    widths = set()
+    work = torch.empty(ccl.ccl_plan_topk_work_bytes(N), dtype=torch.uint8, device=DEV)
+    off = N * (4096 * 8 + 4096 * 4 + 5 * (1 << 19) * 4 + 256 * 8)
+    for K, k in ((1 << 20, 10_486), (1 << 18, 2_621), (65_536 + 13, 655), (40_000, 400), (30_000, 1_500)):
+        g = list(W.normal_bf16(N, K, seed_base=K % 97)) if dtype == "bf16" else list(W.normal_fp32(N, K, seed_base=K % 97))
+        e = _res(N, K, seed=K % 89)
+        want_g, want_e = oracle.allreduce_compressed(g, e, "avg", "topk", k=k)
+        gd = [to_dev(x) for x in g]
+        ed = [to_dev(x) for x in e]
+        ccl.ccl_allreduce_topk(gd, ed, k, op="avg", work=work)
+        torch.cuda.synchronize()
+        rec = work[off:off + 32 * N].cpu().numpy().view(np.uint32).reshape(N, 8)
+        widths.update(int(w) for w in rec[:, 7])
+        _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, "K=%d k=%d" % (K, k))
+    assert widths & {1, 2} and widths & {3, 4}, widths
+
+
 def test_nan_is_sent_first():
     N, K = 3, 4096
     g = list(W.normal_fp32(N, K, seed_base=8))
