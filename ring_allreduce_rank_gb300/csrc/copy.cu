@@ -201,6 +201,118 @@ template <int MAXR> struct FanoutParams {
     int vec32;       // every pointer 32-byte aligned
 };
 
+// Eight words (one 32-byte vector) of the sixteen in w (two neighbouring
+// 32-byte vectors), starting d elements in, 0 < d < 2 * (elements a 16-byte
+// vector holds).
+template <int DT> __device__ __forceinline__ void shift_window32(const uint32_t (&w)[16], int d, uint32_t (&o)[8])
+{
+    if (DT == DT_FP32) {
+#define CCL_W32(D)                                                                                                     \
+    case D:                                                                                                            \
+        _Pragma("unroll") for (int i = 0; i < 8; ++i) o[i] = w[D + i];                                                 \
+        break;
+        switch (d) {
+            CCL_W32(1) CCL_W32(2) CCL_W32(3) CCL_W32(4) CCL_W32(5) CCL_W32(6)
+        default:
+            _Pragma("unroll") for (int i = 0; i < 8; ++i) o[i] = w[7 + i];
+        }
+#undef CCL_W32
+    } else {
+        // d halfwords: whole words d/2, then half a word if d is odd
+#define CCL_H32(D)                                                                                                     \
+    case D:                                                                                                            \
+        _Pragma("unroll") for (int i = 0; i < 8; ++i) o[i] =                                                           \
+            (D & 1) ? __funnelshift_r(w[(D >> 1) + i], w[(D >> 1) + i + 1], 16) : w[(D >> 1) + i];                     \
+        break;
+        switch (d) {
+            CCL_H32(1) CCL_H32(2) CCL_H32(3) CCL_H32(4) CCL_H32(5) CCL_H32(6) CCL_H32(7) CCL_H32(8) CCL_H32(9)
+            CCL_H32(10) CCL_H32(11) CCL_H32(12) CCL_H32(13) CCL_H32(14)
+        default:
+            _Pragma("unroll") for (int i = 0; i < 8; ++i) o[i] = __funnelshift_r(w[7 + i], w[8 + i], 16);
+        }
+#undef CCL_H32
+    }
+}
+
+// The ragged fan-out with 32-byte vectors (every buffer 32-byte aligned, the
+// chunk at an offset that is not a whole 16-byte vector).  Each lane loads one
+// aligned 32-byte source vector and takes the next one from its neighbour
+// lane (lane 31 loads it); the destination vector is the window s1 elements
+// into that pair.  As in the 16-byte form, a warp writes 32 destination
+// vectors that start on a multiple of 32, and the chunk's unaligned head and
+// tail go element by element.
+template <int DT, int MAXR>
+__device__ __forceinline__ void fanout_ragged32(const FanoutParams<MAXR> &p, uint32_t t, uint64_t off, uint64_t len,
+                                                const void *src, int M)
+{
+    constexpr int V2 = 2 * DType<DT>::kVec; // elements per 32-byte vector
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t vb = (off + V2 - 1) / V2, ve = (off + len) / V2;
+    const int s1 = (int)(vb * V2 - off); // 0 < s1 < V2
+    if (t == 0) {
+        const uint64_t hb = vb < ve ? vb * V2 : off + len;
+        for (uint64_t d = off + threadIdx.x; d < hb; d += kThreads) {
+            const uint32_t v = ld_elem<DT>(src, d - off);
+            for (int q = 0; q < M; ++q)
+                st_elem<DT>(p.dst[q], d, v);
+        }
+        if (vb < ve)
+            for (uint64_t d = ve * V2 + threadIdx.x; d < off + len; d += kThreads) {
+                const uint32_t v = ld_elem<DT>(src, d - off);
+                for (int q = 0; q < M; ++q)
+                    st_elem<DT>(p.dst[q], d, v);
+            }
+    }
+    if (vb >= ve)
+        return;
+    // this lane's destination vector; whole warps past the end leave together
+    const uint64_t v = (vb / 32 + (uint64_t)t * (kThreads / 32) + warp) * 32 + lane;
+    if (v - lane >= ve)
+        return;
+    // source vector b (32 bytes) feeds destination vectors vb + b - 1 and vb + b
+    auto load_src = [&](int64_t b, uint32_t *h) {
+        if (b < 0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                h[k] = 0u;
+        } else if ((uint64_t)(b + 1) * V2 <= len) {
+            uint4 a, c;
+            ld32(static_cast<const char *>(src) + (uint64_t)b * 32, a, c);
+            h[0] = a.x; h[1] = a.y; h[2] = a.z; h[3] = a.w;
+            h[4] = c.x; h[5] = c.y; h[6] = c.z; h[7] = c.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                h[k] = 0u;
+            for (int k = 0; k < V2; ++k) {
+                const uint64_t e = (uint64_t)b * V2 + k;
+                const uint32_t x = e < len ? ld_elem<DT>(src, e) : 0u;
+                if (DT == DT_FP32)
+                    h[k] = x;
+                else
+                    h[k >> 1] |= x << (16 * (k & 1));
+            }
+        }
+    };
+    const int64_t b = (int64_t)v - (int64_t)vb;
+    uint32_t w[16], nx[8];
+    load_src(b, w);
+    if (lane == 31)
+        load_src(b + 1, nx);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, w[k], 1);
+        w[8 + k] = lane == 31 ? nx[k] : y;
+    }
+    if (v >= vb && v < ve) {
+        uint32_t o[8];
+        shift_window32<DT>(w, s1, o);
+        const uint4 a = make_uint4(o[0], o[1], o[2], o[3]), c = make_uint4(o[4], o[5], o[6], o[7]);
+        for (int q = 0; q < M; ++q)
+            st32(static_cast<char *>(p.dst[q]) + v * 32, a, c);
+    }
+}
+
 template <int DT, int MAXR>
 __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant__ FanoutParams<MAXR> p)
 {
@@ -211,6 +323,10 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
     const uint64_t off = p.part.off(c), len = p.part.len(c);
     const void *src = p.src[c];
     const int M = p.ndst;
+    if (p.vec32 && off % VEC != 0) {
+        fanout_ragged32<DT, MAXR>(p, t, off, len, src, M);
+        return;
+    }
     if (p.vec_aligned && off % VEC != 0) {
         // The chunk lands at an offset that is not a whole vector (ragged
         // partition).  Lanes load aligned source vectors; each aligned
@@ -361,10 +477,11 @@ static cudaError_t launch_fanout_t(const void *const *src, int nchunks, void *co
     bool ragged = false;
     for (int c = 1; c < nchunks && aligned && !ragged; ++c)
         ragged = p.part.off((uint32_t)c) % VEC != 0;
-    // ragged path: kThreads destination vectors per tile, the first block
-    // starting up to 31 vectors before the chunk
+    // ragged path: kThreads destination vectors (32-byte ones when every
+    // buffer allows) per tile, the first block starting up to 31 vectors
+    // before the chunk
     const uint64_t per_tile = (uint64_t)kThreads;
-    const uint64_t shifted = ((p.part.q + 1) / VEC + 31 + per_tile) / per_tile + 1;
+    const uint64_t shifted = ((p.part.q + 1) / (aligned32 ? 2 * VEC : VEC) + 31 + per_tile) / per_tile + 1;
     if (ragged && shifted > tiles)
         tiles = shifted;
     if (tiles > 0x7fffffffull)
