@@ -12,18 +12,37 @@ namespace ccl {
 
 constexpr uint64_t kCopyTileBytes = (uint64_t)kThreads * 4 * 16; // 16 KiB of body per CTA
 
+// 32-byte vector load / store (sm_100 and later); p must be 32-byte aligned
+__device__ __forceinline__ void ld32(const void *p, uint4 &a, uint4 &b)
+{
+    a = b = make_uint4(0, 0, 0, 0);
+    if (dbg_ok(p, 32))
+        asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                     : "l"(p));
+}
+
+__device__ __forceinline__ void st32(void *p, const uint4 &a, const uint4 &b)
+{
+    if (dbg_ok(p, 32))
+        asm volatile("st.global.L1::no_allocate.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x),
+                     "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                     : "memory");
+}
+
 template <int MAXS> struct CopyParams {
     uint32_t nseg;
     uint32_t pad;
     CopySeg seg[MAXS];
 };
 
-// Alignment class of a segment: the widest power of two (<= 16) dividing the
+// Alignment class of a segment: the widest power of two (<= 32) dividing the
 // distance between source and destination; the body is moved in words of that
 // width, aligned on the destination.
 __host__ __device__ __forceinline__ uint32_t copy_grain(const char *src, const char *dst)
 {
     const uintptr_t d = (uintptr_t)src ^ (uintptr_t)dst;
+    if ((d & 31) == 0) return 32;
     if ((d & 15) == 0) return 16;
     if ((d & 7) == 0) return 8;
     if ((d & 3) == 0) return 4;
@@ -84,7 +103,26 @@ __global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_co
     const uint64_t nb = umin64(kCopyTileBytes, body - b0);
     const char *src = s.src + head + b0;
     char *dst = s.dst + head + b0;
-    if (g == 16) {
+    if (g == 32) {
+        // two 32-byte loads in flight per thread before the stores
+        constexpr int B = 2;
+        const uint64_t n = nb / 32;
+        for (uint64_t i0 = threadIdx.x; i0 < n; i0 += (uint64_t)B * kThreads) {
+            uint4 x[B], y[B];
+#pragma unroll
+            for (int k = 0; k < B; ++k) {
+                const uint64_t i = i0 + (uint64_t)k * kThreads;
+                if (i < n)
+                    ld32(src + i * 32, x[k], y[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < B; ++k) {
+                const uint64_t i = i0 + (uint64_t)k * kThreads;
+                if (i < n)
+                    st32(dst + i * 32, x[k], y[k]);
+            }
+        }
+    } else if (g == 16) {
         // four 16-byte loads in flight per thread before the stores (the
         // volatile loads and stores keep program order, so they are batched
         // by hand)
@@ -172,24 +210,6 @@ cudaError_t preload_copy_kernels()
 }
 
 // ------------------------------------------------------------------ fan-out (AllGather, Broadcast)
-
-// 32-byte vector load / store (sm_100 and later); p must be 32-byte aligned
-__device__ __forceinline__ void ld32(const void *p, uint4 &a, uint4 &b)
-{
-    a = b = make_uint4(0, 0, 0, 0);
-    if (dbg_ok(p, 32))
-        asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-                     : "l"(p));
-}
-
-__device__ __forceinline__ void st32(void *p, const uint4 &a, const uint4 &b)
-{
-    if (dbg_ok(p, 32))
-        asm volatile("st.global.L1::no_allocate.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x),
-                     "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
-                     : "memory");
-}
 
 template <int MAXR> struct FanoutParams {
     const void *src[MAXR];
