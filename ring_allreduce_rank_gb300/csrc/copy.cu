@@ -224,6 +224,9 @@ template <int MAXR> struct FanoutParams {
 // Eight words (one 32-byte vector) of the sixteen in w (two neighbouring
 // 32-byte vectors), starting d elements in, 0 < d < 2 * (elements a 16-byte
 // vector holds).
+// Threads per CTA of the fan-out kernel.
+constexpr int kFanThreads = kThreads;
+
 template <int DT> __device__ __forceinline__ void shift_window32(const uint32_t (&w)[16], int d, uint32_t (&o)[8])
 {
     if (DT == DT_FP32) {
@@ -271,13 +274,13 @@ __device__ __forceinline__ void fanout_ragged32(const FanoutParams<MAXR> &p, uin
     const int s1 = (int)(vb * V2 - off); // 0 < s1 < V2
     if (t == 0) {
         const uint64_t hb = vb < ve ? vb * V2 : off + len;
-        for (uint64_t d = off + threadIdx.x; d < hb; d += kThreads) {
+        for (uint64_t d = off + threadIdx.x; d < hb; d += kFanThreads) {
             const uint32_t v = ld_elem<DT>(src, d - off);
             for (int q = 0; q < M; ++q)
                 st_elem<DT>(p.dst[q], d, v);
         }
         if (vb < ve)
-            for (uint64_t d = ve * V2 + threadIdx.x; d < off + len; d += kThreads) {
+            for (uint64_t d = ve * V2 + threadIdx.x; d < off + len; d += kFanThreads) {
                 const uint32_t v = ld_elem<DT>(src, d - off);
                 for (int q = 0; q < M; ++q)
                     st_elem<DT>(p.dst[q], d, v);
@@ -286,7 +289,7 @@ __device__ __forceinline__ void fanout_ragged32(const FanoutParams<MAXR> &p, uin
     if (vb >= ve)
         return;
     // this lane's destination vector; whole warps past the end leave together
-    const uint64_t v = (vb / 32 + (uint64_t)t * (kThreads / 32) + warp) * 32 + lane;
+    const uint64_t v = (vb / 32 + (uint64_t)t * (kFanThreads / 32) + warp) * 32 + lane;
     if (v - lane >= ve)
         return;
     // source vector b (32 bytes) feeds destination vectors vb + b - 1 and vb + b
@@ -334,11 +337,11 @@ __device__ __forceinline__ void fanout_ragged32(const FanoutParams<MAXR> &p, uin
 }
 
 template <int DT, int MAXR>
-__global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant__ FanoutParams<MAXR> p)
+__global__ void __launch_bounds__(kFanThreads) fanout_kernel(const __grid_constant__ FanoutParams<MAXR> p)
 {
     constexpr int VEC = DType<DT>::kVec;
     constexpr int U = 2;
-    constexpr uint64_t TV = (uint64_t)kThreads * U;
+    constexpr uint64_t TV = (uint64_t)kFanThreads * U;
     const uint32_t c = blockIdx.y, t = blockIdx.x;
     const uint64_t off = p.part.off(c), len = p.part.len(c);
     const void *src = p.src[c];
@@ -360,13 +363,13 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
         const int s0 = (int)(vb * VEC - off); // 0 < s0 < VEC
         if (t == 0) {
             const uint64_t hb = vb < ve ? vb * VEC : off + len;
-            for (uint64_t d = off + threadIdx.x; d < hb; d += kThreads) {
+            for (uint64_t d = off + threadIdx.x; d < hb; d += kFanThreads) {
                 const uint32_t v = ld_elem<DT>(src, d - off);
                 for (int q = 0; q < M; ++q)
                     st_elem<DT>(p.dst[q], d, v);
             }
             if (vb < ve)
-                for (uint64_t d = ve * VEC + threadIdx.x; d < off + len; d += kThreads) {
+                for (uint64_t d = ve * VEC + threadIdx.x; d < off + len; d += kFanThreads) {
                     const uint32_t v = ld_elem<DT>(src, d - off);
                     for (int q = 0; q < M; ++q)
                         st_elem<DT>(p.dst[q], d, v);
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
         if (vb >= ve)
             return;
         // this lane's destination vector; whole warps past the end leave together
-        const uint64_t v = (vb / 32 + (uint64_t)t * (kThreads / 32) + warp) * 32 + lane;
+        const uint64_t v = (vb / 32 + (uint64_t)t * (kFanThreads / 32) + warp) * 32 + lane;
         if (v - lane >= ve)
             return;
         // source vector b feeds destination vectors vb + b - 1 and vb + b
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
     if (!(p.vec_aligned && off % VEC == 0)) {
         const uint64_t e0 = (uint64_t)t * TV * VEC;
         for (int k = 0; k < U * VEC; ++k) {
-            const uint64_t e = e0 + (uint64_t)k * kThreads + threadIdx.x;
+            const uint64_t e = e0 + (uint64_t)k * kFanThreads + threadIdx.x;
             if (e < len) {
                 const uint32_t v = ld_elem<DT>(src, e);
                 for (int q = 0; q < M; ++q)
@@ -425,12 +428,12 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
         // 32-byte vectors: one per thread, a warp covering 1 KiB contiguous
         const uint64_t nw = len / (2 * VEC);
         if (t == 0)
-            for (uint64_t e = nw * 2 * VEC + threadIdx.x; e < len; e += kThreads) {
+            for (uint64_t e = nw * 2 * VEC + threadIdx.x; e < len; e += kFanThreads) {
                 const uint32_t v = ld_elem<DT>(src, e);
                 for (int q = 0; q < M; ++q)
                     st_elem<DT>(p.dst[q], off + e, v);
             }
-        const uint64_t w = (uint64_t)t * kThreads + threadIdx.x;
+        const uint64_t w = (uint64_t)t * kFanThreads + threadIdx.x;
         if (w < nw) {
             uint4 a, b;
             ld32(static_cast<const char *>(src) + w * 32, a, b);
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
     }
     const uint64_t nv = len / VEC;
     if (t == 0)
-        for (uint64_t e = nv * VEC + threadIdx.x; e < len; e += kThreads) {
+        for (uint64_t e = nv * VEC + threadIdx.x; e < len; e += kFanThreads) {
             const uint32_t v = ld_elem<DT>(src, e);
             for (int q = 0; q < M; ++q)
                 st_elem<DT>(p.dst[q], off + e, v);
@@ -449,13 +452,13 @@ __global__ void __launch_bounds__(kThreads) fanout_kernel(const __grid_constant_
     uint4 x[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const uint64_t v = (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
+        const uint64_t v = (uint64_t)t * TV + (uint64_t)u * kFanThreads + threadIdx.x;
         if (v < nv)
             x[u] = ld16(static_cast<const char *>(src) + v * 16);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const uint64_t v = (uint64_t)t * TV + (uint64_t)u * kThreads + threadIdx.x;
+        const uint64_t v = (uint64_t)t * TV + (uint64_t)u * kFanThreads + threadIdx.x;
         if (v < nv)
             for (int q = 0; q < M; ++q)
                 st16(static_cast<char *>(p.dst[q]) + (off + v * VEC) * DType<DT>::kSize, x[u]);
@@ -487,8 +490,8 @@ static cudaError_t launch_fanout_t(const void *const *src, int nchunks, void *co
     p.ndst = ndst;
     p.vec_aligned = aligned ? 1 : 0;
     p.vec32 = aligned32 ? 1 : 0;
-    // a tile: kThreads x 32 bytes (two 16-byte vectors per thread, or one 32-byte one)
-    const uint64_t te = (uint64_t)kThreads * 2 * VEC;
+    // a tile: kFanThreads x 32 bytes (two 16-byte vectors per thread, or one 32-byte one)
+    const uint64_t te = (uint64_t)kFanThreads * 2 * VEC;
     uint64_t tiles = (p.part.q + 1 + te - 1) / te;
     // A chunk whose offset is not a whole vector takes the shuffle path (one
     // vector per thread) and needs about twice as many tiles; size the grid for
@@ -497,16 +500,16 @@ static cudaError_t launch_fanout_t(const void *const *src, int nchunks, void *co
     bool ragged = false;
     for (int c = 1; c < nchunks && aligned && !ragged; ++c)
         ragged = p.part.off((uint32_t)c) % VEC != 0;
-    // ragged path: kThreads destination vectors (32-byte ones when every
+    // ragged path: kFanThreads destination vectors (32-byte ones when every
     // buffer allows) per tile, the first block starting up to 31 vectors
     // before the chunk
-    const uint64_t per_tile = (uint64_t)kThreads;
+    const uint64_t per_tile = (uint64_t)kFanThreads;
     const uint64_t shifted = ((p.part.q + 1) / (aligned32 ? 2 * VEC : VEC) + 31 + per_tile) / per_tile + 1;
     if (ragged && shifted > tiles)
         tiles = shifted;
     if (tiles > 0x7fffffffull)
         return cudaErrorInvalidValue;
-    fanout_kernel<DT, MAXR><<<dim3((unsigned)tiles, (unsigned)nchunks), kThreads, 0, stream>>>(p);
+    fanout_kernel<DT, MAXR><<<dim3((unsigned)tiles, (unsigned)nchunks), kFanThreads, 0, stream>>>(p);
     count_launches(1);
     return cudaGetLastError();
 }

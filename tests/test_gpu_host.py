@@ -220,3 +220,30 @@ def test_host_allreduce_path_taken(host_path, pinned):
     want, _ = oracle.ring_allreduce(list(x), "avg")
     for r in range(N):
         assert_bits_equal(_host_bits(recv[r]), want[r], "%s pinned=%s rank %d" % (host_path, pinned, r))
+
+
+def test_host_allreduce_registered_memory(host_path):
+    """Pageable host memory page-locked after the fact (cudaHostRegister) is
+    what many frameworks hand over: the direct path reads and writes it in
+    place like cudaHostAlloc'd memory, and both paths give the oracle's bits."""
+    cudart = torch.cuda.cudart()
+    N, K = 3, 50_003
+    x = W.normal_fp32(N, K, seed_base=61)
+    send = [torch.from_numpy(r.copy()) for r in x]  # pageable
+    recv = [torch.empty(K, dtype=torch.float32) for _ in range(N)]
+    regs = []
+    try:
+        for t in send + recv:
+            assert int(cudart.cudaHostRegister(t.data_ptr(), t.numel() * 4, 0)) == 0
+            regs.append(t)
+        n0 = ccl.ccl_launch_count()
+        ccl.ccl_allreduce_host(send, recv, op="sum", work=_stage_work(N, 4, 1024))
+        torch.cuda.synchronize()
+        launches = ccl.ccl_launch_count() - n0
+        assert (launches == 1) == (host_path == "direct")
+        want, _ = oracle.ring_allreduce(list(x), "sum")
+        for r in range(N):
+            assert_bits_equal(_host_bits(recv[r]), want[r], "registered %s rank %d" % (host_path, r))
+    finally:
+        for t in regs:
+            cudart.cudaHostUnregister(t.data_ptr())
