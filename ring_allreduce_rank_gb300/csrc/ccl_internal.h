@@ -2,6 +2,7 @@
 // units: kernel parameter blocks and launchers.  Not part of the public ABI.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <cuda_runtime_api.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -89,6 +90,36 @@ inline Partition make_partition(size_t count, int nranks)
 ccl_status_t check_reduce_scatter(const void *const *send, void *const *recv, int nranks, size_t count,
                                   ccl_dtype_t dtype, ccl_op_t op, std::vector<Range> &w, std::vector<Range> &r);
 
+
+// ------------------------------------------------------------------ chained launches
+// Kernels that run as a chain of programmatic dependent launches call this
+// first: it waits until the kernel before it in the stream has completed and
+// its writes are visible, then lets the next kernel's CTAs be scheduled, so
+// that a launch and its ramp-up overlap the previous kernel's tail.  In a
+// launch without the attribute the wait returns at once.
+__device__ __forceinline__ void chain_entry()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// A launch in such a chain (programmatic stream serialisation).
+template <class P>
+inline cudaError_t launch_chained(void (*kernel)(P), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  const P &p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
 
 // ------------------------------------------------------------------ step mode
 enum StepKind {

@@ -381,6 +381,8 @@ __device__ __forceinline__ void compress_fold_store(const CompParams &p, uint64_
 template <int DT, int EPL, int NMAX, int COMP>
 __global__ void __launch_bounds__(kThreads, NMAX <= 8 ? 3 : 1) compressed_allreduce_kernel(const __grid_constant__ CompParams p)
 {
+    if (COMP == COMP_TOPK)
+        chain_entry(); // the select's threshold comes from the kernels before
     constexpr int B = 32 * EPL; // compression block
     const int lane = threadIdx.x & 31;
     const uint64_t blk = p.first_block + (((uint64_t)blockIdx.x * kThreads + threadIdx.x) >> 5);
@@ -453,6 +455,8 @@ template <int DT, int EPL> struct PipeLayout {
 template <int DT, int EPL, int COMP>
 __global__ void __launch_bounds__(kPipeThreads) compressed_pipe_kernel(const __grid_constant__ CompParams p)
 {
+    if (COMP == COMP_TOPK)
+        chain_entry(); // the select's threshold comes from the kernels before
     using Lay = PipeLayout<DT, EPL>;
     constexpr int B = 32 * EPL;
     constexpr int NMAX = 8;
@@ -575,7 +579,14 @@ static cudaError_t launch_pipe_t(const CompParams &p, cudaStream_t stream)
         grid = ntiles;
     if (grid == 0)
         return cudaSuccess;
-    compressed_pipe_kernel<DT, EPL, COMP><<<(unsigned)grid, kPipeThreads, Lay::kBytes, stream>>>(p);
+    if (COMP == COMP_TOPK) { // chained after the select's kernels
+        cudaError_t e = launch_chained<CompParams>(compressed_pipe_kernel<DT, EPL, COMP>, dim3((unsigned)grid),
+                                                   dim3(kPipeThreads), Lay::kBytes, stream, p);
+        if (e != cudaSuccess)
+            return e;
+    } else {
+        compressed_pipe_kernel<DT, EPL, COMP><<<(unsigned)grid, kPipeThreads, Lay::kBytes, stream>>>(p);
+    }
     count_launches(1);
     return cudaGetLastError();
 }
@@ -591,7 +602,14 @@ static cudaError_t launch_comp_t(const CompParams &p, cudaStream_t stream)
     const uint64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
     if (blocks > 0x7fffffffull)
         return cudaErrorInvalidValue;
-    compressed_allreduce_kernel<DT, EPL, NMAX, COMP><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    if (COMP == COMP_TOPK) { // chained after the select's kernels
+        cudaError_t e = launch_chained<CompParams>(compressed_allreduce_kernel<DT, EPL, NMAX, COMP>,
+                                                   dim3((unsigned)blocks), dim3(kThreads), 0, stream, p);
+        if (e != cudaSuccess)
+            return e;
+    } else {
+        compressed_allreduce_kernel<DT, EPL, NMAX, COMP><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    }
     count_launches(1);
     return cudaGetLastError();
 }

@@ -170,8 +170,11 @@ __device__ __forceinline__ uint32_t *low_region(const TopkParams &p, int r, uint
     return p.low + ((size_t)r * kRegions + region) * kLowBins;
 }
 
+// The select's kernels, and the compressed pass after them, run as a chain of
+// programmatic dependent launches (chain_entry, launch_chained).
 __global__ void __launch_bounds__(kThreads) topk_init_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     const int r = blockIdx.y;
     if (p.k > 0 && p.k < p.K) { // the window's low histograms, only when a select follows
         uint4 *low = reinterpret_cast<uint4 *>(low_region(p, r, 0));
@@ -205,6 +208,7 @@ __global__ void __launch_bounds__(kThreads) topk_init_kernel(const __grid_consta
 template <int DT>
 __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     __shared__ uint32_t h[kTopBins];
     for (int i = threadIdx.x; i < kTopBins; i += kThreads)
         h[i] = 0u;
@@ -226,6 +230,7 @@ __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const __grid_cons
 // (dA >= dB); two bins cover them when dA - dB < 2.
 __global__ void __launch_bounds__(kThreads) topk_window_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     constexpr int kPer = kTopBins / kThreads;
     __shared__ unsigned long long ws[kThreads / 32];
     __shared__ int dA, dB;
@@ -273,6 +278,7 @@ constexpr uint32_t kEmptySlot = 0xffffffffu;
 template <int DT>
 __global__ void __launch_bounds__(kThreads) topk_main_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     __shared__ uint32_t h[kTopBins];
     __shared__ uint32_t cache_bin[kBinCache], cache_cnt[kBinCache];
     for (int i = threadIdx.x; i < kTopBins; i += kThreads)
@@ -319,6 +325,7 @@ __global__ void __launch_bounds__(kThreads) topk_main_kernel(const __grid_consta
 // whether the window counted its low bits.
 __global__ void __launch_bounds__(kThreads) topk_top_scan_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     constexpr int kPer = kTopBins / kThreads;
     __shared__ unsigned long long ws[kThreads / 32];
     const int r = blockIdx.x, t = threadIdx.x;
@@ -353,6 +360,7 @@ __global__ void __launch_bounds__(kThreads) topk_top_scan_kernel(const __grid_co
 // second full pass counts the low bits of the chosen top bin into it.
 __global__ void __launch_bounds__(kThreads) topk_fallback_clear_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     const int r = blockIdx.y;
     if (gload<TopkState>(p.state + r).hit)
         return;
@@ -364,6 +372,7 @@ __global__ void __launch_bounds__(kThreads) topk_fallback_clear_kernel(const __g
 template <int DT>
 __global__ void __launch_bounds__(kThreads) topk_fallback_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     const int r = blockIdx.y;
     const TopkState st = gload<TopkState>(p.state + r);
     if (st.hit)
@@ -381,6 +390,7 @@ __global__ void __launch_bounds__(kThreads) topk_fallback_kernel(const __grid_co
 // 4. Sum of each 2048-bin block of the low histogram that holds the k-th key.
 __global__ void __launch_bounds__(kThreads) topk_low_sum_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     __shared__ unsigned long long ws[kThreads / 32];
     const int r = blockIdx.y, b = blockIdx.x;
     const uint32_t region = gload<TopkState>(p.state + r).region;
@@ -399,6 +409,7 @@ __global__ void __launch_bounds__(kThreads) topk_low_sum_kernel(const __grid_con
 // key among the keys of the chosen top bin; tau = top digit : low bits.
 __global__ void __launch_bounds__(kThreads) topk_low_scan_kernel(const __grid_constant__ TopkParams p)
 {
+    chain_entry();
     static_assert(kLowBlocks == kThreads, "one block sum per thread");
     constexpr int kPer = kLowPerBlock / kThreads;
     __shared__ unsigned long long ws[kThreads / 32];
@@ -535,25 +546,25 @@ cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, in
         uint64_t sctas = (swarps + kThreads / 32 - 1) / (kThreads / 32);
         if (sctas > per_rank)
             sctas = per_rank;
-        if (dt == DT_FP32)
-            topk_sample_kernel<DT_FP32><<<dim3((unsigned)sctas, (unsigned)nranks), kThreads, 0, stream>>>(p);
-        else
-            topk_sample_kernel<DT_BF16><<<dim3((unsigned)sctas, (unsigned)nranks), kThreads, 0, stream>>>(p);
-        topk_window_kernel<<<(unsigned)nranks, kThreads, 0, stream>>>(p);
+        const dim3 sgrid((unsigned)sctas, (unsigned)nranks), block(kThreads), one((unsigned)nranks);
+        cudaError_t e2 = launch_chained<TopkParams>(
+            dt == DT_FP32 ? topk_sample_kernel<DT_FP32> : topk_sample_kernel<DT_BF16>, sgrid, block, 0, stream, p);
+        if (e2 == cudaSuccess)
+            e2 = launch_chained<TopkParams>(topk_window_kernel, one, block, 0, stream, p);
+        if (e2 != cudaSuccess)
+            return e2;
         launches += 2;
     }
-    if (dt == DT_FP32)
-        topk_main_kernel<DT_FP32><<<grid, kThreads, 0, stream>>>(p);
-    else
-        topk_main_kernel<DT_BF16><<<grid, kThreads, 0, stream>>>(p);
-    topk_top_scan_kernel<<<(unsigned)nranks, kThreads, 0, stream>>>(p);
-    topk_fallback_clear_kernel<<<dim3(kInitCtas, (unsigned)nranks), kThreads, 0, stream>>>(p);
-    if (dt == DT_FP32)
-        topk_fallback_kernel<DT_FP32><<<grid, kThreads, 0, stream>>>(p);
-    else
-        topk_fallback_kernel<DT_BF16><<<grid, kThreads, 0, stream>>>(p);
-    topk_low_sum_kernel<<<dim3(kLowBlocks, (unsigned)nranks), kThreads, 0, stream>>>(p);
-    topk_low_scan_kernel<<<(unsigned)nranks, kThreads, 0, stream>>>(p);
+    const bool f32 = dt == DT_FP32;
+    const dim3 block(kThreads), one((unsigned)nranks);
+    using K = void (*)(TopkParams);
+    const K chain[] = {f32 ? topk_main_kernel<DT_FP32> : topk_main_kernel<DT_BF16>, topk_top_scan_kernel,
+                       topk_fallback_clear_kernel, f32 ? topk_fallback_kernel<DT_FP32> : topk_fallback_kernel<DT_BF16>,
+                       topk_low_sum_kernel, topk_low_scan_kernel};
+    const dim3 grids[] = {grid, one, dim3(kInitCtas, (unsigned)nranks), grid, dim3(kLowBlocks, (unsigned)nranks), one};
+    for (int i = 0; i < 6; ++i)
+        if (cudaError_t e2 = launch_chained<TopkParams>(chain[i], grids[i], block, 0, stream, p))
+            return e2;
     count_launches(launches + 6);
     return cudaGetLastError();
 }
