@@ -48,6 +48,7 @@ __device__ __forceinline__ void step_elem(const StepParams<MAXR> &p, int kind, i
 template <int DT, int OP, int MAXR>
 __global__ void __launch_bounds__(kThreads) ring_step_kernel(const __grid_constant__ StepParams<MAXR> p)
 {
+    chain_entry(); // every step after a phase's first is chained to the step before
     constexpr int VEC = DType<DT>::kVec;
     constexpr int U = 2;
     constexpr uint64_t TV = (uint64_t)kThreads * U;
@@ -137,7 +138,17 @@ static cudaError_t launch_step_t(int kind, int s, void *const *bufs, int nranks,
     if (tiles > 0x7fffffffull)
         return cudaErrorInvalidValue;
     p.tiles = (uint32_t)tiles;
-    ring_step_kernel<DT, OP, MAXR><<<dim3((unsigned)tiles, (unsigned)nranks), kThreads, 0, stream>>>(p);
+    // A ring step depends on the step before it; every step but a phase's
+    // first (which follows whatever the stream held) is a chained launch.  With
+    // one rank there is no step before the scaling launch.
+    const bool first = ((kind == STEP_RS || kind == STEP_AG_API) && s == 0) || nranks == 1;
+    if (first) {
+        ring_step_kernel<DT, OP, MAXR><<<dim3((unsigned)tiles, (unsigned)nranks), kThreads, 0, stream>>>(p);
+    } else if (cudaError_t e = launch_chained<StepParams<MAXR>>(ring_step_kernel<DT, OP, MAXR>,
+                                                                dim3((unsigned)tiles, (unsigned)nranks), dim3(kThreads),
+                                                                0, stream, p)) {
+        return e;
+    }
     count_launches(1);
     return cudaGetLastError();
 }
