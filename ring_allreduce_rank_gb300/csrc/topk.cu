@@ -9,8 +9,8 @@
 // 30..19, a 4096-bin histogram) and then the low 19 bits of the keys in the
 // top bin that holds the k-th key (a 2^19-bin histogram, 2 MB per rank,
 // resident in L2).  Both histograms come out of ONE full pass over g and e:
-//   1. a sample (one run of 256 elements in every 16) histograms its top
-//      bits, and a scan picks a window of top bins that holds the k-th key
+//   1. a sample (one run of 256 elements in every 16, 32 or 64) histograms
+//      its top bits, and a scan picks a window of top bins that holds the k-th key
 //      with high probability: the bins between the sample's order statistics
 //      k f -+ m (f the sampled fraction, m five standard deviations of the
 //      count), at most kWindowMax of them;
@@ -46,7 +46,11 @@ constexpr int kLowPerBlock = (int)(kLowBins / kLowBlocks);
 constexpr int kWindowMax = 4;
 constexpr int kRegions = kWindowMax + 1; // low histograms per rank: the window's, then the fallback's
 constexpr int kRun = 32;                // groups of 8 elements in a sampled run (one group per lane)
-constexpr int kSampleEvery = 16;        // one run in every 16 is sampled
+// The sample takes one run in every 16; for large k one in every 32 or 64, as
+// long as the sparser sample still expects kSampleTarget keys at or above the
+// k-th: its window stays one or two digits wide and it reads less of g and e.
+constexpr uint32_t kSampleMin = 16, kSampleMax = 64;
+constexpr uint64_t kSampleTarget = 4096;
 constexpr int kInitCtas = 64;           // CTAs per rank that clear low histograms
 constexpr uint32_t kNoWindow = 0xffffffffu;
 
@@ -75,6 +79,7 @@ struct TopkParams {
     uint64_t K;
     unsigned long long k;
     unsigned long long qa, qb; // the sample's order statistics that bound the window (qa < qb)
+    uint32_t every;            // the sample takes run q when q % every == 0
     int nranks;
     int vec_ok; // every gradient and residual 16-byte aligned
 };
@@ -202,9 +207,9 @@ __global__ void __launch_bounds__(kThreads) topk_init_kernel(const __grid_consta
     }
 }
 
-// 1. The sample: run q of 32 groups (one per lane of a warp) for q = 0, 16,
-// 32, ...: whole 512-byte (bf16) or 1 KB (fp32, residuals) spans, so the
-// sample reads about 1/16 of the bytes.
+// 1. The sample: run q of 32 groups (one per lane of a warp) for q = 0, f,
+// 2f, ... (f = p.every): whole 512-byte (bf16) or 1 KB (fp32, residuals)
+// spans, so the sample reads about 1/f of the bytes.
 template <int DT>
 __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const __grid_constant__ TopkParams p)
 {
@@ -215,10 +220,10 @@ __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const __grid_cons
     __syncthreads();
     const int r = blockIdx.y, lane = threadIdx.x & 31;
     const uint64_t ng = p.K / 8, nruns = (ng + kRun - 1) / kRun;
-    const uint64_t nsampled = (nruns + kSampleEvery - 1) / kSampleEvery;
+    const uint64_t nsampled = (nruns + p.every - 1) / p.every;
     const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
     for (uint64_t w = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); w < nsampled; w += warps) {
-        const uint64_t gi = w * kSampleEvery * kRun + (uint64_t)lane;
+        const uint64_t gi = w * p.every * kRun + (uint64_t)lane;
         if (gi < ng)
             group_keys<DT>(p.grads[r], p.res[r], gi, [&](uint32_t key) { atomicAdd(&h[key >> kLowBits], 1u); });
     }
@@ -466,15 +471,25 @@ size_t topk_work_bytes(int nranks)
                 sizeof(TopkState) + sizeof(uint32_t));
 }
 
+// The sample's density: the sparsest of one run in 16, 32 or 64 that still
+// expects kSampleTarget keys at or above the k-th.
+static uint32_t sample_every(uint64_t k)
+{
+    uint32_t every = kSampleMin;
+    while (every < kSampleMax && k / (2 * every) >= kSampleTarget)
+        every *= 2;
+    return every;
+}
+
 // The sample's size, and the order statistics that bound the window: the
 // number of sampled keys at or above the k-th key is about k f (f the
 // sampled fraction), with a standard deviation below sqrt(k f); five of them
 // on each side.  false when the sample is too small to place a window.
-static bool sample_bounds(uint64_t count, uint64_t k, unsigned long long *qa, unsigned long long *qb)
+static bool sample_bounds(uint64_t count, uint64_t k, uint32_t every, unsigned long long *qa, unsigned long long *qb)
 {
     const uint64_t ng = count / 8, nruns = (ng + kRun - 1) / kRun;
     uint64_t groups = 0;
-    for (uint64_t q = 0; q < nruns; q += kSampleEvery)
+    for (uint64_t q = 0; q < nruns; q += every)
         groups += ng - q * kRun < (uint64_t)kRun ? ng - q * kRun : (uint64_t)kRun;
     const double nsamp = 8.0 * (double)groups;
     const double mean = (double)k * nsamp / (double)count;
@@ -515,6 +530,7 @@ cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, in
     p.K = count;
     p.k = k;
     p.qa = p.qb = 0;
+    p.every = sample_every(k);
     p.nranks = nranks;
     p.vec_ok = vec ? 1 : 0;
     *tau_out = p.tau;
@@ -540,9 +556,9 @@ cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, in
         per_rank = items > 0 ? items : 1;
     const dim3 grid((unsigned)per_rank, (unsigned)nranks);
     unsigned long long launches = 0;
-    if (vec && sample_bounds(count, k, &p.qa, &p.qb)) {
+    if (vec && sample_bounds(count, k, p.every, &p.qa, &p.qb)) {
         const uint64_t nruns = (count / 8 + kRun - 1) / kRun;
-        const uint64_t swarps = (nruns + kSampleEvery - 1) / kSampleEvery;
+        const uint64_t swarps = (nruns + p.every - 1) / p.every;
         uint64_t sctas = (swarps + kThreads / 32 - 1) / (kThreads / 32);
         if (sctas > per_rank)
             sctas = per_rank;

@@ -116,7 +116,7 @@ def _window_record(work, N):
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 def test_sampled_window_hit_miss_and_none(dtype):
     """Every way through the select gives the oracle's bits.
-    - Normal data: the 1/16 sample places a window of top digits around the
+    - Normal data: the sample (one run in 16 at this k) places a window of top digits around the
       k-th key's (one full pass; hit).
     - Zero residuals and sampled runs (the first 256 elements of every 4096)
       that all hold +-1e-6: the sample puts the window on that one digit, far
@@ -153,6 +153,25 @@ def test_sampled_window_hit_miss_and_none(dtype):
         hit, placed = _window_record(work, N)
         assert (hit, placed) == ([want_rec[0]] * N, [want_rec[1]] * N), name
         _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, name)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("k", [200_000, 300_000, 1 << 19])
+def test_sparse_sample_for_large_k(dtype, k):
+    """For large k the sample takes one run in 32 (k = 200,000) or 64
+    (k >= 262,144) instead of 16: it still places a window that holds the k-th
+    key's digit, and the result is the oracle's."""
+    N, K = 3, 1 << 20
+    g = list(W.normal_bf16(N, K, seed_base=k % 101)) if dtype == "bf16" else list(W.normal_fp32(N, K, seed_base=k % 101))
+    e = _res(N, K, seed=k % 103)
+    want_g, want_e = oracle.allreduce_compressed(g, e, "avg", "topk", k=k)
+    gd = [to_dev(x) for x in g]
+    ed = [to_dev(x) for x in e]
+    work = torch.empty(ccl.ccl_plan_topk_work_bytes(N), dtype=torch.uint8, device=DEV)
+    ccl.ccl_allreduce_topk(gd, ed, k, op="avg", work=work)
+    torch.cuda.synchronize()
+    assert _window_record(work, N) == ([1] * N, [1] * N)
+    _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, "k=%d" % k)
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
