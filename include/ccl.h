@@ -306,9 +306,10 @@ ccl_status_t ccl_allreduce_compressed(void *const *grads, float *const *residual
  * (CCL_SUM, or CCL_AVG dividing once by N; CCL_AVG_PREMUL returns
  * CCL_ERR_UNSUPPORTED) and rounded once to dtype, written to every grads[r].
  * The threshold is found on the device by a radix select, with no host round
- * trip: a sample (one 256-element run in 16; in 32 or 64 when k is large
- * enough that the sparser sample still expects 4096 keys at or above the
- * k-th) places a window of one to four top-12-bit bins, one full pass
+ * trip: a sample (one 256-element run in 16; in 32, 64 or 128 when the
+ * sparser sample still expects 4096 keys at or above the k-th and the
+ * standard deviation of its estimate of that key's rank, sqrt(k * 128) for
+ * one run in 128, is at most count / 2048) places a window of one to four top-12-bit bins, one full pass
  * over g and e counts every key's top bits and the low 19 bits of the keys
  * in the window, and a second full pass runs only when the k-th key's top
  * bin fell outside the window.  One more pass then sends, keeps the

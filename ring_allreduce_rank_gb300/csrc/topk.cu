@@ -9,8 +9,8 @@
 // 30..19, a 4096-bin histogram) and then the low 19 bits of the keys in the
 // top bin that holds the k-th key (a 2^19-bin histogram, 2 MB per rank,
 // resident in L2).  Both histograms come out of ONE full pass over g and e:
-//   1. a sample (one run of 256 elements in every 16, 32 or 64) histograms
-//      its top bits, and a scan picks a window of top bins that holds the k-th key
+//   1. a sample (one run of 256 elements in every 16, 32, 64 or 128)
+//      histograms its top bits, and a scan picks a window of top bins that holds the k-th key
 //      with high probability: the bins between the sample's order statistics
 //      k f -+ m (f the sampled fraction, m five standard deviations of the
 //      count), at most kWindowMax of them;
@@ -46,10 +46,10 @@ constexpr int kLowPerBlock = (int)(kLowBins / kLowBlocks);
 constexpr int kWindowMax = 4;
 constexpr int kRegions = kWindowMax + 1; // low histograms per rank: the window's, then the fallback's
 constexpr int kRun = 32;                // groups of 8 elements in a sampled run (one group per lane)
-// The sample takes one run in every 16; for large k one in every 32 or 64, as
-// long as the sparser sample still expects kSampleTarget keys at or above the
-// k-th: its window stays one or two digits wide and it reads less of g and e.
-constexpr uint32_t kSampleMin = 16, kSampleMax = 64;
+// The sample takes one run in every 16; for large inputs one in every 32, 64
+// or 128, which reads less of g and e, as long as its window stays as narrow:
+// see sample_every.
+constexpr uint32_t kSampleMin = 16, kSampleMax = 128;
 constexpr uint64_t kSampleTarget = 4096;
 constexpr int kInitCtas = 64;           // CTAs per rank that clear low histograms
 constexpr uint32_t kNoWindow = 0xffffffffu;
@@ -471,12 +471,18 @@ size_t topk_work_bytes(int nranks)
                 sizeof(TopkState) + sizeof(uint32_t));
 }
 
-// The sample's density: the sparsest of one run in 16, 32 or 64 that still
-// expects kSampleTarget keys at or above the k-th.
-static uint32_t sample_every(uint64_t k)
+// The sample's density, one run in `every`: 16, or the sparsest of 32, 64 and
+// 128 under which (a) the sample still expects kSampleTarget keys at or above
+// the k-th, and (b) the sample's estimate of the k-th key's rank among all
+// count keys, whose standard deviation is about sqrt(k every), stays within
+// count / 2048.  (a) bounds the window's relative width in ranks; (b) keeps
+// it narrow in values where k is a large share of the keys (near the median a
+// band of ranks spans far more of a binade than in the tail).
+static uint32_t sample_every(uint64_t count, uint64_t k)
 {
+    const uint64_t band = count / 2048; // count < 2^32: band^2 < 2^42
     uint32_t every = kSampleMin;
-    while (every < kSampleMax && k / (2 * every) >= kSampleTarget)
+    while (every < kSampleMax && k / (2 * every) >= kSampleTarget && k * (2 * every) <= band * band)
         every *= 2;
     return every;
 }
@@ -530,7 +536,7 @@ cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, in
     p.K = count;
     p.k = k;
     p.qa = p.qb = 0;
-    p.every = sample_every(k);
+    p.every = sample_every(count, k);
     p.nranks = nranks;
     p.vec_ok = vec ? 1 : 0;
     *tau_out = p.tau;

@@ -155,13 +155,25 @@ def test_sampled_window_hit_miss_and_none(dtype):
         _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, name)
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("k", [200_000, 300_000, 1 << 19])
-def test_sparse_sample_for_large_k(dtype, k):
-    """For large k the sample takes one run in 32 (k = 200,000) or 64
-    (k >= 262,144) instead of 16: it still places a window that holds the k-th
-    key's digit, and the result is the oracle's."""
-    N, K = 3, 1 << 20
+def _sampled_keys(work, N):
+    """Keys the sample counted, per rank: the sums of its 4096-bin histograms
+    (u32[N][4096] after the exact u64[N][4096] ones in the work buffer)."""
+    h = work[N * 4096 * 8:N * 4096 * 12].cpu().numpy().view(np.uint32).reshape(N, 4096)
+    return h.sum(axis=1, dtype=np.int64).tolist()
+
+
+@pytest.mark.parametrize("dtype,K,k,every", [("fp32", 16 << 20, 167_772, 32), ("bf16", 16 << 20, 300_000, 64),
+                                             ("fp32", 20 << 20, 600_000, 128), ("bf16", 20 << 20, 600_000, 128),
+                                             ("bf16", 1 << 20, 1 << 19, 16), ("fp32", 16 << 20, 1 << 23, 16)])
+def test_sample_density(dtype, K, k, every):
+    """The sample takes one 256-element run in 16, or in 32, 64 or 128 when the
+    sparser sample still expects 4096 keys at or above the k-th and
+    sqrt(k * every) <= K / 2048.  k = 1 % of 16 Mi allows 32; 300,000 allows 64
+    and 600,000 of 20 Mi 128; half of 1 Mi or of 16 Mi (the median, where a
+    band of ranks spans many digits) keeps 16.  Each time the sample counts
+    exactly its runs' keys, its window holds the k-th key's digit, and the
+    result is the oracle's."""
+    N = 2
     g = list(W.normal_bf16(N, K, seed_base=k % 101)) if dtype == "bf16" else list(W.normal_fp32(N, K, seed_base=k % 101))
     e = _res(N, K, seed=k % 103)
     want_g, want_e = oracle.allreduce_compressed(g, e, "avg", "topk", k=k)
@@ -170,8 +182,10 @@ def test_sparse_sample_for_large_k(dtype, k):
     work = torch.empty(ccl.ccl_plan_topk_work_bytes(N), dtype=torch.uint8, device=DEV)
     ccl.ccl_allreduce_topk(gd, ed, k, op="avg", work=work)
     torch.cuda.synchronize()
+    runs = K // 256  # K is a multiple of 256 here
+    assert _sampled_keys(work, N) == [256 * ((runs + every - 1) // every)] * N
     assert _window_record(work, N) == ([1] * N, [1] * N)
-    _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, "k=%d" % k)
+    _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, "K=%d k=%d" % (K, k))
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
