@@ -33,8 +33,9 @@
 
 namespace ccl {
 
-// A top digit is 1/16 of a binade: the window's two digits hold few keys (one
-// histogram increment each) and their low histograms stay small, 4 MB per rank.
+// A top digit (8 exponent bits, 4 mantissa bits) is 1/16 of a binade: the
+// window's digits hold few keys (one low-histogram increment each), and each
+// digit's low histogram is 2 MB per rank.
 constexpr int kTopBins = 4096;          // key bits 30..19
 constexpr int kLowBits = 19;            // key bits 18..0
 constexpr uint32_t kLowBins = 1u << kLowBits;
@@ -231,8 +232,8 @@ __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const __grid_cons
     merge_hist<uint32_t>(h, p.stop + (size_t)r * kTopBins);
 }
 
-// The window: the top digits of the sample's qa-th and qb-th largest keys
-// (dA >= dB); two bins cover them when dA - dB < 2.
+// The window: the top digits dB..dA of the sample's qb-th and qa-th largest
+// keys, when there are at most kWindowMax of them.
 __global__ void __launch_bounds__(kThreads) topk_window_kernel(const __grid_constant__ TopkParams p)
 {
     chain_entry();
