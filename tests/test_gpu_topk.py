@@ -164,7 +164,8 @@ def _sampled_keys(work, N):
 
 @pytest.mark.parametrize("dtype,K,k,every", [("fp32", 16 << 20, 167_772, 32), ("bf16", 16 << 20, 300_000, 64),
                                              ("fp32", 20 << 20, 600_000, 128), ("bf16", 20 << 20, 600_000, 128),
-                                             ("bf16", 1 << 20, 1 << 19, 16), ("fp32", 16 << 20, 1 << 23, 16)])
+                                             ("bf16", 1 << 20, 1 << 19, 16), ("fp32", 16 << 20, 1 << 23, 16),
+                                             ("bf16", (16 << 20) + 13, 300_000, 64)])
 def test_sample_density(dtype, K, k, every):
     """The sample takes one 256-element run in 16, or in 32, 64 or 128 when the
     sparser sample still expects 4096 keys at or above the k-th and
@@ -172,7 +173,9 @@ def test_sample_density(dtype, K, k, every):
     and 600,000 of 20 Mi 128; half of 1 Mi or of 16 Mi (the median, where a
     band of ranks spans many digits) keeps 16.  Each time the sample counts
     exactly its runs' keys, its window holds the k-th key's digit, and the
-    result is the oracle's."""
+    result is the oracle's.  The ragged size ends in a run of one group of 8
+    elements (sampled: 65,536 is a multiple of 64) and 5 elements outside any
+    group (never sampled)."""
     N = 2
     g = list(W.normal_bf16(N, K, seed_base=k % 101)) if dtype == "bf16" else list(W.normal_fp32(N, K, seed_base=k % 101))
     e = _res(N, K, seed=k % 103)
@@ -182,8 +185,10 @@ def test_sample_density(dtype, K, k, every):
     work = torch.empty(ccl.ccl_plan_topk_work_bytes(N), dtype=torch.uint8, device=DEV)
     ccl.ccl_allreduce_topk(gd, ed, k, op="avg", work=work)
     torch.cuda.synchronize()
-    runs = K // 256  # K is a multiple of 256 here
-    assert _sampled_keys(work, N) == [256 * ((runs + every - 1) // every)] * N
+    groups = K // 8                   # whole groups of 8 elements
+    runs = (groups + 31) // 32        # runs of 32 groups, the last maybe partial
+    sampled = sum(min(32, groups - 32 * q) for q in range(0, runs, every))
+    assert _sampled_keys(work, N) == [8 * sampled] * N
     assert _window_record(work, N) == ([1] * N, [1] * N)
     _check([bits(x) for x in gd], [bits(x) for x in ed], want_g, want_e, "K=%d k=%d" % (K, k))
 
