@@ -123,3 +123,74 @@ def test_graph_replay_rooted_collectives_orders_compressed_and_check():
         assert_bits_equal(bits(grads[r]), wq[r], "graph compressed grads %d" % r)
         assert_bits_equal(res[r].cpu().numpy().view(np.uint32), we[r].view(np.uint32), "graph residual %d" % r)
     assert int(mism.item()) == 0
+
+
+def test_graph_replay_step_mode():
+    """Step mode: one launch per ring step, every step after a phase's first
+    chained to the one before it (programmatic dependent launch).  The first
+    calls, outside the capture, set up the working space; the captured calls
+    then enqueue kernels only, and two replays give the oracle's bits."""
+    N, K = 8, 70003
+    x = W.normal_bf16(N, K, std=1e-3, seed_base=14)
+    bufs = [to_dev(r) for r in x]
+    _, ln = ccl.ccl_plan_chunks(K, N)
+    rs = [torch.empty(ln[r], dtype=torch.bfloat16, device=DEV) for r in range(N)]
+    ag = [torch.empty(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    out = [torch.empty(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+
+    def calls():
+        ccl.ccl_reduce_scatter(bufs, rs, op="avg", mode="step")
+        ccl.ccl_allgather(rs, ag, mode="step")
+        ccl.ccl_allreduce(bufs, out, op="avg", mode="step")
+
+    calls()
+    torch.cuda.synchronize()
+    for t in rs + ag + out:
+        t.zero_()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls()
+    want, _ = oracle.ring_allreduce(list(x), "avg")
+    want_rs = oracle.reduce_scatter(list(x), "avg")
+    for rep in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        for r in range(N):
+            assert_bits_equal(bits(rs[r]), want_rs[r], "graph step RS rank %d, replay %d" % (r, rep))
+            assert_bits_equal(bits(ag[r]), want[r], "graph step RS+AG rank %d, replay %d" % (r, rep))
+            assert_bits_equal(bits(out[r]), want[r], "graph step AR rank %d, replay %d" % (r, rep))
+
+
+def test_graph_replay_no_allocation_reduce_scatter():
+    """ccl_reduce_scatter_step_static under capture: after its set-up call
+    (count = 0) it needs no device memory, so a graph can hold it; two
+    replays give the oracle's bits."""
+    import ctypes
+    fn = ccl.lib().ccl_reduce_scatter_step_static
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    fn.argtypes = [pp, pp, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    N, K = 6, 6 * 10007 + 3
+    x = W.mixed_fp32(N, K, seed_base=61)
+    send = [to_dev(r) for r in x]
+    _, ln = ccl.ccl_plan_chunks(K, N)
+    recv = [torch.zeros(ln[r], dtype=torch.float32, device=DEV) for r in range(N)]
+    P = lambda ts: (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    sum_op = ccl.ccl.OPS["sum"]
+    assert fn(P(send), P(recv), N, 0, 0, sum_op, None) == 0  # set-up call
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        g.capture_begin()
+        rc = fn(P(send), P(recv), N, K, 0, sum_op, ctypes.c_void_p(side.cuda_stream))
+        g.capture_end()
+    assert rc == 0, ccl.ccl_status_string(rc)
+    want = oracle.reduce_scatter(list(x), "sum")
+    for rep in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        for r in range(N):
+            assert_bits_equal(bits(recv[r]), want[r], "graph static RS rank %d, replay %d" % (r, rep))
