@@ -65,11 +65,16 @@
  *     whose arguments travel by value and allocate nothing, so they may be
  *     captured; a graph replays them on the pointers it was captured with.
  *     ccl_allreduce_compressed sets up its kernel (shared-memory opt-in) on
- *     its first call on a device: make that call before capturing.  Step
- *     mode is not capturable: step-mode ReduceScatter, Reduce and bucket
- *     AllReduce use a library-cached device workspace that a first or larger
- *     call allocates (and frees the old one).  ccl_allreduce_host refuses
- *     capture.
+ *     its first call on a device: make that call before capturing.  In step
+ *     mode, AllReduce, AllGather, Broadcast, Gather, Scatter and AllToAll(v)
+ *     allocate nothing either and may be captured.  Step-mode ReduceScatter,
+ *     Reduce and bucket AllReduce use a library-cached device workspace that
+ *     a first or larger call allocates (and frees the old one): capture them
+ *     only after a call at least as large has run on that device outside the
+ *     capture, and while the graph may still be replayed make no larger such
+ *     call and no ccl_finalize (either frees the memory the graph uses).
+ *     ccl_reduce_scatter_step_static may be captured after its set-up call
+ *     (count = 0).  ccl_allreduce_host refuses capture.
  *   - That step-mode workspace is one per device, shared by every call:
  *     step-mode ReduceScatter, Reduce or bucket AllReduce calls whose work
  *     overlaps on the GPU (different streams, different host threads) race on

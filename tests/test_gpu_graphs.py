@@ -194,3 +194,52 @@ def test_graph_replay_no_allocation_reduce_scatter():
         torch.cuda.synchronize()
         for r in range(N):
             assert_bits_equal(bits(recv[r]), want[r], "graph static RS rank %d, replay %d" % (r, rep))
+
+
+def test_graph_replay_step_mode_copies():
+    """Step-mode Broadcast, Gather, Scatter and AllToAll(v) allocate nothing:
+    captured after one call outside the capture, and replayed twice, they give
+    the oracle's bits."""
+    N, K = 5, 5 * 4099 + 2
+    x = W.normal_bf16(N, K, std=1e-2, seed_base=71)
+    off, ln = ccl.ccl_plan_chunks(K, N)
+    full = [to_dev(r) for r in x]
+    bc = [torch.empty(K, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    parts_h = [x[r][off[r]:off[r] + ln[r]] for r in range(N)]
+    parts = [to_dev(p) for p in parts_h]
+    gat = [None] * N
+    gat[1] = torch.empty(K, dtype=torch.bfloat16, device=DEV)
+    sc_send = [None] * N
+    sc_send[2] = full[2]
+    sc = [torch.empty(ln[r], dtype=torch.bfloat16, device=DEV) for r in range(N)]
+    counts = np.array([[3, 0, 5, 7, 2], [1, 1, 1, 1, 1], [0, 9, 2, 4, 0], [6, 6, 0, 3, 8], [2, 0, 0, 0, 11]])
+    sends_h = [W.random_bits_u16(int(counts[i].sum()), seed=80 + i) for i in range(N)]
+    sends = [to_dev(s) for s in sends_h]
+    recv_v = [torch.empty(int(counts[:, j].sum()), dtype=torch.bfloat16, device=DEV) for j in range(N)]
+
+    def calls():
+        ccl.ccl_broadcast(full, bc, root=3, mode="step")
+        ccl.ccl_gather(parts, gat, root=1, mode="step")
+        ccl.ccl_scatter(sc_send, sc, root=2, mode="step")
+        ccl.ccl_alltoallv(sends, recv_v, counts.tolist(), mode="step")
+
+    calls()
+    torch.cuda.synchronize()
+    for t in bc + sc + recv_v + [gat[1]]:
+        t.zero_()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls()
+    want_bc = oracle.broadcast(list(x), 3)
+    want_gat = oracle.gather(parts_h, K)
+    want_sc = oracle.scatter(x[2], N)
+    want_v = oracle.alltoallv(sends_h, counts)
+    for rep in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(bits(gat[1]), want_gat, "graph step gather, replay %d" % rep)
+        for r in range(N):
+            assert_bits_equal(bits(bc[r]), want_bc[r], "graph step broadcast rank %d, replay %d" % (r, rep))
+            assert_bits_equal(bits(sc[r]), want_sc[r], "graph step scatter rank %d, replay %d" % (r, rep))
+            assert_bits_equal(bits(recv_v[r]), want_v[r], "graph step alltoallv rank %d, replay %d" % (r, rep))
