@@ -221,9 +221,6 @@ template <int MAXR> struct FanoutParams {
     int vec32;       // every pointer 32-byte aligned
 };
 
-// Eight words (one 32-byte vector) of the sixteen in w (two neighbouring
-// 32-byte vectors), starting d elements in, 0 < d < 2 * (elements a 16-byte
-// vector holds).
 // Threads per CTA of the fan-out kernel.
 constexpr int kFanThreads = kThreads;
 // Shared memory each fan-out CTA reserves and does not use: with 228 KB per
@@ -236,6 +233,9 @@ constexpr int kFanThreads = kThreads;
 // at seven).
 constexpr size_t kFanOccupancySmem = 31 * 1024;
 
+// Eight words (one 32-byte vector) of the sixteen in w (two neighbouring
+// 32-byte vectors), starting d elements in, 0 < d < 2 * (elements a 16-byte
+// vector holds).
 template <int DT> __device__ __forceinline__ void shift_window32(const uint32_t (&w)[16], int d, uint32_t (&o)[8])
 {
     if (DT == DT_FP32) {
