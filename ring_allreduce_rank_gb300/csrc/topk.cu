@@ -10,10 +10,10 @@
 // top bin that holds the k-th key (a 2^19-bin histogram, 2 MB per rank,
 // resident in L2).  Both histograms come out of ONE full pass over g and e:
 //   1. a sample (one run of 256 elements in every 16, 32, 64 or 128)
-//      histograms its top bits, and a scan picks a window of top bins that holds the k-th key
-//      with high probability: the bins between the sample's order statistics
-//      k f -+ m (f the sampled fraction, m five standard deviations of the
-//      count), at most kWindowMax of them;
+//      histograms its top bits, and a scan picks a window of top bins that
+//      holds the k-th key with high probability: the bins between the
+//      sample's order statistics k f -+ m (f the sampled fraction, m five
+//      standard deviations of the count), at most kWindowMax of them;
 //   2. the full pass counts every key's top bits exactly (shared-memory
 //      atomics per CTA, merged into a 64-bit histogram per rank) and the low
 //      bits of the keys inside the window (global atomics);
