@@ -334,6 +334,16 @@ ccl_status_t ccl_allreduce_topk(void *const *grads, float *const *residuals, int
 /* Bytes of the work buffer ccl_allreduce_topk needs for nranks ranks. */
 ccl_status_t ccl_plan_topk_work_bytes(int nranks, size_t *bytes);
 
+/* The sample ccl_allreduce_topk takes for count elements per rank and this
+ * k, when every gradient and residual is 16-byte aligned (others are never
+ * sampled): *every = f when the sample reads one 256-element run in f (16,
+ * 32, 64 or 128, by the rule in ccl_allreduce_topk's description), 0 when it
+ * takes none -- k = 0, k >= count, or too few elements for the sample to
+ * place a window (the select then counts the k-th key's top bin in a second
+ * full pass).  Host only; CCL_ERR_INVALID_ARG for a null every or
+ * count >= 2^32. */
+ccl_status_t ccl_plan_topk_sample(size_t count, size_t k, uint32_t *every);
+
 /* Bytes one rank would put on a link for Top-k with fp32 values and int32
  * indices: 8 * min(k, count), a ratio of 4 count / bytes = count / (2k) over
  * dense fp32 (Collective Communication, "Top-k sparsification": 500x, not

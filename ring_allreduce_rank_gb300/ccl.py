@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
                 "ccl_plan_compressed_bytes": [sz, i32, i32, psz],
                 "ccl_allreduce_topk": [pp, pp, i32, sz, i32, i32, sz, vp, sz, vp],
                 "ccl_plan_topk_work_bytes": [i32, psz],
+                "ccl_plan_topk_sample": [sz, sz, ctypes.POINTER(ctypes.c_uint32)],
                 "ccl_plan_topk_bytes": [sz, sz, psz],
                 "ccl_gather": [pp, pp, i32, i32, sz, i32, i32, vp],
                 "ccl_scatter": [pp, pp, i32, i32, sz, i32, i32, vp],
@@ -241,6 +242,14 @@ def ccl_allreduce_topk(grads: Sequence[torch.Tensor], residuals: Sequence[torch.
 def ccl_plan_topk_work_bytes(nranks: int) -> int:
     out = ctypes.c_size_t()
     _check(lib().ccl_plan_topk_work_bytes(int(nranks), ctypes.byref(out)), "ccl_plan_topk_work_bytes")
+    return out.value
+
+
+def ccl_plan_topk_sample(count: int, k: int) -> int:
+    """One run of 256 elements in this many is sampled by ccl_allreduce_topk
+    (aligned buffers); 0 when it takes no sample."""
+    out = ctypes.c_uint32()
+    _check(lib().ccl_plan_topk_sample(int(count), int(k), ctypes.byref(out)), "ccl_plan_topk_sample")
     return out.value
 
 

@@ -862,6 +862,14 @@ ccl_status_t ccl_plan_topk_work_bytes(int nranks, size_t *bytes)
     return CCL_OK;
 }
 
+ccl_status_t ccl_plan_topk_sample(size_t count, size_t k, uint32_t *every)
+{
+    if (!every || count >= ((size_t)1 << 32))
+        return CCL_ERR_INVALID_ARG;
+    *every = topk_sample_every(count, k);
+    return CCL_OK;
+}
+
 static ccl_status_t ccl_allreduce_topk_impl(void *const *grads, float *const *residuals, int nranks, size_t count,
                                             ccl_dtype_t dtype, ccl_op_t op, size_t k, void *work, size_t work_bytes,
                                             cudaStream_t stream)

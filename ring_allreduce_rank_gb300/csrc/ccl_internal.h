@@ -217,6 +217,10 @@ cudaError_t launch_compressed_allreduce(int dt, bool avg, int comp, int block, f
 // u = g + e, written to *tau_out[rank] in `work` (topk_work_bytes(nranks)).
 constexpr int kTopkMaxRanks = 16;
 size_t topk_work_bytes(int nranks);
+// The sample's density for count elements and this k (one run of 256 in the
+// returned number), or 0 when the select takes no sample; for buffers that
+// are all 16-byte aligned (others are never sampled).
+uint32_t topk_sample_every(uint64_t count, uint64_t k);
 cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, int nranks, uint64_t count,
                                uint64_t k, void *work, const uint32_t **tau_out, cudaStream_t stream);
 

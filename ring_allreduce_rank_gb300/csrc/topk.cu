@@ -508,6 +508,15 @@ static bool sample_bounds(uint64_t count, uint64_t k, uint32_t every, unsigned l
     return true;
 }
 
+uint32_t topk_sample_every(uint64_t count, uint64_t k)
+{
+    if (k == 0 || k >= count)
+        return 0; // tau is final after the first launch
+    const uint32_t every = sample_every(count, k);
+    unsigned long long qa = 0, qb = 0;
+    return sample_bounds(count, k, every, &qa, &qb) ? every : 0;
+}
+
 cudaError_t launch_topk_select(int dt, void *const *grads, float *const *res, int nranks, uint64_t count,
                                uint64_t k, void *work, const uint32_t **tau_out, cudaStream_t stream)
 {

@@ -108,6 +108,38 @@ def test_planner_topk_bytes(L):
         ccl.ccl_plan_compressed_bytes(1000, "topk", 10)
 
 
+@pytest.mark.parametrize("count,k,every", [
+    (64 << 20, 671_088, 128),      # the bench's Top-k row: 1 % of 64 Mi
+    (16 << 20, 167_772, 32), (16 << 20, 300_000, 64), (20 << 20, 600_000, 128),
+    ((16 << 20) + 13, 300_000, 64),
+    (1 << 20, 10_486, 16),         # too few keys above the k-th for a sparser sample
+    (1 << 20, 1 << 19, 16), (16 << 20, 1 << 23, 16),  # the median: the rank band rule keeps 16
+    (100, 5, 0),                   # too small for the sample to place a window
+    (1000, 0, 0), (1000, 1000, 0), (1000, 5000, 0)])  # tau is known without a select
+def test_planner_topk_sample(L, count, k, every):
+    """The sample density ccl_allreduce_topk uses: the same cases the GPU
+    test checks by counting the keys the sample histogrammed."""
+    assert ccl.ccl_plan_topk_sample(count, k) == every
+
+
+def test_planner_topk_sample_rule(L):
+    """Over a grid of sizes: the density is one of 16, 32, 64, 128 (or 0),
+    a sparser sample still expects 4096 keys at or above the k-th, and the
+    standard deviation of its rank estimate stays within count / 2048."""
+    for count in (1 << 16, 1 << 20, 3 << 22, 64 << 20, (1 << 32) - 1):
+        for frac in (1e-4, 1e-3, 1e-2, 0.05, 0.3, 0.5, 0.9):
+            k = max(1, int(count * frac))
+            e = ccl.ccl_plan_topk_sample(count, k)
+            assert e in (0, 16, 32, 64, 128), (count, k, e)
+            if e > 16:
+                assert k // e >= 4096 and k * e <= (count // 2048) ** 2, (count, k, e)
+    with pytest.raises(C.CclError):
+        ccl.ccl_plan_topk_sample(1 << 32, 10)
+    out = ctypes.c_uint32()
+    assert L.ccl_plan_topk_sample(1000, 10, None) == 1
+    assert L.ccl_plan_topk_sample(1000, 10, ctypes.byref(out)) == 0
+
+
 def test_arena_layout(L):
     assert ccl.ccl_arena_layout(8, 134217728) == (134217728, 8 * 134217728)
     assert ccl.ccl_arena_layout(3, 1000, 256) == (1024, 3072)

@@ -177,6 +177,7 @@ def test_sample_density(dtype, K, k, every):
     elements (sampled: 65,536 is a multiple of 64) and 5 elements outside any
     group (never sampled)."""
     N = 2
+    assert ccl.ccl_plan_topk_sample(K, k) == every
     g = list(W.normal_bf16(N, K, seed_base=k % 101)) if dtype == "bf16" else list(W.normal_fp32(N, K, seed_base=k % 101))
     e = _res(N, K, seed=k % 103)
     want_g, want_e = oracle.allreduce_compressed(g, e, "avg", "topk", k=k)
